@@ -1,0 +1,41 @@
+/*
+ * FP64 oracle for C = A*B and y = A*x -- TEST INFRASTRUCTURE ONLY.
+ * See oracle.c for the definitions followed and their sources.
+ *
+ * All pointers are host pointers to row-major FP64 arrays owned by the caller.
+ * Return 0 on success, 1 on invalid arguments, 2 on allocation failure.
+ */
+#ifndef GTG_ORACLE_H
+#define GTG_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* C = A*B (M x N), A is M x K (lda >= K), B is K x N (ldb >= N), ldc >= N.
+ * If E is non-NULL it receives sum_k |A[i][k]*B[k][j]| (lde >= N).
+ * nthreads <= 0 uses every online core. */
+int oracle_gemm_f64(int64_t M, int64_t N, int64_t K,
+                    const double *A, int64_t lda,
+                    const double *B, int64_t ldb,
+                    double *C, int64_t ldc,
+                    double *E, int64_t lde,
+                    int nthreads);
+
+/* y = A*x, A is M x N (lda >= N), x has N entries, y has M.
+ * If E is non-NULL it receives sum_j |A[i][j]*x[j]|. Single-threaded. */
+int oracle_gemv_f64(int64_t M, int64_t N,
+                    const double *A, int64_t lda,
+                    const double *x,
+                    double *y, double *E);
+
+/* Number of threads nthreads <= 0 resolves to. */
+int oracle_threads_default(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif
