@@ -1,0 +1,253 @@
+"""gtg -- dense GEMM and GEMV on one NVIDIA GB300, through libgtg.so.
+
+This module is argument marshalling only: every step of every product runs
+in the CUDA kernels behind the C ABI declared in ``include/gtg.h``. PyTorch
+supplies device memory and streams; nothing here computes a result. If the
+library has not been built the first call raises ``GtgError`` -- there is no
+fallback of any kind.
+
+Two layers:
+  * the raw C ABI under the same names (``gemm_f32``, ``gemm_tf32``,
+    ``gemm_bf16``, ``gemv_f32``, ``gtg_sync_status`` ...) taking integers for
+    pointers, sizes and the stream handle, returning the status code;
+  * tensor helpers ``matmul`` and ``matvec`` that take torch tensors (CUDA
+    tensors, or host tensors that are copied in and the result copied out).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgtg.so")
+
+GTG_OK, GTG_ERR_INVALID_VALUE, GTG_ERR_MISALIGNED, GTG_ERR_ALIAS = 0, 1, 2, 3
+GTG_ERR_UNSUPPORTED, GTG_ERR_LAUNCH, GTG_ERR_TIMEOUT, GTG_ERR_DEVICE = 4, 5, 6, 7
+PREC = {"f32": 0, "tf32": 1, "bf16": 2}
+KERNELS = {0: "none", 1: "simt", 2: "tcgen05", 3: "zero_fill", 4: "gemv"}
+
+# names and C signatures of every exported function of include/gtg.h
+_i64, _ptr, _int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+
+
+class GtgPlan(ctypes.Structure):
+    _fields_ = [("kernel", _int), ("bm", _int), ("bn", _int), ("bk", _int), ("stages", _int),
+                ("grid", _int), ("threads", _int), ("smem", _int)]
+
+    def as_dict(self) -> dict:
+        d = {f: getattr(self, f) for f, _ in self._fields_}
+        d["kernel"] = KERNELS.get(self.kernel, str(self.kernel))
+        return d
+
+
+SIGNATURES = {
+    "gemm_f32": (_int, [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr]),
+    "gemm_tf32": (_int, [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr]),
+    "gemm_bf16": (_int, [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr]),
+    "gemv_f32": (_int, [_i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _int, _ptr]),
+    "gtg_status_string": (ctypes.c_char_p, [_int]),
+    "gtg_sync_status": (_int, [_ptr]),
+    "gtg_last_cuda_error": (ctypes.c_char_p, []),
+    "gtg_plan_gemm": (_int, [_int, _i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64,
+                             ctypes.POINTER(GtgPlan)]),
+    "gtg_plan_gemv": (_int, [_i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _int,
+                             ctypes.POINTER(GtgPlan)]),
+    "gtg_force_simt": (None, [_int]),
+    "gtg_version": (_int, []),
+}
+
+
+class GtgError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        text = status_string(status) if status >= 0 and _lib is not None else ""
+        super().__init__(f"{what}: gtg status {status} ({text})" if what else f"gtg status {status} ({text})")
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib():
+    """The loaded libgtg.so (ctypes). Raises GtgError if it is not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise GtgError(-1, f"{LIB_PATH} is missing: build it first "
+                                   "(python -c 'import __graft_entry__ as g; g.build()')")
+            handle = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = handle
+    return _lib
+
+
+# ---- raw C ABI, same names and argument order as include/gtg.h ---------------
+
+def gemm_f32(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    return lib().gemm_f32(M, N, K, A, lda, B, ldb, C, ldc, stream)
+
+
+def gemm_tf32(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    return lib().gemm_tf32(M, N, K, A, lda, B, ldb, C, ldc, stream)
+
+
+def gemm_bf16(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    return lib().gemm_bf16(M, N, K, A, lda, B, ldb, C, ldc, stream)
+
+
+def gemv_f32(M, N, A, lda, x, ldx, y, ldy, batch, stream=0) -> int:
+    return lib().gemv_f32(M, N, A, lda, x, ldx, y, ldy, batch, stream)
+
+
+def status_string(status: int) -> str:
+    return lib().gtg_status_string(status).decode()
+
+
+def gtg_sync_status(stream=0) -> int:
+    return lib().gtg_sync_status(stream)
+
+
+def last_cuda_error() -> str:
+    return lib().gtg_last_cuda_error().decode()
+
+
+def gtg_force_simt(force: bool) -> None:
+    lib().gtg_force_simt(1 if force else 0)
+
+
+def gtg_version() -> int:
+    return lib().gtg_version()
+
+
+def plan_gemm(precision, M, N, K, A, lda, B, ldb, C, ldc) -> dict:
+    plan = GtgPlan()
+    st = lib().gtg_plan_gemm(PREC[precision], M, N, K, A, lda, B, ldb, C, ldc, ctypes.byref(plan))
+    if st != GTG_OK:
+        raise GtgError(st, "gtg_plan_gemm")
+    return plan.as_dict()
+
+
+def plan_gemv(M, N, A, lda, x, ldx, y, ldy, batch) -> dict:
+    plan = GtgPlan()
+    st = lib().gtg_plan_gemv(M, N, A, lda, x, ldx, y, ldy, batch, ctypes.byref(plan))
+    if st != GTG_OK:
+        raise GtgError(st, "gtg_plan_gemv")
+    return plan.as_dict()
+
+
+# ---- torch tensor helpers ------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream) -> int:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _rowmajor_ld(t, name) -> int:
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be a 2-D row-major tensor (unit column stride)")
+    return max(int(t.stride(0)), int(t.shape[1]), 1)
+
+
+def _check(status: int, what: str):
+    if status != GTG_OK:
+        extra = f" [{last_cuda_error()}]" if status in (GTG_ERR_LAUNCH, GTG_ERR_DEVICE) else ""
+        raise GtgError(status, what + extra)
+
+
+_IN_DTYPE = {"f32": "float32", "tf32": "float32", "bf16": "bfloat16"}
+_GEMM = {"f32": gemm_f32, "tf32": gemm_tf32, "bf16": gemm_bf16}
+
+
+def matmul(A, B, precision: str = "f32", out=None, stream=None):
+    """C = A @ B on the GPU through gemm_<precision>; C is FP32.
+
+    A (M x K) and B (K x N) are row-major torch tensors: float32 for "f32" and
+    "tf32", bfloat16 for "bf16". CUDA tensors are used in place. Host tensors
+    are copied to the device (pinned host memory makes the copies
+    asynchronous) and the result is copied back into a host tensor.
+    """
+    torch = _torch()
+    want = getattr(torch, _IN_DTYPE[precision])
+    if A.dtype != want or B.dtype != want:
+        raise TypeError(f"{precision} GEMM takes {want} operands, got {A.dtype}, {B.dtype}")
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
+        raise ValueError(f"shape mismatch {tuple(A.shape)} x {tuple(B.shape)}")
+    host = not A.is_cuda
+    if host:
+        dA = A.to("cuda", non_blocking=True)
+        dB = B.to("cuda", non_blocking=True)
+    else:
+        dA, dB = A, B
+    M, K = dA.shape
+    N = dB.shape[1]
+    if out is not None and not host:
+        C = out
+    else:
+        C = torch.empty((M, N), dtype=torch.float32, device=dA.device)
+    st = _GEMM[precision](M, N, K, dA.data_ptr(), _rowmajor_ld(dA, "A"), dB.data_ptr(),
+                          _rowmajor_ld(dB, "B"), C.data_ptr(), _rowmajor_ld(C, "C"),
+                          _stream_handle(stream))
+    _check(st, f"gemm_{precision}")
+    if host:
+        res = out if out is not None else torch.empty((M, N), dtype=torch.float32,
+                                                      pin_memory=A.is_pinned())
+        res.copy_(C, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return res
+    return C
+
+
+def matvec(A, x, out=None, stream=None):
+    """y = A @ x (x of shape (N,)) or Y = X @ A^T per row of X (shape (batch, N)).
+
+    FP32 only, batch <= 8, through gemv_f32. Host tensors are copied in and
+    the result copied back, as in `matmul`.
+    """
+    torch = _torch()
+    if A.dtype != torch.float32 or x.dtype != torch.float32:
+        raise TypeError("gemv_f32 takes float32 tensors")
+    single = x.dim() == 1
+    X = x.unsqueeze(0) if single else x
+    if A.dim() != 2 or X.dim() != 2 or X.shape[1] != A.shape[1]:
+        raise ValueError(f"shape mismatch {tuple(A.shape)} x {tuple(x.shape)}")
+    host = not A.is_cuda
+    dA = A.to("cuda", non_blocking=True) if host else A
+    dX = X.to("cuda", non_blocking=True) if host else X
+    M, N = dA.shape
+    batch = dX.shape[0]
+    if out is not None and not host:
+        Y = out.unsqueeze(0) if single else out
+    else:
+        Y = torch.empty((batch, M), dtype=torch.float32, device=dA.device)
+    st = gemv_f32(M, N, dA.data_ptr(), _rowmajor_ld(dA, "A"), dX.data_ptr(), _rowmajor_ld(dX, "x"),
+                  Y.data_ptr(), _rowmajor_ld(Y, "y"), batch, _stream_handle(stream))
+    _check(st, "gemv_f32")
+    if host:
+        res = torch.empty((batch, M), dtype=torch.float32, pin_memory=A.is_pinned())
+        res.copy_(Y, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        Y = res
+        if out is not None:
+            out.copy_(Y[0] if single else Y)
+            return out
+    return Y[0] if single else Y
+
+
+def sync_status(stream=None) -> None:
+    """Wait for the stream and raise GtgError if a kernel reported a device-side failure."""
+    st = gtg_sync_status(_stream_handle(stream))
+    _check(st, "device status")

@@ -1,0 +1,272 @@
+// C ABI of libgtg: argument validation, kernel choice and launch.
+// The operations and their argument conventions are documented in gtg.h.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "gtg.h"
+#include "internal.h"
+
+namespace gtg {
+namespace {
+
+// Device status word: kernels latch an error code here (e.g. a pipeline wait
+// that ran out of time); gtg_sync_status() reads and clears it. A file-scope
+// device variable, so reporting errors never needs an allocation.
+__device__ int g_device_status = 0;
+
+thread_local char t_cuda_error[256] = "no error";
+std::atomic<int> g_force_simt{0};
+
+void note_cuda_error(cudaError_t e) {
+    std::strncpy(t_cuda_error, cudaGetErrorString(e), sizeof(t_cuda_error) - 1);
+    t_cuda_error[sizeof(t_cuda_error) - 1] = '\0';
+}
+
+struct DeviceTable {
+    std::mutex mu;
+    std::vector<DeviceInfo> devs;
+};
+DeviceTable &device_table() {
+    static DeviceTable t;
+    return t;
+}
+
+// Facts about the current device, gathered once per device.
+gtg_status current_device(DeviceInfo *out) {
+    int id = -1;
+    cudaError_t e = cudaGetDevice(&id);
+    if (e != cudaSuccess) {
+        note_cuda_error(e);
+        return GTG_ERR_DEVICE;
+    }
+    DeviceTable &t = device_table();
+    std::lock_guard<std::mutex> lk(t.mu);
+    for (const DeviceInfo &d : t.devs)
+        if (d.id == id) {
+            *out = d;
+            return GTG_OK;
+        }
+    DeviceInfo d;
+    d.id = id;
+    if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, id)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, id)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, id)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, id)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, id)) != cudaSuccess ||
+        (e = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_device_status)) != cudaSuccess) {
+        note_cuda_error(e);
+        return GTG_ERR_DEVICE;
+    }
+    t.devs.push_back(d);
+    *out = d;
+    return GTG_OK;
+}
+
+// Byte range [lo, hi) spanned by a rows x cols matrix with leading dimension ld.
+struct Span {
+    uintptr_t lo, hi;
+};
+Span span_of(const void *p, int64_t rows, int64_t cols, int64_t ld, int64_t elem) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    if (rows <= 0 || cols <= 0) return {lo, lo};
+    const uint64_t n = static_cast<uint64_t>((rows - 1) * ld + cols) * static_cast<uint64_t>(elem);
+    return {lo, lo + n};
+}
+bool overlaps(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
+
+gtg_status validate_gemm(const GemmArgs &g) {
+    if (g.M < 0 || g.N < 0 || g.K < 0) return GTG_ERR_INVALID_VALUE;
+    if (g.M > INT32_MAX || g.N > INT32_MAX || g.K > INT32_MAX) return GTG_ERR_INVALID_VALUE;
+    if (g.lda < (g.K > 1 ? g.K : 1) || g.ldb < (g.N > 1 ? g.N : 1) || g.ldc < (g.N > 1 ? g.N : 1))
+        return GTG_ERR_INVALID_VALUE;
+    if (g.M == 0 || g.N == 0) return GTG_OK;  // nothing to write
+    if (g.C == nullptr) return GTG_ERR_INVALID_VALUE;
+    if (g.K > 0 && (g.A == nullptr || g.B == nullptr)) return GTG_ERR_INVALID_VALUE;
+    const int64_t in_elem = g.prec == GTG_PREC_BF16 ? 2 : 4;
+    if ((reinterpret_cast<uintptr_t>(g.A) % in_elem) || (reinterpret_cast<uintptr_t>(g.B) % in_elem) ||
+        (reinterpret_cast<uintptr_t>(g.C) % 4))
+        return GTG_ERR_MISALIGNED;
+    const Span c = span_of(g.C, g.M, g.N, g.ldc, 4);
+    if (g.K > 0 && (overlaps(c, span_of(g.A, g.M, g.K, g.lda, in_elem)) ||
+                    overlaps(c, span_of(g.B, g.K, g.N, g.ldb, in_elem))))
+        return GTG_ERR_ALIAS;
+    return GTG_OK;
+}
+
+gtg_status validate_gemv(const GemvArgs &g) {
+    if (g.M < 0 || g.N < 0 || g.M > INT32_MAX || g.N > INT32_MAX) return GTG_ERR_INVALID_VALUE;
+    if (g.batch < 1 || g.batch > 8) return GTG_ERR_INVALID_VALUE;
+    if (g.lda < (g.N > 1 ? g.N : 1)) return GTG_ERR_INVALID_VALUE;
+    if (g.batch > 1 && (g.ldx < g.N || g.ldy < g.M)) return GTG_ERR_INVALID_VALUE;
+    if (g.M == 0) return GTG_OK;
+    if (g.y == nullptr) return GTG_ERR_INVALID_VALUE;
+    if (g.N > 0 && (g.A == nullptr || g.x == nullptr)) return GTG_ERR_INVALID_VALUE;
+    if ((reinterpret_cast<uintptr_t>(g.A) % 4) || (reinterpret_cast<uintptr_t>(g.x) % 4) ||
+        (reinterpret_cast<uintptr_t>(g.y) % 4))
+        return GTG_ERR_MISALIGNED;
+    const int64_t ldx = g.batch > 1 ? g.ldx : g.N, ldy = g.batch > 1 ? g.ldy : g.M;
+    const Span y = span_of(g.y, g.batch, g.M, ldy, 4);
+    if (g.N > 0 && (overlaps(y, span_of(g.A, g.M, g.N, g.lda, 4)) ||
+                    overlaps(y, span_of(g.x, g.batch, g.N, ldx, 4))))
+        return GTG_ERR_ALIAS;
+    return GTG_OK;
+}
+
+gtg_status plan_gemm_impl(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
+    std::memset(plan, 0, sizeof(*plan));
+    if (g.M == 0 || g.N == 0) {
+        plan->kernel = GTG_KERNEL_NONE;
+        return GTG_OK;
+    }
+    if (g.K == 0) {
+        plan->kernel = GTG_KERNEL_ZERO_FILL;
+        return GTG_OK;
+    }
+    if (!(dev.cc_major == 10 && dev.cc_minor == 3)) return GTG_ERR_UNSUPPORTED;
+    if (g.prec != GTG_PREC_F32 && !g_force_simt.load() && tc_supported(dev) && tc_eligible(g))
+        tc_plan(dev, g, plan);
+    else
+        simt_plan(dev, g, plan);
+    return GTG_OK;
+}
+
+gtg_status run_gemm(const GemmArgs &g, cudaStream_t stream) {
+    gtg_status st = validate_gemm(g);
+    if (st != GTG_OK) return st;
+    if (g.M == 0 || g.N == 0) return GTG_OK;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != GTG_OK) return st;
+    gtg_plan plan;
+    if ((st = plan_gemm_impl(dev, g, &plan)) != GTG_OK) return st;
+    cudaError_t e = cudaSuccess;
+    switch (plan.kernel) {
+        case GTG_KERNEL_ZERO_FILL: e = zero_fill_launch(g.C, g.M, g.N, g.ldc, stream); break;
+        case GTG_KERNEL_TCGEN05: e = tc_launch(dev, g, plan, stream); break;
+        case GTG_KERNEL_SIMT: e = simt_launch(dev, g, plan, stream); break;
+        default: break;
+    }
+    if (e != cudaSuccess) {
+        note_cuda_error(e);
+        return GTG_ERR_LAUNCH;
+    }
+    return GTG_OK;
+}
+
+}  // namespace
+}  // namespace gtg
+
+using namespace gtg;
+
+extern "C" {
+
+gtg_status gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
+                    int64_t ldb, float *C, int64_t ldc, cudaStream_t stream) {
+    return run_gemm(GemmArgs{GTG_PREC_F32, M, N, K, A, lda, B, ldb, C, ldc}, stream);
+}
+
+gtg_status gemm_tf32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
+                     int64_t ldb, float *C, int64_t ldc, cudaStream_t stream) {
+    return run_gemm(GemmArgs{GTG_PREC_TF32, M, N, K, A, lda, B, ldb, C, ldc}, stream);
+}
+
+gtg_status gemm_bf16(int64_t M, int64_t N, int64_t K, const gtg_bf16 *A, int64_t lda,
+                     const gtg_bf16 *B, int64_t ldb, float *C, int64_t ldc, cudaStream_t stream) {
+    return run_gemm(GemmArgs{GTG_PREC_BF16, M, N, K, A, lda, B, ldb, C, ldc}, stream);
+}
+
+gtg_status gemv_f32(int64_t M, int64_t N, const float *A, int64_t lda, const float *x, int64_t ldx,
+                    float *y, int64_t ldy, int batch, cudaStream_t stream) {
+    const GemvArgs g{M, N, A, lda, x, batch > 1 ? ldx : N, y, batch > 1 ? ldy : M, batch};
+    gtg_status st = validate_gemv(g);
+    if (st != GTG_OK || M == 0) return st;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != GTG_OK) return st;
+    if (!(dev.cc_major == 10 && dev.cc_minor == 3)) return GTG_ERR_UNSUPPORTED;
+    cudaError_t e;
+    if (N == 0) {
+        // empty sums: every output is zero
+        e = zero_fill_launch(y, batch, M, g.ldy, stream);
+    } else {
+        gtg_plan plan;
+        gemv_plan(dev, g, &plan);
+        e = gemv_launch(dev, g, plan, stream);
+    }
+    if (e != cudaSuccess) {
+        note_cuda_error(e);
+        return GTG_ERR_LAUNCH;
+    }
+    return GTG_OK;
+}
+
+const char *gtg_status_string(gtg_status s) {
+    switch (s) {
+        case GTG_OK: return "success";
+        case GTG_ERR_INVALID_VALUE: return "invalid value (size, leading dimension, null pointer or batch)";
+        case GTG_ERR_MISALIGNED: return "pointer not aligned to its element size";
+        case GTG_ERR_ALIAS: return "output overlaps an input";
+        case GTG_ERR_UNSUPPORTED: return "unsupported device (needs sm_103a)";
+        case GTG_ERR_LAUNCH: return "kernel launch failed";
+        case GTG_ERR_TIMEOUT: return "a device pipeline wait exceeded its time limit";
+        case GTG_ERR_DEVICE: return "CUDA runtime error";
+        default: return "unknown status";
+    }
+}
+
+gtg_status gtg_sync_status(cudaStream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) {
+        note_cuda_error(e);
+        return GTG_ERR_DEVICE;
+    }
+    int v = 0;
+    const int zero = 0;
+    if ((e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int))) != cudaSuccess ||
+        (e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int))) != cudaSuccess) {
+        note_cuda_error(e);
+        return GTG_ERR_DEVICE;
+    }
+    return v;
+}
+
+const char *gtg_last_cuda_error(void) { return t_cuda_error; }
+
+gtg_status gtg_plan_gemm(int precision, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
+                         const void *B, int64_t ldb, const void *C, int64_t ldc, gtg_plan *plan) {
+    if (plan == nullptr || precision < GTG_PREC_F32 || precision > GTG_PREC_BF16) return GTG_ERR_INVALID_VALUE;
+    const GemmArgs g{precision, M, N, K, A, lda, B, ldb, const_cast<float *>(static_cast<const float *>(C)), ldc};
+    gtg_status st = validate_gemm(g);
+    if (st != GTG_OK) return st;
+    std::memset(plan, 0, sizeof(*plan));
+    if (M == 0 || N == 0) return GTG_OK;   // GTG_KERNEL_NONE, as the call itself
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != GTG_OK) return st;
+    return plan_gemm_impl(dev, g, plan);
+}
+
+gtg_status gtg_plan_gemv(int64_t M, int64_t N, const float *A, int64_t lda, const float *x, int64_t ldx,
+                         const float *y, int64_t ldy, int batch, gtg_plan *plan) {
+    if (plan == nullptr) return GTG_ERR_INVALID_VALUE;
+    const GemvArgs g{M, N, A, lda, x, batch > 1 ? ldx : N, const_cast<float *>(y), batch > 1 ? ldy : M, batch};
+    gtg_status st = validate_gemv(g);
+    if (st != GTG_OK) return st;
+    std::memset(plan, 0, sizeof(*plan));
+    if (M == 0) return GTG_OK;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != GTG_OK) return st;
+    if (N == 0) {
+        plan->kernel = GTG_KERNEL_ZERO_FILL;
+        return GTG_OK;
+    }
+    gemv_plan(dev, g, plan);
+    return GTG_OK;
+}
+
+void gtg_force_simt(int force) { g_force_simt.store(force ? 1 : 0); }
+
+int gtg_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,268 @@
+// SIMT GEMM with exact FP32 arithmetic: C = A * B, FP32 (or BF16, widened
+// exactly) operands, IEEE FP32 fused multiply-adds on the CUDA cores.
+//
+// This is the shared-memory tiled GEMM of "CUDA Programming (6)" (section
+// 3.2) and "Matrix Operations" ("Tiled Implementation with Shared Memory"),
+// with the refinements those pages list as next steps:
+//   * register blocking ("Register Blocking"; section 3.4 "thread-level
+//     tiling"): each thread owns an 8 x 8 block of C, so every value read
+//     from shared memory feeds 8 multiply-adds;
+//   * vectorised 128-bit global loads ("Vectorization");
+//   * prefetching ("Prefetching"): the next K-slice is loaded into registers
+//     while the current one is multiplied from the other shared buffer, so
+//     one barrier per slice suffices;
+//   * boundary handling as on the pages: out-of-range tile elements are
+//     zero-filled, out-of-range outputs are not stored, and no thread leaves
+//     before the barriers.
+// A is stored transposed in shared memory (k-major) so that a thread's 8 rows
+// are two 16-byte reads; B keeps its row-major layout.
+#include <cuda_bf16.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace gtg {
+namespace {
+
+constexpr int kBK = 16;
+
+template <typename T>
+struct Load;
+
+template <>
+struct Load<float> {
+    static __device__ __forceinline__ float4 vec4(const float *p) {
+        return __ldg(reinterpret_cast<const float4 *>(p));
+    }
+    static __device__ __forceinline__ float one(const float *p) { return __ldg(p); }
+};
+
+// BF16 stored as 16-bit patterns; widening to FP32 is exact.
+template <>
+struct Load<uint16_t> {
+    static __device__ __forceinline__ float bf(uint32_t bits) { return __uint_as_float(bits << 16); }
+    static __device__ __forceinline__ float4 vec4(const uint16_t *p) {
+        const uint2 v = __ldg(reinterpret_cast<const uint2 *>(p));
+        return make_float4(bf(v.x & 0xFFFFu), bf(v.x >> 16), bf(v.y & 0xFFFFu), bf(v.y >> 16));
+    }
+    static __device__ __forceinline__ float one(const uint16_t *p) { return bf(__ldg(p)); }
+};
+
+template <typename T, int BM, int BN, bool VEC>
+struct SimtTile {
+    static constexpr int TX = BN / 8;              // threads along N
+    static constexpr int TY = BM / 8;              // threads along M
+    static constexpr int THREADS = TX * TY;
+    static constexpr int A_V4 = BM * kBK / 4 / THREADS;   // 4-element A groups per thread
+    static constexpr int B_V4 = BN * kBK / 4 / THREADS;
+    static_assert(A_V4 >= 1 && B_V4 >= 1, "tile too small for its thread count");
+};
+
+template <typename T, int BM, int BN, bool VEC>
+__global__ void __launch_bounds__(SimtTile<T, BM, BN, VEC>::THREADS)
+    simt_gemm_kernel(int M, int N, int K, const T *__restrict__ A, long long lda,
+                     const T *__restrict__ B, long long ldb, float *__restrict__ C, long long ldc,
+                     int c_vec) {
+    using L = SimtTile<T, BM, BN, VEC>;
+    __shared__ __align__(16) float As[2][kBK][BM];
+    __shared__ __align__(16) float Bs[2][kBK][BN];
+
+    const int tid = threadIdx.x;
+    const int tx = tid % L::TX, ty = tid / L::TX;
+    const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+
+    float4 ra[L::A_V4], rb[L::B_V4];
+
+    // A: group g covers row (g % BM), k-quad (g / BM): consecutive threads take
+    // consecutive rows so the transposed shared-memory stores hit distinct banks.
+    auto load_a = [&](int k0) {
+#pragma unroll
+        for (int i = 0; i < L::A_V4; ++i) {
+            const int g = tid + i * L::THREADS;
+            const int r = g % BM, kq = g / BM;
+            const int row = m0 + r, k = k0 + kq * 4;
+            const T *p = A + static_cast<long long>(row) * lda + k;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (row < M) {
+                if (VEC && k + 3 < K) {
+                    v = Load<T>::vec4(p);
+                } else {
+                    if (k < K) v.x = Load<T>::one(p);
+                    if (k + 1 < K) v.y = Load<T>::one(p + 1);
+                    if (k + 2 < K) v.z = Load<T>::one(p + 2);
+                    if (k + 3 < K) v.w = Load<T>::one(p + 3);
+                }
+            }
+            ra[i] = v;
+        }
+    };
+    auto store_a = [&](int buf) {
+#pragma unroll
+        for (int i = 0; i < L::A_V4; ++i) {
+            const int g = tid + i * L::THREADS;
+            const int r = g % BM, kq = g / BM;
+            As[buf][kq * 4 + 0][r] = ra[i].x;
+            As[buf][kq * 4 + 1][r] = ra[i].y;
+            As[buf][kq * 4 + 2][r] = ra[i].z;
+            As[buf][kq * 4 + 3][r] = ra[i].w;
+        }
+    };
+    // B: group g covers k-row (g / (BN/4)), columns 4*(g % (BN/4)) .. +3.
+    auto load_b = [&](int k0) {
+#pragma unroll
+        for (int i = 0; i < L::B_V4; ++i) {
+            const int g = tid + i * L::THREADS;
+            const int kr = g / (BN / 4), c4 = g % (BN / 4);
+            const int k = k0 + kr, col = n0 + c4 * 4;
+            const T *p = B + static_cast<long long>(k) * ldb + col;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (k < K) {
+                if (VEC && col + 3 < N) {
+                    v = Load<T>::vec4(p);
+                } else {
+                    if (col < N) v.x = Load<T>::one(p);
+                    if (col + 1 < N) v.y = Load<T>::one(p + 1);
+                    if (col + 2 < N) v.z = Load<T>::one(p + 2);
+                    if (col + 3 < N) v.w = Load<T>::one(p + 3);
+                }
+            }
+            rb[i] = v;
+        }
+    };
+    auto store_b = [&](int buf) {
+#pragma unroll
+        for (int i = 0; i < L::B_V4; ++i) {
+            const int g = tid + i * L::THREADS;
+            const int kr = g / (BN / 4), c4 = g % (BN / 4);
+            *reinterpret_cast<float4 *>(&Bs[buf][kr][c4 * 4]) = rb[i];
+        }
+    };
+
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+    const int ntiles = (K + kBK - 1) / kBK;
+    if (ntiles > 0) {
+        load_a(0);
+        load_b(0);
+        store_a(0);
+        store_b(0);
+    }
+    __syncthreads();
+
+    for (int t = 0; t < ntiles; ++t) {
+        const int cur = t & 1;
+        if (t + 1 < ntiles) {
+            load_a((t + 1) * kBK);
+            load_b((t + 1) * kBK);
+        }
+#pragma unroll
+        for (int k = 0; k < kBK; ++k) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(&As[cur][k][ty * 4]);
+            const float4 a1 = *reinterpret_cast<const float4 *>(&As[cur][k][BM / 2 + ty * 4]);
+            const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[cur][k][tx * 4]);
+            const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[cur][k][BN / 2 + tx * 4]);
+            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        if (t + 1 < ntiles) {
+            store_a(cur ^ 1);
+            store_b(cur ^ 1);
+        }
+        __syncthreads();
+    }
+
+    // rows ty*4 + i (i < 4) and BM/2 + ty*4 + i; columns likewise in N.
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int row = m0 + (i < 4 ? ty * 4 + i : BM / 2 + ty * 4 + (i - 4));
+        if (row >= M) continue;
+        float *crow = C + static_cast<long long>(row) * ldc;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int col = n0 + (h == 0 ? tx * 4 : BN / 2 + tx * 4);
+            const float *v = &acc[i][h * 4];
+            if (c_vec && col + 3 < N) {
+                *reinterpret_cast<float4 *>(crow + col) = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (col + j < N) crow[col + j] = v[j];
+            }
+        }
+    }
+}
+
+__global__ void zero_fill_kernel(float *C, long long M, long long N, long long ldc) {
+    const long long total = M * N;
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x)
+        C[(i / N) * ldc + (i % N)] = 0.f;
+}
+
+template <typename T, int BM, int BN, bool VEC>
+cudaError_t launch_one(const GemmArgs &g, cudaStream_t stream) {
+    using L = SimtTile<T, BM, BN, VEC>;
+    dim3 grid(static_cast<unsigned>((g.N + BN - 1) / BN), static_cast<unsigned>((g.M + BM - 1) / BM));
+    const int c_vec = ((reinterpret_cast<uintptr_t>(g.C) & 15) == 0 && (g.ldc & 3) == 0) ? 1 : 0;
+    simt_gemm_kernel<T, BM, BN, VEC><<<grid, L::THREADS, 0, stream>>>(
+        static_cast<int>(g.M), static_cast<int>(g.N), static_cast<int>(g.K),
+        static_cast<const T *>(g.A), g.lda, static_cast<const T *>(g.B), g.ldb, g.C, g.ldc, c_vec);
+    return cudaGetLastError();
+}
+
+template <typename T, bool VEC>
+cudaError_t launch_typed(const GemmArgs &g, const gtg_plan &plan, cudaStream_t stream) {
+    if (plan.bm == 128) return launch_one<T, 128, 128, VEC>(g, stream);
+    return launch_one<T, 64, 64, VEC>(g, stream);
+}
+
+bool vec_ok(const GemmArgs &g) {
+    // 4 consecutive elements per load: 16 bytes for FP32, 8 for BF16.
+    const uintptr_t mask = g.prec == GTG_PREC_BF16 ? 7 : 15;
+    return (reinterpret_cast<uintptr_t>(g.A) & mask) == 0 && (reinterpret_cast<uintptr_t>(g.B) & mask) == 0 &&
+           (g.lda % 4) == 0 && (g.ldb % 4) == 0;
+}
+
+}  // namespace
+
+void simt_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
+    const int64_t big_tiles = ((g.M + 127) / 128) * ((g.N + 127) / 128);
+    const bool big = big_tiles >= dev.sms;
+    plan->kernel = GTG_KERNEL_SIMT;
+    plan->bm = plan->bn = big ? 128 : 64;
+    plan->bk = kBK;
+    plan->stages = 2;
+    plan->threads = big ? 256 : 64;
+    plan->smem = 0;
+    const int64_t tiles = ((g.M + plan->bm - 1) / plan->bm) * ((g.N + plan->bn - 1) / plan->bn);
+    plan->grid = static_cast<int>(tiles);
+}
+
+cudaError_t simt_launch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan,
+                        cudaStream_t stream) {
+    (void)dev;
+    const bool vec = vec_ok(g);
+    if (g.prec == GTG_PREC_BF16)
+        return vec ? launch_typed<uint16_t, true>(g, plan, stream) : launch_typed<uint16_t, false>(g, plan, stream);
+    return vec ? launch_typed<float, true>(g, plan, stream) : launch_typed<float, false>(g, plan, stream);
+}
+
+cudaError_t zero_fill_launch(float *C, int64_t M, int64_t N, int64_t ldc, cudaStream_t stream) {
+    const long long total = M * N;
+    long long blocks = (total + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    if (blocks < 1) blocks = 1;
+    zero_fill_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(C, M, N, ldc);
+    return cudaGetLastError();
+}
+
+}  // namespace gtg

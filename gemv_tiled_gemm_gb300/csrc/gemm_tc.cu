@@ -1,0 +1,465 @@
+// Tensor-core GEMM for sm_103a: C (FP32) = A * B with BF16 or TF32 operands.
+//
+// The tiling principle is the one of "GPU Matrix Multiplication: Tiling and
+// Shared Memory" (section 3) and "CUDA Programming (6)" (section 3.2): each
+// output tile is accumulated from K-slices of A and B staged in shared
+// memory, out-of-range elements contributing zeros and out-of-range outputs
+// not being stored. On GB300 the pieces are:
+//
+//   * staging: TMA tensor copies (128-byte swizzled) into a ring of STAGES
+//     shared-memory slots, each guarded by a pair of mbarriers (full/empty)
+//     instead of the pages' two __syncthreads per tile; the copy of slice
+//     k+1.. overlaps the multiply of slice k (the pages' "Prefetching");
+//     TMA fills out-of-bounds box elements with zeros (the pages' padding);
+//   * multiply: tcgen05.mma issued by one thread, accumulating a 128 x BN
+//     FP32 tile in tensor memory (TMEM); two accumulators so that the
+//     epilogue of one tile overlaps the main loop of the next;
+//   * epilogue: four warps read TMEM (tcgen05.ld, one row per thread) and
+//     store the rows that exist (row < M, col < N);
+//   * scheduling: a persistent grid (at most one CTA per SM) walks the
+//     output tiles in groups of GROUP row-tiles for L2 reuse.
+//
+// Operand layouts: A is row-major M x K, i.e. "K-major" for the MMA; B is
+// row-major K x N, i.e. "MN-major". Both are read in their given layout; no
+// transposition pass.
+//
+// Every mbarrier wait is bounded in time. On expiry the waiting thread
+// latches GTG_ERR_TIMEOUT in the library status word, raises a shared abort
+// flag that makes the other roles stop, waits (bounded) for its own copies
+// and MMAs in flight, and the CTA releases its TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gtg {
+namespace {
+
+constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2-5 epilogue
+constexpr int kBM = 128;
+constexpr int kGroup = 16;     // row-tiles per raster group
+constexpr int kSmemBudget = 200 * 1024;
+
+template <bool TF32, int BN_>
+struct Shape {
+    static constexpr int BN = BN_;
+    static constexpr int ELEM = TF32 ? 4 : 2;
+    static constexpr int BM = kBM;
+    static constexpr int BK = 128 / ELEM;          // K elements in one 128-byte row
+    static constexpr int UK = 32 / ELEM;           // K per tcgen05.mma
+    static constexpr int KSTEPS = BK / UK;
+    static constexpr int A_BYTES = BM * 128;       // BM rows x 128 bytes of K
+    static constexpr int BCH_N = 128 / ELEM;       // N elements per 128-byte row of B
+    static constexpr int B_CHUNKS = BN / BCH_N;
+    static constexpr int BCH_BYTES = BK * 128;     // one 128-byte-wide column block of B
+    static constexpr int B_BYTES = B_CHUNKS * BCH_BYTES;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES_RAW = kSmemBudget / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+    static constexpr int TMEM_COLS = 2 * BN;       // two FP32 accumulators
+    static constexpr int NBARS = 2 * STAGES + 5;
+    static constexpr int SMEM = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + NBARS * 8 + 16;
+    static constexpr uint32_t IDESC = ptx::make_idesc(TF32 ? 2u : 1u, 0u, 1u, BM, BN);
+    static_assert(BN % BCH_N == 0 && BN >= 64 && BN <= 256, "tile width");
+    static_assert(STAGE_BYTES % 1024 == 0, "stages keep 1024-byte alignment");
+    static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
+                  "TMEM allocation must be a power of two in [32, 512]");
+};
+
+struct TcParams {
+    float *C;
+    long long ldc;
+    int M, N;
+    int num_m, num_n, num_kb, num_tiles;
+    int c_vec;                   // 16-byte stores allowed for whole rows of a tile
+    int *status;
+    unsigned long long wait_limit_ns;
+};
+
+__device__ __forceinline__ void tile_coords(int t, const TcParams &p, int &mb, int &nb) {
+    const int per_group = kGroup * p.num_n;
+    const int g = t / per_group;
+    const int first = g * kGroup;
+    const int gs = min(p.num_m - first, kGroup);
+    const int r = t - g * per_group;
+    mb = first + r % gs;
+    nb = r / gs;
+}
+
+// Bounded wait used by the pipeline roles. Returns false if this CTA must stop.
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                       const TcParams &p) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i)
+            if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer_ns() - t0 > p.wait_limit_ns) {
+            *abort_flag = 1;
+            atomicCAS(p.status, 0, static_cast<int>(GTG_ERR_TIMEOUT));
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                         const TcParams &p) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, abort_flag, p);
+}
+
+// Wait that ignores the abort flag: used only to let work already in flight
+// finish before shared memory or TMEM is released. Bounded as well.
+__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, const TcParams &p) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (ptx::globaltimer_ns() - t0 > p.wait_limit_ns) {
+            atomicCAS(p.status, 0, static_cast<int>(GTG_ERR_TIMEOUT));
+            return;
+        }
+    }
+}
+
+template <bool TF32, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const TcParams p) {
+    using S = Shape<TF32, BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sA = ptx::smem_addr(smem);
+    const uint32_t sB = sA + S::STAGES * S::A_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::STAGES * S::STAGE_BYTES);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + S::NBARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    const uint32_t bar0 = ptx::smem_addr(bars);
+    // barrier map: full[s] = s, empty[s] = STAGES + s, acc_full[a] = 2*STAGES + a,
+    // acc_empty[a] = 2*STAGES + 2 + a, drain = 2*STAGES + 4
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (S::STAGES + s); };
+    auto accf_bar = [&](int a) { return bar0 + 8u * (2 * S::STAGES + a); };
+    auto acce_bar = [&](int a) { return bar0 + 8u * (2 * S::STAGES + 2 + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * S::STAGES + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S::STAGES; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(accf_bar(a), 1);
+            ptx::mbar_init(acce_bar(a), 4);  // one arrive per epilogue warp
+        }
+        ptx::mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), S::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t it = 0;  // slices issued so far
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                int mb, nb;
+                tile_coords(t, p, mb, nb);
+                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                    const int s = static_cast<int>(it % S::STAGES);
+                    const uint32_t ph = (it / S::STAGES) & 1u;
+                    if (!wait_bar(empty_bar(s), ph ^ 1u, abort_flag, p)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(full_bar(s), S::STAGE_BYTES);
+                    ptx::tma_load_2d(sA + s * S::A_BYTES, &tmA, full_bar(s), kb * S::BK, mb * S::BM);
+#pragma unroll
+                    for (int c = 0; c < S::B_CHUNKS; ++c)
+                        ptx::tma_load_2d(sB + s * S::B_BYTES + c * S::BCH_BYTES, &tmB, full_bar(s),
+                                         nb * BN + c * S::BCH_N, kb * S::BK);
+                }
+            }
+            if (!ok) {
+                // let the copies already issued land before the CTA exits
+                const uint32_t n = it < S::STAGES ? it : S::STAGES;
+                for (uint32_t j = 1; j <= n; ++j) {
+                    const uint32_t i = it - j;
+                    wait_drain(full_bar(static_cast<int>(i % S::STAGES)), (i / S::STAGES) & 1u, p);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t it = 0;
+            int local = 0;
+            bool ok = true, issued = false;
+            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++local) {
+                const int acc = local & 1;
+                const uint32_t aph = (static_cast<uint32_t>(local) >> 1) & 1u;
+                if (!wait_bar(acce_bar(acc), aph ^ 1u, abort_flag, p)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                    const int s = static_cast<int>(it % S::STAGES);
+                    const uint32_t ph = (it / S::STAGES) & 1u;
+                    if (!wait_bar(full_bar(s), ph, abort_flag, p)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after_sync();
+                    const uint32_t a0 = sA + s * S::A_BYTES;
+                    const uint32_t b0 = sB + s * S::B_BYTES;
+#pragma unroll
+                    for (int k = 0; k < S::KSTEPS; ++k) {
+                        // A, K-major, 128B swizzle: 8-row groups 1024 B apart; the K
+                        // step moves the start by 32 bytes inside the swizzle row.
+                        const uint64_t ad = ptx::smem_desc_sw128(a0 + k * 32, 16, 1024);
+                        // B, MN-major, 128B swizzle: 128-byte-wide column blocks BCH_BYTES
+                        // apart (leading offset), 8-row K groups 1024 B apart (stride
+                        // offset); the K step moves UK rows of 128 bytes.
+                        const uint64_t bd =
+                            ptx::smem_desc_sw128(b0 + k * S::UK * 128, S::BCH_BYTES, 1024);
+                        const uint32_t accum = (kb > 0 || k > 0) ? 1u : 0u;
+                        if constexpr (TF32)
+                            ptx::mma_tf32(d_tmem, ad, bd, S::IDESC, accum);
+                        else
+                            ptx::mma_bf16(d_tmem, ad, bd, S::IDESC, accum);
+                    }
+                    ptx::mma_commit(empty_bar(s));  // slot free once these MMAs have read it
+                    issued = true;
+                }
+                if (!ok) break;
+                ptx::mma_commit(accf_bar(acc));     // accumulator ready for the epilogue
+            }
+            if (issued) {
+                // nothing may still be writing TMEM when it is released
+                ptx::mma_commit(drain_bar);
+                wait_drain(drain_bar, 0u, p);
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue (warps 2..5)
+        const int quarter = warp & 3;  // TMEM lanes this warp may access
+        const int r_in_tile = quarter * 32 + lane;
+        int local = 0;
+        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++local) {
+            int mb, nb;
+            tile_coords(t, p, mb, nb);
+            const int acc = local & 1;
+            const uint32_t aph = (static_cast<uint32_t>(local) >> 1) & 1u;
+            if (!wait_bar(accf_bar(acc), aph, abort_flag, p)) break;
+            ptx::tc_fence_after_sync();
+            const int row = mb * S::BM + r_in_tile;
+            const int col0 = nb * BN;
+            const bool row_ok = row < p.M;
+            const bool whole = p.c_vec && (col0 + BN <= p.N);
+            float *crow = p.C + static_cast<long long>(row) * p.ldc + col0;
+            const uint32_t taddr =
+                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
+                ptx::tmem_ld_wait();
+                if (row_ok) {
+                    if (whole) {
+                        float4 *dst = reinterpret_cast<float4 *>(crow + c * 32);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                 __uint_as_float(r[4 * j + 2]),
+                                                 __uint_as_float(r[4 * j + 3]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col0 + c * 32 + j < p.N) crow[c * 32 + j] = __uint_as_float(r[j]);
+                    }
+                }
+            }
+            ptx::tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(acce_bar(acc));
+        }
+    }
+
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc(tmem_base, S::TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool encode_2d(CUtensorMap *map, bool tf32, const void *base, uint64_t inner, uint64_t outer,
+               uint64_t ld_elems, uint32_t box_inner, uint32_t box_outer) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const uint64_t elem = tf32 ? 4 : 2;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {ld_elems * elem};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, tf32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct AttrCache {
+    std::mutex mu;
+    uint64_t done[64] = {};  // per device: bit per kernel instantiation
+};
+AttrCache &attr_cache() {
+    static AttrCache c;
+    return c;
+}
+
+template <bool TF32, int BN>
+cudaError_t launch_impl(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan,
+                        cudaStream_t stream, int attr_bit) {
+    using S = Shape<TF32, BN>;
+    auto kern = tc_gemm_kernel<TF32, BN>;
+    {
+        AttrCache &ac = attr_cache();
+        std::lock_guard<std::mutex> lk(ac.mu);
+        const int d = dev.id & 63;
+        if (!(ac.done[d] >> attr_bit & 1)) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+            if (e != cudaSuccess) return e;
+            ac.done[d] |= 1ull << attr_bit;
+        }
+    }
+    CUtensorMap ta, tb;
+    if (!encode_2d(&ta, TF32, g.A, g.K, g.M, g.lda, S::BK, S::BM)) return cudaErrorInvalidValue;
+    if (!encode_2d(&tb, TF32, g.B, g.N, g.K, g.ldb, S::BCH_N, S::BK)) return cudaErrorInvalidValue;
+    TcParams p;
+    p.C = g.C;
+    p.ldc = g.ldc;
+    p.M = static_cast<int>(g.M);
+    p.N = static_cast<int>(g.N);
+    p.num_m = static_cast<int>((g.M + S::BM - 1) / S::BM);
+    p.num_n = static_cast<int>((g.N + BN - 1) / BN);
+    p.num_kb = static_cast<int>((g.K + S::BK - 1) / S::BK);
+    p.num_tiles = p.num_m * p.num_n;
+    p.c_vec = ((reinterpret_cast<uintptr_t>(g.C) & 15) == 0 && (g.ldc & 3) == 0) ? 1 : 0;
+    p.status = dev.status;
+    p.wait_limit_ns = kWaitLimitNs;
+    kern<<<plan.grid, kThreads, S::SMEM, stream>>>(ta, tb, p);
+    return cudaGetLastError();
+}
+
+template <bool TF32, int BN>
+void fill_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
+    using S = Shape<TF32, BN>;
+    const int64_t tiles = ((g.M + S::BM - 1) / S::BM) * ((g.N + BN - 1) / BN);
+    plan->kernel = GTG_KERNEL_TCGEN05;
+    plan->bm = S::BM;
+    plan->bn = BN;
+    plan->bk = S::BK;
+    plan->stages = S::STAGES;
+    plan->grid = static_cast<int>(tiles < dev.sms ? tiles : dev.sms);
+    plan->threads = kThreads;
+    plan->smem = S::SMEM;
+}
+
+}  // namespace
+
+bool tc_supported(const DeviceInfo &dev) {
+    // tcgen05 exists on the sm_100 family; this library is built for sm_103a.
+    return dev.cc_major == 10 && dev.cc_minor == 3 && encode_fn() != nullptr;
+}
+
+bool tc_eligible(const GemmArgs &g) {
+    if (g.prec != GTG_PREC_TF32 && g.prec != GTG_PREC_BF16) return false;
+    const int64_t elem = g.prec == GTG_PREC_TF32 ? 4 : 2;
+    const auto a = reinterpret_cast<uintptr_t>(g.A), b = reinterpret_cast<uintptr_t>(g.B);
+    if ((a & 15) || (b & 15)) return false;                   // TMA base alignment
+    if ((g.lda * elem) % 16 || (g.ldb * elem) % 16) return false;  // TMA row stride
+    if (g.M > INT32_MAX || g.N > INT32_MAX || g.K > INT32_MAX) return false;
+    if ((g.lda * elem) >= (1ll << 40) || (g.ldb * elem) >= (1ll << 40)) return false;
+    return g.M > 0 && g.N > 0 && g.K > 0;
+}
+
+// Tile width: minimise (waves of tiles) x (tile width / relative efficiency).
+// With M = 128 per CTA, a 256-wide tile reads 96 shared-memory bytes per
+// tensor-core cycle, a 128-wide one 128 (the SM's limit) and a 64-wide one
+// 192, so narrower tiles only pay when they fill otherwise idle SMs.
+void tc_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
+    const int widths[3] = {256, 128, 64};
+    const double eff[3] = {1.0, 0.8, 0.5};
+    int best = 0;
+    double best_cost = 0;
+    for (int i = 0; i < 3; ++i) {
+        const int64_t tiles = ((g.M + kBM - 1) / kBM) * ((g.N + widths[i] - 1) / widths[i]);
+        const int64_t waves = (tiles + dev.sms - 1) / dev.sms;
+        const double cost = static_cast<double>(waves) * widths[i] / eff[i];
+        if (i == 0 || cost < best_cost) {
+            best = i;
+            best_cost = cost;
+        }
+    }
+    const bool tf32 = g.prec == GTG_PREC_TF32;
+    switch (widths[best]) {
+        case 256: tf32 ? fill_plan<true, 256>(dev, g, plan) : fill_plan<false, 256>(dev, g, plan); break;
+        case 128: tf32 ? fill_plan<true, 128>(dev, g, plan) : fill_plan<false, 128>(dev, g, plan); break;
+        default: tf32 ? fill_plan<true, 64>(dev, g, plan) : fill_plan<false, 64>(dev, g, plan); break;
+    }
+}
+
+cudaError_t tc_launch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan,
+                      cudaStream_t stream) {
+    const bool tf32 = g.prec == GTG_PREC_TF32;
+    switch (plan.bn) {
+        case 256:
+            return tf32 ? launch_impl<true, 256>(dev, g, plan, stream, 0)
+                        : launch_impl<false, 256>(dev, g, plan, stream, 1);
+        case 128:
+            return tf32 ? launch_impl<true, 128>(dev, g, plan, stream, 2)
+                        : launch_impl<false, 128>(dev, g, plan, stream, 3);
+        case 64:
+            return tf32 ? launch_impl<true, 64>(dev, g, plan, stream, 4)
+                        : launch_impl<false, 64>(dev, g, plan, stream, 5);
+        default:
+            return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace gtg

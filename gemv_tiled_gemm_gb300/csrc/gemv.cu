@@ -1,0 +1,292 @@
+// Bandwidth-bound FP32 GEMV: y_b = A * x_b for up to 8 vectors at once.
+//
+// "Matrix Operations" (section "Matrix-Vector Multiplication") computes
+// y[i] = sum_j A[i][j] x[j] with one thread per row and, in its optimised
+// form, the vector staged in shared memory once per work group so that it
+// is not re-read from global memory for every row; vectors too large for
+// shared memory are staged in chunks with a barrier on each side
+// ("Handling Large Vectors"). The matrix, read exactly once, is the traffic
+// that sets the speed.
+//
+// GB300 form:
+//   * a warp (not a thread) owns ROWS rows at a time and streams them with
+//     coalesced 128-bit loads that bypass L1 (each lane keeps U x ROWS loads
+//     in flight), so a row is one contiguous burst instead of the pages'
+//     one-row-per-thread pattern whose neighbouring threads are a full row
+//     apart;
+//   * every CTA stages x (all `batch` vectors) in shared memory once; if they
+//     do not fit, chunk by chunk with the barriers of the pages' chunked
+//     loop, which every thread of the CTA reaches (no early return);
+//   * partial sums are combined with a warp-shuffle butterfly;
+//   * the grid is persistent (a multiple of the SM count) and each CTA owns
+//     one contiguous, equally sized range of rows, so every SM streams the
+//     same number of bytes;
+//   * each matrix element loaded is used for all `batch` vectors.
+#include <algorithm>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gtg {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kSmemBudget = 200 * 1024;   // per CTA, for the staged vectors
+
+struct GemvParams {
+    const float *A;
+    long long lda;
+    const float *x;
+    long long ldx;
+    float *y;
+    long long ldy;
+    int M, N;
+    int chunk;     // vector entries staged per pass (multiple of 4)
+    int nchunks;
+};
+
+template <int BATCH>
+__device__ __forceinline__ void stage_x(float *xs, const GemvParams &p, int c0, int len) {
+#pragma unroll
+    for (int b = 0; b < BATCH; ++b) {
+        const float *src = p.x + static_cast<long long>(b) * p.ldx + c0;
+        float *dst = xs + b * p.chunk;
+        for (int j = threadIdx.x; j < len; j += kThreads) dst[j] = __ldg(src + j);
+    }
+}
+
+template <int BATCH, int ROWS, int U, bool VEC>
+__device__ __forceinline__ void accumulate(float (&acc)[ROWS][BATCH], const float *const (&arow)[ROWS],
+                                           const float *xs, int chunk, int c0, int len, int lane) {
+    if constexpr (VEC) {
+        const int n4 = len >> 2;
+        int j = lane;
+        for (; j + 32 * (U - 1) < n4; j += 32 * U) {
+            float4 a[U][ROWS];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) a[u][r] = ptx::ld_stream_f4(arow[r] + c0 + 4 * (j + 32 * u));
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int b = 0; b < BATCH; ++b) {
+                    const float4 xv = reinterpret_cast<const float4 *>(xs + b * chunk)[j + 32 * u];
+#pragma unroll
+                    for (int r = 0; r < ROWS; ++r) {
+                        float s = acc[r][b];
+                        s = fmaf(a[u][r].x, xv.x, s);
+                        s = fmaf(a[u][r].y, xv.y, s);
+                        s = fmaf(a[u][r].z, xv.z, s);
+                        s = fmaf(a[u][r].w, xv.w, s);
+                        acc[r][b] = s;
+                    }
+                }
+        }
+        for (; j < n4; j += 32) {
+            float4 a[ROWS];
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) a[r] = ptx::ld_stream_f4(arow[r] + c0 + 4 * j);
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) {
+                const float4 xv = reinterpret_cast<const float4 *>(xs + b * chunk)[j];
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) {
+                    float s = acc[r][b];
+                    s = fmaf(a[r].x, xv.x, s);
+                    s = fmaf(a[r].y, xv.y, s);
+                    s = fmaf(a[r].z, xv.z, s);
+                    s = fmaf(a[r].w, xv.w, s);
+                    acc[r][b] = s;
+                }
+            }
+        }
+        const int jt = 4 * n4 + lane;   // at most 3 trailing entries
+        if (jt < len) {
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) {
+                const float a = ptx::ld_stream_f1(arow[r] + c0 + jt);
+#pragma unroll
+                for (int b = 0; b < BATCH; ++b) acc[r][b] = fmaf(a, xs[b * chunk + jt], acc[r][b]);
+            }
+        }
+    } else {
+        int j = lane;
+        for (; j + 32 * (U - 1) < len; j += 32 * U) {
+            float a[U][ROWS];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) a[u][r] = ptx::ld_stream_f1(arow[r] + c0 + j + 32 * u);
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int b = 0; b < BATCH; ++b) {
+                    const float xv = xs[b * chunk + j + 32 * u];
+#pragma unroll
+                    for (int r = 0; r < ROWS; ++r) acc[r][b] = fmaf(a[u][r], xv, acc[r][b]);
+                }
+        }
+        for (; j < len; j += 32) {
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) {
+                const float a = ptx::ld_stream_f1(arow[r] + c0 + j);
+#pragma unroll
+                for (int b = 0; b < BATCH; ++b) acc[r][b] = fmaf(a, xs[b * chunk + j], acc[r][b]);
+            }
+        }
+    }
+}
+
+template <int BATCH, int ROWS, int U, bool VEC>
+__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
+    extern __shared__ float4 xs_raw[];
+    float *xs = reinterpret_cast<float *>(xs_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // this CTA's rows: [r_begin, r_end), equal shares of M
+    const int r_begin = static_cast<int>(static_cast<long long>(p.M) * blockIdx.x / gridDim.x);
+    const int r_end = static_cast<int>(static_cast<long long>(p.M) * (blockIdx.x + 1) / gridDim.x);
+    const int ntasks = (r_end - r_begin + ROWS - 1) / ROWS;
+    const int rounds = (ntasks + kWarps - 1) / kWarps;
+
+    if (p.nchunks == 1) {
+        stage_x<BATCH>(xs, p, 0, p.N);
+        __syncthreads();
+    }
+    for (int round = 0; round < rounds; ++round) {  // same trip count for every warp
+        const int task = round * kWarps + warp;
+        const bool active = task < ntasks;
+        const int row0 = r_begin + task * ROWS;
+        const float *arow[ROWS];
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r)  // rows past the range re-read the last one; never stored
+            arow[r] = p.A + static_cast<long long>(min(row0 + r, r_end - 1)) * p.lda;
+
+        float acc[ROWS][BATCH];
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) acc[r][b] = 0.f;
+
+        for (int c = 0; c < p.nchunks; ++c) {
+            const int c0 = c * p.chunk;
+            const int len = min(p.chunk, p.N - c0);
+            if (p.nchunks > 1) {
+                __syncthreads();              // everyone is done with the previous chunk
+                stage_x<BATCH>(xs, p, c0, len);
+                __syncthreads();              // the chunk is in place
+            }
+            if (active) accumulate<BATCH, ROWS, U, VEC>(acc, arow, xs, p.chunk, c0, len, lane);
+        }
+        if (active) {
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+                for (int b = 0; b < BATCH; ++b) {
+                    float s = acc[r][b];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+                    acc[r][b] = s;
+                }
+            // every lane now holds every total; lane (r * BATCH + b) stores one
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+                for (int b = 0; b < BATCH; ++b)
+                    if (lane == (r * BATCH + b) % 32 && row0 + r < r_end)
+                        p.y[static_cast<long long>(b) * p.ldy + row0 + r] = acc[r][b];
+        }
+    }
+}
+
+template <int BATCH, int ROWS, int U>
+struct GemvKernels {
+    static void *get(bool vec) {
+        return vec ? reinterpret_cast<void *>(gemv_kernel<BATCH, ROWS, U, true>)
+                   : reinterpret_cast<void *>(gemv_kernel<BATCH, ROWS, U, false>);
+    }
+};
+
+constexpr int kRows = 2;
+constexpr int kUnroll = 4;
+
+void *kernel_for(int batch, bool vec) {
+    switch (batch) {
+        case 1: return GemvKernels<1, kRows, kUnroll>::get(vec);
+        case 2: return GemvKernels<2, kRows, kUnroll>::get(vec);
+        case 3: return GemvKernels<3, kRows, kUnroll>::get(vec);
+        case 4: return GemvKernels<4, kRows, kUnroll>::get(vec);
+        case 5: return GemvKernels<5, kRows, kUnroll>::get(vec);
+        case 6: return GemvKernels<6, kRows, kUnroll>::get(vec);
+        case 7: return GemvKernels<7, kRows, kUnroll>::get(vec);
+        default: return GemvKernels<8, kRows, kUnroll>::get(vec);
+    }
+}
+
+bool gemv_vec(const GemvArgs &g) {
+    return (reinterpret_cast<uintptr_t>(g.A) & 15) == 0 && (g.lda & 3) == 0;
+}
+
+struct Layout {
+    int chunk, nchunks, smem;
+};
+
+Layout layout(const GemvArgs &g) {
+    const int64_t per_entry = 4ll * g.batch;
+    int64_t chunk = std::max<int64_t>(4, kSmemBudget / per_entry / 4 * 4);
+    const int64_t n_pad = (g.N + 3) / 4 * 4;
+    if (chunk > n_pad) chunk = n_pad;
+    if (chunk < 4) chunk = 4;
+    Layout l;
+    l.chunk = static_cast<int>(chunk);
+    l.nchunks = static_cast<int>(g.N == 0 ? 1 : (g.N + chunk - 1) / chunk);
+    l.smem = static_cast<int>(chunk * per_entry);
+    return l;
+}
+
+}  // namespace
+
+void gemv_plan(const DeviceInfo &dev, const GemvArgs &g, gtg_plan *plan) {
+    const Layout l = layout(g);
+    // One CTA of 16 warps per SM (the kernel keeps up to 128 registers per
+    // thread); every CTA owns an equal share of the rows.
+    int64_t grid = dev.sms;
+    if (grid > g.M) grid = g.M;
+    plan->kernel = GTG_KERNEL_GEMV;
+    plan->bm = kRows;
+    plan->bn = l.chunk;
+    plan->bk = kUnroll;
+    plan->stages = l.nchunks;
+    plan->grid = static_cast<int>(std::max<int64_t>(grid, 1));
+    plan->threads = kThreads;
+    plan->smem = l.smem;
+}
+
+cudaError_t gemv_launch(const DeviceInfo &dev, const GemvArgs &g, const gtg_plan &plan,
+                        cudaStream_t stream) {
+    (void)dev;
+    const Layout l = layout(g);
+    const bool vec = gemv_vec(g);
+    void *kern = kernel_for(g.batch, vec);
+    if (l.smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, l.smem);
+        if (e != cudaSuccess) return e;
+    }
+    GemvParams p;
+    p.A = g.A;
+    p.lda = g.lda;
+    p.x = g.x;
+    p.ldx = g.ldx;
+    p.y = g.y;
+    p.ldy = g.ldy;
+    p.M = static_cast<int>(g.M);
+    p.N = static_cast<int>(g.N);
+    p.chunk = l.chunk;
+    p.nchunks = l.nchunks;
+    void *args[] = {&p};
+    return cudaLaunchKernel(kern, dim3(plan.grid), dim3(kThreads), args, static_cast<size_t>(l.smem), stream);
+}
+
+}  // namespace gtg

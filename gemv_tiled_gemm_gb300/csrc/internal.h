@@ -1,0 +1,59 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "gtg.h"
+
+namespace gtg {
+
+// Per-device facts the planners need (filled once per device by api.cu).
+struct DeviceInfo {
+    int id = -1;
+    int sms = 0;                 // streaming multiprocessors
+    int cc_major = 0, cc_minor = 0;
+    int smem_optin = 0;          // max dynamic shared memory per block (bytes)
+    int l2_bytes = 0;
+    int *status = nullptr;       // device address of the library's status word
+};
+
+// One GEMM call after validation. Pointers are device pointers.
+struct GemmArgs {
+    int prec;                    // GTG_PREC_*
+    int64_t M, N, K;
+    const void *A; int64_t lda;
+    const void *B; int64_t ldb;
+    float *C; int64_t ldc;
+};
+
+struct GemvArgs {
+    int64_t M, N;
+    const float *A; int64_t lda;
+    const float *x; int64_t ldx;
+    float *y; int64_t ldy;
+    int batch;
+};
+
+// Time limit for any pipeline wait inside a kernel (nanoseconds).
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+// ---- tcgen05 tensor-core GEMM (gemm_tc.cu)
+bool tc_supported(const DeviceInfo &dev);
+bool tc_eligible(const GemmArgs &g);
+void tc_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan);
+cudaError_t tc_launch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan,
+                      cudaStream_t stream);
+
+// ---- SIMT GEMM (gemm_simt.cu): FP32 or BF16 inputs, FP32 arithmetic
+void simt_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan);
+cudaError_t simt_launch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan,
+                        cudaStream_t stream);
+cudaError_t zero_fill_launch(float *C, int64_t M, int64_t N, int64_t ldc, cudaStream_t stream);
+
+// ---- GEMV (gemv.cu)
+void gemv_plan(const DeviceInfo &dev, const GemvArgs &g, gtg_plan *plan);
+cudaError_t gemv_launch(const DeviceInfo &dev, const GemvArgs &g, const gtg_plan &plan,
+                        cudaStream_t stream);
+
+}  // namespace gtg

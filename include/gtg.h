@@ -1,0 +1,207 @@
+/*
+ * gtg -- dense matrix products on one NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of libgtg.so. Every entry point is callable from C, C++, ctypes or
+ * any FFI: plain pointers, 64-bit sizes and a CUDA stream handle.
+ *
+ * The operations are the two defined in "Matrix Operations" (Vulkan
+ * ML-inference tutorial, sections "Matrix-Vector Multiplication" and
+ * "Matrix-Matrix Multiplication (GEMM)"), also given in "CUDA Programming (6):
+ * Shared Memory and Matrix Multiplication Optimization" (section 3) and "GPU
+ * Matrix Multiplication: Tiling and Shared Memory" (section 1):
+ *
+ *     GEMM   C[i][j] = sum_{k<K} A[i][k] * B[k][j]     A: M x K, B: K x N, C: M x N
+ *     GEMV   y[i]    = sum_{j<N} A[i][j] * x[j]        A: M x N, x: N,     y: M
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Layout: row-major. Element (r, c) of a matrix with leading dimension ld
+ *    is at p[r * ld + c]. The pages index A[row*K + k], B[k*N + col] and
+ *    C[row*N + col]; the leading dimensions generalise that to padded rows
+ *    and require ld >= the row length.
+ *  - Memory: every array pointer is a DEVICE pointer (cudaMalloc, or any
+ *    memory the device can address) on the current device. The caller owns
+ *    all buffers; the library never frees or keeps them after the call.
+ *  - Output: C (or y) is overwritten, never read ("writeonly" in the pages'
+ *    shaders): no alpha/beta scaling. K = 0 writes zeros (the empty sum).
+ *  - Stream: work is enqueued on `stream` (0 = legacy default stream) and
+ *    the call returns without waiting for it. Inputs must stay valid and
+ *    unmodified, and outputs untouched, until the stream reaches that point.
+ *  - Aliasing: C (or y) must not overlap A, B (or A, x): GTG_ERR_ALIAS.
+ *  - Errors: a non-zero status means nothing was launched (except
+ *    GTG_ERR_LAUNCH, reported when the launch itself failed). Device-side
+ *    failures (a pipeline wait that ran out of time) are latched in a device
+ *    status word and returned by gtg_sync_status().
+ *  - Allocation: the calls allocate no device memory and do not synchronise.
+ *    Per device, the library keeps only host-side state (device properties
+ *    and a table of kernel attributes), created on first use.
+ *  - Thread safety: calls may be made concurrently from several host
+ *    threads; the host-side state is guarded by a mutex.
+ */
+#ifndef GTG_H
+#define GTG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GTG_API __attribute__((visibility("default")))
+#else
+#define GTG_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as the CUDA runtime's cudaStream_t (a redeclaration is allowed). */
+typedef struct CUstream_st *cudaStream_t;
+
+/* A bfloat16 value stored as its 16-bit pattern (1 sign, 8 exponent, 7 mantissa). */
+typedef uint16_t gtg_bf16;
+
+typedef int gtg_status;
+enum {
+    GTG_OK = 0,
+    GTG_ERR_INVALID_VALUE = 1, /* negative size, ld < row length, NULL with non-zero extent, batch out of range */
+    GTG_ERR_MISALIGNED = 2,    /* a pointer not aligned to its element size */
+    GTG_ERR_ALIAS = 3,         /* the output overlaps an input */
+    GTG_ERR_UNSUPPORTED = 4,   /* no kernel for this device (not sm_103a / sm_100-class) */
+    GTG_ERR_LAUNCH = 5,        /* the CUDA launch failed (cudaGetLastError text via gtg_last_cuda_error) */
+    GTG_ERR_TIMEOUT = 6,       /* device side: a pipeline wait exceeded its time limit */
+    GTG_ERR_DEVICE = 7         /* a CUDA runtime call failed (no device, context error, ...) */
+};
+
+/*
+ * gemm_f32 -- C = A*B in FP32 with exact-FP32 arithmetic: every product and
+ * sum is an IEEE binary32 fused multiply-add on the CUDA cores
+ * (register-blocked, shared-memory-tiled SIMT kernel; "CUDA Programming (6)",
+ * section 3.2 tiling and 3.4 thread-level tiling; "Matrix Operations",
+ * "Register Blocking"). Out-of-range tile elements are zero-padded and
+ * out-of-range stores skipped, so any M, N, K >= 0 is accepted.
+ *   M, N, K    sizes (>= 0)
+ *   A          M x K, leading dimension lda >= max(K, 1)
+ *   B          K x N, leading dimension ldb >= max(N, 1)
+ *   C          M x N, leading dimension ldc >= max(N, 1), overwritten
+ * Pointers must be 4-byte aligned. 16-byte alignment and ld % 4 == 0 enable
+ * 128-bit loads; other layouts use a scalar-load variant with the same result.
+ */
+GTG_API gtg_status gemm_f32(int64_t M, int64_t N, int64_t K,
+                    const float *A, int64_t lda,
+                    const float *B, int64_t ldb,
+                    float *C, int64_t ldc,
+                    cudaStream_t stream);
+
+/*
+ * gemm_tf32 -- C = A*B with FP32 storage, TF32 multiplication on the tensor
+ * cores (tcgen05.mma kind::tf32) and FP32 accumulation in tensor memory
+ * ("Matrix Operations", "Performance Considerations": tensor cores). Same
+ * arguments and layouts as gemm_f32. Each product uses the operands reduced
+ * to TF32 precision (10 explicit mantissa bits) by the tensor core.
+ * The tensor-core kernel needs 16-byte aligned A and B and lda, ldb
+ * multiples of 4 (the TMA rules); other layouts are computed by the exact
+ * FP32 kernel of gemm_f32, whose result also meets the TF32 accuracy.
+ */
+GTG_API gtg_status gemm_tf32(int64_t M, int64_t N, int64_t K,
+                     const float *A, int64_t lda,
+                     const float *B, int64_t ldb,
+                     float *C, int64_t ldc,
+                     cudaStream_t stream);
+
+/*
+ * gemm_bf16 -- C = A*B with BF16 inputs, FP32 accumulation on the tensor
+ * cores (tcgen05.mma kind::f16) and an FP32 output ("Matrix Operations",
+ * "Performance Considerations": half-precision data types and tensor cores).
+ * BF16 products are exact in FP32; only the accumulation rounds.
+ *   A  M x K bf16, lda >= max(K, 1);  B  K x N bf16, ldb >= max(N, 1)
+ *   C  M x N FP32, ldc >= max(N, 1), overwritten
+ * Pointers must be 2-byte (A, B) and 4-byte (C) aligned. The tensor-core
+ * kernel needs 16-byte aligned A and B and lda, ldb multiples of 8 (the TMA
+ * rules); other layouts are computed by the SIMT kernel in FP32 (exact
+ * products, FP32 accumulation), which meets the same accuracy.
+ */
+GTG_API gtg_status gemm_bf16(int64_t M, int64_t N, int64_t K,
+                     const gtg_bf16 *A, int64_t lda,
+                     const gtg_bf16 *B, int64_t ldb,
+                     float *C, int64_t ldc,
+                     cudaStream_t stream);
+
+/*
+ * gemv_f32 -- y_b = A*x_b for `batch` vectors at once, in FP32 ("Matrix
+ * Operations", "Matrix-Vector Multiplication": the fully connected layer;
+ * the vector is staged in shared memory once per thread block as in its
+ * "Optimized Implementation with Shared Memory", in chunks when it is too
+ * large, as in "Handling Large Vectors"). Every row of A is read once from
+ * memory for all `batch` vectors.
+ *   M, N   A is M x N (M rows, N columns), lda >= max(N, 1)
+ *   x      batch vectors of N entries; vector b starts at x + b * ldx
+ *          (ldx >= N; ignored when batch == 1)
+ *   y      batch outputs of M entries; output b starts at y + b * ldy
+ *          (ldy >= M; ignored when batch == 1), overwritten
+ *   batch  1 <= batch <= 8
+ * Pointers must be 4-byte aligned; a 16-byte aligned A with lda % 4 == 0
+ * enables 128-bit row loads.
+ */
+GTG_API gtg_status gemv_f32(int64_t M, int64_t N,
+                    const float *A, int64_t lda,
+                    const float *x, int64_t ldx,
+                    float *y, int64_t ldy,
+                    int batch,
+                    cudaStream_t stream);
+
+/* Static English text for a status code (never NULL). */
+GTG_API const char *gtg_status_string(gtg_status status);
+
+/*
+ * Waits for `stream`, then returns and clears the device status word of the
+ * current device: GTG_OK, or GTG_ERR_TIMEOUT if some kernel launched since
+ * the last call gave up a pipeline wait (its output is then incomplete).
+ * GTG_ERR_DEVICE if the synchronisation itself failed.
+ */
+GTG_API gtg_status gtg_sync_status(cudaStream_t stream);
+
+/* Text of the last CUDA runtime error seen by the library on this thread. */
+GTG_API const char *gtg_last_cuda_error(void);
+
+/*
+ * Which kernel a GEMM call with these arguments would run (no launch, no
+ * device work). Fills *plan. `precision` is GTG_PREC_F32, _TF32 or _BF16.
+ * Returns the same validation status the GEMM call itself would.
+ */
+enum { GTG_PREC_F32 = 0, GTG_PREC_TF32 = 1, GTG_PREC_BF16 = 2 };
+enum { GTG_KERNEL_NONE = 0, GTG_KERNEL_SIMT = 1, GTG_KERNEL_TCGEN05 = 2,
+       GTG_KERNEL_ZERO_FILL = 3, GTG_KERNEL_GEMV = 4 };
+typedef struct {
+    int kernel;   /* GTG_KERNEL_* */
+    int bm, bn, bk;
+    int stages;   /* shared-memory pipeline depth */
+    int grid;     /* thread blocks launched */
+    int threads;  /* threads per block */
+    int smem;     /* dynamic shared memory per block, bytes */
+} gtg_plan;
+
+GTG_API gtg_status gtg_plan_gemm(int precision, int64_t M, int64_t N, int64_t K,
+                         const void *A, int64_t lda,
+                         const void *B, int64_t ldb,
+                         const void *C, int64_t ldc,
+                         gtg_plan *plan);
+
+/* Same for gemv_f32 (bm = rows per warp, bn = shared-memory chunk length). */
+GTG_API gtg_status gtg_plan_gemv(int64_t M, int64_t N, const float *A, int64_t lda,
+                         const float *x, int64_t ldx, const float *y, int64_t ldy,
+                         int batch, gtg_plan *plan);
+
+/*
+ * Testing hook: force the tensor-core GEMM paths onto the SIMT kernel
+ * (force = 1) or restore the normal choice (force = 0). Process-wide.
+ */
+GTG_API void gtg_force_simt(int force);
+
+/* Version of this ABI (major * 10000 + minor * 100 + patch). */
+GTG_API int gtg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GTG_H */

@@ -1,0 +1,113 @@
+"""The C ABI library loads, exports every declared symbol, and rejects bad
+arguments on the host (no device work is started by any call here)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import gemv_tiled_gemm_gb300 as gtg
+from gemv_tiled_gemm_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gtg.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    _build.build()
+    gtg.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"GTG_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_header_declares_the_entry_points():
+    names = set(declared_functions())
+    for want in ("gemm_f32", "gemm_tf32", "gemm_bf16", "gemv_f32", "gtg_status_string",
+                 "gtg_sync_status"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol():
+    handle = ctypes.CDLL(gtg.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(handle, name), f"{name} declared in gtg.h but not exported"
+    # and the binding covers each one with a signature
+    assert set(declared_functions()) == set(gtg.SIGNATURES)
+
+
+def test_only_the_c_abi_is_exported():
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", gtg.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    text_syms = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    assert text_syms == set(declared_functions())
+
+
+def test_status_strings():
+    for s in range(8):
+        assert gtg.status_string(s)
+    assert "unknown" in gtg.status_string(99)
+
+
+# Fake but aligned, non-overlapping "device" addresses: validation never
+# dereferences them, and every call below fails validation before any CUDA call.
+A, B, C = 1 << 32, 2 << 32, 3 << 32
+
+
+@pytest.mark.parametrize("fn", [gtg.gemm_f32, gtg.gemm_tf32, gtg.gemm_bf16])
+def test_gemm_argument_validation(fn):
+    E = gtg.GTG_ERR_INVALID_VALUE
+    assert fn(-1, 4, 4, A, 4, B, 4, C, 4) == E
+    assert fn(4, -1, 4, A, 4, B, 4, C, 4) == E
+    assert fn(4, 4, -1, A, 4, B, 4, C, 4) == E
+    assert fn(4, 4, 8, A, 7, B, 4, C, 4) == E          # lda < K
+    assert fn(4, 8, 4, A, 4, B, 7, C, 8) == E          # ldb < N
+    assert fn(4, 8, 4, A, 4, B, 8, C, 7) == E          # ldc < N
+    assert fn(4, 4, 4, A, 4, B, 4, 0, 4) == E          # null C
+    assert fn(4, 4, 4, 0, 4, B, 4, C, 4) == E          # null A with K > 0
+    assert fn(1 << 31, 4, 4, A, 4, B, 4, C, 4) == E    # beyond 32-bit sizes
+    # empty outputs are valid and launch nothing (no device needed)
+    assert fn(0, 4, 4, 0, 4, 0, 4, 0, 4) == gtg.GTG_OK
+    assert fn(4, 0, 4, 0, 4, 0, 1, 0, 1) == gtg.GTG_OK
+
+
+@pytest.mark.parametrize("fn,elem", [(gtg.gemm_f32, 4), (gtg.gemm_tf32, 4), (gtg.gemm_bf16, 2)])
+def test_gemm_alignment_and_alias(fn, elem):
+    assert fn(4, 4, 4, A + 1, 4, B, 4, C, 4) == gtg.GTG_ERR_MISALIGNED
+    assert fn(4, 4, 4, A, 4, B, 4, C + 2, 4) == gtg.GTG_ERR_MISALIGNED
+    # C overlapping A or B
+    assert fn(4, 4, 4, A, 4, B, 4, A + 4 * elem, 4) == gtg.GTG_ERR_ALIAS
+    assert fn(4, 4, 4, A, 4, B, 4, B, 4) == gtg.GTG_ERR_ALIAS
+    # adjacent, touching but not overlapping, is fine as far as validation goes
+    # (it then needs a device, which this container does not have)
+    st = fn(4, 4, 4, A, 4, A + 16 * elem, 4, A + 32 * elem, 4)
+    assert st not in (gtg.GTG_ERR_ALIAS, gtg.GTG_ERR_INVALID_VALUE, gtg.GTG_ERR_MISALIGNED)
+
+
+def test_gemv_argument_validation():
+    E = gtg.GTG_ERR_INVALID_VALUE
+    f = gtg.gemv_f32
+    assert f(-1, 4, A, 4, B, 4, C, 4, 1) == E
+    assert f(4, 8, A, 7, B, 8, C, 4, 1) == E        # lda < N
+    assert f(4, 4, A, 4, B, 4, C, 4, 0) == E        # batch < 1
+    assert f(4, 4, A, 4, B, 4, C, 4, 9) == E        # batch > 8
+    assert f(4, 8, A, 8, B, 7, C, 4, 2) == E        # ldx < N with batch > 1
+    assert f(8, 4, A, 4, B, 4, C, 7, 2) == E        # ldy < M with batch > 1
+    assert f(4, 4, A, 4, B, 4, 0, 4, 1) == E        # null y
+    assert f(4, 4, A + 2, 4, B, 4, C, 4, 1) == gtg.GTG_ERR_MISALIGNED
+    assert f(4, 4, A, 4, B, 4, A + 8, 4, 1) == gtg.GTG_ERR_ALIAS
+    assert f(4, 4, A, 4, B, 4, B, 4, 1) == gtg.GTG_ERR_ALIAS
+    assert f(0, 4, 0, 4, 0, 4, 0, 4, 1) == gtg.GTG_OK
+
+
+def test_plan_validation_matches_the_call():
+    with pytest.raises(gtg.GtgError) as e:
+        gtg.plan_gemm("bf16", 4, 4, 8, A, 7, B, 4, C, 4)
+    assert e.value.status == gtg.GTG_ERR_INVALID_VALUE
+    assert gtg.plan_gemm("f32", 0, 4, 4, A, 4, B, 4, C, 4)["kernel"] == "none"

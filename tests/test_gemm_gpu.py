@@ -1,0 +1,228 @@
+"""GPU parity of the three GEMM paths against the FP64 oracle, through the C ABI.
+
+Bounds (per element, E = sum_k |a_ik b_kj| from the oracle):
+  FP32 |c - ref| <= 4 K 2^-24 E,  TF32 <= 4 2^-11 E,  BF16 <= 4 2^-8 E.
+"""
+
+import numpy as np
+import pytest
+
+import gemv_tiled_gemm_gb300 as gtg
+from seeded import PCG32, gemm_normal_bf16, gemm_uniform_f32
+from tests._gpu import check_gemm, run_gemm, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def inputs(prec, M, N, K, seed):
+    g = PCG32(seed)
+    if prec == "bf16":
+        return g.normal_bf16((M, K)), g.normal_bf16((K, N))
+    return g.uniform_f32((M, K)), g.uniform_f32((K, N))
+
+
+# ---- the workload configurations -------------------------------------------
+
+def test_f32_256_cubed_seed1():
+    A, B = gemm_uniform_f32(1, 256, 256, 256)
+    C = run_gemm("f32", A, B, expect_kernel="simt")
+    check_gemm("f32", A, B, C)
+
+
+@pytest.mark.parametrize("prec,kernel", [("f32", "simt"), ("tf32", "tcgen05")])
+def test_1024_cubed_seed3(prec, kernel):
+    A, B = gemm_uniform_f32(3, 1024, 1024, 1024)
+    C = run_gemm(prec, A, B, expect_kernel=kernel)
+    check_gemm(prec, A, B, C)
+
+
+@pytest.mark.parametrize("prec,kernel", [("f32", "simt"), ("tf32", "tcgen05")])
+def test_ragged_1000x1500x700_seed4(prec, kernel):
+    # M = 1000, K = 1500, N = 700: partial tiles in every dimension
+    A, B = gemm_uniform_f32(4, 1000, 700, 1500)
+    C = run_gemm(prec, A, B, expect_kernel=kernel)
+    check_gemm(prec, A, B, C)
+
+
+def test_bf16_4096_cubed_seed5():
+    (A, B), = gemm_normal_bf16(5, [(4096, 4096, 4096)])
+    C = run_gemm("bf16", A, B, expect_kernel="tcgen05")
+    check_gemm("bf16", A, B, C, rows=sample_rows(4096))
+
+
+@pytest.mark.slow
+def test_bf16_large_and_skinny_seed6():
+    # 8192^3 then 16384 x 4096 x 4096 from one continuing stream, sigma = 1/sqrt(K)
+    shapes = [(8192, 8192, 8192), (16384, 4096, 4096)]
+    for (M, N, K), (A, B) in zip(shapes, gemm_normal_bf16(6, shapes, lambda k: k ** -0.5)):
+        C = run_gemm("bf16", A, B, expect_kernel="tcgen05")
+        check_gemm("bf16", A, B, C, rows=sample_rows(M))
+
+
+# ---- edges, tails and every tile width -----------------------------------------
+
+EDGE = [(1, 1, 1), (7, 5, 3), (127, 129, 65), (129, 127, 1), (1, 300, 17), (300, 1, 17),
+        (33, 65, 257), (128, 256, 64), (257, 513, 129)]
+
+
+@pytest.mark.parametrize("M,N,K", EDGE)
+def test_f32_edge_shapes(M, N, K):
+    A, B = inputs("f32", M, N, K, 100 + M)
+    check_gemm("f32", A, B, run_gemm("f32", A, B))
+
+
+TC_EDGE = [(1, 8, 8), (128, 256, 64), (128, 256, 128), (130, 72, 24), (129, 264, 1000),
+           (300, 64, 8), (512, 256, 4096), (1536, 1536, 64), (1, 520, 72)]
+
+
+@pytest.mark.parametrize("prec", ["tf32", "bf16"])
+@pytest.mark.parametrize("M,N,K", TC_EDGE)
+def test_tcgen05_edge_shapes(prec, M, N, K):
+    A, B = inputs(prec, M, N, K, 200 + N)
+    check_gemm(prec, A, B, run_gemm(prec, A, B, expect_kernel="tcgen05"))
+
+
+@pytest.mark.parametrize("prec", ["tf32", "bf16"])
+def test_every_tile_width_is_exercised(prec):
+    seen = set()
+    for (M, N, K) in [(4096, 4096, 64), (1536, 1536, 64), (1024, 1024, 64)]:
+        A, B = inputs(prec, M, N, K, 7)
+        C = run_gemm(prec, A, B, expect_kernel="tcgen05")
+        check_gemm(prec, A, B, C, rows=sample_rows(M))
+        t = gtg_plan(prec, M, N, K)
+        seen.add(t["bn"])
+    assert seen == {64, 128, 256}
+
+
+def gtg_plan(prec, M, N, K):
+    import torch
+    esz = 2 if prec == "bf16" else 4
+    a = torch.empty(M * K * esz // 4 + 4, dtype=torch.float32, device="cuda")
+    b = torch.empty(K * N * esz // 4 + 4, dtype=torch.float32, device="cuda")
+    c = torch.empty(M * N + 4, dtype=torch.float32, device="cuda")
+    return gtg.plan_gemm(prec, M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N)
+
+
+@pytest.mark.parametrize("prec", ["tf32", "bf16"])
+def test_many_tiles_per_cta(prec):
+    # ~7 output tiles per persistent CTA: exercises both TMEM accumulators and
+    # several phases of every pipeline barrier
+    M, N, K = 8192, 4096, 96
+    A, B = inputs(prec, M, N, K, 9)
+    C = run_gemm(prec, A, B, expect_kernel="tcgen05")
+    check_gemm(prec, A, B, C, rows=sample_rows(M, seed=1))
+    # and every row of one band of tiles, every column
+    check_gemm(prec, A, B, C, rows=np.arange(1024, 1152))
+
+
+# ---- layouts the tensor-memory path cannot take: the SIMT fallback --------------
+
+@pytest.mark.parametrize("prec", ["f32", "tf32", "bf16"])
+def test_padded_leading_dimensions(prec):
+    M, N, K = 200, 136, 96
+    A, B = inputs(prec, M, N, K, 11)
+    C = run_gemm(prec, A, B, lda=K + 8, ldb=N + 24, ldc=N + 5,
+                 expect_kernel="simt" if prec == "f32" else "tcgen05")
+    check_gemm(prec, A, B, C)
+
+
+@pytest.mark.parametrize("prec", ["f32", "tf32", "bf16"])
+def test_unaligned_layouts_fall_back(prec):
+    M, N, K = 97, 61, 43   # odd leading dimensions: no 16-byte rows
+    A, B = inputs(prec, M, N, K, 12)
+    C = run_gemm(prec, A, B, a_off=1, b_off=3, c_off=1, expect_kernel="simt")
+    check_gemm(prec, A, B, C)
+
+
+@pytest.mark.parametrize("prec", ["tf32", "bf16"])
+def test_forced_simt_matches_bound(prec):
+    M, N, K = 256, 192, 320
+    A, B = inputs(prec, M, N, K, 13)
+    gtg.gtg_force_simt(True)
+    try:
+        C = run_gemm(prec, A, B, expect_kernel="simt")
+    finally:
+        gtg.gtg_force_simt(False)
+    check_gemm(prec, A, B, C)
+
+
+# ---- closed forms, exactness, degenerate sizes, determinism --------------------
+
+@pytest.mark.parametrize("prec", ["f32", "tf32", "bf16"])
+def test_identity_gives_B_exactly(prec):
+    M = K = 256
+    N = 320
+    g = PCG32(14)
+    if prec == "bf16":
+        A = np.full((M, K), 0, dtype=np.uint16)
+        A[np.arange(M), np.arange(K)] = 0x3F80          # 1.0
+        B = g.normal_bf16((K, N))
+        from seeded import bf16_bits_to_f32
+        ref = bf16_bits_to_f32(B)
+    else:
+        A = np.eye(M, K, dtype=np.float32)
+        B = g.uniform_f32((K, N))
+        if prec == "tf32":   # values with at most 11 significant bits pass through
+            B = (np.round(B * 1024) / 1024).astype(np.float32)
+        ref = B
+    C = run_gemm(prec, A, B)
+    assert np.array_equal(C, ref)
+
+
+@pytest.mark.parametrize("prec", ["f32", "tf32", "bf16"])
+def test_all_ones_gives_K(prec):
+    M, N, K = 130, 260, 1000
+    if prec == "bf16":
+        A = np.full((M, K), 0x3F80, dtype=np.uint16)
+        B = np.full((K, N), 0x3F80, dtype=np.uint16)
+    else:
+        A = np.ones((M, K), dtype=np.float32)
+        B = np.ones((K, N), dtype=np.float32)
+    assert np.all(run_gemm(prec, A, B) == K)
+
+
+@pytest.mark.parametrize("prec", ["f32", "tf32", "bf16"])
+def test_small_integers_are_exact(prec):
+    # |entries| <= 8, K <= 1024: every partial sum is an integer below 2^24
+    M, N, K = 192, 272, 1024
+    rng = np.random.default_rng(15)
+    Ai = rng.integers(-8, 9, (M, K))
+    Bi = rng.integers(-8, 9, (K, N))
+    ref = (Ai @ Bi).astype(np.float32)
+    if prec == "bf16":
+        from seeded import f64_to_bf16_bits
+        A, B = f64_to_bf16_bits(Ai.astype(np.float64)), f64_to_bf16_bits(Bi.astype(np.float64))
+    else:
+        A, B = Ai.astype(np.float32), Bi.astype(np.float32)
+    assert np.array_equal(run_gemm(prec, A, B), ref)
+
+
+@pytest.mark.parametrize("prec", ["f32", "tf32", "bf16"])
+def test_K_zero_writes_zeros(prec):
+    M, N = 37, 45
+    dt = np.uint16 if prec == "bf16" else np.float32
+    C = run_gemm(prec, np.zeros((M, 0), dtype=dt), np.zeros((0, N), dtype=dt))
+    assert np.all(C == 0)
+
+
+@pytest.mark.parametrize("prec", ["f32", "tf32", "bf16"])
+def test_deterministic(prec):
+    M, N, K = 640, 512, 768
+    A, B = inputs(prec, M, N, K, 16)
+    C1 = run_gemm(prec, A, B)
+    C2 = run_gemm(prec, A, B)
+    assert np.array_equal(C1, C2)
+
+
+def test_side_stream_and_tensor_helper():
+    import torch
+    A, B = gemm_uniform_f32(17, 300, 200, 100)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        C = gtg.matmul(torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda(), "tf32")
+    s.synchronize()
+    check_gemm("tf32", A, B, C.cpu().numpy())
+    # host tensors in, host tensor out (the end-to-end form)
+    Ch = gtg.matmul(torch.from_numpy(A).pin_memory(), torch.from_numpy(B).pin_memory(), "f32")
+    assert not Ch.is_cuda
+    check_gemm("f32", A, B, Ch.numpy())

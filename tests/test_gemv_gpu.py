@@ -1,0 +1,123 @@
+"""GPU parity of gemv_f32 against the FP64 oracle, through the C ABI.
+
+Bound per output: |y - ref| <= 4 N 2^-24 E with E = sum_j |a_ij x_j|.
+"""
+
+import numpy as np
+import pytest
+
+import gemv_tiled_gemm_gb300 as gtg
+import oracle
+from seeded import PCG32, gemv_uniform_f32
+from tests._gpu import run_gemv
+from tests._util import parity_ratio
+
+pytestmark = pytest.mark.gpu
+
+
+def check(A, X, Y):
+    worst = 0.0
+    for b in range(X.shape[0]):
+        ref, E = oracle.gemv(A, X[b])
+        ratio, bad = parity_ratio(Y[b], ref, E, "f32", A.shape[1])
+        assert bad == 0, f"vector {b}: {bad} outputs out of bound (max ratio {ratio:.3g})"
+        worst = max(worst, ratio)
+    return worst
+
+
+def test_fc_layer_4096_seed2_batch1_and_batch8():
+    A, x, X = gemv_uniform_f32(2, 4096, 4096, batch=8)
+    check(A, x[None, :], run_gemv(A, x[None, :]))
+    check(A, X, run_gemv(A, X))
+
+
+@pytest.mark.parametrize("n", [8192, 16384])
+def test_larger_square(n):
+    A, x, X = gemv_uniform_f32(2, n, n, batch=8)
+    check(A, x[None, :], run_gemv(A, x[None, :]))
+    check(A, X[:2], run_gemv(A, X[:2]))
+
+
+@pytest.mark.parametrize("batch", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_every_batch_size(batch):
+    g = PCG32(20 + batch)
+    A = g.uniform_f32((523, 1031))
+    X = g.uniform_f32((batch, 1031))
+    check(A, X, run_gemv(A, X))
+
+
+@pytest.mark.parametrize("M,N", [(1, 1), (1, 5), (5, 1), (3, 7), (31, 33), (152, 4), (151, 4097),
+                                 (2049, 130), (10, 100003)])
+def test_edge_shapes(M, N):
+    g = PCG32(M * 7 + N)
+    A = g.uniform_f32((M, N))
+    X = g.uniform_f32((2, N))
+    check(A, X[:1], run_gemv(A, X[:1]))
+    check(A, X, run_gemv(A, X))
+
+
+def test_vectors_that_do_not_fit_shared_memory():
+    # batch 8 x 7000 entries and batch 1 x 60000 entries exceed one staging
+    # chunk: the chunked loop with barriers on both sides is used
+    g = PCG32(31)
+    A = g.uniform_f32((300, 7000))
+    X = g.uniform_f32((8, 7000))
+    check(A, X, run_gemv(A, X))
+    A = g.uniform_f32((97, 60000))
+    x = g.uniform_f32((1, 60000))
+    check(A, x, run_gemv(A, x))
+
+
+def test_scalar_path_for_unaligned_rows():
+    g = PCG32(32)
+    A = g.uniform_f32((257, 1001))
+    X = g.uniform_f32((3, 1001))
+    check(A, X, run_gemv(A, X, a_off=1))               # A not 16-byte aligned
+    check(A, X, run_gemv(A, X, lda=1003))              # lda not a multiple of 4
+
+
+def test_padded_batch_strides():
+    g = PCG32(33)
+    A = g.uniform_f32((400, 512))
+    X = g.uniform_f32((4, 512))
+    check(A, X, run_gemv(A, X, lda=520, ldx=515, ldy=405))
+
+
+def test_closed_forms():
+    M, N = 300, 4096
+    ones = run_gemv(np.ones((M, N), dtype=np.float32), np.ones((2, N), dtype=np.float32))
+    assert np.all(ones == N)
+    # A with one non-zero per row picks out entries of x exactly
+    rng = np.random.default_rng(34)
+    cols = rng.integers(0, N, M)
+    A = np.zeros((M, N), dtype=np.float32)
+    A[np.arange(M), cols] = 1.0
+    x = PCG32(34).uniform_f32((1, N))
+    assert np.array_equal(run_gemv(A, x)[0], x[0, cols])
+
+
+def test_N_zero_writes_zeros():
+    y = run_gemv(np.zeros((17, 0), dtype=np.float32), np.zeros((3, 0), dtype=np.float32))
+    assert np.all(y == 0)
+
+
+def test_deterministic_and_plan():
+    A, x, X = gemv_uniform_f32(2, 4096, 4096, batch=8)
+    assert np.array_equal(run_gemv(A, X), run_gemv(A, X))
+    import torch
+    dA = torch.from_numpy(A).cuda()
+    dX = torch.from_numpy(X).cuda()
+    dY = torch.empty((8, 4096), device="cuda")
+    plan = gtg.plan_gemv(4096, 4096, dA.data_ptr(), 4096, dX.data_ptr(), 4096, dY.data_ptr(), 4096, 8)
+    assert plan["kernel"] == "gemv"
+    assert plan["grid"] % torch.cuda.get_device_properties(0).multi_processor_count == 0
+
+
+def test_tensor_helper_host_and_device():
+    import torch
+    A, x, X = gemv_uniform_f32(2, 512, 768, batch=3)
+    y = gtg.matvec(torch.from_numpy(A).cuda(), torch.from_numpy(x).cuda()).cpu().numpy()
+    check(A, x[None, :], y[None, :])
+    Y = gtg.matvec(torch.from_numpy(A).pin_memory(), torch.from_numpy(X).pin_memory())
+    assert not Y.is_cuda
+    check(A, X, Y.numpy())
