@@ -1,0 +1,522 @@
+"""Benchmark of the dense-product hot path on GB300.
+
+One step = one pass of the hot path over its workload:
+  * gemm_bf16  M = N = K = 8192, BF16 operands (normal, sigma = 1/sqrt(K),
+    seed 6), FP32 accumulate and output  -- the headline (TFLOP/s);
+  * gemv_f32   y = A x, A 4096 x 4096, batch 1, then batch 8 (uniform [-1, 1),
+    seed 2) -- the fully connected layer (HBM GB/s).
+Every kernel runs through the C ABI (libgtg.so) on the current torch stream.
+`value` is the BF16 GEMM's throughput; the GEMV's is reported beside it with
+its own roofline. The remaining workload configurations are measured after
+the timed region (`configs`, skipped with --no-sweep).
+
+Prints ONE JSON line on rank 0. `--impl reference` times the FP64 CPU oracle
+(the reference arm of this project) on host cores instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s (% of GB300 peak) and GEMV HBM GB/s (% of peak), 1 GPU"
+GEMM_SHAPE = (8192, 8192, 8192)
+GEMV_SHAPE = (4096, 4096)
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["gtg", "reference"], default="gtg")
+    p.add_argument("--no-sweep", action="store_true", help="skip the per-configuration sweep")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=10)
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK), "fallback"
+
+
+def kernel_source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "gemv_tiled_gemm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(key, files):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel source
+    is unchanged since it was taken (else None)."""
+    path = os.path.join(ROOT, "profiles", "counters.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(key)
+    if not e or e.get("source_sha") != kernel_source_sha(files):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the GPU works."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        self.out.flush()
+        self.out.seek(0)
+        rows = []
+        for line in self.out.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]), "power": float(parts[3]),
+                             "hw": parts[5], "hw_thermal": parts[6], "sw_thermal": parts[7],
+                             "power_cap": parts[8]})
+            except ValueError:
+                continue
+        os.unlink(self.out.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        loaded = [r for r in rows if r["power"] > 200.0] or rows
+        reasons = set()
+        for r in loaded:
+            for k, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                            ("sw_thermal", "sw_thermal_slowdown"), ("power_cap", "sw_power_cap")):
+                if r[k].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+                "sm_max_mhz": max(r["max"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(loaded), "power_w_max": max(r["power"] for r in rows)}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def gpu_arm(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import gemv_tiled_gemm_gb300 as gtg
+    from seeded import gemm_normal_bf16, gemm_uniform_f32, gemv_uniform_f32
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    sh = int(stream.cuda_stream)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or 0
+    peaks, peak_src = load_peaks()
+
+    def bf16_dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    def ok(st, what):
+        if st != gtg.GTG_OK:
+            raise gtg.GtgError(st, what)
+
+    # ---- inputs (seeded, synthetic, resident in HBM before timing)
+    M, N, K = GEMM_SHAPE
+    (Ab, Bb), = gemm_normal_bf16(6, [GEMM_SHAPE], lambda k: k ** -0.5)
+    dA, dB = bf16_dev(Ab), bf16_dev(Bb)
+    dC = torch.empty((M, N), dtype=torch.float32, device=dev)
+    gm, gn = GEMV_SHAPE
+    Av, xv, Xv = gemv_uniform_f32(2, gm, gn, batch=8)
+    # four copies of the GEMV operands at distinct addresses: consecutive
+    # launches never find their matrix in L2 (4 x 64 MiB > L2)
+    nrot = max(4, math.ceil(3 * l2 / (4 * gm * gn)) if l2 else 4)
+    vA = [torch.from_numpy(Av).to(dev) for _ in range(nrot)]
+    vx = torch.from_numpy(xv).to(dev)
+    vX = torch.from_numpy(Xv).to(dev)
+    vy = torch.empty(gn, device=dev)
+    vY = torch.empty((8, gm), device=dev)
+
+    def gemm_call():
+        ok(gtg.gemm_bf16(M, N, K, dA.data_ptr(), K, dB.data_ptr(), N, dC.data_ptr(), N, sh), "gemm_bf16")
+
+    def gemv_call(i, batch):
+        A_ = vA[i % nrot]
+        if batch == 1:
+            ok(gtg.gemv_f32(gm, gn, A_.data_ptr(), gn, vx.data_ptr(), gn, vy.data_ptr(), gm, 1, sh), "gemv_f32")
+        else:
+            ok(gtg.gemv_f32(gm, gn, A_.data_ptr(), gn, vX.data_ptr(), gn, vY.data_ptr(), gm, batch, sh),
+               "gemv_f32")
+
+    plan = gtg.plan_gemm("bf16", M, N, K, dA.data_ptr(), K, dB.data_ptr(), N, dC.data_ptr(), N)
+    vplan = gtg.plan_gemv(gm, gn, vA[0].data_ptr(), gn, vx.data_ptr(), gn, vy.data_ptr(), gm, 1)
+
+    # ---- warm-up
+    for i in range(args.warmup):
+        gemm_call()
+        gemv_call(i, 1)
+        gemv_call(i, 8)
+    torch.cuda.synchronize()
+    ok(gtg.gtg_sync_status(sh), "device status after warm-up")
+
+    # ---- timed region: K steps, per-kernel events on the launching stream
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    e_gemm = [(ev(), ev()) for _ in range(args.steps)]
+    e_v1 = [(ev(), ev()) for _ in range(args.steps)]
+    e_v8 = [(ev(), ev()) for _ in range(args.steps)]
+    start, stop = ev(), ev()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clocks:
+        start.record(stream)
+        for i in range(args.steps):
+            e_gemm[i][0].record(stream)
+            gemm_call()
+            e_gemm[i][1].record(stream)
+            e_v1[i][0].record(stream)
+            gemv_call(i, 1)
+            e_v1[i][1].record(stream)
+            e_v8[i][0].record(stream)
+            gemv_call(i + 1, 8)
+            e_v8[i][1].record(stream)
+        stop.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ok(gtg.gtg_sync_status(sh), "device status after timing")
+    launches = 3 * args.steps
+
+    total_ms = start.elapsed_time(stop)
+    gemm_ms = [a.elapsed_time(b) for a, b in e_gemm]
+    v1_ms = [a.elapsed_time(b) for a, b in e_v1]
+    v8_ms = [a.elapsed_time(b) for a, b in e_v8]
+
+    # max over ranks
+    def rank_max(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    total_ms = rank_max(total_ms)
+    gemm_avg = rank_max(sum(gemm_ms) / len(gemm_ms))
+    v1_avg = rank_max(sum(v1_ms) / len(v1_ms))
+    v8_avg = rank_max(sum(v8_ms) / len(v8_ms))
+
+    flops = 2.0 * M * N * K
+    gemm_tflops = world * flops / (gemm_avg * 1e-3) / 1e12
+    v1_bytes = 4.0 * gm * gn + 4.0 * gn + 4.0 * gm
+    v8_bytes = 4.0 * gm * gn + 8 * (4.0 * gn + 4.0 * gm)
+    v1_gbs = world * v1_bytes / (v1_avg * 1e-3) / 1e9
+    v8_gbs = world * v8_bytes / (v8_avg * 1e-3) / 1e9
+
+    long_region = total_ms > 1000.0
+    peak_kind = "sustained" if long_region else "burst"
+    bf16_peak = peaks.get("bf16_tflops_sustained" if long_region else "bf16_tflops")
+    hbm_peak = peaks.get("hbm_gbs")
+    tc_files = ["gemm_tc.cu", "ptx.cuh"]
+    gv_files = ["gemv.cu", "ptx.cuh"]
+    roofline = {"bound": "tensor", "achieved": round(gemm_tflops / world, 1), "peak": bf16_peak,
+                "unit": "TFLOP/s", "frac": round(gemm_tflops / world / bf16_peak, 4),
+                "traffic": committed_traffic("gemm_bf16_8192", tc_files),
+                "peak_source": f"{peak_src} bf16 {peak_kind}",
+                "algorithmic_flops_per_launch": flops, "kernel": "tc_gemm_kernel<bf16>",
+                "plan": plan}
+    gemv_roofline = {"bound": "hbm", "achieved": round(v1_gbs / world, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(v1_gbs / world / hbm_peak, 4),
+                     "traffic": committed_traffic("gemv_f32_4096_b1", gv_files),
+                     "peak_source": f"{peak_src} hbm copy", "algorithmic_bytes_per_launch": v1_bytes,
+                     "kernel": "gemv_kernel<1>", "plan": vplan}
+
+    result = {
+        "metric": METRIC, "value": round(gemm_tflops, 1), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "bf16 GEMM M=N=K=8192 (FP32 accumulate/output) + fp32 GEMV 4096x4096 "
+                               "batch 1 and batch 8", "gemm_seed": 6, "gemm_inputs": "normal(0, 1/sqrt(K)) -> bf16",
+                   "gemv_seed": 2, "gemv_inputs": "uniform[-1,1) fp32",
+                   "l2": f"GEMM inputs 256 MiB + output 256 MiB exceed L2 ({l2 >> 20} MiB); GEMV rotates "
+                         f"{nrot} copies of A ({nrot * 64} MiB)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roofline,
+        "gemv": {"value": round(v1_gbs, 1), "unit": "GB/s", "batch8_gbs": round(v8_gbs, 1),
+                 "batch8_frac": round(v8_gbs / world / hbm_peak, 4), "roofline": gemv_roofline},
+        "gpu_launches": launches,
+        "clocks": clocks.summary(),
+    }
+
+    # ---- end to end through the public API: pinned host buffers in, host result out
+    if args.e2e_steps > 0:
+        hA = torch.from_numpy(Ab.view(np.int16)).view(torch.bfloat16).pin_memory()
+        hB = torch.from_numpy(Bb.view(np.int16)).view(torch.bfloat16).pin_memory()
+        hC = torch.empty((M, N), dtype=torch.float32).pin_memory()
+        for _ in range(2):
+            gtg.matmul(hA, hB, "bf16", out=hC)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            gtg.matmul(hA, hB, "bf16", out=hC)   # copies in, computes, copies out, syncs
+        torch.cuda.synchronize()
+        e2e_s = rank_max(time.perf_counter() - t0)
+        result["e2e"] = {"value": round(world * flops * args.e2e_steps / e2e_s / 1e12, 1), "unit": "TFLOP/s",
+                         "h2d_bytes_per_step": int(hA.numel() * 2 + hB.numel() * 2),
+                         "d2h_bytes_per_step": int(hC.numel() * 4), "steps": args.e2e_steps,
+                         "api": "gemv_tiled_gemm_gb300.matmul(host pinned bf16, 'bf16')"}
+        del hA, hB, hC
+
+    del dA, dB, dC
+    torch.cuda.empty_cache()
+    if not args.no_sweep:
+        result["configs"] = sweep(dev, stream, peaks, l2)
+    return result
+
+
+def time_launches(fn, iters, stream):
+    import torch
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(3):
+        fn(i)
+    torch.cuda.synchronize()
+    s.record(stream)
+    for i in range(iters):
+        fn(i)
+    e.record(stream)
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / iters
+
+
+def sweep(dev, stream, peaks, l2):
+    """Every workload configuration, each timed on its own (back-to-back
+    launches; operands rotated where one set would fit in L2)."""
+    import numpy as np
+    import torch
+
+    import gemv_tiled_gemm_gb300 as gtg
+    from seeded import gemm_normal_bf16, gemm_uniform_f32, gemv_uniform_f32
+
+    sh = int(stream.cuda_stream)
+    out = []
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+
+    def gemm_cfg(name, prec, M, N, K, A, B, peak, peak_name, iters):
+        esz = 2 if prec == "bf16" else 4
+        need = (M * K + K * N) * esz + M * N * 4
+        nrot = max(1, math.ceil(2 * l2 / need)) if l2 else 1
+        if prec == "bf16":
+            mk = lambda X: torch.from_numpy(X.view(np.int16)).view(torch.bfloat16).to(dev)
+        else:
+            mk = lambda X: torch.from_numpy(X).to(dev)
+        sets = [(mk(A), mk(B), torch.empty((M, N), device=dev)) for _ in range(nrot)]
+        fn = {"f32": gtg.gemm_f32, "tf32": gtg.gemm_tf32, "bf16": gtg.gemm_bf16}[prec]
+
+        def call(i):
+            a, b, c = sets[i % nrot]
+            st = fn(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N, sh)
+            assert st == gtg.GTG_OK, st
+
+        ms = time_launches(call, iters, stream)
+        a, b, c = sets[0]
+        plan = gtg.plan_gemm(prec, M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N)
+        tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        out.append({"config": name, "path": prec, "shape": [M, N, K], "ms": round(ms, 4),
+                    "TFLOP/s": round(tf, 2), "peak": peak, "peak_name": peak_name,
+                    "frac": round(tf / peak, 4) if peak else None, "kernel": plan["kernel"],
+                    "tile": [plan["bm"], plan["bn"], plan["bk"]], "grid": plan["grid"], "buffer_sets": nrot})
+        del sets
+
+    # FP32 SIMT peak: SMs x 128 FP32 lanes x 2 flops x the max SM clock
+    f32_peak = sms * 128 * 2 * 2.070e9 / 1e12
+    tf32_peak = peaks.get("bf16_tflops", FALLBACK["bf16_tflops"]) / 2.0
+    bf16_peak = peaks.get("bf16_tflops", FALLBACK["bf16_tflops"])
+
+    A, B = gemm_uniform_f32(1, 256, 256, 256)
+    gemm_cfg("1: f32 256^3", "f32", 256, 256, 256, A, B, f32_peak, "fp32 simt (2070 MHz)", 200)
+    A, B = gemm_uniform_f32(3, 1024, 1024, 1024)
+    gemm_cfg("3a: f32 1024^3", "f32", 1024, 1024, 1024, A, B, f32_peak, "fp32 simt (2070 MHz)", 50)
+    gemm_cfg("3a: tf32 1024^3", "tf32", 1024, 1024, 1024, A, B, tf32_peak, "bf16 burst / 2", 100)
+    A, B = gemm_uniform_f32(4, 1000, 700, 1500)
+    gemm_cfg("3b: f32 1000x700x1500", "f32", 1000, 700, 1500, A, B, f32_peak, "fp32 simt (2070 MHz)", 50)
+    gemm_cfg("3b: tf32 1000x700x1500", "tf32", 1000, 700, 1500, A, B, tf32_peak, "bf16 burst / 2", 100)
+    (A, B), = gemm_normal_bf16(5, [(4096, 4096, 4096)])
+    gemm_cfg("4: bf16 4096^3", "bf16", 4096, 4096, 4096, A, B, bf16_peak, "bf16 burst", 50)
+    shapes = [(8192, 8192, 8192), (16384, 4096, 4096)]
+    (A1, B1), (A2, B2) = gemm_normal_bf16(6, shapes, lambda k: k ** -0.5)
+    gemm_cfg("5a: bf16 8192^3", "bf16", 8192, 8192, 8192, A1, B1, bf16_peak, "bf16 burst", 20)
+    gemm_cfg("5b: bf16 16384x4096x4096", "bf16", 16384, 4096, 4096, A2, B2, bf16_peak, "bf16 burst", 20)
+    del A1, B1, A2, B2
+
+    hbm = peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])
+    for n in (4096, 8192, 16384):
+        Av, xv, Xv = gemv_uniform_f32(2, n, n, batch=8)
+        nrot = max(2, math.ceil(3 * l2 / (4 * n * n))) if l2 else 2
+        As = [torch.from_numpy(Av).to(dev) for _ in range(nrot)]
+        X = torch.from_numpy(Xv).to(dev)
+        Y = torch.empty((8, n), device=dev)
+        for batch in (1, 8):
+            def call(i, batch=batch):
+                st = gtg.gemv_f32(n, n, As[i % nrot].data_ptr(), n, X.data_ptr(), n, Y.data_ptr(), n, batch, sh)
+                assert st == gtg.GTG_OK, st
+            ms = time_launches(call, 100, stream)
+            byt = 4.0 * n * n + batch * 4.0 * (2 * n)
+            gbs = byt / (ms * 1e-3) / 1e9
+            out.append({"config": f"2: f32 gemv {n}x{n} batch {batch}", "path": "gemv_f32", "shape": [n, n],
+                        "batch": batch, "ms": round(ms, 5), "GB/s": round(gbs, 1), "peak": hbm,
+                        "frac": round(gbs / hbm, 4), "buffer_sets": nrot})
+        del As, X, Y
+    torch.cuda.empty_cache()
+    return out
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+_ORACLE_INPUTS = {}
+
+
+def _oracle_inputs(rows: int):
+    """The first `rows` rows of A and all of B of the 8192^3 BF16 workload,
+    widened exactly to FP64 (generated once per process)."""
+    import numpy as np
+
+    from seeded import PCG32, bf16_bits_to_f32
+
+    M, N, K = GEMM_SHAPE
+    if "B" not in _ORACLE_INPUTS:
+        g = PCG32(6)
+        g.next_u32(2 * ((M * K + 1) // 2))        # skip all of A
+        _ORACLE_INPUTS["B"] = bf16_bits_to_f32(g.normal_bf16((K, N), K ** -0.5)).astype(np.float64)
+    if _ORACLE_INPUTS.get("rows", 0) < rows:
+        g = PCG32(6)                              # the first rows of A: same draws as the workload
+        _ORACLE_INPUTS["A"] = bf16_bits_to_f32(g.normal_bf16((rows, K), K ** -0.5)).astype(np.float64)
+        _ORACLE_INPUTS["rows"] = rows
+    return _ORACLE_INPUTS["A"][:rows], _ORACLE_INPUTS["B"]
+
+
+def oracle_gemm_sample(rows: int, threads: int = 0):
+    """The FP64 oracle on `rows` rows of the 8192^3 BF16 workload (full N, K)."""
+    import oracle
+
+    M, N, K = GEMM_SHAPE
+    Af, Bf = _oracle_inputs(rows)
+    t0 = time.perf_counter()
+    oracle.gemm(Af, Bf, threads=threads)
+    return time.perf_counter() - t0, 2.0 * rows * N * K
+
+
+def cpu_baseline(target_s: float = 10.0):
+    import oracle
+    cores = oracle.threads_default()
+    dt, fl = oracle_gemm_sample(4)
+    rows = max(4, min(8192, int(4 * target_s / max(dt, 1e-3))))
+    dt, fl = oracle_gemm_sample(rows)
+    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{rows} rows x 8192 x 8192 of the 8192^3 BF16 GEMM (FP64, with the error magnitude E), "
+                      f"{dt:.1f} s", "seconds": round(dt, 2)}
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    cores = oracle.threads_default()
+    # each step: the oracle on a slab of rows sized to ~2 s
+    dt, fl = oracle_gemm_sample(2)
+    rows = max(2, int(2 * 2.0 / max(dt, 1e-3)))
+    for _ in range(max(0, args.warmup)):
+        oracle_gemm_sample(rows)
+        break  # one warm-up pass is enough for a CPU loop; more only lengthens the run
+    t_total, f_total = 0.0, 0.0
+    for _ in range(args.steps if args.steps <= 20 else 20):
+        dt, fl = oracle_gemm_sample(rows)
+        t_total += dt
+        f_total += fl
+    steps = args.steps if args.steps <= 20 else 20
+    v = f_total / t_total / 1e12
+    sample = f"{rows} rows x 8192 x 8192 of the 8192^3 BF16 GEMM per step (FP64 oracle with E)"
+    return {"metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": round(1000 * t_total / steps, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "bf16 GEMM M=N=K=8192 (row slab per step)", "gemm_seed": 6,
+                       "parallelism": "host threads"},
+            "impl": "reference",
+            "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        res = reference_arm(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = gpu_arm(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -20,8 +20,11 @@
 //     output tiles in groups of GROUP row-tiles for L2 reuse.
 //
 // Operand layouts: A is row-major M x K, i.e. "K-major" for the MMA; B is
-// row-major K x N, i.e. "MN-major". Both are read in their given layout; no
-// transposition pass.
+// row-major K x N, i.e. "MN-major". BF16 operands are read in their given
+// layouts. The TF32 MMA does not take an MN-major B on this hardware (it
+// leaves the accumulator untouched), so for TF32 a transpose kernel first
+// writes B^T (N x K, K-major) into a temporary buffer taken from the
+// device's stream-ordered memory pool, and both operands are then K-major.
 //
 // Every mbarrier wait is bounded in time. On expiry the waiting thread
 // latches GTG_ERR_TIMEOUT in the library status word, raises a shared abort
@@ -30,6 +33,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "internal.h"
@@ -52,18 +56,20 @@ struct Shape {
     static constexpr int UK = 32 / ELEM;           // K per tcgen05.mma
     static constexpr int KSTEPS = BK / UK;
     static constexpr int A_BYTES = BM * 128;       // BM rows x 128 bytes of K
-    static constexpr int BCH_N = 128 / ELEM;       // N elements per 128-byte row of B
-    static constexpr int B_CHUNKS = BN / BCH_N;
-    static constexpr int BCH_BYTES = BK * 128;     // one 128-byte-wide column block of B
-    static constexpr int B_BYTES = B_CHUNKS * BCH_BYTES;
+    static constexpr bool B_KMAJOR = TF32;         // B staged from its transpose
+    static constexpr int BCH_N = 128 / ELEM;       // N elements per 128-byte row of B (MN-major)
+    static constexpr int B_CHUNKS = B_KMAJOR ? 1 : BN / BCH_N;
+    static constexpr int BCH_BYTES = BK * 128;     // one 128-byte-wide column block of B (MN-major)
+    static constexpr int B_BYTES = BN * BK * ELEM; // = BN rows x 128 bytes when K-major
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES_RAW = kSmemBudget / STAGE_BYTES;
     static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
     static constexpr int TMEM_COLS = 2 * BN;       // two FP32 accumulators
     static constexpr int NBARS = 2 * STAGES + 5;
     static constexpr int SMEM = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + NBARS * 8 + 16;
-    static constexpr uint32_t IDESC = ptx::make_idesc(TF32 ? 2u : 1u, 0u, 1u, BM, BN);
+    static constexpr uint32_t IDESC = ptx::make_idesc(TF32 ? 2u : 1u, 0u, B_KMAJOR ? 0u : 1u, BM, BN);
     static_assert(BN % BCH_N == 0 && BN >= 64 && BN <= 256, "tile width");
+    static_assert(B_KMAJOR || B_CHUNKS * BCH_BYTES == B_BYTES, "MN-major B is whole column blocks");
     static_assert(STAGE_BYTES % 1024 == 0, "stages keep 1024-byte alignment");
     static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
                   "TMEM allocation must be a power of two in [32, 512]");
@@ -190,10 +196,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ptx::mbar_arrive_expect_tx(full_bar(s), S::STAGE_BYTES);
                     ptx::tma_load_2d(sA + s * S::A_BYTES, &tmA, full_bar(s), kb * S::BK, mb * S::BM);
+                    if constexpr (S::B_KMAJOR) {
+                        // B^T tile: BN rows of BK elements
+                        ptx::tma_load_2d(sB + s * S::B_BYTES, &tmB, full_bar(s), kb * S::BK, nb * BN);
+                    } else {
 #pragma unroll
-                    for (int c = 0; c < S::B_CHUNKS; ++c)
-                        ptx::tma_load_2d(sB + s * S::B_BYTES + c * S::BCH_BYTES, &tmB, full_bar(s),
-                                         nb * BN + c * S::BCH_N, kb * S::BK);
+                        for (int c = 0; c < S::B_CHUNKS; ++c)
+                            ptx::tma_load_2d(sB + s * S::B_BYTES + c * S::BCH_BYTES, &tmB, full_bar(s),
+                                             nb * BN + c * S::BCH_N, kb * S::BK);
+                    }
                 }
             }
             if (!ok) {
@@ -237,9 +248,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t ad = ptx::smem_desc_sw128(a0 + k * 32, 16, 1024);
                         // B, MN-major, 128B swizzle: 128-byte-wide column blocks BCH_BYTES
                         // apart (leading offset), 8-row K groups 1024 B apart (stride
-                        // offset); the K step moves UK rows of 128 bytes.
-                        const uint64_t bd =
-                            ptx::smem_desc_sw128(b0 + k * S::UK * 128, S::BCH_BYTES, 1024);
+                        // offset); the K step moves UK rows of 128 bytes. K-major B
+                        // (TF32) is laid out like A.
+                        const uint64_t bd = S::B_KMAJOR
+                                                ? ptx::smem_desc_sw128(b0 + k * 32, 16, 1024)
+                                                : ptx::smem_desc_sw128(b0 + k * S::UK * 128, S::BCH_BYTES, 1024);
                         const uint32_t accum = (kb > 0 || k > 0) ? 1u : 0u;
                         if constexpr (TF32)
                             ptx::mma_tf32(d_tmem, ad, bd, S::IDESC, accum);
@@ -312,6 +325,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// B (K x N, leading dimension ldb) -> Bt (N x K, leading dimension ldbt),
+// through a padded shared-memory tile so that reads and writes are both
+// coalesced.
+__global__ void __launch_bounds__(256) transpose_kernel(const float *__restrict__ B, long long ldb,
+                                                        float *__restrict__ Bt, long long ldbt, int K, int N) {
+    __shared__ float tile[32][33];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
+    const int n0 = blockIdx.x * 32;
+    for (int k0 = blockIdx.y * 32; k0 < K; k0 += gridDim.y * 32) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int k = k0 + ty + 8 * j, n = n0 + tx;
+            if (k < K && n < N) tile[ty + 8 * j][tx] = __ldg(B + static_cast<long long>(k) * ldb + n);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int n = n0 + ty + 8 * j, k = k0 + tx;
+            if (n < N && k < K) Bt[static_cast<long long>(n) * ldbt + k] = tile[tx][ty + 8 * j];
+        }
+        __syncthreads();
+    }
+}
+
 // ---------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -369,7 +406,26 @@ cudaError_t launch_impl(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
     }
     CUtensorMap ta, tb;
     if (!encode_2d(&ta, TF32, g.A, g.K, g.M, g.lda, S::BK, S::BM)) return cudaErrorInvalidValue;
-    if (!encode_2d(&tb, TF32, g.B, g.N, g.K, g.ldb, S::BCH_N, S::BK)) return cudaErrorInvalidValue;
+    float *bt = nullptr;
+    if constexpr (S::B_KMAJOR) {
+        const int64_t ldbt = (g.K + 3) / 4 * 4;   // 16-byte rows for the tensor map
+        cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&bt), static_cast<size_t>(g.N * ldbt) * 4, stream);
+        if (e != cudaSuccess) return e;
+        const dim3 tgrid(static_cast<unsigned>((g.N + 31) / 32),
+                         static_cast<unsigned>(std::min<int64_t>((g.K + 31) / 32, 65535)));
+        transpose_kernel<<<tgrid, 256, 0, stream>>>(static_cast<const float *>(g.B), g.ldb, bt, ldbt,
+                                                    static_cast<int>(g.K), static_cast<int>(g.N));
+        if ((e = cudaGetLastError()) != cudaSuccess) {
+            cudaFreeAsync(bt, stream);
+            return e;
+        }
+        if (!encode_2d(&tb, TF32, bt, g.K, g.N, ldbt, S::BK, BN)) {
+            cudaFreeAsync(bt, stream);
+            return cudaErrorInvalidValue;
+        }
+    } else {
+        if (!encode_2d(&tb, TF32, g.B, g.N, g.K, g.ldb, S::BCH_N, S::BK)) return cudaErrorInvalidValue;
+    }
     TcParams p;
     p.C = g.C;
     p.ldc = g.ldc;
@@ -383,7 +439,13 @@ cudaError_t launch_impl(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
     p.status = dev.status;
     p.wait_limit_ns = kWaitLimitNs;
     kern<<<plan.grid, kThreads, S::SMEM, stream>>>(ta, tb, p);
-    return cudaGetLastError();
+    cudaError_t e = cudaGetLastError();
+    if (bt != nullptr) {
+        // stream-ordered: released once the GEMM has finished reading it
+        cudaError_t f = cudaFreeAsync(bt, stream);
+        if (e == cudaSuccess) e = f;
+    }
+    return e;
 }
 
 template <bool TF32, int BN>
@@ -411,8 +473,9 @@ bool tc_eligible(const GemmArgs &g) {
     if (g.prec != GTG_PREC_TF32 && g.prec != GTG_PREC_BF16) return false;
     const int64_t elem = g.prec == GTG_PREC_TF32 ? 4 : 2;
     const auto a = reinterpret_cast<uintptr_t>(g.A), b = reinterpret_cast<uintptr_t>(g.B);
-    if ((a & 15) || (b & 15)) return false;                   // TMA base alignment
-    if ((g.lda * elem) % 16 || (g.ldb * elem) % 16) return false;  // TMA row stride
+    if ((a & 15) || (g.lda * elem) % 16) return false;           // TMA base and row stride of A
+    // BF16 B is read by TMA in place; TF32 B goes through the transpose kernel
+    if (g.prec == GTG_PREC_BF16 && ((b & 15) || (g.ldb * elem) % 16)) return false;
     if (g.M > INT32_MAX || g.N > INT32_MAX || g.K > INT32_MAX) return false;
     if ((g.lda * elem) >= (1ll << 40) || (g.ldb * elem) >= (1ll << 40)) return false;
     return g.M > 0 && g.N > 0 && g.K > 0;

@@ -32,9 +32,10 @@
  *    GTG_ERR_LAUNCH, reported when the launch itself failed). Device-side
  *    failures (a pipeline wait that ran out of time) are latched in a device
  *    status word and returned by gtg_sync_status().
- *  - Allocation: the calls allocate no device memory and do not synchronise.
- *    Per device, the library keeps only host-side state (device properties
- *    and a table of kernel attributes), created on first use.
+ *  - Allocation: the calls do not synchronise and, except for gemm_tf32 on
+ *    its tensor-core path (see there), allocate no device memory. Per device
+ *    the library keeps only host-side state (device properties and a table
+ *    of kernel attributes), created on first use.
  *  - Thread safety: calls may be made concurrently from several host
  *    threads; the host-side state is guarded by a mutex.
  */
@@ -98,9 +99,15 @@ GTG_API gtg_status gemm_f32(int64_t M, int64_t N, int64_t K,
  * ("Matrix Operations", "Performance Considerations": tensor cores). Same
  * arguments and layouts as gemm_f32. Each product uses the operands reduced
  * to TF32 precision (10 explicit mantissa bits) by the tensor core.
- * The tensor-core kernel needs 16-byte aligned A and B and lda, ldb
- * multiples of 4 (the TMA rules); other layouts are computed by the exact
- * FP32 kernel of gemm_f32, whose result also meets the TF32 accuracy.
+ * The TF32 tensor-core MMA reads B only K-major, so the call first writes
+ * B^T into a temporary buffer of 4 * N * roundup(K, 4) bytes. That buffer
+ * comes from the current device's default stream-ordered memory pool
+ * (cudaMallocAsync on `stream`) and is returned to it (cudaFreeAsync on
+ * `stream`) after the multiply, so it never blocks the host; if the pool
+ * cannot supply it the call returns GTG_ERR_LAUNCH and launches nothing.
+ * The tensor-core kernel needs a 16-byte aligned A with lda a multiple of 4
+ * (the TMA rules); other layouts are computed by the exact FP32 kernel of
+ * gemm_f32, whose result also meets the TF32 accuracy.
  */
 GTG_API gtg_status gemm_tf32(int64_t M, int64_t N, int64_t K,
                      const float *A, int64_t lda,
