@@ -25,6 +25,7 @@ LIB_PATH = os.path.join(_PKG, "libgtg.so")
 
 GTG_OK, GTG_ERR_INVALID_VALUE, GTG_ERR_MISALIGNED, GTG_ERR_ALIAS = 0, 1, 2, 3
 GTG_ERR_UNSUPPORTED, GTG_ERR_LAUNCH, GTG_ERR_TIMEOUT, GTG_ERR_DEVICE = 4, 5, 6, 7
+GTG_ERR_SCRATCH_LIMIT = 8
 PREC = {"f32": 0, "tf32": 1, "bf16": 2}
 KERNELS = {0: "none", 1: "simt", 2: "tcgen05", 3: "zero_fill", 4: "gemv"}
 
@@ -47,6 +48,7 @@ SIGNATURES = {
     "gemm_tf32": (_int, [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr]),
     "gemm_bf16": (_int, [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr]),
     "gemv_f32": (_int, [_i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _int, _ptr]),
+    "gemm_tf32_noalloc": (_int, [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr]),
     "gtg_status_string": (ctypes.c_char_p, [_int]),
     "gtg_sync_status": (_int, [_ptr]),
     "gtg_last_cuda_error": (ctypes.c_char_p, []),
@@ -105,6 +107,11 @@ def gemm_bf16(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
 
 def gemv_f32(M, N, A, lda, x, ldx, y, ldy, batch, stream=0) -> int:
     return lib().gemv_f32(M, N, A, lda, x, ldx, y, ldy, batch, stream)
+
+
+def gemm_tf32_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    """gemm_tf32 without any device allocation (fixed 16 MiB scratch; see gtg.h)."""
+    return lib().gemm_tf32_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream)
 
 
 def status_string(status: int) -> str:

@@ -202,6 +202,31 @@ gtg_status gemv_f32(int64_t M, int64_t N, const float *A, int64_t lda, const flo
     return GTG_OK;
 }
 
+gtg_status gemm_tf32_noalloc(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
+                             int64_t ldb, float *C, int64_t ldc, cudaStream_t stream) {
+    const GemmArgs g{GTG_PREC_TF32, M, N, K, A, lda, B, ldb, C, ldc};
+    gtg_status st = validate_gemm(g);
+    if (st != GTG_OK) return st;
+    if (M == 0 || N == 0) return GTG_OK;
+    if (tf32_bt_bytes(N, K) > tf32_fixed_scratch_bytes()) return GTG_ERR_SCRATCH_LIMIT;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != GTG_OK) return st;
+    gtg_plan plan;
+    if ((st = plan_gemm_impl(dev, g, &plan)) != GTG_OK) return st;
+    cudaError_t e = cudaSuccess;
+    switch (plan.kernel) {
+        case GTG_KERNEL_ZERO_FILL: e = zero_fill_launch(g.C, g.M, g.N, g.ldc, stream); break;
+        case GTG_KERNEL_TCGEN05: e = tc_launch_tf32_fixed_scratch(dev, g, plan, stream); break;
+        case GTG_KERNEL_SIMT: e = simt_launch(dev, g, plan, stream); break;
+        default: break;
+    }
+    if (e != cudaSuccess) {
+        note_cuda_error(e);
+        return GTG_ERR_LAUNCH;
+    }
+    return GTG_OK;
+}
+
 const char *gtg_status_string(gtg_status s) {
     switch (s) {
         case GTG_OK: return "success";
@@ -212,6 +237,8 @@ const char *gtg_status_string(gtg_status s) {
         case GTG_ERR_LAUNCH: return "kernel launch failed";
         case GTG_ERR_TIMEOUT: return "a device pipeline wait exceeded its time limit";
         case GTG_ERR_DEVICE: return "CUDA runtime error";
+        case GTG_ERR_SCRATCH_LIMIT:
+            return "problem too large for the fixed scratch of gemm_tf32_noalloc (N * roundup(K, 4) * 4 > 16 MiB)";
         default: return "unknown status";
     }
 }

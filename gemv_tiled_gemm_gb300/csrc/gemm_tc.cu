@@ -526,3 +526,102 @@ cudaError_t tc_launch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &
 }
 
 }  // namespace gtg
+
+// ---------------------------------------------------------------- fixed-scratch TF32 variant
+// For callers that cannot allocate device memory: the B^T staging buffer of
+// the TF32 path lives in a fixed array compiled into the library instead of
+// coming from the memory pool. Every device that loads the library holds the
+// array until the process exits; every call shares it.
+namespace gtg {
+namespace {
+constexpr size_t kFixedScratchBytes = static_cast<size_t>(16) << 20;   // 16 MiB
+}
+
+static __device__ __align__(256) float g_tf32_fixed_scratch[kFixedScratchBytes / sizeof(float)];
+
+size_t tf32_fixed_scratch_bytes() { return kFixedScratchBytes; }
+
+size_t tf32_bt_bytes(int64_t N, int64_t K) {
+    return static_cast<size_t>(N) * static_cast<size_t>((K + 3) / 4 * 4) * sizeof(float);
+}
+
+namespace {
+
+// Device address of the fixed array on `device` (which must be current). In
+// host code the array's name is only a host-side stand-in, so the address is
+// looked up once per device and cached.
+cudaError_t fixed_scratch_address(int device, float **out) {
+    static std::mutex mu;
+    static float *addr[64] = {};
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
+    if (addr[device] == nullptr) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_tf32_fixed_scratch);
+        if (e != cudaSuccess) return e;
+        addr[device] = static_cast<float *>(p);
+    }
+    *out = addr[device];
+    return cudaSuccess;
+}
+
+template <int BN>
+cudaError_t launch_tf32_fixed(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan,
+                              cudaStream_t stream, float *bt, int attr_bit) {
+    using S = Shape<true, BN>;
+    auto kern = tc_gemm_kernel<true, BN>;
+    {
+        AttrCache &ac = attr_cache();
+        std::lock_guard<std::mutex> lk(ac.mu);
+        const int d = dev.id & 63;
+        if (!(ac.done[d] >> attr_bit & 1)) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+            if (e != cudaSuccess) return e;
+            ac.done[d] |= 1ull << attr_bit;
+        }
+    }
+    CUtensorMap ta, tb;
+    if (!encode_2d(&ta, true, g.A, g.K, g.M, g.lda, S::BK, S::BM)) return cudaErrorInvalidValue;
+    const int64_t ldbt = (g.K + 3) / 4 * 4;
+    if (!encode_2d(&tb, true, bt, g.K, g.N, ldbt, S::BK, BN)) return cudaErrorInvalidValue;
+    // B^T overwrites every element the GEMM reads, so the array's previous
+    // contents never matter and nothing needs clearing.
+    const dim3 tgrid(static_cast<unsigned>((g.N + 31) / 32),
+                     static_cast<unsigned>(std::min<int64_t>((g.K + 31) / 32, 65535)));
+    transpose_kernel<<<tgrid, 256, 0, stream>>>(static_cast<const float *>(g.B), g.ldb, bt, ldbt,
+                                                static_cast<int>(g.K), static_cast<int>(g.N));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    TcParams p;
+    p.C = g.C;
+    p.ldc = g.ldc;
+    p.M = static_cast<int>(g.M);
+    p.N = static_cast<int>(g.N);
+    p.num_m = static_cast<int>((g.M + S::BM - 1) / S::BM);
+    p.num_n = static_cast<int>((g.N + BN - 1) / BN);
+    p.num_kb = static_cast<int>((g.K + S::BK - 1) / S::BK);
+    p.num_tiles = p.num_m * p.num_n;
+    p.c_vec = ((reinterpret_cast<uintptr_t>(g.C) & 15) == 0 && (g.ldc & 3) == 0) ? 1 : 0;
+    p.status = dev.status;
+    p.wait_limit_ns = kWaitLimitNs;
+    kern<<<plan.grid, kThreads, S::SMEM, stream>>>(ta, tb, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t tc_launch_tf32_fixed_scratch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan,
+                                         cudaStream_t stream) {
+    if (tf32_bt_bytes(g.N, g.K) > kFixedScratchBytes) return cudaErrorInvalidValue;
+    float *bt = nullptr;
+    const cudaError_t e = fixed_scratch_address(dev.id, &bt);
+    if (e != cudaSuccess) return e;
+    switch (plan.bn) {
+        case 256: return launch_tf32_fixed<256>(dev, g, plan, stream, bt, 0);
+        case 128: return launch_tf32_fixed<128>(dev, g, plan, stream, bt, 2);
+        case 64: return launch_tf32_fixed<64>(dev, g, plan, stream, bt, 4);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace gtg

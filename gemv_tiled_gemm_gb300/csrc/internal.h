@@ -45,6 +45,13 @@ void tc_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan);
 cudaError_t tc_launch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan,
                       cudaStream_t stream);
 
+// ---- TF32 GEMM whose B^T staging buffer is a fixed array in the library
+// (gemm_tc.cu), for callers that cannot allocate device memory
+size_t tf32_fixed_scratch_bytes();
+size_t tf32_bt_bytes(int64_t N, int64_t K);
+cudaError_t tc_launch_tf32_fixed_scratch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan,
+                                         cudaStream_t stream);
+
 // ---- SIMT GEMM (gemm_simt.cu): FP32 or BF16 inputs, FP32 arithmetic
 void simt_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan);
 cudaError_t simt_launch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan,

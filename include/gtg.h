@@ -70,7 +70,8 @@ enum {
     GTG_ERR_UNSUPPORTED = 4,   /* no kernel for this device (not sm_103a / sm_100-class) */
     GTG_ERR_LAUNCH = 5,        /* the CUDA launch failed (cudaGetLastError text via gtg_last_cuda_error) */
     GTG_ERR_TIMEOUT = 6,       /* device side: a pipeline wait exceeded its time limit */
-    GTG_ERR_DEVICE = 7         /* a CUDA runtime call failed (no device, context error, ...) */
+    GTG_ERR_DEVICE = 7,        /* a CUDA runtime call failed (no device, context error, ...) */
+    GTG_ERR_SCRATCH_LIMIT = 8  /* gemm_tf32_noalloc: B^T would not fit its fixed 16 MiB scratch */
 };
 
 /*
@@ -155,6 +156,46 @@ GTG_API gtg_status gemv_f32(int64_t M, int64_t N,
                     float *y, int64_t ldy,
                     int batch,
                     cudaStream_t stream);
+
+/*
+ * gemm_tf32_noalloc -- the product of gemm_tf32, for callers that cannot
+ * allocate device memory. The pages have no counterpart to this entry point;
+ * it exists for users of this library.
+ *
+ * Who needs it: code that must not allocate once it is running. Examples: a
+ * serving process whose own allocator has already reserved nearly all of the
+ * GPU's memory for weights and caches, so a pool allocation would fail or
+ * fragment that reservation; a driver or virtualisation set-up that offers no
+ * stream-ordered memory pools; a latency-critical loop that forbids
+ * allocation calls because their cost is unbounded. gemm_tf32 takes its B^T
+ * staging buffer from the memory pool; this entry point uses instead a fixed
+ * array of 16 MiB that is part of the library's device image.
+ *
+ * Arguments, layouts, result and accuracy are those of gemm_tf32; the caller
+ * still provides A, B and C. The call makes no cudaMalloc, cudaMallocAsync,
+ * cudaFree or other allocating call.
+ *
+ * Limit: B^T takes N * roundup(K, 4) * 4 bytes, which must not exceed the
+ * array's 16 MiB (16777216 bytes; K = N = 2048 just fits). A larger problem
+ * returns GTG_ERR_SCRATCH_LIMIT and launches nothing.
+ *
+ * Sharing: there is one array per device; every device that loads the
+ * library holds it until the process exits, and all calls on that device
+ * share it. It keeps the last call's contents. A call overwrites every
+ * element it reads before reading it, so nothing needs clearing, but two
+ * calls whose GPU work overlaps (issued on streams not ordered with each
+ * other, e.g. from different host threads) race on the array and can give
+ * wrong results: order them, for instance on one stream.
+ *
+ * Set-up: the first call on a device, made with that device current, looks up
+ * the array's device address (cudaGetSymbolAddress) and caches it. Make that
+ * first call before any stream capture begins.
+ */
+GTG_API gtg_status gemm_tf32_noalloc(int64_t M, int64_t N, int64_t K,
+                             const float *A, int64_t lda,
+                             const float *B, int64_t ldb,
+                             float *C, int64_t ldc,
+                             cudaStream_t stream);
 
 /* Static English text for a status code (never NULL). */
 GTG_API const char *gtg_status_string(gtg_status status);
