@@ -3,8 +3,10 @@
 One step = one pass of the hot path over its workload:
   * gemm_bf16  M = N = K = 8192, BF16 operands (normal, sigma = 1/sqrt(K),
     seed 6), FP32 accumulate and output  -- the headline (TFLOP/s);
-  * gemv_f32   y = A x, A 4096 x 4096, batch 1, then batch 8 (uniform [-1, 1),
-    seed 2) -- the fully connected layer (HBM GB/s).
+  * gemv_f32   y = A x with A 4096 x 4096 (uniform [-1, 1), seed 2) -- the
+    fully connected layer (HBM GB/s): GEMV_GROUP back-to-back launches at
+    batch 1 over distinct copies of A (a stack of layers), then
+    GEMV_GROUP launches at batch 8.
 Every kernel runs through the C ABI (libgtg.so) on the current torch stream.
 `value` is the BF16 GEMM's throughput; the GEMV's is reported beside it with
 its own roofline. The remaining workload configurations are measured after
@@ -34,13 +36,14 @@ if ROOT not in sys.path:
 METRIC = "GEMM TFLOP/s (% of GB300 peak) and GEMV HBM GB/s (% of peak), 1 GPU"
 GEMM_SHAPE = (8192, 8192, 8192)
 GEMV_SHAPE = (4096, 4096)
+GEMV_GROUP = 8
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--steps", type=int, default=1500)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["gtg", "reference"], default="gtg")
     p.add_argument("--no-sweep", action="store_true", help="skip the per-configuration sweep")
@@ -199,12 +202,15 @@ def gpu_arm(args, rank, world, local_rank):
     # ---- warm-up
     for i in range(args.warmup):
         gemm_call()
-        gemv_call(i, 1)
-        gemv_call(i, 8)
+        for g in range(GEMV_GROUP):
+            gemv_call(g, 1)
+        for g in range(GEMV_GROUP):
+            gemv_call(g + 1, 8)
     torch.cuda.synchronize()
     ok(gtg.gtg_sync_status(sh), "device status after warm-up")
 
-    # ---- timed region: K steps, per-kernel events on the launching stream
+    # ---- timed region: K steps; events on the launching stream around the
+    # GEMM and around each group of back-to-back GEMV launches
     ev = lambda: torch.cuda.Event(enable_timing=True)
     e_gemm = [(ev(), ev()) for _ in range(args.steps)]
     e_v1 = [(ev(), ev()) for _ in range(args.steps)]
@@ -220,22 +226,24 @@ def gpu_arm(args, rank, world, local_rank):
             gemm_call()
             e_gemm[i][1].record(stream)
             e_v1[i][0].record(stream)
-            gemv_call(i, 1)
+            for g in range(GEMV_GROUP):
+                gemv_call(i * GEMV_GROUP + g, 1)
             e_v1[i][1].record(stream)
             e_v8[i][0].record(stream)
-            gemv_call(i + 1, 8)
+            for g in range(GEMV_GROUP):
+                gemv_call(i * GEMV_GROUP + g + 1, 8)
             e_v8[i][1].record(stream)
         stop.record(stream)
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     ok(gtg.gtg_sync_status(sh), "device status after timing")
-    launches = 3 * args.steps
+    launches = (1 + 2 * GEMV_GROUP) * args.steps
 
     total_ms = start.elapsed_time(stop)
     gemm_ms = [a.elapsed_time(b) for a, b in e_gemm]
-    v1_ms = [a.elapsed_time(b) for a, b in e_v1]
-    v8_ms = [a.elapsed_time(b) for a, b in e_v8]
+    v1_ms = [a.elapsed_time(b) / GEMV_GROUP for a, b in e_v1]
+    v8_ms = [a.elapsed_time(b) / GEMV_GROUP for a, b in e_v8]
 
     # max over ranks
     def rank_max(x):
@@ -280,8 +288,9 @@ def gpu_arm(args, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "bf16 GEMM M=N=K=8192 (FP32 accumulate/output) + fp32 GEMV 4096x4096 "
-                               "batch 1 and batch 8", "gemm_seed": 6, "gemm_inputs": "normal(0, 1/sqrt(K)) -> bf16",
+        "config": {"workload": f"bf16 GEMM M=N=K=8192 (FP32 accumulate/output) + {GEMV_GROUP} x fp32 GEMV "
+                               f"4096x4096 batch 1 + {GEMV_GROUP} x batch 8", "gemm_seed": 6,
+                   "gemm_inputs": "normal(0, 1/sqrt(K)) -> bf16",
                    "gemv_seed": 2, "gemv_inputs": "uniform[-1,1) fp32",
                    "l2": f"GEMM inputs 256 MiB + output 256 MiB exceed L2 ({l2 >> 20} MiB); GEMV rotates "
                          f"{nrot} copies of A ({nrot * 64} MiB)",

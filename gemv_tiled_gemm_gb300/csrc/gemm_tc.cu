@@ -178,6 +178,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // set-up above overlaps the previous kernel's tail (dependent launch);
+    // no global memory is touched before that kernel has completed
+    ptx::wait_prior_grid();
+    ptx::allow_next_grid();
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -389,6 +393,25 @@ AttrCache &attr_cache() {
     return c;
 }
 
+// Launch with programmatic dependent launch allowed: the CTAs may be
+// scheduled while the previous kernel in the stream finishes; the kernel
+// itself waits for that kernel before touching global memory.
+template <typename Kern>
+cudaError_t launch_pdl(Kern kern, int grid, int smem, cudaStream_t stream, const CUtensorMap &ta,
+                       const CUtensorMap &tb, const TcParams &p) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
+}
+
 template <bool TF32, int BN>
 cudaError_t launch_impl(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan,
                         cudaStream_t stream, int attr_bit) {
@@ -438,8 +461,7 @@ cudaError_t launch_impl(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
     p.c_vec = ((reinterpret_cast<uintptr_t>(g.C) & 15) == 0 && (g.ldc & 3) == 0) ? 1 : 0;
     p.status = dev.status;
     p.wait_limit_ns = kWaitLimitNs;
-    kern<<<plan.grid, kThreads, S::SMEM, stream>>>(ta, tb, p);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(kern, plan.grid, S::SMEM, stream, ta, tb, p);
     if (bt != nullptr) {
         // stream-ordered: released once the GEMM has finished reading it
         cudaError_t f = cudaFreeAsync(bt, stream);

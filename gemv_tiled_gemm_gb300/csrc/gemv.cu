@@ -30,8 +30,6 @@
 namespace gtg {
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
 constexpr int kSmemBudget = 200 * 1024;   // per CTA, for the staged vectors
 
 struct GemvParams {
@@ -46,7 +44,7 @@ struct GemvParams {
     int nchunks;
 };
 
-template <int BATCH>
+template <int BATCH, int kThreads>
 __device__ __forceinline__ void stage_x(float *xs, const GemvParams &p, int c0, int len) {
 #pragma unroll
     for (int b = 0; b < BATCH; ++b) {
@@ -139,8 +137,9 @@ __device__ __forceinline__ void accumulate(float (&acc)[ROWS][BATCH], const floa
     }
 }
 
-template <int BATCH, int ROWS, int U, bool VEC>
+template <int BATCH, int ROWS, int U, bool VEC, int kThreads>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
+    constexpr int kWarps = kThreads / 32;
     extern __shared__ float4 xs_raw[];
     float *xs = reinterpret_cast<float *>(xs_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -151,8 +150,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
     const int ntasks = (r_end - r_begin + ROWS - 1) / ROWS;
     const int rounds = (ntasks + kWarps - 1) / kWarps;
 
+    ptx::wait_prior_grid();
+    ptx::allow_next_grid();
     if (p.nchunks == 1) {
-        stage_x<BATCH>(xs, p, 0, p.N);
+        stage_x<BATCH, kThreads>(xs, p, 0, p.N);
         __syncthreads();
     }
     for (int round = 0; round < rounds; ++round) {  // same trip count for every warp
@@ -175,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
             const int len = min(p.chunk, p.N - c0);
             if (p.nchunks > 1) {
                 __syncthreads();              // everyone is done with the previous chunk
-                stage_x<BATCH>(xs, p, c0, len);
+                stage_x<BATCH, kThreads>(xs, p, c0, len);
                 __syncthreads();              // the chunk is in place
             }
             if (active) accumulate<BATCH, ROWS, U, VEC>(acc, arow, xs, p.chunk, c0, len, lane);
@@ -201,28 +202,150 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
     }
 }
 
-template <int BATCH, int ROWS, int U>
-struct GemvKernels {
-    static void *get(bool vec) {
-        return vec ? reinterpret_cast<void *>(gemv_kernel<BATCH, ROWS, U, true>)
-                   : reinterpret_cast<void *>(gemv_kernel<BATCH, ROWS, U, false>);
-    }
-};
+// The main case for one or two vectors: 16-byte aligned rows and all of x in
+// one staging chunk. A warp's work is a flat sequence of iterations (ROWS rows
+// x 32*U float4 columns each); the loads of iteration it+1 are issued before
+// the FMAs of iteration it, and the first loads before x is staged, so the
+// matrix stream starts at once and never drains between iterations. While
+// the previous kernel in the stream is still finishing, the first 4 KB of
+// each of the CTA's rows is already requested into L2 (a prefetch cannot
+// observe stale data: L2 is the point of coherence).
+template <int BATCH, int ROWS, int U, int kThreads>
+__global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const GemvParams p) {
+    constexpr int kWarps = kThreads / 32;
+    extern __shared__ float4 xs_raw[];
+    float *xs = reinterpret_cast<float *>(xs_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r_begin = static_cast<int>(static_cast<long long>(p.M) * blockIdx.x / gridDim.x);
+    const int r_end = static_cast<int>(static_cast<long long>(p.M) * (blockIdx.x + 1) / gridDim.x);
+    const int ntasks = (r_end - r_begin + ROWS - 1) / ROWS;
+    const int my_tasks = ntasks > warp ? (ntasks - warp + kWarps - 1) / kWarps : 0;
+    const int n4 = p.N >> 2;
+    const int ipr = (n4 + 32 * U - 1) / (32 * U);    // iterations per task
+    const int total = my_tasks * ipr;
 
+    if (threadIdx.x < 32) {
+        const uint32_t bytes = min(4096u, static_cast<uint32_t>(n4) * 16u);
+        for (int r = r_begin + static_cast<int>(threadIdx.x); bytes > 0 && r < r_end; r += 32)
+            ptx::prefetch_l2(p.A + static_cast<long long>(r) * p.lda, bytes);
+    }
+    ptx::wait_prior_grid();
+    ptx::allow_next_grid();
+
+    auto row_of = [&](int t, int r) { return r_begin + (warp + t * kWarps) * ROWS + r; };
+    auto load = [&](int it, float4 (&dst)[U][ROWS]) {
+        const int t = it / ipr, blk = it - t * ipr;
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            const float *a = p.A + static_cast<long long>(min(row_of(t, r), r_end - 1)) * p.lda;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = blk * 32 * U + 32 * u + lane;
+                dst[u][r] = j < n4 ? ptx::ld_stream_f4(a + 4 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+    };
+
+    float4 nxt[U][ROWS];
+    if (total > 0) load(0, nxt);
+    stage_x<BATCH, kThreads>(xs, p, 0, p.N);
+    __syncthreads();
+
+    float acc[ROWS][BATCH];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+        for (int b = 0; b < BATCH; ++b) acc[r][b] = 0.f;
+
+    for (int it = 0; it < total; ++it) {
+        float4 cur[U][ROWS];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) cur[u][r] = nxt[u][r];
+        if (it + 1 < total) load(it + 1, nxt);
+        const int t = it / ipr, blk = it - t * ipr;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = blk * 32 * U + 32 * u + lane;
+            if (j < n4) {
+#pragma unroll
+                for (int b = 0; b < BATCH; ++b) {
+                    const float4 xv = reinterpret_cast<const float4 *>(xs + b * p.chunk)[j];
+#pragma unroll
+                    for (int r = 0; r < ROWS; ++r) {
+                        float s = acc[r][b];
+                        s = fmaf(cur[u][r].x, xv.x, s);
+                        s = fmaf(cur[u][r].y, xv.y, s);
+                        s = fmaf(cur[u][r].z, xv.z, s);
+                        s = fmaf(cur[u][r].w, xv.w, s);
+                        acc[r][b] = s;
+                    }
+                }
+            }
+        }
+        if (blk == ipr - 1) {
+            // at most 3 trailing entries when N % 4 != 0
+            const int jt = 4 * n4 + lane;
+            if (jt < p.N) {
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) {
+                    const float a = ptx::ld_stream_f1(p.A + static_cast<long long>(min(row_of(t, r), r_end - 1)) * p.lda + jt);
+#pragma unroll
+                    for (int b = 0; b < BATCH; ++b) acc[r][b] = fmaf(a, xs[b * p.chunk + jt], acc[r][b]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+                for (int b = 0; b < BATCH; ++b) {
+                    float s = acc[r][b];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+                    acc[r][b] = s;
+                }
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+                for (int b = 0; b < BATCH; ++b) {
+                    const int row = row_of(t, r);
+                    if (lane == (r * BATCH + b) % 32 && row < r_end)
+                        p.y[static_cast<long long>(b) * p.ldy + row] = acc[r][b];
+                    acc[r][b] = 0.f;
+                }
+        }
+    }
+}
+
+// batch <= 2 on aligned rows with x in one chunk: 32 warps, one row each;
+// otherwise 16 warps, two rows per task.
+constexpr int kStreamThreads = 1024;
+constexpr int kRoundThreads = 512;
 constexpr int kRows = 2;
 constexpr int kUnroll = 4;
 
-void *kernel_for(int batch, bool vec) {
+template <int BATCH>
+void *pick(bool vec, bool stream) {
+    if (vec && stream && BATCH <= 2) return reinterpret_cast<void *>(gemv_stream_kernel<BATCH, 1, kUnroll, kStreamThreads>);
+    return vec ? reinterpret_cast<void *>(gemv_kernel<BATCH, kRows, kUnroll, true, kRoundThreads>)
+               : reinterpret_cast<void *>(gemv_kernel<BATCH, kRows, kUnroll, false, kRoundThreads>);
+}
+
+void *kernel_for(int batch, bool vec, bool stream) {
     switch (batch) {
-        case 1: return GemvKernels<1, kRows, kUnroll>::get(vec);
-        case 2: return GemvKernels<2, kRows, kUnroll>::get(vec);
-        case 3: return GemvKernels<3, kRows, kUnroll>::get(vec);
-        case 4: return GemvKernels<4, kRows, kUnroll>::get(vec);
-        case 5: return GemvKernels<5, kRows, kUnroll>::get(vec);
-        case 6: return GemvKernels<6, kRows, kUnroll>::get(vec);
-        case 7: return GemvKernels<7, kRows, kUnroll>::get(vec);
-        default: return GemvKernels<8, kRows, kUnroll>::get(vec);
+        case 1: return pick<1>(vec, stream);
+        case 2: return pick<2>(vec, stream);
+        case 3: return pick<3>(vec, stream);
+        case 4: return pick<4>(vec, stream);
+        case 5: return pick<5>(vec, stream);
+        case 6: return pick<6>(vec, stream);
+        case 7: return pick<7>(vec, stream);
+        default: return pick<8>(vec, stream);
     }
+}
+
+bool uses_stream_kernel(const GemvArgs &g, int nchunks) {
+    return g.batch <= 2 && nchunks == 1 && (reinterpret_cast<uintptr_t>(g.A) & 15) == 0 && (g.lda & 3) == 0;
 }
 
 bool gemv_vec(const GemvArgs &g) {
@@ -250,17 +373,18 @@ Layout layout(const GemvArgs &g) {
 
 void gemv_plan(const DeviceInfo &dev, const GemvArgs &g, gtg_plan *plan) {
     const Layout l = layout(g);
-    // One CTA of 16 warps per SM (the kernel keeps up to 128 registers per
-    // thread); every CTA owns an equal share of the rows.
+    // One CTA per SM (it fills the register file); every CTA owns an equal
+    // share of the rows.
     int64_t grid = dev.sms;
     if (grid > g.M) grid = g.M;
+    const bool stream = uses_stream_kernel(g, l.nchunks);
     plan->kernel = GTG_KERNEL_GEMV;
-    plan->bm = kRows;
+    plan->bm = stream ? 1 : kRows;
     plan->bn = l.chunk;
     plan->bk = kUnroll;
     plan->stages = l.nchunks;
     plan->grid = static_cast<int>(std::max<int64_t>(grid, 1));
-    plan->threads = kThreads;
+    plan->threads = stream ? kStreamThreads : kRoundThreads;
     plan->smem = l.smem;
 }
 
@@ -269,7 +393,8 @@ cudaError_t gemv_launch(const DeviceInfo &dev, const GemvArgs &g, const gtg_plan
     (void)dev;
     const Layout l = layout(g);
     const bool vec = gemv_vec(g);
-    void *kern = kernel_for(g.batch, vec);
+    const bool stream_kernel = uses_stream_kernel(g, l.nchunks);
+    void *kern = kernel_for(g.batch, vec, stream_kernel);
     if (l.smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, l.smem);
         if (e != cudaSuccess) return e;
@@ -286,7 +411,19 @@ cudaError_t gemv_launch(const DeviceInfo &dev, const GemvArgs &g, const gtg_plan
     p.chunk = l.chunk;
     p.nchunks = l.nchunks;
     void *args[] = {&p};
-    return cudaLaunchKernel(kern, dim3(plan.grid), dim3(kThreads), args, static_cast<size_t>(l.smem), stream);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.grid);
+    cfg.blockDim = dim3(plan.threads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(l.smem);
+    cfg.stream = stream;
+    // may start while the previous kernel in the stream drains; both kernels
+    // wait for it (griddepcontrol.wait) before reading or writing its data
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, kern, args);
 }
 
 }  // namespace gtg

@@ -185,7 +185,25 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_format, uint32_t a
            (b_mn_major << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// ---------------------------------------------------------------- dependent launch
+// With programmatic dependent launch, a kernel may start while the previous
+// kernel in the stream is finishing. wait_prior_grid() blocks until that
+// kernel has completed and its memory is visible (a no-op without PDL);
+// allow_next_grid() lets the next kernel in the stream be scheduled early.
+__device__ __forceinline__ void wait_prior_grid() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void allow_next_grid() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- loads
+// Bulk prefetch of `bytes` (a multiple of 16) starting at `p` into L2.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // 128-bit read-only streaming load that does not allocate in L1.
 __device__ __forceinline__ float4 ld_stream_f4(const float *p) {
     float4 v;
