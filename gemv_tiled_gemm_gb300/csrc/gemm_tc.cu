@@ -34,6 +34,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "internal.h"
@@ -329,6 +330,246 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------- CTA-pair BF16 kernel
+// Two CTAs of a cluster share one 256 x 256 output tile: each stages its own
+// 128 rows of A and its half (128 columns) of B, and one thread of the even
+// CTA issues tcgen05.mma.cta_group::2 (M = 256), which reads A and B half from
+// each CTA's shared memory and writes each CTA's 128 rows of D into that CTA's
+// TMEM. Per SM this moves 32 KB per 64-deep K slice instead of 48 KB for the
+// same multiply work, so six stages fit and operand delivery keeps up.
+//
+// Synchronisation across the pair: both CTAs' TMA loads complete on the even
+// CTA's full barrier (which expects both CTAs' bytes); the MMA thread's
+// commits are multicast to the empty / accumulator-full barriers of both
+// CTAs; both CTAs' epilogue warps arrive on the even CTA's accumulator-empty
+// barrier. A cluster barrier after set-up and before exit keeps either CTA
+// from touching a peer that has not initialised its barriers or has left.
+struct PairShape {
+    static constexpr int BM = 128;                 // rows per CTA (256 per pair)
+    static constexpr int BN = 256;                 // columns per pair tile
+    static constexpr int BK = 64;                  // BF16 elements = 128 bytes
+    static constexpr int UK = 16;
+    static constexpr int KSTEPS = BK / UK;
+    static constexpr int A_BYTES = BM * 128;       // 16 KB
+    static constexpr int BCH_N = 64;               // columns per 128-byte block of B
+    static constexpr int B_CHUNKS = (BN / 2) / BCH_N;
+    static constexpr int BCH_BYTES = BK * 128;     // 8 KB
+    static constexpr int B_BYTES = B_CHUNKS * BCH_BYTES;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 32 KB per CTA
+    static constexpr int STAGES = 6;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int NBARS = 2 * STAGES + 5;
+    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + NBARS * 8 + 16;
+    static constexpr uint32_t IDESC = ptx::make_idesc(1u, 0u, 1u, 2 * BM, BN);
+    static constexpr int GROUP = 8;                // pair row-tiles per raster group
+};
+
+__device__ __forceinline__ void pair_tile_coords(int t, const TcParams &p, int &mb, int &nb) {
+    const int per_group = PairShape::GROUP * p.num_n;
+    const int g = t / per_group;
+    const int first = g * PairShape::GROUP;
+    const int gs = min(p.num_m - first, PairShape::GROUP);
+    const int r = t - g * per_group;
+    mb = first + r % gs;
+    nb = r / gs;
+}
+
+__device__ __noinline__ void spin_ns(uint64_t ns) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (ptx::globaltimer_ns() - t0 < ns) {
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const TcParams p) {
+    using S = PairShape;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sA = ptx::smem_addr(smem);
+    const uint32_t sB = sA + S::STAGES * S::A_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::STAGES * S::STAGE_BYTES);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + S::NBARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    const uint32_t bar0 = ptx::smem_addr(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (S::STAGES + s); };
+    auto accf_bar = [&](int a) { return bar0 + 8u * (2 * S::STAGES + a); };
+    auto acce_bar = [&](int a) { return bar0 + 8u * (2 * S::STAGES + 2 + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * S::STAGES + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_ctarank();
+    const bool leader = rank == 0;
+    const int cluster_id = static_cast<int>(blockIdx.x >> 1);
+    const int nclusters = static_cast<int>(gridDim.x >> 1);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S::STAGES; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(accf_bar(a), 1);
+            ptx::mbar_init(acce_bar(a), 8);  // 4 epilogue warps in each CTA of the pair
+        }
+        ptx::mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc_pair(ptx::smem_addr(tmem_slot), S::TMEM_COLS);
+        ptx::tmem_relinquish_pair();
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::cluster_sync();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    ptx::wait_prior_grid();
+    ptx::allow_next_grid();
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            const uint32_t leader_full0 = ptx::map_to_rank(full_bar(0), 0);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = cluster_id; ok && t < p.num_tiles; t += nclusters) {
+                int mb, nb;
+                pair_tile_coords(t, p, mb, nb);
+                const int row0 = mb * 2 * S::BM + static_cast<int>(rank) * S::BM;
+                const int col0 = nb * S::BN + static_cast<int>(rank) * (S::BN / 2);
+                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                    const int s = static_cast<int>(it % S::STAGES);
+                    const uint32_t ph = (it / S::STAGES) & 1u;
+                    if (!wait_bar(empty_bar(s), ph ^ 1u, abort_flag, p)) {
+                        ok = false;
+                        break;
+                    }
+                    if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), 2 * S::STAGE_BYTES);
+                    const uint32_t fb = leader_full0 + 8u * s;
+                    ptx::tma_load_2d_pair(sA + s * S::A_BYTES, &tmA, fb, kb * S::BK, row0);
+#pragma unroll
+                    for (int c = 0; c < S::B_CHUNKS; ++c)
+                        ptx::tma_load_2d_pair(sB + s * S::B_BYTES + c * S::BCH_BYTES, &tmB, fb, col0 + c * S::BCH_N,
+                                              kb * S::BK);
+                }
+            }
+            if (!ok) {
+                if (leader) {
+                    const uint32_t n = it < S::STAGES ? it : S::STAGES;
+                    for (uint32_t j = 1; j <= n; ++j) {
+                        const uint32_t i = it - j;
+                        wait_drain(full_bar(static_cast<int>(i % S::STAGES)), (i / S::STAGES) & 1u, p);
+                    }
+                } else {
+                    // this CTA's copies complete on the even CTA's barrier, which it
+                    // cannot wait on; give them ample time to land
+                    spin_ns(200000);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (even CTA only)
+        if (leader && lane == 0) {
+            uint32_t it = 0;
+            int local = 0;
+            bool ok = true;
+            for (int t = cluster_id; ok && t < p.num_tiles; t += nclusters, ++local) {
+                const int acc = local & 1;
+                const uint32_t aph = (static_cast<uint32_t>(local) >> 1) & 1u;
+                if (!wait_bar(acce_bar(acc), aph ^ 1u, abort_flag, p)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * S::BN);
+                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                    const int s = static_cast<int>(it % S::STAGES);
+                    const uint32_t ph = (it / S::STAGES) & 1u;
+                    if (!wait_bar(full_bar(s), ph, abort_flag, p)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after_sync();
+                    const uint32_t a0 = sA + s * S::A_BYTES;
+                    const uint32_t b0 = sB + s * S::B_BYTES;
+#pragma unroll
+                    for (int k = 0; k < S::KSTEPS; ++k) {
+                        const uint64_t ad = ptx::smem_desc_sw128(a0 + k * 32, 16, 1024);
+                        const uint64_t bd = ptx::smem_desc_sw128(b0 + k * S::UK * 128, S::BCH_BYTES, 1024);
+                        ptx::mma_bf16_pair(d_tmem, ad, bd, S::IDESC, (kb > 0 || k > 0) ? 1u : 0u);
+                    }
+                    ptx::mma_commit_pair(empty_bar(s), 0x3);
+                }
+                if (!ok) break;
+                ptx::mma_commit_pair(accf_bar(acc), 0x3);
+            }
+            // both CTAs release TMEM only after every MMA writing it has landed
+            ptx::mma_commit_pair(drain_bar, 0x3);
+        }
+    } else {
+        // ------------------------------------------------ epilogue (both CTAs)
+        const int quarter = warp & 3;
+        const int r_in_tile = quarter * 32 + lane;
+        const uint32_t leader_acce0 = ptx::map_to_rank(acce_bar(0), 0);
+        int local = 0;
+        for (int t = cluster_id; t < p.num_tiles; t += nclusters, ++local) {
+            int mb, nb;
+            pair_tile_coords(t, p, mb, nb);
+            const int acc = local & 1;
+            const uint32_t aph = (static_cast<uint32_t>(local) >> 1) & 1u;
+            if (!wait_bar(accf_bar(acc), aph, abort_flag, p)) break;
+            ptx::tc_fence_after_sync();
+            const int row = mb * 2 * S::BM + static_cast<int>(rank) * S::BM + r_in_tile;
+            const int col0 = nb * S::BN;
+            const bool row_ok = row < p.M;
+            const bool whole = p.c_vec && (col0 + S::BN <= p.N);
+            float *crow = p.C + static_cast<long long>(row) * p.ldc + col0;
+            const uint32_t taddr =
+                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * S::BN);
+#pragma unroll 1
+            for (int c = 0; c < S::BN / 32; ++c) {
+                uint32_t r[32];
+                ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
+                ptx::tmem_ld_wait();
+                if (row_ok) {
+                    if (whole) {
+                        float4 *dst = reinterpret_cast<float4 *>(crow + c * 32);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col0 + c * 32 + j < p.N) crow[c * 32 + j] = __uint_as_float(r[j]);
+                    }
+                }
+            }
+            ptx::tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_cluster(leader_acce0 + 8u * acc);
+        }
+    }
+
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        if (lane == 0) wait_drain(drain_bar, 0u, p);
+        __syncwarp();
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc_pair(tmem_base, S::TMEM_COLS);
+    }
+    __syncwarp();
+    ptx::cluster_sync();
+}
+
 // B (K x N, leading dimension ldb) -> Bt (N x K, leading dimension ldbt),
 // through a padded shared-memory tile so that reads and writes are both
 // coalesced.
@@ -383,6 +624,8 @@ bool encode_2d(CUtensorMap *map, bool tf32, const void *base, uint64_t inner, ui
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
+
+std::atomic<int> g_pair_enabled{1};
 
 struct AttrCache {
     std::mutex mu;
@@ -470,6 +713,65 @@ cudaError_t launch_impl(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
     return e;
 }
 
+cudaError_t launch_pair(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan, cudaStream_t stream) {
+    using S = PairShape;
+    {
+        AttrCache &ac = attr_cache();
+        std::lock_guard<std::mutex> lk(ac.mu);
+        const int d = dev.id & 63;
+        if (!(ac.done[d] >> 6 & 1)) {
+            cudaError_t e =
+                cudaFuncSetAttribute(tc_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+            if (e != cudaSuccess) return e;
+            ac.done[d] |= 1ull << 6;
+        }
+    }
+    CUtensorMap ta, tb;
+    if (!encode_2d(&ta, false, g.A, g.K, g.M, g.lda, S::BK, S::BM)) return cudaErrorInvalidValue;
+    if (!encode_2d(&tb, false, g.B, g.N, g.K, g.ldb, S::BCH_N, S::BK)) return cudaErrorInvalidValue;
+    TcParams p;
+    p.C = g.C;
+    p.ldc = g.ldc;
+    p.M = static_cast<int>(g.M);
+    p.N = static_cast<int>(g.N);
+    p.num_m = static_cast<int>((g.M + 2 * S::BM - 1) / (2 * S::BM));
+    p.num_n = static_cast<int>((g.N + S::BN - 1) / S::BN);
+    p.num_kb = static_cast<int>((g.K + S::BK - 1) / S::BK);
+    p.num_tiles = p.num_m * p.num_n;
+    p.c_vec = ((reinterpret_cast<uintptr_t>(g.C) & 15) == 0 && (g.ldc & 3) == 0) ? 1 : 0;
+    p.status = dev.status;
+    p.wait_limit_ns = kWaitLimitNs;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(plan.grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(S::SMEM);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel, ta, tb, p);
+}
+
+void fill_pair_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
+    using S = PairShape;
+    const int64_t tiles = ((g.M + 2 * S::BM - 1) / (2 * S::BM)) * ((g.N + S::BN - 1) / S::BN);
+    const int64_t clusters = std::min<int64_t>(tiles, dev.sms / 2);
+    plan->kernel = GTG_KERNEL_TCGEN05;
+    plan->bm = 2 * S::BM;
+    plan->bn = S::BN;
+    plan->bk = S::BK;
+    plan->stages = S::STAGES;
+    plan->grid = static_cast<int>(2 * clusters);
+    plan->threads = kThreads;
+    plan->smem = S::SMEM;
+}
+
 template <bool TF32, int BN>
 void fill_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
     using S = Shape<TF32, BN>;
@@ -522,6 +824,17 @@ void tc_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
         }
     }
     const bool tf32 = g.prec == GTG_PREC_TF32;
+    if (!tf32 && (dev.sms & 1) == 0) {
+        // CTA pairs: 256 x 256 tiles on sms/2 clusters, operands 2/3 of the
+        // single-CTA 128 x 256 tile's bytes per SM
+        const int64_t tiles = ((g.M + 255) / 256) * ((g.N + 255) / 256);
+        const int64_t waves = (tiles + dev.sms / 2 - 1) / (dev.sms / 2);
+        const double cost = static_cast<double>(waves) * 256 / 1.15;
+        if (cost < best_cost && g_pair_enabled.load()) {
+            fill_pair_plan(dev, g, plan);
+            return;
+        }
+    }
     switch (widths[best]) {
         case 256: tf32 ? fill_plan<true, 256>(dev, g, plan) : fill_plan<false, 256>(dev, g, plan); break;
         case 128: tf32 ? fill_plan<true, 128>(dev, g, plan) : fill_plan<false, 128>(dev, g, plan); break;
@@ -532,6 +845,7 @@ void tc_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
 cudaError_t tc_launch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan,
                       cudaStream_t stream) {
     const bool tf32 = g.prec == GTG_PREC_TF32;
+    if (!tf32 && plan.bm == 2 * PairShape::BM) return launch_pair(dev, g, plan, stream);
     switch (plan.bn) {
         case 256:
             return tf32 ? launch_impl<true, 256>(dev, g, plan, stream, 0)
