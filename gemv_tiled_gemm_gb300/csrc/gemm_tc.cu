@@ -81,7 +81,7 @@ struct TcParams {
     long long ldc;
     int M, N;
     int num_m, num_n, num_kb, num_tiles;
-    int c_vec;                   // 16-byte stores allowed for whole rows of a tile
+    int c_vec;                   // widest store for whole rows of a tile: 2 = 32 B, 1 = 16 B, 0 = 4 B
     int *status;
     unsigned long long wait_limit_ns;
 };
@@ -301,7 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
                 ptx::tmem_ld_wait();
                 if (row_ok) {
-                    if (whole) {
+                    if (whole && p.c_vec == 2) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) ptx::st_global_v8(crow + c * 32 + 8 * j, r + 8 * j);
+                    } else if (whole) {
                         float4 *dst = reinterpret_cast<float4 *>(crow + c * 32);
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
@@ -539,7 +542,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
                 ptx::tmem_ld_wait();
                 if (row_ok) {
-                    if (whole) {
+                    if (whole && p.c_vec == 2) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) ptx::st_global_v8(crow + c * 32 + 8 * j, r + 8 * j);
+                    } else if (whole) {
                         float4 *dst = reinterpret_cast<float4 *>(crow + c * 32);
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
@@ -595,6 +601,14 @@ __global__ void __launch_bounds__(256) transpose_kernel(const float *__restrict_
 }
 
 // ---------------------------------------------------------------- host side
+// Widest aligned store the epilogue may use for whole rows of C.
+int c_store_width(const GemmArgs &g) {
+    const auto c = reinterpret_cast<uintptr_t>(g.C);
+    if ((c & 31) == 0 && (g.ldc & 7) == 0) return 2;
+    if ((c & 15) == 0 && (g.ldc & 3) == 0) return 1;
+    return 0;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -701,7 +715,7 @@ cudaError_t launch_impl(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
     p.num_n = static_cast<int>((g.N + BN - 1) / BN);
     p.num_kb = static_cast<int>((g.K + S::BK - 1) / S::BK);
     p.num_tiles = p.num_m * p.num_n;
-    p.c_vec = ((reinterpret_cast<uintptr_t>(g.C) & 15) == 0 && (g.ldc & 3) == 0) ? 1 : 0;
+    p.c_vec = c_store_width(g);
     p.status = dev.status;
     p.wait_limit_ns = kWaitLimitNs;
     cudaError_t e = launch_pdl(kern, plan.grid, S::SMEM, stream, ta, tb, p);
@@ -738,7 +752,7 @@ cudaError_t launch_pair(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
     p.num_n = static_cast<int>((g.N + S::BN - 1) / S::BN);
     p.num_kb = static_cast<int>((g.K + S::BK - 1) / S::BK);
     p.num_tiles = p.num_m * p.num_n;
-    p.c_vec = ((reinterpret_cast<uintptr_t>(g.C) & 15) == 0 && (g.ldc & 3) == 0) ? 1 : 0;
+    p.c_vec = c_store_width(g);
     p.status = dev.status;
     p.wait_limit_ns = kWaitLimitNs;
     cudaLaunchConfig_t cfg = {};
@@ -937,7 +951,7 @@ cudaError_t launch_tf32_fixed(const DeviceInfo &dev, const GemmArgs &g, const gt
     p.num_n = static_cast<int>((g.N + BN - 1) / BN);
     p.num_kb = static_cast<int>((g.K + S::BK - 1) / S::BK);
     p.num_tiles = p.num_m * p.num_n;
-    p.c_vec = ((reinterpret_cast<uintptr_t>(g.C) & 15) == 0 && (g.ldc & 3) == 0) ? 1 : 0;
+    p.c_vec = c_store_width(g);
     p.status = dev.status;
     p.wait_limit_ns = kWaitLimitNs;
     kern<<<plan.grid, kThreads, S::SMEM, stream>>>(ta, tb, p);

@@ -269,6 +269,13 @@ __device__ __forceinline__ void allow_next_grid() {
 }
 
 // ---------------------------------------------------------------- loads
+// 256-bit store of 8 floats (32-byte aligned address): one full sector per lane.
+__device__ __forceinline__ void st_global_v8(float *p, const uint32_t *r) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(r[0]), "r"(r[1]),
+                 "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
 // Bulk prefetch of `bytes` (a multiple of 16) starting at `p` into L2.
 __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");

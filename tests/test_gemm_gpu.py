@@ -128,11 +128,13 @@ def test_cta_pair_kernel_ragged(M, N, K):
 
 # ---- layouts the tensor-memory path cannot take: the SIMT fallback --------------
 
+@pytest.mark.parametrize("cpad", [5, 4, 8])
 @pytest.mark.parametrize("prec", ["f32", "tf32", "bf16"])
-def test_padded_leading_dimensions(prec):
+def test_padded_leading_dimensions(prec, cpad):
+    # ldc padding 5 / 4 / 8 selects the epilogue's 4-, 16- and 32-byte stores
     M, N, K = 200, 136, 96
     A, B = inputs(prec, M, N, K, 11)
-    C = run_gemm(prec, A, B, lda=K + 8, ldb=N + 24, ldc=N + 5,
+    C = run_gemm(prec, A, B, lda=K + 8, ldb=N + 24, ldc=N + cpad,
                  expect_kernel="simt" if prec == "f32" else "tcgen05")
     check_gemm(prec, A, B, C)
 
