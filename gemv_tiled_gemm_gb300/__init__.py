@@ -57,6 +57,8 @@ SIGNATURES = {
     "gtg_plan_gemv": (_int, [_i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _int,
                              ctypes.POINTER(GtgPlan)]),
     "gtg_force_simt": (None, [_int]),
+    "gtg_set_wait_limit_ns": (None, [ctypes.c_uint64]),
+    "gtg_test_drop_load": (None, [_int]),
     "gtg_version": (_int, []),
 }
 
@@ -128,6 +130,14 @@ def last_cuda_error() -> str:
 
 def gtg_force_simt(force: bool) -> None:
     lib().gtg_force_simt(1 if force else 0)
+
+
+def gtg_set_wait_limit_ns(ns: int) -> None:
+    lib().gtg_set_wait_limit_ns(ns)
+
+
+def gtg_test_drop_load(slice_index: int) -> None:
+    lib().gtg_test_drop_load(slice_index)
 
 
 def gtg_version() -> int:

@@ -294,6 +294,10 @@ gtg_status gtg_plan_gemv(int64_t M, int64_t N, const float *A, int64_t lda, cons
 
 void gtg_force_simt(int force) { g_force_simt.store(force ? 1 : 0); }
 
+void gtg_set_wait_limit_ns(uint64_t ns) { tc_set_wait_limit_ns(ns); }
+
+void gtg_test_drop_load(int slice) { tc_drop_next_load(slice); }
+
 int gtg_version(void) { return 100; }
 
 }  // extern "C"

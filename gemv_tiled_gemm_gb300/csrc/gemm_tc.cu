@@ -84,6 +84,7 @@ struct TcParams {
     int c_vec;                   // widest store for whole rows of a tile: 2 = 32 B, 1 = 16 B, 0 = 4 B
     int *status;
     unsigned long long wait_limit_ns;
+    int drop_slice;              // testing hook: K slice whose load CTA 0 never issues (-1: none)
 };
 
 __device__ __forceinline__ void tile_coords(int t, const TcParams &p, int &mb, int &nb) {
@@ -199,6 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
+                    if (p.drop_slice == static_cast<int>(it) && blockIdx.x == 0) continue;
                     ptx::mbar_arrive_expect_tx(full_bar(s), S::STAGE_BYTES);
                     ptx::tma_load_2d(sA + s * S::A_BYTES, &tmA, full_bar(s), kb * S::BK, mb * S::BM);
                     if constexpr (S::B_KMAJOR) {
@@ -454,6 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
+                    if (p.drop_slice == static_cast<int>(it) && cluster_id == 0 && leader) continue;
                     if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), 2 * S::STAGE_BYTES);
                     const uint32_t fb = leader_full0 + 8u * s;
                     ptx::tma_load_2d_pair(sA + s * S::A_BYTES, &tmA, fb, kb * S::BK, row0);
@@ -601,6 +604,15 @@ __global__ void __launch_bounds__(256) transpose_kernel(const float *__restrict_
 }
 
 // ---------------------------------------------------------------- host side
+// Testing hooks (process-wide): the pipeline-wait time limit, and one K
+// slice whose load the next tensor-core launch leaves out in CTA 0 so that a
+// wait runs out on purpose.
+std::atomic<unsigned long long> g_wait_limit_ns{kWaitLimitNs};
+std::atomic<int> g_drop_slice{-1};
+
+unsigned long long wait_limit_ns() { return g_wait_limit_ns.load(); }
+int take_drop_slice() { return g_drop_slice.exchange(-1); }
+
 // Widest aligned store the epilogue may use for whole rows of C.
 int c_store_width(const GemmArgs &g) {
     const auto c = reinterpret_cast<uintptr_t>(g.C);
@@ -717,7 +729,8 @@ cudaError_t launch_impl(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
     p.num_tiles = p.num_m * p.num_n;
     p.c_vec = c_store_width(g);
     p.status = dev.status;
-    p.wait_limit_ns = kWaitLimitNs;
+    p.wait_limit_ns = wait_limit_ns();
+    p.drop_slice = take_drop_slice();
     cudaError_t e = launch_pdl(kern, plan.grid, S::SMEM, stream, ta, tb, p);
     if (bt != nullptr) {
         // stream-ordered: released once the GEMM has finished reading it
@@ -754,7 +767,8 @@ cudaError_t launch_pair(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
     p.num_tiles = p.num_m * p.num_n;
     p.c_vec = c_store_width(g);
     p.status = dev.status;
-    p.wait_limit_ns = kWaitLimitNs;
+    p.wait_limit_ns = wait_limit_ns();
+    p.drop_slice = take_drop_slice();
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(plan.grid));
     cfg.blockDim = dim3(kThreads);
@@ -801,6 +815,9 @@ void fill_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
 }
 
 }  // namespace
+
+void tc_set_wait_limit_ns(unsigned long long ns) { g_wait_limit_ns.store(ns ? ns : kWaitLimitNs); }
+void tc_drop_next_load(int slice) { g_drop_slice.store(slice); }
 
 bool tc_supported(const DeviceInfo &dev) {
     // tcgen05 exists on the sm_100 family; this library is built for sm_103a.
@@ -953,7 +970,8 @@ cudaError_t launch_tf32_fixed(const DeviceInfo &dev, const GemmArgs &g, const gt
     p.num_tiles = p.num_m * p.num_n;
     p.c_vec = c_store_width(g);
     p.status = dev.status;
-    p.wait_limit_ns = kWaitLimitNs;
+    p.wait_limit_ns = wait_limit_ns();
+    p.drop_slice = take_drop_slice();
     kern<<<plan.grid, kThreads, S::SMEM, stream>>>(ta, tb, p);
     return cudaGetLastError();
 }

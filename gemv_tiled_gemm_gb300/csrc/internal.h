@@ -45,6 +45,10 @@ void tc_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan);
 cudaError_t tc_launch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan,
                       cudaStream_t stream);
 
+// testing hooks of the tensor-core kernels (gemm_tc.cu)
+void tc_set_wait_limit_ns(unsigned long long ns);
+void tc_drop_next_load(int slice);
+
 // ---- TF32 GEMM whose B^T staging buffer is a fixed array in the library
 // (gemm_tc.cu), for callers that cannot allocate device memory
 size_t tf32_fixed_scratch_bytes();

@@ -245,6 +245,23 @@ GTG_API gtg_status gtg_plan_gemv(int64_t M, int64_t N, const float *A, int64_t l
  */
 GTG_API void gtg_force_simt(int force);
 
+/*
+ * Time limit of every pipeline wait inside the tensor-core kernels, in
+ * nanoseconds (0 restores the default of 2 s). A wait that runs out makes the
+ * kernel stop, release its resources and latch GTG_ERR_TIMEOUT for
+ * gtg_sync_status(). Process-wide; applies to later launches.
+ */
+GTG_API void gtg_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Testing hook for the failure path: the next tensor-core GEMM launch leaves
+ * out the load of K slice `slice` (counted over the tiles of the first CTA or
+ * CTA pair), so the wait for it can only run out. The call that launches it
+ * returns GTG_OK; gtg_sync_status() then reports GTG_ERR_TIMEOUT and later
+ * calls work normally. A negative value cancels a pending drop.
+ */
+GTG_API void gtg_test_drop_load(int slice);
+
 /* Version of this ABI (major * 10000 + minor * 100 + patch). */
 GTG_API int gtg_version(void);
 
