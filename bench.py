@@ -145,6 +145,24 @@ class ClockSampler:
                 "samples": len(loaded), "power_w_max": max(r["power"] for r in rows)}
 
 
+# ------------------------------------------------------------------ ranks
+
+def reduce_max(x: float, world: int, device) -> float:
+    """Maximum of `x` over all ranks (the slowest rank sets the job's time)."""
+    if world == 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, max_seconds: float, scale: float = 1e12) -> float:
+    """Whole-job throughput: every rank processes `units_per_rank` (replicas,
+    weak scaling), and the job takes as long as its slowest rank."""
+    return world * units_per_rank / max_seconds / scale
+
+
 # ------------------------------------------------------------------ GPU arm
 
 def gpu_arm(args, rank, world, local_rank):
@@ -247,11 +265,7 @@ def gpu_arm(args, rank, world, local_rank):
 
     # max over ranks
     def rank_max(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(x, world, dev)
 
     total_ms = rank_max(total_ms)
     gemm_avg = rank_max(sum(gemm_ms) / len(gemm_ms))
@@ -259,11 +273,11 @@ def gpu_arm(args, rank, world, local_rank):
     v8_avg = rank_max(sum(v8_ms) / len(v8_ms))
 
     flops = 2.0 * M * N * K
-    gemm_tflops = world * flops / (gemm_avg * 1e-3) / 1e12
+    gemm_tflops = job_throughput(flops, world, gemm_avg * 1e-3, 1e12)
     v1_bytes = 4.0 * gm * gn + 4.0 * gn + 4.0 * gm
     v8_bytes = 4.0 * gm * gn + 8 * (4.0 * gn + 4.0 * gm)
-    v1_gbs = world * v1_bytes / (v1_avg * 1e-3) / 1e9
-    v8_gbs = world * v8_bytes / (v8_avg * 1e-3) / 1e9
+    v1_gbs = job_throughput(v1_bytes, world, v1_avg * 1e-3, 1e9)
+    v8_gbs = job_throughput(v8_bytes, world, v8_avg * 1e-3, 1e9)
 
     long_region = total_ms > 1000.0
     peak_kind = "sustained" if long_region else "burst"
@@ -315,7 +329,7 @@ def gpu_arm(args, rank, world, local_rank):
             gtg.matmul(hA, hB, "bf16", out=hC)   # copies in, computes, copies out, syncs
         torch.cuda.synchronize()
         e2e_s = rank_max(time.perf_counter() - t0)
-        result["e2e"] = {"value": round(world * flops * args.e2e_steps / e2e_s / 1e12, 1), "unit": "TFLOP/s",
+        result["e2e"] = {"value": round(job_throughput(flops * args.e2e_steps, world, e2e_s), 1), "unit": "TFLOP/s",
                          "h2d_bytes_per_step": int(hA.numel() * 2 + hB.numel() * 2),
                          "d2h_bytes_per_step": int(hC.numel() * 4), "steps": args.e2e_steps,
                          "api": "gemv_tiled_gemm_gb300.matmul(host pinned bf16, 'bf16')"}
