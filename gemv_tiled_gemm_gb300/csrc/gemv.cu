@@ -317,35 +317,156 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const GemvPara
     }
 }
 
-// batch <= 2 on aligned rows with x in one chunk: 32 warps, one row each;
-// otherwise 16 warps, two rows per task.
+// Three or more vectors: a warp's task is ROWS rows x one of WC column
+// segments, so every x value read from shared memory serves ROWS rows (the
+// x reads, not the matrix, are the per-element cost at batch 8) while the
+// few rows per SM still give every warp work. Each task's per-row partial
+// sums go to shared memory and are added in segment order after a barrier,
+// so the result does not depend on scheduling.
+template <int BATCH, int ROWS, int WC, int U, int kThreads>
+__global__ void __launch_bounds__(kThreads, 1) gemv_split_kernel(const GemvParams p) {
+    constexpr int kWarps = kThreads / 32;
+    extern __shared__ float4 xs_raw[];
+    float *xs = reinterpret_cast<float *>(xs_raw);
+    float *part = xs + BATCH * p.chunk;   // [group][segment][row][batch]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r_begin = static_cast<int>(static_cast<long long>(p.M) * blockIdx.x / gridDim.x);
+    const int r_end = static_cast<int>(static_cast<long long>(p.M) * (blockIdx.x + 1) / gridDim.x);
+    const int rows = r_end - r_begin;
+    const int ngroups = (rows + ROWS - 1) / ROWS;
+    const int ntasks = ngroups * WC;
+    const int n4 = p.N >> 2;
+    const int seg4 = ((n4 + WC - 1) / WC + 31) / 32 * 32;   // float4 columns per segment
+
+    if (threadIdx.x < 32) {
+        const uint32_t bytes = min(4096u, static_cast<uint32_t>(n4) * 16u);
+        for (int r = r_begin + static_cast<int>(threadIdx.x); bytes > 0 && r < r_end; r += 32)
+            ptx::prefetch_l2(p.A + static_cast<long long>(r) * p.lda, bytes);
+    }
+    ptx::wait_prior_grid();
+    ptx::allow_next_grid();
+    stage_x<BATCH, kThreads>(xs, p, 0, p.N);
+    __syncthreads();
+
+    for (int task = warp; task < ntasks; task += kWarps) {
+        const int rg = task / WC, cs = task - rg * WC;
+        const float *arow[ROWS];
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r)
+            arow[r] = p.A + static_cast<long long>(min(r_begin + rg * ROWS + r, r_end - 1)) * p.lda;
+        const int j0 = cs * seg4, j1 = min(j0 + seg4, n4);
+        float acc[ROWS][BATCH];
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) acc[r][b] = 0.f;
+
+        auto load = [&](int jb, float4 (&dst)[U][ROWS]) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = jb + 32 * u + lane;
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r)
+                    dst[u][r] = j < j1 ? ptx::ld_stream_f4(arow[r] + 4 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        };
+        float4 nxt[U][ROWS];
+        if (j0 < j1) load(j0, nxt);
+        for (int jb = j0; jb < j1; jb += 32 * U) {
+            float4 cur[U][ROWS];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) cur[u][r] = nxt[u][r];
+            if (jb + 32 * U < j1) load(jb + 32 * U, nxt);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = jb + 32 * u + lane;
+                if (j < j1) {
+#pragma unroll
+                    for (int b = 0; b < BATCH; ++b) {
+                        const float4 xv = reinterpret_cast<const float4 *>(xs + b * p.chunk)[j];
+#pragma unroll
+                        for (int r = 0; r < ROWS; ++r) {
+                            float s = acc[r][b];
+                            s = fmaf(cur[u][r].x, xv.x, s);
+                            s = fmaf(cur[u][r].y, xv.y, s);
+                            s = fmaf(cur[u][r].z, xv.z, s);
+                            s = fmaf(cur[u][r].w, xv.w, s);
+                            acc[r][b] = s;
+                        }
+                    }
+                }
+            }
+        }
+        if (cs == WC - 1) {
+            const int jt = 4 * n4 + lane;   // at most 3 trailing entries
+            if (jt < p.N) {
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) {
+                    const float a = ptx::ld_stream_f1(arow[r] + jt);
+#pragma unroll
+                    for (int b = 0; b < BATCH; ++b) acc[r][b] = fmaf(a, xs[b * p.chunk + jt], acc[r][b]);
+                }
+            }
+        }
+        float *dst = part + static_cast<long long>(task) * ROWS * BATCH;
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) {
+                float v = acc[r][b];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+                if (lane == (r * BATCH + b) % 32) dst[r * BATCH + b] = v;
+            }
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < rows * BATCH; idx += kThreads) {
+        const int rl = idx / BATCH, b = idx - rl * BATCH;
+        const int rg = rl / ROWS, r = rl - rg * ROWS;
+        float v = 0.f;
+#pragma unroll
+        for (int cs = 0; cs < WC; ++cs) v += part[((rg * WC + cs) * ROWS + r) * BATCH + b];
+        p.y[static_cast<long long>(b) * p.ldy + r_begin + rl] = v;
+    }
+}
+
+// Kernel choice, for aligned rows with x in one staging chunk: batch <= 2 ->
+// gemv_stream_kernel (32 warps, one row each); batch >= 3 ->
+// gemv_split_kernel (16 warps, 4 rows x half the columns per task).
+// Otherwise gemv_kernel (16 warps, two rows per task, x chunked if needed).
 constexpr int kStreamThreads = 1024;
 constexpr int kRoundThreads = 512;
 constexpr int kRows = 2;
 constexpr int kUnroll = 4;
+constexpr int kSplitRows = 4, kSplitSegs = 2, kSplitUnroll = 2;
+
+enum class GemvKind { Stream, Split, Round };
 
 template <int BATCH>
-void *pick(bool vec, bool stream) {
-    if (vec && stream && BATCH <= 2) return reinterpret_cast<void *>(gemv_stream_kernel<BATCH, 1, kUnroll, kStreamThreads>);
+void *pick(GemvKind kind, bool vec) {
+    if constexpr (BATCH <= 2) {
+        if (kind == GemvKind::Stream)
+            return reinterpret_cast<void *>(gemv_stream_kernel<BATCH, 1, kUnroll, kStreamThreads>);
+    }
+    if (kind == GemvKind::Split)
+        return reinterpret_cast<void *>(gemv_split_kernel<BATCH, kSplitRows, kSplitSegs, kSplitUnroll, kRoundThreads>);
     return vec ? reinterpret_cast<void *>(gemv_kernel<BATCH, kRows, kUnroll, true, kRoundThreads>)
                : reinterpret_cast<void *>(gemv_kernel<BATCH, kRows, kUnroll, false, kRoundThreads>);
 }
 
-void *kernel_for(int batch, bool vec, bool stream) {
+void *kernel_for(int batch, GemvKind kind, bool vec) {
     switch (batch) {
-        case 1: return pick<1>(vec, stream);
-        case 2: return pick<2>(vec, stream);
-        case 3: return pick<3>(vec, stream);
-        case 4: return pick<4>(vec, stream);
-        case 5: return pick<5>(vec, stream);
-        case 6: return pick<6>(vec, stream);
-        case 7: return pick<7>(vec, stream);
-        default: return pick<8>(vec, stream);
+        case 1: return pick<1>(kind, vec);
+        case 2: return pick<2>(kind, vec);
+        case 3: return pick<3>(kind, vec);
+        case 4: return pick<4>(kind, vec);
+        case 5: return pick<5>(kind, vec);
+        case 6: return pick<6>(kind, vec);
+        case 7: return pick<7>(kind, vec);
+        default: return pick<8>(kind, vec);
     }
-}
-
-bool uses_stream_kernel(const GemvArgs &g, int nchunks) {
-    return g.batch <= 2 && nchunks == 1 && (reinterpret_cast<uintptr_t>(g.A) & 15) == 0 && (g.lda & 3) == 0;
 }
 
 bool gemv_vec(const GemvArgs &g) {
@@ -354,9 +475,11 @@ bool gemv_vec(const GemvArgs &g) {
 
 struct Layout {
     int chunk, nchunks, smem;
+    GemvKind kind;
+    int threads;
 };
 
-Layout layout(const GemvArgs &g) {
+Layout layout(const DeviceInfo &dev, const GemvArgs &g) {
     const int64_t per_entry = 4ll * g.batch;
     int64_t chunk = std::max<int64_t>(4, kSmemBudget / per_entry / 4 * 4);
     const int64_t n_pad = (g.N + 3) / 4 * 4;
@@ -366,35 +489,47 @@ Layout layout(const GemvArgs &g) {
     l.chunk = static_cast<int>(chunk);
     l.nchunks = static_cast<int>(g.N == 0 ? 1 : (g.N + chunk - 1) / chunk);
     l.smem = static_cast<int>(chunk * per_entry);
+    l.kind = GemvKind::Round;
+    l.threads = kRoundThreads;
+    if (gemv_vec(g) && l.nchunks == 1) {
+        if (g.batch <= 2) {
+            l.kind = GemvKind::Stream;
+            l.threads = kStreamThreads;
+        } else {
+            // partial sums of one CTA's rows: groups x segments x rows x batch floats
+            const int64_t rows_cta = (g.M + dev.sms - 1) / dev.sms;
+            const int64_t part = (rows_cta + kSplitRows - 1) / kSplitRows * kSplitSegs * kSplitRows * g.batch * 4;
+            if (l.smem + part <= dev.smem_optin) {
+                l.kind = GemvKind::Split;
+                l.smem = static_cast<int>(l.smem + part);
+            }
+        }
+    }
     return l;
 }
 
 }  // namespace
 
 void gemv_plan(const DeviceInfo &dev, const GemvArgs &g, gtg_plan *plan) {
-    const Layout l = layout(g);
+    const Layout l = layout(dev, g);
     // One CTA per SM (it fills the register file); every CTA owns an equal
     // share of the rows.
     int64_t grid = dev.sms;
     if (grid > g.M) grid = g.M;
-    const bool stream = uses_stream_kernel(g, l.nchunks);
     plan->kernel = GTG_KERNEL_GEMV;
-    plan->bm = stream ? 1 : kRows;
+    plan->bm = l.kind == GemvKind::Stream ? 1 : (l.kind == GemvKind::Split ? kSplitRows : kRows);
     plan->bn = l.chunk;
-    plan->bk = kUnroll;
+    plan->bk = l.kind == GemvKind::Split ? kSplitUnroll : kUnroll;
     plan->stages = l.nchunks;
     plan->grid = static_cast<int>(std::max<int64_t>(grid, 1));
-    plan->threads = stream ? kStreamThreads : kRoundThreads;
+    plan->threads = l.threads;
     plan->smem = l.smem;
 }
 
 cudaError_t gemv_launch(const DeviceInfo &dev, const GemvArgs &g, const gtg_plan &plan,
                         cudaStream_t stream) {
-    (void)dev;
-    const Layout l = layout(g);
-    const bool vec = gemv_vec(g);
-    const bool stream_kernel = uses_stream_kernel(g, l.nchunks);
-    void *kern = kernel_for(g.batch, vec, stream_kernel);
+    const Layout l = layout(dev, g);
+    void *kern = kernel_for(g.batch, l.kind, gemv_vec(g));
     if (l.smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, l.smem);
         if (e != cudaSuccess) return e;
@@ -416,8 +551,8 @@ cudaError_t gemv_launch(const DeviceInfo &dev, const GemvArgs &g, const gtg_plan
     cfg.blockDim = dim3(plan.threads);
     cfg.dynamicSmemBytes = static_cast<size_t>(l.smem);
     cfg.stream = stream;
-    // may start while the previous kernel in the stream drains; both kernels
-    // wait for it (griddepcontrol.wait) before reading or writing its data
+    // may start while the previous kernel in the stream drains; every GEMV
+    // kernel waits for it (griddepcontrol.wait) before reading or writing data
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;

@@ -269,6 +269,24 @@ __device__ __forceinline__ void allow_next_grid() {
 }
 
 // ---------------------------------------------------------------- loads
+// Two independent IEEE FP32 fused multiply-adds (round to nearest) in one
+// instruction: {d.lo, d.hi} = {a.lo * b.lo + c.lo, a.hi * b.hi + c.hi}.
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void fma2(unsigned long long &acc, unsigned long long a, unsigned long long b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+
+__device__ __forceinline__ float sum2(unsigned long long v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return lo + hi;
+}
+
 // 256-bit store of 8 floats (32-byte aligned address): one full sector per lane.
 __device__ __forceinline__ void st_global_v8(float *p, const uint32_t *r) {
     asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(r[0]), "r"(r[1]),

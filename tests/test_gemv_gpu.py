@@ -56,6 +56,23 @@ def test_edge_shapes(M, N):
     check(A, X, run_gemv(A, X))
 
 
+@pytest.mark.parametrize("batch", [3, 4, 5, 6, 7, 8])
+def test_column_split_kernel_with_ragged_rows_and_width(batch):
+    # aligned rows (lda % 4 == 0) but N % 4 != 0, and a row count that leaves
+    # partial 4-row groups in the CTAs: the kernel for batch >= 3
+    g = PCG32(40 + batch)
+    M, N, lda = 1523, 1030, 1032
+    A = g.uniform_f32((M, N))
+    X = g.uniform_f32((batch, N))
+    check(A, X, run_gemv(A, X, lda=lda))
+    import torch
+    dA = torch.empty(M * lda, device="cuda")
+    dX = torch.empty((batch, N), device="cuda")
+    dY = torch.empty((batch, M), device="cuda")
+    plan = gtg.plan_gemv(M, N, dA.data_ptr(), lda, dX.data_ptr(), N, dY.data_ptr(), M, batch)
+    assert plan["bm"] == 4 and plan["threads"] == 512
+
+
 def test_vectors_that_do_not_fit_shared_memory():
     # batch 8 x 7000 entries and batch 1 x 60000 entries exceed one staging
     # chunk: the chunked loop with barriers on both sides is used
