@@ -213,6 +213,11 @@ gtg_status gemm_tf32_noalloc(int64_t M, int64_t N, int64_t K, const float *A, in
     if ((st = current_device(&dev)) != GTG_OK) return st;
     gtg_plan plan;
     if ((st = plan_gemm_impl(dev, g, &plan)) != GTG_OK) return st;
+    if (plan.kernel == GTG_KERNEL_SIMT) {
+        // one K split: the SIMT kernel then writes C directly and needs no workspace
+        plan.grid /= plan.stages;
+        plan.stages = 1;
+    }
     cudaError_t e = cudaSuccess;
     switch (plan.kernel) {
         case GTG_KERNEL_ZERO_FILL: e = zero_fill_launch(g.C, g.M, g.N, g.ldc, stream); break;

@@ -18,6 +18,7 @@
 // are two 16-byte reads; B keeps its row-major layout.
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "internal.h"
@@ -59,12 +60,25 @@ struct SimtTile {
     static_assert(A_V4 >= 1 && B_V4 >= 1, "tile too small for its thread count");
 };
 
+// Split K: with gridDim.z = S > 1 the CTA at blockIdx.z = z multiplies the
+// K range [z * k_per, (z + 1) * k_per) and writes its FP32 partial product to
+// the workspace slice ws + z * M * N (leading dimension N) instead of C;
+// split_reduce_kernel then adds the S slices in order z = 0 .. S-1.
 template <typename T, int BM, int BN, bool VEC>
 __global__ void __launch_bounds__(SimtTile<T, BM, BN, VEC>::THREADS)
     simt_gemm_kernel(int M, int N, int K, const T *__restrict__ A, long long lda,
                      const T *__restrict__ B, long long ldb, float *__restrict__ C, long long ldc,
-                     int c_vec) {
+                     int c_vec, int k_per, float *__restrict__ ws) {
     using L = SimtTile<T, BM, BN, VEC>;
+    if (gridDim.z > 1) {
+        const int z = blockIdx.z;
+        A += static_cast<long long>(z) * k_per;
+        B += static_cast<long long>(z) * k_per * ldb;
+        K = max(0, min(k_per, K - z * k_per));
+        C = ws + static_cast<long long>(z) * M * N;
+        ldc = N;
+        c_vec = (N & 3) == 0;
+    }
     __shared__ __align__(16) float As[2][kBK][BM];
     __shared__ __align__(16) float Bs[2][kBK][BN];
 
@@ -201,6 +215,38 @@ __global__ void __launch_bounds__(SimtTile<T, BM, BN, VEC>::THREADS)
     }
 }
 
+// C[i][j] = sum over z = 0 .. S-1 of ws[z][i][j], in that order. One thread
+// per 4 consecutive columns of a row (16-byte accesses when they are aligned).
+__global__ void split_reduce_kernel(const float *__restrict__ ws, int splits, int M, int N,
+                                    float *__restrict__ C, long long ldc, int vec) {
+    const int n4 = (N + 3) / 4;
+    const long long slice = static_cast<long long>(M) * N;
+    for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+         t < static_cast<long long>(M) * n4; t += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int row = static_cast<int>(t / n4);
+        const int col = static_cast<int>(t - static_cast<long long>(row) * n4) * 4;
+        const long long src = static_cast<long long>(row) * N + col;
+        float *dst = C + static_cast<long long>(row) * ldc + col;
+        if (vec && col + 3 < N) {
+            float4 v = *reinterpret_cast<const float4 *>(ws + src);
+            for (int z = 1; z < splits; ++z) {
+                const float4 w = *reinterpret_cast<const float4 *>(ws + z * slice + src);
+                v.x += w.x;
+                v.y += w.y;
+                v.z += w.z;
+                v.w += w.w;
+            }
+            *reinterpret_cast<float4 *>(dst) = v;
+        } else {
+            for (int c = 0; c < 4 && col + c < N; ++c) {
+                float v = ws[src + c];
+                for (int z = 1; z < splits; ++z) v += ws[z * slice + src + c];
+                dst[c] = v;
+            }
+        }
+    }
+}
+
 __global__ void zero_fill_kernel(float *C, long long M, long long N, long long ldc) {
     const long long total = M * N;
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
@@ -209,20 +255,43 @@ __global__ void zero_fill_kernel(float *C, long long M, long long N, long long l
 }
 
 template <typename T, int BM, int BN, bool VEC>
-cudaError_t launch_one(const GemmArgs &g, cudaStream_t stream) {
+cudaError_t launch_one(const GemmArgs &g, int splits, cudaStream_t stream) {
     using L = SimtTile<T, BM, BN, VEC>;
-    dim3 grid(static_cast<unsigned>((g.N + BN - 1) / BN), static_cast<unsigned>((g.M + BM - 1) / BM));
+    dim3 grid(static_cast<unsigned>((g.N + BN - 1) / BN), static_cast<unsigned>((g.M + BM - 1) / BM),
+              static_cast<unsigned>(splits));
     const int c_vec = ((reinterpret_cast<uintptr_t>(g.C) & 15) == 0 && (g.ldc & 3) == 0) ? 1 : 0;
+    const int k_per = static_cast<int>(((g.K + kBK - 1) / kBK + splits - 1) / splits * kBK);
+    float *ws = nullptr;
+    cudaError_t e;
+    if (splits > 1) {
+        e = cudaMallocAsync(reinterpret_cast<void **>(&ws), static_cast<size_t>(splits) * g.M * g.N * sizeof(float),
+                            stream);
+        if (e != cudaSuccess) return e;
+    }
     simt_gemm_kernel<T, BM, BN, VEC><<<grid, L::THREADS, 0, stream>>>(
         static_cast<int>(g.M), static_cast<int>(g.N), static_cast<int>(g.K),
-        static_cast<const T *>(g.A), g.lda, static_cast<const T *>(g.B), g.ldb, g.C, g.ldc, c_vec);
-    return cudaGetLastError();
+        static_cast<const T *>(g.A), g.lda, static_cast<const T *>(g.B), g.ldb, g.C, g.ldc, c_vec, k_per, ws);
+    e = cudaGetLastError();
+    if (splits > 1) {
+        if (e == cudaSuccess) {
+            const long long quads = g.M * ((g.N + 3) / 4);
+            const unsigned blocks = static_cast<unsigned>(std::min<long long>((quads + 255) / 256, 8192));
+            // ws rows are N floats, 256-byte aligned base: 16-byte accesses need N % 4 == 0
+            const int vec = ((g.N & 3) == 0 && c_vec) ? 1 : 0;
+            split_reduce_kernel<<<blocks, 256, 0, stream>>>(ws, splits, static_cast<int>(g.M), static_cast<int>(g.N),
+                                                            g.C, g.ldc, vec);
+            e = cudaGetLastError();
+        }
+        const cudaError_t f = cudaFreeAsync(ws, stream);   // stream-ordered: after the reduction
+        if (e == cudaSuccess) e = f;
+    }
+    return e;
 }
 
 template <typename T, bool VEC>
 cudaError_t launch_typed(const GemmArgs &g, const gtg_plan &plan, cudaStream_t stream) {
-    if (plan.bm == 128) return launch_one<T, 128, 128, VEC>(g, stream);
-    return launch_one<T, 64, 64, VEC>(g, stream);
+    if (plan.bm == 128) return launch_one<T, 128, 128, VEC>(g, plan.stages, stream);
+    return launch_one<T, 64, 64, VEC>(g, plan.stages, stream);
 }
 
 bool vec_ok(const GemmArgs &g) {
@@ -234,17 +303,43 @@ bool vec_ok(const GemmArgs &g) {
 
 }  // namespace
 
+// Tile: 128 x 128 (8 warps) when there are enough such tiles for every SM,
+// else 64 x 64 (2 warps). Small grids then split K (plan->stages = splits)
+// so that about six CTAs run on every SM, each split keeping at least two
+// 16-deep K slices; the partial products go through a workspace.
 void simt_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
     const int64_t big_tiles = ((g.M + 127) / 128) * ((g.N + 127) / 128);
     const bool big = big_tiles >= dev.sms;
     plan->kernel = GTG_KERNEL_SIMT;
     plan->bm = plan->bn = big ? 128 : 64;
     plan->bk = kBK;
-    plan->stages = 2;
     plan->threads = big ? 256 : 64;
     plan->smem = 0;
     const int64_t tiles = ((g.M + plan->bm - 1) / plan->bm) * ((g.N + plan->bn - 1) / plan->bn);
-    plan->grid = static_cast<int>(tiles);
+    int64_t splits = 1;
+    if (!big) {
+        // the busiest SM's K work: ceil(CTAs / SMs) CTAs of ceil(slices / S)
+        // slices each; a split must save more than a fixed allowance for the
+        // extra partial-product traffic and the reduction launch
+        const int64_t kslices = (g.K + kBK - 1) / kBK;
+        auto work = [&](int64_t sp) {
+            const int64_t per = (kslices + sp - 1) / sp;
+            return static_cast<double>((tiles * sp + dev.sms - 1) / dev.sms) * per + (sp > 1 ? 0.25 * kslices + 4 : 0);
+        };
+        double best = work(1);
+        for (int64_t sp = 2; sp <= 16 && sp <= kslices / 2; ++sp) {
+            const double w = work(sp);
+            if (w < best) {
+                best = w;
+                splits = sp;
+            }
+        }
+        // every split must own at least one K slice
+        const int64_t k_per = (kslices + splits - 1) / splits;
+        splits = (kslices + k_per - 1) / k_per;
+    }
+    plan->stages = static_cast<int>(splits);
+    plan->grid = static_cast<int>(tiles * splits);
 }
 
 cudaError_t simt_launch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan,

@@ -32,10 +32,16 @@
  *    GTG_ERR_LAUNCH, reported when the launch itself failed). Device-side
  *    failures (a pipeline wait that ran out of time) are latched in a device
  *    status word and returned by gtg_sync_status().
- *  - Allocation: the calls do not synchronise and, except for gemm_tf32 on
- *    its tensor-core path (see there), allocate no device memory. Per device
- *    the library keeps only host-side state (device properties and a table
- *    of kernel attributes), created on first use.
+ *  - Allocation: the calls never synchronise. Two paths need a temporary
+ *    device buffer and take it from the current device's default
+ *    stream-ordered memory pool (cudaMallocAsync on `stream`, returned with
+ *    cudaFreeAsync on `stream` after use, so the host never waits): the TF32
+ *    tensor-core path (B^T, see gemm_tf32) and the SIMT path of small
+ *    problems, which splits K and adds the partial products (splits * M * N
+ *    * 4 bytes, see gemm_f32). gemv_f32 and the BF16 tensor-core path
+ *    allocate nothing; gemm_tf32_noalloc never allocates. Per device the
+ *    library keeps only host-side state (device properties and a table of
+ *    kernel attributes), created on first use.
  *  - Thread safety: calls may be made concurrently from several host
  *    threads; the host-side state is guarded by a mutex.
  */
@@ -87,6 +93,10 @@ enum {
  *   C          M x N, leading dimension ldc >= max(N, 1), overwritten
  * Pointers must be 4-byte aligned. 16-byte alignment and ld % 4 == 0 enable
  * 128-bit loads; other layouts use a scalar-load variant with the same result.
+ * When the output has too few tiles to keep every SM busy, K is split into
+ * up to 16 ranges computed concurrently; their FP32 partial products go to a
+ * pool buffer of splits * M * N * 4 bytes and are added in a fixed order
+ * (results are the same run to run).
  */
 GTG_API gtg_status gemm_f32(int64_t M, int64_t N, int64_t K,
                     const float *A, int64_t lda,
@@ -173,7 +183,8 @@ GTG_API gtg_status gemv_f32(int64_t M, int64_t N,
  *
  * Arguments, layouts, result and accuracy are those of gemm_tf32; the caller
  * still provides A, B and C. The call makes no cudaMalloc, cudaMallocAsync,
- * cudaFree or other allocating call.
+ * cudaFree or other allocating call (on the SIMT path it multiplies without
+ * splitting K).
  *
  * Limit: B^T takes N * roundup(K, 4) * 4 bytes, which must not exceed the
  * array's 16 MiB (16777216 bytes; K = N = 2048 just fits). A larger problem
