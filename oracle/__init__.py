@@ -60,6 +60,8 @@ def _bind(lib):
     lib.oracle_gemm_f64.restype = ci
     lib.oracle_gemv_f64.argtypes = [i64, i64, dp, i64, dp, dp, dp]
     lib.oracle_gemv_f64.restype = ci
+    lib.oracle_bias_act_f64.argtypes = [i64, i64, dp, i64, dp, ci, ci]
+    lib.oracle_bias_act_f64.restype = ci
     lib.oracle_threads_default.argtypes = []
     lib.oracle_threads_default.restype = ci
     return lib
@@ -124,3 +126,38 @@ def gemv(A, x, with_E: bool = True, lib=None):
     if rc != 0:
         raise RuntimeError(f"oracle_gemv_f64 returned {rc}")
     return (y, E) if with_E else y
+
+
+ACT = {"none": 0, "relu": 1}
+
+
+def bias_act(C, bias=None, per_column=True, act="none", lib=None):
+    """act(C + bias) in FP64 on a copy of C (bias per column, or per row)."""
+    lib = lib or load()
+    C = np.array(C, dtype=np.float64, order="C", copy=True)
+    if C.ndim == 1:
+        C = C[:, None]
+        squeeze = True
+    else:
+        squeeze = False
+    M, N = C.shape
+    b = None if bias is None else _as_f64(bias)
+    if b is not None and b.size != (N if per_column else M):
+        raise ValueError("bias length must match the output columns (per_column) or rows")
+    rc = lib.oracle_bias_act_f64(M, N, _ptr(C), max(N, 1), _ptr(b) if b is not None else None,
+                                 1 if per_column else 0, ACT[act])
+    if rc != 0:
+        raise RuntimeError(f"oracle_bias_act_f64 returned {rc}")
+    return C[:, 0] if squeeze else C
+
+
+def dense_layer(A, B, bias=None, act="none", threads=0, lib=None):
+    """act(A @ B + bias), bias per output column (a batch of inputs in A's rows)."""
+    C, E = gemm(A, B, threads=threads, lib=lib)
+    return bias_act(C, bias, True, act, lib=lib), E
+
+
+def dense_vector(A, x, bias=None, act="none", lib=None):
+    """act(A @ x + bias), bias per output row (one fully connected layer)."""
+    y, E = gemv(A, x, lib=lib)
+    return bias_act(y, bias, False, act, lib=lib), E

@@ -20,6 +20,15 @@
  *   E[i][j] = sum_k |A[i][k] * B[k][j]|     (E[i] = sum_j |A[i][j] x[j]|)
  * which scales the per-element acceptance bounds used by the tests.
  *
+ * A fully connected layer adds a bias to each output and applies an
+ * activation ("Matrix Operations": fully connected layers are the
+ * matrix-vector products, activation functions add the non-linearity):
+ *
+ *   out = act(product + bias),  act = identity or ReLU(v) = max(v, 0),
+ *
+ * with one bias per output column for the GEMM (C = X * W^T, a batch of
+ * inputs in the rows of X) and one per output row for the GEMV (y = W x).
+ *
  * Every matrix is row-major with an explicit leading dimension (the pages
  * index A[row*K + k], B[k*N + col], C[row*N + col]; a leading dimension
  * larger than the row length only skips padding).
@@ -149,6 +158,22 @@ int oracle_gemv_f64(int64_t M, int64_t N,
         }
         y[i] = sum;
         if (E) E[i] = mag;
+    }
+    return 0;
+}
+
+int oracle_bias_act_f64(int64_t M, int64_t N, double *C, int64_t ldc,
+                        const double *bias, int bias_per_column, int act)
+{
+    if (M < 0 || N < 0 || (M > 0 && N > 0 && (!C || ldc < N))) return 1;
+    if (act != 0 && act != 1) return 1;
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            double v = C[i * ldc + j];
+            if (bias) v += bias_per_column ? bias[j] : bias[i];
+            if (act == 1 && v < 0.0) v = 0.0;
+            C[i * ldc + j] = v;
+        }
     }
     return 0;
 }

@@ -31,6 +31,12 @@ int oracle_gemv_f64(int64_t M, int64_t N,
                     const double *x,
                     double *y, double *E);
 
+/* In place: C[i][j] = act(C[i][j] + bias), bias[j] when bias_per_column
+ * (GEMM: one bias per output column), else bias[i] (GEMV: one per row);
+ * bias may be NULL. act: 0 = identity, 1 = ReLU, max(v, 0). */
+int oracle_bias_act_f64(int64_t M, int64_t N, double *C, int64_t ldc,
+                        const double *bias, int bias_per_column, int act);
+
 /* Number of threads nthreads <= 0 resolves to. */
 int oracle_threads_default(void);
 

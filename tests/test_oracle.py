@@ -174,7 +174,31 @@ def pin_thread_invariance(lib):
         assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
 
 
-PINS = [pin_golden_gemm, pin_golden_gemv, pin_identity, pin_all_ones,
+def pin_golden_dense_layer(lib):
+    """Hand-worked batch of a fully connected layer: bias per column, ReLU."""
+    g = read_golden("dense_layer_hand.txt")
+    lin, _ = oracle.dense_layer(g["X"], g["WT"], g["bias"][0], "none", lib=lib)
+    out, _ = oracle.dense_layer(g["X"], g["WT"], g["bias"][0], "relu", lib=lib)
+    assert np.array_equal(lin, g["linear"]) and np.array_equal(out, g["relu"])
+
+
+def pin_bias_act_closed_forms(lib):
+    """A = 0 gives act(bias); ReLU keeps non-negative values and zeroes the
+    rest; a GEMV bias is per row, a GEMM bias per column."""
+    rng = np.random.default_rng(19)
+    b = rng.uniform(-1, 1, 6)
+    out, _ = oracle.dense_layer(np.zeros((4, 5)), np.zeros((5, 6)), b, "relu", lib=lib)
+    assert np.array_equal(out, np.tile(np.maximum(b, 0), (4, 1)))
+    y, _ = oracle.dense_vector(np.zeros((6, 3)), np.ones(3), b, "none", lib=lib)
+    assert np.array_equal(y, b)
+    v = rng.uniform(-1, 1, (7, 9))
+    r = oracle.bias_act(v, None, True, "relu", lib=lib)
+    assert np.array_equal(r, np.where(v > 0, v, 0.0))
+    rows = oracle.bias_act(np.zeros((3, 2)), np.array([1.0, -2.0, 3.0]), False, "none", lib=lib)
+    assert np.array_equal(rows, np.array([[1.0, 1.0], [-2.0, -2.0], [3.0, 3.0]]))
+
+
+PINS = [pin_golden_dense_layer, pin_bias_act_closed_forms, pin_golden_gemm, pin_golden_gemv, pin_identity, pin_all_ones,
         pin_small_integers_exact, pin_exact_rational, pin_rank_one,
         pin_gemv_is_gemm_with_one_column, pin_magnitude, pin_vs_library_matmul,
         pin_leading_dimensions, pin_empty_sum, pin_thread_invariance]

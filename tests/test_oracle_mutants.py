@@ -39,6 +39,13 @@ MUTANTS = {
     "gemv_wrong_x_index": [("A[i * lda + j] * x[j]", "A[i * lda + j] * x[i % N]")],
     "gemv_float_accumulator": [("double sum = 0.0, mag = 0.0;",
                                 "float sum = 0.0f; double mag = 0.0;")],
+    "bias_on_wrong_axis": [("if (bias) v += bias_per_column ? bias[j] : bias[i];",
+                            "if (bias) v += bias_per_column ? bias[i % N] : bias[j % M];")],
+    "bias_subtracted": [("if (bias) v += bias_per_column ? bias[j] : bias[i];",
+                         "if (bias) v -= bias_per_column ? bias[j] : bias[i];")],
+    "relu_as_abs": [("if (act == 1 && v < 0.0) v = 0.0;", "if (act == 1 && v < 0.0) v = -v;")],
+    "relu_before_bias": [("            double v = C[i * ldc + j];\n            if (bias) v += bias_per_column ? bias[j] : bias[i];\n            if (act == 1 && v < 0.0) v = 0.0;",
+                          "            double v = C[i * ldc + j];\n            if (act == 1 && v < 0.0) v = 0.0;\n            if (bias) v += bias_per_column ? bias[j] : bias[i];")],
 }
 
 RUNNER = r"""
