@@ -369,7 +369,7 @@ def sweep(dev, stream, peaks, l2):
     out = []
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
 
-    def gemm_cfg(name, prec, M, N, K, A, B, peak, peak_name, iters):
+    def gemm_cfg(name, prec, M, N, K, A, B, peak, peak_name, iters, bias=None, act="none"):
         esz = 2 if prec == "bf16" else 4
         need = (M * K + K * N) * esz + M * N * 4
         nrot = max(1, math.ceil(2 * l2 / need)) if l2 else 1
@@ -378,11 +378,13 @@ def sweep(dev, stream, peaks, l2):
         else:
             mk = lambda X: torch.from_numpy(X).to(dev)
         sets = [(mk(A), mk(B), torch.empty((M, N), device=dev)) for _ in range(nrot)]
-        fn = {"f32": gtg.gemm_f32, "tf32": gtg.gemm_tf32, "bf16": gtg.gemm_bf16}[prec]
+        fn = {"f32": gtg.gemm_f32_ex, "tf32": gtg.gemm_tf32_ex, "bf16": gtg.gemm_bf16_ex}[prec]
+        dbias = torch.from_numpy(bias).to(dev) if bias is not None else None
+        ep = gtg.epilogue(dbias.data_ptr() if dbias is not None else 0, act) if (bias is not None or act != "none") else None
 
         def call(i):
             a, b, c = sets[i % nrot]
-            st = fn(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N, sh)
+            st = fn(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N, ep, sh)
             assert st == gtg.GTG_OK, st
 
         ms = time_launches(call, iters, stream)
@@ -414,23 +416,35 @@ def sweep(dev, stream, peaks, l2):
     (A1, B1), (A2, B2) = gemm_normal_bf16(6, shapes, lambda k: k ** -0.5)
     gemm_cfg("5a: bf16 8192^3", "bf16", 8192, 8192, 8192, A1, B1, bf16_peak, "bf16 burst", 20)
     gemm_cfg("5b: bf16 16384x4096x4096", "bf16", 16384, 4096, 4096, A2, B2, bf16_peak, "bf16 burst", 20)
+    from seeded import PCG32
+    layer_bias = PCG32(7).uniform_f32((8192,))
+    gemm_cfg("f1: bf16 dense layer 8192^3, bias + ReLU", "bf16", 8192, 8192, 8192, A1, B1, bf16_peak,
+             "bf16 burst", 20, bias=layer_bias, act="relu")
     del A1, B1, A2, B2
 
     hbm = peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])
+    from seeded import PCG32
     for n in (4096, 8192, 16384):
         Av, xv, Xv = gemv_uniform_f32(2, n, n, batch=8)
         nrot = max(2, math.ceil(3 * l2 / (4 * n * n))) if l2 else 2
         As = [torch.from_numpy(Av).to(dev) for _ in range(nrot)]
         X = torch.from_numpy(Xv).to(dev)
         Y = torch.empty((8, n), device=dev)
-        for batch in (1, 8):
-            def call(i, batch=batch):
-                st = gtg.gemv_f32(n, n, As[i % nrot].data_ptr(), n, X.data_ptr(), n, Y.data_ptr(), n, batch, sh)
+        layer_bias = torch.from_numpy(PCG32(8).uniform_f32((n,))).to(dev)
+        variants = [(1, None), (8, None)] + ([(1, "relu")] if n == 4096 else [])
+        for batch, act in variants:
+            ep = gtg.epilogue(layer_bias.data_ptr(), act) if act else None
+
+            def call(i, batch=batch, ep=ep):
+                st = gtg.gemv_f32_ex(n, n, As[i % nrot].data_ptr(), n, X.data_ptr(), n, Y.data_ptr(), n, batch,
+                                     ep, sh)
                 assert st == gtg.GTG_OK, st
             ms = time_launches(call, 100, stream)
-            byt = 4.0 * n * n + batch * 4.0 * (2 * n)
+            byt = 4.0 * n * n + batch * 4.0 * (2 * n) + (4.0 * n if act else 0.0)
             gbs = byt / (ms * 1e-3) / 1e9
-            out.append({"config": f"2: f32 gemv {n}x{n} batch {batch}", "path": "gemv_f32", "shape": [n, n],
+            name = (f"f1: f32 dense vector {n}x{n}, bias + ReLU" if act else
+                    f"2: f32 gemv {n}x{n} batch {batch}")
+            out.append({"config": name, "path": "gemv_f32", "shape": [n, n],
                         "batch": batch, "ms": round(ms, 5), "GB/s": round(gbs, 1), "peak": hbm,
                         "frac": round(gbs / hbm, 4), "buffer_sets": nrot})
         del As, X, Y

@@ -43,12 +43,23 @@ class GtgPlan(ctypes.Structure):
         return d
 
 
+class GtgEpilogue(ctypes.Structure):
+    _fields_ = [("bias", _ptr), ("activation", _int)]
+
+
+ACT = {"none": 0, "relu": 1}
+_ep = ctypes.POINTER(GtgEpilogue)
+
 SIGNATURES = {
     "gemm_f32": (_int, [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr]),
     "gemm_tf32": (_int, [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr]),
     "gemm_bf16": (_int, [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr]),
     "gemv_f32": (_int, [_i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _int, _ptr]),
     "gemm_tf32_noalloc": (_int, [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr]),
+    "gemm_f32_ex": (_int, [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ep, _ptr]),
+    "gemm_tf32_ex": (_int, [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ep, _ptr]),
+    "gemm_bf16_ex": (_int, [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ep, _ptr]),
+    "gemv_f32_ex": (_int, [_i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _int, _ep, _ptr]),
     "gtg_status_string": (ctypes.c_char_p, [_int]),
     "gtg_sync_status": (_int, [_ptr]),
     "gtg_last_cuda_error": (ctypes.c_char_p, []),
@@ -114,6 +125,27 @@ def gemv_f32(M, N, A, lda, x, ldx, y, ldy, batch, stream=0) -> int:
 def gemm_tf32_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
     """gemm_tf32 without any device allocation (fixed 16 MiB scratch; see gtg.h)."""
     return lib().gemm_tf32_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream)
+
+
+def epilogue(bias=0, activation="none"):
+    """A gtg_epilogue for the *_ex calls (bias: device address or 0)."""
+    return GtgEpilogue(bias or None, ACT[activation] if isinstance(activation, str) else int(activation))
+
+
+def gemm_f32_ex(M, N, K, A, lda, B, ldb, C, ldc, ep=None, stream=0) -> int:
+    return lib().gemm_f32_ex(M, N, K, A, lda, B, ldb, C, ldc, ctypes.byref(ep) if ep else None, stream)
+
+
+def gemm_tf32_ex(M, N, K, A, lda, B, ldb, C, ldc, ep=None, stream=0) -> int:
+    return lib().gemm_tf32_ex(M, N, K, A, lda, B, ldb, C, ldc, ctypes.byref(ep) if ep else None, stream)
+
+
+def gemm_bf16_ex(M, N, K, A, lda, B, ldb, C, ldc, ep=None, stream=0) -> int:
+    return lib().gemm_bf16_ex(M, N, K, A, lda, B, ldb, C, ldc, ctypes.byref(ep) if ep else None, stream)
+
+
+def gemv_f32_ex(M, N, A, lda, x, ldx, y, ldy, batch, ep=None, stream=0) -> int:
+    return lib().gemv_f32_ex(M, N, A, lda, x, ldx, y, ldy, batch, ctypes.byref(ep) if ep else None, stream)
 
 
 def status_string(status: int) -> str:
@@ -186,16 +218,18 @@ def _check(status: int, what: str):
 
 
 _IN_DTYPE = {"f32": "float32", "tf32": "float32", "bf16": "bfloat16"}
-_GEMM = {"f32": gemm_f32, "tf32": gemm_tf32, "bf16": gemm_bf16}
+_GEMM_EX = {"f32": gemm_f32_ex, "tf32": gemm_tf32_ex, "bf16": gemm_bf16_ex}
 
 
-def matmul(A, B, precision: str = "f32", out=None, stream=None):
-    """C = A @ B on the GPU through gemm_<precision>; C is FP32.
+def matmul(A, B, precision: str = "f32", out=None, stream=None, bias=None, activation="none"):
+    """C = act(A @ B + bias) on the GPU through gemm_<precision>_ex; C is FP32.
 
     A (M x K) and B (K x N) are row-major torch tensors: float32 for "f32" and
-    "tf32", bfloat16 for "bf16". CUDA tensors are used in place. Host tensors
-    are copied to the device (pinned host memory makes the copies
-    asynchronous) and the result is copied back into a host tensor.
+    "tf32", bfloat16 for "bf16". `bias` (N float32 values, one per output
+    column) and `activation` ("none" or "relu") form the fused epilogue.
+    CUDA tensors are used in place. Host tensors are copied to the device
+    (pinned host memory makes the copies asynchronous) and the result is
+    copied back into a host tensor.
     """
     torch = _torch()
     want = getattr(torch, _IN_DTYPE[precision])
@@ -215,9 +249,11 @@ def matmul(A, B, precision: str = "f32", out=None, stream=None):
         C = out
     else:
         C = torch.empty((M, N), dtype=torch.float32, device=dA.device)
-    st = _GEMM[precision](M, N, K, dA.data_ptr(), _rowmajor_ld(dA, "A"), dB.data_ptr(),
-                          _rowmajor_ld(dB, "B"), C.data_ptr(), _rowmajor_ld(C, "C"),
-                          _stream_handle(stream))
+    dbias = _device_bias(bias, N, dA.device)
+    ep = epilogue(dbias.data_ptr() if dbias is not None else 0, activation)
+    st = _GEMM_EX[precision](M, N, K, dA.data_ptr(), _rowmajor_ld(dA, "A"), dB.data_ptr(),
+                             _rowmajor_ld(dB, "B"), C.data_ptr(), _rowmajor_ld(C, "C"), ep,
+                             _stream_handle(stream))
     _check(st, f"gemm_{precision}")
     if host:
         res = out if out is not None else torch.empty((M, N), dtype=torch.float32,
@@ -228,11 +264,22 @@ def matmul(A, B, precision: str = "f32", out=None, stream=None):
     return C
 
 
-def matvec(A, x, out=None, stream=None):
-    """y = A @ x (x of shape (N,)) or Y = X @ A^T per row of X (shape (batch, N)).
+def _device_bias(bias, n, device):
+    if bias is None:
+        return None
+    torch = _torch()
+    if bias.dtype != torch.float32 or bias.numel() != n:
+        raise ValueError(f"bias must hold {n} float32 values")
+    return bias.reshape(-1).to(device, non_blocking=True).contiguous()
 
-    FP32 only, batch <= 8, through gemv_f32. Host tensors are copied in and
-    the result copied back, as in `matmul`.
+
+def matvec(A, x, out=None, stream=None, bias=None, activation="none"):
+    """y = act(A @ x + bias) (x of shape (N,)), or Y = act(X @ A^T + bias)
+    per row of X (shape (batch, N)): a fully connected layer with weight A.
+
+    FP32 only, batch <= 8, through gemv_f32_ex; `bias` holds M float32 values
+    (one per output). Host tensors are copied in and the result copied back,
+    as in `matmul`.
     """
     torch = _torch()
     if A.dtype != torch.float32 or x.dtype != torch.float32:
@@ -250,8 +297,10 @@ def matvec(A, x, out=None, stream=None):
         Y = out.unsqueeze(0) if single else out
     else:
         Y = torch.empty((batch, M), dtype=torch.float32, device=dA.device)
-    st = gemv_f32(M, N, dA.data_ptr(), _rowmajor_ld(dA, "A"), dX.data_ptr(), _rowmajor_ld(dX, "x"),
-                  Y.data_ptr(), _rowmajor_ld(Y, "y"), batch, _stream_handle(stream))
+    dbias = _device_bias(bias, M, dA.device)
+    ep = epilogue(dbias.data_ptr() if dbias is not None else 0, activation)
+    st = gemv_f32_ex(M, N, dA.data_ptr(), _rowmajor_ld(dA, "A"), dX.data_ptr(), _rowmajor_ld(dX, "x"),
+                     Y.data_ptr(), _rowmajor_ld(Y, "y"), batch, ep, _stream_handle(stream))
     _check(st, "gemv_f32")
     if host:
         res = torch.empty((batch, M), dtype=torch.float32, pin_memory=A.is_pinned())

@@ -94,6 +94,11 @@ gtg_status validate_gemm(const GemmArgs &g) {
     if (g.K > 0 && (overlaps(c, span_of(g.A, g.M, g.K, g.lda, in_elem)) ||
                     overlaps(c, span_of(g.B, g.K, g.N, g.ldb, in_elem))))
         return GTG_ERR_ALIAS;
+    if (g.act != GTG_ACT_NONE && g.act != GTG_ACT_RELU) return GTG_ERR_INVALID_VALUE;
+    if (g.bias) {
+        if (reinterpret_cast<uintptr_t>(g.bias) % 4) return GTG_ERR_MISALIGNED;
+        if (overlaps(c, span_of(g.bias, 1, g.N, g.N, 4))) return GTG_ERR_ALIAS;
+    }
     return GTG_OK;
 }
 
@@ -113,6 +118,11 @@ gtg_status validate_gemv(const GemvArgs &g) {
     if (g.N > 0 && (overlaps(y, span_of(g.A, g.M, g.N, g.lda, 4)) ||
                     overlaps(y, span_of(g.x, g.batch, g.N, ldx, 4))))
         return GTG_ERR_ALIAS;
+    if (g.act != GTG_ACT_NONE && g.act != GTG_ACT_RELU) return GTG_ERR_INVALID_VALUE;
+    if (g.bias) {
+        if (reinterpret_cast<uintptr_t>(g.bias) % 4) return GTG_ERR_MISALIGNED;
+        if (overlaps(y, span_of(g.bias, 1, g.M, g.M, 4))) return GTG_ERR_ALIAS;
+    }
     return GTG_OK;
 }
 
@@ -144,7 +154,10 @@ gtg_status run_gemm(const GemmArgs &g, cudaStream_t stream) {
     if ((st = plan_gemm_impl(dev, g, &plan)) != GTG_OK) return st;
     cudaError_t e = cudaSuccess;
     switch (plan.kernel) {
-        case GTG_KERNEL_ZERO_FILL: e = zero_fill_launch(g.C, g.M, g.N, g.ldc, stream); break;
+        case GTG_KERNEL_ZERO_FILL:
+            e = (g.bias || g.act) ? epilogue_fill_launch(g.C, g.M, g.N, g.ldc, g.bias, 1, g.act, stream)
+                                  : zero_fill_launch(g.C, g.M, g.N, g.ldc, stream);
+            break;
         case GTG_KERNEL_TCGEN05: e = tc_launch(dev, g, plan, stream); break;
         case GTG_KERNEL_SIMT: e = simt_launch(dev, g, plan, stream); break;
         default: break;
@@ -178,9 +191,9 @@ gtg_status gemm_bf16(int64_t M, int64_t N, int64_t K, const gtg_bf16 *A, int64_t
     return run_gemm(GemmArgs{GTG_PREC_BF16, M, N, K, A, lda, B, ldb, C, ldc}, stream);
 }
 
-gtg_status gemv_f32(int64_t M, int64_t N, const float *A, int64_t lda, const float *x, int64_t ldx,
-                    float *y, int64_t ldy, int batch, cudaStream_t stream) {
-    const GemvArgs g{M, N, A, lda, x, batch > 1 ? ldx : N, y, batch > 1 ? ldy : M, batch};
+static gtg_status run_gemv(const GemvArgs &g, cudaStream_t stream) {
+    const int64_t M = g.M, N = g.N;
+    const int batch = g.batch;
     gtg_status st = validate_gemv(g);
     if (st != GTG_OK || M == 0) return st;
     DeviceInfo dev;
@@ -188,8 +201,9 @@ gtg_status gemv_f32(int64_t M, int64_t N, const float *A, int64_t lda, const flo
     if (!(dev.cc_major == 10 && dev.cc_minor == 3)) return GTG_ERR_UNSUPPORTED;
     cudaError_t e;
     if (N == 0) {
-        // empty sums: every output is zero
-        e = zero_fill_launch(y, batch, M, g.ldy, stream);
+        // empty sums: every output is act(0 + bias) (zero without an epilogue)
+        e = (g.bias || g.act) ? epilogue_fill_launch(g.y, batch, M, g.ldy, g.bias, 1, g.act, stream)
+                              : zero_fill_launch(g.y, batch, M, g.ldy, stream);
     } else {
         gtg_plan plan;
         gemv_plan(dev, g, &plan);
@@ -230,6 +244,44 @@ gtg_status gemm_tf32_noalloc(int64_t M, int64_t N, int64_t K, const float *A, in
         return GTG_ERR_LAUNCH;
     }
     return GTG_OK;
+}
+
+gtg_status gemv_f32(int64_t M, int64_t N, const float *A, int64_t lda, const float *x, int64_t ldx,
+                    float *y, int64_t ldy, int batch, cudaStream_t stream) {
+    return run_gemv(GemvArgs{M, N, A, lda, x, batch > 1 ? ldx : N, y, batch > 1 ? ldy : M, batch}, stream);
+}
+
+gtg_status gemv_f32_ex(int64_t M, int64_t N, const float *A, int64_t lda, const float *x, int64_t ldx,
+                       float *y, int64_t ldy, int batch, const gtg_epilogue *ep, cudaStream_t stream) {
+    GemvArgs g{M, N, A, lda, x, batch > 1 ? ldx : N, y, batch > 1 ? ldy : M, batch};
+    if (ep) {
+        g.bias = ep->bias;
+        g.act = ep->activation;
+    }
+    return run_gemv(g, stream);
+}
+
+static GemmArgs with_epilogue(GemmArgs g, const gtg_epilogue *ep) {
+    if (ep) {
+        g.bias = ep->bias;
+        g.act = ep->activation;
+    }
+    return g;
+}
+
+gtg_status gemm_f32_ex(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
+                       int64_t ldb, float *C, int64_t ldc, const gtg_epilogue *ep, cudaStream_t stream) {
+    return run_gemm(with_epilogue(GemmArgs{GTG_PREC_F32, M, N, K, A, lda, B, ldb, C, ldc}, ep), stream);
+}
+
+gtg_status gemm_tf32_ex(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
+                        int64_t ldb, float *C, int64_t ldc, const gtg_epilogue *ep, cudaStream_t stream) {
+    return run_gemm(with_epilogue(GemmArgs{GTG_PREC_TF32, M, N, K, A, lda, B, ldb, C, ldc}, ep), stream);
+}
+
+gtg_status gemm_bf16_ex(int64_t M, int64_t N, int64_t K, const gtg_bf16 *A, int64_t lda, const gtg_bf16 *B,
+                        int64_t ldb, float *C, int64_t ldc, const gtg_epilogue *ep, cudaStream_t stream) {
+    return run_gemm(with_epilogue(GemmArgs{GTG_PREC_BF16, M, N, K, A, lda, B, ldb, C, ldc}, ep), stream);
 }
 
 const char *gtg_status_string(gtg_status s) {

@@ -68,9 +68,11 @@ template <typename T, int BM, int BN, bool VEC>
 __global__ void __launch_bounds__(SimtTile<T, BM, BN, VEC>::THREADS)
     simt_gemm_kernel(int M, int N, int K, const T *__restrict__ A, long long lda,
                      const T *__restrict__ B, long long ldb, float *__restrict__ C, long long ldc,
-                     int c_vec, int k_per, float *__restrict__ ws) {
+                     int c_vec, int k_per, float *__restrict__ ws, const float *__restrict__ bias, int act) {
     using L = SimtTile<T, BM, BN, VEC>;
     if (gridDim.z > 1) {
+        bias = nullptr;   // partial products: the reduction applies the epilogue
+        act = 0;
         const int z = blockIdx.z;
         A += static_cast<long long>(z) * k_per;
         B += static_cast<long long>(z) * k_per * ldb;
@@ -203,7 +205,10 @@ __global__ void __launch_bounds__(SimtTile<T, BM, BN, VEC>::THREADS)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int col = n0 + (h == 0 ? tx * 4 : BN / 2 + tx * 4);
-            const float *v = &acc[i][h * 4];
+            float v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                v[j] = apply_epilogue(acc[i][h * 4 + j], col + j < N ? bias : nullptr, col + j, act);
             if (c_vec && col + 3 < N) {
                 *reinterpret_cast<float4 *>(crow + col) = make_float4(v[0], v[1], v[2], v[3]);
             } else {
@@ -218,7 +223,8 @@ __global__ void __launch_bounds__(SimtTile<T, BM, BN, VEC>::THREADS)
 // C[i][j] = sum over z = 0 .. S-1 of ws[z][i][j], in that order. One thread
 // per 4 consecutive columns of a row (16-byte accesses when they are aligned).
 __global__ void split_reduce_kernel(const float *__restrict__ ws, int splits, int M, int N,
-                                    float *__restrict__ C, long long ldc, int vec) {
+                                    float *__restrict__ C, long long ldc, int vec,
+                                    const float *__restrict__ bias, int act) {
     const int n4 = (N + 3) / 4;
     const long long slice = static_cast<long long>(M) * N;
     for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
@@ -236,14 +242,28 @@ __global__ void split_reduce_kernel(const float *__restrict__ ws, int splits, in
                 v.z += w.z;
                 v.w += w.w;
             }
+            v.x = apply_epilogue(v.x, bias, col, act);
+            v.y = apply_epilogue(v.y, bias, col + 1, act);
+            v.z = apply_epilogue(v.z, bias, col + 2, act);
+            v.w = apply_epilogue(v.w, bias, col + 3, act);
             *reinterpret_cast<float4 *>(dst) = v;
         } else {
             for (int c = 0; c < 4 && col + c < N; ++c) {
                 float v = ws[src + c];
                 for (int z = 1; z < splits; ++z) v += ws[z * slice + src + c];
-                dst[c] = v;
+                dst[c] = apply_epilogue(v, bias, col + c, act);
             }
         }
+    }
+}
+
+__global__ void epilogue_fill_kernel(float *C, long long M, long long N, long long ldc, const float *bias,
+                                     int per_column, int act) {
+    const long long total = M * N;
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long r = i / N, c = i % N;
+        C[r * ldc + c] = apply_epilogue(0.f, bias, static_cast<int>(per_column ? c : r), act);
     }
 }
 
@@ -270,7 +290,8 @@ cudaError_t launch_one(const GemmArgs &g, int splits, cudaStream_t stream) {
     }
     simt_gemm_kernel<T, BM, BN, VEC><<<grid, L::THREADS, 0, stream>>>(
         static_cast<int>(g.M), static_cast<int>(g.N), static_cast<int>(g.K),
-        static_cast<const T *>(g.A), g.lda, static_cast<const T *>(g.B), g.ldb, g.C, g.ldc, c_vec, k_per, ws);
+        static_cast<const T *>(g.A), g.lda, static_cast<const T *>(g.B), g.ldb, g.C, g.ldc, c_vec, k_per, ws,
+        g.bias, g.act);
     e = cudaGetLastError();
     if (splits > 1) {
         if (e == cudaSuccess) {
@@ -279,7 +300,7 @@ cudaError_t launch_one(const GemmArgs &g, int splits, cudaStream_t stream) {
             // ws rows are N floats, 256-byte aligned base: 16-byte accesses need N % 4 == 0
             const int vec = ((g.N & 3) == 0 && c_vec) ? 1 : 0;
             split_reduce_kernel<<<blocks, 256, 0, stream>>>(ws, splits, static_cast<int>(g.M), static_cast<int>(g.N),
-                                                            g.C, g.ldc, vec);
+                                                            g.C, g.ldc, vec, g.bias, g.act);
             e = cudaGetLastError();
         }
         const cudaError_t f = cudaFreeAsync(ws, stream);   // stream-ordered: after the reduction
@@ -349,6 +370,16 @@ cudaError_t simt_launch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
     if (g.prec == GTG_PREC_BF16)
         return vec ? launch_typed<uint16_t, true>(g, plan, stream) : launch_typed<uint16_t, false>(g, plan, stream);
     return vec ? launch_typed<float, true>(g, plan, stream) : launch_typed<float, false>(g, plan, stream);
+}
+
+cudaError_t epilogue_fill_launch(float *C, int64_t M, int64_t N, int64_t ldc, const float *bias, int per_column,
+                                 int act, cudaStream_t stream) {
+    const long long total = M * N;
+    long long blocks = (total + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    if (blocks < 1) blocks = 1;
+    epilogue_fill_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(C, M, N, ldc, bias, per_column, act);
+    return cudaGetLastError();
 }
 
 cudaError_t zero_fill_launch(float *C, int64_t M, int64_t N, int64_t ldc, cudaStream_t stream) {

@@ -85,7 +85,20 @@ struct TcParams {
     int *status;
     unsigned long long wait_limit_ns;
     int drop_slice;              // testing hook: K slice whose load CTA 0 never issues (-1: none)
+    const float *bias;           // epilogue: C = act(acc + bias[col]); null for none
+    int act;
 };
+
+// Apply the layer epilogue to 32 accumulator columns starting at column col.
+__device__ __forceinline__ void epilogue32(uint32_t (&r)[32], const TcParams &p, int col) {
+    if (p.bias == nullptr && p.act == 0) return;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const bool in = col + j < p.N;
+        const float v = apply_epilogue(__uint_as_float(r[j]), in ? p.bias : nullptr, col + j, p.act);
+        r[j] = __float_as_uint(v);
+    }
+}
 
 __device__ __forceinline__ void tile_coords(int t, const TcParams &p, int &mb, int &nb) {
     const int per_group = kGroup * p.num_n;
@@ -302,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t r[32];
                 ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
                 ptx::tmem_ld_wait();
+                epilogue32(r, p, col0 + c * 32);
                 if (row_ok) {
                     if (whole && p.c_vec == 2) {
 #pragma unroll
@@ -544,6 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t r[32];
                 ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
                 ptx::tmem_ld_wait();
+                epilogue32(r, p, col0 + c * 32);
                 if (row_ok) {
                     if (whole && p.c_vec == 2) {
 #pragma unroll
@@ -731,6 +746,8 @@ cudaError_t launch_impl(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
     p.status = dev.status;
     p.wait_limit_ns = wait_limit_ns();
     p.drop_slice = take_drop_slice();
+    p.bias = g.bias;
+    p.act = g.act;
     cudaError_t e = launch_pdl(kern, plan.grid, S::SMEM, stream, ta, tb, p);
     if (bt != nullptr) {
         // stream-ordered: released once the GEMM has finished reading it
@@ -769,6 +786,8 @@ cudaError_t launch_pair(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
     p.status = dev.status;
     p.wait_limit_ns = wait_limit_ns();
     p.drop_slice = take_drop_slice();
+    p.bias = g.bias;
+    p.act = g.act;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(plan.grid));
     cfg.blockDim = dim3(kThreads);
@@ -972,6 +991,8 @@ cudaError_t launch_tf32_fixed(const DeviceInfo &dev, const GemmArgs &g, const gt
     p.status = dev.status;
     p.wait_limit_ns = wait_limit_ns();
     p.drop_slice = take_drop_slice();
+    p.bias = g.bias;
+    p.act = g.act;
     kern<<<plan.grid, kThreads, S::SMEM, stream>>>(ta, tb, p);
     return cudaGetLastError();
 }

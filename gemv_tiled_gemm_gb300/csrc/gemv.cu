@@ -42,6 +42,8 @@ struct GemvParams {
     int M, N;
     int chunk;     // vector entries staged per pass (multiple of 4)
     int nchunks;
+    const float *bias;   // epilogue: y = act(acc + bias[row]); null for none
+    int act;
 };
 
 template <int BATCH, int kThreads>
@@ -197,7 +199,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
 #pragma unroll
                 for (int b = 0; b < BATCH; ++b)
                     if (lane == (r * BATCH + b) % 32 && row0 + r < r_end)
-                        p.y[static_cast<long long>(b) * p.ldy + row0 + r] = acc[r][b];
+                        p.y[static_cast<long long>(b) * p.ldy + row0 + r] =
+                            apply_epilogue(acc[r][b], p.bias, row0 + r, p.act);
         }
     }
 }
@@ -310,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const GemvPara
                 for (int b = 0; b < BATCH; ++b) {
                     const int row = row_of(t, r);
                     if (lane == (r * BATCH + b) % 32 && row < r_end)
-                        p.y[static_cast<long long>(b) * p.ldy + row] = acc[r][b];
+                        p.y[static_cast<long long>(b) * p.ldy + row] = apply_epilogue(acc[r][b], p.bias, row, p.act);
                     acc[r][b] = 0.f;
                 }
         }
@@ -428,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_split_kernel(const GemvParam
         float v = 0.f;
 #pragma unroll
         for (int cs = 0; cs < WC; ++cs) v += part[((rg * WC + cs) * ROWS + r) * BATCH + b];
-        p.y[static_cast<long long>(b) * p.ldy + r_begin + rl] = v;
+        p.y[static_cast<long long>(b) * p.ldy + r_begin + rl] = apply_epilogue(v, p.bias, r_begin + rl, p.act);
     }
 }
 
@@ -545,6 +548,8 @@ cudaError_t gemv_launch(const DeviceInfo &dev, const GemvArgs &g, const gtg_plan
     p.N = static_cast<int>(g.N);
     p.chunk = l.chunk;
     p.nchunks = l.nchunks;
+    p.bias = g.bias;
+    p.act = g.act;
     void *args[] = {&p};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.grid);

@@ -18,22 +18,35 @@ struct DeviceInfo {
     int *status = nullptr;       // device address of the library's status word
 };
 
-// One GEMM call after validation. Pointers are device pointers.
+// One GEMM call after validation. Pointers are device pointers. The optional
+// epilogue computes C = act(A * B + bias) with one bias per column of C.
 struct GemmArgs {
     int prec;                    // GTG_PREC_*
     int64_t M, N, K;
     const void *A; int64_t lda;
     const void *B; int64_t ldb;
     float *C; int64_t ldc;
+    const float *bias = nullptr; // N entries or null
+    int act = 0;                 // GTG_ACT_*
 };
 
+// y_b = act(A * x_b + bias) with one bias per row of A.
 struct GemvArgs {
     int64_t M, N;
     const float *A; int64_t lda;
     const float *x; int64_t ldx;
     float *y; int64_t ldy;
     int batch;
+    const float *bias = nullptr; // M entries or null
+    int act = 0;
 };
+
+// The epilogue applied to one FP32 result before it is stored.
+__host__ __device__ __forceinline__ float apply_epilogue(float v, const float *bias, int index, int act) {
+    if (bias) v += bias[index];
+    if (act == GTG_ACT_RELU) v = v > 0.f ? v : 0.f;
+    return v;
+}
 
 // Time limit for any pipeline wait inside a kernel (nanoseconds).
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
@@ -61,6 +74,9 @@ void simt_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan);
 cudaError_t simt_launch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan,
                         cudaStream_t stream);
 cudaError_t zero_fill_launch(float *C, int64_t M, int64_t N, int64_t ldc, cudaStream_t stream);
+// C[i][j] = act(bias[j] or bias[i]) -- the result of an empty product with an epilogue
+cudaError_t epilogue_fill_launch(float *C, int64_t M, int64_t N, int64_t ldc, const float *bias, int per_column,
+                                 int act, cudaStream_t stream);
 
 // ---- GEMV (gemv.cu)
 void gemv_plan(const DeviceInfo &dev, const GemvArgs &g, gtg_plan *plan);

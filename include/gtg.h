@@ -208,6 +208,45 @@ GTG_API gtg_status gemm_tf32_noalloc(int64_t M, int64_t N, int64_t K,
                              float *C, int64_t ldc,
                              cudaStream_t stream);
 
+/*
+ * Fully connected layers: the same products with an epilogue applied to each
+ * FP32 result before it is stored ("Matrix Operations": fully connected
+ * layers are matrix-vector products; activation functions add the
+ * non-linearity):
+ *
+ *   GEMM  C[i][j] = act(sum_k A[i][k] B[k][j] + bias[j])   (a batch of inputs
+ *                                                            in the rows of A)
+ *   GEMV  y_b[i]  = act(sum_j A[i][j] x_b[j] + bias[i])     (one layer, W = A)
+ *
+ *   bias        device pointer to N (GEMM) or M (GEMV) FP32 values, 4-byte
+ *               aligned, not overlapping the output; NULL for no bias
+ *   activation  GTG_ACT_NONE (identity) or GTG_ACT_RELU (max(v, 0))
+ *
+ * The epilogue is fused into the kernels' stores: it adds no pass over C.
+ * epilogue == NULL is the plain product. Other arguments and errors are
+ * those of the corresponding call above; an unknown activation or a bias
+ * overlapping the output returns GTG_ERR_INVALID_VALUE / GTG_ERR_ALIAS.
+ * With K = 0 (or N = 0 for the GEMV) the outputs are act(bias).
+ */
+enum { GTG_ACT_NONE = 0, GTG_ACT_RELU = 1 };
+typedef struct {
+    const float *bias;
+    int activation;
+} gtg_epilogue;
+
+GTG_API gtg_status gemm_f32_ex(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                               const float *B, int64_t ldb, float *C, int64_t ldc,
+                               const gtg_epilogue *epilogue, cudaStream_t stream);
+GTG_API gtg_status gemm_tf32_ex(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                                const float *B, int64_t ldb, float *C, int64_t ldc,
+                                const gtg_epilogue *epilogue, cudaStream_t stream);
+GTG_API gtg_status gemm_bf16_ex(int64_t M, int64_t N, int64_t K, const gtg_bf16 *A, int64_t lda,
+                                const gtg_bf16 *B, int64_t ldb, float *C, int64_t ldc,
+                                const gtg_epilogue *epilogue, cudaStream_t stream);
+GTG_API gtg_status gemv_f32_ex(int64_t M, int64_t N, const float *A, int64_t lda,
+                               const float *x, int64_t ldx, float *y, int64_t ldy, int batch,
+                               const gtg_epilogue *epilogue, cudaStream_t stream);
+
 /* Static English text for a status code (never NULL). */
 GTG_API const char *gtg_status_string(gtg_status status);
 

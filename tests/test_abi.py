@@ -111,3 +111,15 @@ def test_plan_validation_matches_the_call():
         gtg.plan_gemm("bf16", 4, 4, 8, A, 7, B, 4, C, 4)
     assert e.value.status == gtg.GTG_ERR_INVALID_VALUE
     assert gtg.plan_gemm("f32", 0, 4, 4, A, 4, B, 4, C, 4)["kernel"] == "none"
+
+
+def test_epilogue_validation():
+    E = gtg.GTG_ERR_INVALID_VALUE
+    ep_bad_act = gtg.epilogue(0, 7)
+    for fn in (gtg.gemm_f32_ex, gtg.gemm_tf32_ex, gtg.gemm_bf16_ex):
+        assert fn(4, 4, 4, A, 4, B, 4, C, 4, ep_bad_act) == E
+        # bias overlapping C, misaligned bias
+        assert fn(4, 4, 4, A, 4, B, 4, C, 4, gtg.epilogue(C + 4, "relu")) == gtg.GTG_ERR_ALIAS
+        assert fn(4, 4, 4, A, 4, B, 4, C, 4, gtg.epilogue(A + (1 << 20) + 2, "none")) == gtg.GTG_ERR_MISALIGNED
+    assert gtg.gemv_f32_ex(4, 4, A, 4, B, 4, C, 4, 1, ep_bad_act) == E
+    assert gtg.gemv_f32_ex(4, 4, A, 4, B, 4, C, 4, 1, gtg.epilogue(C + 8, "relu")) == gtg.GTG_ERR_ALIAS
