@@ -49,6 +49,9 @@ def parse_args():
     p.add_argument("--no-sweep", action="store_true", help="skip the per-configuration sweep")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--only-ablation", action="store_true",
+                   help="run only the pages' kernel designs beside the library's (prints their table)")
+    p.add_argument("--ablation-iters", type=int, default=0, help="timed launches per ablation kernel (0: default)")
     return p.parse_args()
 
 
@@ -422,6 +425,8 @@ def sweep(dev, stream, peaks, l2):
              "bf16 burst", 20, bias=layer_bias, act="relu")
     del A1, B1, A2, B2
 
+    out.extend(ablation(dev, stream, f32_peak, peaks.get("hbm_gbs", FALLBACK["hbm_gbs"]), l2))
+
     hbm = peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])
     from seeded import PCG32
     for n in (4096, 8192, 16384):
@@ -448,6 +453,62 @@ def sweep(dev, stream, peaks, l2):
                         "batch": batch, "ms": round(ms, 5), "GB/s": round(gbs, 1), "peak": hbm,
                         "frac": round(gbs / hbm, 4), "buffer_sets": nrot})
         del As, X, Y
+    torch.cuda.empty_cache()
+    return out
+
+
+def ablation(dev, stream, f32_peak, hbm, l2, iters=0):
+    """The pages' own kernel designs beside the library's kernels on the same
+    workloads, to test the pages' speed-up claims on this GPU."""
+    import torch
+
+    import gemv_tiled_gemm_gb300 as gtg
+    from seeded import gemm_uniform_f32, gemv_uniform_f32
+
+    sh = int(stream.cuda_stream)
+    out = []
+    M = N = K = 1024
+    A, B = gemm_uniform_f32(3, M, N, K)
+    nrot = max(1, math.ceil(2 * l2 / (3 * 4 * M * N))) if l2 else 1
+    sets = [(torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev), torch.empty((M, N), device=dev))
+            for _ in range(nrot)]
+    times = {}
+    for variant in ("naive16", "naive32", "tiled16", "tiled32", "library"):
+        def call(i, variant=variant):
+            a, b, c = sets[i % nrot]
+            if variant == "library":
+                st = gtg.gemm_f32(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N, sh)
+            else:
+                st = gtg.gtg_ablation_gemm_f32(variant, M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(),
+                                               N, sh)
+            assert st == gtg.GTG_OK, st
+        times[variant] = time_launches(call, iters or (10 if variant.startswith("naive") else 30), stream)
+        tf = 2.0 * M * N * K / (times[variant] * 1e-3) / 1e12
+        out.append({"config": f"f3: f32 gemm 1024^3, {variant}", "path": "ablation" if variant != "library" else "f32",
+                    "shape": [M, N, K], "ms": round(times[variant], 4), "TFLOP/s": round(tf, 2), "peak": f32_peak,
+                    "frac": round(tf / f32_peak, 4),
+                    "speedup_vs_naive16": round(times["naive16"] / times[variant], 2)})
+    del sets
+    M = N = 4096
+    Av, xv, _ = gemv_uniform_f32(2, M, N, batch=1)
+    nrot = max(2, math.ceil(3 * l2 / (4 * M * N))) if l2 else 2
+    As = [torch.from_numpy(Av).to(dev) for _ in range(nrot)]
+    x = torch.from_numpy(xv).to(dev)
+    y = torch.empty(M, device=dev)
+    for variant in ("naive", "shared", "library"):
+        def call(i, variant=variant):
+            if variant == "library":
+                st = gtg.gemv_f32(M, N, As[i % nrot].data_ptr(), N, x.data_ptr(), N, y.data_ptr(), M, 1, sh)
+            else:
+                st = gtg.gtg_ablation_gemv_f32(variant, M, N, As[i % nrot].data_ptr(), N, x.data_ptr(),
+                                               y.data_ptr(), sh)
+            assert st == gtg.GTG_OK, st
+        times[variant] = time_launches(call, iters or (20 if variant != "library" else 100), stream)
+        gbs = (4.0 * M * N + 8.0 * M) / (times[variant] * 1e-3) / 1e9
+        out.append({"config": f"f3: f32 gemv 4096^2, {variant}", "path": "ablation" if variant != "library" else "gemv_f32",
+                    "shape": [M, N], "ms": round(times[variant], 5), "GB/s": round(gbs, 1), "peak": hbm,
+                    "frac": round(gbs / hbm, 4), "speedup_vs_naive": round(times["naive"] / times[variant], 2)})
+    del As
     torch.cuda.empty_cache()
     return out
 
@@ -538,6 +599,18 @@ def main():
         res = reference_arm(args, rank, world)
         if res is not None:
             print(json.dumps(res), flush=True)
+        return 0
+
+    if args.only_ablation:
+        import torch
+        torch.cuda.set_device(local_rank)
+        dev = torch.device("cuda", local_rank)
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        peaks, _ = load_peaks()
+        l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 0
+        rows = ablation(dev, torch.cuda.current_stream(), sms * 128 * 2 * 2.070e9 / 1e12,
+                        peaks.get("hbm_gbs", FALLBACK["hbm_gbs"]), l2, args.ablation_iters)
+        print(json.dumps({"ablation": rows}), flush=True)
         return 0
 
     if world > 1:

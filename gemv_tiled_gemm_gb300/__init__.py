@@ -60,6 +60,8 @@ SIGNATURES = {
     "gemm_tf32_ex": (_int, [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ep, _ptr]),
     "gemm_bf16_ex": (_int, [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ep, _ptr]),
     "gemv_f32_ex": (_int, [_i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _int, _ep, _ptr]),
+    "gtg_ablation_gemm_f32": (_int, [_int, _i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr]),
+    "gtg_ablation_gemv_f32": (_int, [_int, _i64, _i64, _ptr, _i64, _ptr, _ptr, _ptr]),
     "gtg_status_string": (ctypes.c_char_p, [_int]),
     "gtg_sync_status": (_int, [_ptr]),
     "gtg_last_cuda_error": (ctypes.c_char_p, []),
@@ -146,6 +148,20 @@ def gemm_bf16_ex(M, N, K, A, lda, B, ldb, C, ldc, ep=None, stream=0) -> int:
 
 def gemv_f32_ex(M, N, A, lda, x, ldx, y, ldy, batch, ep=None, stream=0) -> int:
     return lib().gemv_f32_ex(M, N, A, lda, x, ldx, y, ldy, batch, ctypes.byref(ep) if ep else None, stream)
+
+
+ABLATION_GEMM = {"naive16": 0, "naive32": 1, "tiled16": 2, "tiled32": 3}
+ABLATION_GEMV = {"naive": 0, "shared": 1}
+
+
+def gtg_ablation_gemm_f32(variant, M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    v = ABLATION_GEMM[variant] if isinstance(variant, str) else variant
+    return lib().gtg_ablation_gemm_f32(v, M, N, K, A, lda, B, ldb, C, ldc, stream)
+
+
+def gtg_ablation_gemv_f32(variant, M, N, A, lda, x, y, stream=0) -> int:
+    v = ABLATION_GEMV[variant] if isinstance(variant, str) else variant
+    return lib().gtg_ablation_gemv_f32(v, M, N, A, lda, x, y, stream)
 
 
 def status_string(status: int) -> str:

@@ -284,6 +284,41 @@ gtg_status gemm_bf16_ex(int64_t M, int64_t N, int64_t K, const gtg_bf16 *A, int6
     return run_gemm(with_epilogue(GemmArgs{GTG_PREC_BF16, M, N, K, A, lda, B, ldb, C, ldc}, ep), stream);
 }
 
+gtg_status gtg_ablation_gemm_f32(int variant, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                                 const float *B, int64_t ldb, float *C, int64_t ldc, cudaStream_t stream) {
+    if (variant < GTG_ABL_GEMM_NAIVE_16 || variant > GTG_ABL_GEMM_TILED_32) return GTG_ERR_INVALID_VALUE;
+    const GemmArgs g{GTG_PREC_F32, M, N, K, A, lda, B, ldb, C, ldc};
+    gtg_status st = validate_gemm(g);
+    if (st != GTG_OK || M == 0 || N == 0) return st;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != GTG_OK) return st;
+    if (!(dev.cc_major == 10 && dev.cc_minor == 3)) return GTG_ERR_UNSUPPORTED;
+    if (grid_too_large(M, N, 16)) return GTG_ERR_UNSUPPORTED;
+    const cudaError_t e = K == 0 ? zero_fill_launch(C, M, N, ldc, stream) : ablation_gemm_launch(variant, g, stream);
+    if (e != cudaSuccess) {
+        note_cuda_error(e);
+        return GTG_ERR_LAUNCH;
+    }
+    return GTG_OK;
+}
+
+gtg_status gtg_ablation_gemv_f32(int variant, int64_t M, int64_t N, const float *A, int64_t lda, const float *x,
+                                 float *y, cudaStream_t stream) {
+    if (variant != GTG_ABL_GEMV_NAIVE && variant != GTG_ABL_GEMV_SHARED) return GTG_ERR_INVALID_VALUE;
+    const GemvArgs g{M, N, A, lda, x, N, y, M, 1};
+    gtg_status st = validate_gemv(g);
+    if (st != GTG_OK || M == 0) return st;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != GTG_OK) return st;
+    if (!(dev.cc_major == 10 && dev.cc_minor == 3)) return GTG_ERR_UNSUPPORTED;
+    const cudaError_t e = N == 0 ? zero_fill_launch(y, 1, M, M, stream) : ablation_gemv_launch(variant, g, stream);
+    if (e != cudaSuccess) {
+        note_cuda_error(e);
+        return GTG_ERR_LAUNCH;
+    }
+    return GTG_OK;
+}
+
 const char *gtg_status_string(gtg_status s) {
     switch (s) {
         case GTG_OK: return "success";

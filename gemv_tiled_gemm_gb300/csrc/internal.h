@@ -78,6 +78,11 @@ cudaError_t zero_fill_launch(float *C, int64_t M, int64_t N, int64_t ldc, cudaSt
 cudaError_t epilogue_fill_launch(float *C, int64_t M, int64_t N, int64_t ldc, const float *bias, int per_column,
                                  int act, cudaStream_t stream);
 
+// ---- the pages' kernel designs, for measurement (ablation.cu)
+cudaError_t ablation_gemm_launch(int variant, const GemmArgs &g, cudaStream_t stream);
+cudaError_t ablation_gemv_launch(int variant, const GemvArgs &g, cudaStream_t stream);
+bool grid_too_large(int64_t M, int64_t N, int tile);
+
 // ---- GEMV (gemv.cu)
 void gemv_plan(const DeviceInfo &dev, const GemvArgs &g, gtg_plan *plan);
 cudaError_t gemv_launch(const DeviceInfo &dev, const GemvArgs &g, const gtg_plan &plan,

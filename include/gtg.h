@@ -247,6 +247,38 @@ GTG_API gtg_status gemv_f32_ex(int64_t M, int64_t N, const float *A, int64_t lda
                                const float *x, int64_t ldx, float *y, int64_t ldy, int batch,
                                const gtg_epilogue *epilogue, cudaStream_t stream);
 
+/*
+ * The pages' own kernel designs, kept for measurement against the kernels
+ * above (they are not used by any other call). FP32, same products, same
+ * argument conventions as gemm_f32 / gemv_f32 (batch 1):
+ *
+ *   GTG_ABL_GEMM_NAIVE_16 / _32  one thread per output of C, 16 x 16 or
+ *        32 x 32 threads per block, operands read from global memory for
+ *        every multiply-add ("Matrix Operations", GEMM "Naive
+ *        Implementation"; "CUDA Programming (6)" section 3.1);
+ *   GTG_ABL_GEMM_TILED_16 / _32  16 x 16 or 32 x 32 shared-memory tiles,
+ *        zero-padded edges, two barriers per tile ("Tiled Implementation with
+ *        Shared Memory"; section 3.2);
+ *   GTG_ABL_GEMV_NAIVE   one thread per row, the vector read from global
+ *        memory by every thread ("Matrix-Vector Multiplication", "Naive
+ *        Implementation");
+ *   GTG_ABL_GEMV_SHARED  the vector staged in shared memory in chunks of 256
+ *        with a barrier on each side ("Optimized Implementation with Shared
+ *        Memory", "Handling Large Vectors").
+ *
+ * An unknown variant returns GTG_ERR_INVALID_VALUE; a grid beyond the CUDA
+ * limits (more than 65535 row blocks) returns GTG_ERR_UNSUPPORTED.
+ */
+enum { GTG_ABL_GEMM_NAIVE_16 = 0, GTG_ABL_GEMM_NAIVE_32 = 1, GTG_ABL_GEMM_TILED_16 = 2,
+       GTG_ABL_GEMM_TILED_32 = 3 };
+enum { GTG_ABL_GEMV_NAIVE = 0, GTG_ABL_GEMV_SHARED = 1 };
+
+GTG_API gtg_status gtg_ablation_gemm_f32(int variant, int64_t M, int64_t N, int64_t K,
+                                         const float *A, int64_t lda, const float *B, int64_t ldb,
+                                         float *C, int64_t ldc, cudaStream_t stream);
+GTG_API gtg_status gtg_ablation_gemv_f32(int variant, int64_t M, int64_t N, const float *A,
+                                         int64_t lda, const float *x, float *y, cudaStream_t stream);
+
 /* Static English text for a status code (never NULL). */
 GTG_API const char *gtg_status_string(gtg_status status);
 
