@@ -373,15 +373,16 @@ def sweep(dev, stream, peaks, l2):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
 
     def gemm_cfg(name, prec, M, N, K, A, B, peak, peak_name, iters, bias=None, act="none"):
-        esz = 2 if prec == "bf16" else 4
+        esz = 2 if prec in ("bf16", "f16") else 4
         need = (M * K + K * N) * esz + M * N * 4
         nrot = max(1, math.ceil(2 * l2 / need)) if l2 else 1
-        if prec == "bf16":
-            mk = lambda X: torch.from_numpy(X.view(np.int16)).view(torch.bfloat16).to(dev)
+        if prec in ("bf16", "f16"):
+            mk = lambda X: torch.from_numpy(X.view(np.int16)).to(dev)
         else:
             mk = lambda X: torch.from_numpy(X).to(dev)
         sets = [(mk(A), mk(B), torch.empty((M, N), device=dev)) for _ in range(nrot)]
-        fn = {"f32": gtg.gemm_f32_ex, "tf32": gtg.gemm_tf32_ex, "bf16": gtg.gemm_bf16_ex}[prec]
+        fn = {"f32": gtg.gemm_f32_ex, "tf32": gtg.gemm_tf32_ex, "bf16": gtg.gemm_bf16_ex,
+              "f16": gtg.gemm_f16_ex}[prec]
         dbias = torch.from_numpy(bias).to(dev) if bias is not None else None
         ep = gtg.epilogue(dbias.data_ptr() if dbias is not None else 0, act) if (bias is not None or act != "none") else None
 
@@ -424,6 +425,33 @@ def sweep(dev, stream, peaks, l2):
     gemm_cfg("f1: bf16 dense layer 8192^3, bias + ReLU", "bf16", 8192, 8192, 8192, A1, B1, bf16_peak,
              "bf16 burst", 20, bias=layer_bias, act="relu")
     del A1, B1, A2, B2
+    g16 = PCG32(9)
+    A16, B16 = g16.normal_f16((8192, 8192), 8192 ** -0.25), g16.normal_f16((8192, 8192), 8192 ** -0.25)
+    gemm_cfg("f2: f16 8192^3", "f16", 8192, 8192, 8192, A16, B16, bf16_peak, "bf16 burst (same rate)", 20)
+    del A16, B16
+
+    def batched_cfg(name, batch, M, N, K, iters, shared_B=False):
+        g = PCG32(10 + batch)
+        A = torch.from_numpy(g.normal_bf16((batch, M, K), K ** -0.25).view(np.int16)).to(dev)
+        B = torch.from_numpy(g.normal_bf16((1 if shared_B else batch, K, N), K ** -0.25).view(np.int16)).to(dev)
+        C = torch.empty((batch, M, N), device=dev)
+        sB = 0 if shared_B else K * N
+
+        def call(i):
+            st = gtg.gemm_strided_batched("bf16", M, N, K, A.data_ptr(), K, M * K, B.data_ptr(), N, sB,
+                                          C.data_ptr(), N, M * N, batch, None, sh)
+            assert st == gtg.GTG_OK, st
+
+        ms = time_launches(call, iters, stream)
+        tf = 2.0 * batch * M * N * K / (ms * 1e-3) / 1e12
+        out.append({"config": name, "path": "bf16 strided batch", "shape": [M, N, K], "batch": batch,
+                    "ms": round(ms, 4), "TFLOP/s": round(tf, 2), "peak": bf16_peak, "peak_name": "bf16 burst",
+                    "frac": round(tf / bf16_peak, 4)})
+
+    batched_cfg("f2: bf16 strided batch 16 x 2048^3", 16, 2048, 2048, 2048, 20)
+    batched_cfg("f2: bf16 strided batch 256 x 512x512x512", 256, 512, 512, 512, 50)
+    batched_cfg("f2: bf16 strided batch 64 x 1024x1024x256, shared B", 64, 1024, 1024, 256, 50, shared_B=True)
+    torch.cuda.empty_cache()
 
     out.extend(ablation(dev, stream, f32_peak, peaks.get("hbm_gbs", FALLBACK["hbm_gbs"]), l2))
 

@@ -26,7 +26,7 @@ LIB_PATH = os.path.join(_PKG, "libgtg.so")
 GTG_OK, GTG_ERR_INVALID_VALUE, GTG_ERR_MISALIGNED, GTG_ERR_ALIAS = 0, 1, 2, 3
 GTG_ERR_UNSUPPORTED, GTG_ERR_LAUNCH, GTG_ERR_TIMEOUT, GTG_ERR_DEVICE = 4, 5, 6, 7
 GTG_ERR_SCRATCH_LIMIT = 8
-PREC = {"f32": 0, "tf32": 1, "bf16": 2}
+PREC = {"f32": 0, "tf32": 1, "bf16": 2, "f16": 3}
 KERNELS = {0: "none", 1: "simt", 2: "tcgen05", 3: "zero_fill", 4: "gemv"}
 
 # names and C signatures of every exported function of include/gtg.h
@@ -59,6 +59,10 @@ SIGNATURES = {
     "gemm_f32_ex": (_int, [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ep, _ptr]),
     "gemm_tf32_ex": (_int, [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ep, _ptr]),
     "gemm_bf16_ex": (_int, [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ep, _ptr]),
+    "gemm_f16": (_int, [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr]),
+    "gemm_f16_ex": (_int, [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ep, _ptr]),
+    "gemm_strided_batched": (_int, [_int, _i64, _i64, _i64, _ptr, _i64, _i64, _ptr, _i64, _i64, _ptr, _i64, _i64,
+                                    _i64, _ep, _ptr]),
     "gemv_f32_ex": (_int, [_i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _int, _ep, _ptr]),
     "gtg_ablation_gemm_f32": (_int, [_int, _i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr]),
     "gtg_ablation_gemv_f32": (_int, [_int, _i64, _i64, _ptr, _i64, _ptr, _ptr, _ptr]),
@@ -118,6 +122,21 @@ def gemm_tf32(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
 
 def gemm_bf16(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
     return lib().gemm_bf16(M, N, K, A, lda, B, ldb, C, ldc, stream)
+
+
+def gemm_f16(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    return lib().gemm_f16(M, N, K, A, lda, B, ldb, C, ldc, stream)
+
+
+def gemm_f16_ex(M, N, K, A, lda, B, ldb, C, ldc, ep=None, stream=0) -> int:
+    return lib().gemm_f16_ex(M, N, K, A, lda, B, ldb, C, ldc, ctypes.byref(ep) if ep else None, stream)
+
+
+def gemm_strided_batched(precision, M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc, strideC, batch,
+                         ep=None, stream=0) -> int:
+    prec = PREC[precision] if isinstance(precision, str) else precision
+    return lib().gemm_strided_batched(prec, M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc, strideC, batch,
+                                      ctypes.byref(ep) if ep else None, stream)
 
 
 def gemv_f32(M, N, A, lda, x, ldx, y, ldy, batch, stream=0) -> int:
@@ -233,15 +252,15 @@ def _check(status: int, what: str):
         raise GtgError(status, what + extra)
 
 
-_IN_DTYPE = {"f32": "float32", "tf32": "float32", "bf16": "bfloat16"}
-_GEMM_EX = {"f32": gemm_f32_ex, "tf32": gemm_tf32_ex, "bf16": gemm_bf16_ex}
+_IN_DTYPE = {"f32": "float32", "tf32": "float32", "bf16": "bfloat16", "f16": "float16"}
+_GEMM_EX = {"f32": gemm_f32_ex, "tf32": gemm_tf32_ex, "bf16": gemm_bf16_ex, "f16": gemm_f16_ex}
 
 
 def matmul(A, B, precision: str = "f32", out=None, stream=None, bias=None, activation="none"):
     """C = act(A @ B + bias) on the GPU through gemm_<precision>_ex; C is FP32.
 
     A (M x K) and B (K x N) are row-major torch tensors: float32 for "f32" and
-    "tf32", bfloat16 for "bf16". `bias` (N float32 values, one per output
+    "tf32", bfloat16 for "bf16", float16 for "f16". `bias` (N float32 values, one per output
     column) and `activation` ("none" or "relu") form the fused epilogue.
     CUDA tensors are used in place. Host tensors are copied to the device
     (pinned host memory makes the copies asynchronous) and the result is

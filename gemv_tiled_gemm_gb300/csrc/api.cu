@@ -86,7 +86,7 @@ gtg_status validate_gemm(const GemmArgs &g) {
     if (g.M == 0 || g.N == 0) return GTG_OK;  // nothing to write
     if (g.C == nullptr) return GTG_ERR_INVALID_VALUE;
     if (g.K > 0 && (g.A == nullptr || g.B == nullptr)) return GTG_ERR_INVALID_VALUE;
-    const int64_t in_elem = g.prec == GTG_PREC_BF16 ? 2 : 4;
+    const int64_t in_elem = (g.prec == GTG_PREC_BF16 || g.prec == GTG_PREC_F16) ? 2 : 4;
     if ((reinterpret_cast<uintptr_t>(g.A) % in_elem) || (reinterpret_cast<uintptr_t>(g.B) % in_elem) ||
         (reinterpret_cast<uintptr_t>(g.C) % 4))
         return GTG_ERR_MISALIGNED;
@@ -99,6 +99,33 @@ gtg_status validate_gemm(const GemmArgs &g) {
         if (reinterpret_cast<uintptr_t>(g.bias) % 4) return GTG_ERR_MISALIGNED;
         if (overlaps(c, span_of(g.bias, 1, g.N, g.N, 4))) return GTG_ERR_ALIAS;
     }
+    return GTG_OK;
+}
+
+// A strided batch: every item is a valid single product (checked on item 0;
+// the others differ only by the strides), the outputs are pairwise apart,
+// and no output overlaps any input.
+gtg_status validate_batched(const GemmArgs &g) {
+    if (g.batch < 0 || g.strideA < 0 || g.strideB < 0 || g.strideC < 0) return GTG_ERR_INVALID_VALUE;
+    if (g.batch == 0 || g.M == 0 || g.N == 0) return GTG_OK;
+    GemmArgs one = g;
+    one.batch = 1;
+    gtg_status st = validate_gemm(one);
+    if (st != GTG_OK || g.batch == 1) return st;
+    const int64_t in_elem = (g.prec == GTG_PREC_BF16 || g.prec == GTG_PREC_F16) ? 2 : 4;
+    if (g.strideC < (g.M - 1) * g.ldc + g.N) return GTG_ERR_INVALID_VALUE;   // outputs would overlap
+    auto whole = [&](const void *p, int64_t rows, int64_t cols, int64_t ld, int64_t stride, int64_t elem) {
+        Span first = span_of(p, rows, cols, ld, elem);
+        first.hi += static_cast<uint64_t>((g.batch - 1) * stride * elem);
+        return first;
+    };
+    const Span c = whole(g.C, g.M, g.N, g.ldc, g.strideC, 4);
+    if (g.K > 0 && (overlaps(c, whole(g.A, g.M, g.K, g.lda, g.strideA, in_elem)) ||
+                    overlaps(c, whole(g.B, g.K, g.N, g.ldb, g.strideB, in_elem))))
+        return GTG_ERR_ALIAS;
+    if (g.bias && overlaps(c, span_of(g.bias, 1, g.N, g.N, 4))) return GTG_ERR_ALIAS;
+    const int64_t last = (g.batch - 1) * g.strideC + (g.M - 1) * g.ldc + g.N;
+    if (last > (int64_t{1} << 62)) return GTG_ERR_INVALID_VALUE;
     return GTG_OK;
 }
 
@@ -145,9 +172,9 @@ gtg_status plan_gemm_impl(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *pl
 }
 
 gtg_status run_gemm(const GemmArgs &g, cudaStream_t stream) {
-    gtg_status st = validate_gemm(g);
+    gtg_status st = g.batch == 1 ? validate_gemm(g) : validate_batched(g);
     if (st != GTG_OK) return st;
-    if (g.M == 0 || g.N == 0) return GTG_OK;
+    if (g.M == 0 || g.N == 0 || g.batch == 0) return GTG_OK;
     DeviceInfo dev;
     if ((st = current_device(&dev)) != GTG_OK) return st;
     gtg_plan plan;
@@ -155,8 +182,11 @@ gtg_status run_gemm(const GemmArgs &g, cudaStream_t stream) {
     cudaError_t e = cudaSuccess;
     switch (plan.kernel) {
         case GTG_KERNEL_ZERO_FILL:
-            e = (g.bias || g.act) ? epilogue_fill_launch(g.C, g.M, g.N, g.ldc, g.bias, 1, g.act, stream)
-                                  : zero_fill_launch(g.C, g.M, g.N, g.ldc, stream);
+            for (int64_t b = 0; b < g.batch && e == cudaSuccess; ++b) {
+                float *Cb = g.C + b * g.strideC;
+                e = (g.bias || g.act) ? epilogue_fill_launch(Cb, g.M, g.N, g.ldc, g.bias, 1, g.act, stream)
+                                      : zero_fill_launch(Cb, g.M, g.N, g.ldc, stream);
+            }
             break;
         case GTG_KERNEL_TCGEN05: e = tc_launch(dev, g, plan, stream); break;
         case GTG_KERNEL_SIMT: e = simt_launch(dev, g, plan, stream); break;
@@ -269,6 +299,30 @@ static GemmArgs with_epilogue(GemmArgs g, const gtg_epilogue *ep) {
     return g;
 }
 
+gtg_status gemm_f16(int64_t M, int64_t N, int64_t K, const gtg_f16 *A, int64_t lda, const gtg_f16 *B,
+                    int64_t ldb, float *C, int64_t ldc, cudaStream_t stream) {
+    return run_gemm(GemmArgs{GTG_PREC_F16, M, N, K, A, lda, B, ldb, C, ldc}, stream);
+}
+
+gtg_status gemm_f16_ex(int64_t M, int64_t N, int64_t K, const gtg_f16 *A, int64_t lda, const gtg_f16 *B,
+                       int64_t ldb, float *C, int64_t ldc, const gtg_epilogue *ep, cudaStream_t stream) {
+    return run_gemm(with_epilogue(GemmArgs{GTG_PREC_F16, M, N, K, A, lda, B, ldb, C, ldc}, ep), stream);
+}
+
+gtg_status gemm_strided_batched(int precision, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
+                                int64_t strideA, const void *B, int64_t ldb, int64_t strideB, float *C,
+                                int64_t ldc, int64_t strideC, int64_t batch, const gtg_epilogue *ep,
+                                cudaStream_t stream) {
+    if (precision < GTG_PREC_F32 || precision > GTG_PREC_F16) return GTG_ERR_INVALID_VALUE;
+    GemmArgs g = with_epilogue(GemmArgs{precision, M, N, K, A, lda, B, ldb, C, ldc}, ep);
+    g.batch = batch;
+    g.strideA = strideA;
+    g.strideB = strideB;
+    g.strideC = strideC;
+    if (batch < 0) return GTG_ERR_INVALID_VALUE;
+    return run_gemm(g, stream);
+}
+
 gtg_status gemm_f32_ex(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
                        int64_t ldb, float *C, int64_t ldc, const gtg_epilogue *ep, cudaStream_t stream) {
     return run_gemm(with_epilogue(GemmArgs{GTG_PREC_F32, M, N, K, A, lda, B, ldb, C, ldc}, ep), stream);
@@ -355,7 +409,7 @@ const char *gtg_last_cuda_error(void) { return t_cuda_error; }
 
 gtg_status gtg_plan_gemm(int precision, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
                          const void *B, int64_t ldb, const void *C, int64_t ldc, gtg_plan *plan) {
-    if (plan == nullptr || precision < GTG_PREC_F32 || precision > GTG_PREC_BF16) return GTG_ERR_INVALID_VALUE;
+    if (plan == nullptr || precision < GTG_PREC_F32 || precision > GTG_PREC_F16) return GTG_ERR_INVALID_VALUE;
     const GemmArgs g{precision, M, N, K, A, lda, B, ldb, const_cast<float *>(static_cast<const float *>(C)), ldc};
     gtg_status st = validate_gemm(g);
     if (st != GTG_OK) return st;

@@ -17,6 +17,7 @@
 // A is stored transposed in shared memory (k-major) so that a thread's 8 rows
 // are two 16-byte reads; B keeps its row-major layout.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <algorithm>
 #include <mutex>
@@ -48,6 +49,21 @@ struct Load<uint16_t> {
         return make_float4(bf(v.x & 0xFFFFu), bf(v.x >> 16), bf(v.y & 0xFFFFu), bf(v.y >> 16));
     }
     static __device__ __forceinline__ float one(const uint16_t *p) { return bf(__ldg(p)); }
+};
+
+// FP16 stored as 16-bit patterns; widening to FP32 is exact.
+template <>
+struct Load<__half> {
+    static __device__ __forceinline__ float h(uint32_t bits) {
+        return __half2float(__ushort_as_half(static_cast<unsigned short>(bits)));
+    }
+    static __device__ __forceinline__ float4 vec4(const __half *p) {
+        const uint2 v = __ldg(reinterpret_cast<const uint2 *>(p));
+        return make_float4(h(v.x & 0xFFFFu), h(v.x >> 16), h(v.y & 0xFFFFu), h(v.y >> 16));
+    }
+    static __device__ __forceinline__ float one(const __half *p) {
+        return h(__ldg(reinterpret_cast<const unsigned short *>(p)));
+    }
 };
 
 template <typename T, int BM, int BN, bool VEC>
@@ -316,8 +332,8 @@ cudaError_t launch_typed(const GemmArgs &g, const gtg_plan &plan, cudaStream_t s
 }
 
 bool vec_ok(const GemmArgs &g) {
-    // 4 consecutive elements per load: 16 bytes for FP32, 8 for BF16.
-    const uintptr_t mask = g.prec == GTG_PREC_BF16 ? 7 : 15;
+    // 4 consecutive elements per load: 16 bytes for FP32, 8 for BF16 / FP16.
+    const uintptr_t mask = (g.prec == GTG_PREC_BF16 || g.prec == GTG_PREC_F16) ? 7 : 15;
     return (reinterpret_cast<uintptr_t>(g.A) & mask) == 0 && (reinterpret_cast<uintptr_t>(g.B) & mask) == 0 &&
            (g.lda % 4) == 0 && (g.ldb % 4) == 0;
 }
@@ -366,10 +382,24 @@ void simt_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
 cudaError_t simt_launch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan,
                         cudaStream_t stream) {
     (void)dev;
-    const bool vec = vec_ok(g);
-    if (g.prec == GTG_PREC_BF16)
-        return vec ? launch_typed<uint16_t, true>(g, plan, stream) : launch_typed<uint16_t, false>(g, plan, stream);
-    return vec ? launch_typed<float, true>(g, plan, stream) : launch_typed<float, false>(g, plan, stream);
+    const int64_t elem = (g.prec == GTG_PREC_BF16 || g.prec == GTG_PREC_F16) ? 2 : 4;
+    for (int64_t b = 0; b < g.batch; ++b) {   // a strided batch runs item by item
+        GemmArgs gb = g;
+        gb.A = static_cast<const char *>(g.A) + b * g.strideA * elem;
+        gb.B = static_cast<const char *>(g.B) + b * g.strideB * elem;
+        gb.C = g.C + b * g.strideC;
+        gb.batch = 1;
+        const bool vec = vec_ok(gb);
+        cudaError_t e;
+        if (g.prec == GTG_PREC_BF16)
+            e = vec ? launch_typed<uint16_t, true>(gb, plan, stream) : launch_typed<uint16_t, false>(gb, plan, stream);
+        else if (g.prec == GTG_PREC_F16)
+            e = vec ? launch_typed<__half, true>(gb, plan, stream) : launch_typed<__half, false>(gb, plan, stream);
+        else
+            e = vec ? launch_typed<float, true>(gb, plan, stream) : launch_typed<float, false>(gb, plan, stream);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t epilogue_fill_launch(float *C, int64_t M, int64_t N, int64_t ldc, const float *bias, int per_column,

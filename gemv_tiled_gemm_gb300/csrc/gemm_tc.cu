@@ -1,4 +1,5 @@
-// Tensor-core GEMM for sm_103a: C (FP32) = A * B with BF16 or TF32 operands.
+// Tensor-core GEMM for sm_103a: C (FP32) = A * B with BF16, FP16 or TF32 operands,
+// one matrix or a strided batch of them.
 //
 // The tiling principle is the one of "GPU Matrix Multiplication: Tiling and
 // Shared Memory" (section 3) and "CUDA Programming (6)" (section 3.2): each
@@ -80,7 +81,10 @@ struct TcParams {
     float *C;
     long long ldc;
     int M, N;
-    int num_m, num_n, num_kb, num_tiles;
+    int num_m, num_n, num_kb, num_tiles;   // num_tiles counts every item of a batch
+    int tiles_per_batch;
+    long long strideC;           // elements between the C matrices of consecutive batch items
+    uint32_t idesc;              // instruction descriptor (A/B format: FP16 or BF16) of the 16-bit kernels
     int c_vec;                   // widest store for whole rows of a tile: 2 = 32 B, 1 = 16 B, 0 = 4 B
     int *status;
     unsigned long long wait_limit_ns;
@@ -205,7 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
                 int mb, nb;
-                tile_coords(t, p, mb, nb);
+                const int bi = t / p.tiles_per_batch;
+                tile_coords(t - bi * p.tiles_per_batch, p, mb, nb);
                 for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
                     const int s = static_cast<int>(it % S::STAGES);
                     const uint32_t ph = (it / S::STAGES) & 1u;
@@ -215,15 +220,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (p.drop_slice == static_cast<int>(it) && blockIdx.x == 0) continue;
                     ptx::mbar_arrive_expect_tx(full_bar(s), S::STAGE_BYTES);
-                    ptx::tma_load_2d(sA + s * S::A_BYTES, &tmA, full_bar(s), kb * S::BK, mb * S::BM);
+                    ptx::tma_load_3d(sA + s * S::A_BYTES, &tmA, full_bar(s), kb * S::BK, mb * S::BM, bi);
                     if constexpr (S::B_KMAJOR) {
                         // B^T tile: BN rows of BK elements
-                        ptx::tma_load_2d(sB + s * S::B_BYTES, &tmB, full_bar(s), kb * S::BK, nb * BN);
+                        ptx::tma_load_3d(sB + s * S::B_BYTES, &tmB, full_bar(s), kb * S::BK, nb * BN, bi);
                     } else {
 #pragma unroll
                         for (int c = 0; c < S::B_CHUNKS; ++c)
-                            ptx::tma_load_2d(sB + s * S::B_BYTES + c * S::BCH_BYTES, &tmB, full_bar(s),
-                                             nb * BN + c * S::BCH_N, kb * S::BK);
+                            ptx::tma_load_3d(sB + s * S::B_BYTES + c * S::BCH_BYTES, &tmB, full_bar(s),
+                                             nb * BN + c * S::BCH_N, kb * S::BK, bi);
                     }
                 }
             }
@@ -277,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if constexpr (TF32)
                             ptx::mma_tf32(d_tmem, ad, bd, S::IDESC, accum);
                         else
-                            ptx::mma_bf16(d_tmem, ad, bd, S::IDESC, accum);
+                            ptx::mma_bf16(d_tmem, ad, bd, p.idesc, accum);
                     }
                     ptx::mma_commit(empty_bar(s));  // slot free once these MMAs have read it
                     issued = true;
@@ -298,7 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int local = 0;
         for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++local) {
             int mb, nb;
-            tile_coords(t, p, mb, nb);
+            const int bi = t / p.tiles_per_batch;
+            tile_coords(t - bi * p.tiles_per_batch, p, mb, nb);
             const int acc = local & 1;
             const uint32_t aph = (static_cast<uint32_t>(local) >> 1) & 1u;
             if (!wait_bar(accf_bar(acc), aph, abort_flag, p)) break;
@@ -307,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int col0 = nb * BN;
             const bool row_ok = row < p.M;
             const bool whole = p.c_vec && (col0 + BN <= p.N);
-            float *crow = p.C + static_cast<long long>(row) * p.ldc + col0;
+            float *crow = p.C + bi * p.strideC + static_cast<long long>(row) * p.ldc + col0;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
@@ -460,7 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int t = cluster_id; ok && t < p.num_tiles; t += nclusters) {
                 int mb, nb;
-                pair_tile_coords(t, p, mb, nb);
+                const int bi = t / p.tiles_per_batch;
+                pair_tile_coords(t - bi * p.tiles_per_batch, p, mb, nb);
                 const int row0 = mb * 2 * S::BM + static_cast<int>(rank) * S::BM;
                 const int col0 = nb * S::BN + static_cast<int>(rank) * (S::BN / 2);
                 for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
@@ -473,11 +480,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (p.drop_slice == static_cast<int>(it) && cluster_id == 0 && leader) continue;
                     if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), 2 * S::STAGE_BYTES);
                     const uint32_t fb = leader_full0 + 8u * s;
-                    ptx::tma_load_2d_pair(sA + s * S::A_BYTES, &tmA, fb, kb * S::BK, row0);
+                    ptx::tma_load_3d_pair(sA + s * S::A_BYTES, &tmA, fb, kb * S::BK, row0, bi);
 #pragma unroll
                     for (int c = 0; c < S::B_CHUNKS; ++c)
-                        ptx::tma_load_2d_pair(sB + s * S::B_BYTES + c * S::BCH_BYTES, &tmB, fb, col0 + c * S::BCH_N,
-                                              kb * S::BK);
+                        ptx::tma_load_3d_pair(sB + s * S::B_BYTES + c * S::BCH_BYTES, &tmB, fb, col0 + c * S::BCH_N,
+                                              kb * S::BK, bi);
                 }
             }
             if (!ok) {
@@ -523,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int k = 0; k < S::KSTEPS; ++k) {
                         const uint64_t ad = ptx::smem_desc_sw128(a0 + k * 32, 16, 1024);
                         const uint64_t bd = ptx::smem_desc_sw128(b0 + k * S::UK * 128, S::BCH_BYTES, 1024);
-                        ptx::mma_bf16_pair(d_tmem, ad, bd, S::IDESC, (kb > 0 || k > 0) ? 1u : 0u);
+                        ptx::mma_bf16_pair(d_tmem, ad, bd, p.idesc, (kb > 0 || k > 0) ? 1u : 0u);
                     }
                     ptx::mma_commit_pair(empty_bar(s), 0x3);
                 }
@@ -541,7 +548,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int local = 0;
         for (int t = cluster_id; t < p.num_tiles; t += nclusters, ++local) {
             int mb, nb;
-            pair_tile_coords(t, p, mb, nb);
+            const int bi = t / p.tiles_per_batch;
+            pair_tile_coords(t - bi * p.tiles_per_batch, p, mb, nb);
             const int acc = local & 1;
             const uint32_t aph = (static_cast<uint32_t>(local) >> 1) & 1u;
             if (!wait_bar(accf_bar(acc), aph, abort_flag, p)) break;
@@ -550,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int col0 = nb * S::BN;
             const bool row_ok = row < p.M;
             const bool whole = p.c_vec && (col0 + S::BN <= p.N);
-            float *crow = p.C + static_cast<long long>(row) * p.ldc + col0;
+            float *crow = p.C + bi * p.strideC + static_cast<long long>(row) * p.ldc + col0;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * S::BN);
 #pragma unroll 1
@@ -596,10 +604,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // B (K x N, leading dimension ldb) -> Bt (N x K, leading dimension ldbt),
 // through a padded shared-memory tile so that reads and writes are both
-// coalesced.
+// coalesced. blockIdx.z walks the items of a batch (strideB apart in B,
+// N * ldbt apart in Bt).
 __global__ void __launch_bounds__(256) transpose_kernel(const float *__restrict__ B, long long ldb,
-                                                        float *__restrict__ Bt, long long ldbt, int K, int N) {
+                                                        float *__restrict__ Bt, long long ldbt, int K, int N,
+                                                        long long strideB) {
     __shared__ float tile[32][33];
+    B += blockIdx.z * strideB;
+    Bt += blockIdx.z * static_cast<long long>(N) * ldbt;
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
     const int n0 = blockIdx.x * 32;
     for (int k0 = blockIdx.y * 32; k0 < K; k0 += gridDim.y * 32) {
@@ -650,20 +662,37 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-bool encode_2d(CUtensorMap *map, bool tf32, const void *base, uint64_t inner, uint64_t outer,
-               uint64_t ld_elems, uint32_t box_inner, uint32_t box_outer) {
+CUtensorMapDataType tma_type(int prec) {
+    switch (prec) {
+        case GTG_PREC_TF32: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+        case GTG_PREC_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+        default: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    }
+}
+
+// A row-major matrix (outer rows of `inner` elements, ld_elems apart) as a
+// 3-D tensor map whose third dimension walks `batch` matrices
+// batch_stride_elems apart; boxes of box_inner x box_outer x 1, 128-byte
+// swizzled, out-of-range elements read as zero.
+bool encode_3d(CUtensorMap *map, int prec, const void *base, uint64_t inner, uint64_t outer, uint64_t ld_elems,
+               uint64_t batch, uint64_t batch_stride_elems, uint32_t box_inner, uint32_t box_outer) {
     auto fn = encode_fn();
     if (!fn) return false;
-    const uint64_t elem = tf32 ? 4 : 2;
-    cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {ld_elems * elem};
-    cuuint32_t box[2] = {box_inner, box_outer};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, tf32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                    const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    const uint64_t elem = prec == GTG_PREC_TF32 ? 4 : 2;
+    if (batch <= 1) batch_stride_elems = (ld_elems * outer * elem + 15) / 16 * 16 / elem;  // unused, but valid
+    cuuint64_t dims[3] = {inner, outer, batch < 1 ? 1 : batch};
+    cuuint64_t strides[2] = {ld_elems * elem, batch_stride_elems * elem};
+    cuuint32_t box[3] = {box_inner, box_outer, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, tma_type(prec), 3, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// Instruction descriptor of the 16-bit kernels for this call's input format.
+uint32_t idesc16(int prec, uint32_t M, uint32_t N) {
+    return ptx::make_idesc(prec == GTG_PREC_F16 ? 0u : 1u, 0u, 1u, M, N);
 }
 
 std::atomic<int> g_pair_enabled{1};
@@ -712,26 +741,29 @@ cudaError_t launch_impl(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
         }
     }
     CUtensorMap ta, tb;
-    if (!encode_2d(&ta, TF32, g.A, g.K, g.M, g.lda, S::BK, S::BM)) return cudaErrorInvalidValue;
+    if (!encode_3d(&ta, g.prec, g.A, g.K, g.M, g.lda, g.batch, g.strideA, S::BK, S::BM)) return cudaErrorInvalidValue;
     float *bt = nullptr;
     if constexpr (S::B_KMAJOR) {
         const int64_t ldbt = (g.K + 3) / 4 * 4;   // 16-byte rows for the tensor map
-        cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&bt), static_cast<size_t>(g.N * ldbt) * 4, stream);
+        cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&bt),
+                                        static_cast<size_t>(g.batch * g.N * ldbt) * 4, stream);
         if (e != cudaSuccess) return e;
         const dim3 tgrid(static_cast<unsigned>((g.N + 31) / 32),
-                         static_cast<unsigned>(std::min<int64_t>((g.K + 31) / 32, 65535)));
+                         static_cast<unsigned>(std::min<int64_t>((g.K + 31) / 32, 65535)),
+                         static_cast<unsigned>(g.batch));
         transpose_kernel<<<tgrid, 256, 0, stream>>>(static_cast<const float *>(g.B), g.ldb, bt, ldbt,
-                                                    static_cast<int>(g.K), static_cast<int>(g.N));
+                                                    static_cast<int>(g.K), static_cast<int>(g.N), g.strideB);
         if ((e = cudaGetLastError()) != cudaSuccess) {
             cudaFreeAsync(bt, stream);
             return e;
         }
-        if (!encode_2d(&tb, TF32, bt, g.K, g.N, ldbt, S::BK, BN)) {
+        if (!encode_3d(&tb, g.prec, bt, g.K, g.N, ldbt, g.batch, g.N * ldbt, S::BK, BN)) {
             cudaFreeAsync(bt, stream);
             return cudaErrorInvalidValue;
         }
     } else {
-        if (!encode_2d(&tb, TF32, g.B, g.N, g.K, g.ldb, S::BCH_N, S::BK)) return cudaErrorInvalidValue;
+        if (!encode_3d(&tb, g.prec, g.B, g.N, g.K, g.ldb, g.batch, g.strideB, S::BCH_N, S::BK))
+            return cudaErrorInvalidValue;
     }
     TcParams p;
     p.C = g.C;
@@ -741,7 +773,10 @@ cudaError_t launch_impl(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
     p.num_m = static_cast<int>((g.M + S::BM - 1) / S::BM);
     p.num_n = static_cast<int>((g.N + BN - 1) / BN);
     p.num_kb = static_cast<int>((g.K + S::BK - 1) / S::BK);
-    p.num_tiles = p.num_m * p.num_n;
+    p.tiles_per_batch = p.num_m * p.num_n;
+    p.num_tiles = static_cast<int>(p.tiles_per_batch * g.batch);
+    p.strideC = g.strideC;
+    p.idesc = TF32 ? S::IDESC : idesc16(g.prec, S::BM, BN);
     p.c_vec = c_store_width(g);
     p.status = dev.status;
     p.wait_limit_ns = wait_limit_ns();
@@ -771,8 +806,9 @@ cudaError_t launch_pair(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
         }
     }
     CUtensorMap ta, tb;
-    if (!encode_2d(&ta, false, g.A, g.K, g.M, g.lda, S::BK, S::BM)) return cudaErrorInvalidValue;
-    if (!encode_2d(&tb, false, g.B, g.N, g.K, g.ldb, S::BCH_N, S::BK)) return cudaErrorInvalidValue;
+    if (!encode_3d(&ta, g.prec, g.A, g.K, g.M, g.lda, g.batch, g.strideA, S::BK, S::BM)) return cudaErrorInvalidValue;
+    if (!encode_3d(&tb, g.prec, g.B, g.N, g.K, g.ldb, g.batch, g.strideB, S::BCH_N, S::BK))
+        return cudaErrorInvalidValue;
     TcParams p;
     p.C = g.C;
     p.ldc = g.ldc;
@@ -781,7 +817,10 @@ cudaError_t launch_pair(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
     p.num_m = static_cast<int>((g.M + 2 * S::BM - 1) / (2 * S::BM));
     p.num_n = static_cast<int>((g.N + S::BN - 1) / S::BN);
     p.num_kb = static_cast<int>((g.K + S::BK - 1) / S::BK);
-    p.num_tiles = p.num_m * p.num_n;
+    p.tiles_per_batch = p.num_m * p.num_n;
+    p.num_tiles = static_cast<int>(p.tiles_per_batch * g.batch);
+    p.strideC = g.strideC;
+    p.idesc = idesc16(g.prec, 2 * S::BM, S::BN);
     p.c_vec = c_store_width(g);
     p.status = dev.status;
     p.wait_limit_ns = wait_limit_ns();
@@ -807,7 +846,7 @@ cudaError_t launch_pair(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
 
 void fill_pair_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
     using S = PairShape;
-    const int64_t tiles = ((g.M + 2 * S::BM - 1) / (2 * S::BM)) * ((g.N + S::BN - 1) / S::BN);
+    const int64_t tiles = g.batch * ((g.M + 2 * S::BM - 1) / (2 * S::BM)) * ((g.N + S::BN - 1) / S::BN);
     const int64_t clusters = std::min<int64_t>(tiles, dev.sms / 2);
     plan->kernel = GTG_KERNEL_TCGEN05;
     plan->bm = 2 * S::BM;
@@ -822,7 +861,7 @@ void fill_pair_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
 template <bool TF32, int BN>
 void fill_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
     using S = Shape<TF32, BN>;
-    const int64_t tiles = ((g.M + S::BM - 1) / S::BM) * ((g.N + BN - 1) / BN);
+    const int64_t tiles = g.batch * ((g.M + S::BM - 1) / S::BM) * ((g.N + BN - 1) / BN);
     plan->kernel = GTG_KERNEL_TCGEN05;
     plan->bm = S::BM;
     plan->bn = BN;
@@ -844,12 +883,18 @@ bool tc_supported(const DeviceInfo &dev) {
 }
 
 bool tc_eligible(const GemmArgs &g) {
-    if (g.prec != GTG_PREC_TF32 && g.prec != GTG_PREC_BF16) return false;
+    if (g.prec != GTG_PREC_TF32 && g.prec != GTG_PREC_BF16 && g.prec != GTG_PREC_F16) return false;
     const int64_t elem = g.prec == GTG_PREC_TF32 ? 4 : 2;
+    if (g.batch > 1) {
+        // batch strides are tensor-map strides (A always; B unless it goes through the transpose)
+        if ((g.strideA * elem) % 16 || (g.strideA * elem) >= (1ll << 40)) return false;
+        if (g.prec != GTG_PREC_TF32 && ((g.strideB * elem) % 16 || (g.strideB * elem) >= (1ll << 40))) return false;
+        if (g.batch > 65535 || g.batch * ((g.M + 127) / 128) * ((g.N + 63) / 64) > INT32_MAX) return false;
+    }
     const auto a = reinterpret_cast<uintptr_t>(g.A), b = reinterpret_cast<uintptr_t>(g.B);
     if ((a & 15) || (g.lda * elem) % 16) return false;           // TMA base and row stride of A
-    // BF16 B is read by TMA in place; TF32 B goes through the transpose kernel
-    if (g.prec == GTG_PREC_BF16 && ((b & 15) || (g.ldb * elem) % 16)) return false;
+    // 16-bit B is read by TMA in place; TF32 B goes through the transpose kernel
+    if (g.prec != GTG_PREC_TF32 && ((b & 15) || (g.ldb * elem) % 16)) return false;
     if (g.M > INT32_MAX || g.N > INT32_MAX || g.K > INT32_MAX) return false;
     if ((g.lda * elem) >= (1ll << 40) || (g.ldb * elem) >= (1ll << 40)) return false;
     return g.M > 0 && g.N > 0 && g.K > 0;
@@ -865,7 +910,7 @@ void tc_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
     int best = 0;
     double best_cost = 0;
     for (int i = 0; i < 3; ++i) {
-        const int64_t tiles = ((g.M + kBM - 1) / kBM) * ((g.N + widths[i] - 1) / widths[i]);
+        const int64_t tiles = g.batch * ((g.M + kBM - 1) / kBM) * ((g.N + widths[i] - 1) / widths[i]);
         const int64_t waves = (tiles + dev.sms - 1) / dev.sms;
         const double cost = static_cast<double>(waves) * widths[i] / eff[i];
         if (i == 0 || cost < best_cost) {
@@ -877,7 +922,7 @@ void tc_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
     if (!tf32 && (dev.sms & 1) == 0) {
         // CTA pairs: 256 x 256 tiles on sms/2 clusters, operands 2/3 of the
         // single-CTA 128 x 256 tile's bytes per SM
-        const int64_t tiles = ((g.M + 255) / 256) * ((g.N + 255) / 256);
+        const int64_t tiles = g.batch * ((g.M + 255) / 256) * ((g.N + 255) / 256);
         const int64_t waves = (tiles + dev.sms / 2 - 1) / (dev.sms / 2);
         const double cost = static_cast<double>(waves) * 256 / 1.15;
         if (cost < best_cost && g_pair_enabled.load()) {
@@ -967,15 +1012,15 @@ cudaError_t launch_tf32_fixed(const DeviceInfo &dev, const GemmArgs &g, const gt
         }
     }
     CUtensorMap ta, tb;
-    if (!encode_2d(&ta, true, g.A, g.K, g.M, g.lda, S::BK, S::BM)) return cudaErrorInvalidValue;
+    if (!encode_3d(&ta, GTG_PREC_TF32, g.A, g.K, g.M, g.lda, 1, 0, S::BK, S::BM)) return cudaErrorInvalidValue;
     const int64_t ldbt = (g.K + 3) / 4 * 4;
-    if (!encode_2d(&tb, true, bt, g.K, g.N, ldbt, S::BK, BN)) return cudaErrorInvalidValue;
+    if (!encode_3d(&tb, GTG_PREC_TF32, bt, g.K, g.N, ldbt, 1, 0, S::BK, BN)) return cudaErrorInvalidValue;
     // B^T overwrites every element the GEMM reads, so the array's previous
     // contents never matter and nothing needs clearing.
     const dim3 tgrid(static_cast<unsigned>((g.N + 31) / 32),
                      static_cast<unsigned>(std::min<int64_t>((g.K + 31) / 32, 65535)));
     transpose_kernel<<<tgrid, 256, 0, stream>>>(static_cast<const float *>(g.B), g.ldb, bt, ldbt,
-                                                static_cast<int>(g.K), static_cast<int>(g.N));
+                                                static_cast<int>(g.K), static_cast<int>(g.N), 0);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     TcParams p;
@@ -986,7 +1031,10 @@ cudaError_t launch_tf32_fixed(const DeviceInfo &dev, const GemmArgs &g, const gt
     p.num_m = static_cast<int>((g.M + S::BM - 1) / S::BM);
     p.num_n = static_cast<int>((g.N + BN - 1) / BN);
     p.num_kb = static_cast<int>((g.K + S::BK - 1) / S::BK);
-    p.num_tiles = p.num_m * p.num_n;
+    p.tiles_per_batch = p.num_m * p.num_n;
+    p.num_tiles = p.tiles_per_batch;
+    p.strideC = 0;
+    p.idesc = S::IDESC;
     p.c_vec = c_store_width(g);
     p.status = dev.status;
     p.wait_limit_ns = wait_limit_ns();

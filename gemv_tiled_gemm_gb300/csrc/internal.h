@@ -28,6 +28,8 @@ struct GemmArgs {
     float *C; int64_t ldc;
     const float *bias = nullptr; // N entries or null
     int act = 0;                 // GTG_ACT_*
+    // strided batch: item b uses A + b*strideA, B + b*strideB, C + b*strideC (elements)
+    int64_t batch = 1, strideA = 0, strideB = 0, strideC = 0;
 };
 
 // y_b = act(A * x_b + bias) with one bias per row of A.

@@ -144,6 +144,21 @@ GTG_API gtg_status gemm_bf16(int64_t M, int64_t N, int64_t K,
                      float *C, int64_t ldc,
                      cudaStream_t stream);
 
+/* An IEEE binary16 value stored as its 16-bit pattern. */
+typedef uint16_t gtg_f16;
+
+/*
+ * gemm_f16 -- C = A*B with FP16 inputs, FP32 accumulation on the tensor cores
+ * (tcgen05.mma kind::f16) and an FP32 output ("Matrix Operations",
+ * "Performance Considerations": half precision). FP16 products are exact in
+ * FP32. Same arguments, alignment rules and fallback as gemm_bf16.
+ */
+GTG_API gtg_status gemm_f16(int64_t M, int64_t N, int64_t K,
+                            const gtg_f16 *A, int64_t lda,
+                            const gtg_f16 *B, int64_t ldb,
+                            float *C, int64_t ldc,
+                            cudaStream_t stream);
+
 /*
  * gemv_f32 -- y_b = A*x_b for `batch` vectors at once, in FP32 ("Matrix
  * Operations", "Matrix-Vector Multiplication": the fully connected layer;
@@ -246,6 +261,37 @@ GTG_API gtg_status gemm_bf16_ex(int64_t M, int64_t N, int64_t K, const gtg_bf16 
 GTG_API gtg_status gemv_f32_ex(int64_t M, int64_t N, const float *A, int64_t lda,
                                const float *x, int64_t ldx, float *y, int64_t ldy, int batch,
                                const gtg_epilogue *epilogue, cudaStream_t stream);
+GTG_API gtg_status gemm_f16_ex(int64_t M, int64_t N, int64_t K, const gtg_f16 *A, int64_t lda,
+                               const gtg_f16 *B, int64_t ldb, float *C, int64_t ldc,
+                               const gtg_epilogue *epilogue, cudaStream_t stream);
+
+/*
+ * gemm_strided_batched -- `batch` independent products in one call ("Matrix
+ * Operations", "Performance Considerations": processing several matrix
+ * multiplications in parallel):
+ *
+ *   C_b = act(A_b * B_b + bias),  A_b = A + b*strideA, B_b = B + b*strideB,
+ *   C_b = C + b*strideC  (strides in elements, b = 0 .. batch-1)
+ *
+ *   precision  GTG_PREC_F32, _TF32, _BF16 or _F16 (A and B element type as in
+ *              the single-matrix calls; C is FP32)
+ *   batch      >= 0; strideA, strideB >= 0 (0 reuses one operand for every
+ *              item); strideC must keep the outputs apart
+ *              (strideC >= (M-1)*ldc + N when batch > 1)
+ *   epilogue   as for gemm_*_ex (the same bias for every item), or NULL
+ *
+ * The tensor-core kernels walk the output tiles of all items in one launch
+ * (their tensor maps get the batch as a third dimension, so strideA and,
+ * for 16-bit inputs, strideB must be multiples of 16 bytes); other layouts
+ * run item by item on the SIMT kernel. Errors as for the single calls; no
+ * item is computed if the arguments of any item are invalid.
+ */
+GTG_API gtg_status gemm_strided_batched(int precision, int64_t M, int64_t N, int64_t K,
+                                        const void *A, int64_t lda, int64_t strideA,
+                                        const void *B, int64_t ldb, int64_t strideB,
+                                        float *C, int64_t ldc, int64_t strideC,
+                                        int64_t batch, const gtg_epilogue *epilogue,
+                                        cudaStream_t stream);
 
 /*
  * The pages' own kernel designs, kept for measurement against the kernels
@@ -298,7 +344,7 @@ GTG_API const char *gtg_last_cuda_error(void);
  * device work). Fills *plan. `precision` is GTG_PREC_F32, _TF32 or _BF16.
  * Returns the same validation status the GEMM call itself would.
  */
-enum { GTG_PREC_F32 = 0, GTG_PREC_TF32 = 1, GTG_PREC_BF16 = 2 };
+enum { GTG_PREC_F32 = 0, GTG_PREC_TF32 = 1, GTG_PREC_BF16 = 2, GTG_PREC_F16 = 3 };
 enum { GTG_KERNEL_NONE = 0, GTG_KERNEL_SIMT = 1, GTG_KERNEL_TCGEN05 = 2,
        GTG_KERNEL_ZERO_FILL = 3, GTG_KERNEL_GEMV = 4 };
 typedef struct {

@@ -22,7 +22,7 @@ Distributions:
     u1 = ((r0 >> 8) + 1) * 2^-24 in (0, 1], u2 = (r1 >> 8) * 2^-24 in [0, 1);
     z0 = sqrt(-2 ln u1) cos(2 pi u2), z1 = sqrt(-2 ln u1) sin(2 pi u2), both
     used, in that order; then scaled by sigma.
-  * BF16: round-to-nearest-even directly from the FP64 value.
+  * BF16 and FP16: round-to-nearest-even directly from the FP64 value.
 """
 
 from __future__ import annotations
@@ -133,6 +133,14 @@ class PCG32:
             out[off:off + z.size] = z
         return out.reshape(shape)
 
+    def normal_f16(self, shape, sigma: float = 1.0) -> np.ndarray:
+        """normal(0, sigma) rounded to FP16; returned as uint16 bit patterns."""
+        n = int(np.prod(shape))
+        out = np.empty(n, dtype=np.uint16)
+        for off, z in self._normal_chunks(n, sigma):
+            out[off:off + z.size] = f64_to_f16_bits(z)
+        return out.reshape(shape)
+
     def normal_bf16(self, shape, sigma: float = 1.0) -> np.ndarray:
         """normal(0, sigma) rounded to BF16; returned as uint16 bit patterns."""
         n = int(np.prod(shape))
@@ -155,6 +163,16 @@ def f64_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     r = (b + (np.uint64((1 << 44) - 1) + lsb)) & ~np.uint64((1 << 45) - 1)
     f = r.view(np.float64).astype(np.float32)
     return (f.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def f64_to_f16_bits(x: np.ndarray) -> np.ndarray:
+    """Round FP64 values to the nearest IEEE binary16 (ties to even); uint16 bits."""
+    return np.asarray(x, dtype=np.float64).astype(np.float16).view(np.uint16)
+
+
+def f16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of binary16 bit patterns to FP32."""
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float32)
 
 
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:

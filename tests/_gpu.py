@@ -6,11 +6,12 @@ import numpy as np
 
 import gemv_tiled_gemm_gb300 as gtg
 import oracle
-from seeded import bf16_bits_to_f32
+from seeded import bf16_bits_to_f32, f16_bits_to_f32
 from tests._util import parity_ratio
 
 CANARY = np.float32(-12345.5)
 BF16_NAN = np.uint16(0x7FC0)
+F16_NAN = np.uint16(0x7E00)
 
 
 def torch():
@@ -39,7 +40,7 @@ def run_gemm(prec: str, A: np.ndarray, B: np.ndarray, lda=None, ldb=None, ldc=No
     lda = lda or max(K, 1)
     ldb = ldb or max(N, 1)
     ldc = ldc or max(N, 1)
-    fill = BF16_NAN if prec == "bf16" else np.float32(np.nan)
+    fill = {"bf16": BF16_NAN, "f16": F16_NAN}.get(prec, np.float32(np.nan))
     dA = _dev_buffer(A, M, K, lda, a_off, fill)
     dB = _dev_buffer(B, K, N, ldb, b_off, fill)
     # C: one guard row above and below, padding columns, NaN in the interior
@@ -49,7 +50,7 @@ def run_gemm(prec: str, A: np.ndarray, B: np.ndarray, lda=None, ldb=None, ldc=No
     body[c_off + guard:c_off + guard + M * ldc].reshape(M, ldc)[:, :N] = True
     host_c[body] = np.nan
     dC = t.from_numpy(host_c).cuda()
-    esz = 2 if prec == "bf16" else 4
+    esz = 2 if prec in ("bf16", "f16") else 4
     pA = dA.data_ptr() + a_off * esz
     pB = dB.data_ptr() + b_off * esz
     pC = dC.data_ptr() + (c_off + guard) * 4
@@ -57,7 +58,7 @@ def run_gemm(prec: str, A: np.ndarray, B: np.ndarray, lda=None, ldb=None, ldc=No
         plan = gtg.plan_gemm(prec, M, N, K, pA, lda, pB, ldb, pC, ldc)
         assert plan["kernel"] == expect_kernel, plan
     s = stream if stream is not None else t.cuda.current_stream()
-    fn = {"f32": gtg.gemm_f32, "tf32": gtg.gemm_tf32, "bf16": gtg.gemm_bf16}[prec]
+    fn = {"f32": gtg.gemm_f32, "tf32": gtg.gemm_tf32, "bf16": gtg.gemm_bf16, "f16": gtg.gemm_f16}[prec]
     st = fn(M, N, K, pA, lda, pB, ldb, pC, ldc, int(s.cuda_stream))
     assert st == gtg.GTG_OK, gtg.status_string(st)
     assert gtg.gtg_sync_status(int(s.cuda_stream)) == gtg.GTG_OK
@@ -92,7 +93,9 @@ def run_gemv(A: np.ndarray, X: np.ndarray, lda=None, ldx=None, ldy=None, a_off=0
 
 
 def as_f32(prec, X):
-    return bf16_bits_to_f32(X) if prec == "bf16" else X
+    if prec == "bf16":
+        return bf16_bits_to_f32(X)
+    return f16_bits_to_f32(X) if prec == "f16" else X
 
 
 def check_gemm(prec, A, B, C, rows=None):

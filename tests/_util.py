@@ -25,7 +25,14 @@ def bound_bf16(E, K=None):
     return 4.0 * 2.0 ** -8 * np.asarray(E)
 
 
-BOUNDS = {"f32": bound_f32, "tf32": bound_tf32, "bf16": bound_bf16}
+def bound_f16(E, K=None):
+    # FP16 inputs are exact in the products (11 x 11 significant bits fit in
+    # FP32); what rounds is the FP32 accumulation, far inside 4 * 2^-11 E for
+    # every K used here (K * 2^-24 <= 2^-11 up to K = 8192)
+    return 4.0 * 2.0 ** -11 * np.asarray(E)
+
+
+BOUNDS = {"f32": bound_f32, "tf32": bound_tf32, "bf16": bound_bf16, "f16": bound_f16}
 
 
 def read_golden(name: str) -> dict[str, np.ndarray]:

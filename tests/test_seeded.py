@@ -2,8 +2,8 @@
 
 import numpy as np
 
-from seeded import (PCG32, bf16_bits_to_f32, f64_to_bf16_bits, gemm_normal_bf16,
-                    gemm_uniform_f32, gemv_uniform_f32)
+from seeded import (PCG32, bf16_bits_to_f32, f16_bits_to_f32, f64_to_bf16_bits, f64_to_f16_bits,
+                    gemm_normal_bf16, gemm_uniform_f32, gemv_uniform_f32)
 
 
 def test_pcg32_published_stream():
@@ -76,3 +76,21 @@ def test_recipes_shapes_and_stream_continuation():
     assert np.array_equal(A2, g.normal_bf16((2, 3), 3 ** -0.5))
     A, x, X = gemv_uniform_f32(2, 6, 9, batch=8)
     assert A.shape == (6, 9) and x.shape == (9,) and X.shape == (8, 9)
+
+
+def test_f16_rounding_is_nearest_even():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal(20000) * 3.0
+    base = f16_bits_to_f32(f64_to_f16_bits(rng.standard_normal(300))).astype(np.float64)
+    up = np.nextafter(base.astype(np.float16), np.float16(np.inf)).astype(np.float64)
+    x = np.concatenate([x, (base + up) / 2])            # exact midpoints: ties to even
+    got = f64_to_f16_bits(x)
+    h = x.astype(np.float32).astype(np.float16)          # a nearby candidate
+    cands = np.stack([np.nextafter(h, np.float16(-np.inf)), h, np.nextafter(h, np.float16(np.inf))])
+    d = np.abs(cands.astype(np.float64) - x[None, :])
+    best = d.min(axis=0)
+    for i in range(x.size):
+        ties = [c for c, dd in zip(cands[:, i], d[:, i]) if dd == best[i]]
+        even = [c for c in ties if (int(np.array(c).view(np.uint16)) & 1) == 0]
+        want = (even or ties)[0]
+        assert got[i] == np.array(want).view(np.uint16), (x[i], got[i])

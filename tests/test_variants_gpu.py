@@ -1,0 +1,140 @@
+"""GEMM variants: FP16 inputs, and strided batches of independent products
+(one call), against the FP64 oracle through the C ABI."""
+
+import numpy as np
+import pytest
+
+import gemv_tiled_gemm_gb300 as gtg
+import oracle
+from seeded import PCG32, bf16_bits_to_f32, f16_bits_to_f32
+from tests._gpu import check_gemm, run_gemm, sample_rows
+from tests._util import parity_ratio
+
+pytestmark = pytest.mark.gpu
+
+
+def _t():
+    import torch
+    return torch
+
+
+# ---- FP16 ------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,N,K,bm", [(4096, 4096, 256, 256), (1024, 1024, 320, 128), (130, 72, 24, 128),
+                                      (1000, 712, 208, 128)])
+def test_f16_tensor_core(M, N, K, bm):
+    g = PCG32(800 + K)
+    A, B = g.normal_f16((M, K)), g.normal_f16((K, N))
+    C = run_gemm("f16", A, B, expect_kernel="tcgen05")
+    Af, Bf = f16_bits_to_f32(A), f16_bits_to_f32(B)
+    rows = sample_rows(M, seed=3) if M > 1024 else None
+    ref, E = oracle.gemm(Af[rows] if rows is not None else Af, Bf)
+    ratio, bad = parity_ratio(C[rows] if rows is not None else C, ref, E, "f16", K)
+    assert bad == 0, ratio
+
+
+def test_f16_unaligned_falls_back_to_simt():
+    g = PCG32(810)
+    M, N, K = 97, 61, 43
+    A, B = g.normal_f16((M, K)), g.normal_f16((K, N))
+    C = run_gemm("f16", A, B, a_off=1, b_off=3, expect_kernel="simt")
+    ref, E = oracle.gemm(f16_bits_to_f32(A), f16_bits_to_f32(B))
+    ratio, bad = parity_ratio(C, ref, E, "f16", K)
+    assert bad == 0, ratio
+
+
+def test_f16_small_integers_exact():
+    rng = np.random.default_rng(811)
+    Ai = rng.integers(-8, 9, (256, 512))
+    Bi = rng.integers(-8, 9, (512, 320))
+    from seeded import f64_to_f16_bits
+    C = run_gemm("f16", f64_to_f16_bits(Ai.astype(np.float64)), f64_to_f16_bits(Bi.astype(np.float64)))
+    assert np.array_equal(C, (Ai @ Bi).astype(np.float32))
+
+
+# ---- strided batches ---------------------------------------------------------
+
+def _draw(prec, g, shape):
+    if prec == "bf16":
+        bits = g.normal_bf16(shape)
+        return bits, bf16_bits_to_f32(bits)
+    if prec == "f16":
+        bits = g.normal_f16(shape)
+        return bits, f16_bits_to_f32(bits)
+    v = g.uniform_f32(shape)
+    return v, v
+
+
+def _dev(prec, host):
+    torch = _t()
+    if prec in ("bf16", "f16"):
+        return torch.from_numpy(np.ascontiguousarray(host).view(np.int16)).cuda()
+    return torch.from_numpy(np.ascontiguousarray(host)).cuda()
+
+
+@pytest.mark.parametrize("prec", ["bf16", "f16", "tf32", "f32"])
+@pytest.mark.parametrize("case", ["packed", "shared_B", "padded", "unaligned"])
+def test_strided_batched(prec, case):
+    torch = _t()
+    g = PCG32(900 + len(case))
+    batch, M, N, K = 3, 300, 264, 136
+    lda, ldb, ldc = K, N, N
+    sA, sB, sC = M * lda, K * ldb, M * ldc
+    if case == "shared_B":
+        sB = 0
+    if case == "padded":
+        sA, sB, sC = sA + 64, sB + 128, sC + 40
+    if case == "unaligned":            # strides that are not multiples of 16 bytes
+        sA, sB = sA + 1, (sB + 3 if sB else 0)
+    A_host, A_f = _draw(prec, g, (batch * sA + 8,))
+    B_host, B_f = _draw(prec, g, (max(1, batch * sB) + K * ldb + 8,))
+    dA, dB = _dev(prec, A_host), _dev(prec, B_host)
+    dC = torch.full((batch * sC + 8,), float("nan"), device="cuda")
+    bias = g.uniform_f32((N,))
+    db = torch.from_numpy(bias).cuda()
+    s = int(torch.cuda.current_stream().cuda_stream)
+    st = gtg.gemm_strided_batched(prec, M, N, K, dA.data_ptr(), lda, sA, dB.data_ptr(), ldb, sB,
+                                  dC.data_ptr(), ldc, sC, batch, gtg.epilogue(db.data_ptr(), "relu"), s)
+    assert st == gtg.GTG_OK, gtg.status_string(st)
+    assert gtg.gtg_sync_status(s) == gtg.GTG_OK
+    C = dC.cpu().numpy()
+    for b in range(batch):
+        Ab = A_f[b * sA: b * sA + M * lda].reshape(M, lda)[:, :K]
+        Bb = B_f[b * sB: b * sB + K * ldb].reshape(K, ldb)[:, :N]
+        ref, E = oracle.dense_layer(Ab, Bb, bias, "relu")
+        got = C[b * sC: b * sC + M * ldc].reshape(M, ldc)[:, :N]
+        ratio, bad = parity_ratio(got, ref, E + np.abs(ref), prec if prec != "f32" else "f32", K)
+        assert bad == 0, (b, ratio)
+    # nothing written between the items (the padding keeps its NaN)
+    if case == "padded":
+        for b in range(batch - 1):
+            assert np.all(np.isnan(C[b * sC + M * ldc: (b + 1) * sC]))
+
+
+def test_strided_batched_plans_one_launch_for_all_items():
+    torch = _t()
+    batch, M, N, K = 40, 512, 512, 64
+    g = PCG32(950)
+    A = g.normal_bf16((batch, M, K))
+    B = g.normal_bf16((batch, K, N))
+    dA, dB = _dev("bf16", A), _dev("bf16", B)
+    dC = torch.empty((batch, M, N), device="cuda")
+    s = int(torch.cuda.current_stream().cuda_stream)
+    assert gtg.gemm_strided_batched("bf16", M, N, K, dA.data_ptr(), K, M * K, dB.data_ptr(), N, K * N,
+                                    dC.data_ptr(), N, M * N, batch, None, s) == gtg.GTG_OK
+    C = dC.cpu().numpy()
+    for b in (0, 17, batch - 1):
+        ref, E = oracle.gemm(bf16_bits_to_f32(A[b]), bf16_bits_to_f32(B[b]))
+        ratio, bad = parity_ratio(C[b], ref, E, "bf16", K)
+        assert bad == 0, (b, ratio)
+
+
+def test_strided_batched_validation():
+    A, B, C = 1 << 32, 2 << 32, 3 << 32
+    f = gtg.gemm_strided_batched
+    assert f("bf16", 4, 4, 4, A, 4, 16, B, 4, 16, C, 4, 10, 2) == gtg.GTG_ERR_INVALID_VALUE   # outputs overlap
+    assert f("bf16", 4, 4, 4, A, 4, -16, B, 4, 16, C, 4, 16, 2) == gtg.GTG_ERR_INVALID_VALUE
+    assert f("bf16", 4, 4, 4, A, 4, 16, B, 4, 16, C, 4, 16, -1) == gtg.GTG_ERR_INVALID_VALUE
+    assert f(7, 4, 4, 4, A, 4, 16, B, 4, 16, C, 4, 16, 2) == gtg.GTG_ERR_INVALID_VALUE
+    assert f("f32", 4, 4, 4, A, 4, 16, B, 4, 16, A + 64, 4, 16, 2) == gtg.GTG_ERR_ALIAS          # C reaches A's items
+    assert f("f32", 4, 4, 4, A, 4, 16, B, 4, 16, C, 4, 16, 0) == gtg.GTG_OK
