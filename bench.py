@@ -481,6 +481,24 @@ def sweep(dev, stream, peaks, l2):
                         "batch": batch, "ms": round(ms, 5), "GB/s": round(gbs, 1), "peak": hbm,
                         "frac": round(gbs / hbm, 4), "buffer_sets": nrot})
         del As, X, Y
+        # the same layer with its weights stored in BF16 (half the bytes)
+        from seeded import f64_to_bf16_bits
+        Ab = f64_to_bf16_bits(Av.astype(np.float64)).view(np.int16)
+        nrot = max(2, math.ceil(3 * l2 / (2 * n * n))) if l2 else 2
+        As = [torch.from_numpy(Ab).to(dev) for _ in range(nrot)]
+        X = torch.from_numpy(Xv).to(dev)
+        Y = torch.empty((8, n), device=dev)
+        for batch in (1, 8):
+            def call(i, batch=batch):
+                st = gtg.gemv_bf16(n, n, As[i % nrot].data_ptr(), n, X.data_ptr(), n, Y.data_ptr(), n, batch, sh)
+                assert st == gtg.GTG_OK, st
+            ms = time_launches(call, 100, stream)
+            byt = 2.0 * n * n + batch * 4.0 * (2 * n)
+            gbs = byt / (ms * 1e-3) / 1e9
+            out.append({"config": f"f2: bf16-matrix gemv {n}x{n} batch {batch}", "path": "gemv_bf16",
+                        "shape": [n, n], "batch": batch, "ms": round(ms, 5), "GB/s": round(gbs, 1), "peak": hbm,
+                        "frac": round(gbs / hbm, 4), "buffer_sets": nrot})
+        del As, X, Y
     torch.cuda.empty_cache()
     return out
 

@@ -64,6 +64,8 @@ SIGNATURES = {
     "gemm_strided_batched": (_int, [_int, _i64, _i64, _i64, _ptr, _i64, _i64, _ptr, _i64, _i64, _ptr, _i64, _i64,
                                     _i64, _ep, _ptr]),
     "gemv_f32_ex": (_int, [_i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _int, _ep, _ptr]),
+    "gemv_bf16": (_int, [_i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _int, _ptr]),
+    "gemv_bf16_ex": (_int, [_i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _int, _ep, _ptr]),
     "gtg_ablation_gemm_f32": (_int, [_int, _i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr]),
     "gtg_ablation_gemv_f32": (_int, [_int, _i64, _i64, _ptr, _i64, _ptr, _ptr, _ptr]),
     "gtg_status_string": (ctypes.c_char_p, [_int]),
@@ -167,6 +169,14 @@ def gemm_bf16_ex(M, N, K, A, lda, B, ldb, C, ldc, ep=None, stream=0) -> int:
 
 def gemv_f32_ex(M, N, A, lda, x, ldx, y, ldy, batch, ep=None, stream=0) -> int:
     return lib().gemv_f32_ex(M, N, A, lda, x, ldx, y, ldy, batch, ctypes.byref(ep) if ep else None, stream)
+
+
+def gemv_bf16(M, N, A, lda, x, ldx, y, ldy, batch, stream=0) -> int:
+    return lib().gemv_bf16(M, N, A, lda, x, ldx, y, ldy, batch, stream)
+
+
+def gemv_bf16_ex(M, N, A, lda, x, ldx, y, ldy, batch, ep=None, stream=0) -> int:
+    return lib().gemv_bf16_ex(M, N, A, lda, x, ldx, y, ldy, batch, ctypes.byref(ep) if ep else None, stream)
 
 
 ABLATION_GEMM = {"naive16": 0, "naive32": 1, "tiled16": 2, "tiled32": 3}
@@ -312,13 +322,14 @@ def matvec(A, x, out=None, stream=None, bias=None, activation="none"):
     """y = act(A @ x + bias) (x of shape (N,)), or Y = act(X @ A^T + bias)
     per row of X (shape (batch, N)): a fully connected layer with weight A.
 
-    FP32 only, batch <= 8, through gemv_f32_ex; `bias` holds M float32 values
-    (one per output). Host tensors are copied in and the result copied back,
-    as in `matmul`.
+    A in float32 (gemv_f32_ex) or bfloat16 (gemv_bf16_ex); x, the bias and the
+    result in float32; batch <= 8; `bias` holds M values (one per output).
+    Host tensors are copied in and the result copied back, as in `matmul`.
     """
     torch = _torch()
-    if A.dtype != torch.float32 or x.dtype != torch.float32:
-        raise TypeError("gemv_f32 takes float32 tensors")
+    if A.dtype not in (torch.float32, torch.bfloat16) or x.dtype != torch.float32:
+        raise TypeError("matvec takes a float32 or bfloat16 matrix and a float32 vector")
+    fn, name = (gemv_bf16_ex, "gemv_bf16") if A.dtype == torch.bfloat16 else (gemv_f32_ex, "gemv_f32")
     single = x.dim() == 1
     X = x.unsqueeze(0) if single else x
     if A.dim() != 2 or X.dim() != 2 or X.shape[1] != A.shape[1]:
@@ -334,9 +345,9 @@ def matvec(A, x, out=None, stream=None, bias=None, activation="none"):
         Y = torch.empty((batch, M), dtype=torch.float32, device=dA.device)
     dbias = _device_bias(bias, M, dA.device)
     ep = epilogue(dbias.data_ptr() if dbias is not None else 0, activation)
-    st = gemv_f32_ex(M, N, dA.data_ptr(), _rowmajor_ld(dA, "A"), dX.data_ptr(), _rowmajor_ld(dX, "x"),
-                     Y.data_ptr(), _rowmajor_ld(Y, "y"), batch, ep, _stream_handle(stream))
-    _check(st, "gemv_f32")
+    st = fn(M, N, dA.data_ptr(), _rowmajor_ld(dA, "A"), dX.data_ptr(), _rowmajor_ld(dX, "x"),
+            Y.data_ptr(), _rowmajor_ld(Y, "y"), batch, ep, _stream_handle(stream))
+    _check(st, name)
     if host:
         res = torch.empty((batch, M), dtype=torch.float32, pin_memory=A.is_pinned())
         res.copy_(Y, non_blocking=True)

@@ -125,12 +125,13 @@ cudaError_t ablation_gemm_launch(int variant, const GemmArgs &g, cudaStream_t st
 cudaError_t ablation_gemv_launch(int variant, const GemvArgs &g, cudaStream_t stream) {
     const unsigned blocks = static_cast<unsigned>((g.M + kVecThreads - 1) / kVecThreads);
     const int M = static_cast<int>(g.M), N = static_cast<int>(g.N);
+    const auto *A = static_cast<const float *>(g.A);
     switch (variant) {
         case GTG_ABL_GEMV_NAIVE:
-            gemv_naive_kernel<<<blocks, kVecThreads, 0, stream>>>(M, N, g.A, g.lda, g.x, g.y);
+            gemv_naive_kernel<<<blocks, kVecThreads, 0, stream>>>(M, N, A, g.lda, g.x, g.y);
             break;
         case GTG_ABL_GEMV_SHARED:
-            gemv_shared_kernel<<<blocks, kVecThreads, 0, stream>>>(M, N, g.A, g.lda, g.x, g.y);
+            gemv_shared_kernel<<<blocks, kVecThreads, 0, stream>>>(M, N, A, g.lda, g.x, g.y);
             break;
         default:
             return cudaErrorInvalidValue;

@@ -137,12 +137,12 @@ gtg_status validate_gemv(const GemvArgs &g) {
     if (g.M == 0) return GTG_OK;
     if (g.y == nullptr) return GTG_ERR_INVALID_VALUE;
     if (g.N > 0 && (g.A == nullptr || g.x == nullptr)) return GTG_ERR_INVALID_VALUE;
-    if ((reinterpret_cast<uintptr_t>(g.A) % 4) || (reinterpret_cast<uintptr_t>(g.x) % 4) ||
+    if ((reinterpret_cast<uintptr_t>(g.A) % g.a_elem) || (reinterpret_cast<uintptr_t>(g.x) % 4) ||
         (reinterpret_cast<uintptr_t>(g.y) % 4))
         return GTG_ERR_MISALIGNED;
     const int64_t ldx = g.batch > 1 ? g.ldx : g.N, ldy = g.batch > 1 ? g.ldy : g.M;
     const Span y = span_of(g.y, g.batch, g.M, ldy, 4);
-    if (g.N > 0 && (overlaps(y, span_of(g.A, g.M, g.N, g.lda, 4)) ||
+    if (g.N > 0 && (overlaps(y, span_of(g.A, g.M, g.N, g.lda, g.a_elem)) ||
                     overlaps(y, span_of(g.x, g.batch, g.N, ldx, 4))))
         return GTG_ERR_ALIAS;
     if (g.act != GTG_ACT_NONE && g.act != GTG_ACT_RELU) return GTG_ERR_INVALID_VALUE;
@@ -284,6 +284,24 @@ gtg_status gemv_f32(int64_t M, int64_t N, const float *A, int64_t lda, const flo
 gtg_status gemv_f32_ex(int64_t M, int64_t N, const float *A, int64_t lda, const float *x, int64_t ldx,
                        float *y, int64_t ldy, int batch, const gtg_epilogue *ep, cudaStream_t stream) {
     GemvArgs g{M, N, A, lda, x, batch > 1 ? ldx : N, y, batch > 1 ? ldy : M, batch};
+    if (ep) {
+        g.bias = ep->bias;
+        g.act = ep->activation;
+    }
+    return run_gemv(g, stream);
+}
+
+gtg_status gemv_bf16(int64_t M, int64_t N, const gtg_bf16 *A, int64_t lda, const float *x, int64_t ldx,
+                     float *y, int64_t ldy, int batch, cudaStream_t stream) {
+    GemvArgs g{M, N, A, lda, x, batch > 1 ? ldx : N, y, batch > 1 ? ldy : M, batch};
+    g.a_elem = 2;
+    return run_gemv(g, stream);
+}
+
+gtg_status gemv_bf16_ex(int64_t M, int64_t N, const gtg_bf16 *A, int64_t lda, const float *x, int64_t ldx,
+                        float *y, int64_t ldy, int batch, const gtg_epilogue *ep, cudaStream_t stream) {
+    GemvArgs g{M, N, A, lda, x, batch > 1 ? ldx : N, y, batch > 1 ? ldy : M, batch};
+    g.a_elem = 2;
     if (ep) {
         g.bias = ep->bias;
         g.act = ep->activation;

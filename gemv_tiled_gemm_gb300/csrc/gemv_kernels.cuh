@@ -1,0 +1,606 @@
+// Bandwidth-bound GEMV kernels: y_b = A * x_b for up to 8 vectors at once,
+// with A in FP32 or BF16 and x, y and all arithmetic in FP32.
+//
+// "Matrix Operations" (section "Matrix-Vector Multiplication") computes
+// y[i] = sum_j A[i][j] x[j] with one thread per row and, in its optimised
+// form, the vector staged in shared memory once per work group so that it
+// is not re-read from global memory for every row; vectors too large for
+// shared memory are staged in chunks with a barrier on each side
+// ("Handling Large Vectors"). The matrix, read exactly once, is the traffic
+// that sets the speed.
+//
+// GB300 form:
+//   * a warp (not a thread) owns ROWS rows at a time and streams them with
+//     coalesced 128-bit loads that bypass L1 (each lane keeps U x ROWS loads
+//     in flight), so a row is one contiguous burst instead of the pages'
+//     one-row-per-thread pattern whose neighbouring threads are a full row
+//     apart;
+//   * every CTA stages x (all `batch` vectors) in shared memory once; if they
+//     do not fit, chunk by chunk with the barriers of the pages' chunked
+//     loop, which every thread of the CTA reaches (no early return);
+//   * partial sums are combined with a warp-shuffle butterfly;
+//   * the grid is persistent (a multiple of the SM count) and each CTA owns
+//     one contiguous, equally sized range of rows, so every SM streams the
+//     same number of bytes;
+//   * each matrix element loaded is used for all `batch` vectors;
+//   * a 16-byte load carries 4 FP32 or 8 BF16 matrix elements; BF16 values are
+//     widened to FP32 in registers (exactly), so a BF16 matrix halves the
+//     bytes that bound the kernel and changes nothing else.
+//
+// Included by gemv.cu (FP32 matrices, and the planner) and gemv_bf16.cu
+// (BF16 matrices), so that the two sets of instantiations compile in
+// parallel.
+#pragma once
+
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gtg {
+namespace gemv {
+
+constexpr int kSmemBudget = 200 * 1024;   // per CTA, for the staged vectors
+
+struct Params {
+    const void *A;       // M x N, row-major with leading dimension lda (elements)
+    long long lda;
+    const float *x;
+    long long ldx;
+    float *y;
+    long long ldy;
+    int M, N;
+    int chunk;           // vector entries staged per pass (multiple of 8)
+    int nchunks;
+    const float *bias;   // epilogue: y = act(acc + bias[row]); null for none
+    int act;
+    int x_bulk;          // x rows 16-byte aligned, ldx and N multiples of 4: stage x by bulk copies
+    int *status;         // the library's device status word (set on a timed-out wait)
+};
+
+// Matrix element types. kVec = elements per 16-byte load; widen() turns one
+// such load into FP32 values in column order; one() reads a single element.
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<float> {
+    static constexpr int kVec = 4;
+    static __device__ __forceinline__ void widen(const float4 &raw, float (&a)[4]) {
+        a[0] = raw.x;
+        a[1] = raw.y;
+        a[2] = raw.z;
+        a[3] = raw.w;
+    }
+    static __device__ __forceinline__ float one(const float *p) { return ptx::ld_stream_f1(p); }
+};
+
+// BF16 as its 16-bit pattern: two elements per 32-bit word, the lower-addressed
+// one in the low half. A BF16 value is the upper half of the FP32 value with
+// the same bits, so widening is a shift (or a mask) and exact.
+template <>
+struct Elem<uint16_t> {
+    static constexpr int kVec = 8;
+    static __device__ __forceinline__ float lo(uint32_t w) { return __uint_as_float(w << 16); }
+    static __device__ __forceinline__ float hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+    static __device__ __forceinline__ void widen(const float4 &raw, float (&a)[8]) {
+        const uint32_t w[4] = {__float_as_uint(raw.x), __float_as_uint(raw.y), __float_as_uint(raw.z),
+                               __float_as_uint(raw.w)};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            a[2 * q] = lo(w[q]);
+            a[2 * q + 1] = hi(w[q]);
+        }
+    }
+    static __device__ __forceinline__ float one(const uint16_t *p) {
+        return __uint_as_float(static_cast<uint32_t>(ptx::ld_stream_u16(p)) << 16);
+    }
+};
+
+template <typename T>
+__device__ __forceinline__ float4 ld16(const T *p) {
+    return ptx::ld_stream_f4(reinterpret_cast<const float *>(p));
+}
+
+template <int BATCH, int kThreads>
+__device__ __forceinline__ void stage_x(float *xs, const Params &p, int c0, int len) {
+#pragma unroll
+    for (int b = 0; b < BATCH; ++b) {
+        const float *src = p.x + static_cast<long long>(b) * p.ldx + c0;
+        float *dst = xs + b * p.chunk;
+        for (int j = threadIdx.x; j < len; j += kThreads) dst[j] = __ldg(src + j);
+    }
+}
+
+// Staging of all BATCH vectors by bulk copies (one per vector, issued by one
+// thread, completing on one mbarrier): no registers or load instructions are
+// spent on x, and the warps issue their first matrix loads while it arrives.
+// The barrier must have been initialised (count 1) and made visible.
+template <int BATCH>
+__device__ __forceinline__ void stage_x_bulk(float *xs, const Params &p, uint32_t bar) {
+    if (threadIdx.x == 0) {
+        ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(BATCH * p.N * 4));
+#pragma unroll
+        for (int b = 0; b < BATCH; ++b)
+            ptx::bulk_load(ptx::smem_addr(xs + b * p.chunk), p.x + static_cast<long long>(b) * p.ldx,
+                           static_cast<uint32_t>(p.N * 4), bar);
+    }
+}
+
+// Waits (bounded) for the bulk-staged vectors. On time-out the status word
+// records GTG_ERR_TIMEOUT, the copies are given one more bounded wait so that
+// none is left writing into shared memory, and false is returned; the caller
+// then skips its arithmetic but still reaches every later barrier of the CTA.
+__device__ __forceinline__ bool wait_x(uint32_t bar, int *status) {
+    if (ptx::mbar_try_wait(bar, 0)) return true;
+    uint64_t t0 = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait(bar, 0)) {
+        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicCAS(status, 0, GTG_ERR_TIMEOUT);
+            t0 = ptx::globaltimer_ns();
+            while (!ptx::mbar_try_wait(bar, 0) && ptx::globaltimer_ns() - t0 < kWaitLimitNs) {
+            }
+            return false;
+        }
+    }
+    return true;
+}
+
+// acc[r][b] += sum over one 16-byte unit of row r (starting at column `col`
+// of the staged chunk) times vector b. The x values are read from shared
+// memory once per vector and serve all ROWS rows.
+template <typename T, int ROWS, int BATCH>
+__device__ __forceinline__ void fma_unit(float (&acc)[ROWS][BATCH], const float4 (&raw)[ROWS], const float *xs,
+                                         int chunk, int col) {
+    constexpr int VE = Elem<T>::kVec;
+    float a[ROWS][VE];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) Elem<T>::widen(raw[r], a[r]);
+#pragma unroll
+    for (int b = 0; b < BATCH; ++b) {
+        float xv[VE];
+        const float4 *xp = reinterpret_cast<const float4 *>(xs + b * chunk + col);
+#pragma unroll
+        for (int q = 0; q < VE / 4; ++q) {
+            const float4 v = xp[q];
+            xv[4 * q] = v.x;
+            xv[4 * q + 1] = v.y;
+            xv[4 * q + 2] = v.z;
+            xv[4 * q + 3] = v.w;
+        }
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            float s = acc[r][b];
+#pragma unroll
+            for (int e = 0; e < VE; ++e) s = fmaf(a[r][e], xv[e], s);
+            acc[r][b] = s;
+        }
+    }
+}
+
+template <typename T, int BATCH, int ROWS, int U, bool VEC>
+__device__ __forceinline__ void accumulate(float (&acc)[ROWS][BATCH], const T *const (&arow)[ROWS],
+                                           const float *xs, int chunk, int c0, int len, int lane) {
+    if constexpr (VEC) {
+        constexpr int VE = Elem<T>::kVec;
+        const int nu = len / VE;
+        int j = lane;
+        for (; j + 32 * (U - 1) < nu; j += 32 * U) {
+            float4 a[U][ROWS];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) a[u][r] = ld16(arow[r] + c0 + VE * (j + 32 * u));
+#pragma unroll
+            for (int u = 0; u < U; ++u) fma_unit<T, ROWS, BATCH>(acc, a[u], xs, chunk, VE * (j + 32 * u));
+        }
+        for (; j < nu; j += 32) {
+            float4 a[ROWS];
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) a[r] = ld16(arow[r] + c0 + VE * j);
+            fma_unit<T, ROWS, BATCH>(acc, a, xs, chunk, VE * j);
+        }
+        const int jt = VE * nu + lane;   // fewer than VE trailing entries
+        if (jt < len) {
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) {
+                const float a = Elem<T>::one(arow[r] + c0 + jt);
+#pragma unroll
+                for (int b = 0; b < BATCH; ++b) acc[r][b] = fmaf(a, xs[b * chunk + jt], acc[r][b]);
+            }
+        }
+    } else {
+        int j = lane;
+        for (; j + 32 * (U - 1) < len; j += 32 * U) {
+            float a[U][ROWS];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) a[u][r] = Elem<T>::one(arow[r] + c0 + j + 32 * u);
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int b = 0; b < BATCH; ++b) {
+                    const float xv = xs[b * chunk + j + 32 * u];
+#pragma unroll
+                    for (int r = 0; r < ROWS; ++r) acc[r][b] = fmaf(a[u][r], xv, acc[r][b]);
+                }
+        }
+        for (; j < len; j += 32) {
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) {
+                const float a = Elem<T>::one(arow[r] + c0 + j);
+#pragma unroll
+                for (int b = 0; b < BATCH; ++b) acc[r][b] = fmaf(a, xs[b * chunk + j], acc[r][b]);
+            }
+        }
+    }
+}
+
+// The general kernel: any row alignment, x chunked when it does not fit.
+template <typename T, int BATCH, int ROWS, int U, bool VEC, int kThreads>
+__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Params p) {
+    constexpr int kWarps = kThreads / 32;
+    extern __shared__ float4 xs_raw[];
+    float *xs = reinterpret_cast<float *>(xs_raw);
+    const T *A = static_cast<const T *>(p.A);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // this CTA's rows: [r_begin, r_end), equal shares of M
+    const int r_begin = static_cast<int>(static_cast<long long>(p.M) * blockIdx.x / gridDim.x);
+    const int r_end = static_cast<int>(static_cast<long long>(p.M) * (blockIdx.x + 1) / gridDim.x);
+    const int ntasks = (r_end - r_begin + ROWS - 1) / ROWS;
+    const int rounds = (ntasks + kWarps - 1) / kWarps;
+
+    ptx::wait_prior_grid();
+    ptx::allow_next_grid();
+    if (p.nchunks == 1) {
+        stage_x<BATCH, kThreads>(xs, p, 0, p.N);
+        __syncthreads();
+    }
+    for (int round = 0; round < rounds; ++round) {  // same trip count for every warp
+        const int task = round * kWarps + warp;
+        const bool active = task < ntasks;
+        const int row0 = r_begin + task * ROWS;
+        const T *arow[ROWS];
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r)  // rows past the range re-read the last one; never stored
+            arow[r] = A + static_cast<long long>(min(row0 + r, r_end - 1)) * p.lda;
+
+        float acc[ROWS][BATCH];
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) acc[r][b] = 0.f;
+
+        for (int c = 0; c < p.nchunks; ++c) {
+            const int c0 = c * p.chunk;
+            const int len = min(p.chunk, p.N - c0);
+            if (p.nchunks > 1) {
+                __syncthreads();              // everyone is done with the previous chunk
+                stage_x<BATCH, kThreads>(xs, p, c0, len);
+                __syncthreads();              // the chunk is in place
+            }
+            if (active) accumulate<T, BATCH, ROWS, U, VEC>(acc, arow, xs, p.chunk, c0, len, lane);
+        }
+        if (active) {
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+                for (int b = 0; b < BATCH; ++b) {
+                    float s = acc[r][b];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+                    acc[r][b] = s;
+                }
+            // every lane now holds every total; lane (r * BATCH + b) stores one
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+                for (int b = 0; b < BATCH; ++b)
+                    if (lane == (r * BATCH + b) % 32 && row0 + r < r_end)
+                        p.y[static_cast<long long>(b) * p.ldy + row0 + r] =
+                            apply_epilogue(acc[r][b], p.bias, row0 + r, p.act);
+        }
+    }
+}
+
+// The main case for one or two vectors: 16-byte aligned rows and all of x in
+// one staging chunk. A warp's work is a flat sequence of iterations (ROWS rows
+// x 32*U sixteen-byte columns each); the loads of iteration it+1 are issued
+// before the FMAs of iteration it, and the first loads before x is staged, so
+// the matrix stream starts at once and never drains between iterations. While
+// the previous kernel in the stream is still finishing, the first 4 KB of
+// each of the CTA's rows is already requested into L2 (a prefetch cannot
+// observe stale data: L2 is the point of coherence).
+template <typename T, int BATCH, int ROWS, int U, int kThreads>
+__global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const Params p) {
+    constexpr int kWarps = kThreads / 32;
+    constexpr int VE = Elem<T>::kVec;
+    extern __shared__ float4 xs_raw[];
+    float *xs = reinterpret_cast<float *>(xs_raw);
+    const T *A = static_cast<const T *>(p.A);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r_begin = static_cast<int>(static_cast<long long>(p.M) * blockIdx.x / gridDim.x);
+    const int r_end = static_cast<int>(static_cast<long long>(p.M) * (blockIdx.x + 1) / gridDim.x);
+    const int ntasks = (r_end - r_begin + ROWS - 1) / ROWS;
+    const int my_tasks = ntasks > warp ? (ntasks - warp + kWarps - 1) / kWarps : 0;
+    const int nu = p.N / VE;                          // whole 16-byte units per row
+    const int ipr = (nu + 32 * U - 1) / (32 * U);     // iterations per task
+    const int total = my_tasks * ipr;
+
+    if (threadIdx.x < 32) {
+        const uint32_t bytes = min(4096u, static_cast<uint32_t>(nu) * 16u);
+        for (int r = r_begin + static_cast<int>(threadIdx.x); bytes > 0 && r < r_end; r += 32)
+            ptx::prefetch_l2(A + static_cast<long long>(r) * p.lda, bytes);
+    }
+    ptx::wait_prior_grid();
+    ptx::allow_next_grid();
+
+    auto row_of = [&](int t, int r) { return r_begin + (warp + t * kWarps) * ROWS + r; };
+    auto load = [&](int it, float4 (&dst)[U][ROWS]) {
+        const int t = it / ipr, blk = it - t * ipr;
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            const T *a = A + static_cast<long long>(min(row_of(t, r), r_end - 1)) * p.lda;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = blk * 32 * U + 32 * u + lane;
+                dst[u][r] = j < nu ? ld16(a + VE * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+    };
+
+    __shared__ __align__(8) unsigned long long xbar;
+    const uint32_t bar = ptx::smem_addr(&xbar);
+    if (p.x_bulk) {
+        if (threadIdx.x == 0) {
+            ptx::mbar_init(bar, 1);
+            ptx::fence_barrier_init();
+        }
+        __syncthreads();
+        stage_x_bulk<BATCH>(xs, p, bar);
+    }
+    float4 nxt[U][ROWS];
+    if (total > 0) load(0, nxt);
+    bool ok = true;
+    if (p.x_bulk) {
+        ok = __all_sync(0xFFFFFFFFu, wait_x(bar, p.status));   // warp-uniform: shuffles follow
+    } else {
+        stage_x<BATCH, kThreads>(xs, p, 0, p.N);
+        __syncthreads();
+    }
+    if (!ok) return;   // no barrier follows in this kernel
+
+    float acc[ROWS][BATCH];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+        for (int b = 0; b < BATCH; ++b) acc[r][b] = 0.f;
+
+    for (int it = 0; it < total; ++it) {
+        float4 cur[U][ROWS];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) cur[u][r] = nxt[u][r];
+        if (it + 1 < total) load(it + 1, nxt);
+        const int t = it / ipr, blk = it - t * ipr;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = blk * 32 * U + 32 * u + lane;
+            if (j < nu) fma_unit<T, ROWS, BATCH>(acc, cur[u], xs, p.chunk, VE * j);
+        }
+        if (blk == ipr - 1) {
+            // fewer than VE trailing entries when N is not a multiple of VE
+            const int jt = VE * nu + lane;
+            if (jt < p.N) {
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) {
+                    const float a = Elem<T>::one(A + static_cast<long long>(min(row_of(t, r), r_end - 1)) * p.lda + jt);
+#pragma unroll
+                    for (int b = 0; b < BATCH; ++b) acc[r][b] = fmaf(a, xs[b * p.chunk + jt], acc[r][b]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+                for (int b = 0; b < BATCH; ++b) {
+                    float s = acc[r][b];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+                    acc[r][b] = s;
+                }
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+                for (int b = 0; b < BATCH; ++b) {
+                    const int row = row_of(t, r);
+                    if (lane == (r * BATCH + b) % 32 && row < r_end)
+                        p.y[static_cast<long long>(b) * p.ldy + row] = apply_epilogue(acc[r][b], p.bias, row, p.act);
+                    acc[r][b] = 0.f;
+                }
+        }
+    }
+}
+
+// Three or more vectors: a warp's task is ROWS rows x one of WC column
+// segments, so every x value read from shared memory serves ROWS rows (the
+// x reads, not the matrix, are the per-element cost at batch 8) while the
+// few rows per SM still give every warp work. Each task's per-row partial
+// sums go to shared memory and are added in segment order after a barrier,
+// so the result does not depend on scheduling.
+template <typename T, int BATCH, int ROWS, int WC, int U, int kThreads>
+__global__ void __launch_bounds__(kThreads, 1) gemv_split_kernel(const Params p) {
+    constexpr int kWarps = kThreads / 32;
+    constexpr int VE = Elem<T>::kVec;
+    extern __shared__ float4 xs_raw[];
+    __shared__ __align__(8) unsigned long long xbar;
+    float *xs = reinterpret_cast<float *>(xs_raw);
+    float *part = xs + BATCH * p.chunk;   // [group][segment][row][batch]
+    const T *A = static_cast<const T *>(p.A);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r_begin = static_cast<int>(static_cast<long long>(p.M) * blockIdx.x / gridDim.x);
+    const int r_end = static_cast<int>(static_cast<long long>(p.M) * (blockIdx.x + 1) / gridDim.x);
+    const int rows = r_end - r_begin;
+    const int ngroups = (rows + ROWS - 1) / ROWS;
+    const int ntasks = ngroups * WC;
+    const int nu = p.N / VE;
+    const int segu = ((nu + WC - 1) / WC + 31) / 32 * 32;   // 16-byte units per segment
+    const uint32_t bar = ptx::smem_addr(&xbar);
+
+    if (p.x_bulk && threadIdx.x == 0) {
+        ptx::mbar_init(bar, 1);
+        ptx::fence_barrier_init();
+    }
+    if (threadIdx.x < 32) {
+        const uint32_t bytes = min(4096u, static_cast<uint32_t>(nu) * 16u);
+        for (int r = r_begin + static_cast<int>(threadIdx.x); bytes > 0 && r < r_end; r += 32)
+            ptx::prefetch_l2(A + static_cast<long long>(r) * p.lda, bytes);
+    }
+    ptx::wait_prior_grid();
+    ptx::allow_next_grid();
+    if (p.x_bulk) {
+        __syncthreads();   // the barrier is initialised
+        stage_x_bulk<BATCH>(xs, p, bar);
+    }
+
+    // the current task: its rows and its segment [j0, j1) of 16-byte units
+    const T *arow[ROWS];
+    int j0 = 0, j1 = 0;
+    auto setup = [&](int task) {
+        const int rg = task / WC, cs = task - rg * WC;
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r)
+            arow[r] = A + static_cast<long long>(min(r_begin + rg * ROWS + r, r_end - 1)) * p.lda;
+        j0 = cs * segu;
+        j1 = min(j0 + segu, nu);
+    };
+    auto load = [&](int jb, float4 (&dst)[U][ROWS]) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = jb + 32 * u + lane;
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r)
+                dst[u][r] = j < j1 ? ld16(arow[r] + VE * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+
+    // the first task's first loads go out before x has arrived
+    float4 nxt[U][ROWS];
+    if (warp < ntasks) {
+        setup(warp);
+        if (j0 < j1) load(j0, nxt);
+    }
+    bool ok = true;
+    if (p.x_bulk) {
+        ok = __all_sync(0xFFFFFFFFu, wait_x(bar, p.status));   // warp-uniform: shuffles follow
+    } else {
+        stage_x<BATCH, kThreads>(xs, p, 0, p.N);
+        __syncthreads();
+    }
+
+    for (int task = warp; ok && task < ntasks; task += kWarps) {
+        if (task != warp) {
+            setup(task);
+            if (j0 < j1) load(j0, nxt);
+        }
+        const int cs = task % WC;
+        float acc[ROWS][BATCH];
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) acc[r][b] = 0.f;
+        for (int jb = j0; jb < j1; jb += 32 * U) {
+            float4 cur[U][ROWS];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) cur[u][r] = nxt[u][r];
+            if (jb + 32 * U < j1) load(jb + 32 * U, nxt);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = jb + 32 * u + lane;
+                if (j < j1) fma_unit<T, ROWS, BATCH>(acc, cur[u], xs, p.chunk, VE * j);
+            }
+        }
+        if (cs == WC - 1) {
+            const int jt = VE * nu + lane;   // fewer than VE trailing entries
+            if (jt < p.N) {
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) {
+                    const float a = Elem<T>::one(arow[r] + jt);
+#pragma unroll
+                    for (int b = 0; b < BATCH; ++b) acc[r][b] = fmaf(a, xs[b * p.chunk + jt], acc[r][b]);
+                }
+            }
+        }
+        float *dst = part + static_cast<long long>(task) * ROWS * BATCH;
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) {
+                float v = acc[r][b];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+                if (lane == (r * BATCH + b) % 32) dst[r * BATCH + b] = v;
+            }
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < rows * BATCH; idx += kThreads) {
+        const int rl = idx / BATCH, b = idx - rl * BATCH;
+        const int rg = rl / ROWS, r = rl - rg * ROWS;
+        float v = 0.f;
+#pragma unroll
+        for (int cs = 0; cs < WC; ++cs) v += part[((rg * WC + cs) * ROWS + r) * BATCH + b];
+        p.y[static_cast<long long>(b) * p.ldy + r_begin + rl] = apply_epilogue(v, p.bias, r_begin + rl, p.act);
+    }
+}
+
+// Kernel choice, for aligned rows with x in one staging chunk: batch <= 2 ->
+// gemv_stream_kernel (32 warps, one row each); batch >= 3 ->
+// gemv_split_kernel (16 warps, 4 rows x half the columns per task).
+// Otherwise gemv_kernel (16 warps, two rows per task, x chunked if needed).
+constexpr int kStreamThreads = 1024;
+constexpr int kRoundThreads = 512;
+constexpr int kRows = 2;
+constexpr int kUnroll = 4;
+constexpr int kSplitRows = 4, kSplitSegs = 2;
+// 16-byte loads in flight per row in the split kernel: a BF16 load carries 8
+// values, and two of them per row with 4 rows and 8 vectors do not fit the
+// 128 registers a thread of a 512-thread CTA has
+constexpr int split_unroll(int elem_bytes) { return elem_bytes == 2 ? 1 : 2; }
+
+enum Kind { kStream = 0, kSplit = 1, kRound = 2 };
+
+template <typename T, int BATCH>
+void *pick(int kind, bool vec) {
+    if constexpr (BATCH <= 2) {
+        if (kind == kStream) return reinterpret_cast<void *>(gemv_stream_kernel<T, BATCH, 1, kUnroll, kStreamThreads>);
+    }
+    if (kind == kSplit)
+        return reinterpret_cast<void *>(
+            gemv_split_kernel<T, BATCH, kSplitRows, kSplitSegs, split_unroll(sizeof(T)), kRoundThreads>);
+    return vec ? reinterpret_cast<void *>(gemv_kernel<T, BATCH, kRows, kUnroll, true, kRoundThreads>)
+               : reinterpret_cast<void *>(gemv_kernel<T, BATCH, kRows, kUnroll, false, kRoundThreads>);
+}
+
+template <typename T>
+void *kernel_for(int batch, int kind, bool vec) {
+    switch (batch) {
+        case 1: return pick<T, 1>(kind, vec);
+        case 2: return pick<T, 2>(kind, vec);
+        case 3: return pick<T, 3>(kind, vec);
+        case 4: return pick<T, 4>(kind, vec);
+        case 5: return pick<T, 5>(kind, vec);
+        case 6: return pick<T, 6>(kind, vec);
+        case 7: return pick<T, 7>(kind, vec);
+        default: return pick<T, 8>(kind, vec);
+    }
+}
+
+// The BF16-matrix kernels (instantiated in gemv_bf16.cu).
+void *kernel_for_bf16(int batch, int kind, bool vec);
+
+}  // namespace gemv
+}  // namespace gtg

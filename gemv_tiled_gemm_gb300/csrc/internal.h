@@ -32,15 +32,17 @@ struct GemmArgs {
     int64_t batch = 1, strideA = 0, strideB = 0, strideC = 0;
 };
 
-// y_b = act(A * x_b + bias) with one bias per row of A.
+// y_b = act(A * x_b + bias) with one bias per row of A. A holds FP32 values
+// (a_elem 4) or BF16 bit patterns (a_elem 2); x and y are FP32.
 struct GemvArgs {
     int64_t M, N;
-    const float *A; int64_t lda;
+    const void *A; int64_t lda;
     const float *x; int64_t ldx;
     float *y; int64_t ldy;
     int batch;
     const float *bias = nullptr; // M entries or null
     int act = 0;
+    int a_elem = 4;              // bytes per element of A
 };
 
 // The epilogue applied to one FP32 result before it is stored.

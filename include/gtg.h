@@ -183,6 +183,24 @@ GTG_API gtg_status gemv_f32(int64_t M, int64_t N,
                     cudaStream_t stream);
 
 /*
+ * gemv_bf16 -- gemv_f32 with the matrix stored in BF16 (bit patterns, 2 bytes
+ * per element); x, y and every multiply-add stay FP32. The matrix is the
+ * traffic that bounds a matrix-vector product ("Matrix Operations",
+ * "Matrix-Vector Multiplication", and its "Performance Considerations" on
+ * half-precision storage), so halving its bytes halves the time; each BF16
+ * value is widened to FP32 exactly before it is used, and the result differs
+ * from gemv_f32 on the widened matrix only by the order of FP32 additions.
+ *   Arguments as gemv_f32; A must be 2-byte aligned (x and y 4-byte); a
+ *   16-byte aligned A with lda % 8 == 0 enables 128-bit row loads.
+ */
+GTG_API gtg_status gemv_bf16(int64_t M, int64_t N,
+                             const gtg_bf16 *A, int64_t lda,
+                             const float *x, int64_t ldx,
+                             float *y, int64_t ldy,
+                             int batch,
+                             cudaStream_t stream);
+
+/*
  * gemm_tf32_noalloc -- the product of gemm_tf32, for callers that cannot
  * allocate device memory. The pages have no counterpart to this entry point;
  * it exists for users of this library.
@@ -264,6 +282,9 @@ GTG_API gtg_status gemv_f32_ex(int64_t M, int64_t N, const float *A, int64_t lda
 GTG_API gtg_status gemm_f16_ex(int64_t M, int64_t N, int64_t K, const gtg_f16 *A, int64_t lda,
                                const gtg_f16 *B, int64_t ldb, float *C, int64_t ldc,
                                const gtg_epilogue *epilogue, cudaStream_t stream);
+GTG_API gtg_status gemv_bf16_ex(int64_t M, int64_t N, const gtg_bf16 *A, int64_t lda,
+                                const float *x, int64_t ldx, float *y, int64_t ldy, int batch,
+                                const gtg_epilogue *epilogue, cudaStream_t stream);
 
 /*
  * gemm_strided_batched -- `batch` independent products in one call ("Matrix

@@ -67,24 +67,27 @@ def run_gemm(prec: str, A: np.ndarray, B: np.ndarray, lda=None, ldb=None, ldc=No
     return out[c_off + guard:c_off + guard + M * ldc].reshape(M, ldc)[:, :N].copy()
 
 
-def run_gemv(A: np.ndarray, X: np.ndarray, lda=None, ldx=None, ldy=None, a_off=0, stream=None):
-    """Y = X @ A^T through gemv_f32 (X: batch x N). Checks guard bands."""
+def run_gemv(A: np.ndarray, X: np.ndarray, lda=None, ldx=None, ldy=None, a_off=0, stream=None, prec="f32",
+             x_off=0):
+    """Y = X @ A^T through gemv_f32, or gemv_bf16 when prec == "bf16" (A then
+    holds BF16 bit patterns); X: batch x N. Checks guard bands."""
     t = torch()
     M, N = A.shape
     batch = X.shape[0]
     lda = lda or max(N, 1)
     ldx = ldx or max(N, 1)
     ldy = ldy or max(M, 1)
-    dA = _dev_buffer(A, M, N, lda, a_off, np.float32(np.nan))
-    dX = _dev_buffer(X, batch, N, ldx, 0, np.float32(np.nan))
+    dA = _dev_buffer(A, M, N, lda, a_off, BF16_NAN if prec == "bf16" else np.float32(np.nan))
+    dX = _dev_buffer(X, batch, N, ldx, x_off, np.float32(np.nan))
     host_y = np.full((batch + 2) * ldy + 8, CANARY, dtype=np.float32)
     body = np.zeros(host_y.shape, dtype=bool)
     body[ldy:ldy + batch * ldy].reshape(batch, ldy)[:, :M] = True
     host_y[body] = np.nan
     dY = t.from_numpy(host_y).cuda()
     s = stream if stream is not None else t.cuda.current_stream()
-    st = gtg.gemv_f32(M, N, dA.data_ptr() + 4 * a_off, lda, dX.data_ptr(), ldx,
-                      dY.data_ptr() + 4 * ldy, ldy, batch, int(s.cuda_stream))
+    fn, esz = (gtg.gemv_bf16, 2) if prec == "bf16" else (gtg.gemv_f32, 4)
+    st = fn(M, N, dA.data_ptr() + esz * a_off, lda, dX.data_ptr() + 4 * x_off, ldx,
+            dY.data_ptr() + 4 * ldy, ldy, batch, int(s.cuda_stream))
     assert st == gtg.GTG_OK, gtg.status_string(st)
     assert gtg.gtg_sync_status(int(s.cuda_stream)) == gtg.GTG_OK
     out = dY.cpu().numpy()

@@ -138,3 +138,13 @@ def test_tensor_helper_host_and_device():
     Y = gtg.matvec(torch.from_numpy(A).pin_memory(), torch.from_numpy(X).pin_memory())
     assert not Y.is_cuda
     check(A, X, Y.numpy())
+
+
+@pytest.mark.parametrize("batch,ldx,x_off", [(1, 1024, 1), (2, 1025, 0), (2, 1024, 3), (5, 1026, 0), (8, 1024, 2)])
+def test_vectors_staged_by_threads_when_not_16_byte_aligned(batch, ldx, x_off):
+    """x rows that are not 16-byte aligned cannot be staged by bulk copies;
+    the kernels then stage them with plain loads (same results)."""
+    g = PCG32(70 + batch + ldx + x_off)
+    A = g.uniform_f32((700, 1024))
+    X = g.uniform_f32((batch, 1024))
+    check(A, X, run_gemv(A, X, ldx=ldx, x_off=x_off))

@@ -7,7 +7,7 @@ import pytest
 import gemv_tiled_gemm_gb300 as gtg
 import oracle
 from seeded import PCG32, bf16_bits_to_f32, f16_bits_to_f32
-from tests._gpu import check_gemm, run_gemm, sample_rows
+from tests._gpu import check_gemm, run_gemm, run_gemv, sample_rows
 from tests._util import parity_ratio
 
 pytestmark = pytest.mark.gpu
@@ -103,7 +103,7 @@ def test_strided_batched(prec, case):
         Bb = B_f[b * sB: b * sB + K * ldb].reshape(K, ldb)[:, :N]
         ref, E = oracle.dense_layer(Ab, Bb, bias, "relu")
         got = C[b * sC: b * sC + M * ldc].reshape(M, ldc)[:, :N]
-        ratio, bad = parity_ratio(got, ref, E + np.abs(ref), prec if prec != "f32" else "f32", K)
+        ratio, bad = parity_ratio(got, ref, E, prec, K, rel=2.0 ** -23)
         assert bad == 0, (b, ratio)
     # nothing written between the items (the padding keeps its NaN)
     if case == "padded":
@@ -138,3 +138,58 @@ def test_strided_batched_validation():
     assert f(7, 4, 4, 4, A, 4, 16, B, 4, 16, C, 4, 16, 2) == gtg.GTG_ERR_INVALID_VALUE
     assert f("f32", 4, 4, 4, A, 4, 16, B, 4, 16, A + 64, 4, 16, 2) == gtg.GTG_ERR_ALIAS          # C reaches A's items
     assert f("f32", 4, 4, 4, A, 4, 16, B, 4, 16, C, 4, 16, 0) == gtg.GTG_OK
+
+
+# ---- BF16 matrix GEMV ----------------------------------------------------------
+# A in BF16 is widened exactly, so the reference is the FP64 product with the
+# widened matrix and the FP32 bound of gemv_f32 applies unchanged.
+
+def _check_gemv(Abits, X, Y):
+    Af = bf16_bits_to_f32(Abits)
+    for b in range(X.shape[0]):
+        ref, E = oracle.gemv(Af, X[b])
+        ratio, bad = parity_ratio(Y[b], ref, E, "f32", Af.shape[1])
+        assert bad == 0, (b, ratio)
+
+
+@pytest.mark.parametrize("M,N,batch", [(4096, 4096, 1), (4096, 4096, 8), (8192, 8192, 2), (523, 1031, 3),
+                                       (151, 4097, 1), (2049, 130, 5), (1, 1, 1), (10, 100003, 2),
+                                       (7, 9, 8), (300, 16, 4)])
+def test_gemv_bf16(M, N, batch):
+    g = PCG32(1000 + M + N + batch)
+    A = g.normal_bf16((M, N))
+    X = g.uniform_f32((batch, N))
+    _check_gemv(A, X, run_gemv(A, X, prec="bf16"))
+
+
+@pytest.mark.parametrize("lda,a_off", [(1040, 0), (1033, 0), (1032, 3), (1024, 1)])
+def test_gemv_bf16_unaligned_and_padded_rows(lda, a_off):
+    g = PCG32(1100 + lda + a_off)
+    A = g.normal_bf16((333, 1024))
+    X = g.uniform_f32((2, 1024))
+    _check_gemv(A, X, run_gemv(A, X, lda=lda, a_off=a_off, prec="bf16"))
+
+
+def test_gemv_bf16_matches_f32_on_the_widened_matrix_exactly_for_integers():
+    rng = np.random.default_rng(1200)
+    Ai = rng.integers(-64, 65, (777, 2056))
+    xi = rng.integers(-64, 65, (3, 2056))
+    from seeded import f64_to_bf16_bits
+    Y = run_gemv(f64_to_bf16_bits(Ai.astype(np.float64)), xi.astype(np.float32), prec="bf16")
+    assert np.array_equal(Y, (xi @ Ai.T).astype(np.float32))
+
+
+def test_matvec_bf16_with_epilogue():
+    torch = _t()
+    g = PCG32(1300)
+    A = g.normal_bf16((640, 520))
+    x = g.uniform_f32((520,))
+    bias = g.uniform_f32((640,))
+    tA = torch.from_numpy(A.view(np.int16)).view(torch.bfloat16)
+    y = gtg.matvec(tA.cuda(), torch.from_numpy(x).cuda(), bias=torch.from_numpy(bias), activation="relu")
+    ref, E = oracle.dense_vector(bf16_bits_to_f32(A), x, bias, "relu")
+    ratio, bad = parity_ratio(y.cpu().numpy(), ref, E, "f32", 520, rel=2.0 ** -23)
+    assert bad == 0, ratio
+    # host tensors: copied in and out
+    yh = gtg.matvec(tA, torch.from_numpy(x), bias=torch.from_numpy(bias), activation="relu")
+    assert torch.equal(yh, y.cpu())
