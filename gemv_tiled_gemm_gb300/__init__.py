@@ -35,7 +35,7 @@ _i64, _ptr, _int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
 
 class GtgPlan(ctypes.Structure):
     _fields_ = [("kernel", _int), ("bm", _int), ("bn", _int), ("bk", _int), ("stages", _int),
-                ("grid", _int), ("threads", _int), ("smem", _int)]
+                ("grid", _int), ("threads", _int), ("smem", _int), ("cluster", _int)]
 
     def as_dict(self) -> dict:
         d = {f: getattr(self, f) for f, _ in self._fields_}
@@ -74,6 +74,8 @@ SIGNATURES = {
     "gtg_plan_gemm": (_int, [_int, _i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64,
                              ctypes.POINTER(GtgPlan)]),
     "gtg_plan_gemv": (_int, [_i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _int,
+                             ctypes.POINTER(GtgPlan)]),
+    "gtg_plan_gemv_bf16": (_int, [_i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _int,
                              ctypes.POINTER(GtgPlan)]),
     "gtg_force_simt": (None, [_int]),
     "gtg_set_wait_limit_ns": (None, [ctypes.c_uint64]),
@@ -229,11 +231,14 @@ def plan_gemm(precision, M, N, K, A, lda, B, ldb, C, ldc) -> dict:
     return plan.as_dict()
 
 
-def plan_gemv(M, N, A, lda, x, ldx, y, ldy, batch) -> dict:
+def plan_gemv(M, N, A, lda, x, ldx, y, ldy, batch, precision="f32") -> dict:
+    """The kernel a gemv_f32 (precision "f32") or gemv_bf16 ("bf16") call
+    with these arguments would launch."""
     plan = GtgPlan()
-    st = lib().gtg_plan_gemv(M, N, A, lda, x, ldx, y, ldy, batch, ctypes.byref(plan))
+    name = {"f32": "gtg_plan_gemv", "bf16": "gtg_plan_gemv_bf16"}[precision]
+    st = getattr(lib(), name)(M, N, A, lda, x, ldx, y, ldy, batch, ctypes.byref(plan))
     if st != GTG_OK:
-        raise GtgError(st, "gtg_plan_gemv")
+        raise GtgError(st, name)
     return plan.as_dict()
 
 

@@ -438,10 +438,9 @@ gtg_status gtg_plan_gemm(int precision, int64_t M, int64_t N, int64_t K, const v
     return plan_gemm_impl(dev, g, plan);
 }
 
-gtg_status gtg_plan_gemv(int64_t M, int64_t N, const float *A, int64_t lda, const float *x, int64_t ldx,
-                         const float *y, int64_t ldy, int batch, gtg_plan *plan) {
+static gtg_status plan_gemv_impl(const GemvArgs &g, gtg_plan *plan) {
+    const int64_t M = g.M, N = g.N;
     if (plan == nullptr) return GTG_ERR_INVALID_VALUE;
-    const GemvArgs g{M, N, A, lda, x, batch > 1 ? ldx : N, const_cast<float *>(y), batch > 1 ? ldy : M, batch};
     gtg_status st = validate_gemv(g);
     if (st != GTG_OK) return st;
     std::memset(plan, 0, sizeof(*plan));
@@ -454,6 +453,20 @@ gtg_status gtg_plan_gemv(int64_t M, int64_t N, const float *A, int64_t lda, cons
     }
     gemv_plan(dev, g, plan);
     return GTG_OK;
+}
+
+gtg_status gtg_plan_gemv(int64_t M, int64_t N, const float *A, int64_t lda, const float *x, int64_t ldx,
+                         const float *y, int64_t ldy, int batch, gtg_plan *plan) {
+    return plan_gemv_impl(GemvArgs{M, N, A, lda, x, batch > 1 ? ldx : N, const_cast<float *>(y),
+                                   batch > 1 ? ldy : M, batch},
+                          plan);
+}
+
+gtg_status gtg_plan_gemv_bf16(int64_t M, int64_t N, const gtg_bf16 *A, int64_t lda, const float *x, int64_t ldx,
+                              const float *y, int64_t ldy, int batch, gtg_plan *plan) {
+    GemvArgs g{M, N, A, lda, x, batch > 1 ? ldx : N, const_cast<float *>(y), batch > 1 ? ldy : M, batch};
+    g.a_elem = 2;
+    return plan_gemv_impl(g, plan);
 }
 
 void gtg_force_simt(int force) { g_force_simt.store(force ? 1 : 0); }

@@ -352,6 +352,7 @@ void simt_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
     plan->bk = kBK;
     plan->threads = big ? 256 : 64;
     plan->smem = 0;
+    plan->cluster = 1;
     const int64_t tiles = ((g.M + plan->bm - 1) / plan->bm) * ((g.N + plan->bn - 1) / plan->bn);
     int64_t splits = 1;
     if (!big) {

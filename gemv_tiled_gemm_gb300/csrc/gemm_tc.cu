@@ -856,6 +856,7 @@ void fill_pair_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
     plan->grid = static_cast<int>(2 * clusters);
     plan->threads = kThreads;
     plan->smem = S::SMEM;
+    plan->cluster = 2;
 }
 
 template <bool TF32, int BN>
@@ -870,6 +871,7 @@ void fill_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
     plan->grid = static_cast<int>(tiles < dev.sms ? tiles : dev.sms);
     plan->threads = kThreads;
     plan->smem = S::SMEM;
+    plan->cluster = 1;
 }
 
 }  // namespace

@@ -1,6 +1,9 @@
 // GEMV planning and launch, and the FP32-matrix instantiations of the GEMV
 // kernels (the kernels themselves and their design are in gemv_kernels.cuh).
 #include <algorithm>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "gemv_kernels.cuh"
 
@@ -8,6 +11,9 @@ namespace gtg {
 namespace {
 
 using namespace gemv;
+
+// Room left in shared memory for the kernels' static variables (one mbarrier).
+constexpr int kStaticSmemMargin = 1024;
 
 // 16-byte loads are possible when the matrix starts on a 16-byte boundary and
 // every row does too.
@@ -19,10 +25,60 @@ struct Layout {
     int chunk, nchunks, smem;
     int kind;
     int threads;
+    int grid;
+    int cluster;   // CTAs per cluster (column blocks); 1 unless kind == kCluster
+    int ublock;    // kCluster: 16-byte units per column block
 };
+
+void *kernel_of(const GemvArgs &g, int kind) {
+    return g.a_elem == 2 ? kernel_for_bf16(g.batch, kind, gemv_vec(g)) : kernel_for<float>(g.batch, kind, gemv_vec(g));
+}
+
+// How many clusters of `cluster` CTAs with `smem` bytes each can be resident at
+// once. Not every cluster size tiles the GPU's SMs: on a 152-SM GB300 all 76
+// pairs fit but only 36 of 38 quads, so the grid is sized to what fits (a
+// second wave of clusters would double the time). Cached per configuration.
+int max_active_clusters(const DeviceInfo &dev, const GemvArgs &g, int cluster, int smem, int grid) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int, int, int>, int> cache;
+    const auto key = std::make_tuple(dev.id, g.a_elem, g.batch, cluster, smem);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    void *kern = kernel_of(g, kCluster);
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(kRoundThreads);
+        cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = cluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();   // a refused query only rules this cluster size out
+    std::lock_guard<std::mutex> lock(mu);
+    cache[key] = n;
+    return n;
+}
+
+// Shared memory of gemv_cluster_kernel: x blocks, per-task partials, per-row partials.
+int cluster_smem(const GemvArgs &g, int rows_cl, int chunk) {
+    const int64_t groups = (rows_cl + kSplitRows - 1) / kSplitRows;
+    return static_cast<int>((g.batch * int64_t{chunk} + groups * kSplitSegs * kSplitRows * g.batch +
+                             int64_t{rows_cl} * g.batch) * 4);
+}
 
 Layout layout(const DeviceInfo &dev, const GemvArgs &g) {
     const int64_t per_entry = 4ll * g.batch;
+    const int limit = dev.smem_optin - kStaticSmemMargin;
     // a multiple of 8 entries keeps every chunk start on a 16-byte unit of
     // either matrix type
     int64_t chunk = std::max<int64_t>(8, kSmemBudget / per_entry / 8 * 8);
@@ -35,46 +91,75 @@ Layout layout(const DeviceInfo &dev, const GemvArgs &g) {
     l.smem = static_cast<int>(chunk * per_entry);
     l.kind = kRound;
     l.threads = kRoundThreads;
-    if (gemv_vec(g) && l.nchunks == 1) {
+    l.grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(dev.sms, g.M)));
+    l.cluster = 1;
+    l.ublock = 0;
+    if (!gemv_vec(g)) return l;
+    if (l.nchunks == 1) {
         if (g.batch <= 2) {
             l.kind = kStream;
             l.threads = kStreamThreads;
-        } else {
-            // partial sums of one CTA's rows: groups x segments x rows x batch floats
-            const int64_t rows_cta = (g.M + dev.sms - 1) / dev.sms;
-            const int64_t part = (rows_cta + kSplitRows - 1) / kSplitRows * kSplitSegs * kSplitRows * g.batch * 4;
-            if (l.smem + part <= dev.smem_optin) {
-                l.kind = kSplit;
-                l.smem = static_cast<int>(l.smem + part);
-            }
+            return l;
+        }
+        // partial sums of one CTA's rows: groups x segments x rows x batch floats
+        const int64_t rows_cta = (g.M + dev.sms - 1) / dev.sms;
+        const int64_t part = (rows_cta + kSplitRows - 1) / kSplitRows * kSplitSegs * kSplitRows * g.batch * 4;
+        if (l.smem + part <= limit) {
+            l.kind = kSplit;
+            l.smem = static_cast<int>(l.smem + part);
+            return l;
         }
     }
-    return l;
+    // x does not fit one CTA: split the columns over the CTAs of a cluster
+    const int VE = 16 / g.a_elem;
+    const int64_t nu = g.N / VE;
+    for (int C = 2; C <= 8; C *= 2) {
+        int grid = dev.sms / C * C;
+        if (grid == 0) continue;
+        const int ub = static_cast<int>((nu + C - 1) / C);
+        const int cchunk = ((ub + 1) * VE + 7) / 8 * 8;
+        int smem = cluster_smem(g, static_cast<int>((g.M + grid / C - 1) / (grid / C)), cchunk);
+        if (smem > limit) continue;
+        const int fit = max_active_clusters(dev, g, C, smem, grid);
+        if (fit <= 0) continue;
+        if (fit < grid / C) {
+            grid = fit * C;
+            smem = cluster_smem(g, static_cast<int>((g.M + fit - 1) / fit), cchunk);
+            if (smem > limit) continue;
+        }
+        l.kind = kCluster;
+        l.cluster = C;
+        l.grid = grid;
+        l.chunk = cchunk;
+        l.nchunks = 1;
+        l.ublock = ub;
+        l.smem = smem;
+        return l;
+    }
+    return l;   // the round kernel, x staged chunk by chunk
 }
 
 }  // namespace
 
 void gemv_plan(const DeviceInfo &dev, const GemvArgs &g, gtg_plan *plan) {
     const Layout l = layout(dev, g);
-    // One CTA per SM (it fills the register file); every CTA owns an equal
-    // share of the rows.
-    int64_t grid = dev.sms;
-    if (grid > g.M) grid = g.M;
+    // One CTA per SM (it fills the register file); every CTA (cluster) owns an
+    // equal share of the rows.
     plan->kernel = GTG_KERNEL_GEMV;
-    plan->bm = l.kind == kStream ? 1 : (l.kind == kSplit ? kSplitRows : kRows);
+    plan->bm = l.kind == kStream ? 1 : (l.kind == kRound ? kRows : kSplitRows);
     plan->bn = l.chunk;
-    plan->bk = l.kind == kSplit ? split_unroll(g.a_elem) : kUnroll;
+    plan->bk = l.kind == kSplit || l.kind == kCluster ? split_unroll(g.a_elem) : kUnroll;
     plan->stages = l.nchunks;
-    plan->grid = static_cast<int>(std::max<int64_t>(grid, 1));
+    plan->grid = l.grid;
     plan->threads = l.threads;
     plan->smem = l.smem;
+    plan->cluster = l.cluster;
 }
 
 cudaError_t gemv_launch(const DeviceInfo &dev, const GemvArgs &g, const gtg_plan &plan,
                         cudaStream_t stream) {
     const Layout l = layout(dev, g);
-    void *kern = g.a_elem == 2 ? kernel_for_bf16(g.batch, l.kind, gemv_vec(g))
-                               : kernel_for<float>(g.batch, l.kind, gemv_vec(g));
+    void *kern = kernel_of(g, l.kind);
     if (l.smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, l.smem);
         if (e != cudaSuccess) return e;
@@ -92,6 +177,7 @@ cudaError_t gemv_launch(const DeviceInfo &dev, const GemvArgs &g, const gtg_plan
     p.nchunks = l.nchunks;
     p.bias = g.bias;
     p.act = g.act;
+    p.ublock = l.ublock;
     // bulk copies of x need 16-byte aligned rows of a multiple of 16 bytes
     p.x_bulk = l.kind != kRound && (reinterpret_cast<uintptr_t>(g.x) & 15) == 0 && g.N % 4 == 0 &&
                (g.batch == 1 || g.ldx % 4 == 0);
@@ -104,11 +190,15 @@ cudaError_t gemv_launch(const DeviceInfo &dev, const GemvArgs &g, const gtg_plan
     cfg.stream = stream;
     // may start while the previous kernel in the stream drains; every GEMV
     // kernel waits for it (griddepcontrol.wait) before reading or writing data
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = l.cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = l.kind == kCluster ? 2 : 1;
     return cudaLaunchKernelExC(&cfg, kern, args);
 }
 

@@ -54,6 +54,7 @@ struct Params {
     int nchunks;
     const float *bias;   // epilogue: y = act(acc + bias[row]); null for none
     int act;
+    int ublock;          // gemv_cluster_kernel: 16-byte units per column block
     int x_bulk;          // x rows 16-byte aligned, ldx and N multiples of 4: stage x by bulk copies
     int *status;         // the library's device status word (set on a timed-out wait)
 };
@@ -557,6 +558,173 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_split_kernel(const Params p)
     }
 }
 
+// Three or more vectors whose staged x would not fit one CTA's shared memory
+// (or would leave it too little): a cluster of C CTAs shares one block of
+// rows, and CTA c of the cluster takes column block c, so it stages only its
+// 1/C of every vector. Within a CTA the work is that of gemv_split_kernel
+// over its column block. Each CTA leaves one partial sum per (row, vector)
+// in its shared memory; after a cluster barrier every CTA finishes a share
+// of the rows by adding the C partials, read through distributed shared
+// memory, in rank order (deterministic), and a second cluster barrier keeps
+// every CTA's shared memory alive until the others have read it.
+//
+// Column blocks are ub = p.ublock 16-byte units wide (the last one takes the
+// rest, plus the N % VE trailing entries); p.chunk >= ub * VE + VE.
+template <typename T, int BATCH, int ROWS, int WC, int U, int kThreads>
+__global__ void __launch_bounds__(kThreads, 1) gemv_cluster_kernel(const Params p) {
+    constexpr int kWarps = kThreads / 32;
+    constexpr int VE = Elem<T>::kVec;
+    extern __shared__ float4 xs_raw[];
+    __shared__ __align__(8) unsigned long long xbar;
+    const int C = static_cast<int>(ptx::cluster_nctarank());
+    const int c = static_cast<int>(ptx::cluster_ctarank());
+    const int cid = static_cast<int>(blockIdx.x) / C, ncl = static_cast<int>(gridDim.x) / C;
+    const int r_begin = static_cast<int>(static_cast<long long>(p.M) * cid / ncl);
+    const int r_end = static_cast<int>(static_cast<long long>(p.M) * (cid + 1) / ncl);
+    const int rows = r_end - r_begin;
+    const int ngroups = (rows + ROWS - 1) / ROWS;
+    const int ntasks = ngroups * WC;
+    const int nu = p.N / VE;
+    const int ub0 = min(c * p.ublock, nu);                       // this CTA's units [ub0, ub1)
+    const int ub1 = c == C - 1 ? nu : min(ub0 + p.ublock, nu);
+    const int nub = ub1 - ub0;
+    const int tail = c == C - 1 ? p.N - VE * nu : 0;             // trailing entries (last block)
+    const int xlen = VE * nub + tail;                            // staged entries per vector
+    const int segu = ((nub + WC - 1) / WC + 31) / 32 * 32;
+    float *xs = reinterpret_cast<float *>(xs_raw);               // [BATCH][chunk]
+    float *part = xs + BATCH * p.chunk;                          // [group][segment][row][batch]
+    float *mine = part + static_cast<long long>(ngroups) * WC * ROWS * BATCH;   // [row][batch]
+    const T *A = static_cast<const T *>(p.A) + VE * static_cast<long long>(ub0);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t bar = ptx::smem_addr(&xbar);
+
+    if (p.x_bulk && threadIdx.x == 0) {
+        ptx::mbar_init(bar, 1);
+        ptx::fence_barrier_init();
+    }
+    if (threadIdx.x < 32) {
+        const uint32_t bytes = min(4096u, static_cast<uint32_t>(nub) * 16u);
+        for (int r = r_begin + static_cast<int>(threadIdx.x); bytes > 0 && r < r_end; r += 32)
+            ptx::prefetch_l2(A + static_cast<long long>(r) * p.lda, bytes);
+    }
+    ptx::wait_prior_grid();
+    ptx::allow_next_grid();
+    if (p.x_bulk) {
+        __syncthreads();   // the barrier is initialised
+        if (threadIdx.x == 0) {
+            ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(BATCH * xlen * 4));
+            if (xlen > 0)
+#pragma unroll
+                for (int b = 0; b < BATCH; ++b)
+                    ptx::bulk_load(ptx::smem_addr(xs + b * p.chunk),
+                                   p.x + static_cast<long long>(b) * p.ldx + VE * ub0,
+                                   static_cast<uint32_t>(xlen * 4), bar);
+        }
+    }
+
+    const T *arow[ROWS];
+    int j0 = 0, j1 = 0;
+    auto setup = [&](int task) {
+        const int rg = task / WC, cs = task - rg * WC;
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r)
+            arow[r] = A + static_cast<long long>(min(r_begin + rg * ROWS + r, r_end - 1)) * p.lda;
+        j0 = cs * segu;
+        j1 = min(j0 + segu, nub);
+    };
+    auto load = [&](int jb, float4 (&dst)[U][ROWS]) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = jb + 32 * u + lane;
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r)
+                dst[u][r] = j < j1 ? ld16(arow[r] + VE * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+
+    float4 nxt[U][ROWS];
+    if (warp < ntasks) {
+        setup(warp);
+        if (j0 < j1) load(j0, nxt);
+    }
+    bool ok = true;
+    if (p.x_bulk) {
+        ok = __all_sync(0xFFFFFFFFu, wait_x(bar, p.status));
+    } else {
+#pragma unroll
+        for (int b = 0; b < BATCH; ++b) {
+            const float *src = p.x + static_cast<long long>(b) * p.ldx + VE * ub0;
+            for (int j = threadIdx.x; j < xlen; j += kThreads) xs[b * p.chunk + j] = __ldg(src + j);
+        }
+        __syncthreads();
+    }
+
+    for (int task = warp; ok && task < ntasks; task += kWarps) {
+        if (task != warp) {
+            setup(task);
+            if (j0 < j1) load(j0, nxt);
+        }
+        const int cs = task % WC;
+        float acc[ROWS][BATCH];
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) acc[r][b] = 0.f;
+        for (int jb = j0; jb < j1; jb += 32 * U) {
+            float4 cur[U][ROWS];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) cur[u][r] = nxt[u][r];
+            if (jb + 32 * U < j1) load(jb + 32 * U, nxt);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = jb + 32 * u + lane;
+                if (j < j1) fma_unit<T, ROWS, BATCH>(acc, cur[u], xs, p.chunk, VE * j);
+            }
+        }
+        if (cs == WC - 1 && lane < tail) {
+            const int jt = VE * nub + lane;
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) {
+                const float a = Elem<T>::one(arow[r] + jt);
+#pragma unroll
+                for (int b = 0; b < BATCH; ++b) acc[r][b] = fmaf(a, xs[b * p.chunk + jt], acc[r][b]);
+            }
+        }
+        float *dst = part + static_cast<long long>(task) * ROWS * BATCH;
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) {
+                float v = acc[r][b];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+                if (lane == (r * BATCH + b) % 32) dst[r * BATCH + b] = v;
+            }
+    }
+    __syncthreads();
+    // this CTA's partial per (row, vector): its segments added in order
+    for (int idx = threadIdx.x; idx < rows * BATCH; idx += kThreads) {
+        const int rl = idx / BATCH, b = idx - rl * BATCH;
+        const int rg = rl / ROWS, r = rl - rg * ROWS;
+        float v = 0.f;
+#pragma unroll
+        for (int cs = 0; cs < WC; ++cs) v += part[((rg * WC + cs) * ROWS + r) * BATCH + b];
+        mine[idx] = v;
+    }
+    ptx::cluster_sync();   // every CTA's partials are complete and visible to the cluster
+    const uint32_t mine_addr = ptx::smem_addr(mine);
+    for (int idx = threadIdx.x; idx < rows * BATCH; idx += kThreads) {
+        const int rl = idx / BATCH, b = idx - rl * BATCH;
+        if (rl % C != c) continue;   // rows are shared out round-robin over the cluster
+        float v = 0.f;
+        for (int cc = 0; cc < C; ++cc) v += ptx::ld_cluster_f32(ptx::map_to_rank(mine_addr, cc) + 4u * idx);
+        p.y[static_cast<long long>(b) * p.ldy + r_begin + rl] = apply_epilogue(v, p.bias, r_begin + rl, p.act);
+    }
+    ptx::cluster_sync();   // no CTA leaves while another may still read its shared memory
+}
+
 // Kernel choice, for aligned rows with x in one staging chunk: batch <= 2 ->
 // gemv_stream_kernel (32 warps, one row each); batch >= 3 ->
 // gemv_split_kernel (16 warps, 4 rows x half the columns per task).
@@ -571,7 +739,7 @@ constexpr int kSplitRows = 4, kSplitSegs = 2;
 // 128 registers a thread of a 512-thread CTA has
 constexpr int split_unroll(int elem_bytes) { return elem_bytes == 2 ? 1 : 2; }
 
-enum Kind { kStream = 0, kSplit = 1, kRound = 2 };
+enum Kind { kStream = 0, kSplit = 1, kRound = 2, kCluster = 3 };
 
 template <typename T, int BATCH>
 void *pick(int kind, bool vec) {
@@ -581,6 +749,9 @@ void *pick(int kind, bool vec) {
     if (kind == kSplit)
         return reinterpret_cast<void *>(
             gemv_split_kernel<T, BATCH, kSplitRows, kSplitSegs, split_unroll(sizeof(T)), kRoundThreads>);
+    if (kind == kCluster)
+        return reinterpret_cast<void *>(
+            gemv_cluster_kernel<T, BATCH, kSplitRows, kSplitSegs, split_unroll(sizeof(T)), kRoundThreads>);
     return vec ? reinterpret_cast<void *>(gemv_kernel<T, BATCH, kRows, kUnroll, true, kRoundThreads>)
                : reinterpret_cast<void *>(gemv_kernel<T, BATCH, kRows, kUnroll, false, kRoundThreads>);
 }

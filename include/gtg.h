@@ -375,6 +375,7 @@ typedef struct {
     int grid;     /* thread blocks launched */
     int threads;  /* threads per block */
     int smem;     /* dynamic shared memory per block, bytes */
+    int cluster;  /* thread blocks per cluster (1: no cluster launch) */
 } gtg_plan;
 
 GTG_API gtg_status gtg_plan_gemm(int precision, int64_t M, int64_t N, int64_t K,
@@ -383,10 +384,18 @@ GTG_API gtg_status gtg_plan_gemm(int precision, int64_t M, int64_t N, int64_t K,
                          const void *C, int64_t ldc,
                          gtg_plan *plan);
 
-/* Same for gemv_f32 (bm = rows per warp, bn = shared-memory chunk length). */
+/* Same for gemv_f32 (bm = rows per warp task, bn = entries of each vector
+ * staged per CTA, bk = 16-byte loads in flight per row, stages = staging
+ * passes, cluster = CTAs sharing a block of rows, each with its own block of
+ * columns). */
 GTG_API gtg_status gtg_plan_gemv(int64_t M, int64_t N, const float *A, int64_t lda,
                          const float *x, int64_t ldx, const float *y, int64_t ldy,
                          int batch, gtg_plan *plan);
+
+/* Same for gemv_bf16. */
+GTG_API gtg_status gtg_plan_gemv_bf16(int64_t M, int64_t N, const gtg_bf16 *A, int64_t lda,
+                              const float *x, int64_t ldx, const float *y, int64_t ldy,
+                              int batch, gtg_plan *plan);
 
 /*
  * Testing hook: force the tensor-core GEMM paths onto the SIMT kernel

@@ -148,3 +148,43 @@ def test_vectors_staged_by_threads_when_not_16_byte_aligned(batch, ldx, x_off):
     A = g.uniform_f32((700, 1024))
     X = g.uniform_f32((batch, 1024))
     check(A, X, run_gemv(A, X, ldx=ldx, x_off=x_off))
+
+
+def _plan(A, X, prec="f32", lda=None):
+    """The plan of the call run_gemv makes (fake, aligned, non-overlapping addresses)."""
+    M, N = A.shape
+    return gtg.plan_gemv(M, N, 1 << 32, lda or N, 2 << 32, N, 3 << 32, M, X.shape[0], precision=prec)
+
+
+@pytest.mark.parametrize("M,N,batch,lda,cluster", [(8192, 8192, 8, None, 2), (3000, 20000, 3, None, 2),
+                                                   (200, 60000, 1, None, 2), (300, 16384, 8, None, 4),
+                                                   (10, 30000, 8, None, 8), (999, 20003, 3, 20004, 2),
+                                                   (517, 13000, 6, None, 2)])
+def test_column_blocks_over_a_cluster(M, N, batch, lda, cluster):
+    """Vectors too large for one CTA's shared memory: the CTAs of a cluster
+    each stage one block of columns and add their partial sums through
+    distributed shared memory (fewer rows than clusters included; N = 20003
+    has trailing entries and x rows that bulk copies cannot take)."""
+    g = PCG32(90 + M + N + batch)
+    A = g.uniform_f32((M, N))
+    X = g.uniform_f32((batch, N))
+    plan = _plan(A, X, lda=lda)
+    assert plan["cluster"] == cluster, plan
+    Y = run_gemv(A, X, lda=lda)
+    if M > 2048:
+        rows = np.unique(np.concatenate([np.arange(0, M, 37), [M - 1]]))
+        for b in range(batch):
+            ref, E = oracle.gemv(A[rows], X[b])
+            ratio, bad = parity_ratio(Y[b][rows], ref, E, "f32", N)
+            assert bad == 0, (b, ratio)
+    else:
+        check(A, X, Y)
+
+
+def test_cluster_results_do_not_depend_on_the_run():
+    g = PCG32(95)
+    A = g.uniform_f32((1500, 24000))
+    X = g.uniform_f32((4, 24000))
+    assert _plan(A, X)["cluster"] == 2
+    Y1, Y2 = run_gemv(A, X), run_gemv(A, X)
+    assert np.array_equal(Y1, Y2)

@@ -193,3 +193,21 @@ def test_matvec_bf16_with_epilogue():
     # host tensors: copied in and out
     yh = gtg.matvec(tA, torch.from_numpy(x), bias=torch.from_numpy(bias), activation="relu")
     assert torch.equal(yh, y.cpu())
+
+
+@pytest.mark.parametrize("M,N,batch,lda,cluster", [(8192, 8192, 8, 8192, 2), (700, 20004, 3, 20008, 2),
+                                                   (300, 16384, 8, 16384, 4)])
+def test_gemv_bf16_column_blocks_over_a_cluster(M, N, batch, lda, cluster):
+    """N = 20004 leaves 4 trailing entries after the last 8-entry load."""
+    g = PCG32(1400 + M + batch)
+    A = g.normal_bf16((M, N))
+    X = g.uniform_f32((batch, N))
+    plan = gtg.plan_gemv(M, N, 1 << 32, lda, 2 << 32, N, 3 << 32, M, batch, precision="bf16")
+    assert plan["cluster"] == cluster, plan
+    Y = run_gemv(A, X, lda=lda, prec="bf16")
+    rows = np.unique(np.concatenate([np.arange(0, M, 29), [M - 1]]))
+    Af = bf16_bits_to_f32(A[rows])
+    for b in range(batch):
+        ref, E = oracle.gemv(Af, X[b])
+        ratio, bad = parity_ratio(Y[b][rows], ref, E, "f32", N)
+        assert bad == 0, (b, ratio)
