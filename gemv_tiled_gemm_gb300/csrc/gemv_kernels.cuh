@@ -179,6 +179,62 @@ __device__ __forceinline__ void fma_unit(float (&acc)[ROWS][BATCH], const float4
     }
 }
 
+// Reduce-scatter over the 32 lanes of a warp for P values per lane (P a power
+// of two, at most 32). Lane offsets go 16, 8, 4, 2, 1: while a lane holds more
+// than one value, each level sends half of them to the partner lane and keeps
+// the sum of the other half; the remaining levels are plain butterfly
+// additions. Afterwards lane L holds the warp total of value L >> (5 - log2 P)
+// (31 shuffles for 32 values, against 160 for a butterfly per value).
+template <int P>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[P], int lane) {
+#pragma unroll
+    for (int lvl = 0; lvl < 5; ++lvl) {
+        const int o = 16 >> lvl;
+        const int k = P >> lvl;   // values per lane before this level
+        if (k > 1) {
+            const bool hi = (lane & o) != 0;
+#pragma unroll
+            for (int i = 0; i < k / 2; ++i) {
+                const float send = hi ? v[i] : v[i + k / 2];
+                const float keep = hi ? v[i + k / 2] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
+            }
+        } else {
+            v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], o);
+        }
+    }
+    return v[0];
+}
+
+__host__ __device__ constexpr int pow2_at_least(int v) { return v <= 1 ? 1 : 2 * pow2_at_least((v + 1) / 2); }
+__host__ __device__ constexpr int log2_of(int v) { return v <= 1 ? 0 : 1 + log2_of(v / 2); }
+
+// The warp totals of a task's ROWS x BATCH per-lane partial sums. Returns the
+// total that this lane owns and sets `vi` to its index r * BATCH + b, or to -1
+// when the lane owns none (each total is owned by exactly one lane).
+template <int ROWS, int BATCH>
+__device__ __forceinline__ float task_total(const float (&acc)[ROWS][BATCH], int lane, int &vi) {
+    constexpr int V = ROWS * BATCH;
+    constexpr int P = pow2_at_least(V);
+    constexpr int SHIFT = 5 - log2_of(P);
+    static_assert(P <= 32, "at most 32 totals per warp");
+    float v[P];
+#pragma unroll
+    for (int i = 0; i < P; ++i) v[i] = i < V ? acc[i / BATCH][i % BATCH] : 0.f;
+    const float tot = warp_reduce_scatter<P>(v, lane);
+    vi = lane >> SHIFT;
+    if ((lane & ((1 << SHIFT) - 1)) != 0 || vi >= V) vi = -1;
+    return tot;
+}
+
+// The task totals stored to dst[r * BATCH + b].
+template <int ROWS, int BATCH>
+__device__ __forceinline__ void store_task_totals(const float (&acc)[ROWS][BATCH], float *dst, int lane) {
+    int vi;
+    const float tot = task_total<ROWS, BATCH>(acc, lane, vi);
+    if (vi >= 0) dst[vi] = tot;
+}
+
 template <typename T, int BATCH, int ROWS, int U, bool VEC>
 __device__ __forceinline__ void accumulate(float (&acc)[ROWS][BATCH], const T *const (&arow)[ROWS],
                                            const float *xs, int chunk, int c0, int len, int lane) {
@@ -285,23 +341,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Params p) {
             if (active) accumulate<T, BATCH, ROWS, U, VEC>(acc, arow, xs, p.chunk, c0, len, lane);
         }
         if (active) {
-#pragma unroll
-            for (int r = 0; r < ROWS; ++r)
-#pragma unroll
-                for (int b = 0; b < BATCH; ++b) {
-                    float s = acc[r][b];
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
-                    acc[r][b] = s;
-                }
-            // every lane now holds every total; lane (r * BATCH + b) stores one
-#pragma unroll
-            for (int r = 0; r < ROWS; ++r)
-#pragma unroll
-                for (int b = 0; b < BATCH; ++b)
-                    if (lane == (r * BATCH + b) % 32 && row0 + r < r_end)
-                        p.y[static_cast<long long>(b) * p.ldy + row0 + r] =
-                            apply_epilogue(acc[r][b], p.bias, row0 + r, p.act);
+            int vi;
+            const float tot = task_total<ROWS, BATCH>(acc, lane, vi);
+            if (vi >= 0) {
+                const int r = vi / BATCH, b = vi - r * BATCH;
+                if (row0 + r < r_end)
+                    p.y[static_cast<long long>(b) * p.ldy + row0 + r] = apply_epilogue(tot, p.bias, row0 + r, p.act);
+            }
         }
     }
 }
@@ -403,24 +449,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const Params p
                     for (int b = 0; b < BATCH; ++b) acc[r][b] = fmaf(a, xs[b * p.chunk + jt], acc[r][b]);
                 }
             }
+            int vi;
+            const float tot = task_total<ROWS, BATCH>(acc, lane, vi);
+            if (vi >= 0) {
+                const int r = vi / BATCH, b = vi - r * BATCH;
+                const int row = row_of(t, r);
+                if (row < r_end) p.y[static_cast<long long>(b) * p.ldy + row] = apply_epilogue(tot, p.bias, row, p.act);
+            }
 #pragma unroll
             for (int r = 0; r < ROWS; ++r)
 #pragma unroll
-                for (int b = 0; b < BATCH; ++b) {
-                    float s = acc[r][b];
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
-                    acc[r][b] = s;
-                }
-#pragma unroll
-            for (int r = 0; r < ROWS; ++r)
-#pragma unroll
-                for (int b = 0; b < BATCH; ++b) {
-                    const int row = row_of(t, r);
-                    if (lane == (r * BATCH + b) % 32 && row < r_end)
-                        p.y[static_cast<long long>(b) * p.ldy + row] = apply_epilogue(acc[r][b], p.bias, row, p.act);
-                    acc[r][b] = 0.f;
-                }
+                for (int b = 0; b < BATCH; ++b) acc[r][b] = 0.f;
         }
     }
 }
@@ -536,16 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_split_kernel(const Params p)
                 }
             }
         }
-        float *dst = part + static_cast<long long>(task) * ROWS * BATCH;
-#pragma unroll
-        for (int r = 0; r < ROWS; ++r)
-#pragma unroll
-            for (int b = 0; b < BATCH; ++b) {
-                float v = acc[r][b];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-                if (lane == (r * BATCH + b) % 32) dst[r * BATCH + b] = v;
-            }
+        store_task_totals<ROWS, BATCH>(acc, part + static_cast<long long>(task) * ROWS * BATCH, lane);
     }
     __syncthreads();
     for (int idx = threadIdx.x; idx < rows * BATCH; idx += kThreads) {
@@ -692,16 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_cluster_kernel(const Params 
                 for (int b = 0; b < BATCH; ++b) acc[r][b] = fmaf(a, xs[b * p.chunk + jt], acc[r][b]);
             }
         }
-        float *dst = part + static_cast<long long>(task) * ROWS * BATCH;
-#pragma unroll
-        for (int r = 0; r < ROWS; ++r)
-#pragma unroll
-            for (int b = 0; b < BATCH; ++b) {
-                float v = acc[r][b];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-                if (lane == (r * BATCH + b) % 32) dst[r * BATCH + b] = v;
-            }
+        store_task_totals<ROWS, BATCH>(acc, part + static_cast<long long>(task) * ROWS * BATCH, lane);
     }
     __syncthreads();
     // this CTA's partial per (row, vector): its segments added in order
