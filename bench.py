@@ -287,18 +287,21 @@ def gpu_arm(args, rank, world, local_rank):
     bf16_peak = peaks.get("bf16_tflops_sustained" if long_region else "bf16_tflops")
     hbm_peak = peaks.get("hbm_gbs")
     tc_files = ["gemm_tc.cu", "ptx.cuh"]
-    gv_files = ["gemv.cu", "ptx.cuh"]
+    gv_files = ["gemv.cu", "gemv_kernels.cuh", "ptx.cuh"]
+    gemm_kernel = ("tc_gemm_pair_kernel (CTA pair, 256x256 tile)" if plan.get("cluster") == 2
+                   else f"tc_gemm_kernel<bf16, BN={plan.get('bn')}>")
+    gemv_kernel = {1: "gemv_stream_kernel<batch=1>", 4: "gemv_split_kernel"}.get(vplan.get("bm"), "gemv_kernel")
     roofline = {"bound": "tensor", "achieved": round(gemm_tflops / world, 1), "peak": bf16_peak,
                 "unit": "TFLOP/s", "frac": round(gemm_tflops / world / bf16_peak, 4),
                 "traffic": committed_traffic("gemm_bf16_8192", tc_files),
                 "peak_source": f"{peak_src} bf16 {peak_kind}",
-                "algorithmic_flops_per_launch": flops, "kernel": "tc_gemm_kernel<bf16>",
+                "algorithmic_flops_per_launch": flops, "kernel": gemm_kernel,
                 "plan": plan}
     gemv_roofline = {"bound": "hbm", "achieved": round(v1_gbs / world, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(v1_gbs / world / hbm_peak, 4),
                      "traffic": committed_traffic("gemv_f32_4096_b1", gv_files),
                      "peak_source": f"{peak_src} hbm copy", "algorithmic_bytes_per_launch": v1_bytes,
-                     "kernel": "gemv_kernel<1>", "plan": vplan}
+                     "kernel": gemv_kernel, "plan": vplan}
 
     result = {
         "metric": METRIC, "value": round(gemm_tflops, 1), "unit": "TFLOP/s", "n_gpus": world,
