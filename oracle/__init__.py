@@ -62,6 +62,8 @@ def _bind(lib):
     lib.oracle_gemv_f64.restype = ci
     lib.oracle_bias_act_f64.argtypes = [i64, i64, dp, i64, dp, ci, ci]
     lib.oracle_bias_act_f64.restype = ci
+    lib.oracle_conv2d_f64.argtypes = [i64] * 13 + [dp, dp, dp, dp, ci]
+    lib.oracle_conv2d_f64.restype = ci
     lib.oracle_threads_default.argtypes = []
     lib.oracle_threads_default.restype = ci
     return lib
@@ -161,3 +163,41 @@ def dense_vector(A, x, bias=None, act="none", lib=None):
     """act(A @ x + bias), bias per output row (one fully connected layer)."""
     y, E = gemv(A, x, lib=lib)
     return bias_act(y, bias, False, act, lib=lib), E
+
+
+def _pair(v):
+    return (int(v), int(v)) if np.isscalar(v) else (int(v[0]), int(v[1]))
+
+
+def conv2d(X, Wt, stride=1, pad=0, dil=1, threads: int = 0, with_E: bool = True, lib=None):
+    """Y = conv2d(X, Wt) in FP64 from the definition (zero padding), and E.
+
+    X: N x H x W x C (channels last); Wt: KH x KW x C x CO; Y: N x OH x OW x CO.
+    stride, pad, dil: an int or an (h, w) pair.
+    """
+    lib = lib or load()
+    X, Wt = _as_f64(X), _as_f64(Wt)
+    if X.ndim != 4 or Wt.ndim != 4 or X.shape[3] != Wt.shape[2]:
+        raise ValueError(f"shape mismatch {X.shape} * {Wt.shape}")
+    N, H, W, C = X.shape
+    KH, KW, _, CO = Wt.shape
+    (sh, sw), (ph, pw), (dh, dw) = _pair(stride), _pair(pad), _pair(dil)
+    OH = (H + 2 * ph - dh * (KH - 1) - 1) // sh + 1
+    OW = (W + 2 * pw - dw * (KW - 1) - 1) // sw + 1
+    if OH < 1 or OW < 1:
+        raise ValueError("kernel window larger than the padded image")
+    Y = np.empty((N, OH, OW, CO), dtype=np.float64)
+    E = np.empty((N, OH, OW, CO), dtype=np.float64) if with_E else None
+    rc = lib.oracle_conv2d_f64(N, H, W, C, CO, KH, KW, sh, sw, ph, pw, dh, dw, _ptr(X), _ptr(Wt), _ptr(Y),
+                               _ptr(E) if with_E else None, int(threads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_conv2d_f64 returned {rc}")
+    return (Y, E) if with_E else Y
+
+
+def conv_layer(X, Wt, bias=None, act="none", stride=1, pad=0, dil=1, threads=0, lib=None):
+    """act(conv2d(X, Wt) + bias), one bias per output channel."""
+    Y, E = conv2d(X, Wt, stride, pad, dil, threads=threads, lib=lib)
+    shape = Y.shape
+    out = bias_act(Y.reshape(-1, shape[3]), bias, True, act, lib=lib).reshape(shape)
+    return out, E

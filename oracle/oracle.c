@@ -29,6 +29,18 @@
  * with one bias per output column for the GEMM (C = X * W^T, a batch of
  * inputs in the rows of X) and one per output row for the GEMV (y = W x).
  *
+ * A convolutional layer is reduced to a matrix product by the pages
+ * ("GPU Matrix Multiplication: Tiling and Shared Memory", closing section:
+ * convolutions map to matrix multiplication through im2col; "Matrix
+ * Operations", introduction). The oracle does not take that route: it
+ * computes the convolution from its definition, a sum over the kernel window
+ * of input times weight with zero padding outside the image,
+ *
+ *   Y[n][oh][ow][co] = sum_{kh, kw, ci} X[n][oh*sh - ph + kh*dh]
+ *                                       [ow*sw - pw + kw*dw][ci] * W[kh][kw][ci][co],
+ *
+ * taken kh, then kw, then ci ascending, one FP64 accumulator per output.
+ *
  * Every matrix is row-major with an explicit leading dimension (the pages
  * index A[row*K + k], B[k*N + col], C[row*N + col]; a leading dimension
  * larger than the row length only skips padding).
@@ -175,5 +187,92 @@ int oracle_bias_act_f64(int64_t M, int64_t N, double *C, int64_t ldc,
             C[i * ldc + j] = v;
         }
     }
+    return 0;
+}
+
+typedef struct {
+    int64_t row_begin, row_end;   /* rows of the output = (n, oh) pairs */
+    int64_t H, W, C, CO, KH, KW, sh, sw, ph, pw, dh, dw, OH, OW;
+    const double *X, *Wt;
+    double *Y, *E;
+} conv_job;
+
+static void conv_rows(const conv_job *j)
+{
+    for (int64_t r = j->row_begin; r < j->row_end; ++r) {
+        const int64_t n = r / j->OH, oh = r % j->OH;
+        for (int64_t ow = 0; ow < j->OW; ++ow) {
+            double *y = j->Y + ((n * j->OH + oh) * j->OW + ow) * j->CO;
+            double *e = j->E ? j->E + ((n * j->OH + oh) * j->OW + ow) * j->CO : NULL;
+            for (int64_t co = 0; co < j->CO; ++co) {
+                double sum = 0.0, mag = 0.0;
+                for (int64_t kh = 0; kh < j->KH; ++kh) {
+                    const int64_t ih = oh * j->sh - j->ph + kh * j->dh;
+                    if (ih < 0 || ih >= j->H) continue;   /* zero padding */
+                    for (int64_t kw = 0; kw < j->KW; ++kw) {
+                        const int64_t iw = ow * j->sw - j->pw + kw * j->dw;
+                        if (iw < 0 || iw >= j->W) continue;
+                        const double *x = j->X + ((n * j->H + ih) * j->W + iw) * j->C;
+                        const double *w = j->Wt + (kh * j->KW + kw) * j->C * j->CO + co;
+                        for (int64_t ci = 0; ci < j->C; ++ci) {
+                            const double p = x[ci] * w[ci * j->CO];
+                            sum += p;
+                            mag += fabs(p);
+                        }
+                    }
+                }
+                y[co] = sum;
+                if (e) e[co] = mag;
+            }
+        }
+    }
+}
+
+static void *conv_thread(void *arg)
+{
+    conv_rows((const conv_job *)arg);
+    return NULL;
+}
+
+int oracle_conv2d_f64(int64_t N, int64_t H, int64_t W, int64_t C, int64_t CO,
+                      int64_t KH, int64_t KW, int64_t sh, int64_t sw, int64_t ph, int64_t pw,
+                      int64_t dh, int64_t dw, const double *X, const double *Wt,
+                      double *Y, double *E, int nthreads)
+{
+    if (N < 0 || H < 1 || W < 1 || C < 0 || CO < 0 || KH < 1 || KW < 1) return 1;
+    if (sh < 1 || sw < 1 || dh < 1 || dw < 1 || ph < 0 || pw < 0) return 1;
+    const int64_t span_h = H + 2 * ph - dh * (KH - 1) - 1, span_w = W + 2 * pw - dw * (KW - 1) - 1;
+    if (span_h < 0 || span_w < 0) return 1;
+    const int64_t OH = span_h / sh + 1, OW = span_w / sw + 1;
+    if (N == 0 || CO == 0) return 0;
+    if (!Y || (C > 0 && (!X || !Wt))) return 1;
+    const int64_t rows = N * OH;
+    const int t = resolve_threads(nthreads, rows);
+    conv_job *jobs = (conv_job *)calloc((size_t)t, sizeof(conv_job));
+    pthread_t *tid = (pthread_t *)calloc((size_t)t, sizeof(pthread_t));
+    if (!jobs || !tid) {
+        free(jobs);
+        free(tid);
+        return 2;
+    }
+    for (int i = 0; i < t; ++i) {
+        conv_job *j = &jobs[i];
+        j->row_begin = rows * i / t;
+        j->row_end = rows * (i + 1) / t;
+        j->H = H; j->W = W; j->C = C; j->CO = CO; j->KH = KH; j->KW = KW;
+        j->sh = sh; j->sw = sw; j->ph = ph; j->pw = pw; j->dh = dh; j->dw = dw;
+        j->OH = OH; j->OW = OW;
+        j->X = X; j->Wt = Wt; j->Y = Y; j->E = E;
+    }
+    int started = 0;
+    for (int i = 1; i < t; ++i) {
+        if (pthread_create(&tid[i], NULL, conv_thread, &jobs[i]) != 0) break;
+        started = i;
+    }
+    for (int i = started + 1; i < t; ++i) conv_rows(&jobs[i]);   /* threads that did not start */
+    conv_rows(&jobs[0]);
+    for (int i = 1; i <= started; ++i) pthread_join(tid[i], NULL);
+    free(jobs);
+    free(tid);
     return 0;
 }

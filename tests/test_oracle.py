@@ -198,7 +198,91 @@ def pin_bias_act_closed_forms(lib):
     assert np.array_equal(rows, np.array([[1.0, 1.0], [-2.0, -2.0], [3.0, 3.0]]))
 
 
-PINS = [pin_golden_dense_layer, pin_bias_act_closed_forms, pin_golden_gemm, pin_golden_gemv, pin_identity, pin_all_ones,
+def pin_conv_golden(lib):
+    """Hand-worked convolutions: padding, stride, dilation, a non-square
+    kernel and two input and output channels (catches swapped indices)."""
+    g = read_golden("conv2d_hand.txt")
+    X1 = g["X1"].reshape(1, 3, 3, 1)
+    W1 = g["W1"].reshape(2, 2, 1, 1)
+    Y, _ = oracle.conv2d(X1, W1, lib=lib)
+    assert np.array_equal(Y[0, :, :, 0], g["Y1_valid"])
+    Y, _ = oracle.conv2d(X1, W1, stride=2, pad=1, lib=lib)
+    assert np.array_equal(Y[0, :, :, 0], g["Y1_s2p1"])
+    X2 = np.stack([g["X2c0"], g["X2c1"]], axis=-1)[None]
+    W2 = np.stack([g["W2k0"], g["W2k1"]])[:, None]          # KH=2, KW=1, C=2, CO=2
+    Y, E = oracle.conv2d(X2, W2, lib=lib)
+    assert Y.shape == (1, 1, 3, 2)
+    assert np.array_equal(Y[0, 0], g["Y2"]) and np.array_equal(E[0, 0], g["E2"])
+    X3 = np.arange(1, 17, dtype=np.float64).reshape(1, 4, 4, 1)
+    Y, _ = oracle.conv2d(X3, W1, dil=2, lib=lib)
+    assert np.array_equal(Y[0, :, :, 0], g["Y3"])
+
+
+def pin_conv_1x1_is_gemm(lib):
+    """A 1x1 kernel at stride 1 is the matrix product of pixels x channels
+    with the C x CO weight matrix (the GEMM, a separate loop nest); same
+    ascending channel order, so bit-identical."""
+    rng = np.random.default_rng(30)
+    X = rng.uniform(-1, 1, (2, 5, 7, 6))
+    Wt = rng.uniform(-1, 1, (1, 1, 6, 4))
+    Y, E = oracle.conv2d(X, Wt, lib=lib)
+    C, Eg = oracle.gemm(X.reshape(-1, 6), Wt.reshape(6, 4), lib=lib)
+    assert np.array_equal(Y.reshape(-1, 4), C) and np.array_equal(E.reshape(-1, 4), Eg)
+
+
+def pin_conv_vs_library_correlate(lib):
+    """Against scipy's 2-D cross-correlation, one (input, output) channel pair
+    at a time: stride by subsampling the stride-1 result, padding by padding
+    the image, dilation by spreading the kernel with zeros."""
+    signal = pytest.importorskip("scipy.signal")
+    rng = np.random.default_rng(31)
+    for (H, W_, C, CO, KH, KW, s, p, d) in [(7, 9, 3, 2, 3, 2, 1, 0, 1), (8, 6, 2, 3, 3, 3, 2, 1, 1),
+                                             (9, 9, 2, 2, 2, 3, 1, 2, 2), (6, 11, 1, 2, 1, 4, 3, 1, 1)]:
+        X = rng.uniform(-1, 1, (2, H, W_, C))
+        Wt = rng.uniform(-1, 1, (KH, KW, C, CO))
+        Y, E = oracle.conv2d(X, Wt, stride=s, pad=p, dil=d, lib=lib)
+        Kd = np.zeros((d * (KH - 1) + 1, d * (KW - 1) + 1, C, CO))
+        Kd[::d, ::d] = Wt
+        for n in range(2):
+            for co in range(CO):
+                ref = sum(signal.correlate2d(np.pad(X[n, :, :, ci], p), Kd[:, :, ci, co], mode="valid")
+                          for ci in range(C))[::s, ::s]
+                assert ref.shape == Y.shape[1:3]
+                assert np.all(np.abs(Y[n, :, :, co] - ref) <= 4 * KH * KW * C * 2.0 ** -53 * E[n, :, :, co])
+
+
+def pin_conv_delta_kernel_shifts(lib):
+    """A kernel that is one at (kh0, kw0, ci0 -> co0) and zero elsewhere copies
+    channel ci0, shifted by the tap, into output channel co0 (zeros where the
+    tap falls in the padding); every other output channel is zero."""
+    rng = np.random.default_rng(32)
+    X = rng.uniform(-1, 1, (1, 5, 6, 3))
+    Wt = np.zeros((3, 3, 3, 2))
+    Wt[2, 0, 1, 1] = 1.0
+    Y, _ = oracle.conv2d(X, Wt, pad=1, lib=lib)
+    assert np.all(Y[..., 0] == 0)
+    want = np.zeros((5, 6))
+    want[:4, 1:] = X[0, 1:, :5, 1]        # output (oh, ow) reads input (oh + 1, ow - 1)
+    assert np.array_equal(Y[0, :, :, 1], want)
+
+
+def pin_conv_magnitude(lib):
+    """E >= |Y|; E == Y for non-negative operands; all-ones counts the taps
+    inside the image times C."""
+    rng = np.random.default_rng(33)
+    X = rng.uniform(-1, 1, (1, 6, 5, 2))
+    Wt = rng.uniform(-1, 1, (3, 2, 2, 3))
+    Y, E = oracle.conv2d(X, Wt, stride=(2, 1), pad=(1, 2), lib=lib)
+    assert np.all(E >= np.abs(Y))
+    Yp, Ep = oracle.conv2d(np.abs(X), np.abs(Wt), stride=(2, 1), pad=(1, 2), lib=lib)
+    assert np.array_equal(Yp, Ep)
+    Y1, _ = oracle.conv2d(np.ones((1, 4, 4, 3)), np.ones((3, 3, 3, 1)), pad=1, lib=lib)
+    # interior outputs see 9 taps, edges 6, corners 4
+    assert np.array_equal(Y1[0, :, :, 0], 3 * np.array([[4, 6, 6, 4], [6, 9, 9, 6], [6, 9, 9, 6], [4, 6, 6, 4]]))
+
+
+PINS = [pin_conv_golden, pin_conv_1x1_is_gemm, pin_conv_vs_library_correlate, pin_conv_delta_kernel_shifts,
+        pin_conv_magnitude, pin_golden_dense_layer, pin_bias_act_closed_forms, pin_golden_gemm, pin_golden_gemv, pin_identity, pin_all_ones,
         pin_small_integers_exact, pin_exact_rational, pin_rank_one,
         pin_gemv_is_gemm_with_one_column, pin_magnitude, pin_vs_library_matmul,
         pin_leading_dimensions, pin_empty_sum, pin_thread_invariance]

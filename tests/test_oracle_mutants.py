@@ -44,6 +44,20 @@ MUTANTS = {
     "bias_subtracted": [("if (bias) v += bias_per_column ? bias[j] : bias[i];",
                          "if (bias) v -= bias_per_column ? bias[j] : bias[i];")],
     "relu_as_abs": [("if (act == 1 && v < 0.0) v = 0.0;", "if (act == 1 && v < 0.0) v = -v;")],
+    "conv_kernel_axes_swapped": [("const double *w = j->Wt + (kh * j->KW + kw) * j->C * j->CO + co;",
+                                  "const double *w = j->Wt + (kw * j->KH + kh) * j->C * j->CO + co;")],
+    "conv_padding_ignored": [("const int64_t ih = oh * j->sh - j->ph + kh * j->dh;",
+                              "const int64_t ih = oh * j->sh + kh * j->dh;")],
+    "conv_column_stride_ignored": [("const int64_t iw = ow * j->sw - j->pw + kw * j->dw;",
+                                    "const int64_t iw = ow - j->pw + kw * j->dw;")],
+    "conv_row_dilation_ignored": [("const int64_t ih = oh * j->sh - j->ph + kh * j->dh;",
+                                   "const int64_t ih = oh * j->sh - j->ph + kh;")],
+    "conv_weights_as_co_ci": [("const double *w = j->Wt + (kh * j->KW + kw) * j->C * j->CO + co;",
+                               "const double *w = j->Wt + (kh * j->KW + kw) * j->C * j->CO + co * j->C;"),
+                              ("const double p = x[ci] * w[ci * j->CO];", "const double p = x[ci] * w[ci];")],
+    "conv_column_bound_off_by_one": [("if (iw < 0 || iw >= j->W) continue;", "if (iw < 0 || iw > j->W) continue;")],
+    "conv_E_without_abs": [("sum += p;\n                            mag += fabs(p);",
+                            "sum += p;\n                            mag += p;")],
     "relu_before_bias": [("            double v = C[i * ldc + j];\n            if (bias) v += bias_per_column ? bias[j] : bias[i];\n            if (act == 1 && v < 0.0) v = 0.0;",
                           "            double v = C[i * ldc + j];\n            if (act == 1 && v < 0.0) v = 0.0;\n            if (bias) v += bias_per_column ? bias[j] : bias[i];")],
 }
