@@ -451,6 +451,33 @@ def sweep(dev, stream, peaks, l2):
                     "ms": round(ms, 4), "TFLOP/s": round(tf, 2), "peak": bf16_peak, "peak_name": "bf16 burst",
                     "frac": round(tf / bf16_peak, 4)})
 
+    def conv_cfg(name, N, H, W, C, CO, KH, KW, st, pd, iters):
+        g = PCG32(20 + C + CO)
+        X = torch.from_numpy(g.normal_bf16((N, H, W, C)).view(np.int16)).to(dev)
+        Wt = torch.from_numpy(g.normal_bf16((KH, KW, C, CO), (KH * KW * C) ** -0.5).view(np.int16)).to(dev)
+        OH, OW = gtg.conv_out_size(H, W, KH, KW, st, pd)
+        Y = torch.empty((N, OH, OW, CO), device=dev)
+
+        def call(i):
+            rc = gtg.conv2d_nhwc("bf16", N, H, W, C, CO, KH, KW, st, st, pd, pd, 1, 1, X.data_ptr(), Wt.data_ptr(),
+                                 Y.data_ptr(), None, sh)
+            assert rc == gtg.GTG_OK, rc
+
+        ms = time_launches(call, iters, stream)
+        M, K = N * OH * OW, KH * KW * C
+        tf = 2.0 * M * K * CO / (ms * 1e-3) / 1e12
+        direct = KH == 1 and KW == 1 and st == 1 and pd == 0
+        out.append({"config": name, "path": "bf16 conv (im2col + GEMM)" if not direct else "bf16 conv (GEMM on X)",
+                    "gemm_shape": [M, CO, K], "ms": round(ms, 4), "TFLOP/s": round(tf, 2), "peak": bf16_peak,
+                    "peak_name": "bf16 burst", "frac": round(tf / bf16_peak, 4),
+                    "im2col_bytes": 0 if direct else M * ((K + 7) // 8 * 8) * 2})
+
+    conv_cfg("f4: bf16 conv 3x3 64->64, 56x56, batch 32, pad 1", 32, 56, 56, 64, 64, 3, 3, 1, 1, 20)
+    conv_cfg("f4: bf16 conv 3x3 256->256, 14x14, batch 64, pad 1", 64, 14, 14, 256, 256, 3, 3, 1, 1, 20)
+    conv_cfg("f4: bf16 conv 1x1 256->1024, 14x14, batch 64", 64, 14, 14, 256, 1024, 1, 1, 1, 0, 20)
+    conv_cfg("f4: bf16 conv 7x7/2 3->64, 224x224, batch 16, pad 3", 16, 224, 224, 3, 64, 7, 7, 2, 3, 10)
+    torch.cuda.empty_cache()
+
     batched_cfg("f2: bf16 strided batch 16 x 2048^3", 16, 2048, 2048, 2048, 20)
     batched_cfg("f2: bf16 strided batch 256 x 512x512x512", 256, 512, 512, 512, 50)
     batched_cfg("f2: bf16 strided batch 64 x 1024x1024x256, shared B", 64, 1024, 1024, 256, 50, shared_B=True)

@@ -64,6 +64,7 @@ SIGNATURES = {
     "gemm_strided_batched": (_int, [_int, _i64, _i64, _i64, _ptr, _i64, _i64, _ptr, _i64, _i64, _ptr, _i64, _i64,
                                     _i64, _ep, _ptr]),
     "gemv_f32_ex": (_int, [_i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _int, _ep, _ptr]),
+    "conv2d_nhwc": (_int, [_int] + [_i64] * 13 + [_ptr, _ptr, _ptr, _ep, _ptr]),
     "gemv_bf16": (_int, [_i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _int, _ptr]),
     "gemv_bf16_ex": (_int, [_i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _int, _ep, _ptr]),
     "gtg_ablation_gemm_f32": (_int, [_int, _i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr]),
@@ -179,6 +180,23 @@ def gemv_bf16(M, N, A, lda, x, ldx, y, ldy, batch, stream=0) -> int:
 
 def gemv_bf16_ex(M, N, A, lda, x, ldx, y, ldy, batch, ep=None, stream=0) -> int:
     return lib().gemv_bf16_ex(M, N, A, lda, x, ldx, y, ldy, batch, ctypes.byref(ep) if ep else None, stream)
+
+
+def conv2d_nhwc(precision, N, H, W, C, CO, KH, KW, stride_h, stride_w, pad_h, pad_w, dil_h, dil_w, X, Wt, Y,
+                ep=None, stream=0) -> int:
+    prec = PREC[precision] if isinstance(precision, str) else precision
+    return lib().conv2d_nhwc(prec, N, H, W, C, CO, KH, KW, stride_h, stride_w, pad_h, pad_w, dil_h, dil_w, X, Wt, Y,
+                             ctypes.byref(ep) if ep else None, stream)
+
+
+def conv_out_size(H, W, KH, KW, stride=1, pad=0, dil=1):
+    """(OH, OW) of conv2d_nhwc for these sizes."""
+    (sh, sw), (ph, pw), (dh, dw) = _pair(stride), _pair(pad), _pair(dil)
+    return (H + 2 * ph - dh * (KH - 1) - 1) // sh + 1, (W + 2 * pw - dw * (KW - 1) - 1) // sw + 1
+
+
+def _pair(v):
+    return (int(v), int(v)) if isinstance(v, int) else (int(v[0]), int(v[1]))
 
 
 ABLATION_GEMM = {"naive16": 0, "naive32": 1, "tiled16": 2, "tiled32": 3}
@@ -368,3 +386,50 @@ def sync_status(stream=None) -> None:
     """Wait for the stream and raise GtgError if a kernel reported a device-side failure."""
     st = gtg_sync_status(_stream_handle(stream))
     _check(st, "device status")
+
+
+def conv2d(X, Wt, stride=1, pad=0, dil=1, precision=None, out=None, stream=None, bias=None, activation="none"):
+    """A convolutional layer: Y = act(conv(X, Wt) + bias) through conv2d_nhwc.
+
+    X: (N, H, W, C) channels last; Wt: (KH, KW, C, CO); Y: (N, OH, OW, CO)
+    float32. precision defaults to the tensors' type ("f32" for float32,
+    "bf16" / "f16" for bfloat16 / float16); "tf32" runs float32 tensors on
+    the TF32 tensor path. `bias` holds CO float32 values (one per output
+    channel). Host tensors are copied in and the result copied back.
+    """
+    torch = _torch()
+    kinds = {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16"}
+    if X.dtype not in kinds or Wt.dtype != X.dtype:
+        raise TypeError("conv2d takes float32, bfloat16 or float16 X and Wt of the same type")
+    prec = precision or kinds[X.dtype]
+    if (prec in ("f32", "tf32")) != (X.dtype == torch.float32) or (prec in ("bf16", "f16") and kinds[X.dtype] != prec):
+        raise TypeError(f"precision {prec} does not match tensors of type {X.dtype}")
+    if X.dim() != 4 or Wt.dim() != 4 or X.shape[3] != Wt.shape[2]:
+        raise ValueError(f"shape mismatch {tuple(X.shape)} * {tuple(Wt.shape)}")
+    N, H, W, C = X.shape
+    KH, KW, _, CO = Wt.shape
+    (sh, sw), (ph, pw), (dh, dw) = _pair(stride), _pair(pad), _pair(dil)
+    OH, OW = conv_out_size(H, W, KH, KW, (sh, sw), (ph, pw), (dh, dw))
+    host = not X.is_cuda
+    dX = (X.to("cuda", non_blocking=True) if host else X).contiguous()
+    dW = (Wt.to("cuda", non_blocking=True) if host else Wt).contiguous()
+    if out is not None and not host:
+        Y = out
+    else:
+        Y = torch.empty((N, OH, OW, CO), dtype=torch.float32, device=dX.device)
+    if not Y.is_contiguous() or tuple(Y.shape) != (N, OH, OW, CO):
+        raise ValueError("out must be a contiguous (N, OH, OW, CO) float32 tensor")
+    dbias = _device_bias(bias, CO, dX.device)
+    ep = epilogue(dbias.data_ptr() if dbias is not None else 0, activation)
+    st = conv2d_nhwc(prec, N, H, W, C, CO, KH, KW, sh, sw, ph, pw, dh, dw, dX.data_ptr(), dW.data_ptr(),
+                     Y.data_ptr(), ep, _stream_handle(stream))
+    _check(st, "conv2d_nhwc")
+    if host:
+        res = torch.empty_like(Y, device="cpu", pin_memory=X.is_pinned())
+        res.copy_(Y, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        if out is not None:
+            out.copy_(res)
+            return out
+        return res
+    return Y

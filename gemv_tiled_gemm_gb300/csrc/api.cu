@@ -309,6 +309,35 @@ gtg_status gemv_bf16_ex(int64_t M, int64_t N, const gtg_bf16 *A, int64_t lda, co
     return run_gemv(g, stream);
 }
 
+static gtg_status validate_conv(ConvArgs &c) {
+    if (c.prec < GTG_PREC_F32 || c.prec > GTG_PREC_F16) return GTG_ERR_INVALID_VALUE;
+    c.elem = c.prec == GTG_PREC_BF16 || c.prec == GTG_PREC_F16 ? 2 : 4;
+    if (c.N < 0 || c.H < 1 || c.W < 1 || c.C < 1 || c.CO < 0 || c.KH < 1 || c.KW < 1) return GTG_ERR_INVALID_VALUE;
+    if (c.sh < 1 || c.sw < 1 || c.dh < 1 || c.dw < 1 || c.ph < 0 || c.pw < 0) return GTG_ERR_INVALID_VALUE;
+    const int64_t lim = INT32_MAX;
+    if (c.H > lim || c.W > lim || c.C > lim || c.CO > lim || c.KH > lim || c.KW > lim || c.sh > lim ||
+        c.sw > lim || c.dh > lim || c.dw > lim || c.ph > lim || c.pw > lim || c.N > lim)
+        return GTG_ERR_INVALID_VALUE;
+    const int64_t span_h = c.H + 2 * c.ph - c.dh * (c.KH - 1) - 1, span_w = c.W + 2 * c.pw - c.dw * (c.KW - 1) - 1;
+    if (span_h < 0 || span_w < 0) return GTG_ERR_INVALID_VALUE;   // the window does not fit the padded image
+    c.OH = span_h / c.sh + 1;
+    c.OW = span_w / c.sw + 1;
+    // the product's sizes: M = N*OH*OW rows, K = KH*KW*C
+    if (c.N * c.OH * c.OW > lim || c.KH * c.KW * c.C > lim) return GTG_ERR_INVALID_VALUE;
+    if (c.act != GTG_ACT_NONE && c.act != GTG_ACT_RELU) return GTG_ERR_INVALID_VALUE;
+    if (c.N == 0 || c.CO == 0) return GTG_OK;
+    if (!c.X || !c.Wt || !c.Y) return GTG_ERR_INVALID_VALUE;
+    if (reinterpret_cast<uintptr_t>(c.X) % c.elem || reinterpret_cast<uintptr_t>(c.Wt) % c.elem ||
+        reinterpret_cast<uintptr_t>(c.Y) % 4 || (c.bias && reinterpret_cast<uintptr_t>(c.bias) % 4))
+        return GTG_ERR_MISALIGNED;
+    const Span y = span_of(c.Y, c.N * c.OH * c.OW, c.CO, c.CO, 4);
+    if (overlaps(y, span_of(c.X, c.N * c.H * c.W, c.C, c.C, c.elem)) ||
+        overlaps(y, span_of(c.Wt, c.KH * c.KW * c.C, c.CO, c.CO, c.elem)) ||
+        (c.bias && overlaps(y, span_of(c.bias, 1, c.CO, c.CO, 4))))
+        return GTG_ERR_ALIAS;
+    return GTG_OK;
+}
+
 static GemmArgs with_epilogue(GemmArgs g, const gtg_epilogue *ep) {
     if (ep) {
         g.bias = ep->bias;
@@ -453,6 +482,49 @@ static gtg_status plan_gemv_impl(const GemvArgs &g, gtg_plan *plan) {
     }
     gemv_plan(dev, g, plan);
     return GTG_OK;
+}
+
+gtg_status conv2d_nhwc(int precision, int64_t N, int64_t H, int64_t W, int64_t C, int64_t CO, int64_t KH,
+                       int64_t KW, int64_t stride_h, int64_t stride_w, int64_t pad_h, int64_t pad_w, int64_t dil_h,
+                       int64_t dil_w, const void *X, const void *Wt, float *Y, const gtg_epilogue *ep,
+                       cudaStream_t stream) {
+    ConvArgs c;
+    c.prec = precision;
+    c.N = N; c.H = H; c.W = W; c.C = C; c.CO = CO; c.KH = KH; c.KW = KW;
+    c.sh = stride_h; c.sw = stride_w; c.ph = pad_h; c.pw = pad_w; c.dh = dil_h; c.dw = dil_w;
+    c.X = X; c.Wt = Wt; c.Y = Y;
+    if (ep) {
+        c.bias = ep->bias;
+        c.act = ep->activation;
+    }
+    gtg_status st = validate_conv(c);
+    if (st != GTG_OK || N == 0 || CO == 0) return st;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != GTG_OK) return st;
+    if (!(dev.cc_major == 10 && dev.cc_minor == 3)) return GTG_ERR_UNSUPPORTED;
+    const int64_t M = N * c.OH * c.OW, K = KH * KW * C;
+    // a 1x1 window at stride 1 without padding reads X itself as the patch matrix
+    const bool direct = KH == 1 && KW == 1 && stride_h == 1 && stride_w == 1 && pad_h == 0 && pad_w == 0;
+    const void *A = X;
+    int64_t lda = C;
+    void *P = nullptr;
+    if (!direct) {
+        lda = (K + 7) / 8 * 8;   // 16-byte aligned rows for the tensor-memory-access path
+        cudaError_t e = cudaMallocAsync(&P, static_cast<size_t>(M * lda * c.elem), stream);
+        if (e == cudaSuccess) e = im2col_launch(dev, c, P, lda, stream);
+        if (e != cudaSuccess) {
+            note_cuda_error(e);
+            if (P) cudaFreeAsync(P, stream);
+            return GTG_ERR_LAUNCH;
+        }
+        A = P;
+    }
+    GemmArgs g{precision, M, CO, K, A, lda, Wt, CO, Y, CO};
+    g.bias = c.bias;
+    g.act = c.act;
+    st = run_gemm(g, stream);
+    if (P) cudaFreeAsync(P, stream);   // stream-ordered: after the product has read it
+    return st;
 }
 
 gtg_status gtg_plan_gemv(int64_t M, int64_t N, const float *A, int64_t lda, const float *x, int64_t ldx,

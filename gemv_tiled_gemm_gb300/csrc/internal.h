@@ -45,6 +45,19 @@ struct GemvArgs {
     int a_elem = 4;              // bytes per element of A
 };
 
+// One convolutional layer after validation: X channels-last N x H x W x C,
+// weights KH x KW x C x CO, Y channels-last N x OH x OW x CO (FP32).
+struct ConvArgs {
+    int prec;                    // GTG_PREC_*
+    int elem;                    // bytes per element of X and the weights
+    int64_t N, H, W, C, CO, KH, KW, sh, sw, ph, pw, dh, dw, OH, OW;
+    const void *X;
+    const void *Wt;
+    float *Y;
+    const float *bias = nullptr; // CO entries or null
+    int act = 0;
+};
+
 // The epilogue applied to one FP32 result before it is stored.
 __host__ __device__ __forceinline__ float apply_epilogue(float v, const float *bias, int index, int act) {
     if (bias) v += bias[index];
@@ -86,6 +99,9 @@ cudaError_t epilogue_fill_launch(float *C, int64_t M, int64_t N, int64_t ldc, co
 cudaError_t ablation_gemm_launch(int variant, const GemmArgs &g, cudaStream_t stream);
 cudaError_t ablation_gemv_launch(int variant, const GemvArgs &g, cudaStream_t stream);
 bool grid_too_large(int64_t M, int64_t N, int tile);
+
+// ---- im2col (im2col.cu): the patch matrix P (N*OH*OW x KH*KW*C, ldp >= K)
+cudaError_t im2col_launch(const DeviceInfo &dev, const ConvArgs &c, void *P, int64_t ldp, cudaStream_t stream);
 
 // ---- GEMV (gemv.cu)
 void gemv_plan(const DeviceInfo &dev, const GemvArgs &g, gtg_plan *plan);

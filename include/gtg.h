@@ -287,6 +287,43 @@ GTG_API gtg_status gemv_bf16_ex(int64_t M, int64_t N, const gtg_bf16 *A, int64_t
                                 const gtg_epilogue *epilogue, cudaStream_t stream);
 
 /*
+ * conv2d_nhwc -- a convolutional layer as one matrix product: the im2col
+ * route that "GPU Matrix Multiplication: Tiling and Shared Memory" (closing
+ * section) and "Matrix Operations" (introduction) name for convolutions.
+ *
+ *   Y[n][oh][ow][co] = act(bias[co] + sum_{kh, kw, ci}
+ *       X[n][oh*stride_h - pad_h + kh*dil_h][ow*stride_w - pad_w + kw*dil_w][ci]
+ *       * Wt[kh][kw][ci][co])
+ *
+ * with input positions outside the image contributing zero (zero padding).
+ *   precision  GTG_PREC_F32, _TF32 (X, Wt FP32), _BF16 or _F16 (X, Wt 16-bit);
+ *              arithmetic and accumulation as gemm_<precision>
+ *   X          N x H x W x C, channels last, packed (device)
+ *   Wt         KH x KW x C x CO, packed: read row-major it is the
+ *              (KH*KW*C) x CO weight matrix (device)
+ *   Y          N x OH x OW x CO, channels last, packed, FP32, overwritten;
+ *              OH = (H + 2 pad_h - dil_h (KH - 1) - 1) / stride_h + 1 (floor),
+ *              OW likewise
+ *   epilogue   optional bias (CO values, one per output channel) and activation
+ * The call writes the patch matrix P (N*OH*OW x KH*KW*C, rows padded to a
+ * multiple of 8 elements) into a temporary from the device's stream-ordered
+ * memory pool, freed on the stream after the product; a 1x1 window with
+ * stride 1 and no padding needs none (X is P). Then Y = P * Wt through the
+ * GEMM kernels of gemm_<precision>.
+ * Errors: GTG_ERR_INVALID_VALUE for sizes < 1 (N, CO may be 0: nothing is
+ * done), strides or dilations < 1, negative padding, a window larger than the
+ * padded image, N*OH*OW or KH*KW*C above 2^31 - 1, an unknown precision or
+ * activation; GTG_ERR_MISALIGNED for element-misaligned pointers;
+ * GTG_ERR_ALIAS when Y overlaps X, Wt or the bias; GTG_ERR_LAUNCH when the
+ * temporary cannot be allocated or a launch fails.
+ */
+GTG_API gtg_status conv2d_nhwc(int precision, int64_t N, int64_t H, int64_t W, int64_t C, int64_t CO,
+                               int64_t KH, int64_t KW, int64_t stride_h, int64_t stride_w,
+                               int64_t pad_h, int64_t pad_w, int64_t dil_h, int64_t dil_w,
+                               const void *X, const void *Wt, float *Y,
+                               const gtg_epilogue *epilogue, cudaStream_t stream);
+
+/*
  * gemm_strided_batched -- `batch` independent products in one call ("Matrix
  * Operations", "Performance Considerations": processing several matrix
  * multiplications in parallel):

@@ -123,3 +123,17 @@ def test_epilogue_validation():
         assert fn(4, 4, 4, A, 4, B, 4, C, 4, gtg.epilogue(A + (1 << 20) + 2, "none")) == gtg.GTG_ERR_MISALIGNED
     assert gtg.gemv_f32_ex(4, 4, A, 4, B, 4, C, 4, 1, ep_bad_act) == E
     assert gtg.gemv_f32_ex(4, 4, A, 4, B, 4, C, 4, 1, gtg.epilogue(C + 8, "relu")) == gtg.GTG_ERR_ALIAS
+
+
+def test_conv_validation():
+    X, Wt, Y = A, B, C
+    f = gtg.conv2d_nhwc
+    E = gtg.GTG_ERR_INVALID_VALUE
+    assert f("bf16", 1, 4, 4, 8, 8, 5, 5, 1, 1, 0, 0, 1, 1, X, Wt, Y) == E      # window larger than the image
+    assert f("bf16", 1, 4, 4, 8, 8, 3, 3, 0, 1, 0, 0, 1, 1, X, Wt, Y) == E      # stride 0
+    assert f("bf16", 1, 4, 4, 8, 8, 3, 3, 1, 1, -1, 0, 1, 1, X, Wt, Y) == E     # negative padding
+    assert f("bf16", 1, 4, 4, 8, 8, 3, 3, 1, 1, 0, 0, 0, 1, X, Wt, Y) == E      # dilation 0
+    assert f(9, 1, 4, 4, 8, 8, 3, 3, 1, 1, 0, 0, 1, 1, X, Wt, Y) == E
+    assert f("bf16", 1, 4, 4, 8, 8, 3, 3, 1, 1, 0, 0, 1, 1, X + 1, Wt, Y) == gtg.GTG_ERR_MISALIGNED
+    assert f("f32", 1, 4, 4, 8, 8, 3, 3, 1, 1, 0, 0, 1, 1, X, Wt, X + 64) == gtg.GTG_ERR_ALIAS
+    assert f("bf16", 0, 4, 4, 8, 8, 3, 3, 1, 1, 0, 0, 1, 1, 0, 0, 0) == gtg.GTG_OK   # empty batch
