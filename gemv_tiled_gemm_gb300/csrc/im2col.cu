@@ -10,14 +10,18 @@
 // that position lies in the padding. Then Y (N x OH x OW x CO, channels last)
 // = P * B, the GEMM of the tensor-core or SIMT kernels.
 //
-// GB300 form: a warp per output pixel; each lane moves 16-byte chunks of
-// channels (8 BF16/FP16 or 4 FP32 values) when C allows, single elements
-// otherwise; consecutive lanes read consecutive chunks of one input pixel's
-// channels and write consecutive chunks of the row, so both sides coalesce.
-// The (kh, kw, channel) position of a lane's chunk advances by carries,
-// without a division per chunk. The kernel is bound by HBM writes of P
-// (the reads of X are mostly L2 hits: each input pixel is read KH*KW times).
+// GB300 form: a warp per output pixel (row of P); every lane writes whole
+// 16-byte chunks of the row (8 BF16/FP16 or 4 FP32 values), so a warp stores
+// 512 contiguous bytes per instruction. Each CTA first builds, in shared
+// memory, a table giving for every chunk (or, when C is not a multiple of the
+// chunk, every element) of a row its offset (dy, dx, channel) from the
+// window's corner; a row then needs one 32-bit decode of (n, oh, ow) and,
+// per chunk, one table read and one 16-byte load of 8 contiguous channels
+// (or 8 element gathers). The kernel is bound by HBM writes of P (the reads
+// of X are mostly L2 hits: each input pixel is read KH*KW times).
 #include <algorithm>
+#include <cstring>
+#include <type_traits>
 
 #include "internal.h"
 
@@ -72,6 +76,71 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) im2col_kernel(const Im2col 
     }
 }
 
+// One entry of the row table: the tap's row and column offsets from the
+// window corner (oh*sh - ph, ow*sw - pw) and the element offset of the value
+// from that corner pixel's first channel.
+struct Tap {
+    int dy_dx;   // dy in the high 16 bits, dx in the low 16 bits (both >= 0)
+    int off;     // (dy * W + dx) * C + channel
+};
+
+constexpr int kMaxTaps = 6144;   // 48 KB of table
+
+// G elements of ESZ bytes make one 16-byte output chunk. VEC: every chunk is
+// G contiguous channels of one tap (C % G == 0), read with one 16-byte load;
+// otherwise each of the G elements is gathered on its own.
+template <int ESZ, bool VEC>
+__global__ void __launch_bounds__(32 * kWarpsPerCta) im2col_table_kernel(const Im2col g, int K) {
+    constexpr int G = 16 / ESZ;
+    using E = typename std::conditional<ESZ == 2, uint16_t, float>::type;
+    extern __shared__ Tap tab[];
+    const int nchunks = (K + G - 1) / G;                 // 16-byte chunks per row (the last may run into padding)
+    const int ntab = VEC ? nchunks : K;
+    for (int t = threadIdx.x; t < ntab; t += blockDim.x) {
+        const int k = VEC ? t * G : t;
+        const int kh = k / (g.KW * g.C), r = k - kh * (g.KW * g.C);
+        const int kw = r / g.C, ci = r - kw * g.C;
+        const int dy = kh * g.dh, dx = kw * g.dw;
+        tab[t].dy_dx = (dy << 16) | dx;
+        tab[t].off = (dy * g.W + dx) * g.C + ci;
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int nwarps = gridDim.x * kWarpsPerCta;
+    const E *X = static_cast<const E *>(g.X);
+    for (int m = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5); m < g.M; m += nwarps) {
+        const int ow = m % g.OW, t = m / g.OW;
+        const int oh = t % g.OH, n = t / g.OH;
+        const int ih0 = oh * g.sh - g.ph, iw0 = ow * g.sw - g.pw;
+        // element index of the window corner (it may lie in the padding; only
+        // positions inside the image are read)
+        const long long corner = ((static_cast<long long>(n) * g.H + ih0) * g.W + iw0) * g.C;
+        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<char *>(g.P) + static_cast<long long>(m) * g.ldp * ESZ);
+        for (int q = lane; q < nchunks; q += 32) {
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if constexpr (VEC) {
+                const Tap tp = tab[q];
+                const int ih = ih0 + (tp.dy_dx >> 16), iw = iw0 + (tp.dy_dx & 0xFFFF);
+                if (ih >= 0 && ih < g.H && iw >= 0 && iw < g.W) v = *reinterpret_cast<const uint4 *>(X + (corner + tp.off));
+            } else {
+                E e[G];
+#pragma unroll
+                for (int j = 0; j < G; ++j) {
+                    const int k = q * G + j;
+                    e[j] = E{};
+                    if (k < K) {
+                        const Tap tp = tab[k];
+                        const int ih = ih0 + (tp.dy_dx >> 16), iw = iw0 + (tp.dy_dx & 0xFFFF);
+                        if (ih >= 0 && ih < g.H && iw >= 0 && iw < g.W) e[j] = X[corner + tp.off];
+                    }
+                }
+                memcpy(&v, e, 16);
+            }
+            dst[q] = v;
+        }
+    }
+}
+
 template <typename V, int VE>
 cudaError_t launch_typed(const DeviceInfo &dev, const Im2col &g, cudaStream_t stream) {
     const long long ctas = (g.M + kWarpsPerCta - 1) / kWarpsPerCta;
@@ -104,10 +173,29 @@ cudaError_t im2col_launch(const DeviceInfo &dev, const ConvArgs &c, void *P, int
     g.M = c.N * c.OH * c.OW;
     const int esz = c.elem;
     const int ve = 16 / esz;
-    // 16-byte chunks need C a multiple of the chunk and 16-byte aligned X and P rows
-    const bool vec = c.C % ve == 0 && (reinterpret_cast<uintptr_t>(c.X) & 15) == 0 &&
-                     (reinterpret_cast<uintptr_t>(P) & 15) == 0 && (ldp * esz) % 16 == 0;
-    if (vec) return esz == 2 ? launch_typed<uint4, 8>(dev, g, stream) : launch_typed<uint4, 4>(dev, g, stream);
+    const int K = static_cast<int>(c.KH * c.KW * c.C);
+    // the table kernel: 16-byte aligned rows of P and taps addressable in 32 bits
+    const bool vec = c.C % ve == 0 && (reinterpret_cast<uintptr_t>(c.X) & 15) == 0;
+    const int ntab = vec ? (K + ve - 1) / ve : K;
+    const bool table = (reinterpret_cast<uintptr_t>(P) & 15) == 0 && (ldp * esz) % 16 == 0 && ldp >= (K + ve - 1) / ve * ve &&
+                       ntab <= kMaxTaps && (c.KH - 1) * c.dh < 32768 && (c.KW - 1) * c.dw < 32768 &&
+                       ((c.KH - 1) * c.dh * c.W + (c.KW - 1) * c.dw + 1) * c.C < INT32_MAX;
+    if (table) {
+        const long long ctas = (g.M + kWarpsPerCta - 1) / kWarpsPerCta;
+        const int grid = static_cast<int>(std::min<long long>(ctas, static_cast<long long>(dev.sms) * 16));
+        const size_t smem = static_cast<size_t>(ntab) * sizeof(Tap);
+        if (esz == 2) {
+            if (vec) im2col_table_kernel<2, true><<<grid, 32 * kWarpsPerCta, smem, stream>>>(g, K);
+            else im2col_table_kernel<2, false><<<grid, 32 * kWarpsPerCta, smem, stream>>>(g, K);
+        } else {
+            if (vec) im2col_table_kernel<4, true><<<grid, 32 * kWarpsPerCta, smem, stream>>>(g, K);
+            else im2col_table_kernel<4, false><<<grid, 32 * kWarpsPerCta, smem, stream>>>(g, K);
+        }
+        return cudaGetLastError();
+    }
+    // otherwise: chunk by chunk with carries (very wide windows, unaligned buffers)
+    const bool vchunks = vec && (reinterpret_cast<uintptr_t>(P) & 15) == 0 && (ldp * esz) % 16 == 0;
+    if (vchunks) return esz == 2 ? launch_typed<uint4, 8>(dev, g, stream) : launch_typed<uint4, 4>(dev, g, stream);
     return esz == 2 ? launch_typed<uint16_t, 1>(dev, g, stream) : launch_typed<float, 1>(dev, g, stream);
 }
 
