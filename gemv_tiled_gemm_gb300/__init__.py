@@ -35,7 +35,7 @@ _i64, _ptr, _int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
 
 class GtgPlan(ctypes.Structure):
     _fields_ = [("kernel", _int), ("bm", _int), ("bn", _int), ("bk", _int), ("stages", _int),
-                ("grid", _int), ("threads", _int), ("smem", _int), ("cluster", _int)]
+                ("grid", _int), ("threads", _int), ("smem", _int), ("cluster", _int), ("splits", _int)]
 
     def as_dict(self) -> dict:
         d = {f: getattr(self, f) for f, _ in self._fields_}
@@ -79,6 +79,7 @@ SIGNATURES = {
     "gtg_plan_gemv_bf16": (_int, [_i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _int,
                              ctypes.POINTER(GtgPlan)]),
     "gtg_force_simt": (None, [_int]),
+    "gtg_force_gemm_splits": (None, [_int]),
     "gtg_set_wait_limit_ns": (None, [ctypes.c_uint64]),
     "gtg_test_drop_load": (None, [_int]),
     "gtg_version": (_int, []),
@@ -227,6 +228,11 @@ def last_cuda_error() -> str:
 
 def gtg_force_simt(force: bool) -> None:
     lib().gtg_force_simt(1 if force else 0)
+
+
+def gtg_force_gemm_splits(splits: int) -> None:
+    """Testing / tuning hook: split K of tensor-core GEMMs `splits` ways (0: planner's choice)."""
+    lib().gtg_force_gemm_splits(int(splits))
 
 
 def gtg_set_wait_limit_ns(ns: int) -> None:

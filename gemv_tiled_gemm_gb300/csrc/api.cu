@@ -259,8 +259,8 @@ gtg_status gemm_tf32_noalloc(int64_t M, int64_t N, int64_t K, const float *A, in
     if ((st = plan_gemm_impl(dev, g, &plan)) != GTG_OK) return st;
     if (plan.kernel == GTG_KERNEL_SIMT) {
         // one K split: the SIMT kernel then writes C directly and needs no workspace
-        plan.grid /= plan.stages;
-        plan.stages = 1;
+        plan.grid /= plan.splits;
+        plan.splits = 1;
     }
     cudaError_t e = cudaSuccess;
     switch (plan.kernel) {
@@ -546,6 +546,8 @@ void gtg_force_simt(int force) { g_force_simt.store(force ? 1 : 0); }
 void gtg_set_wait_limit_ns(uint64_t ns) { tc_set_wait_limit_ns(ns); }
 
 void gtg_test_drop_load(int slice) { tc_drop_next_load(slice); }
+
+void gtg_force_gemm_splits(int splits) { tc_force_splits(splits); }
 
 int gtg_version(void) { return 100; }
 

@@ -310,15 +310,7 @@ cudaError_t launch_one(const GemmArgs &g, int splits, cudaStream_t stream) {
         g.bias, g.act);
     e = cudaGetLastError();
     if (splits > 1) {
-        if (e == cudaSuccess) {
-            const long long quads = g.M * ((g.N + 3) / 4);
-            const unsigned blocks = static_cast<unsigned>(std::min<long long>((quads + 255) / 256, 8192));
-            // ws rows are N floats, 256-byte aligned base: 16-byte accesses need N % 4 == 0
-            const int vec = ((g.N & 3) == 0 && c_vec) ? 1 : 0;
-            split_reduce_kernel<<<blocks, 256, 0, stream>>>(ws, splits, static_cast<int>(g.M), static_cast<int>(g.N),
-                                                            g.C, g.ldc, vec, g.bias, g.act);
-            e = cudaGetLastError();
-        }
+        if (e == cudaSuccess) e = split_reduce_launch(ws, splits, g.M, g.N, g.C, g.ldc, g.bias, g.act, stream);
         const cudaError_t f = cudaFreeAsync(ws, stream);   // stream-ordered: after the reduction
         if (e == cudaSuccess) e = f;
     }
@@ -327,8 +319,8 @@ cudaError_t launch_one(const GemmArgs &g, int splits, cudaStream_t stream) {
 
 template <typename T, bool VEC>
 cudaError_t launch_typed(const GemmArgs &g, const gtg_plan &plan, cudaStream_t stream) {
-    if (plan.bm == 128) return launch_one<T, 128, 128, VEC>(g, plan.stages, stream);
-    return launch_one<T, 64, 64, VEC>(g, plan.stages, stream);
+    if (plan.bm == 128) return launch_one<T, 128, 128, VEC>(g, plan.splits, stream);
+    return launch_one<T, 64, 64, VEC>(g, plan.splits, stream);
 }
 
 bool vec_ok(const GemmArgs &g) {
@@ -341,7 +333,7 @@ bool vec_ok(const GemmArgs &g) {
 }  // namespace
 
 // Tile: 128 x 128 (8 warps) when there are enough such tiles for every SM,
-// else 64 x 64 (2 warps). Small grids then split K (plan->stages = splits)
+// else 64 x 64 (2 warps). Small grids then split K (plan->splits)
 // so that about six CTAs run on every SM, each split keeping at least two
 // 16-deep K slices; the partial products go through a workspace.
 void simt_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
@@ -376,7 +368,8 @@ void simt_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
         const int64_t k_per = (kslices + splits - 1) / splits;
         splits = (kslices + k_per - 1) / k_per;
     }
-    plan->stages = static_cast<int>(splits);
+    plan->stages = 2;   // double-buffered shared-memory slices
+    plan->splits = static_cast<int>(splits);
     plan->grid = static_cast<int>(tiles * splits);
 }
 
@@ -410,6 +403,18 @@ cudaError_t epilogue_fill_launch(float *C, int64_t M, int64_t N, int64_t ldc, co
     if (blocks > 4096) blocks = 4096;
     if (blocks < 1) blocks = 1;
     epilogue_fill_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(C, M, N, ldc, bias, per_column, act);
+    return cudaGetLastError();
+}
+
+cudaError_t split_reduce_launch(const float *ws, int splits, int64_t M, int64_t N, float *C, int64_t ldc,
+                                const float *bias, int act, cudaStream_t stream) {
+    const long long quads = M * ((N + 3) / 4);
+    const unsigned blocks = static_cast<unsigned>(std::min<long long>((quads + 255) / 256, 8192));
+    // ws is a pool allocation (256-byte aligned) of rows of N floats: 16-byte
+    // accesses need N % 4 == 0, and C a 16-byte aligned base and ldc % 4 == 0
+    const int vec = ((N & 3) == 0 && (reinterpret_cast<uintptr_t>(C) & 15) == 0 && (ldc & 3) == 0) ? 1 : 0;
+    split_reduce_kernel<<<blocks, 256, 0, stream>>>(ws, splits, static_cast<int>(M), static_cast<int>(N), C, ldc, vec,
+                                                    bias, act);
     return cudaGetLastError();
 }
 

@@ -83,6 +83,8 @@ struct TcParams {
     int M, N;
     int num_m, num_n, num_kb, num_tiles;   // num_tiles counts every item of a batch
     int tiles_per_batch;
+    int splits, kps;             // K split into `splits` ranges of kps slices (1: none)
+    int num_units;               // num_tiles * splits
     long long strideC;           // elements between the C matrices of consecutive batch items
     uint32_t idesc;              // instruction descriptor (A/B format: FP16 or BF16) of the 16-bit kernels
     int c_vec;                   // widest store for whole rows of a tile: 2 = 32 B, 1 = 16 B, 0 = 4 B
@@ -102,6 +104,31 @@ __device__ __forceinline__ void epilogue32(uint32_t (&r)[32], const TcParams &p,
         const float v = apply_epilogue(__uint_as_float(r[j]), in ? p.bias : nullptr, col + j, p.act);
         r[j] = __float_as_uint(v);
     }
+}
+
+// Work unit t of a launch: a tile (batch item bi, index tt within the item)
+// and its K-slice range [kb0, kb1). With p.splits > 1 (never together with a
+// batch) unit t is K range s = t / num_tiles of tile t % num_tiles and its
+// partial tile goes to slab s of the workspace (coff = s * strideC), to be
+// added in order by the split reduction.
+struct Unit {
+    int bi, tt, kb0, kb1;
+    long long coff;
+};
+
+__device__ __forceinline__ Unit unit_of(int t, const TcParams &p) {
+    Unit u;
+    int s = 0;
+    if (p.splits > 1) {
+        s = t / p.num_tiles;
+        t -= s * p.num_tiles;
+    }
+    u.bi = t / p.tiles_per_batch;
+    u.tt = t - u.bi * p.tiles_per_batch;
+    u.kb0 = s * p.kps;
+    u.kb1 = min(u.kb0 + p.kps, p.num_kb);
+    u.coff = static_cast<long long>(p.splits > 1 ? s : u.bi) * p.strideC;
+    return u;
 }
 
 __device__ __forceinline__ void tile_coords(int t, const TcParams &p, int &mb, int &nb) {
@@ -207,11 +234,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             uint32_t it = 0;  // slices issued so far
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            for (int t = blockIdx.x; ok && t < p.num_units; t += gridDim.x) {
                 int mb, nb;
-                const int bi = t / p.tiles_per_batch;
-                tile_coords(t - bi * p.tiles_per_batch, p, mb, nb);
-                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                const Unit u = unit_of(t, p);
+                const int bi = u.bi;
+                tile_coords(u.tt, p, mb, nb);
+                for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
                     const int s = static_cast<int>(it % S::STAGES);
                     const uint32_t ph = (it / S::STAGES) & 1u;
                     if (!wait_bar(empty_bar(s), ph ^ 1u, abort_flag, p)) {
@@ -247,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t it = 0;
             int local = 0;
             bool ok = true, issued = false;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++local) {
+            for (int t = blockIdx.x; ok && t < p.num_units; t += gridDim.x, ++local) {
                 const int acc = local & 1;
                 const uint32_t aph = (static_cast<uint32_t>(local) >> 1) & 1u;
                 if (!wait_bar(acce_bar(acc), aph ^ 1u, abort_flag, p)) {
@@ -256,7 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                const Unit u = unit_of(t, p);
+                for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
                     const int s = static_cast<int>(it % S::STAGES);
                     const uint32_t ph = (it / S::STAGES) & 1u;
                     if (!wait_bar(full_bar(s), ph, abort_flag, p)) {
@@ -278,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t bd = S::B_KMAJOR
                                                 ? ptx::smem_desc_sw128(b0 + k * 32, 16, 1024)
                                                 : ptx::smem_desc_sw128(b0 + k * S::UK * 128, S::BCH_BYTES, 1024);
-                        const uint32_t accum = (kb > 0 || k > 0) ? 1u : 0u;
+                        const uint32_t accum = (kb > u.kb0 || k > 0) ? 1u : 0u;
                         if constexpr (TF32)
                             ptx::mma_tf32(d_tmem, ad, bd, S::IDESC, accum);
                         else
@@ -301,10 +330,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;  // TMEM lanes this warp may access
         const int r_in_tile = quarter * 32 + lane;
         int local = 0;
-        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++local) {
+        for (int t = blockIdx.x; t < p.num_units; t += gridDim.x, ++local) {
             int mb, nb;
-            const int bi = t / p.tiles_per_batch;
-            tile_coords(t - bi * p.tiles_per_batch, p, mb, nb);
+            const Unit u = unit_of(t, p);
+            tile_coords(u.tt, p, mb, nb);
             const int acc = local & 1;
             const uint32_t aph = (static_cast<uint32_t>(local) >> 1) & 1u;
             if (!wait_bar(accf_bar(acc), aph, abort_flag, p)) break;
@@ -313,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int col0 = nb * BN;
             const bool row_ok = row < p.M;
             const bool whole = p.c_vec && (col0 + BN <= p.N);
-            float *crow = p.C + bi * p.strideC + static_cast<long long>(row) * p.ldc + col0;
+            float *crow = p.C + u.coff + static_cast<long long>(row) * p.ldc + col0;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
@@ -464,13 +493,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t leader_full0 = ptx::map_to_rank(full_bar(0), 0);
             uint32_t it = 0;
             bool ok = true;
-            for (int t = cluster_id; ok && t < p.num_tiles; t += nclusters) {
+            for (int t = cluster_id; ok && t < p.num_units; t += nclusters) {
                 int mb, nb;
-                const int bi = t / p.tiles_per_batch;
-                pair_tile_coords(t - bi * p.tiles_per_batch, p, mb, nb);
+                const Unit u = unit_of(t, p);
+                const int bi = u.bi;
+                pair_tile_coords(u.tt, p, mb, nb);
                 const int row0 = mb * 2 * S::BM + static_cast<int>(rank) * S::BM;
                 const int col0 = nb * S::BN + static_cast<int>(rank) * (S::BN / 2);
-                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
                     const int s = static_cast<int>(it % S::STAGES);
                     const uint32_t ph = (it / S::STAGES) & 1u;
                     if (!wait_bar(empty_bar(s), ph ^ 1u, abort_flag, p)) {
@@ -507,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t it = 0;
             int local = 0;
             bool ok = true;
-            for (int t = cluster_id; ok && t < p.num_tiles; t += nclusters, ++local) {
+            for (int t = cluster_id; ok && t < p.num_units; t += nclusters, ++local) {
                 const int acc = local & 1;
                 const uint32_t aph = (static_cast<uint32_t>(local) >> 1) & 1u;
                 if (!wait_bar(acce_bar(acc), aph ^ 1u, abort_flag, p)) {
@@ -516,7 +546,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * S::BN);
-                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                const Unit u = unit_of(t, p);
+                for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
                     const int s = static_cast<int>(it % S::STAGES);
                     const uint32_t ph = (it / S::STAGES) & 1u;
                     if (!wait_bar(full_bar(s), ph, abort_flag, p)) {
@@ -530,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int k = 0; k < S::KSTEPS; ++k) {
                         const uint64_t ad = ptx::smem_desc_sw128(a0 + k * 32, 16, 1024);
                         const uint64_t bd = ptx::smem_desc_sw128(b0 + k * S::UK * 128, S::BCH_BYTES, 1024);
-                        ptx::mma_bf16_pair(d_tmem, ad, bd, p.idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                        ptx::mma_bf16_pair(d_tmem, ad, bd, p.idesc, (kb > u.kb0 || k > 0) ? 1u : 0u);
                     }
                     ptx::mma_commit_pair(empty_bar(s), 0x3);
                 }
@@ -546,10 +577,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r_in_tile = quarter * 32 + lane;
         const uint32_t leader_acce0 = ptx::map_to_rank(acce_bar(0), 0);
         int local = 0;
-        for (int t = cluster_id; t < p.num_tiles; t += nclusters, ++local) {
+        for (int t = cluster_id; t < p.num_units; t += nclusters, ++local) {
             int mb, nb;
-            const int bi = t / p.tiles_per_batch;
-            pair_tile_coords(t - bi * p.tiles_per_batch, p, mb, nb);
+            const Unit u = unit_of(t, p);
+            pair_tile_coords(u.tt, p, mb, nb);
             const int acc = local & 1;
             const uint32_t aph = (static_cast<uint32_t>(local) >> 1) & 1u;
             if (!wait_bar(accf_bar(acc), aph, abort_flag, p)) break;
@@ -558,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int col0 = nb * S::BN;
             const bool row_ok = row < p.M;
             const bool whole = p.c_vec && (col0 + S::BN <= p.N);
-            float *crow = p.C + bi * p.strideC + static_cast<long long>(row) * p.ldc + col0;
+            float *crow = p.C + u.coff + static_cast<long long>(row) * p.ldc + col0;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * S::BN);
 #pragma unroll 1
@@ -648,6 +679,39 @@ int c_store_width(const GemmArgs &g) {
     return 0;
 }
 
+// K split of a launch (plan.splits > 1, single products only): the units'
+// partial tiles go to a workspace of `splits` packed M x N slabs from the
+// stream-ordered pool, without the epilogue, and finish_split adds them in
+// order into C and applies the epilogue. Sets the unit count either way.
+cudaError_t begin_split(const GemmArgs &g, const gtg_plan &plan, TcParams &p, float **ws, cudaStream_t stream) {
+    *ws = nullptr;
+    p.splits = 1;
+    p.kps = p.num_kb;
+    if (plan.splits > 1 && g.batch == 1 && p.num_kb > 1) {
+        p.kps = (p.num_kb + plan.splits - 1) / plan.splits;
+        p.splits = (p.num_kb + p.kps - 1) / p.kps;   // every range non-empty
+    }
+    p.num_units = p.num_tiles * p.splits;
+    if (p.splits == 1) return cudaSuccess;
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(ws),
+                                    static_cast<size_t>(p.splits) * g.M * g.N * sizeof(float), stream);
+    if (e != cudaSuccess) return e;
+    p.C = *ws;
+    p.ldc = g.N;
+    p.strideC = g.M * g.N;
+    p.bias = nullptr;
+    p.act = 0;
+    p.c_vec = (g.N & 7) == 0 ? 2 : ((g.N & 3) == 0 ? 1 : 0);   // pool memory is 256-byte aligned
+    return cudaSuccess;
+}
+
+cudaError_t finish_split(const GemmArgs &g, const TcParams &p, float *ws, cudaError_t e, cudaStream_t stream) {
+    if (ws == nullptr) return e;
+    if (e == cudaSuccess) e = split_reduce_launch(ws, p.splits, g.M, g.N, g.C, g.ldc, g.bias, g.act, stream);
+    const cudaError_t f = cudaFreeAsync(ws, stream);   // stream-ordered: after the reduction
+    return e == cudaSuccess ? f : e;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -696,6 +760,7 @@ uint32_t idesc16(int prec, uint32_t M, uint32_t N) {
 }
 
 std::atomic<int> g_pair_enabled{1};
+std::atomic<int> g_force_splits{0};   // testing / tuning hook: K splits of every eligible product
 
 struct AttrCache {
     std::mutex mu;
@@ -783,7 +848,10 @@ cudaError_t launch_impl(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
     p.drop_slice = take_drop_slice();
     p.bias = g.bias;
     p.act = g.act;
-    cudaError_t e = launch_pdl(kern, plan.grid, S::SMEM, stream, ta, tb, p);
+    float *ws = nullptr;
+    cudaError_t e = begin_split(g, plan, p, &ws, stream);
+    if (e == cudaSuccess) e = launch_pdl(kern, plan.grid, S::SMEM, stream, ta, tb, p);
+    e = finish_split(g, p, ws, e, stream);
     if (bt != nullptr) {
         // stream-ordered: released once the GEMM has finished reading it
         cudaError_t f = cudaFreeAsync(bt, stream);
@@ -827,6 +895,9 @@ cudaError_t launch_pair(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
     p.drop_slice = take_drop_slice();
     p.bias = g.bias;
     p.act = g.act;
+    float *ws = nullptr;
+    cudaError_t e = begin_split(g, plan, p, &ws, stream);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(plan.grid));
     cfg.blockDim = dim3(kThreads);
@@ -841,13 +912,14 @@ cudaError_t launch_pair(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel, ta, tb, p);
+    e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel, ta, tb, p);
+    return finish_split(g, p, ws, e, stream);
 }
 
-void fill_pair_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
+void fill_pair_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan, int splits) {
     using S = PairShape;
     const int64_t tiles = g.batch * ((g.M + 2 * S::BM - 1) / (2 * S::BM)) * ((g.N + S::BN - 1) / S::BN);
-    const int64_t clusters = std::min<int64_t>(tiles, dev.sms / 2);
+    const int64_t clusters = std::min<int64_t>(tiles * splits, dev.sms / 2);
     plan->kernel = GTG_KERNEL_TCGEN05;
     plan->bm = 2 * S::BM;
     plan->bn = S::BN;
@@ -857,12 +929,13 @@ void fill_pair_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
     plan->threads = kThreads;
     plan->smem = S::SMEM;
     plan->cluster = 2;
+    plan->splits = splits;
 }
 
 template <bool TF32, int BN>
-void fill_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
+void fill_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan, int splits) {
     using S = Shape<TF32, BN>;
-    const int64_t tiles = g.batch * ((g.M + S::BM - 1) / S::BM) * ((g.N + BN - 1) / BN);
+    const int64_t tiles = g.batch * ((g.M + S::BM - 1) / S::BM) * ((g.N + BN - 1) / BN) * splits;
     plan->kernel = GTG_KERNEL_TCGEN05;
     plan->bm = S::BM;
     plan->bn = BN;
@@ -872,12 +945,14 @@ void fill_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
     plan->threads = kThreads;
     plan->smem = S::SMEM;
     plan->cluster = 1;
+    plan->splits = splits;
 }
 
 }  // namespace
 
 void tc_set_wait_limit_ns(unsigned long long ns) { g_wait_limit_ns.store(ns ? ns : kWaitLimitNs); }
 void tc_drop_next_load(int slice) { g_drop_slice.store(slice); }
+void tc_force_splits(int splits) { g_force_splits.store(splits > 0 ? splits : 0); }
 
 bool tc_supported(const DeviceInfo &dev) {
     // tcgen05 exists on the sm_100 family; this library is built for sm_103a.
@@ -902,40 +977,79 @@ bool tc_eligible(const GemmArgs &g) {
     return g.M > 0 && g.N > 0 && g.K > 0;
 }
 
-// Tile width: minimise (waves of tiles) x (tile width / relative efficiency).
-// With M = 128 per CTA, a 256-wide tile reads 96 shared-memory bytes per
-// tensor-core cycle, a 128-wide one 128 (the SM's limit) and a 64-wide one
-// 192, so narrower tiles only pay when they fill otherwise idle SMs.
+// Kernel, tile width and K split: minimise the estimated time
+//   waves x (slices per unit + kFill) x slice time  [+ the split reduction]
+// where a wave is one unit (tile x K range) on every SM (CTA pair), kFill
+// counts pipeline fill, set-up and the epilogue in slice times, and a slice
+// of a 128 x w tile takes w/256 of a 256-wide one divided by the tile's
+// relative efficiency (with M = 128 per CTA a 256-wide tile reads 96
+// shared-memory bytes per tensor-core cycle, a 128-wide one 128 -- the SM's
+// limit -- and a 64-wide one 192), and a 256 x 256 pair tile 1/1.15 of the
+// 128 x 256 single-CTA time (2/3 of its operand bytes per SM). A split adds
+// a second kernel that reads the S partial slabs and writes C once.
+namespace {
+constexpr double kSliceUs = 0.30;        // one 128 x 256 x (128 bytes of K) slice on one SM
+constexpr double kFillSlices = 4.0;
+constexpr double kReduceFixedUs = 3.0;   // the reduction's launch and allocation
+constexpr double kHbmBytesPerUs = 6.0e6;
+double tc_cost(const DeviceInfo &dev, const GemmArgs &g, int bm, int bn, int slots, double rel, int splits,
+               int bk_elems) {
+    const int64_t num_kb = (g.K + bk_elems - 1) / bk_elems;
+    const int64_t kps = (num_kb + splits - 1) / splits;
+    const int64_t units = g.batch * ((g.M + bm - 1) / bm) * ((g.N + bn - 1) / bn) * ((num_kb + kps - 1) / kps);
+    const int64_t waves = (units + slots - 1) / slots;
+    double t = static_cast<double>(waves) * (static_cast<double>(kps) + kFillSlices) * kSliceUs * rel;
+    if (splits > 1) t += kReduceFixedUs + (splits + 1.0) * static_cast<double>(g.M) * g.N * 4.0 / kHbmBytesPerUs;
+    (void)dev;
+    return t;
+}
+}  // namespace
+
 void tc_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
-    const int widths[3] = {256, 128, 64};
-    const double eff[3] = {1.0, 0.8, 0.5};
-    int best = 0;
-    double best_cost = 0;
-    for (int i = 0; i < 3; ++i) {
-        const int64_t tiles = g.batch * ((g.M + kBM - 1) / kBM) * ((g.N + widths[i] - 1) / widths[i]);
-        const int64_t waves = (tiles + dev.sms - 1) / dev.sms;
-        const double cost = static_cast<double>(waves) * widths[i] / eff[i];
-        if (i == 0 || cost < best_cost) {
-            best = i;
-            best_cost = cost;
-        }
-    }
     const bool tf32 = g.prec == GTG_PREC_TF32;
-    if (!tf32 && (dev.sms & 1) == 0) {
-        // CTA pairs: 256 x 256 tiles on sms/2 clusters, operands 2/3 of the
-        // single-CTA 128 x 256 tile's bytes per SM
-        const int64_t tiles = g.batch * ((g.M + 255) / 256) * ((g.N + 255) / 256);
-        const int64_t waves = (tiles + dev.sms / 2 - 1) / (dev.sms / 2);
-        const double cost = static_cast<double>(waves) * 256 / 1.15;
-        if (cost < best_cost && g_pair_enabled.load()) {
-            fill_pair_plan(dev, g, plan);
-            return;
+    const int bk = tf32 ? 32 : 64;               // K elements per 128-byte slice
+    const int64_t num_kb = (g.K + bk - 1) / bk;
+    int forced = g_force_splits.load();
+    if (forced > 1 && (g.batch > 1 || num_kb < 2 * forced)) forced = 0;   // not applicable: plan as usual
+    const int split_opts[6] = {1, 2, 3, 4, 6, 8};
+    const int widths[3] = {256, 128, 64};
+    const double rel[3] = {1.0, 0.5 / 0.8, 0.25 / 0.5};
+    int best_w = 0, best_s = 1;
+    bool best_pair = false;
+    double best_cost = 0;
+    bool first = true;
+    for (int si = 0; si < 6; ++si) {
+        const int sp = split_opts[si];
+        const int want = forced > 0 ? forced : sp;
+        if (forced > 0 && si > 0) break;             // a forced split is the only option
+        if (want > 1 && (g.batch > 1 || num_kb < 2 * want)) continue;
+        for (int i = 0; i < 3; ++i) {
+            const double c = tc_cost(dev, g, kBM, widths[i], dev.sms, rel[i], want, bk);
+            if (first || c < best_cost) {
+                best_cost = c;
+                best_w = i;
+                best_s = want;
+                best_pair = false;
+                first = false;
+            }
+        }
+        if (!tf32 && (dev.sms & 1) == 0 && g_pair_enabled.load()) {
+            const double c = tc_cost(dev, g, 2 * kBM, 256, dev.sms / 2, 1.0 / 1.15, want, bk);
+            if (c < best_cost) {
+                best_cost = c;
+                best_s = want;
+                best_pair = true;
+            }
         }
     }
-    switch (widths[best]) {
-        case 256: tf32 ? fill_plan<true, 256>(dev, g, plan) : fill_plan<false, 256>(dev, g, plan); break;
-        case 128: tf32 ? fill_plan<true, 128>(dev, g, plan) : fill_plan<false, 128>(dev, g, plan); break;
-        default: tf32 ? fill_plan<true, 64>(dev, g, plan) : fill_plan<false, 64>(dev, g, plan); break;
+    if (best_pair) {
+        fill_pair_plan(dev, g, plan, best_s);
+        return;
+    }
+    switch (widths[best_w]) {
+        case 256: tf32 ? fill_plan<true, 256>(dev, g, plan, best_s) : fill_plan<false, 256>(dev, g, plan, best_s); break;
+        case 128: tf32 ? fill_plan<true, 128>(dev, g, plan, best_s) : fill_plan<false, 128>(dev, g, plan, best_s); break;
+        default: tf32 ? fill_plan<true, 64>(dev, g, plan, best_s) : fill_plan<false, 64>(dev, g, plan, best_s); break;
     }
 }
 
@@ -1035,6 +1149,9 @@ cudaError_t launch_tf32_fixed(const DeviceInfo &dev, const GemmArgs &g, const gt
     p.num_kb = static_cast<int>((g.K + S::BK - 1) / S::BK);
     p.tiles_per_batch = p.num_m * p.num_n;
     p.num_tiles = p.tiles_per_batch;
+    p.splits = 1;             // no workspace: K is never split here
+    p.kps = p.num_kb;
+    p.num_units = p.num_tiles;
     p.strideC = 0;
     p.idesc = S::IDESC;
     p.c_vec = c_store_width(g);

@@ -78,6 +78,7 @@ cudaError_t tc_launch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &
 // testing hooks of the tensor-core kernels (gemm_tc.cu)
 void tc_set_wait_limit_ns(unsigned long long ns);
 void tc_drop_next_load(int slice);
+void tc_force_splits(int splits);   // > 0: every eligible single product splits K that many ways
 
 // ---- TF32 GEMM whose B^T staging buffer is a fixed array in the library
 // (gemm_tc.cu), for callers that cannot allocate device memory
@@ -91,6 +92,10 @@ void simt_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan);
 cudaError_t simt_launch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan,
                         cudaStream_t stream);
 cudaError_t zero_fill_launch(float *C, int64_t M, int64_t N, int64_t ldc, cudaStream_t stream);
+// C = act(sum_{z < splits} ws[z] + bias), the slabs ws[z] (M x N, packed)
+// added in order z = 0, 1, ... (results independent of scheduling)
+cudaError_t split_reduce_launch(const float *ws, int splits, int64_t M, int64_t N, float *C, int64_t ldc,
+                                const float *bias, int act, cudaStream_t stream);
 // C[i][j] = act(bias[j] or bias[i]) -- the result of an empty product with an epilogue
 cudaError_t epilogue_fill_launch(float *C, int64_t M, int64_t N, int64_t ldc, const float *bias, int per_column,
                                  int act, cudaStream_t stream);

@@ -413,6 +413,8 @@ typedef struct {
     int threads;  /* threads per block */
     int smem;     /* dynamic shared memory per block, bytes */
     int cluster;  /* thread blocks per cluster (1: no cluster launch) */
+    int splits;   /* GEMM: slices of K computed apart (partial products added in
+                     order by a second kernel; 1: none) */
 } gtg_plan;
 
 GTG_API gtg_status gtg_plan_gemm(int precision, int64_t M, int64_t N, int64_t K,
@@ -433,6 +435,15 @@ GTG_API gtg_status gtg_plan_gemv(int64_t M, int64_t N, const float *A, int64_t l
 GTG_API gtg_status gtg_plan_gemv_bf16(int64_t M, int64_t N, const gtg_bf16 *A, int64_t lda,
                               const float *x, int64_t ldx, const float *y, int64_t ldy,
                               int batch, gtg_plan *plan);
+
+/*
+ * Testing and tuning hook: with splits > 0 every tensor-core GEMM of a single
+ * product that has at least 2 * splits K slices computes K in `splits`
+ * ranges whose partial tiles are added in order by a second kernel (workspace
+ * from the stream-ordered pool); 0 restores the planner's own choice.
+ * Process-wide; results stay within the same bounds.
+ */
+GTG_API void gtg_force_gemm_splits(int splits);
 
 /*
  * Testing hook: force the tensor-core GEMM paths onto the SIMT kernel
