@@ -80,6 +80,7 @@ SIGNATURES = {
                              ctypes.POINTER(GtgPlan)]),
     "gtg_force_simt": (None, [_int]),
     "gtg_force_gemm_splits": (None, [_int]),
+    "gtg_conv_force_path": (None, [_int]),
     "gtg_set_wait_limit_ns": (None, [ctypes.c_uint64]),
     "gtg_test_drop_load": (None, [_int]),
     "gtg_version": (_int, []),
@@ -228,6 +229,11 @@ def last_cuda_error() -> str:
 
 def gtg_force_simt(force: bool) -> None:
     lib().gtg_force_simt(1 if force else 0)
+
+
+def gtg_conv_force_path(mode: str) -> None:
+    """Testing hook: conv2d_nhwc path, "auto", "explicit" (im2col + GEMM) or "implicit"."""
+    lib().gtg_conv_force_path({"auto": 0, "explicit": 1, "implicit": 2}[mode])
 
 
 def gtg_force_gemm_splits(splits: int) -> None:

@@ -309,6 +309,10 @@ gtg_status gemv_bf16_ex(int64_t M, int64_t N, const gtg_bf16 *A, int64_t lda, co
     return run_gemv(g, stream);
 }
 
+// Testing hook: 0 chooses the convolution path, 1 always writes the patch
+// matrix, 2 requires the implicit GEMM (GTG_ERR_UNSUPPORTED otherwise).
+static std::atomic<int> g_conv_mode{0};
+
 static gtg_status validate_conv(ConvArgs &c) {
     if (c.prec < GTG_PREC_F32 || c.prec > GTG_PREC_F16) return GTG_ERR_INVALID_VALUE;
     c.elem = c.prec == GTG_PREC_BF16 || c.prec == GTG_PREC_F16 ? 2 : 4;
@@ -505,6 +509,17 @@ gtg_status conv2d_nhwc(int precision, int64_t N, int64_t H, int64_t W, int64_t C
     const int64_t M = N * c.OH * c.OW, K = KH * KW * C;
     // a 1x1 window at stride 1 without padding reads X itself as the patch matrix
     const bool direct = KH == 1 && KW == 1 && stride_h == 1 && stride_w == 1 && pad_h == 0 && pad_w == 0;
+    const int mode = g_conv_mode.load();
+    if ((mode == 2 || (mode == 0 && !direct)) && tc_conv_eligible(dev, c)) {
+        // implicit GEMM: the tensor-core kernel reads the patches from X itself
+        const cudaError_t e = tc_conv_launch(dev, c, stream);
+        if (e != cudaSuccess) {
+            note_cuda_error(e);
+            return GTG_ERR_LAUNCH;
+        }
+        return GTG_OK;
+    }
+    if (mode == 2) return GTG_ERR_UNSUPPORTED;
     const void *A = X;
     int64_t lda = C;
     void *P = nullptr;
@@ -548,6 +563,8 @@ void gtg_set_wait_limit_ns(uint64_t ns) { tc_set_wait_limit_ns(ns); }
 void gtg_test_drop_load(int slice) { tc_drop_next_load(slice); }
 
 void gtg_force_gemm_splits(int splits) { tc_force_splits(splits); }
+
+void gtg_conv_force_path(int mode) { g_conv_mode.store(mode == 1 || mode == 2 ? mode : 0); }
 
 int gtg_version(void) { return 100; }
 

@@ -93,6 +93,10 @@ struct TcParams {
     int drop_slice;              // testing hook: K slice whose load CTA 0 never issues (-1: none)
     const float *bias;           // epilogue: C = act(acc + bias[col]); null for none
     int act;
+    // implicit-GEMM convolution (A read from the image by TMA im2col loads):
+    // output width and height, 64-channel blocks per pixel, window width,
+    // strides, paddings, dilations
+    int cv_ow, cv_oh, cv_cb, cv_kw, cv_sw, cv_sh, cv_pw, cv_ph, cv_dw, cv_dh;
 };
 
 // Apply the layer epilogue to 32 accumulator columns starting at column col.
@@ -176,7 +180,11 @@ __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, const TcP
     }
 }
 
-template <bool TF32, int BN>
+// IM2COL: A is not a matrix in memory but the patch matrix of a convolution
+// (rows = output pixels in (n, oh, ow) order, K = (kh, kw, channel)); each
+// 128 x 64 A tile is one TMA im2col load of 128 output pixels' 64 channels
+// at one window tap, straight from the channels-last image.
+template <bool TF32, int BN, bool IM2COL = false>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const TcParams p) {
@@ -239,6 +247,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Unit u = unit_of(t, p);
                 const int bi = u.bi;
                 tile_coords(u.tt, p, mb, nb);
+                int w0 = 0, h0 = 0, n0 = 0;   // IM2COL: window corner of the tile's first output pixel
+                if constexpr (IM2COL) {
+                    const int m0 = mb * S::BM;
+                    const int q = m0 / p.cv_ow;
+                    w0 = (m0 - q * p.cv_ow) * p.cv_sw - p.cv_pw;
+                    h0 = (q % p.cv_oh) * p.cv_sh - p.cv_ph;
+                    n0 = q / p.cv_oh;
+                }
                 for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
                     const int s = static_cast<int>(it % S::STAGES);
                     const uint32_t ph = (it / S::STAGES) & 1u;
@@ -248,7 +264,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (p.drop_slice == static_cast<int>(it) && blockIdx.x == 0) continue;
                     ptx::mbar_arrive_expect_tx(full_bar(s), S::STAGE_BYTES);
-                    ptx::tma_load_3d(sA + s * S::A_BYTES, &tmA, full_bar(s), kb * S::BK, mb * S::BM, bi);
+                    if constexpr (IM2COL) {
+                        // K slice kb = (kh, kw, channel block cb)
+                        const int tap = kb / p.cv_cb, cb = kb - tap * p.cv_cb;
+                        const int kh = tap / p.cv_kw, kw = tap - kh * p.cv_kw;
+                        ptx::tma_load_im2col_4d(sA + s * S::A_BYTES, &tmA, full_bar(s), cb * S::BK, w0, h0, n0,
+                                                static_cast<uint16_t>(kw * p.cv_dw), static_cast<uint16_t>(kh * p.cv_dh));
+                    } else {
+                        ptx::tma_load_3d(sA + s * S::A_BYTES, &tmA, full_bar(s), kb * S::BK, mb * S::BM, bi);
+                    }
                     if constexpr (S::B_KMAJOR) {
                         // B^T tile: BN rows of BK elements
                         ptx::tma_load_3d(sB + s * S::B_BYTES, &tmB, full_bar(s), kb * S::BK, nb * BN, bi);
@@ -738,6 +762,44 @@ CUtensorMapDataType tma_type(int prec) {
 // 3-D tensor map whose third dimension walks `batch` matrices
 // batch_stride_elems apart; boxes of box_inner x box_outer x 1, 128-byte
 // swizzled, out-of-range elements read as zero.
+PFN_cuTensorMapEncodeIm2col_v12000 encode_im2col_fn() {
+    static PFN_cuTensorMapEncodeIm2col_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeIm2col_v12000>(p);
+    });
+    return fn;
+}
+
+// Bounding-box corners of the im2col map: the window corners of the output
+// pixels run from -pad to (last output) * stride - pad, i.e. the box is the
+// image widened by the padding below and cut by pad - (window - 1) * dilation
+// above; each corner is an offset from the image's first / last position.
+int im2col_lower(int64_t pad) { return static_cast<int>(-pad); }
+int im2col_upper(int64_t pad, int64_t window, int64_t dil) { return static_cast<int>(pad - (window - 1) * dil); }
+
+// X (N x H x W x C, 16-bit, channels last) as 128-pixel x 64-channel im2col tiles.
+bool encode_im2col(CUtensorMap *map, const ConvArgs &c) {
+    auto fn = encode_im2col_fn();
+    if (!fn) return false;
+    const uint64_t e = 2;
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(c.C), static_cast<cuuint64_t>(c.W), static_cast<cuuint64_t>(c.H),
+                          static_cast<cuuint64_t>(c.N)};
+    cuuint64_t strides[3] = {c.C * e, c.W * c.C * e, c.H * c.W * c.C * e};
+    int lower[2] = {im2col_lower(c.pw), im2col_lower(c.ph)};                   // W, then H
+    int upper[2] = {im2col_upper(c.pw, c.KW, c.dw), im2col_upper(c.ph, c.KH, c.dh)};
+    cuuint32_t estr[4] = {1, static_cast<cuuint32_t>(c.sw), static_cast<cuuint32_t>(c.sh), 1};
+    CUresult r = fn(map, tma_type(c.prec), 4, const_cast<void *>(c.X), dims, strides, lower, upper, 64, 128, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool encode_3d(CUtensorMap *map, int prec, const void *base, uint64_t inner, uint64_t outer, uint64_t ld_elems,
                uint64_t batch, uint64_t batch_stride_elems, uint32_t box_inner, uint32_t box_outer) {
     auto fn = encode_fn();
@@ -948,7 +1010,64 @@ void fill_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan, int spl
     plan->splits = splits;
 }
 
+// Implicit-GEMM convolution on the single-CTA kernel: Y (N*OH*OW x CO) =
+// patches(X) x Wt with the A tiles loaded by TMA in im2col mode.
+template <int BN>
+cudaError_t conv_launch_impl(const DeviceInfo &dev, const ConvArgs &c, cudaStream_t stream, int attr_bit) {
+    using S = Shape<false, BN>;
+    auto kern = tc_gemm_kernel<false, BN, true>;
+    {
+        AttrCache &ac = attr_cache();
+        std::lock_guard<std::mutex> lk(ac.mu);
+        const int d = dev.id & 63;
+        if (!(ac.done[d] >> attr_bit & 1)) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+            if (e != cudaSuccess) return e;
+            ac.done[d] |= 1ull << attr_bit;
+        }
+    }
+    const int64_t M = c.N * c.OH * c.OW, K = c.KH * c.KW * c.C;
+    CUtensorMap ta, tb;
+    if (!encode_im2col(&ta, c)) return cudaErrorInvalidValue;
+    if (!encode_3d(&tb, c.prec, c.Wt, c.CO, K, c.CO, 1, 0, S::BCH_N, S::BK)) return cudaErrorInvalidValue;
+    TcParams p;
+    p.C = c.Y;
+    p.ldc = c.CO;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(c.CO);
+    p.num_m = static_cast<int>((M + S::BM - 1) / S::BM);
+    p.num_n = static_cast<int>((c.CO + BN - 1) / BN);
+    p.num_kb = static_cast<int>(K / S::BK);
+    p.tiles_per_batch = p.num_m * p.num_n;
+    p.num_tiles = p.tiles_per_batch;
+    p.splits = 1;
+    p.kps = p.num_kb;
+    p.num_units = p.num_tiles;
+    p.strideC = 0;
+    p.idesc = idesc16(c.prec, S::BM, BN);
+    const auto yaddr = reinterpret_cast<uintptr_t>(c.Y);
+    p.c_vec = ((yaddr & 31) == 0 && (c.CO & 7) == 0) ? 2 : (((yaddr & 15) == 0 && (c.CO & 3) == 0) ? 1 : 0);
+    p.status = dev.status;
+    p.wait_limit_ns = wait_limit_ns();
+    p.drop_slice = take_drop_slice();
+    p.bias = c.bias;
+    p.act = c.act;
+    p.cv_ow = static_cast<int>(c.OW);
+    p.cv_oh = static_cast<int>(c.OH);
+    p.cv_cb = static_cast<int>(c.C / S::BK);
+    p.cv_kw = static_cast<int>(c.KW);
+    p.cv_sw = static_cast<int>(c.sw);
+    p.cv_sh = static_cast<int>(c.sh);
+    p.cv_pw = static_cast<int>(c.pw);
+    p.cv_ph = static_cast<int>(c.ph);
+    p.cv_dw = static_cast<int>(c.dw);
+    p.cv_dh = static_cast<int>(c.dh);
+    const int grid = static_cast<int>(std::min<int64_t>(p.num_tiles, dev.sms));
+    return launch_pdl(kern, grid, S::SMEM, stream, ta, tb, p);
+}
+
 }  // namespace
+
 
 void tc_set_wait_limit_ns(unsigned long long ns) { g_wait_limit_ns.store(ns ? ns : kWaitLimitNs); }
 void tc_drop_next_load(int slice) { g_drop_slice.store(slice); }
@@ -1052,6 +1171,42 @@ void tc_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
         default: tf32 ? fill_plan<true, 64>(dev, g, plan, best_s) : fill_plan<false, 64>(dev, g, plan, best_s); break;
     }
 }
+
+bool tc_conv_eligible(const DeviceInfo &dev, const ConvArgs &c) {
+    if (!tc_supported(dev) || encode_im2col_fn() == nullptr) return false;
+    if (c.prec != GTG_PREC_BF16 && c.prec != GTG_PREC_F16) return false;
+    if (c.C % 64 || (c.CO * 2) % 16) return false;                          // 128-byte channel blocks, B rows
+    if ((reinterpret_cast<uintptr_t>(c.X) & 15) || (reinterpret_cast<uintptr_t>(c.Wt) & 15)) return false;
+    if (c.sw > 8 || c.sh > 8) return false;                                  // TMA traversal steps
+    const int64_t corners[4] = {-c.pw, -c.ph, c.pw - (c.KW - 1) * c.dw, c.ph - (c.KH - 1) * c.dh};
+    for (int64_t v : corners)
+        if (v < -128 || v > 127) return false;                               // 8-bit corners of a 4-D map
+    if ((c.KW - 1) * c.dw > 255 || (c.KH - 1) * c.dh > 255) return false;    // im2col offsets
+    if (c.N * c.OH * c.OW > INT32_MAX || c.KH * c.KW * c.C > INT32_MAX) return false;
+    return true;
+}
+
+cudaError_t tc_conv_launch(const DeviceInfo &dev, const ConvArgs &c, cudaStream_t stream) {
+    // tile width by the same estimate as the GEMM planner (single CTAs, whole K)
+    GemmArgs g{c.prec, c.N * c.OH * c.OW, c.CO, c.KH * c.KW * c.C, nullptr, 0, nullptr, 0, nullptr, 0};
+    const int widths[3] = {256, 128, 64};
+    const double rel[3] = {1.0, 0.5 / 0.8, 0.25 / 0.5};
+    int best = 0;
+    double best_cost = 0;
+    for (int i = 0; i < 3; ++i) {
+        const double cost = tc_cost(dev, g, kBM, widths[i], dev.sms, rel[i], 1, 64);
+        if (i == 0 || cost < best_cost) {
+            best = i;
+            best_cost = cost;
+        }
+    }
+    switch (widths[best]) {
+        case 256: return conv_launch_impl<256>(dev, c, stream, 7);
+        case 128: return conv_launch_impl<128>(dev, c, stream, 8);
+        default: return conv_launch_impl<64>(dev, c, stream, 9);
+    }
+}
+
 
 cudaError_t tc_launch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan,
                       cudaStream_t stream) {

@@ -105,6 +105,11 @@ cudaError_t ablation_gemm_launch(int variant, const GemmArgs &g, cudaStream_t st
 cudaError_t ablation_gemv_launch(int variant, const GemvArgs &g, cudaStream_t stream);
 bool grid_too_large(int64_t M, int64_t N, int tile);
 
+// ---- implicit-GEMM convolution on the tensor cores (gemm_tc.cu): A tiles
+// loaded from X by TMA in im2col mode (16-bit, C % 64 == 0, small windows)
+bool tc_conv_eligible(const DeviceInfo &dev, const ConvArgs &c);
+cudaError_t tc_conv_launch(const DeviceInfo &dev, const ConvArgs &c, cudaStream_t stream);
+
 // ---- im2col (im2col.cu): the patch matrix P (N*OH*OW x KH*KW*C, ldp >= K)
 cudaError_t im2col_launch(const DeviceInfo &dev, const ConvArgs &c, void *P, int64_t ldp, cudaStream_t stream);
 

@@ -91,6 +91,19 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
 }
 
 // Same, with an L2 eviction-priority policy (createpolicy result).
+// TMA load in im2col mode from a 4-D (C, W, H, N) tensor map: the
+// map's pixelsPerColumn pixels, channelsPerPixel channels each, starting
+// with channel c at the pixel (w, h, n) and walking the map's bounding box
+// with its element strides; every pixel is read at (w + off_w, h + off_h).
+__device__ __forceinline__ void tma_load_im2col_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t c,
+                                                   int32_t w, int32_t h, int32_t n, uint16_t off_w, uint16_t off_h) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.im2col.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], {%7, %8};" ::"r"(dst),
+        "l"(map), "r"(bar), "r"(c), "r"(w), "r"(h), "r"(n), "h"(off_w), "h"(off_h)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map, uint32_t bar,
                                                  int32_t x, int32_t y, uint64_t policy) {
     asm volatile(

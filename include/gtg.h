@@ -446,6 +446,15 @@ GTG_API gtg_status gtg_plan_gemv_bf16(int64_t M, int64_t N, const gtg_bf16 *A, i
 GTG_API void gtg_force_gemm_splits(int splits);
 
 /*
+ * Testing hook for conv2d_nhwc: 0 (default) lets each call choose; 1 always
+ * writes the patch matrix and multiplies it (im2col + GEMM); 2 requires the
+ * implicit GEMM, whose tensor-core kernel loads the patches straight from X
+ * with TMA in im2col mode, and makes a call that cannot take it return
+ * GTG_ERR_UNSUPPORTED. Process-wide.
+ */
+GTG_API void gtg_conv_force_path(int mode);
+
+/*
  * Testing hook: force the tensor-core GEMM paths onto the SIMT kernel
  * (force = 1) or restore the normal choice (force = 0). Process-wide.
  */

@@ -138,3 +138,62 @@ def test_conv2d_helper_on_torch_tensors():
     Yh = gtg.conv2d(tX, tW, stride=1, pad=1)                # host tensors: copied in and out
     assert torch.equal(Yd.cpu(), Yh)
     check("bf16", Xf, Wf, Yh.numpy(), 1, 1, 1)
+
+
+# ---- implicit GEMM: the tensor-core kernel loads the patches from X with TMA
+# in im2col mode (16-bit inputs, C a multiple of 64); the tests require that
+# path, so a silent fall-back to the patch matrix fails them
+
+@pytest.fixture
+def conv_path():
+    yield gtg.gtg_conv_force_path
+    gtg.gtg_conv_force_path("auto")
+
+
+IMPLICIT_CASES = [
+    (2, 14, 14, 64, 64, 3, 3, 1, 1, 1),
+    (1, 17, 13, 128, 96, 3, 3, 2, 1, 1),             # stride 2, ragged output, CO = 96
+    (1, 12, 10, 64, 40, 3, 3, 1, 2, 2),              # dilation 2
+    (2, 8, 20, 64, 16, 1, 5, 1, (0, 2), 1),          # 1 x 5, padding along W only
+    (1, 9, 7, 64, 24, 3, 2, (2, 1), (1, 0), (1, 2)),  # per-axis strides, paddings, dilations
+    (2, 32, 32, 64, 128, 7, 7, 2, 3, 1),             # 7 x 7 / 2
+    (3, 5, 6, 64, 8, 1, 1, 2, 0, 1),                 # 1 x 1 / 2
+    (1, 7, 7, 192, 64, 3, 3, 1, 1, 1),               # three 64-channel blocks
+    (3, 9, 11, 64, 32, 1, 1, 1, 0, 1),               # 1 x 1 / 1
+    (5, 11, 13, 64, 264, 3, 3, 1, 1, 1),             # CO beyond one 256-wide tile
+]
+
+
+@pytest.mark.parametrize("prec", ["bf16", "f16"])
+@pytest.mark.parametrize("case", IMPLICIT_CASES, ids=lambda c: "x".join(str(v) for v in c))
+def test_implicit_gemm_conv(conv_path, prec, case):
+    N, H, W, C, CO, KH, KW, s, p, d = case
+    g = PCG32(2500 + N * H * W + C * CO + KH)
+    X, Xf = _draw(prec, g, (N, H, W, C))
+    Wt, Wf = _draw(prec, g, (KH, KW, C, CO), (KH * KW * C) ** -0.5)
+    conv_path("implicit")
+    Y = run_conv(prec, X, Wt, s, p, d)
+    check(prec, Xf, Wf, Y, s, p, d)
+
+
+def test_implicit_gemm_conv_with_epilogue_and_both_paths(conv_path):
+    g = PCG32(2600)
+    X, Xf = _draw("bf16", g, (2, 20, 18, 128))
+    Wt, Wf = _draw("bf16", g, (3, 3, 128, 72), (9 * 128) ** -0.5)
+    bias = g.uniform_f32((72,))
+    for path in ("implicit", "explicit"):
+        conv_path(path)
+        Y = run_conv("bf16", X, Wt, 2, 1, 1, bias, "relu")
+        check("bf16", Xf, Wf, Y, 2, 1, 1, bias, "relu")
+
+
+def test_implicit_gemm_refuses_what_it_cannot_take(conv_path):
+    torch = _t()
+    conv_path("implicit")
+    X = torch.zeros((1, 8, 8, 32), dtype=torch.int16, device="cuda")          # C = 32: not a 64-channel block
+    Wt = torch.zeros((3, 3, 32, 16), dtype=torch.int16, device="cuda")
+    Y = torch.empty((1, 6, 6, 16), device="cuda")
+    s = int(torch.cuda.current_stream().cuda_stream)
+    st = gtg.conv2d_nhwc("bf16", 1, 8, 8, 32, 16, 3, 3, 1, 1, 0, 0, 1, 1, X.data_ptr(), Wt.data_ptr(), Y.data_ptr(),
+                         None, s)
+    assert st == gtg.GTG_ERR_UNSUPPORTED
