@@ -81,6 +81,7 @@ SIGNATURES = {
     "gtg_force_simt": (None, [_int]),
     "gtg_force_gemm_splits": (None, [_int]),
     "gtg_conv_force_path": (None, [_int]),
+    "gtg_test_skip_vector_copy": (None, [_int]),
     "gtg_set_wait_limit_ns": (None, [ctypes.c_uint64]),
     "gtg_test_drop_load": (None, [_int]),
     "gtg_version": (_int, []),
@@ -229,6 +230,11 @@ def last_cuda_error() -> str:
 
 def gtg_force_simt(force: bool) -> None:
     lib().gtg_force_simt(1 if force else 0)
+
+
+def gtg_test_skip_vector_copy(on: bool) -> None:
+    """Testing hook: the next bulk-staged GEMV announces its vector copies but issues none."""
+    lib().gtg_test_skip_vector_copy(1 if on else 0)
 
 
 def gtg_conv_force_path(mode: str) -> None:

@@ -1070,6 +1070,7 @@ cudaError_t conv_launch_impl(const DeviceInfo &dev, const ConvArgs &c, cudaStrea
 
 
 void tc_set_wait_limit_ns(unsigned long long ns) { g_wait_limit_ns.store(ns ? ns : kWaitLimitNs); }
+unsigned long long wait_limit_setting() { return g_wait_limit_ns.load(); }
 void tc_drop_next_load(int slice) { g_drop_slice.store(slice); }
 void tc_force_splits(int splits) { g_force_splits.store(splits > 0 ? splits : 0); }
 

@@ -1,6 +1,7 @@
 // GEMV planning and launch, and the FP32-matrix instantiations of the GEMV
 // kernels (the kernels themselves and their design are in gemv_kernels.cuh).
 #include <algorithm>
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -8,6 +9,14 @@
 #include "gemv_kernels.cuh"
 
 namespace gtg {
+
+namespace {
+std::atomic<int> g_gemv_skip_x{0};
+}
+
+void gemv_skip_next_x(int on) { g_gemv_skip_x.store(on ? 1 : 0); }
+int take_gemv_skip_x() { return g_gemv_skip_x.exchange(0); }
+
 namespace {
 
 using namespace gemv;
@@ -182,6 +191,8 @@ cudaError_t gemv_launch(const DeviceInfo &dev, const GemvArgs &g, const gtg_plan
     p.x_bulk = l.kind != kRound && (reinterpret_cast<uintptr_t>(g.x) & 15) == 0 && g.N % 4 == 0 &&
                (g.batch == 1 || g.ldx % 4 == 0);
     p.status = dev.status;
+    p.wait_limit_ns = wait_limit_setting();
+    p.skip_x = p.x_bulk ? take_gemv_skip_x() : 0;
     void *args[] = {&p};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.grid);

@@ -57,6 +57,8 @@ struct Params {
     int ublock;          // gemv_cluster_kernel: 16-byte units per column block
     int x_bulk;          // x rows 16-byte aligned, ldx and N multiples of 4: stage x by bulk copies
     int *status;         // the library's device status word (set on a timed-out wait)
+    unsigned long long wait_limit_ns;   // bound of every mbarrier wait
+    int skip_x;          // testing hook: announce the bulk copies of x but issue none (the wait runs out)
 };
 
 // Matrix element types. kVec = elements per 16-byte load; widen() turns one
@@ -121,10 +123,11 @@ template <int BATCH>
 __device__ __forceinline__ void stage_x_bulk(float *xs, const Params &p, uint32_t bar) {
     if (threadIdx.x == 0) {
         ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(BATCH * p.N * 4));
+        if (!p.skip_x)
 #pragma unroll
-        for (int b = 0; b < BATCH; ++b)
-            ptx::bulk_load(ptx::smem_addr(xs + b * p.chunk), p.x + static_cast<long long>(b) * p.ldx,
-                           static_cast<uint32_t>(p.N * 4), bar);
+            for (int b = 0; b < BATCH; ++b)
+                ptx::bulk_load(ptx::smem_addr(xs + b * p.chunk), p.x + static_cast<long long>(b) * p.ldx,
+                               static_cast<uint32_t>(p.N * 4), bar);
     }
 }
 
@@ -132,14 +135,14 @@ __device__ __forceinline__ void stage_x_bulk(float *xs, const Params &p, uint32_
 // records GTG_ERR_TIMEOUT, the copies are given one more bounded wait so that
 // none is left writing into shared memory, and false is returned; the caller
 // then skips its arithmetic but still reaches every later barrier of the CTA.
-__device__ __forceinline__ bool wait_x(uint32_t bar, int *status) {
+__device__ __forceinline__ bool wait_x(uint32_t bar, const Params &p) {
     if (ptx::mbar_try_wait(bar, 0)) return true;
     uint64_t t0 = ptx::globaltimer_ns();
     while (!ptx::mbar_try_wait(bar, 0)) {
-        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
-            atomicCAS(status, 0, GTG_ERR_TIMEOUT);
+        if (ptx::globaltimer_ns() - t0 > p.wait_limit_ns) {
+            atomicCAS(p.status, 0, GTG_ERR_TIMEOUT);
             t0 = ptx::globaltimer_ns();
-            while (!ptx::mbar_try_wait(bar, 0) && ptx::globaltimer_ns() - t0 < kWaitLimitNs) {
+            while (!ptx::mbar_try_wait(bar, 0) && ptx::globaltimer_ns() - t0 < p.wait_limit_ns) {
             }
             return false;
         }
@@ -412,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const Params p
     if (total > 0) load(0, nxt);
     bool ok = true;
     if (p.x_bulk) {
-        ok = __all_sync(0xFFFFFFFFu, wait_x(bar, p.status));   // warp-uniform: shuffles follow
+        ok = __all_sync(0xFFFFFFFFu, wait_x(bar, p));   // warp-uniform: shuffles follow
     } else {
         stage_x<BATCH, kThreads>(xs, p, 0, p.N);
         __syncthreads();
@@ -534,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_split_kernel(const Params p)
     }
     bool ok = true;
     if (p.x_bulk) {
-        ok = __all_sync(0xFFFFFFFFu, wait_x(bar, p.status));   // warp-uniform: shuffles follow
+        ok = __all_sync(0xFFFFFFFFu, wait_x(bar, p));   // warp-uniform: shuffles follow
     } else {
         stage_x<BATCH, kThreads>(xs, p, 0, p.N);
         __syncthreads();
@@ -643,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_cluster_kernel(const Params 
         __syncthreads();   // the barrier is initialised
         if (threadIdx.x == 0) {
             ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(BATCH * xlen * 4));
-            if (xlen > 0)
+            if (xlen > 0 && !p.skip_x)
 #pragma unroll
                 for (int b = 0; b < BATCH; ++b)
                     ptx::bulk_load(ptx::smem_addr(xs + b * p.chunk),
@@ -679,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_cluster_kernel(const Params 
     }
     bool ok = true;
     if (p.x_bulk) {
-        ok = __all_sync(0xFFFFFFFFu, wait_x(bar, p.status));
+        ok = __all_sync(0xFFFFFFFFu, wait_x(bar, p));
     } else {
 #pragma unroll
         for (int b = 0; b < BATCH; ++b) {

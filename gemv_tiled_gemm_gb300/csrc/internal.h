@@ -113,7 +113,14 @@ cudaError_t tc_conv_launch(const DeviceInfo &dev, const ConvArgs &c, cudaStream_
 // ---- im2col (im2col.cu): the patch matrix P (N*OH*OW x KH*KW*C, ldp >= K)
 cudaError_t im2col_launch(const DeviceInfo &dev, const ConvArgs &c, void *P, int64_t ldp, cudaStream_t stream);
 
+// Current bound of in-kernel waits (gtg_set_wait_limit_ns; gemm_tc.cu).
+unsigned long long wait_limit_setting();
+
 // ---- GEMV (gemv.cu)
+// testing hook: the next GEMV launch that stages x by bulk copies announces
+// them but issues none, so its wait runs out
+void gemv_skip_next_x(int on);
+int take_gemv_skip_x();
 void gemv_plan(const DeviceInfo &dev, const GemvArgs &g, gtg_plan *plan);
 cudaError_t gemv_launch(const DeviceInfo &dev, const GemvArgs &g, const gtg_plan &plan,
                         cudaStream_t stream);

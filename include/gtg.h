@@ -461,8 +461,9 @@ GTG_API void gtg_conv_force_path(int mode);
 GTG_API void gtg_force_simt(int force);
 
 /*
- * Time limit of every pipeline wait inside the tensor-core kernels, in
- * nanoseconds (0 restores the default of 2 s). A wait that runs out makes the
+ * Time limit of every pipeline wait inside the tensor-core GEMM kernels and
+ * of the GEMV kernels' wait for their bulk-copied vectors, in nanoseconds
+ * (0 restores the default of 2 s). A wait that runs out makes the
  * kernel stop, release its resources and latch GTG_ERR_TIMEOUT for
  * gtg_sync_status(). Process-wide; applies to later launches.
  */
@@ -476,6 +477,14 @@ GTG_API void gtg_set_wait_limit_ns(uint64_t ns);
  * calls work normally. A negative value cancels a pending drop.
  */
 GTG_API void gtg_test_drop_load(int slice);
+
+/*
+ * Testing hook for the GEMV failure path: with on != 0, the next GEMV launch
+ * that stages its vectors by bulk copies announces the copies to its
+ * mbarrier but issues none, so its bounded wait can only run out; the call
+ * returns GTG_OK and gtg_sync_status() reports GTG_ERR_TIMEOUT. 0 cancels.
+ */
+GTG_API void gtg_test_skip_vector_copy(int on);
 
 /* Version of this ABI (major * 10000 + minor * 100 + patch). */
 GTG_API int gtg_version(void);

@@ -75,3 +75,36 @@ def test_wait_limit_default_restored():
     A, B = _operands("bf16", 512, 512, 512, 91)
     st, status, _ = _launch("bf16", A, B)
     assert st == gtg.GTG_OK and status == gtg.GTG_OK
+
+
+@pytest.mark.parametrize("M,N,batch,kernel", [
+    (4096, 4096, 1, "stream"),       # one row per warp, vectors in one bulk copy each
+    (4096, 4096, 8, "split"),        # 4 rows x half the columns per task
+    (8192, 8192, 8, "cluster"),      # column blocks over a 2-CTA cluster
+])
+def test_gemv_vector_wait_that_runs_out_is_reported(M, N, batch, kernel):
+    """The GEMV kernels wait (bounded) for their bulk-copied vectors; a hook
+    announces the copies but issues none, so that wait can only run out."""
+    import torch
+    from tests._gpu import run_gemv
+    from tests.test_gemv_gpu import check
+    g = PCG32(95 + batch)
+    A = torch.from_numpy(g.uniform_f32((M, N))).cuda()
+    X = torch.from_numpy(g.uniform_f32((batch, N))).cuda()
+    Y = torch.zeros((batch, M), device="cuda")
+    s = int(torch.cuda.current_stream().cuda_stream)
+    plan = gtg.plan_gemv(M, N, A.data_ptr(), N, X.data_ptr(), N, Y.data_ptr(), M, batch)
+    assert (plan["bm"] == 1) == (kernel == "stream") and (plan["cluster"] > 1) == (kernel == "cluster"), plan
+    gtg.gtg_set_wait_limit_ns(SHORT_LIMIT_NS)
+    try:
+        gtg.gtg_test_skip_vector_copy(True)
+        st = gtg.gemv_f32(M, N, A.data_ptr(), N, X.data_ptr(), N, Y.data_ptr(), M, batch, s)
+        status = gtg.gtg_sync_status(s)
+    finally:
+        gtg.gtg_test_skip_vector_copy(False)
+        gtg.gtg_set_wait_limit_ns(0)
+    assert st == gtg.GTG_OK
+    assert status == gtg.GTG_ERR_TIMEOUT
+    # the context still works and the hook was used up
+    Ah, Xh = g.uniform_f32((333, 1024)), g.uniform_f32((batch, 1024))
+    check(Ah, Xh, run_gemv(Ah, Xh))
