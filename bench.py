@@ -37,6 +37,13 @@ METRIC = "GEMM TFLOP/s (% of GB300 peak) and GEMV HBM GB/s (% of peak), 1 GPU"
 GEMM_SHAPE = (8192, 8192, 8192)
 GEMV_SHAPE = (4096, 4096)
 GEMV_GROUP = 8
+# convolutional layers of a residual image network: (name, N, H, W, C, CO, KH, KW, stride, pad, timed calls)
+CONV_LAYERS = [
+    ("f4: bf16 conv 3x3 64->64, 56x56, batch 32, pad 1", 32, 56, 56, 64, 64, 3, 3, 1, 1, 20),
+    ("f4: bf16 conv 3x3 256->256, 14x14, batch 64, pad 1", 64, 14, 14, 256, 256, 3, 3, 1, 1, 20),
+    ("f4: bf16 conv 1x1 256->1024, 14x14, batch 64", 64, 14, 14, 256, 1024, 1, 1, 1, 0, 20),
+    ("f4: bf16 conv 7x7/2 3->64, 224x224, batch 16, pad 3", 16, 224, 224, 3, 64, 7, 7, 2, 3, 10),
+]
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -52,6 +59,8 @@ def parse_args():
     p.add_argument("--only-ablation", action="store_true",
                    help="run only the pages' kernel designs beside the library's (prints their table)")
     p.add_argument("--ablation-iters", type=int, default=0, help="timed launches per ablation kernel (0: default)")
+    p.add_argument("--only-conv", type=int, default=None, metavar="IDX",
+                   help="run only convolutional layer IDX of the sweep, three calls (for profiling)")
     return p.parse_args()
 
 
@@ -348,6 +357,36 @@ def gpu_arm(args, rank, world, local_rank):
     return result
 
 
+def only_conv(idx, local_rank):
+    """Three conv2d_nhwc calls on one layer of CONV_LAYERS (BF16, seeded normal inputs)."""
+    import numpy as np
+    import torch
+
+    import gemv_tiled_gemm_gb300 as gtg
+    from seeded import PCG32
+
+    torch.cuda.set_device(local_rank)
+    name, N, H, W, C, CO, KH, KW, st, pd, _ = CONV_LAYERS[idx]
+    g = PCG32(20 + C + CO)
+    X = torch.from_numpy(g.normal_bf16((N, H, W, C)).view(np.int16)).cuda()
+    Wt = torch.from_numpy(g.normal_bf16((KH, KW, C, CO), (KH * KW * C) ** -0.5).view(np.int16)).cuda()
+    OH, OW = gtg.conv_out_size(H, W, KH, KW, st, pd)
+    Y = torch.empty((N, OH, OW, CO), device="cuda")
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for _ in range(3):
+        e0.record(s)
+        rc = gtg.conv2d_nhwc("bf16", N, H, W, C, CO, KH, KW, st, st, pd, pd, 1, 1, X.data_ptr(), Wt.data_ptr(),
+                             Y.data_ptr(), None, s.cuda_stream)
+        e1.record(s)
+        assert rc == gtg.GTG_OK, rc
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    assert gtg.gtg_sync_status(s.cuda_stream) == gtg.GTG_OK
+    return {"config": name, "ms_per_call": [round(t, 4) for t in times]}
+
+
 def time_launches(fn, iters, stream):
     import torch
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -472,10 +511,8 @@ def sweep(dev, stream, peaks, l2):
                     "peak_name": "bf16 burst", "frac": round(tf / bf16_peak, 4),
                     "im2col_bytes": 0 if direct else M * ((K + 7) // 8 * 8) * 2})
 
-    conv_cfg("f4: bf16 conv 3x3 64->64, 56x56, batch 32, pad 1", 32, 56, 56, 64, 64, 3, 3, 1, 1, 20)
-    conv_cfg("f4: bf16 conv 3x3 256->256, 14x14, batch 64, pad 1", 64, 14, 14, 256, 256, 3, 3, 1, 1, 20)
-    conv_cfg("f4: bf16 conv 1x1 256->1024, 14x14, batch 64", 64, 14, 14, 256, 1024, 1, 1, 1, 0, 20)
-    conv_cfg("f4: bf16 conv 7x7/2 3->64, 224x224, batch 16, pad 3", 16, 224, 224, 3, 64, 7, 7, 2, 3, 10)
+    for layer in CONV_LAYERS:
+        conv_cfg(*layer)
     torch.cuda.empty_cache()
 
     batched_cfg("f2: bf16 strided batch 16 x 2048^3", 16, 2048, 2048, 2048, 20)
@@ -675,6 +712,10 @@ def main():
         res = reference_arm(args, rank, world)
         if res is not None:
             print(json.dumps(res), flush=True)
+        return 0
+
+    if args.only_conv is not None:
+        print(json.dumps(only_conv(args.only_conv, local_rank)), flush=True)
         return 0
 
     if args.only_ablation:
