@@ -299,7 +299,7 @@ def gpu_arm(args, rank, world, local_rank):
     gv_files = ["gemv.cu", "gemv_kernels.cuh", "ptx.cuh"]
     gemm_kernel = ("tc_gemm_pair_kernel (CTA pair, 256x256 tile)" if plan.get("cluster") == 2
                    else f"tc_gemm_kernel<bf16, BN={plan.get('bn')}>")
-    gemv_kernel = {1: "gemv_stream_kernel<batch=1>", 4: "gemv_split_kernel"}.get(vplan.get("bm"), "gemv_kernel")
+    gemv_kernel = {1: "gemv_stream_kernel<batch=1>", 4: "gemv_blocks_kernel"}.get(vplan.get("bm"), "gemv_kernel")
     roofline = {"bound": "tensor", "achieved": round(gemm_tflops / world, 1), "peak": bf16_peak,
                 "unit": "TFLOP/s", "frac": round(gemm_tflops / world / bf16_peak, 4),
                 "traffic": committed_traffic("gemm_bf16_8192", tc_files),

@@ -78,7 +78,7 @@ int max_active_clusters(const DeviceInfo &dev, const GemvArgs &g, int cluster, i
     return n;
 }
 
-// Shared memory of gemv_cluster_kernel: x blocks, per-task partials, per-row partials.
+// Shared memory of gemv_blocks_kernel over a cluster: x blocks, per-task partials, per-row partials.
 int cluster_smem(const GemvArgs &g, int rows_cl, int chunk) {
     const int64_t groups = (rows_cl + kSplitRows - 1) / kSplitRows;
     return static_cast<int>((g.batch * int64_t{chunk} + groups * kSplitSegs * kSplitRows * g.batch +

@@ -54,7 +54,7 @@ struct Params {
     int nchunks;
     const float *bias;   // epilogue: y = act(acc + bias[row]); null for none
     int act;
-    int ublock;          // gemv_cluster_kernel: 16-byte units per column block
+    int ublock;          // gemv_blocks_kernel: 16-byte units per column block
     int x_bulk;          // x rows 16-byte aligned, ldx and N multiples of 4: stage x by bulk copies
     int *status;         // the library's device status word (set on a timed-out wait)
     unsigned long long wait_limit_ns;   // bound of every mbarrier wait
@@ -467,150 +467,31 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const Params p
     }
 }
 
-// Three or more vectors: a warp's task is ROWS rows x one of WC column
-// segments, so every x value read from shared memory serves ROWS rows (the
-// x reads, not the matrix, are the per-element cost at batch 8) while the
-// few rows per SM still give every warp work. Each task's per-row partial
-// sums go to shared memory and are added in segment order after a barrier,
-// so the result does not depend on scheduling.
-template <typename T, int BATCH, int ROWS, int WC, int U, int kThreads>
-__global__ void __launch_bounds__(kThreads, 1) gemv_split_kernel(const Params p) {
-    constexpr int kWarps = kThreads / 32;
-    constexpr int VE = Elem<T>::kVec;
-    extern __shared__ float4 xs_raw[];
-    __shared__ __align__(8) unsigned long long xbar;
-    float *xs = reinterpret_cast<float *>(xs_raw);
-    float *part = xs + BATCH * p.chunk;   // [group][segment][row][batch]
-    const T *A = static_cast<const T *>(p.A);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r_begin = static_cast<int>(static_cast<long long>(p.M) * blockIdx.x / gridDim.x);
-    const int r_end = static_cast<int>(static_cast<long long>(p.M) * (blockIdx.x + 1) / gridDim.x);
-    const int rows = r_end - r_begin;
-    const int ngroups = (rows + ROWS - 1) / ROWS;
-    const int ntasks = ngroups * WC;
-    const int nu = p.N / VE;
-    const int segu = ((nu + WC - 1) / WC + 31) / 32 * 32;   // 16-byte units per segment
-    const uint32_t bar = ptx::smem_addr(&xbar);
-
-    if (p.x_bulk && threadIdx.x == 0) {
-        ptx::mbar_init(bar, 1);
-        ptx::fence_barrier_init();
-    }
-    if (threadIdx.x < 32) {
-        const uint32_t bytes = min(4096u, static_cast<uint32_t>(nu) * 16u);
-        for (int r = r_begin + static_cast<int>(threadIdx.x); bytes > 0 && r < r_end; r += 32)
-            ptx::prefetch_l2(A + static_cast<long long>(r) * p.lda, bytes);
-    }
-    ptx::wait_prior_grid();
-    ptx::allow_next_grid();
-    if (p.x_bulk) {
-        __syncthreads();   // the barrier is initialised
-        stage_x_bulk<BATCH>(xs, p, bar);
-    }
-
-    // the current task: its rows and its segment [j0, j1) of 16-byte units
-    const T *arow[ROWS];
-    int j0 = 0, j1 = 0;
-    auto setup = [&](int task) {
-        const int rg = task / WC, cs = task - rg * WC;
-#pragma unroll
-        for (int r = 0; r < ROWS; ++r)
-            arow[r] = A + static_cast<long long>(min(r_begin + rg * ROWS + r, r_end - 1)) * p.lda;
-        j0 = cs * segu;
-        j1 = min(j0 + segu, nu);
-    };
-    auto load = [&](int jb, float4 (&dst)[U][ROWS]) {
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int j = jb + 32 * u + lane;
-#pragma unroll
-            for (int r = 0; r < ROWS; ++r)
-                dst[u][r] = j < j1 ? ld16(arow[r] + VE * j) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    };
-
-    // the first task's first loads go out before x has arrived
-    float4 nxt[U][ROWS];
-    if (warp < ntasks) {
-        setup(warp);
-        if (j0 < j1) load(j0, nxt);
-    }
-    bool ok = true;
-    if (p.x_bulk) {
-        ok = __all_sync(0xFFFFFFFFu, wait_x(bar, p));   // warp-uniform: shuffles follow
-    } else {
-        stage_x<BATCH, kThreads>(xs, p, 0, p.N);
-        __syncthreads();
-    }
-
-    for (int task = warp; ok && task < ntasks; task += kWarps) {
-        if (task != warp) {
-            setup(task);
-            if (j0 < j1) load(j0, nxt);
-        }
-        const int cs = task % WC;
-        float acc[ROWS][BATCH];
-#pragma unroll
-        for (int r = 0; r < ROWS; ++r)
-#pragma unroll
-            for (int b = 0; b < BATCH; ++b) acc[r][b] = 0.f;
-        for (int jb = j0; jb < j1; jb += 32 * U) {
-            float4 cur[U][ROWS];
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-#pragma unroll
-                for (int r = 0; r < ROWS; ++r) cur[u][r] = nxt[u][r];
-            if (jb + 32 * U < j1) load(jb + 32 * U, nxt);
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int j = jb + 32 * u + lane;
-                if (j < j1) fma_unit<T, ROWS, BATCH>(acc, cur[u], xs, p.chunk, VE * j);
-            }
-        }
-        if (cs == WC - 1) {
-            const int jt = VE * nu + lane;   // fewer than VE trailing entries
-            if (jt < p.N) {
-#pragma unroll
-                for (int r = 0; r < ROWS; ++r) {
-                    const float a = Elem<T>::one(arow[r] + jt);
-#pragma unroll
-                    for (int b = 0; b < BATCH; ++b) acc[r][b] = fmaf(a, xs[b * p.chunk + jt], acc[r][b]);
-                }
-            }
-        }
-        store_task_totals<ROWS, BATCH>(acc, part + static_cast<long long>(task) * ROWS * BATCH, lane);
-    }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < rows * BATCH; idx += kThreads) {
-        const int rl = idx / BATCH, b = idx - rl * BATCH;
-        const int rg = rl / ROWS, r = rl - rg * ROWS;
-        float v = 0.f;
-#pragma unroll
-        for (int cs = 0; cs < WC; ++cs) v += part[((rg * WC + cs) * ROWS + r) * BATCH + b];
-        p.y[static_cast<long long>(b) * p.ldy + r_begin + rl] = apply_epilogue(v, p.bias, r_begin + rl, p.act);
-    }
-}
-
-// Three or more vectors whose staged x would not fit one CTA's shared memory
-// (or would leave it too little): a cluster of C CTAs shares one block of
-// rows, and CTA c of the cluster takes column block c, so it stages only its
-// 1/C of every vector. Within a CTA the work is that of gemv_split_kernel
-// over its column block. Each CTA leaves one partial sum per (row, vector)
-// in its shared memory; after a cluster barrier every CTA finishes a share
-// of the rows by adding the C partials, read through distributed shared
-// memory, in rank order (deterministic), and a second cluster barrier keeps
-// every CTA's shared memory alive until the others have read it.
+// Three or more vectors (and vectors too large for one CTA's shared memory at
+// any batch): the rows are split into tasks of ROWS rows x one of WC column
+// segments, so every x value read from shared memory serves ROWS rows (at
+// batch 8 the x reads, not the matrix, are the per-element cost) while the
+// few rows per SM still give every warp work. A task's warp totals
+// (reduce-scatter) go to shared memory and are added in segment order after
+// a barrier, so the result does not depend on scheduling.
 //
-// Column blocks are ub = p.ublock 16-byte units wide (the last one takes the
-// rest, plus the N % VE trailing entries); p.chunk >= ub * VE + VE.
-template <typename T, int BATCH, int ROWS, int WC, int U, int kThreads>
-__global__ void __launch_bounds__(kThreads, 1) gemv_cluster_kernel(const Params p) {
+// CLUSTER: launched as clusters of C CTAs (else C = 1, a plain launch), which
+// share one block of rows: CTA c of the cluster takes column block c
+// (p.ublock 16-byte units; the last block takes the rest and the N % VE
+// trailing entries) and stages only its 1/C of every vector. With C > 1 each
+// CTA leaves one partial sum per (row, vector) in its shared memory; after a
+// cluster barrier every CTA finishes a share of the rows by adding the C
+// partials, read through distributed shared memory, in rank order, and a
+// second cluster barrier keeps every CTA's shared memory alive until the
+// others have read it. p.chunk >= (block width + 1) * VE.
+template <typename T, int BATCH, int ROWS, int WC, int U, int kThreads, bool CLUSTER>
+__global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p) {
     constexpr int kWarps = kThreads / 32;
     constexpr int VE = Elem<T>::kVec;
     extern __shared__ float4 xs_raw[];
     __shared__ __align__(8) unsigned long long xbar;
-    const int C = static_cast<int>(ptx::cluster_nctarank());
-    const int c = static_cast<int>(ptx::cluster_ctarank());
+    const int C = CLUSTER ? static_cast<int>(ptx::cluster_nctarank()) : 1;
+    const int c = CLUSTER ? static_cast<int>(ptx::cluster_ctarank()) : 0;
     const int cid = static_cast<int>(blockIdx.x) / C, ncl = static_cast<int>(gridDim.x) / C;
     const int r_begin = static_cast<int>(static_cast<long long>(p.M) * cid / ncl);
     const int r_end = static_cast<int>(static_cast<long long>(p.M) * (cid + 1) / ncl);
@@ -728,6 +609,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_cluster_kernel(const Params 
         store_task_totals<ROWS, BATCH>(acc, part + static_cast<long long>(task) * ROWS * BATCH, lane);
     }
     __syncthreads();
+    if (C == 1) {
+        // one CTA holds whole rows: its segment sums are the totals
+        for (int idx = threadIdx.x; idx < rows * BATCH; idx += kThreads) {
+            const int rl = idx / BATCH, b = idx - rl * BATCH;
+            const int rg = rl / ROWS, r = rl - rg * ROWS;
+            float v = 0.f;
+#pragma unroll
+            for (int cs = 0; cs < WC; ++cs) v += part[((rg * WC + cs) * ROWS + r) * BATCH + b];
+            p.y[static_cast<long long>(b) * p.ldy + r_begin + rl] = apply_epilogue(v, p.bias, r_begin + rl, p.act);
+        }
+        return;
+    }
     // this CTA's partial per (row, vector): its segments added in order
     for (int idx = threadIdx.x; idx < rows * BATCH; idx += kThreads) {
         const int rl = idx / BATCH, b = idx - rl * BATCH;
@@ -749,9 +642,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_cluster_kernel(const Params 
     ptx::cluster_sync();   // no CTA leaves while another may still read its shared memory
 }
 
-// Kernel choice, for aligned rows with x in one staging chunk: batch <= 2 ->
-// gemv_stream_kernel (32 warps, one row each); batch >= 3 ->
-// gemv_split_kernel (16 warps, 4 rows x half the columns per task).
+// Kernel choice, for aligned rows: batch <= 2 with x in one staging chunk ->
+// gemv_stream_kernel (32 warps, one row each); batch >= 3 with x in one CTA ->
+// gemv_blocks_kernel without a cluster (16 warps, 4 rows x half the columns
+// per task); x too large for one CTA -> gemv_blocks_kernel over a cluster.
 // Otherwise gemv_kernel (16 warps, two rows per task, x chunked if needed).
 constexpr int kStreamThreads = 1024;
 constexpr int kRoundThreads = 512;
@@ -772,10 +666,10 @@ void *pick(int kind, bool vec) {
     }
     if (kind == kSplit)
         return reinterpret_cast<void *>(
-            gemv_split_kernel<T, BATCH, kSplitRows, kSplitSegs, split_unroll(sizeof(T)), kRoundThreads>);
+            gemv_blocks_kernel<T, BATCH, kSplitRows, kSplitSegs, split_unroll(sizeof(T)), kRoundThreads, false>);
     if (kind == kCluster)
         return reinterpret_cast<void *>(
-            gemv_cluster_kernel<T, BATCH, kSplitRows, kSplitSegs, split_unroll(sizeof(T)), kRoundThreads>);
+            gemv_blocks_kernel<T, BATCH, kSplitRows, kSplitSegs, split_unroll(sizeof(T)), kRoundThreads, true>);
     return vec ? reinterpret_cast<void *>(gemv_kernel<T, BATCH, kRows, kUnroll, true, kRoundThreads>)
                : reinterpret_cast<void *>(gemv_kernel<T, BATCH, kRows, kUnroll, false, kRoundThreads>);
 }
