@@ -64,6 +64,8 @@ SIGNATURES = {
     "gemm_strided_batched": (_int, [_int, _i64, _i64, _i64, _ptr, _i64, _i64, _ptr, _i64, _i64, _ptr, _i64, _i64,
                                     _i64, _ep, _ptr]),
     "gemv_f32_ex": (_int, [_i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _int, _ep, _ptr]),
+    "gemm_host": (_int, [_int, _i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ep]),
+    "gtg_pool_trim": (_int, []),
     "conv2d_nhwc": (_int, [_int] + [_i64] * 13 + [_ptr, _ptr, _ptr, _ep, _ptr]),
     "gemv_bf16": (_int, [_i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _int, _ptr]),
     "gemv_bf16_ex": (_int, [_i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _int, _ep, _ptr]),
@@ -183,6 +185,15 @@ def gemv_bf16(M, N, A, lda, x, ldx, y, ldy, batch, stream=0) -> int:
 
 def gemv_bf16_ex(M, N, A, lda, x, ldx, y, ldy, batch, ep=None, stream=0) -> int:
     return lib().gemv_bf16_ex(M, N, A, lda, x, ldx, y, ldy, batch, ctypes.byref(ep) if ep else None, stream)
+
+
+def gemm_host(precision, M, N, K, A, lda, B, ldb, C, ldc, ep=None) -> int:
+    prec = PREC[precision] if isinstance(precision, str) else precision
+    return lib().gemm_host(prec, M, N, K, A, lda, B, ldb, C, ldc, ctypes.byref(ep) if ep else None)
+
+
+def gtg_pool_trim() -> int:
+    return lib().gtg_pool_trim()
 
 
 def conv2d_nhwc(precision, N, H, W, C, CO, KH, KW, stride_h, stride_w, pad_h, pad_w, dil_h, dil_w, X, Wt, Y,
@@ -313,9 +324,10 @@ def matmul(A, B, precision: str = "f32", out=None, stream=None, bias=None, activ
     A (M x K) and B (K x N) are row-major torch tensors: float32 for "f32" and
     "tf32", bfloat16 for "bf16", float16 for "f16". `bias` (N float32 values, one per output
     column) and `activation` ("none" or "relu") form the fused epilogue.
-    CUDA tensors are used in place. Host tensors are copied to the device
-    (pinned host memory makes the copies asynchronous) and the result is
-    copied back into a host tensor.
+    CUDA tensors are used in place (on `stream`). Host tensors go through
+    gemm_host, which copies A in and C out in blocks of rows while the blocks
+    before and after them are multiplied (pinned host memory lets the copies
+    overlap); the call then returns a host tensor and has synchronised.
     """
     torch = _torch()
     want = getattr(torch, _IN_DTYPE[precision])
@@ -324,14 +336,27 @@ def matmul(A, B, precision: str = "f32", out=None, stream=None, bias=None, activ
     if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
         raise ValueError(f"shape mismatch {tuple(A.shape)} x {tuple(B.shape)}")
     host = not A.is_cuda
+    M, K = A.shape
+    N = B.shape[1]
     if host:
-        dA = A.to("cuda", non_blocking=True)
-        dB = B.to("cuda", non_blocking=True)
-    else:
-        dA, dB = A, B
-    M, K = dA.shape
-    N = dB.shape[1]
-    if out is not None and not host:
+        # host operands: gemm_host overlaps the copies with the product
+        if B.is_cuda:
+            raise ValueError("A and B must both be host tensors or both device tensors")
+        C = out if out is not None else torch.empty((M, N), dtype=torch.float32, pin_memory=A.is_pinned())
+        if C.is_cuda or C.dtype != torch.float32 or tuple(C.shape) != (M, N):
+            raise ValueError("out must be a host float32 tensor of shape (M, N)")
+        hbias = None
+        if bias is not None:
+            if bias.dtype != torch.float32 or bias.numel() != N:
+                raise ValueError(f"bias must hold {N} float32 values")
+            hbias = bias.reshape(-1).cpu().contiguous()
+        ep = epilogue(hbias.data_ptr() if hbias is not None else 0, activation)
+        st = gemm_host(PREC[precision], M, N, K, A.data_ptr(), _rowmajor_ld(A, "A"), B.data_ptr(),
+                       _rowmajor_ld(B, "B"), C.data_ptr(), _rowmajor_ld(C, "C"), ep)
+        _check(st, "gemm_host")
+        return C
+    dA, dB = A, B
+    if out is not None:
         C = out
     else:
         C = torch.empty((M, N), dtype=torch.float32, device=dA.device)
@@ -341,12 +366,6 @@ def matmul(A, B, precision: str = "f32", out=None, stream=None, bias=None, activ
                              _rowmajor_ld(dB, "B"), C.data_ptr(), _rowmajor_ld(C, "C"), ep,
                              _stream_handle(stream))
     _check(st, f"gemm_{precision}")
-    if host:
-        res = out if out is not None else torch.empty((M, N), dtype=torch.float32,
-                                                      pin_memory=A.is_pinned())
-        res.copy_(C, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
-        return res
     return C
 
 

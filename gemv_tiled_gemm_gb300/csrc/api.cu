@@ -440,6 +440,43 @@ const char *gtg_status_string(gtg_status s) {
     }
 }
 
+gtg_status gemm_host(int precision, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+                     int64_t ldb, float *C, int64_t ldc, const gtg_epilogue *ep) {
+    if (precision < GTG_PREC_F32 || precision > GTG_PREC_F16) return GTG_ERR_INVALID_VALUE;
+    GemmArgs g{precision, M, N, K, A, lda, B, ldb, C, ldc};
+    if (ep) {
+        g.bias = ep->bias;
+        g.act = ep->activation;
+    }
+    gtg_status st = validate_gemm(g);
+    if (st != GTG_OK || M == 0 || N == 0) return st;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != GTG_OK) return st;
+    if (!(dev.cc_major == 10 && dev.cc_minor == 3)) return GTG_ERR_UNSUPPORTED;
+    cudaError_t e = cudaSuccess;
+    st = gemm_host_pipeline(dev, g, run_gemm, &e);
+    if (e != cudaSuccess) note_cuda_error(e);
+    if (st != GTG_OK) return st;
+    // the call has synchronised: report (and clear) what the kernels latched
+    int v = 0;
+    const int zero = 0;
+    if ((e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int))) != cudaSuccess ||
+        (e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int))) != cudaSuccess) {
+        note_cuda_error(e);
+        return GTG_ERR_DEVICE;
+    }
+    return v;
+}
+
+gtg_status gtg_pool_trim(void) {
+    const cudaError_t e = ws_trim();
+    if (e != cudaSuccess) {
+        note_cuda_error(e);
+        return GTG_ERR_DEVICE;
+    }
+    return GTG_OK;
+}
+
 gtg_status gtg_sync_status(cudaStream_t stream) {
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) {
@@ -525,7 +562,7 @@ gtg_status conv2d_nhwc(int precision, int64_t N, int64_t H, int64_t W, int64_t C
     void *P = nullptr;
     if (!direct) {
         lda = (K + 7) / 8 * 8;   // 16-byte aligned rows for the tensor-memory-access path
-        cudaError_t e = cudaMallocAsync(&P, static_cast<size_t>(M * lda * c.elem), stream);
+        cudaError_t e = ws_alloc(&P, static_cast<size_t>(M * lda * c.elem), stream);
         if (e == cudaSuccess) e = im2col_launch(dev, c, P, lda, stream);
         if (e != cudaSuccess) {
             note_cuda_error(e);

@@ -300,8 +300,7 @@ cudaError_t launch_one(const GemmArgs &g, int splits, cudaStream_t stream) {
     float *ws = nullptr;
     cudaError_t e;
     if (splits > 1) {
-        e = cudaMallocAsync(reinterpret_cast<void **>(&ws), static_cast<size_t>(splits) * g.M * g.N * sizeof(float),
-                            stream);
+        e = ws_alloc(reinterpret_cast<void **>(&ws), static_cast<size_t>(splits) * g.M * g.N * sizeof(float), stream);
         if (e != cudaSuccess) return e;
     }
     simt_gemm_kernel<T, BM, BN, VEC><<<grid, L::THREADS, 0, stream>>>(

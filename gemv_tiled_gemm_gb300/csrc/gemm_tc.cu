@@ -717,8 +717,7 @@ cudaError_t begin_split(const GemmArgs &g, const gtg_plan &plan, TcParams &p, fl
     }
     p.num_units = p.num_tiles * p.splits;
     if (p.splits == 1) return cudaSuccess;
-    cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(ws),
-                                    static_cast<size_t>(p.splits) * g.M * g.N * sizeof(float), stream);
+    cudaError_t e = ws_alloc(reinterpret_cast<void **>(ws), static_cast<size_t>(p.splits) * g.M * g.N * sizeof(float), stream);
     if (e != cudaSuccess) return e;
     p.C = *ws;
     p.ldc = g.N;
@@ -872,8 +871,7 @@ cudaError_t launch_impl(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
     float *bt = nullptr;
     if constexpr (S::B_KMAJOR) {
         const int64_t ldbt = (g.K + 3) / 4 * 4;   // 16-byte rows for the tensor map
-        cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&bt),
-                                        static_cast<size_t>(g.batch * g.N * ldbt) * 4, stream);
+        cudaError_t e = ws_alloc(reinterpret_cast<void **>(&bt), static_cast<size_t>(g.batch * g.N * ldbt) * 4, stream);
         if (e != cudaSuccess) return e;
         const dim3 tgrid(static_cast<unsigned>((g.N + 31) / 32),
                          static_cast<unsigned>(std::min<int64_t>((g.K + 31) / 32, 65535)),

@@ -105,6 +105,17 @@ cudaError_t ablation_gemm_launch(int variant, const GemmArgs &g, cudaStream_t st
 cudaError_t ablation_gemv_launch(int variant, const GemvArgs &g, cudaStream_t stream);
 bool grid_too_large(int64_t M, int64_t N, int tile);
 
+// ---- host operands (host.cu): the pipeline of gemm_host; `run` launches one
+// block's product on a stream. Synchronous; on a CUDA error sets *cuda_error.
+gtg_status gemm_host_pipeline(const DeviceInfo &dev, const GemmArgs &g, gtg_status (*run)(const GemmArgs &, cudaStream_t),
+                              cudaError_t *cuda_error);
+
+// ---- device workspaces (pool.cu): stream-ordered allocations from the
+// library's own pool on the current device (release with cudaFreeAsync on a
+// stream ordered after the last use); ws_trim returns the reserved pages.
+cudaError_t ws_alloc(void **p, size_t bytes, cudaStream_t stream);
+cudaError_t ws_trim();
+
 // ---- implicit-GEMM convolution on the tensor cores (gemm_tc.cu): A tiles
 // loaded from X by TMA in im2col mode (16-bit, C % 64 == 0, small windows)
 bool tc_conv_eligible(const DeviceInfo &dev, const ConvArgs &c);

@@ -32,16 +32,18 @@
  *    GTG_ERR_LAUNCH, reported when the launch itself failed). Device-side
  *    failures (a pipeline wait that ran out of time) are latched in a device
  *    status word and returned by gtg_sync_status().
- *  - Allocation: the calls never synchronise. Two paths need a temporary
- *    device buffer and take it from the current device's default
- *    stream-ordered memory pool (cudaMallocAsync on `stream`, returned with
+ *  - Allocation: the calls never synchronise. Paths that need a temporary
+ *    device buffer take it from the library's own stream-ordered memory
+ *    pool on the current device (allocated on `stream`, returned with
  *    cudaFreeAsync on `stream` after use, so the host never waits): the TF32
- *    tensor-core path (B^T, see gemm_tf32) and the SIMT path of small
- *    problems, which splits K and adds the partial products (splits * M * N
- *    * 4 bytes, see gemm_f32). gemv_f32 and the BF16 tensor-core path
- *    allocate nothing; gemm_tf32_noalloc never allocates. Per device the
- *    library keeps only host-side state (device properties and a table of
- *    kernel attributes), created on first use.
+ *    tensor-core path (B^T, see gemm_tf32), products that split K and add
+ *    the partial products (splits * M * N * 4 bytes), the patch matrix of a
+ *    convolution, and gemm_host's device copies. The pool is created on
+ *    first use and keeps up to 1 GiB reserved between calls, so that a call
+ *    after a synchronisation does not map its pages afresh; gtg_pool_trim
+ *    returns them. gemv_f32 allocates nothing; gemm_tf32_noalloc never
+ *    allocates. Per device the library otherwise keeps only host-side state
+ *    (device properties and a table of kernel attributes).
  *  - Thread safety: calls may be made concurrently from several host
  *    threads; the host-side state is guarded by a mutex.
  */
@@ -112,10 +114,10 @@ GTG_API gtg_status gemm_f32(int64_t M, int64_t N, int64_t K,
  * to TF32 precision (10 explicit mantissa bits) by the tensor core.
  * The TF32 tensor-core MMA reads B only K-major, so the call first writes
  * B^T into a temporary buffer of 4 * N * roundup(K, 4) bytes. That buffer
- * comes from the current device's default stream-ordered memory pool
- * (cudaMallocAsync on `stream`) and is returned to it (cudaFreeAsync on
- * `stream`) after the multiply, so it never blocks the host; if the pool
- * cannot supply it the call returns GTG_ERR_LAUNCH and launches nothing.
+ * comes from the library's stream-ordered workspace pool (allocated on
+ * `stream`) and is returned to it (cudaFreeAsync on `stream`) after the
+ * multiply, so it never blocks the host; if the pool cannot supply it the
+ * call returns GTG_ERR_LAUNCH and launches nothing.
  * The tensor-core kernel needs a 16-byte aligned A with lda a multiple of 4
  * (the TMA rules); other layouts are computed by the exact FP32 kernel of
  * gemm_f32, whose result also meets the TF32 accuracy.
@@ -322,6 +324,39 @@ GTG_API gtg_status conv2d_nhwc(int precision, int64_t N, int64_t H, int64_t W, i
                                int64_t pad_h, int64_t pad_w, int64_t dil_h, int64_t dil_w,
                                const void *X, const void *Wt, float *Y,
                                const gtg_epilogue *epilogue, cudaStream_t stream);
+
+/*
+ * gemm_host -- C = act(A * B + bias) with A, B, C (and the bias) in HOST
+ * memory: the end-to-end call for data that is not on the device yet.
+ *   precision  GTG_PREC_F32, _TF32, _BF16 or _F16, as gemm_<precision>
+ *   A, B, C    host pointers, row-major with leading dimensions as gemm_f32;
+ *              A and B of the precision's storage type, C FP32
+ *   epilogue   optional; its bias pointer is a host pointer (N floats)
+ * A goes to the device in blocks of rows and B in panels of columns, in the
+ * order that keeps the rows sent and the columns sent about equal (an output
+ * block needs its rows of A and its columns of B, so this order makes the
+ * most of C computable soonest); each region of C is multiplied as soon as
+ * its pieces are in and copied back while later pieces are still coming in
+ * (three streams of the library's own; A, B and C whole on the device for
+ * the duration of the call, in buffers from the library's workspace pool,
+ * see Allocation above). Page-locked (pinned) host memory lets the copies
+ * run asynchronously and overlap; pageable memory works but serialises them.
+ * Synchronous: returns once C holds the result, with the status
+ * gtg_sync_status would give (GTG_ERR_TIMEOUT if a kernel gave up a wait).
+ * Errors: as gemm_<precision> for the arguments; GTG_ERR_DEVICE when a
+ * copy, allocation or synchronisation fails.
+ */
+GTG_API gtg_status gemm_host(int precision, int64_t M, int64_t N, int64_t K,
+                             const void *A, int64_t lda, const void *B, int64_t ldb,
+                             float *C, int64_t ldc, const gtg_epilogue *epilogue);
+
+/*
+ * gtg_pool_trim -- returns to the driver the device memory that the
+ * library's workspace pools keep reserved between calls (on every device
+ * used so far). Buffers still in use by queued work are not affected.
+ * Errors: GTG_ERR_DEVICE if the driver refuses.
+ */
+GTG_API gtg_status gtg_pool_trim(void);
 
 /*
  * gemm_strided_batched -- `batch` independent products in one call ("Matrix

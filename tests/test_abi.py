@@ -90,6 +90,19 @@ def test_gemm_alignment_and_alias(fn, elem):
     assert st not in (gtg.GTG_ERR_ALIAS, gtg.GTG_ERR_INVALID_VALUE, gtg.GTG_ERR_MISALIGNED)
 
 
+def test_gemm_host_argument_validation():
+    E = gtg.GTG_ERR_INVALID_VALUE
+    f = gtg.gemm_host
+    assert f(9, 4, 4, 4, A, 4, B, 4, C, 4) == E           # no such precision
+    assert f("bf16", 4, 4, 8, A, 7, B, 4, C, 4) == E      # lda < K
+    assert f("f32", 4, 8, 4, A, 4, B, 8, C, 7) == E       # ldc < N
+    assert f("f32", 4, 4, 4, A, 4, B, 4, 0, 4) == E       # null C
+    assert f("tf32", 4, 4, 4, A, 4, B, 4, A + 16, 4) == gtg.GTG_ERR_ALIAS
+    assert f("f16", 4, 4, 4, A + 1, 4, B, 4, C, 4) == gtg.GTG_ERR_MISALIGNED
+    assert f("f32", 4, 4, 4, A, 4, B, 4, C, 4, gtg.epilogue(0, 7)) == E
+    assert f("bf16", 0, 4, 4, 0, 4, 0, 4, 0, 4) == gtg.GTG_OK
+
+
 def test_gemv_argument_validation():
     E = gtg.GTG_ERR_INVALID_VALUE
     f = gtg.gemv_f32
