@@ -408,13 +408,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// ---------------------------------------------------------------- CTA-pair BF16 kernel
+// ---------------------------------------------------------------- CTA-pair kernel
 // Two CTAs of a cluster share one 256 x 256 output tile: each stages its own
 // 128 rows of A and its half (128 columns) of B, and one thread of the even
 // CTA issues tcgen05.mma.cta_group::2 (M = 256), which reads A and B half from
 // each CTA's shared memory and writes each CTA's 128 rows of D into that CTA's
-// TMEM. Per SM this moves 32 KB per 64-deep K slice instead of 48 KB for the
-// same multiply work, so six stages fit and operand delivery keeps up.
+// TMEM. Per SM this moves 32 KB per 128-byte-deep K slice instead of 48 KB for
+// the same multiply work, so six stages fit and operand delivery keeps up.
+// 16-bit B is staged MN-major (two 64-column blocks per CTA); TF32 B is staged
+// from its transpose, K-major like A (128 rows of B^T per CTA).
 //
 // Synchronisation across the pair: both CTAs' TMA loads complete on the even
 // CTA's full barrier (which expects both CTAs' bytes); the MMA thread's
@@ -422,31 +424,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 // CTAs; both CTAs' epilogue warps arrive on the even CTA's accumulator-empty
 // barrier. A cluster barrier after set-up and before exit keeps either CTA
 // from touching a peer that has not initialised its barriers or has left.
+template <bool TF32>
 struct PairShape {
+    static constexpr int ELEM = TF32 ? 4 : 2;
     static constexpr int BM = 128;                 // rows per CTA (256 per pair)
     static constexpr int BN = 256;                 // columns per pair tile
-    static constexpr int BK = 64;                  // BF16 elements = 128 bytes
-    static constexpr int UK = 16;
+    static constexpr int BK = 128 / ELEM;          // K elements in one 128-byte row
+    static constexpr int UK = 32 / ELEM;           // K per tcgen05.mma
     static constexpr int KSTEPS = BK / UK;
     static constexpr int A_BYTES = BM * 128;       // 16 KB
-    static constexpr int BCH_N = 64;               // columns per 128-byte block of B
-    static constexpr int B_CHUNKS = (BN / 2) / BCH_N;
-    static constexpr int BCH_BYTES = BK * 128;     // 8 KB
-    static constexpr int B_BYTES = B_CHUNKS * BCH_BYTES;
+    static constexpr bool B_KMAJOR = TF32;
+    static constexpr int BCH_N = 128 / ELEM;       // MN-major B: columns per 128-byte block
+    static constexpr int B_CHUNKS = B_KMAJOR ? 1 : (BN / 2) / BCH_N;
+    static constexpr int BCH_BYTES = BK * 128;     // MN-major B: one column block, 8 KB
+    static constexpr int B_BYTES = (BN / 2) * 128; // this CTA's half of B: 16 KB either way
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 32 KB per CTA
     static constexpr int STAGES = 6;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int NBARS = 2 * STAGES + 5;
     static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + NBARS * 8 + 16;
-    static constexpr uint32_t IDESC = ptx::make_idesc(1u, 0u, 1u, 2 * BM, BN);
     static constexpr int GROUP = 8;                // pair row-tiles per raster group
+    static_assert(B_KMAJOR || B_CHUNKS * BCH_BYTES == B_BYTES, "MN-major B is whole column blocks");
 };
 
+constexpr int kPairGroup = 8;
+
 __device__ __forceinline__ void pair_tile_coords(int t, const TcParams &p, int &mb, int &nb) {
-    const int per_group = PairShape::GROUP * p.num_n;
+    const int per_group = kPairGroup * p.num_n;
     const int g = t / per_group;
-    const int first = g * PairShape::GROUP;
-    const int gs = min(p.num_m - first, PairShape::GROUP);
+    const int first = g * kPairGroup;
+    const int gs = min(p.num_m - first, kPairGroup);
     const int r = t - g * per_group;
     mb = first + r % gs;
     nb = r / gs;
@@ -458,10 +465,11 @@ __device__ __noinline__ void spin_ns(uint64_t ns) {
     }
 }
 
+template <bool TF32>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const TcParams p) {
-    using S = PairShape;
+    using S = PairShape<TF32>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -535,10 +543,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), 2 * S::STAGE_BYTES);
                     const uint32_t fb = leader_full0 + 8u * s;
                     ptx::tma_load_3d_pair(sA + s * S::A_BYTES, &tmA, fb, kb * S::BK, row0, bi);
+                    if constexpr (S::B_KMAJOR) {
+                        // this CTA's 128 rows of B^T
+                        ptx::tma_load_3d_pair(sB + s * S::B_BYTES, &tmB, fb, kb * S::BK, col0, bi);
+                    } else {
 #pragma unroll
-                    for (int c = 0; c < S::B_CHUNKS; ++c)
-                        ptx::tma_load_3d_pair(sB + s * S::B_BYTES + c * S::BCH_BYTES, &tmB, fb, col0 + c * S::BCH_N,
-                                              kb * S::BK, bi);
+                        for (int c = 0; c < S::B_CHUNKS; ++c)
+                            ptx::tma_load_3d_pair(sB + s * S::B_BYTES + c * S::BCH_BYTES, &tmB, fb,
+                                                  col0 + c * S::BCH_N, kb * S::BK, bi);
+                    }
                 }
             }
             if (!ok) {
@@ -584,8 +597,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < S::KSTEPS; ++k) {
                         const uint64_t ad = ptx::smem_desc_sw128(a0 + k * 32, 16, 1024);
-                        const uint64_t bd = ptx::smem_desc_sw128(b0 + k * S::UK * 128, S::BCH_BYTES, 1024);
-                        ptx::mma_bf16_pair(d_tmem, ad, bd, p.idesc, (kb > u.kb0 || k > 0) ? 1u : 0u);
+                        const uint64_t bd = S::B_KMAJOR
+                                                ? ptx::smem_desc_sw128(b0 + k * 32, 16, 1024)
+                                                : ptx::smem_desc_sw128(b0 + k * S::UK * 128, S::BCH_BYTES, 1024);
+                        const uint32_t accum = (kb > u.kb0 || k > 0) ? 1u : 0u;
+                        if constexpr (TF32)
+                            ptx::mma_tf32_pair(d_tmem, ad, bd, p.idesc, accum);
+                        else
+                            ptx::mma_bf16_pair(d_tmem, ad, bd, p.idesc, accum);
                     }
                     ptx::mma_commit_pair(empty_bar(s), 0x3);
                 }
@@ -920,23 +939,45 @@ cudaError_t launch_impl(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
     return e;
 }
 
-cudaError_t launch_pair(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan, cudaStream_t stream) {
-    using S = PairShape;
+template <bool TF32>
+cudaError_t launch_pair(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan, cudaStream_t stream,
+                        int attr_bit) {
+    using S = PairShape<TF32>;
+    auto kern = tc_gemm_pair_kernel<TF32>;
     {
         AttrCache &ac = attr_cache();
         std::lock_guard<std::mutex> lk(ac.mu);
         const int d = dev.id & 63;
-        if (!(ac.done[d] >> 6 & 1)) {
-            cudaError_t e =
-                cudaFuncSetAttribute(tc_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+        if (!(ac.done[d] >> attr_bit & 1)) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
             if (e != cudaSuccess) return e;
-            ac.done[d] |= 1ull << 6;
+            ac.done[d] |= 1ull << attr_bit;
         }
     }
     CUtensorMap ta, tb;
     if (!encode_3d(&ta, g.prec, g.A, g.K, g.M, g.lda, g.batch, g.strideA, S::BK, S::BM)) return cudaErrorInvalidValue;
-    if (!encode_3d(&tb, g.prec, g.B, g.N, g.K, g.ldb, g.batch, g.strideB, S::BCH_N, S::BK))
-        return cudaErrorInvalidValue;
+    float *bt = nullptr;
+    if constexpr (S::B_KMAJOR) {
+        const int64_t ldbt = (g.K + 3) / 4 * 4;   // 16-byte rows for the tensor map
+        cudaError_t e = ws_alloc(reinterpret_cast<void **>(&bt), static_cast<size_t>(g.batch * g.N * ldbt) * 4, stream);
+        if (e != cudaSuccess) return e;
+        const dim3 tgrid(static_cast<unsigned>((g.N + 31) / 32),
+                         static_cast<unsigned>(std::min<int64_t>((g.K + 31) / 32, 65535)),
+                         static_cast<unsigned>(g.batch));
+        transpose_kernel<<<tgrid, 256, 0, stream>>>(static_cast<const float *>(g.B), g.ldb, bt, ldbt,
+                                                    static_cast<int>(g.K), static_cast<int>(g.N), g.strideB);
+        if ((e = cudaGetLastError()) != cudaSuccess) {
+            cudaFreeAsync(bt, stream);
+            return e;
+        }
+        if (!encode_3d(&tb, g.prec, bt, g.K, g.N, ldbt, g.batch, g.N * ldbt, S::BK, S::BN / 2)) {
+            cudaFreeAsync(bt, stream);
+            return cudaErrorInvalidValue;
+        }
+    } else {
+        if (!encode_3d(&tb, g.prec, g.B, g.N, g.K, g.ldb, g.batch, g.strideB, S::BCH_N, S::BK))
+            return cudaErrorInvalidValue;
+    }
     TcParams p;
     p.C = g.C;
     p.ldc = g.ldc;
@@ -948,7 +989,7 @@ cudaError_t launch_pair(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
     p.tiles_per_batch = p.num_m * p.num_n;
     p.num_tiles = static_cast<int>(p.tiles_per_batch * g.batch);
     p.strideC = g.strideC;
-    p.idesc = idesc16(g.prec, 2 * S::BM, S::BN);
+    p.idesc = TF32 ? ptx::make_idesc(2u, 0u, 0u, 2 * S::BM, S::BN) : idesc16(g.prec, 2 * S::BM, S::BN);
     p.c_vec = c_store_width(g);
     p.status = dev.status;
     p.wait_limit_ns = wait_limit_ns();
@@ -957,33 +998,40 @@ cudaError_t launch_pair(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
     p.act = g.act;
     float *ws = nullptr;
     cudaError_t e = begin_split(g, plan, p, &ws, stream);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(plan.grid));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = static_cast<size_t>(S::SMEM);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel, ta, tb, p);
-    return finish_split(g, p, ws, e, stream);
+    if (e == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(plan.grid));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = static_cast<size_t>(S::SMEM);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        e = cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
+        e = finish_split(g, p, ws, e, stream);
+    }
+    if (bt != nullptr) {
+        // stream-ordered: released once the GEMM has finished reading it
+        cudaError_t f = cudaFreeAsync(bt, stream);
+        if (e == cudaSuccess) e = f;
+    }
+    return e;
 }
 
 void fill_pair_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan, int splits) {
-    using S = PairShape;
+    using S = PairShape<false>;
     const int64_t tiles = g.batch * ((g.M + 2 * S::BM - 1) / (2 * S::BM)) * ((g.N + S::BN - 1) / S::BN);
     const int64_t clusters = std::min<int64_t>(tiles * splits, dev.sms / 2);
     plan->kernel = GTG_KERNEL_TCGEN05;
     plan->bm = 2 * S::BM;
     plan->bn = S::BN;
-    plan->bk = S::BK;
+    plan->bk = g.prec == GTG_PREC_TF32 ? PairShape<true>::BK : S::BK;
     plan->stages = S::STAGES;
     plan->grid = static_cast<int>(2 * clusters);
     plan->threads = kThreads;
@@ -1151,7 +1199,7 @@ void tc_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
                 first = false;
             }
         }
-        if (!tf32 && (dev.sms & 1) == 0 && g_pair_enabled.load()) {
+        if ((dev.sms & 1) == 0 && g_pair_enabled.load()) {
             const double c = tc_cost(dev, g, 2 * kBM, 256, dev.sms / 2, 1.0 / 1.15, want, bk);
             if (c < best_cost) {
                 best_cost = c;
@@ -1210,7 +1258,8 @@ cudaError_t tc_conv_launch(const DeviceInfo &dev, const ConvArgs &c, cudaStream_
 cudaError_t tc_launch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan,
                       cudaStream_t stream) {
     const bool tf32 = g.prec == GTG_PREC_TF32;
-    if (!tf32 && plan.bm == 2 * PairShape::BM) return launch_pair(dev, g, plan, stream);
+    if (plan.bm == 2 * PairShape<false>::BM)
+        return tf32 ? launch_pair<true>(dev, g, plan, stream, 10) : launch_pair<false>(dev, g, plan, stream, 6);
     switch (plan.bn) {
         case 256:
             return tf32 ? launch_impl<true, 256>(dev, g, plan, stream, 0)

@@ -115,15 +115,17 @@ def test_many_tiles_per_cta(prec):
     check_gemm(prec, A, B, C, rows=np.arange(1024, 1152))
 
 
+@pytest.mark.parametrize("prec", ["bf16", "tf32"])
 @pytest.mark.parametrize("M,N,K", [(4252, 4160, 520), (4224, 4160, 72), (4096, 4096, 8)])
-def test_cta_pair_kernel_ragged(M, N, K):
+def test_cta_pair_kernel_ragged(prec, M, N, K):
     # shapes the planner gives to the CTA-pair kernel (256 x 256 tiles): the
     # odd CTA's rows of the last pair tile lie partly or wholly past M, the
-    # last column tile is partial, and K ends inside a 64-wide slice
-    A, B = inputs("bf16", M, N, K, 300 + K)
-    C = run_gemm("bf16", A, B, expect_kernel="tcgen05")
-    assert gtg_plan("bf16", M, N, K)["bm"] == 256
-    check_gemm("bf16", A, B, C, rows=np.concatenate([sample_rows(M, seed=2), np.arange(M - 200, M)]))
+    # last column tile is partial, and K ends inside a 128-byte slice (TF32:
+    # B^T staged K-major in each CTA)
+    A, B = inputs(prec, M, N, K, 300 + K)
+    C = run_gemm(prec, A, B, expect_kernel="tcgen05")
+    assert gtg_plan(prec, M, N, K)["bm"] == 256
+    check_gemm(prec, A, B, C, rows=np.concatenate([sample_rows(M, seed=2), np.arange(M - 200, M)]))
 
 
 # ---- layouts the tensor-memory path cannot take: the SIMT fallback --------------

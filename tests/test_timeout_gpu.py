@@ -48,6 +48,7 @@ def _launch(prec, A, B):
     ("bf16", (1024, 1024, 512), 128),    # single-CTA tensor-core kernel
     ("tf32", (1024, 1024, 512), 128),    # same kernel behind the B^T transpose
     ("bf16", (4096, 4096, 256), 256),    # CTA-pair kernel
+    ("tf32", (4096, 4096, 256), 256),    # CTA-pair kernel, B^T staged K-major
 ])
 def test_wait_that_runs_out_is_reported_and_context_survives(prec, shape, kernel_bm):
     M, N, K = shape
