@@ -11,6 +11,9 @@
 //   * prefetching ("Prefetching"): the next K-slice is loaded into registers
 //     while the current one is multiplied from the other shared buffer, so
 //     one barrier per slice suffices;
+//   * the multiply-adds are issued as packed two-wide FP32 FMAs (sm_100
+//     family), two IEEE fused multiply-adds per instruction, which halves
+//     the instruction count of the inner loop without changing any result;
 //   * boundary handling as on the pages: out-of-range tile elements are
 //     zero-filled, out-of-range outputs are not stored, and no thread leaves
 //     before the barriers.
@@ -71,6 +74,7 @@ struct SimtTile {
     static constexpr int TX = BN / 8;              // threads along N
     static constexpr int TY = BM / 8;              // threads along M
     static constexpr int THREADS = TX * TY;
+
     static constexpr int A_V4 = BM * kBK / 4 / THREADS;   // 4-element A groups per thread
     static constexpr int B_V4 = BN * kBK / 4 / THREADS;
     static_assert(A_V4 >= 1 && B_V4 >= 1, "tile too small for its thread count");
@@ -171,11 +175,19 @@ __global__ void __launch_bounds__(SimtTile<T, BM, BN, VEC>::THREADS)
         }
     };
 
-    float acc[8][8];
+    // The 8 x 8 accumulators in pairs for the packed two-wide FMA: for row
+    // pair p (rows 2p, 2p+1 of the thread's block) and column pair q,
+    // d[p][q][0] = (acc[2p][2q], acc[2p+1][2q+1]) takes (a[2p], a[2p+1]) times
+    // (b[2q], b[2q+1]), and d[p][q][1] = (acc[2p][2q+1], acc[2p+1][2q]) takes
+    // (a[2p], a[2p+1]) times the exchanged columns (b[2q+1], b[2q]). Each lane
+    // of a packed FMA is one IEEE fused multiply-add, so every output sees the
+    // same operations in the same K order as with scalar FMAs (and the same
+    // result).
+    float2 d[4][4][2];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int p = 0; p < 4; ++p)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+        for (int q = 0; q < 4; ++q) d[p][q][0] = d[p][q][1] = make_float2(0.f, 0.f);
 
     const int ntiles = (K + kBK - 1) / kBK;
     if (ntiles > 0) {
@@ -198,12 +210,19 @@ __global__ void __launch_bounds__(SimtTile<T, BM, BN, VEC>::THREADS)
             const float4 a1 = *reinterpret_cast<const float4 *>(&As[cur][k][BM / 2 + ty * 4]);
             const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[cur][k][tx * 4]);
             const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[cur][k][BN / 2 + tx * 4]);
-            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            const float2 ap[4] = {make_float2(a0.x, a0.y), make_float2(a0.z, a0.w), make_float2(a1.x, a1.y),
+                                  make_float2(a1.z, a1.w)};
+            const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
+                                  make_float2(b1.z, b1.w)};
+            const float2 bs[4] = {make_float2(b0.y, b0.x), make_float2(b0.w, b0.z), make_float2(b1.y, b1.x),
+                                  make_float2(b1.w, b1.z)};
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int p = 0; p < 4; ++p)
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+                for (int q = 0; q < 4; ++q) {
+                    d[p][q][0] = __ffma2_rn(ap[p], bp[q], d[p][q][0]);
+                    d[p][q][1] = __ffma2_rn(ap[p], bs[q], d[p][q][1]);
+                }
         }
         if (t + 1 < ntiles) {
             store_a(cur ^ 1);
@@ -212,6 +231,16 @@ __global__ void __launch_bounds__(SimtTile<T, BM, BN, VEC>::THREADS)
         __syncthreads();
     }
 
+    float acc[8][8];
+#pragma unroll
+    for (int p = 0; p < 4; ++p)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            acc[2 * p][2 * q] = d[p][q][0].x;
+            acc[2 * p + 1][2 * q + 1] = d[p][q][0].y;
+            acc[2 * p][2 * q + 1] = d[p][q][1].x;
+            acc[2 * p + 1][2 * q] = d[p][q][1].y;
+        }
     // rows ty*4 + i (i < 4) and BM/2 + ty*4 + i; columns likewise in N.
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
