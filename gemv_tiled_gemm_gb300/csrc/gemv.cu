@@ -36,7 +36,7 @@ struct Layout {
     int threads;
     int grid;
     int cluster;   // CTAs per cluster (column blocks); 1 unless kind == kCluster
-    int ublock;    // kCluster: 16-byte units per column block
+    int ublock;    // kCluster: 4-column units per column block
 };
 
 void *kernel_of(const GemvArgs &g, int kind) {
@@ -120,7 +120,8 @@ Layout layout(const DeviceInfo &dev, const GemvArgs &g) {
         }
     }
     // x does not fit one CTA: split the columns over the CTAs of a cluster
-    const int VE = 16 / g.a_elem;
+    // (units of the blocks kernel's four-column loads)
+    const int VE = 4;
     const int64_t nu = g.N / VE;
     for (int C = 2; C <= 8; C *= 2) {
         int grid = dev.sms / C * C;

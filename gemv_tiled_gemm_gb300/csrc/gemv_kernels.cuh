@@ -54,7 +54,7 @@ struct Params {
     int nchunks;
     const float *bias;   // epilogue: y = act(acc + bias[row]); null for none
     int act;
-    int ublock;          // gemv_blocks_kernel: 16-byte units per column block
+    int ublock;          // gemv_blocks_kernel over a cluster: 4-column units per column block
     int x_bulk;          // x rows 16-byte aligned, ldx and N multiples of 4: stage x by bulk copies
     int *status;         // the library's device status word (set on a timed-out wait)
     unsigned long long wait_limit_ns;   // bound of every mbarrier wait
@@ -97,6 +97,40 @@ struct Elem<uint16_t> {
     }
     static __device__ __forceinline__ float one(const uint16_t *p) {
         return __uint_as_float(static_cast<uint32_t>(ptx::ld_stream_u16(p)) << 16);
+    }
+};
+
+// Four matrix elements per load, for gemv_blocks_kernel: 16 bytes of FP32 or
+// 8 bytes of BF16. With four columns per lane the lanes of a warp read x from
+// shared memory in consecutive 16-byte pieces, so a 128-bit shared load takes
+// four wavefronts; eight BF16 columns per lane would spread them 32 bytes
+// apart and take eight.
+template <typename T>
+struct Quad;
+
+template <>
+struct Quad<float> {
+    using Raw = float4;
+    static __device__ __forceinline__ Raw load(const float *p) { return ptx::ld_stream_f4(p); }
+    static __device__ __forceinline__ Raw zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+    static __device__ __forceinline__ void widen(const Raw &raw, float (&a)[4]) {
+        a[0] = raw.x;
+        a[1] = raw.y;
+        a[2] = raw.z;
+        a[3] = raw.w;
+    }
+};
+
+template <>
+struct Quad<uint16_t> {
+    using Raw = uint2;
+    static __device__ __forceinline__ Raw load(const uint16_t *p) { return ptx::ld_stream_u2(p); }
+    static __device__ __forceinline__ Raw zero() { return make_uint2(0u, 0u); }
+    static __device__ __forceinline__ void widen(const Raw &raw, float (&a)[4]) {
+        a[0] = Elem<uint16_t>::lo(raw.x);
+        a[1] = Elem<uint16_t>::hi(raw.x);
+        a[2] = Elem<uint16_t>::lo(raw.y);
+        a[3] = Elem<uint16_t>::hi(raw.y);
     }
 };
 
@@ -177,6 +211,29 @@ __device__ __forceinline__ void fma_unit(float (&acc)[ROWS][BATCH], const float4
             float s = acc[r][b];
 #pragma unroll
             for (int e = 0; e < VE; ++e) s = fmaf(a[r][e], xv[e], s);
+            acc[r][b] = s;
+        }
+    }
+}
+
+// acc[r][b] += the four elements of row r at column `col` of the staged chunk
+// times vector b (gemv_blocks_kernel's unit).
+template <typename T, int ROWS, int BATCH>
+__device__ __forceinline__ void fma_quad(float (&acc)[ROWS][BATCH], const typename Quad<T>::Raw (&raw)[ROWS],
+                                         const float *xs, int chunk, int col) {
+    float a[ROWS][4];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) Quad<T>::widen(raw[r], a[r]);
+#pragma unroll
+    for (int b = 0; b < BATCH; ++b) {
+        const float4 v = *reinterpret_cast<const float4 *>(xs + b * chunk + col);
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            float s = acc[r][b];
+            s = fmaf(a[r][0], v.x, s);
+            s = fmaf(a[r][1], v.y, s);
+            s = fmaf(a[r][2], v.z, s);
+            s = fmaf(a[r][3], v.w, s);
             acc[r][b] = s;
         }
     }
@@ -477,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const Params p
 //
 // CLUSTER: launched as clusters of C CTAs (else C = 1, a plain launch), which
 // share one block of rows: CTA c of the cluster takes column block c
-// (p.ublock 16-byte units; the last block takes the rest and the N % VE
+// (p.ublock units of VE = 4 columns; the last block takes the rest and the N % VE
 // trailing entries) and stages only its 1/C of every vector. With C > 1 each
 // CTA leaves one partial sum per (row, vector) in its shared memory; after a
 // cluster barrier every CTA finishes a share of the rows by adding the C
@@ -487,7 +544,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const Params p
 template <typename T, int BATCH, int ROWS, int WC, int U, int kThreads, bool CLUSTER>
 __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p) {
     constexpr int kWarps = kThreads / 32;
-    constexpr int VE = Elem<T>::kVec;
+    using Q = Quad<T>;
+    using Raw = typename Q::Raw;
+    constexpr int VE = 4;   // matrix elements per lane load (see Quad)
     extern __shared__ float4 xs_raw[];
     __shared__ __align__(8) unsigned long long xbar;
     const int C = CLUSTER ? static_cast<int>(ptx::cluster_nctarank()) : 1;
@@ -517,9 +576,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
         ptx::fence_barrier_init();
     }
     if (threadIdx.x < 32) {
-        const uint32_t bytes = min(4096u, static_cast<uint32_t>(nub) * 16u);
+        // the first 4 KB of this CTA's part of each row; a bulk prefetch
+        // takes a 16-byte aligned start and length, so it covers the 16-byte
+        // blocks inside [start, end) of the part (rows start on 16 bytes,
+        // a BF16 column block may start 8 bytes past one)
+        const long long skew = static_cast<long long>(VE) * ub0 * static_cast<long long>(sizeof(T)) & 15;
+        const long long lead = skew ? 16 - skew : 0;
+        const long long span = static_cast<long long>(VE) * nub * static_cast<long long>(sizeof(T)) - lead;
+        const uint32_t bytes = span >= 16 ? static_cast<uint32_t>(min(4096ll, span / 16 * 16)) : 0u;
         for (int r = r_begin + static_cast<int>(threadIdx.x); bytes > 0 && r < r_end; r += 32)
-            ptx::prefetch_l2(A + static_cast<long long>(r) * p.lda, bytes);
+            ptx::prefetch_l2(reinterpret_cast<const char *>(A + static_cast<long long>(r) * p.lda) + lead, bytes);
     }
     ptx::wait_prior_grid();
     ptx::allow_next_grid();
@@ -546,17 +612,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
         j0 = cs * segu;
         j1 = min(j0 + segu, nub);
     };
-    auto load = [&](int jb, float4 (&dst)[U][ROWS]) {
+    auto load = [&](int jb, Raw (&dst)[U][ROWS]) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int j = jb + 32 * u + lane;
 #pragma unroll
-            for (int r = 0; r < ROWS; ++r)
-                dst[u][r] = j < j1 ? ld16(arow[r] + VE * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int r = 0; r < ROWS; ++r) dst[u][r] = j < j1 ? Q::load(arow[r] + VE * j) : Q::zero();
         }
     };
 
-    float4 nxt[U][ROWS];
+    Raw nxt[U][ROWS];
     if (warp < ntasks) {
         setup(warp);
         if (j0 < j1) load(j0, nxt);
@@ -585,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
 #pragma unroll
             for (int b = 0; b < BATCH; ++b) acc[r][b] = 0.f;
         for (int jb = j0; jb < j1; jb += 32 * U) {
-            float4 cur[U][ROWS];
+            Raw cur[U][ROWS];
 #pragma unroll
             for (int u = 0; u < U; ++u)
 #pragma unroll
@@ -594,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int j = jb + 32 * u + lane;
-                if (j < j1) fma_unit<T, ROWS, BATCH>(acc, cur[u], xs, p.chunk, VE * j);
+                if (j < j1) fma_quad<T, ROWS, BATCH>(acc, cur[u], xs, p.chunk, VE * j);
             }
         }
         if (cs == WC - 1 && lane < tail) {
@@ -652,10 +717,9 @@ constexpr int kRoundThreads = 512;
 constexpr int kRows = 2;
 constexpr int kUnroll = 4;
 constexpr int kSplitRows = 4, kSplitSegs = 2;
-// 16-byte loads in flight per row in the split kernel: a BF16 load carries 8
-// values, and two of them per row with 4 rows and 8 vectors do not fit the
-// 128 registers a thread of a 512-thread CTA has
-constexpr int split_unroll(int elem_bytes) { return elem_bytes == 2 ? 1 : 2; }
+// Loads of four columns in flight per row in gemv_blocks_kernel: two of
+// 16 bytes (FP32) or four of 8 bytes (BF16), the same bytes either way
+constexpr int split_unroll(int elem_bytes) { return elem_bytes == 2 ? 4 : 2; }
 
 enum Kind { kStream = 0, kSplit = 1, kRound = 2, kCluster = 3 };
 

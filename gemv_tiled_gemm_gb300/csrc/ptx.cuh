@@ -312,6 +312,12 @@ __device__ __forceinline__ float4 ld_stream_f4(const float *p) {
     return v;
 }
 
+__device__ __forceinline__ uint2 ld_stream_u2(const void *p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ uint16_t ld_stream_u16(const uint16_t *p) {
     uint16_t v;
     asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
