@@ -84,6 +84,7 @@ SIGNATURES = {
     "gtg_force_gemm_splits": (None, [_int]),
     "gtg_conv_force_path": (None, [_int]),
     "gtg_test_skip_vector_copy": (None, [_int]),
+    "gtg_gemv_force_path": (None, [_int]),
     "gtg_set_wait_limit_ns": (None, [ctypes.c_uint64]),
     "gtg_test_drop_load": (None, [_int]),
     "gtg_version": (_int, []),
@@ -241,6 +242,15 @@ def last_cuda_error() -> str:
 
 def gtg_force_simt(force: bool) -> None:
     lib().gtg_force_simt(1 if force else 0)
+
+
+GEMV_PATHS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2}
+
+
+def gtg_gemv_force_path(path="auto") -> None:
+    """Tuning/testing hook for BF16 GEMVs of batch 3-8: "auto" (the planner),
+    "cuda_cores", or "tensor_cores" (whenever the layout allows)."""
+    lib().gtg_gemv_force_path(GEMV_PATHS[path] if isinstance(path, str) else int(path))
 
 
 def gtg_test_skip_vector_copy(on: bool) -> None:

@@ -601,6 +601,8 @@ void gtg_test_drop_load(int slice) { tc_drop_next_load(slice); }
 
 void gtg_test_skip_vector_copy(int on) { gemv_skip_next_x(on); }
 
+void gtg_gemv_force_path(int mode) { gemv_force_path(mode); }
+
 void gtg_force_gemm_splits(int splits) { tc_force_splits(splits); }
 
 void gtg_conv_force_path(int mode) { g_conv_mode.store(mode == 1 || mode == 2 ? mode : 0); }

@@ -1116,6 +1116,13 @@ cudaError_t conv_launch_impl(const DeviceInfo &dev, const ConvArgs &c, cudaStrea
 
 
 void tc_set_wait_limit_ns(unsigned long long ns) { g_wait_limit_ns.store(ns ? ns : kWaitLimitNs); }
+bool tma_map_2d(CUtensorMap *map, int prec, const void *base, uint64_t inner, uint64_t outer, uint64_t ld_elems,
+                uint32_t box_inner, uint32_t box_outer) {
+    return encode_3d(map, prec, base, inner, outer, ld_elems, 1, 0, box_inner, box_outer);
+}
+
+int take_test_drop_slice() { return take_drop_slice(); }
+
 unsigned long long wait_limit_setting() { return g_wait_limit_ns.load(); }
 void tc_drop_next_load(int slice) { g_drop_slice.store(slice); }
 void tc_force_splits(int splits) { g_force_splits.store(splits > 0 ? splits : 0); }

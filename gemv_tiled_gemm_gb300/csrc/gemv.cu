@@ -15,6 +15,8 @@ std::atomic<int> g_gemv_skip_x{0};
 }
 
 void gemv_skip_next_x(int on) { g_gemv_skip_x.store(on ? 1 : 0); }
+std::atomic<int> g_gemv_path{0};
+void gemv_force_path(int mode) { g_gemv_path.store(mode == 1 || mode == 2 ? mode : 0); }
 int take_gemv_skip_x() { return g_gemv_skip_x.exchange(0); }
 
 namespace {
@@ -152,6 +154,11 @@ Layout layout(const DeviceInfo &dev, const GemvArgs &g) {
 }  // namespace
 
 void gemv_plan(const DeviceInfo &dev, const GemvArgs &g, gtg_plan *plan) {
+    const int path = g_gemv_path.load();
+    if (path != 1 && gemv_tc_eligible(dev, g, path == 2)) {
+        gemv_tc_plan(dev, g, plan);
+        return;
+    }
     const Layout l = layout(dev, g);
     // One CTA per SM (it fills the register file); every CTA (cluster) owns an
     // equal share of the rows.
@@ -168,6 +175,7 @@ void gemv_plan(const DeviceInfo &dev, const GemvArgs &g, gtg_plan *plan) {
 
 cudaError_t gemv_launch(const DeviceInfo &dev, const GemvArgs &g, const gtg_plan &plan,
                         cudaStream_t stream) {
+    if (plan.kernel == GTG_KERNEL_TCGEN05) return gemv_tc_launch(dev, g, stream);
     const Layout l = layout(dev, g);
     void *kern = kernel_of(g, l.kind);
     if (l.smem > 48 * 1024) {

@@ -1,6 +1,7 @@
 // Internal interface between the C-ABI layer (api.cu) and the kernel files.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -126,12 +127,27 @@ cudaError_t im2col_launch(const DeviceInfo &dev, const ConvArgs &c, void *P, int
 
 // Current bound of in-kernel waits (gtg_set_wait_limit_ns; gemm_tc.cu).
 unsigned long long wait_limit_setting();
+// The K slice whose load a tensor-core kernel leaves out once (gtg_test_drop_load), then -1.
+int take_test_drop_slice();
+// A 2-D tiled tensor map (128-byte swizzle, zero fill outside the tensor):
+// `outer` rows of `inner` elements, `ld_elems` apart; boxes of box_inner x box_outer.
+bool tma_map_2d(CUtensorMap *map, int prec, const void *base, uint64_t inner, uint64_t outer, uint64_t ld_elems,
+                uint32_t box_inner, uint32_t box_outer);
+
+// ---- batched GEMV of a BF16 matrix on the tensor cores (gemv_tc.cu), batch 3..8
+// any_size: also below the size where the CUDA-core kernels are faster
+bool gemv_tc_eligible(const DeviceInfo &dev, const GemvArgs &g, bool any_size);
+void gemv_tc_plan(const DeviceInfo &dev, const GemvArgs &g, gtg_plan *plan);
+cudaError_t gemv_tc_launch(const DeviceInfo &dev, const GemvArgs &g, cudaStream_t stream);
 
 // ---- GEMV (gemv.cu)
 // testing hook: the next GEMV launch that stages x by bulk copies announces
 // them but issues none, so its wait runs out
 void gemv_skip_next_x(int on);
 int take_gemv_skip_x();
+// testing / tuning hook for BF16 GEMVs of batch 3..8: 0 planner's choice,
+// 1 CUDA-core kernels, 2 tensor cores whenever the layout allows
+void gemv_force_path(int mode);
 void gemv_plan(const DeviceInfo &dev, const GemvArgs &g, gtg_plan *plan);
 cudaError_t gemv_launch(const DeviceInfo &dev, const GemvArgs &g, const gtg_plan &plan,
                         cudaStream_t stream);

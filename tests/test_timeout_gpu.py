@@ -109,3 +109,40 @@ def test_gemv_vector_wait_that_runs_out_is_reported(M, N, batch, kernel):
     # the context still works and the hook was used up
     Ah, Xh = g.uniform_f32((333, 1024)), g.uniform_f32((batch, 1024))
     check(Ah, Xh, run_gemv(Ah, Xh))
+
+
+@pytest.mark.parametrize("M,N", [(8192, 4096), (4096, 4096)])
+def test_tensor_core_gemv_wait_that_runs_out_is_reported(M, N):
+    """The BF16 batch-8 GEMV on the tensor cores: one slice load of A left out,
+    so the MMA thread's wait runs out; the kernel drains, frees its tensor
+    memory and returns, and the following calls work."""
+    import torch
+    from tests._gpu import run_gemv
+    from tests._util import parity_ratio
+    import oracle
+    g = PCG32(96)
+    A = torch.from_numpy(g.normal_bf16((M, N)).view(np.int16)).cuda()
+    X = torch.from_numpy(g.uniform_f32((8, N))).cuda()
+    Y = torch.zeros((8, M), device="cuda")
+    s = int(torch.cuda.current_stream().cuda_stream)
+    gtg.gtg_gemv_force_path("tensor_cores")
+    gtg.gtg_set_wait_limit_ns(SHORT_LIMIT_NS)
+    try:
+        plan = gtg.plan_gemv(M, N, A.data_ptr(), N, X.data_ptr(), N, Y.data_ptr(), M, 8, precision="bf16")
+        assert plan["kernel"] == "tcgen05", plan
+        gtg.gtg_test_drop_load(1)
+        st = gtg.gemv_bf16(M, N, A.data_ptr(), N, X.data_ptr(), N, Y.data_ptr(), M, 8, s)
+        status = gtg.gtg_sync_status(s)
+    finally:
+        gtg.gtg_test_drop_load(-1)
+        gtg.gtg_set_wait_limit_ns(0)
+    try:
+        assert st == gtg.GTG_OK
+        assert status == gtg.GTG_ERR_TIMEOUT
+        # the context still works
+        Ah, Xh = g.normal_bf16((300, 1024)), g.uniform_f32((8, 1024))
+        Yh = run_gemv(Ah, Xh, prec="bf16")
+        ref, E = oracle.gemv(bf16_bits_to_f32(Ah), Xh[3])
+        assert parity_ratio(Yh[3], ref, E, "f32", 1024)[1] == 0
+    finally:
+        gtg.gtg_gemv_force_path("auto")

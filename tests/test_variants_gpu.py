@@ -162,6 +162,14 @@ def test_gemv_bf16(M, N, batch):
     _check_gemv(A, X, run_gemv(A, X, prec="bf16"))
 
 
+@pytest.mark.parametrize("M,N,batch", [(4096, 4096, 8), (300, 16, 4), (2000, 1000, 3)])
+def test_gemv_bf16_cuda_cores(cuda_cores, M, N, batch):
+    g = PCG32(1050 + M + N + batch)
+    A = g.normal_bf16((M, N))
+    X = g.uniform_f32((batch, N))
+    _check_gemv(A, X, run_gemv(A, X, prec="bf16"))
+
+
 @pytest.mark.parametrize("lda,a_off", [(1040, 0), (1033, 0), (1032, 3), (1024, 1)])
 def test_gemv_bf16_unaligned_and_padded_rows(lda, a_off):
     g = PCG32(1100 + lda + a_off)
@@ -195,10 +203,20 @@ def test_matvec_bf16_with_epilogue():
     assert torch.equal(yh, y.cpu())
 
 
+@pytest.fixture
+def cuda_cores():
+    """BF16 GEMVs of batch 3..8 on the CUDA-core kernels (the tensor-core
+    path has its own tests)."""
+    gtg.gtg_gemv_force_path("cuda_cores")
+    yield
+    gtg.gtg_gemv_force_path("auto")
+
+
 @pytest.mark.parametrize("M,N,batch,lda,cluster", [(8192, 8192, 8, 8192, 2), (700, 20004, 3, 20008, 2),
                                                    (300, 16384, 8, 16384, 4)])
-def test_gemv_bf16_column_blocks_over_a_cluster(M, N, batch, lda, cluster):
-    """N = 20004 leaves 4 trailing entries after the last 8-entry load."""
+def test_gemv_bf16_column_blocks_over_a_cluster(cuda_cores, M, N, batch, lda, cluster):
+    """Column blocks over a cluster; with 4-column units the second CTA's
+    block of N = 20004 starts 8 bytes past a 16-byte boundary."""
     g = PCG32(1400 + M + batch)
     A = g.normal_bf16((M, N))
     X = g.uniform_f32((batch, N))
