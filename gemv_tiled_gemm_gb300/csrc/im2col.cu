@@ -10,17 +10,18 @@
 // that position lies in the padding. Then Y (N x OH x OW x CO, channels last)
 // = P * B, the GEMM of the tensor-core or SIMT kernels.
 //
-// GB300 form: a warp per output pixel (row of P); every lane writes whole
-// 16-byte chunks of the row (8 BF16/FP16 or 4 FP32 values), so a warp stores
-// 512 contiguous bytes per instruction. Each CTA first builds, in shared
-// memory, a table giving for every chunk (or, when C is not a multiple of the
-// chunk, every element) of a row its offset (dy, dx, channel) from the
-// window's corner; a row then needs one 32-bit decode of (n, oh, ow) and,
-// per chunk, one table read and one 16-byte load of 8 contiguous channels
-// (or 8 element gathers). The kernel is bound by HBM writes of P (the reads
-// of X are mostly L2 hits: each input pixel is read KH*KW times).
+// GB300 form: a warp per output pixel (row of P). When C fills 16-byte
+// chunks (8 BF16/FP16 or 4 FP32 channels) every lane writes whole chunks, so
+// a warp stores 512 contiguous bytes per instruction; each CTA first builds,
+// in shared memory, a table giving for every chunk of a row its offset (dy,
+// dx, channel) from the window's corner, so a row needs one 32-bit decode of
+// (n, oh, ow) and, per chunk, one table read and one 16-byte load. Other
+// channel counts (a first layer's C = 3) take the elements one per lane along
+// the row from a table of every element's offset, so a warp's loads are
+// consecutive elements of each window row of X and its stores consecutive
+// elements of P. Both are bound by HBM writes of P (the reads of X are mostly
+// L2 hits: each input pixel is read about KH*KW / (sh*sw) times).
 #include <algorithm>
-#include <cstring>
 #include <type_traits>
 
 #include "internal.h"
@@ -86,18 +87,15 @@ struct Tap {
 
 constexpr int kMaxTaps = 6144;   // 48 KB of table
 
-// G elements of ESZ bytes make one 16-byte output chunk. VEC: every chunk is
-// G contiguous channels of one tap (C % G == 0), read with one 16-byte load;
-// otherwise each of the G elements is gathered on its own.
-template <int ESZ, bool VEC>
+// G elements of ESZ bytes make one 16-byte output chunk; every chunk is G
+// contiguous channels of one tap (C % G == 0), read with one 16-byte load.
+template <int ESZ>
 __global__ void __launch_bounds__(32 * kWarpsPerCta) im2col_table_kernel(const Im2col g, int K) {
     constexpr int G = 16 / ESZ;
-    using E = typename std::conditional<ESZ == 2, uint16_t, float>::type;
     extern __shared__ Tap tab[];
     const int nchunks = (K + G - 1) / G;                 // 16-byte chunks per row (the last may run into padding)
-    const int ntab = VEC ? nchunks : K;
-    for (int t = threadIdx.x; t < ntab; t += blockDim.x) {
-        const int k = VEC ? t * G : t;
+    for (int t = threadIdx.x; t < nchunks; t += blockDim.x) {
+        const int k = t * G;
         const int kh = k / (g.KW * g.C), r = k - kh * (g.KW * g.C);
         const int kw = r / g.C, ci = r - kw * g.C;
         const int dy = kh * g.dh, dx = kw * g.dw;
@@ -107,7 +105,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) im2col_table_kernel(const I
     __syncthreads();
     const int lane = threadIdx.x & 31;
     const int nwarps = gridDim.x * kWarpsPerCta;
-    const E *X = static_cast<const E *>(g.X);
+    const char *X = static_cast<const char *>(g.X);
     for (int m = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5); m < g.M; m += nwarps) {
         const int ow = m % g.OW, t = m / g.OW;
         const int oh = t % g.OH, n = t / g.OH;
@@ -118,25 +116,70 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) im2col_table_kernel(const I
         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<char *>(g.P) + static_cast<long long>(m) * g.ldp * ESZ);
         for (int q = lane; q < nchunks; q += 32) {
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if constexpr (VEC) {
-                const Tap tp = tab[q];
-                const int ih = ih0 + (tp.dy_dx >> 16), iw = iw0 + (tp.dy_dx & 0xFFFF);
-                if (ih >= 0 && ih < g.H && iw >= 0 && iw < g.W) v = *reinterpret_cast<const uint4 *>(X + (corner + tp.off));
-            } else {
-                E e[G];
+            const Tap tp = tab[q];
+            const int ih = ih0 + (tp.dy_dx >> 16), iw = iw0 + (tp.dy_dx & 0xFFFF);
+            if (ih >= 0 && ih < g.H && iw >= 0 && iw < g.W)
+                v = *reinterpret_cast<const uint4 *>(X + (corner + tp.off) * ESZ);
+            dst[q] = v;
+        }
+    }
+}
+
+// Channel counts that do not fill 16-byte chunks (a first layer's C = 3):
+// lane l of the row's warp writes elements l, l + 32, ... of the row, so the
+// warp's loads are consecutive elements of X within each window row (KW * C
+// values in a row of the image when dw = 1) and its stores are consecutive
+// elements of P. The table holds every element's offset; elements K .. ldp-1
+// of the row (padding) are written as zeros.
+template <int ESZ>
+__global__ void __launch_bounds__(32 * kWarpsPerCta) im2col_linear_kernel(const Im2col g, int K) {
+    using E = typename std::conditional<ESZ == 2, uint16_t, float>::type;
+    extern __shared__ Tap tab[];
+    for (int k = threadIdx.x; k < K; k += blockDim.x) {
+        const int kh = k / (g.KW * g.C), r = k - kh * (g.KW * g.C);
+        const int kw = r / g.C, ci = r - kw * g.C;
+        const int dy = kh * g.dh, dx = kw * g.dw;
+        tab[k].dy_dx = (dy << 16) | dx;
+        tab[k].off = (dy * g.W + dx) * g.C + ci;
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int nwarps = gridDim.x * kWarpsPerCta;
+    const E *X = static_cast<const E *>(g.X);
+    const int width = static_cast<int>(g.ldp);
+    for (int m = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5); m < g.M; m += nwarps) {
+        const int ow = m % g.OW, t = m / g.OW;
+        const int oh = t % g.OH, n = t / g.OH;
+        const int ih0 = oh * g.sh - g.ph, iw0 = ow * g.sw - g.pw;
+        const long long corner = ((static_cast<long long>(n) * g.H + ih0) * g.W + iw0) * g.C;
+        E *dst = static_cast<E *>(g.P) + static_cast<long long>(m) * g.ldp;
+        // a window wholly inside the image (most rows) needs no bounds checks
+        const bool interior = ih0 >= 0 && ih0 + (g.KH - 1) * g.dh < g.H && iw0 >= 0 && iw0 + (g.KW - 1) * g.dw < g.W;
+        // eight steps of 32 elements: all loads first, then the stores, so a
+        // row's loads are in flight together
+        for (int k0 = lane; k0 < width; k0 += 32 * 8) {
+            E v[8];
+            if (interior) {
 #pragma unroll
-                for (int j = 0; j < G; ++j) {
-                    const int k = q * G + j;
-                    e[j] = E{};
+                for (int u = 0; u < 8; ++u) {
+                    const int k = k0 + 32 * u;
+                    v[u] = k < K ? X[corner + tab[k].off] : E{};
+                }
+            } else {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int k = k0 + 32 * u;
+                    v[u] = E{};
                     if (k < K) {
                         const Tap tp = tab[k];
                         const int ih = ih0 + (tp.dy_dx >> 16), iw = iw0 + (tp.dy_dx & 0xFFFF);
-                        if (ih >= 0 && ih < g.H && iw >= 0 && iw < g.W) e[j] = X[corner + tp.off];
+                        if (ih >= 0 && ih < g.H && iw >= 0 && iw < g.W) v[u] = X[corner + tp.off];
                     }
                 }
-                memcpy(&v, e, 16);
             }
-            dst[q] = v;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (k0 + 32 * u < width) dst[k0 + 32 * u] = v[u];
         }
     }
 }
@@ -174,27 +217,30 @@ cudaError_t im2col_launch(const DeviceInfo &dev, const ConvArgs &c, void *P, int
     const int esz = c.elem;
     const int ve = 16 / esz;
     const int K = static_cast<int>(c.KH * c.KW * c.C);
-    // the table kernel: 16-byte aligned rows of P and taps addressable in 32 bits
+    // window offsets addressable by the tables (16-bit dy, dx; 32-bit element offsets)
+    const bool taps_ok = (c.KH - 1) * c.dh < 32768 && (c.KW - 1) * c.dw < 32768 &&
+                         ((c.KH - 1) * c.dh * c.W + (c.KW - 1) * c.dw + 1) * c.C < INT32_MAX;
     const bool vec = c.C % ve == 0 && (reinterpret_cast<uintptr_t>(c.X) & 15) == 0;
-    const int ntab = vec ? (K + ve - 1) / ve : K;
-    const bool table = (reinterpret_cast<uintptr_t>(P) & 15) == 0 && (ldp * esz) % 16 == 0 && ldp >= (K + ve - 1) / ve * ve &&
-                       ntab <= kMaxTaps && (c.KH - 1) * c.dh < 32768 && (c.KW - 1) * c.dw < 32768 &&
-                       ((c.KH - 1) * c.dh * c.W + (c.KW - 1) * c.dw + 1) * c.C < INT32_MAX;
-    if (table) {
-        const long long ctas = (g.M + kWarpsPerCta - 1) / kWarpsPerCta;
-        const int grid = static_cast<int>(std::min<long long>(ctas, static_cast<long long>(dev.sms) * 16));
-        const size_t smem = static_cast<size_t>(ntab) * sizeof(Tap);
-        if (esz == 2) {
-            if (vec) im2col_table_kernel<2, true><<<grid, 32 * kWarpsPerCta, smem, stream>>>(g, K);
-            else im2col_table_kernel<2, false><<<grid, 32 * kWarpsPerCta, smem, stream>>>(g, K);
-        } else {
-            if (vec) im2col_table_kernel<4, true><<<grid, 32 * kWarpsPerCta, smem, stream>>>(g, K);
-            else im2col_table_kernel<4, false><<<grid, 32 * kWarpsPerCta, smem, stream>>>(g, K);
-        }
+    const bool p_chunks = (reinterpret_cast<uintptr_t>(P) & 15) == 0 && (ldp * esz) % 16 == 0 &&
+                          ldp >= (K + ve - 1) / ve * ve;
+    const long long ctas = (g.M + kWarpsPerCta - 1) / kWarpsPerCta;
+    const int grid = static_cast<int>(std::min<long long>(ctas, static_cast<long long>(dev.sms) * 16));
+    if (taps_ok && vec && p_chunks && (K + ve - 1) / ve <= kMaxTaps) {
+        // 16-byte chunks of channels
+        const size_t smem = static_cast<size_t>((K + ve - 1) / ve) * sizeof(Tap);
+        if (esz == 2) im2col_table_kernel<2><<<grid, 32 * kWarpsPerCta, smem, stream>>>(g, K);
+        else im2col_table_kernel<4><<<grid, 32 * kWarpsPerCta, smem, stream>>>(g, K);
+        return cudaGetLastError();
+    }
+    if (taps_ok && !vec && K <= kMaxTaps && ldp >= K) {
+        // element by element, lanes along the row
+        const size_t smem = static_cast<size_t>(K) * sizeof(Tap);
+        if (esz == 2) im2col_linear_kernel<2><<<grid, 32 * kWarpsPerCta, smem, stream>>>(g, K);
+        else im2col_linear_kernel<4><<<grid, 32 * kWarpsPerCta, smem, stream>>>(g, K);
         return cudaGetLastError();
     }
     // otherwise: chunk by chunk with carries (very wide windows, unaligned buffers)
-    const bool vchunks = vec && (reinterpret_cast<uintptr_t>(P) & 15) == 0 && (ldp * esz) % 16 == 0;
+    const bool vchunks = vec && p_chunks;
     if (vchunks) return esz == 2 ? launch_typed<uint4, 8>(dev, g, stream) : launch_typed<uint4, 4>(dev, g, stream);
     return esz == 2 ? launch_typed<uint16_t, 1>(dev, g, stream) : launch_typed<float, 1>(dev, g, stream);
 }
