@@ -84,7 +84,8 @@ struct TcParams {
     int num_m, num_n, num_kb, num_tiles;   // num_tiles counts every item of a batch
     int tiles_per_batch;
     int splits, kps;             // K split into `splits` ranges of kps slices (1: none)
-    int num_units;               // num_tiles * splits
+    int num_units;               // num_tiles * splits, plus the extra halves of a split tail
+    int tail_start;              // pair kernel: units from here on are 128-wide halves of the last tiles
     long long strideC;           // elements between the C matrices of consecutive batch items
     uint32_t idesc;              // instruction descriptor (A/B format: FP16 or BF16) of the 16-bit kernels
     int c_vec;                   // widest store for whole rows of a tile: 2 = 32 B, 1 = 16 B, 0 = 4 B
@@ -459,6 +460,22 @@ __device__ __forceinline__ void pair_tile_coords(int t, const TcParams &p, int &
     nb = r / gs;
 }
 
+// Tile of pair-kernel unit tt: row tile mb, first column c0 and width w.
+// Units before p.tail_start are whole 256 x 256 tiles in raster order; from
+// there on each remaining tile is two units, its 128-column halves, so that
+// a last wave that would leave clusters idle runs as a wave of half tiles.
+__device__ __forceinline__ void pair_tile(int tt, const TcParams &p, int &mb, int &c0, int &w) {
+    int tile = tt, half = -1;
+    if (tt >= p.tail_start) {
+        tile = p.tail_start + (tt - p.tail_start) / 2;
+        half = (tt - p.tail_start) & 1;
+    }
+    int nb;
+    pair_tile_coords(tile, p, mb, nb);
+    c0 = nb * 256 + (half > 0 ? 128 : 0);
+    w = half >= 0 ? 128 : 256;
+}
+
 __device__ __noinline__ void spin_ns(uint64_t ns) {
     const uint64_t t0 = ptx::globaltimer_ns();
     while (ptx::globaltimer_ns() - t0 < ns) {
@@ -526,12 +543,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int t = cluster_id; ok && t < p.num_units; t += nclusters) {
-                int mb, nb;
+                int mb, c0, w;
                 const Unit u = unit_of(t, p);
                 const int bi = u.bi;
-                pair_tile_coords(u.tt, p, mb, nb);
+                pair_tile(u.tt, p, mb, c0, w);
                 const int row0 = mb * 2 * S::BM + static_cast<int>(rank) * S::BM;
-                const int col0 = nb * S::BN + static_cast<int>(rank) * (S::BN / 2);
+                const int col0 = c0 + static_cast<int>(rank) * (w / 2);
+                // both CTAs' A rows and B halves: (16 KB + w/2 columns x 128 B) each
+                const uint32_t stage_tx = 2u * static_cast<uint32_t>(S::A_BYTES + (w / 2) * 128);
                 for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
                     const int s = static_cast<int>(it % S::STAGES);
                     const uint32_t ph = (it / S::STAGES) & 1u;
@@ -540,15 +559,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     if (p.drop_slice == static_cast<int>(it) && cluster_id == 0 && leader) continue;
-                    if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), 2 * S::STAGE_BYTES);
+                    if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), stage_tx);
                     const uint32_t fb = leader_full0 + 8u * s;
                     ptx::tma_load_3d_pair(sA + s * S::A_BYTES, &tmA, fb, kb * S::BK, row0, bi);
                     if constexpr (S::B_KMAJOR) {
                         // this CTA's 128 rows of B^T
                         ptx::tma_load_3d_pair(sB + s * S::B_BYTES, &tmB, fb, kb * S::BK, col0, bi);
                     } else {
-#pragma unroll
-                        for (int c = 0; c < S::B_CHUNKS; ++c)
+                        for (int c = 0; c < (w / 2) / S::BCH_N; ++c)
                             ptx::tma_load_3d_pair(sB + s * S::B_BYTES + c * S::BCH_BYTES, &tmB, fb,
                                                   col0 + c * S::BCH_N, kb * S::BK, bi);
                     }
@@ -584,6 +602,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * S::BN);
                 const Unit u = unit_of(t, p);
+                int mb, c0, w;
+                pair_tile(u.tt, p, mb, c0, w);
+                // the instruction descriptor's N (bits 17-22, N / 8) for this unit's width
+                const uint32_t idesc = (p.idesc & ~(0x3Fu << 17)) | (static_cast<uint32_t>(w >> 3) << 17);
                 for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
                     const int s = static_cast<int>(it % S::STAGES);
                     const uint32_t ph = (it / S::STAGES) & 1u;
@@ -602,9 +624,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                 : ptx::smem_desc_sw128(b0 + k * S::UK * 128, S::BCH_BYTES, 1024);
                         const uint32_t accum = (kb > u.kb0 || k > 0) ? 1u : 0u;
                         if constexpr (TF32)
-                            ptx::mma_tf32_pair(d_tmem, ad, bd, p.idesc, accum);
+                            ptx::mma_tf32_pair(d_tmem, ad, bd, idesc, accum);
                         else
-                            ptx::mma_bf16_pair(d_tmem, ad, bd, p.idesc, accum);
+                            ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, accum);
                     }
                     ptx::mma_commit_pair(empty_bar(s), 0x3);
                 }
@@ -621,22 +643,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t leader_acce0 = ptx::map_to_rank(acce_bar(0), 0);
         int local = 0;
         for (int t = cluster_id; t < p.num_units; t += nclusters, ++local) {
-            int mb, nb;
+            int mb, col0, w;
             const Unit u = unit_of(t, p);
-            pair_tile_coords(u.tt, p, mb, nb);
+            pair_tile(u.tt, p, mb, col0, w);
             const int acc = local & 1;
             const uint32_t aph = (static_cast<uint32_t>(local) >> 1) & 1u;
             if (!wait_bar(accf_bar(acc), aph, abort_flag, p)) break;
             ptx::tc_fence_after_sync();
             const int row = mb * 2 * S::BM + static_cast<int>(rank) * S::BM + r_in_tile;
-            const int col0 = nb * S::BN;
             const bool row_ok = row < p.M;
-            const bool whole = p.c_vec && (col0 + S::BN <= p.N);
+            const bool whole = p.c_vec && (col0 + w <= p.N);
             float *crow = p.C + u.coff + static_cast<long long>(row) * p.ldc + col0;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * S::BN);
 #pragma unroll 1
-            for (int c = 0; c < S::BN / 32; ++c) {
+            for (int c = 0; c < w / 32; ++c) {
                 uint32_t r[32];
                 ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
                 ptx::tmem_ld_wait();
@@ -922,6 +943,7 @@ cudaError_t launch_impl(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
     p.strideC = g.strideC;
     p.idesc = TF32 ? S::IDESC : idesc16(g.prec, S::BM, BN);
     p.c_vec = c_store_width(g);
+    p.tail_start = INT32_MAX;
     p.status = dev.status;
     p.wait_limit_ns = wait_limit_ns();
     p.drop_slice = take_drop_slice();
@@ -937,6 +959,26 @@ cudaError_t launch_impl(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
         if (e == cudaSuccess) e = f;
     }
     return e;
+}
+
+// Units of the pair kernel: whole 256 x 256 tiles, and the tiles of a last
+// partial wave cut into 128-wide halves when the halves fit one wave of
+// clusters (16-bit inputs, a single product, no K split). tail_start = the
+// first half-tile unit, INT32_MAX when there are none.
+struct PairUnits {
+    int units, tail_start;
+};
+PairUnits pair_units(int64_t tiles, int clusters, bool allowed) {
+    if (allowed && clusters > 0) {
+        const int64_t tail = tiles < clusters ? tiles : tiles % clusters;
+        if (tail > 0 && 2 * tail <= clusters)
+            return {static_cast<int>(tiles + tail), static_cast<int>(tiles - tail)};
+    }
+    return {static_cast<int>(tiles), INT32_MAX};
+}
+
+bool pair_halves_allowed(const GemmArgs &g, int splits) {
+    return g.prec != GTG_PREC_TF32 && splits == 1 && g.batch == 1;
 }
 
 template <bool TF32>
@@ -991,6 +1033,7 @@ cudaError_t launch_pair(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
     p.strideC = g.strideC;
     p.idesc = TF32 ? ptx::make_idesc(2u, 0u, 0u, 2 * S::BM, S::BN) : idesc16(g.prec, 2 * S::BM, S::BN);
     p.c_vec = c_store_width(g);
+    p.tail_start = INT32_MAX;
     p.status = dev.status;
     p.wait_limit_ns = wait_limit_ns();
     p.drop_slice = take_drop_slice();
@@ -998,9 +1041,16 @@ cudaError_t launch_pair(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
     p.act = g.act;
     float *ws = nullptr;
     cudaError_t e = begin_split(g, plan, p, &ws, stream);
+    const PairUnits pu = pair_units(p.num_tiles, dev.sms / 2, pair_halves_allowed(g, p.splits));
+    p.tail_start = pu.tail_start;
+    if (pu.tail_start != INT32_MAX) {
+        p.num_units = pu.units;
+        p.tiles_per_batch = pu.units;   // a single product: unit t is tile (or half) t
+    }
+    const int clusters = static_cast<int>(std::min<int64_t>(p.num_units, dev.sms / 2));
     if (e == cudaSuccess) {
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(plan.grid));
+        cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = static_cast<size_t>(S::SMEM);
         cfg.stream = stream;
@@ -1027,7 +1077,9 @@ cudaError_t launch_pair(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
 void fill_pair_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan, int splits) {
     using S = PairShape<false>;
     const int64_t tiles = g.batch * ((g.M + 2 * S::BM - 1) / (2 * S::BM)) * ((g.N + S::BN - 1) / S::BN);
-    const int64_t clusters = std::min<int64_t>(tiles * splits, dev.sms / 2);
+    const PairUnits pu = pair_units(tiles, dev.sms / 2, pair_halves_allowed(g, splits));
+    const int64_t units = pu.tail_start != INT32_MAX ? pu.units : tiles * splits;
+    const int64_t clusters = std::min<int64_t>(units, dev.sms / 2);
     plan->kernel = GTG_KERNEL_TCGEN05;
     plan->bm = 2 * S::BM;
     plan->bn = S::BN;
@@ -1093,6 +1145,7 @@ cudaError_t conv_launch_impl(const DeviceInfo &dev, const ConvArgs &c, cudaStrea
     p.idesc = idesc16(c.prec, S::BM, BN);
     const auto yaddr = reinterpret_cast<uintptr_t>(c.Y);
     p.c_vec = ((yaddr & 31) == 0 && (c.CO & 7) == 0) ? 2 : (((yaddr & 15) == 0 && (c.CO & 3) == 0) ? 1 : 0);
+    p.tail_start = INT32_MAX;
     p.status = dev.status;
     p.wait_limit_ns = wait_limit_ns();
     p.drop_slice = take_drop_slice();
@@ -1207,7 +1260,15 @@ void tc_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
             }
         }
         if ((dev.sms & 1) == 0 && g_pair_enabled.load()) {
-            const double c = tc_cost(dev, g, 2 * kBM, 256, dev.sms / 2, 1.0 / 1.15, want, bk);
+            double c = tc_cost(dev, g, 2 * kBM, 256, dev.sms / 2, 1.0 / 1.15, want, bk);
+            if (pair_halves_allowed(g, want)) {
+                // a last partial wave cut into half tiles costs about 0.6 of a
+                // wave (half the multiplies, three quarters of the operand bytes)
+                const int64_t tiles = ((g.M + 2 * kBM - 1) / (2 * kBM)) * ((g.N + 255) / 256);
+                if (pair_units(tiles, dev.sms / 2, true).tail_start != INT32_MAX)
+                    c = (static_cast<double>(tiles / (dev.sms / 2)) + 0.6) * (static_cast<double>(num_kb) + kFillSlices) *
+                        kSliceUs / 1.15;
+            }
             if (c < best_cost) {
                 best_cost = c;
                 best_s = want;
@@ -1365,6 +1426,7 @@ cudaError_t launch_tf32_fixed(const DeviceInfo &dev, const GemmArgs &g, const gt
     p.strideC = 0;
     p.idesc = S::IDESC;
     p.c_vec = c_store_width(g);
+    p.tail_start = INT32_MAX;
     p.status = dev.status;
     p.wait_limit_ns = wait_limit_ns();
     p.drop_slice = take_drop_slice();

@@ -18,6 +18,8 @@ def inputs(prec, M, N, K, seed):
     g = PCG32(seed)
     if prec == "bf16":
         return g.normal_bf16((M, K)), g.normal_bf16((K, N))
+    if prec == "f16":
+        return g.normal_f16((M, K)), g.normal_f16((K, N))
     return g.uniform_f32((M, K)), g.uniform_f32((K, N))
 
 
@@ -85,7 +87,9 @@ def test_tcgen05_edge_shapes(prec, M, N, K):
 @pytest.mark.parametrize("prec", ["tf32", "bf16"])
 def test_every_tile_width_is_exercised(prec):
     seen = set()
-    for (M, N, K) in [(4096, 4096, 64), (1536, 1536, 64), (1024, 1024, 64)]:
+    # (1408 x 1664: 143 tiles of 128 x 128 fit one wave, while its 42 pair
+    # tiles are too many to run as half tiles in one wave)
+    for (M, N, K) in [(4096, 4096, 64), (1408, 1664, 64), (1024, 1024, 64)]:
         A, B = inputs(prec, M, N, K, 7)
         C = run_gemm(prec, A, B, expect_kernel="tcgen05")
         check_gemm(prec, A, B, C, rows=sample_rows(M))
@@ -126,6 +130,20 @@ def test_cta_pair_kernel_ragged(prec, M, N, K):
     C = run_gemm(prec, A, B, expect_kernel="tcgen05")
     assert gtg_plan(prec, M, N, K)["bm"] == 256
     check_gemm(prec, A, B, C, rows=np.concatenate([sample_rows(M, seed=2), np.arange(M - 200, M)]))
+
+
+@pytest.mark.parametrize("prec", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N,K", [(4000, 4000, 200), (4096, 4096, 72), (2048, 1024, 512), (1536, 1528, 512), (3000, 2008, 1024)])
+def test_cta_pair_kernel_half_tiles(prec, M, N, K):
+    # a last wave of 256 x 256 tiles that would leave clusters idle runs as
+    # 128-wide halves (4000: 256 tiles on 76 clusters, 28 left, their second
+    # halves only 32 columns wide at the right edge; 2048 x 1024 and 1536 x 1528:
+    # every tile in halves)
+    A, B = inputs(prec, M, N, K, 400 + K)
+    C = run_gemm(prec, A, B, expect_kernel="tcgen05")
+    assert gtg_plan(prec, M, N, K)["bm"] == 256
+    rows = np.concatenate([sample_rows(M, seed=3), np.arange(max(0, M - 300), M)])
+    check_gemm(prec, A, B, C, rows=np.unique(rows))
 
 
 # ---- layouts the tensor-memory path cannot take: the SIMT fallback --------------
