@@ -59,6 +59,8 @@ def parse_args():
     p.add_argument("--only-ablation", action="store_true",
                    help="run only the pages' kernel designs beside the library's (prints their table)")
     p.add_argument("--ablation-iters", type=int, default=0, help="timed launches per ablation kernel (0: default)")
+    p.add_argument("--only-gemv", default=None, metavar="PREC:N:BATCH",
+                   help="run only an N x N GEMV (prec f32 or bf16) at the given batch, three calls (for profiling)")
     p.add_argument("--only-conv", type=int, default=None, metavar="IDX",
                    help="run only convolutional layer IDX of the sweep, three calls (for profiling)")
     return p.parse_args()
@@ -360,6 +362,42 @@ def gpu_arm(args, rank, world, local_rank):
     if not args.no_sweep:
         result["configs"] = sweep(dev, stream, peaks, l2)
     return result
+
+
+def only_gemv(spec, local_rank):
+    """Three gemv_f32 / gemv_bf16 calls on one N x N configuration (seeded inputs)."""
+    import numpy as np
+    import torch
+
+    import gemv_tiled_gemm_gb300 as gtg
+    from seeded import PCG32
+
+    prec, n, batch = spec.split(":")
+    n, batch = int(n), int(batch)
+    torch.cuda.set_device(local_rank)
+    g = PCG32(2)
+    if prec == "bf16":
+        A = torch.from_numpy(g.normal_bf16((n, n)).view(np.int16)).cuda()
+        fn = gtg.gemv_bf16
+    else:
+        A = torch.from_numpy(g.uniform_f32((n, n))).cuda()
+        fn = gtg.gemv_f32
+    X = torch.from_numpy(g.uniform_f32((batch, n))).cuda()
+    Y = torch.empty((batch, n), device="cuda")
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for _ in range(3):
+        e0.record(s)
+        rc = fn(n, n, A.data_ptr(), n, X.data_ptr(), n, Y.data_ptr(), n, batch, s.cuda_stream)
+        e1.record(s)
+        assert rc == gtg.GTG_OK, rc
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    assert gtg.gtg_sync_status(s.cuda_stream) == gtg.GTG_OK
+    plan = gtg.plan_gemv(n, n, A.data_ptr(), n, X.data_ptr(), n, Y.data_ptr(), n, batch, precision=prec)
+    return {"config": f"{prec} gemv {n}x{n} batch {batch}", "kernel": plan["kernel"],
+            "ms_per_call": [round(t, 4) for t in times]}
 
 
 def only_conv(idx, local_rank):
@@ -719,6 +757,9 @@ def main():
             print(json.dumps(res), flush=True)
         return 0
 
+    if args.only_gemv is not None:
+        print(json.dumps(only_gemv(args.only_gemv, local_rank)), flush=True)
+        return 0
     if args.only_conv is not None:
         print(json.dumps(only_conv(args.only_conv, local_rank)), flush=True)
         return 0
