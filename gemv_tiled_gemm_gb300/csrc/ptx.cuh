@@ -75,7 +75,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-// Same, with an L2 eviction-priority policy (createpolicy result).
 // TMA load in im2col mode from a 4-D (C, W, H, N) tensor map: the
 // map's pixelsPerColumn pixels, channelsPerPixel channels each, starting
 // with channel c at the pixel (w, h, n) and walking the map's bounding box
