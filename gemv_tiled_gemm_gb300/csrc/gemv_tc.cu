@@ -27,14 +27,15 @@
 // grid (one CTA per SM), so every SM reads the same share of A whatever the
 // tile count. A CTA's range covers parts of one or more tiles; a tile it
 // covers whole is written to y directly, the parts of a tile shared by CTAs
-// go to a workspace and a second kernel adds them in CTA order, so the result
-// does not depend on scheduling.
+// go to a workspace, and whichever CTA finishes its part last adds them all
+// in CTA order (each epilogue warp for its 32 rows, counted by an atomic per
+// tile and warp), so the result does not depend on scheduling.
 //
 // Roles (192 threads): warp 0 issues the TMA loads, warp 1 owns TMEM (two 32-
 // column accumulators) and issues the MMAs, warps 2-5 read the accumulator
 // of a finished tile part (each its 32 TMEM lanes = rows) and write it out.
-// The three kernels of a call are launched as dependent launches, each
-// scheduled while the one before it finishes.
+// The product kernel is a dependent launch after the kernel that writes the
+// vector pieces, scheduled while that kernel finishes.
 // Every wait is bounded; on time-out the kernel latches GTG_ERR_TIMEOUT,
 // drains what it issued, frees TMEM and returns.
 #include <cuda.h>
@@ -65,6 +66,7 @@ struct Params {
     float *y;
     long long ldy;
     float *ws;                   // [tile][part][8][kBM] partial sums of shared tiles
+    int *cnt;                    // [tile][4] parts written so far, per epilogue warp (zeroed by the first kernel)
     int M, batch;
     int ks;                      // K slices per tile
     long long work;              // tiles * ks
@@ -156,7 +158,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
-    ptx::wait_prior_grid();
+    // A never depends on the kernel before this one (that kernel started only
+    // after everything before it had completed), so the first stages' loads
+    // of A go out before waiting for it; the vector pieces it writes, the part
+    // counters it zeroes and the outputs wait for it (griddepcontrol.wait).
     ptx::allow_next_grid();
 
     const long long f0 = range_begin(blockIdx.x, p.work, gridDim.x);
@@ -165,9 +170,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
+            const long long fp = min(f1, f0 + kStages);   // the first stages: A now, the pieces after the wait
             uint32_t it = 0;
+            for (long long f = f0; f < fp; ++f, ++it) {
+                if (p.drop_slice == static_cast<int>(it) && blockIdx.x == 0) continue;
+                const int t = static_cast<int>(f / p.ks);
+                const int k = static_cast<int>(f - static_cast<long long>(t) * p.ks);
+                ptx::mbar_arrive_expect_tx(full_bar(static_cast<int>(it)), kStageBytes);
+                ptx::tma_load_3d(sA + it * kABytes, &tmA, full_bar(static_cast<int>(it)), k * kBK, t * kBM, 0);
+            }
+            ptx::wait_prior_grid();
+            it = 0;
+            for (long long f = f0; f < fp; ++f, ++it) {
+                if (p.drop_slice == static_cast<int>(it) && blockIdx.x == 0) continue;
+                const int k = static_cast<int>(f - (f / p.ks) * p.ks);
+                ptx::tma_load_3d(sB + it * kBBytes, &tmX, full_bar(static_cast<int>(it)), k * kBK, 0, 0);
+            }
             bool ok = true;
-            for (long long f = f0; ok && f < f1; ++f, ++it) {
+            for (long long f = fp; ok && f < f1; ++f, ++it) {
                 const int t = static_cast<int>(f / p.ks);
                 const int k = static_cast<int>(f - static_cast<long long>(t) * p.ks);
                 const int s = static_cast<int>(it % kStages);
@@ -234,6 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------ epilogue (warps 2..5)
+        ptx::wait_prior_grid();   // the part counters are zeroed by the kernel before
         const int quarter = warp & 3;
         const int rr = quarter * 32 + lane;   // row within the tile
         int local = 0;
@@ -263,13 +284,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                 }
             } else {
-                const int part = static_cast<int>(blockIdx.x) - cta_of(tb, p.work, gridDim.x);
-                float *dst = p.ws + (static_cast<long long>(t) * p.maxp + part) * 8 * kBM + rr;
+                const int c0 = cta_of(tb, p.work, gridDim.x), c1 = cta_of(tb + p.ks - 1, p.work, gridDim.x);
+                const int part = static_cast<int>(blockIdx.x) - c0;
+                float *parts = p.ws + static_cast<long long>(t) * p.maxp * 8 * kBM + rr;   // part j at j * 8 * kBM
 #pragma unroll
                 for (int b = 0; b < 8; ++b)
                     if (b < p.batch)
-                        dst[b * kBM] = (__uint_as_float(r[3 * b]) + __uint_as_float(r[3 * b + 1])) +
-                                       __uint_as_float(r[3 * b + 2]);
+                        parts[(part * 8 + b) * kBM] = (__uint_as_float(r[3 * b]) + __uint_as_float(r[3 * b + 1])) +
+                                                      __uint_as_float(r[3 * b + 2]);
+                // the warp that completes the count for its 32 rows adds the parts
+                __threadfence();
+                __syncwarp();
+                int last = 0;
+                if (lane == 0) last = atomicAdd(p.cnt + t * 4 + quarter, 1) == c1 - c0;
+                if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
+                    __threadfence();
+                    if (row < p.M) {
+                        // up to 8 parts x 8 vectors of loads in flight, then added in part order
+                        const int np = c1 - c0 + 1;
+                        float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                        for (int j0 = 0; j0 < np; j0 += 8) {
+                            float w[8][8];
+#pragma unroll
+                            for (int u = 0; u < 8; ++u)
+#pragma unroll
+                                for (int b = 0; b < 8; ++b)
+                                    w[u][b] = (j0 + u < np && b < p.batch) ? parts[((j0 + u) * 8 + b) * kBM] : 0.f;
+#pragma unroll
+                            for (int u = 0; u < 8; ++u)
+                                if (j0 + u < np)
+#pragma unroll
+                                    for (int b = 0; b < 8; ++b) v[b] += w[u][b];
+                        }
+#pragma unroll
+                        for (int b = 0; b < 8; ++b)
+                            if (b < p.batch) p.y[b * p.ldy + row] = apply_epilogue(v[b], p.bias, row, p.act);
+                    }
+                }
             }
             ptx::tc_fence_before_sync();
             __syncwarp();
@@ -288,10 +339,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // The three BF16 pieces of every vector entry: rows 3b, 3b+1, 3b+2 of xp.
+// It also zeroes the part counters of the product kernel.
 __global__ void split_vectors_kernel(const float *__restrict__ x, long long ldx, int N, int batch,
-                                     __nv_bfloat16 *__restrict__ xp, long long ldp) {
+                                     __nv_bfloat16 *__restrict__ xp, long long ldp, int *__restrict__ cnt, int ncnt) {
     ptx::wait_prior_grid();   // x may come from the previous kernel in the stream
     ptx::allow_next_grid();
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < ncnt; i += gridDim.x * blockDim.x) cnt[i] = 0;
     const long long total = static_cast<long long>(batch) * N;
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -308,38 +361,8 @@ __global__ void split_vectors_kernel(const float *__restrict__ x, long long ldx,
     }
 }
 
-// Tiles shared by CTAs: their parts added in CTA order, then the epilogue.
-__global__ void gather_parts_kernel(const float *__restrict__ ws, int M, int batch, int ks, long long work,
-                                    int grid, int maxp, float *__restrict__ y, long long ldy,
-                                    const float *__restrict__ bias, int act) {
-    ptx::wait_prior_grid();   // the parts are complete once the product kernel is
-    ptx::allow_next_grid();
-    const long long total = static_cast<long long>(M) * batch;
-    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const int b = static_cast<int>(i / M), row = static_cast<int>(i - static_cast<long long>(b) * M);
-        const int t = row / kBM, rr = row - t * kBM;
-        const long long tb = static_cast<long long>(t) * ks;
-        const int c0 = cta_of(tb, work, grid), c1 = cta_of(tb + ks - 1, work, grid);
-        if (c0 == c1) continue;   // one CTA held the whole tile and wrote it
-        const int np = c1 - c0 + 1;
-        const float *src = ws + (static_cast<long long>(t) * maxp * 8 + b) * kBM + rr;   // part j at j * 8 * kBM
-        float v = 0.f;
-        int j = 0;
-        for (; j + 8 <= np; j += 8) {   // eight loads in flight, added in part order
-            float w[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) w[u] = src[static_cast<long long>(j + u) * 8 * kBM];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) v += w[u];
-        }
-        for (; j < np; ++j) v += src[static_cast<long long>(j) * 8 * kBM];
-        y[b * ldy + row] = apply_epilogue(v, bias, row, act);
-    }
-}
-
-// Launch with programmatic dependent launch allowed: each kernel of the call
-// is scheduled while the one before it finishes and waits for it
+// Launch with programmatic dependent launch allowed: the product kernel is
+// scheduled while the first kernel finishes and waits for it
 // (griddepcontrol.wait) before reading what it wrote.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_dependent(void (*kern)(KArgs...), int grid, int threads, int smem, cudaStream_t stream,
@@ -361,10 +384,12 @@ cudaError_t launch_dependent(void (*kern)(KArgs...), int grid, int threads, int 
 
 bool gemv_tc_eligible(const DeviceInfo &dev, const GemvArgs &g, bool any_size) {
     if (g.a_elem != 2 || g.batch < 3 || g.batch > 8 || !tc_supported(dev)) return false;
-    // below 2^25 matrix elements the CUDA-core kernel is faster (its single
-    // launch against this path's three; measured at batch 8, 4096^2: 11.7
-    // against 12.6 us; 8192^2: 38.5 against 30.0 us)
-    if (!any_size && g.M * g.N < (int64_t{1} << 25)) return false;
+    // Where the CUDA-core kernel is faster: below 2^25 matrix elements (batch
+    // 8, 4096^2: 11.7 against 13.1 us) and below batch 6, whose per-element
+    // work it carries well (8192^2: batch 5 26.7 against 29.9 us, batch 6
+    // 30.3 against 30.0 us; 16384^2: batch 4 84.0 against 90.5 us, batch 6
+    // 118.5 against 90.7 us).
+    if (!any_size && (g.M * g.N < (int64_t{1} << 25) || g.batch < 6)) return false;
     if ((reinterpret_cast<uintptr_t>(g.A) & 15) || (g.lda * 2) % 16) return false;   // TMA base and rows
     return g.M > 0 && g.N > 0 && g.M <= INT32_MAX - kBM && g.N <= INT32_MAX - kBK;
 }
@@ -399,9 +424,11 @@ cudaError_t gemv_tc_launch(const DeviceInfo &dev, const GemvArgs &g, cudaStream_
     const long long ldp = (g.N + 7) / 8 * 8;   // 16-byte rows of pieces
     const size_t xp_bytes = static_cast<size_t>(3 * g.batch * ldp) * 2;
     const size_t ws_bytes = static_cast<size_t>(tiles * maxp) * 8 * kBM * 4;
-    void *xp = nullptr, *ws = nullptr;
+    const size_t cnt_bytes = static_cast<size_t>(tiles) * 4 * sizeof(int);
+    void *xp = nullptr, *ws = nullptr, *cnt = nullptr;
     cudaError_t e = ws_alloc(&xp, xp_bytes, stream);
     if (e == cudaSuccess) e = ws_alloc(&ws, ws_bytes, stream);
+    if (e == cudaSuccess) e = ws_alloc(&cnt, cnt_bytes, stream);
     CUtensorMap ta, tx;
     if (e == cudaSuccess && (!tma_map_2d(&ta, GTG_PREC_BF16, g.A, g.N, g.M, g.lda, kBK, kBM) ||
                              !tma_map_2d(&tx, GTG_PREC_BF16, xp, g.N, 3 * g.batch, ldp, kBK, kNP)))
@@ -411,13 +438,14 @@ cudaError_t gemv_tc_launch(const DeviceInfo &dev, const GemvArgs &g, cudaStream_
         const int sgrid = static_cast<int>(std::min<long long>((n + 255) / 256, dev.sms * 8ll));
         e = launch_dependent(split_vectors_kernel, sgrid, 256, 0, stream, g.x, static_cast<long long>(g.ldx),
                              static_cast<int>(g.N), static_cast<int>(g.batch), static_cast<__nv_bfloat16 *>(xp),
-                             static_cast<long long>(ldp));
+                             static_cast<long long>(ldp), static_cast<int *>(cnt), static_cast<int>(tiles * 4));
     }
     if (e == cudaSuccess) {
         Params p;
         p.y = g.y;
         p.ldy = g.ldy;
         p.ws = static_cast<float *>(ws);
+        p.cnt = static_cast<int *>(cnt);
         p.M = static_cast<int>(g.M);
         p.batch = static_cast<int>(g.batch);
         p.ks = static_cast<int>(ks);
@@ -430,19 +458,10 @@ cudaError_t gemv_tc_launch(const DeviceInfo &dev, const GemvArgs &g, cudaStream_
         p.drop_slice = take_test_drop_slice();
         e = launch_dependent(gemv_tc_kernel, grid, kThreads, kSmem, stream, ta, tx, p);
     }
-    // a tile is shared when a CTA range boundary falls inside it
-    bool shared = false;
-    for (long long c = 1; c < grid && !shared; ++c) shared = range_begin(c, work, grid) % ks != 0;
-    if (e == cudaSuccess && shared) {
-        const long long n = g.M * g.batch;
-        const int ggrid = static_cast<int>(std::min<long long>((n + 127) / 128, 65535));
-        e = launch_dependent(gather_parts_kernel, ggrid, 128, 0, stream, static_cast<const float *>(ws),
-                             static_cast<int>(g.M), static_cast<int>(g.batch), static_cast<int>(ks), work, grid, maxp,
-                             g.y, static_cast<long long>(g.ldy), g.bias, g.act);
-    }
     // stream-ordered: released after the kernels above have used them
     if (xp) cudaFreeAsync(xp, stream);
     if (ws) cudaFreeAsync(ws, stream);
+    if (cnt) cudaFreeAsync(cnt, stream);
     return e;
 }
 

@@ -192,7 +192,7 @@ GTG_API gtg_status gemv_f32(int64_t M, int64_t N,
  * half-precision storage), so halving its bytes halves the time; each BF16
  * value is widened to FP32 exactly before it is used, and the result differs
  * from gemv_f32 on the widened matrix only by the order of FP32 additions.
- * Batch 3..8 with a 16-byte aligned A, lda % 8 == 0 and M * N >= 2^25 runs
+ * Batch 6..8 with a 16-byte aligned A, lda % 8 == 0 and M * N >= 2^25 runs
  * on the tensor cores: each FP32 vector entry is split into three BF16 pieces (x = x1 + x2
  * + x3 to within 2^-27 |x|), every product of a matrix element with a piece
  * is exact, and the tensor core accumulates in FP32, so the result meets the
@@ -533,7 +533,8 @@ GTG_API void gtg_test_skip_vector_copy(int on);
  * By default (mode 0) such a call runs on the tensor cores (the vectors split
  * into three BF16 pieces each, see gemv_bf16) when the tensor memory
  * accelerator can read the matrix (16-byte aligned A, lda * 2 a multiple of
- * 16) and it has at least 2^25 elements, else on the CUDA-core kernels.
+ * 16), it has at least 2^25 elements and batch >= 6, else on the CUDA-core
+ * kernels.
  * Mode 1 always takes the CUDA-core kernels; mode 2 takes the tensor cores
  * whenever the layout allows, at any size. Other values act as 0.
  * Process-wide.

@@ -77,7 +77,8 @@ def test_planner_sizes():
     assert _plan(8192, 4096, 8)["kernel"] == "tcgen05"    # 2^25 elements
     assert _plan(4096, 4096, 8)["kernel"] == "gemv"       # below: the CUDA cores
     assert _plan(8192, 8192, 2)["kernel"] == "gemv"       # batch 1-2: the streaming kernel
-    assert _plan(8192, 8192, 3)["kernel"] == "tcgen05"
+    assert _plan(8192, 8192, 5)["kernel"] == "gemv"       # batch 3-5: the CUDA cores
+    assert _plan(8192, 8192, 6)["kernel"] == "tcgen05"
 
 
 def test_tc_gemv_unaligned_rows_take_the_cuda_cores():
