@@ -710,9 +710,15 @@ def cpu_baseline(target_s: float = 10.0):
     dt, fl = oracle_gemm_sample(4)
     rows = max(4, min(8192, int(4 * target_s / max(dt, 1e-3))))
     dt, fl = oracle_gemm_sample(rows)
+    # the same oracle on one host thread, a ~3 s sample
+    dt1, _ = oracle_gemm_sample(1, threads=1)
+    rows1 = max(1, min(64, int(3.0 / max(dt1, 1e-3))))
+    dt1, fl1 = oracle_gemm_sample(rows1, threads=1)
     return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{rows} rows x 8192 x 8192 of the 8192^3 BF16 GEMM (FP64, with the error magnitude E), "
-                      f"{dt:.1f} s", "seconds": round(dt, 2)}
+                      f"{dt:.1f} s", "seconds": round(dt, 2),
+            "one_core": {"value": round(fl1 / dt1 / 1e12, 6), "cores": 1,
+                         "sample": f"{rows1} rows x 8192 x 8192, {dt1:.1f} s"}}
 
 
 def reference_arm(args, rank, world):
