@@ -430,18 +430,26 @@ def only_conv(idx, local_rank):
     return {"config": name, "ms_per_call": [round(t, 4) for t in times]}
 
 
-def time_launches(fn, iters, stream):
+def time_launches(fn, iters, stream, groups=5):
+    """Mean time per launch (ms) of `groups` groups of about iters / groups
+    back-to-back launches, each group between CUDA events on `stream`, after
+    three warm-up launches: returns (median over the groups, best group)."""
     import torch
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for i in range(3):
         fn(i)
     torch.cuda.synchronize()
-    s.record(stream)
-    for i in range(iters):
-        fn(i)
-    e.record(stream)
+    per = max(1, iters // groups)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(groups)]
+    i = 0
+    for s, e in evs:
+        s.record(stream)
+        for _ in range(per):
+            fn(i)
+            i += 1
+        e.record(stream)
     torch.cuda.synchronize()
-    return s.elapsed_time(e) / iters
+    ts = sorted(s.elapsed_time(e) / per for s, e in evs)
+    return ts[len(ts) // 2], ts[0]
 
 
 def sweep(dev, stream, peaks, l2):
@@ -476,11 +484,11 @@ def sweep(dev, stream, peaks, l2):
             st = fn(M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N, ep, sh)
             assert st == gtg.GTG_OK, st
 
-        ms = time_launches(call, iters, stream)
+        ms, ms_best = time_launches(call, iters, stream)
         a, b, c = sets[0]
         plan = gtg.plan_gemm(prec, M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(), N)
         tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
-        out.append({"config": name, "path": prec, "shape": [M, N, K], "ms": round(ms, 4),
+        out.append({"config": name, "path": prec, "shape": [M, N, K], "ms": round(ms, 4), "ms_best": round(ms_best, 4),
                     "TFLOP/s": round(tf, 2), "peak": peak, "peak_name": peak_name,
                     "frac": round(tf / peak, 4) if peak else None, "kernel": plan["kernel"],
                     "tile": [plan["bm"], plan["bn"], plan["bk"]], "grid": plan["grid"], "buffer_sets": nrot})
@@ -527,10 +535,10 @@ def sweep(dev, stream, peaks, l2):
                                           C.data_ptr(), N, M * N, batch, None, sh)
             assert st == gtg.GTG_OK, st
 
-        ms = time_launches(call, iters, stream)
+        ms, ms_best = time_launches(call, iters, stream)
         tf = 2.0 * batch * M * N * K / (ms * 1e-3) / 1e12
         out.append({"config": name, "path": "bf16 strided batch", "shape": [M, N, K], "batch": batch,
-                    "ms": round(ms, 4), "TFLOP/s": round(tf, 2), "peak": bf16_peak, "peak_name": "bf16 burst",
+                    "ms": round(ms, 4), "ms_best": round(ms_best, 4), "TFLOP/s": round(tf, 2), "peak": bf16_peak, "peak_name": "bf16 burst",
                     "frac": round(tf / bf16_peak, 4)})
 
     def conv_cfg(name, N, H, W, C, CO, KH, KW, st, pd, iters):
@@ -545,12 +553,12 @@ def sweep(dev, stream, peaks, l2):
                                  Y.data_ptr(), None, sh)
             assert rc == gtg.GTG_OK, rc
 
-        ms = time_launches(call, iters, stream)
+        ms, ms_best = time_launches(call, iters, stream)
         M, K = N * OH * OW, KH * KW * C
         tf = 2.0 * M * K * CO / (ms * 1e-3) / 1e12
         direct = KH == 1 and KW == 1 and st == 1 and pd == 0
         out.append({"config": name, "path": "bf16 conv (im2col + GEMM)" if not direct else "bf16 conv (GEMM on X)",
-                    "gemm_shape": [M, CO, K], "ms": round(ms, 4), "TFLOP/s": round(tf, 2), "peak": bf16_peak,
+                    "gemm_shape": [M, CO, K], "ms": round(ms, 4), "ms_best": round(ms_best, 4), "TFLOP/s": round(tf, 2), "peak": bf16_peak,
                     "peak_name": "bf16 burst", "frac": round(tf / bf16_peak, 4),
                     "im2col_bytes": 0 if direct else M * ((K + 7) // 8 * 8) * 2})
 
@@ -582,13 +590,13 @@ def sweep(dev, stream, peaks, l2):
                 st = gtg.gemv_f32_ex(n, n, As[i % nrot].data_ptr(), n, X.data_ptr(), n, Y.data_ptr(), n, batch,
                                      ep, sh)
                 assert st == gtg.GTG_OK, st
-            ms = time_launches(call, 100, stream)
+            ms, ms_best = time_launches(call, 250, stream)
             byt = 4.0 * n * n + batch * 4.0 * (2 * n) + (4.0 * n if act else 0.0)
             gbs = byt / (ms * 1e-3) / 1e9
             name = (f"f1: f32 dense vector {n}x{n}, bias + ReLU" if act else
                     f"2: f32 gemv {n}x{n} batch {batch}")
             out.append({"config": name, "path": "gemv_f32", "shape": [n, n],
-                        "batch": batch, "ms": round(ms, 5), "GB/s": round(gbs, 1), "peak": hbm,
+                        "batch": batch, "ms": round(ms, 5), "ms_best": round(ms_best, 5), "GB/s": round(gbs, 1), "peak": hbm,
                         "frac": round(gbs / hbm, 4), "buffer_sets": nrot})
         del As, X, Y
         # the same layer with its weights stored in BF16 (half the bytes)
@@ -602,11 +610,11 @@ def sweep(dev, stream, peaks, l2):
             def call(i, batch=batch):
                 st = gtg.gemv_bf16(n, n, As[i % nrot].data_ptr(), n, X.data_ptr(), n, Y.data_ptr(), n, batch, sh)
                 assert st == gtg.GTG_OK, st
-            ms = time_launches(call, 100, stream)
+            ms, ms_best = time_launches(call, 250, stream)
             byt = 2.0 * n * n + batch * 4.0 * (2 * n)
             gbs = byt / (ms * 1e-3) / 1e9
             out.append({"config": f"f2: bf16-matrix gemv {n}x{n} batch {batch}", "path": "gemv_bf16",
-                        "shape": [n, n], "batch": batch, "ms": round(ms, 5), "GB/s": round(gbs, 1), "peak": hbm,
+                        "shape": [n, n], "batch": batch, "ms": round(ms, 5), "ms_best": round(ms_best, 5), "GB/s": round(gbs, 1), "peak": hbm,
                         "frac": round(gbs / hbm, 4), "buffer_sets": nrot})
         del As, X, Y
     torch.cuda.empty_cache()
@@ -638,10 +646,10 @@ def ablation(dev, stream, f32_peak, hbm, l2, iters=0):
                 st = gtg.gtg_ablation_gemm_f32(variant, M, N, K, a.data_ptr(), K, b.data_ptr(), N, c.data_ptr(),
                                                N, sh)
             assert st == gtg.GTG_OK, st
-        times[variant] = time_launches(call, iters or (10 if variant.startswith("naive") else 30), stream)
+        times[variant], best = time_launches(call, iters or (10 if variant.startswith("naive") else 30), stream)
         tf = 2.0 * M * N * K / (times[variant] * 1e-3) / 1e12
         out.append({"config": f"f3: f32 gemm 1024^3, {variant}", "path": "ablation" if variant != "library" else "f32",
-                    "shape": [M, N, K], "ms": round(times[variant], 4), "TFLOP/s": round(tf, 2), "peak": f32_peak,
+                    "shape": [M, N, K], "ms": round(times[variant], 4), "ms_best": round(best, 4), "TFLOP/s": round(tf, 2), "peak": f32_peak,
                     "frac": round(tf / f32_peak, 4),
                     "speedup_vs_naive16": round(times["naive16"] / times[variant], 2)})
     del sets
@@ -659,10 +667,10 @@ def ablation(dev, stream, f32_peak, hbm, l2, iters=0):
                 st = gtg.gtg_ablation_gemv_f32(variant, M, N, As[i % nrot].data_ptr(), N, x.data_ptr(),
                                                y.data_ptr(), sh)
             assert st == gtg.GTG_OK, st
-        times[variant] = time_launches(call, iters or (20 if variant != "library" else 100), stream)
+        times[variant], best = time_launches(call, iters or (20 if variant != "library" else 100), stream)
         gbs = (4.0 * M * N + 8.0 * M) / (times[variant] * 1e-3) / 1e9
         out.append({"config": f"f3: f32 gemv 4096^2, {variant}", "path": "ablation" if variant != "library" else "gemv_f32",
-                    "shape": [M, N], "ms": round(times[variant], 5), "GB/s": round(gbs, 1), "peak": hbm,
+                    "shape": [M, N], "ms": round(times[variant], 5), "ms_best": round(best, 5), "GB/s": round(gbs, 1), "peak": hbm,
                     "frac": round(gbs / hbm, 4), "speedup_vs_naive": round(times["naive"] / times[variant], 2)})
     del As
     torch.cuda.empty_cache()
