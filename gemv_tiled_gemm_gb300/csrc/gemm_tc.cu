@@ -697,32 +697,76 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::cluster_sync();
 }
 
-// B (K x N, leading dimension ldb) -> Bt (N x K, leading dimension ldbt),
-// through a padded shared-memory tile so that reads and writes are both
-// coalesced. blockIdx.z walks the items of a batch (strideB apart in B,
-// N * ldbt apart in Bt).
+// B (K x N, leading dimension ldb) -> Bt (N x K, leading dimension ldbt, a
+// multiple of 4), through a 64 x 64 shared-memory tile. VEC: B's rows are
+// 16-byte aligned (base and ldb), so every thread moves 16-byte pieces both
+// ways (a row of B or Bt is 16 of them per tile); edges of the matrix take
+// single elements. blockIdx.z walks the items of a batch (strideB apart in
+// B, N * ldbt apart in Bt).
+template <bool VEC>
 __global__ void __launch_bounds__(256) transpose_kernel(const float *__restrict__ B, long long ldb,
                                                         float *__restrict__ Bt, long long ldbt, int K, int N,
                                                         long long strideB) {
-    __shared__ float tile[32][33];
+    __shared__ float tile[64][65];
     B += blockIdx.z * strideB;
     Bt += blockIdx.z * static_cast<long long>(N) * ldbt;
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
-    const int n0 = blockIdx.x * 32;
-    for (int k0 = blockIdx.y * 32; k0 < K; k0 += gridDim.y * 32) {
+    const int n0 = blockIdx.x * 64;
+    for (int k0 = blockIdx.y * 64; k0 < K; k0 += gridDim.y * 64) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int k = k0 + ty + 8 * j, n = n0 + tx;
-            if (k < K && n < N) tile[ty + 8 * j][tx] = __ldg(B + static_cast<long long>(k) * ldb + n);
+        for (int i = 0; i < 4; ++i) {
+            const int idx = static_cast<int>(threadIdx.x) + 256 * i;
+            const int r = idx >> 4, c = (idx & 15) * 4;   // row k0 + r, columns n0 + c .. + 3
+            const int k = k0 + r, n = n0 + c;
+            float v[4] = {0.f, 0.f, 0.f, 0.f};
+            if (k < K) {
+                const float *src = B + static_cast<long long>(k) * ldb + n;
+                if (VEC && n + 3 < N) {
+                    const float4 q = __ldg(reinterpret_cast<const float4 *>(src));
+                    v[0] = q.x;
+                    v[1] = q.y;
+                    v[2] = q.z;
+                    v[3] = q.w;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (n + j < N) v[j] = __ldg(src + j);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tile[r][c + j] = v[j];
         }
         __syncthreads();
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int n = n0 + ty + 8 * j, k = k0 + tx;
-            if (n < N && k < K) Bt[static_cast<long long>(n) * ldbt + k] = tile[tx][ty + 8 * j];
+        for (int i = 0; i < 4; ++i) {
+            const int idx = static_cast<int>(threadIdx.x) + 256 * i;
+            const int r = idx >> 4, c = (idx & 15) * 4;   // row n0 + r of Bt, columns k0 + c .. + 3
+            const int n = n0 + r, k = k0 + c;
+            if (n < N) {
+                float *dst = Bt + static_cast<long long>(n) * ldbt + k;
+                if (k + 3 < K) {
+                    *reinterpret_cast<float4 *>(dst) = make_float4(tile[c][r], tile[c + 1][r], tile[c + 2][r], tile[c + 3][r]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (k + j < K) dst[j] = tile[c + j][r];
+                }
+            }
         }
         __syncthreads();
     }
+}
+
+// Bt = B^T on `stream` (the TF32 kernels' K-major copy of B).
+cudaError_t transpose_launch(const float *B, int64_t ldb, float *Bt, int64_t ldbt, int64_t K, int64_t N,
+                             int64_t batch, int64_t strideB, cudaStream_t stream) {
+    const dim3 grid(static_cast<unsigned>((N + 63) / 64), static_cast<unsigned>(std::min<int64_t>((K + 63) / 64, 65535)),
+                    static_cast<unsigned>(batch));
+    const bool vec = (reinterpret_cast<uintptr_t>(B) & 15) == 0 && (ldb & 3) == 0 && (batch == 1 || (strideB & 3) == 0);
+    if (vec)
+        transpose_kernel<true><<<grid, 256, 0, stream>>>(B, ldb, Bt, ldbt, static_cast<int>(K), static_cast<int>(N), strideB);
+    else
+        transpose_kernel<false><<<grid, 256, 0, stream>>>(B, ldb, Bt, ldbt, static_cast<int>(K), static_cast<int>(N), strideB);
+    return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- host side
@@ -913,12 +957,8 @@ cudaError_t launch_impl(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
         const int64_t ldbt = (g.K + 3) / 4 * 4;   // 16-byte rows for the tensor map
         cudaError_t e = ws_alloc(reinterpret_cast<void **>(&bt), static_cast<size_t>(g.batch * g.N * ldbt) * 4, stream);
         if (e != cudaSuccess) return e;
-        const dim3 tgrid(static_cast<unsigned>((g.N + 31) / 32),
-                         static_cast<unsigned>(std::min<int64_t>((g.K + 31) / 32, 65535)),
-                         static_cast<unsigned>(g.batch));
-        transpose_kernel<<<tgrid, 256, 0, stream>>>(static_cast<const float *>(g.B), g.ldb, bt, ldbt,
-                                                    static_cast<int>(g.K), static_cast<int>(g.N), g.strideB);
-        if ((e = cudaGetLastError()) != cudaSuccess) {
+        if ((e = transpose_launch(static_cast<const float *>(g.B), g.ldb, bt, ldbt, g.K, g.N, g.batch, g.strideB,
+                                  stream)) != cudaSuccess) {
             cudaFreeAsync(bt, stream);
             return e;
         }
@@ -1003,12 +1043,8 @@ cudaError_t launch_pair(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
         const int64_t ldbt = (g.K + 3) / 4 * 4;   // 16-byte rows for the tensor map
         cudaError_t e = ws_alloc(reinterpret_cast<void **>(&bt), static_cast<size_t>(g.batch * g.N * ldbt) * 4, stream);
         if (e != cudaSuccess) return e;
-        const dim3 tgrid(static_cast<unsigned>((g.N + 31) / 32),
-                         static_cast<unsigned>(std::min<int64_t>((g.K + 31) / 32, 65535)),
-                         static_cast<unsigned>(g.batch));
-        transpose_kernel<<<tgrid, 256, 0, stream>>>(static_cast<const float *>(g.B), g.ldb, bt, ldbt,
-                                                    static_cast<int>(g.K), static_cast<int>(g.N), g.strideB);
-        if ((e = cudaGetLastError()) != cudaSuccess) {
+        if ((e = transpose_launch(static_cast<const float *>(g.B), g.ldb, bt, ldbt, g.K, g.N, g.batch, g.strideB,
+                                  stream)) != cudaSuccess) {
             cudaFreeAsync(bt, stream);
             return e;
         }
@@ -1404,11 +1440,7 @@ cudaError_t launch_tf32_fixed(const DeviceInfo &dev, const GemmArgs &g, const gt
     if (!encode_3d(&tb, GTG_PREC_TF32, bt, g.K, g.N, ldbt, 1, 0, S::BK, BN)) return cudaErrorInvalidValue;
     // B^T overwrites every element the GEMM reads, so the array's previous
     // contents never matter and nothing needs clearing.
-    const dim3 tgrid(static_cast<unsigned>((g.N + 31) / 32),
-                     static_cast<unsigned>(std::min<int64_t>((g.K + 31) / 32, 65535)));
-    transpose_kernel<<<tgrid, 256, 0, stream>>>(static_cast<const float *>(g.B), g.ldb, bt, ldbt,
-                                                static_cast<int>(g.K), static_cast<int>(g.N), 0);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = transpose_launch(static_cast<const float *>(g.B), g.ldb, bt, ldbt, g.K, g.N, 1, 0, stream);
     if (e != cudaSuccess) return e;
     TcParams p;
     p.C = g.C;
