@@ -42,6 +42,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -409,11 +410,13 @@ void gemv_tc_plan(const DeviceInfo &dev, const GemvArgs &g, gtg_plan *plan) {
 }
 
 cudaError_t gemv_tc_launch(const DeviceInfo &dev, const GemvArgs &g, cudaStream_t stream) {
-    static bool attr_done[64] = {};
-    if (!attr_done[dev.id & 63]) {
+    // the shared-memory attribute, once per device (setting it twice is harmless)
+    static std::atomic<uint64_t> attr_done{0};
+    const uint64_t bit = uint64_t{1} << (dev.id & 63);
+    if (!(attr_done.load() & bit)) {
         const cudaError_t e = cudaFuncSetAttribute(gemv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e != cudaSuccess) return e;
-        attr_done[dev.id & 63] = true;
+        attr_done.fetch_or(bit);
     }
     const long long tiles = (g.M + kBM - 1) / kBM, ks = (g.N + kBK - 1) / kBK;
     const long long work = tiles * ks;
