@@ -82,6 +82,7 @@ SIGNATURES = {
                              ctypes.POINTER(GtgPlan)]),
     "gtg_force_simt": (None, [_int]),
     "gtg_force_gemm_splits": (None, [_int]),
+    "gtg_force_c_store": (None, [_int]),
     "gtg_conv_force_path": (None, [_int]),
     "gtg_test_skip_vector_copy": (None, [_int]),
     "gtg_gemv_force_path": (None, [_int]),
@@ -266,6 +267,11 @@ def gtg_conv_force_path(mode: str) -> None:
 def gtg_force_gemm_splits(splits: int) -> None:
     """Testing / tuning hook: split K of tensor-core GEMMs `splits` ways (0: planner's choice)."""
     lib().gtg_force_gemm_splits(int(splits))
+
+
+def gtg_force_c_store(mode: str) -> None:
+    """Testing / tuning hook: C stores of the CTA-pair GEMM, "auto", "direct" or "tensor"."""
+    lib().gtg_force_c_store({"auto": 0, "direct": 1, "tensor": 2}[mode])
 
 
 def gtg_set_wait_limit_ns(ns: int) -> None:

@@ -605,6 +605,8 @@ void gtg_gemv_force_path(int mode) { gemv_force_path(mode); }
 
 void gtg_force_gemm_splits(int splits) { tc_force_splits(splits); }
 
+void gtg_force_c_store(int mode) { tc_force_c_store(mode); }
+
 void gtg_conv_force_path(int mode) { g_conv_mode.store(mode == 1 || mode == 2 ? mode : 0); }
 
 int gtg_version(void) { return 100; }

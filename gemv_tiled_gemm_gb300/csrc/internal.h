@@ -80,6 +80,7 @@ cudaError_t tc_launch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &
 void tc_set_wait_limit_ns(unsigned long long ns);
 void tc_drop_next_load(int slice);
 void tc_force_splits(int splits);   // > 0: every eligible single product splits K that many ways
+void tc_force_c_store(int mode);    // CTA-pair kernel's C stores: 0 auto, 1 direct, 2 tensor stores
 
 // ---- TF32 GEMM whose B^T staging buffer is a fixed array in the library
 // (gemm_tc.cu), for callers that cannot allocate device memory

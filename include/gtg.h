@@ -488,6 +488,17 @@ GTG_API gtg_status gtg_plan_gemv_bf16(int64_t M, int64_t N, const gtg_bf16 *A, i
 GTG_API void gtg_force_gemm_splits(int splits);
 
 /*
+ * Testing and tuning hook for how the CTA-pair tensor-core kernel (16-bit
+ * and TF32 inputs, 256 x 256 tiles) writes C: 0 (default) lets each call
+ * choose; 1 always stores each thread's row of the tile straight to global
+ * memory; 2 goes through shared memory and tensor stores (32 x 32 FP32
+ * blocks) whenever C's layout allows them (16-byte aligned base, ldc and
+ * batch stride multiples of 4 elements, K not split). Other values act as 0.
+ * Process-wide; results are identical in every mode.
+ */
+GTG_API void gtg_force_c_store(int mode);
+
+/*
  * Testing hook for conv2d_nhwc: 0 (default) lets each call choose; 1 always
  * writes the patch matrix and multiplies it (im2col + GEMM); 2 requires the
  * implicit GEMM, whose tensor-core kernel loads the patches straight from X

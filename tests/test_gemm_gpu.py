@@ -146,6 +146,27 @@ def test_cta_pair_kernel_half_tiles(prec, M, N, K):
     check_gemm(prec, A, B, C, rows=np.unique(rows))
 
 
+@pytest.mark.parametrize("mode", ["direct", "tensor"])
+@pytest.mark.parametrize("prec,M,N,K,cpad", [("bf16", 4252, 4160, 520, 0), ("bf16", 4000, 4000, 200, 4),
+                                             ("f16", 3000, 2008, 1024, 12), ("tf32", 4224, 4160, 72, 4),
+                                             ("bf16", 4096, 4104, 64, 2), ("bf16", 2048, 1544, 256, 8)])
+def test_cta_pair_kernel_c_stores(mode, prec, M, N, K, cpad):
+    # the pair kernel's two ways of writing C (direct row stores, or 32 x 32
+    # blocks through shared memory and tensor stores that clip at M and N):
+    # ragged last row and column tiles, half tiles, padded ldc (ldc = N + 2
+    # has 8-byte rows, so tensor stores are not allowed and direct ones run);
+    # the guard bands around C check that nothing is written past N or M
+    A, B = inputs(prec, M, N, K, 500 + K + cpad)
+    gtg.gtg_force_c_store(mode)
+    try:
+        C = run_gemm(prec, A, B, ldc=N + cpad, expect_kernel="tcgen05")
+        assert gtg_plan(prec, M, N, K)["bm"] == 256
+    finally:
+        gtg.gtg_force_c_store("auto")
+    rows = np.concatenate([sample_rows(M, seed=4), np.arange(M - 130, M)])
+    check_gemm(prec, A, B, C, rows=np.unique(rows))
+
+
 # ---- layouts the tensor-memory path cannot take: the SIMT fallback --------------
 
 @pytest.mark.parametrize("cpad", [5, 4, 8])
