@@ -69,9 +69,11 @@ struct Load<__half> {
     }
 };
 
-template <typename T, int BM, int BN, bool VEC>
+// Each thread owns 8 rows x TN columns of the tile (TN = 8, or 4 for twice
+// the threads on the same tile when tiles are few).
+template <typename T, int BM, int BN, bool VEC, int TN = 8>
 struct SimtTile {
-    static constexpr int TX = BN / 8;              // threads along N
+    static constexpr int TX = BN / TN;             // threads along N
     static constexpr int TY = BM / 8;              // threads along M
     static constexpr int THREADS = TX * TY;
 
@@ -84,12 +86,13 @@ struct SimtTile {
 // K range [z * k_per, (z + 1) * k_per) and writes its FP32 partial product to
 // the workspace slice ws + z * M * N (leading dimension N) instead of C;
 // split_reduce_kernel then adds the S slices in order z = 0 .. S-1.
-template <typename T, int BM, int BN, bool VEC>
-__global__ void __launch_bounds__(SimtTile<T, BM, BN, VEC>::THREADS)
+template <typename T, int BM, int BN, bool VEC, int TN>
+__global__ void __launch_bounds__(SimtTile<T, BM, BN, VEC, TN>::THREADS)
     simt_gemm_kernel(int M, int N, int K, const T *__restrict__ A, long long lda,
                      const T *__restrict__ B, long long ldb, float *__restrict__ C, long long ldc,
                      int c_vec, int k_per, float *__restrict__ ws, const float *__restrict__ bias, int act) {
-    using L = SimtTile<T, BM, BN, VEC>;
+    using L = SimtTile<T, BM, BN, VEC, TN>;
+    constexpr int QN = TN / 2;   // column pairs per thread
     if (gridDim.z > 1) {
         bias = nullptr;   // partial products: the reduction applies the epilogue
         act = 0;
@@ -183,11 +186,11 @@ __global__ void __launch_bounds__(SimtTile<T, BM, BN, VEC>::THREADS)
     // of a packed FMA is one IEEE fused multiply-add, so every output sees the
     // same operations in the same K order as with scalar FMAs (and the same
     // result).
-    float2 d[4][4][2];
+    float2 d[4][QN][2];
 #pragma unroll
     for (int p = 0; p < 4; ++p)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) d[p][q][0] = d[p][q][1] = make_float2(0.f, 0.f);
+        for (int q = 0; q < QN; ++q) d[p][q][0] = d[p][q][1] = make_float2(0.f, 0.f);
 
     const int ntiles = (K + kBK - 1) / kBK;
     if (ntiles > 0) {
@@ -209,7 +212,7 @@ __global__ void __launch_bounds__(SimtTile<T, BM, BN, VEC>::THREADS)
             const float4 a0 = *reinterpret_cast<const float4 *>(&As[cur][k][ty * 4]);
             const float4 a1 = *reinterpret_cast<const float4 *>(&As[cur][k][BM / 2 + ty * 4]);
             const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[cur][k][tx * 4]);
-            const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[cur][k][BN / 2 + tx * 4]);
+            const float4 b1 = TN == 8 ? *reinterpret_cast<const float4 *>(&Bs[cur][k][BN / 2 + tx * 4]) : b0;
             const float2 ap[4] = {make_float2(a0.x, a0.y), make_float2(a0.z, a0.w), make_float2(a1.x, a1.y),
                                   make_float2(a1.z, a1.w)};
             const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
@@ -219,7 +222,7 @@ __global__ void __launch_bounds__(SimtTile<T, BM, BN, VEC>::THREADS)
 #pragma unroll
             for (int p = 0; p < 4; ++p)
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < QN; ++q) {
                     d[p][q][0] = __ffma2_rn(ap[p], bp[q], d[p][q][0]);
                     d[p][q][1] = __ffma2_rn(ap[p], bs[q], d[p][q][1]);
                 }
@@ -231,24 +234,25 @@ __global__ void __launch_bounds__(SimtTile<T, BM, BN, VEC>::THREADS)
         __syncthreads();
     }
 
-    float acc[8][8];
+    float acc[8][TN];
 #pragma unroll
     for (int p = 0; p < 4; ++p)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < QN; ++q) {
             acc[2 * p][2 * q] = d[p][q][0].x;
             acc[2 * p + 1][2 * q + 1] = d[p][q][0].y;
             acc[2 * p][2 * q + 1] = d[p][q][1].x;
             acc[2 * p + 1][2 * q] = d[p][q][1].y;
         }
-    // rows ty*4 + i (i < 4) and BM/2 + ty*4 + i; columns likewise in N.
+    // rows ty*4 + i (i < 4) and BM/2 + ty*4 + i; columns tx*4 + j and (TN = 8)
+    // BN/2 + tx*4 + j.
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int row = m0 + (i < 4 ? ty * 4 + i : BM / 2 + ty * 4 + (i - 4));
         if (row >= M) continue;
         float *crow = C + static_cast<long long>(row) * ldc;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < TN / 4; ++h) {
             const int col = n0 + (h == 0 ? tx * 4 : BN / 2 + tx * 4);
             float v[4];
 #pragma unroll
@@ -319,9 +323,9 @@ __global__ void zero_fill_kernel(float *C, long long M, long long N, long long l
         C[(i / N) * ldc + (i % N)] = 0.f;
 }
 
-template <typename T, int BM, int BN, bool VEC>
+template <typename T, int BM, int BN, bool VEC, int TN>
 cudaError_t launch_one(const GemmArgs &g, int splits, cudaStream_t stream) {
-    using L = SimtTile<T, BM, BN, VEC>;
+    using L = SimtTile<T, BM, BN, VEC, TN>;
     dim3 grid(static_cast<unsigned>((g.N + BN - 1) / BN), static_cast<unsigned>((g.M + BM - 1) / BM),
               static_cast<unsigned>(splits));
     const int c_vec = ((reinterpret_cast<uintptr_t>(g.C) & 15) == 0 && (g.ldc & 3) == 0) ? 1 : 0;
@@ -332,7 +336,7 @@ cudaError_t launch_one(const GemmArgs &g, int splits, cudaStream_t stream) {
         e = ws_alloc(reinterpret_cast<void **>(&ws), static_cast<size_t>(splits) * g.M * g.N * sizeof(float), stream);
         if (e != cudaSuccess) return e;
     }
-    simt_gemm_kernel<T, BM, BN, VEC><<<grid, L::THREADS, 0, stream>>>(
+    simt_gemm_kernel<T, BM, BN, VEC, TN><<<grid, L::THREADS, 0, stream>>>(
         static_cast<int>(g.M), static_cast<int>(g.N), static_cast<int>(g.K),
         static_cast<const T *>(g.A), g.lda, static_cast<const T *>(g.B), g.ldb, g.C, g.ldc, c_vec, k_per, ws,
         g.bias, g.act);
@@ -347,8 +351,8 @@ cudaError_t launch_one(const GemmArgs &g, int splits, cudaStream_t stream) {
 
 template <typename T, bool VEC>
 cudaError_t launch_typed(const GemmArgs &g, const gtg_plan &plan, cudaStream_t stream) {
-    if (plan.bm == 128) return launch_one<T, 128, 128, VEC>(g, plan.splits, stream);
-    return launch_one<T, 64, 64, VEC>(g, plan.splits, stream);
+    if (plan.bm == 128) return launch_one<T, 128, 128, VEC, 8>(g, plan.splits, stream);
+    return launch_one<T, 64, 64, VEC, 4>(g, plan.splits, stream);
 }
 
 bool vec_ok(const GemmArgs &g) {
@@ -360,26 +364,46 @@ bool vec_ok(const GemmArgs &g) {
 
 }  // namespace
 
-// Tile: 128 x 128 (8 warps) when there are enough such tiles for every SM,
-// else 64 x 64 (2 warps). Small grids then split K (plan->splits)
-// so that about six CTAs run on every SM, each split keeping at least two
-// 16-deep K slices; the partial products go through a workspace.
+// Tile: 128 x 128 (8 warps, 8 x 8 outputs per thread) when there are enough
+// such tiles for every SM. Otherwise, when K is long enough, 128 x 128 tiles
+// split in K so that the CTAs fill at least three quarters of the SMs once
+// (one CTA of 8 warps per SM); else 64 x 64 tiles of 4 warps (8 x 4 outputs
+// per thread), whose small grids split K (plan->splits) so that about six
+// CTAs run on every SM, each split keeping at least two 16-deep K slices; the
+// partial products go through a workspace. Measured (FP32, CUDA events):
+// 1024^3 96.5 us with the earlier 2-warp 64 x 64 tiles, 76 us with 4-warp
+// ones, 65.7 us as 128 x 128 tiles in two K ranges; the 4-warp tiles are as
+// fast or faster on every small shape tried (256^3 to 2048^3, 1000 x 700 x
+// 1500, 1024^2 x 4096).
 void simt_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
     const int64_t big_tiles = ((g.M + 127) / 128) * ((g.N + 127) / 128);
+    const int64_t kslices = (g.K + kBK - 1) / kBK;
     const bool big = big_tiles >= dev.sms;
     plan->kernel = GTG_KERNEL_SIMT;
-    plan->bm = plan->bn = big ? 128 : 64;
     plan->bk = kBK;
-    plan->threads = big ? 256 : 64;
     plan->smem = 0;
     plan->cluster = 1;
+    plan->stages = 2;   // double-buffered shared-memory slices
+    if (!big && big_tiles > 0) {
+        int64_t fill = std::min<int64_t>(dev.sms / big_tiles, kslices / 32);
+        if (fill >= 2 && 4 * big_tiles * fill >= 3 * dev.sms) {
+            const int64_t k_per = (kslices + fill - 1) / fill;   // every split owns K slices
+            fill = (kslices + k_per - 1) / k_per;
+            plan->bm = plan->bn = 128;
+            plan->threads = 256;
+            plan->splits = static_cast<int>(fill);
+            plan->grid = static_cast<int>(big_tiles * fill);
+            return;
+        }
+    }
+    plan->bm = plan->bn = big ? 128 : 64;
+    plan->threads = big ? 256 : 128;
     const int64_t tiles = ((g.M + plan->bm - 1) / plan->bm) * ((g.N + plan->bn - 1) / plan->bn);
     int64_t splits = 1;
     if (!big) {
         // the busiest SM's K work: ceil(CTAs / SMs) CTAs of ceil(slices / S)
         // slices each; a split must save more than a fixed allowance for the
         // extra partial-product traffic and the reduction launch
-        const int64_t kslices = (g.K + kBK - 1) / kBK;
         auto work = [&](int64_t sp) {
             const int64_t per = (kslices + sp - 1) / sp;
             return static_cast<double>((tiles * sp + dev.sms - 1) / dev.sms) * per + (sp > 1 ? 0.25 * kslices + 4 : 0);
@@ -396,7 +420,6 @@ void simt_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
         const int64_t k_per = (kslices + splits - 1) / splits;
         splits = (kslices + k_per - 1) / k_per;
     }
-    plan->stages = 2;   // double-buffered shared-memory slices
     plan->splits = static_cast<int>(splits);
     plan->grid = static_cast<int>(tiles * splits);
 }

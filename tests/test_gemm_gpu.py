@@ -167,6 +167,23 @@ def test_cta_pair_kernel_c_stores(mode, prec, M, N, K, cpad):
     check_gemm(prec, A, B, C, rows=np.unique(rows))
 
 
+@pytest.mark.parametrize("M,N,K,bm,threads,splits", [
+    (1024, 1024, 1024, 128, 256, 2),    # 64 big tiles in 2 K ranges: one 8-warp CTA on 128 of 152 SMs
+    (1000, 1100, 2000, 128, 256, 2),    # ragged edges, K ranges of 63 slices
+    (256, 256, 256, 64, 128, None),     # small: 4-warp 64 x 64 tiles (K split by the wave model)
+    (4096, 4096, 512, 128, 256, 1),     # enough big tiles for every SM
+])
+def test_simt_tile_choice_and_parity(M, N, K, bm, threads, splits):
+    p = gtg_plan("f32", M, N, K)
+    assert p["kernel"] == "simt" and p["bm"] == bm and p["threads"] == threads, p
+    if splits is not None:
+        assert p["splits"] == splits, p
+    if M * N * K <= 3e9:
+        A, B = inputs("f32", M, N, K, 700 + M)
+        C = run_gemm("f32", A, B, expect_kernel="simt")
+        check_gemm("f32", A, B, C, rows=np.unique(np.concatenate([sample_rows(M, seed=5), np.arange(M - 70, M)])))
+
+
 # ---- layouts the tensor-memory path cannot take: the SIMT fallback --------------
 
 @pytest.mark.parametrize("cpad", [5, 4, 8])
