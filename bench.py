@@ -465,6 +465,16 @@ def sweep(dev, stream, peaks, l2):
     out = []
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
 
+    hbm_peak = peaks.get("hbm_gbs", FALLBACK["hbm_gbs"])
+
+    def roofline_of(flops, nbytes, ms, peak, compute_bound):
+        # the slower of the two bounds: arithmetic at `peak` TFLOP/s, or the
+        # compulsory bytes (operands read once, output written once) at the HBM peak
+        t_c = flops / (peak * 1e12)
+        t_m = nbytes / (hbm_peak * 1e9)
+        return {"compulsory_bytes": int(nbytes), "bound": "hbm" if t_m > t_c else compute_bound,
+                "roofline_frac": round(max(t_c, t_m) / (ms * 1e-3), 4)}
+
     def gemm_cfg(name, prec, M, N, K, A, B, peak, peak_name, iters, bias=None, act="none"):
         esz = 2 if prec in ("bf16", "f16") else 4
         need = (M * K + K * N) * esz + M * N * 4
@@ -491,7 +501,8 @@ def sweep(dev, stream, peaks, l2):
         out.append({"config": name, "path": prec, "shape": [M, N, K], "ms": round(ms, 4), "ms_best": round(ms_best, 4),
                     "TFLOP/s": round(tf, 2), "peak": peak, "peak_name": peak_name,
                     "frac": round(tf / peak, 4) if peak else None, "kernel": plan["kernel"],
-                    "tile": [plan["bm"], plan["bn"], plan["bk"]], "grid": plan["grid"], "buffer_sets": nrot})
+                    "tile": [plan["bm"], plan["bn"], plan["bk"]], "grid": plan["grid"], "buffer_sets": nrot,
+                    **roofline_of(2.0 * M * N * K, need, ms, peak, "fp32 alu" if prec == "f32" else "tensor")})
         del sets
 
     # FP32 SIMT peak: SMs x 128 FP32 lanes x 2 flops x the max SM clock
@@ -539,7 +550,10 @@ def sweep(dev, stream, peaks, l2):
         tf = 2.0 * batch * M * N * K / (ms * 1e-3) / 1e12
         out.append({"config": name, "path": "bf16 strided batch", "shape": [M, N, K], "batch": batch,
                     "ms": round(ms, 4), "ms_best": round(ms_best, 4), "TFLOP/s": round(tf, 2), "peak": bf16_peak, "peak_name": "bf16 burst",
-                    "frac": round(tf / bf16_peak, 4)})
+                    "frac": round(tf / bf16_peak, 4),
+                    **roofline_of(2.0 * batch * M * N * K,
+                                  2 * batch * M * K + 2 * (1 if shared_B else batch) * K * N + 4 * batch * M * N,
+                                  ms, bf16_peak, "tensor")})
 
     def conv_cfg(name, N, H, W, C, CO, KH, KW, st, pd, iters):
         g = PCG32(20 + C + CO)
@@ -560,7 +574,9 @@ def sweep(dev, stream, peaks, l2):
         out.append({"config": name, "path": "bf16 conv (im2col + GEMM)" if not direct else "bf16 conv (GEMM on X)",
                     "gemm_shape": [M, CO, K], "ms": round(ms, 4), "ms_best": round(ms_best, 4), "TFLOP/s": round(tf, 2), "peak": bf16_peak,
                     "peak_name": "bf16 burst", "frac": round(tf / bf16_peak, 4),
-                    "im2col_bytes": 0 if direct else M * ((K + 7) // 8 * 8) * 2})
+                    "im2col_bytes": 0 if direct else M * ((K + 7) // 8 * 8) * 2,
+                    **roofline_of(2.0 * M * K * CO, 2 * N * H * W * C + 2 * KH * KW * C * CO + 4 * M * CO, ms, bf16_peak,
+                                  "tensor")})
 
     for layer in CONV_LAYERS:
         conv_cfg(*layer)
