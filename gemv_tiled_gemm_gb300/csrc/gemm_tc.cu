@@ -448,11 +448,10 @@ struct PairShape {
     static constexpr int EPI_BYTES = 4 * 2 * 32 * 128;
     static constexpr int NBARS = 2 * STAGES + 5;
     static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + NBARS * 8 + 16;
-    static constexpr int GROUP = 8;                // pair row-tiles per raster group
     static_assert(B_KMAJOR || B_CHUNKS * BCH_BYTES == B_BYTES, "MN-major B is whole column blocks");
 };
 
-constexpr int kPairGroup = 8;
+constexpr int kPairGroup = 8;   // pair row-tiles per raster group
 
 __device__ __forceinline__ void pair_tile_coords(int t, const TcParams &p, int &mb, int &nb) {
     const int per_group = kPairGroup * p.num_n;
