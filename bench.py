@@ -61,6 +61,8 @@ def parse_args():
     p.add_argument("--ablation-iters", type=int, default=0, help="timed launches per ablation kernel (0: default)")
     p.add_argument("--only-gemv", default=None, metavar="PREC:N:BATCH",
                    help="run only an N x N GEMV (prec f32 or bf16) at the given batch, three calls (for profiling)")
+    p.add_argument("--only-gemm", default=None, metavar="PREC:M:N:K",
+                   help="run only one GEMM (prec bf16, f16, tf32 or f32), three calls (for profiling)")
     p.add_argument("--only-conv", type=int, default=None, metavar="IDX",
                    help="run only convolutional layer IDX of the sweep, three calls (for profiling)")
     return p.parse_args()
@@ -398,6 +400,43 @@ def only_gemv(spec, local_rank):
     plan = gtg.plan_gemv(n, n, A.data_ptr(), n, X.data_ptr(), n, Y.data_ptr(), n, batch, precision=prec)
     return {"config": f"{prec} gemv {n}x{n} batch {batch}", "kernel": plan["kernel"],
             "ms_per_call": [round(t, 4) for t in times]}
+
+
+def only_gemm(spec, local_rank):
+    """Three calls of one GEMM configuration (seeded inputs: normal for 16-bit
+    operands, uniform [-1, 1) for FP32 ones)."""
+    import numpy as np
+    import torch
+
+    import gemv_tiled_gemm_gb300 as gtg
+    from seeded import PCG32
+
+    prec, m, n, k = spec.split(":")
+    M, N, K = int(m), int(n), int(k)
+    torch.cuda.set_device(local_rank)
+    g = PCG32(8)
+    if prec in ("bf16", "f16"):
+        draw = g.normal_bf16 if prec == "bf16" else g.normal_f16
+        A = torch.from_numpy(draw((M, K)).view(np.int16)).cuda()
+        B = torch.from_numpy(draw((K, N)).view(np.int16)).cuda()
+    else:
+        A = torch.from_numpy(g.uniform_f32((M, K))).cuda()
+        B = torch.from_numpy(g.uniform_f32((K, N))).cuda()
+    C = torch.empty((M, N), device="cuda")
+    fn = {"bf16": gtg.gemm_bf16, "f16": gtg.gemm_f16, "tf32": gtg.gemm_tf32, "f32": gtg.gemm_f32}[prec]
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for _ in range(3):
+        e0.record(s)
+        rc = fn(M, N, K, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N, s.cuda_stream)
+        e1.record(s)
+        assert rc == gtg.GTG_OK, rc
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    assert gtg.gtg_sync_status(s.cuda_stream) == gtg.GTG_OK
+    plan = gtg.plan_gemm(prec, M, N, K, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N)
+    return {"config": f"{prec} gemm {M}x{N}x{K}", "plan": plan, "ms_per_call": [round(t, 4) for t in times]}
 
 
 def only_conv(idx, local_rank):
@@ -792,6 +831,9 @@ def main():
         return 0
     if args.only_conv is not None:
         print(json.dumps(only_conv(args.only_conv, local_rank)), flush=True)
+        return 0
+    if args.only_gemm is not None:
+        print(json.dumps(only_gemm(args.only_gemm, local_rank)), flush=True)
         return 0
 
     if args.only_ablation:

@@ -111,6 +111,43 @@ def test_strided_batched(prec, case):
             assert np.all(np.isnan(C[b * sC + M * ldc: (b + 1) * sC]))
 
 
+@pytest.mark.parametrize("mode", ["direct", "tensor"])
+def test_strided_batched_c_stores(mode):
+    # items large enough for the CTA-pair kernel (2000 x 1000: ragged last row
+    # and column tiles), padded item strides, bias + ReLU: with tensor stores the
+    # 3-D map (columns, rows, item) must clip each item at M and N and leave the
+    # padding between items untouched
+    torch = _t()
+    g = PCG32(960)
+    batch, M, N, K = 3, 2000, 1000, 200
+    sA, sB, sC = M * K + 64, K * N + 128, M * N + 400
+    A_host, A_f = _draw("bf16", g, (batch * sA + 8,))
+    B_host, B_f = _draw("bf16", g, (batch * sB + 8,))
+    dA, dB = _dev("bf16", A_host), _dev("bf16", B_host)
+    dC = torch.full((batch * sC + 8,), float("nan"), device="cuda")
+    bias = g.uniform_f32((N,))
+    db = torch.from_numpy(bias).cuda()
+    s = int(torch.cuda.current_stream().cuda_stream)
+    gtg.gtg_force_c_store(mode)
+    try:
+        st = gtg.gemm_strided_batched("bf16", M, N, K, dA.data_ptr(), K, sA, dB.data_ptr(), N, sB,
+                                      dC.data_ptr(), N, sC, batch, gtg.epilogue(db.data_ptr(), "relu"), s)
+        assert st == gtg.GTG_OK, gtg.status_string(st)
+        assert gtg.gtg_sync_status(s) == gtg.GTG_OK
+    finally:
+        gtg.gtg_force_c_store("auto")
+    C = dC.cpu().numpy()
+    rows = np.unique(np.concatenate([np.arange(0, M, 37), np.arange(M - 100, M)]))
+    for b in range(batch):
+        Ab = A_f[b * sA: b * sA + M * K].reshape(M, K)
+        Bb = B_f[b * sB: b * sB + K * N].reshape(K, N)
+        ref, E = oracle.dense_layer(Ab[rows], Bb, bias, "relu")
+        got = C[b * sC: b * sC + M * N].reshape(M, N)[rows]
+        ratio, bad = parity_ratio(got, ref, E, "bf16", K, rel=2.0 ** -23)
+        assert bad == 0, (b, ratio)
+        assert np.all(np.isnan(C[b * sC + M * N: (b + 1) * sC]))
+
+
 def test_strided_batched_plans_one_launch_for_all_items():
     torch = _t()
     batch, M, N, K = 40, 512, 512, 64
