@@ -26,6 +26,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace gtg {
 namespace {
@@ -93,6 +94,9 @@ __global__ void __launch_bounds__(SimtTile<T, BM, BN, VEC, TN>::THREADS)
                      int c_vec, int k_per, float *__restrict__ ws, const float *__restrict__ bias, int act) {
     using L = SimtTile<T, BM, BN, VEC, TN>;
     constexpr int QN = TN / 2;   // column pairs per thread
+    // a following dependent launch (the split reduction) may be scheduled now;
+    // it waits for this grid before reading anything this grid writes
+    ptx::allow_next_grid();
     if (gridDim.z > 1) {
         bias = nullptr;   // partial products: the reduction applies the epilogue
         act = 0;
@@ -274,6 +278,7 @@ __global__ void __launch_bounds__(SimtTile<T, BM, BN, VEC, TN>::THREADS)
 __global__ void split_reduce_kernel(const float *__restrict__ ws, int splits, int M, int N,
                                     float *__restrict__ C, long long ldc, int vec,
                                     const float *__restrict__ bias, int act) {
+    ptx::wait_prior_grid();   // a dependent launch: the partial products are complete
     const int n4 = (N + 3) / 4;
     const long long slice = static_cast<long long>(M) * N;
     for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
@@ -464,9 +469,19 @@ cudaError_t split_reduce_launch(const float *ws, int splits, int64_t M, int64_t 
     // ws is a pool allocation (256-byte aligned) of rows of N floats: 16-byte
     // accesses need N % 4 == 0, and C a 16-byte aligned base and ldc % 4 == 0
     const int vec = ((N & 3) == 0 && (reinterpret_cast<uintptr_t>(C) & 15) == 0 && (ldc & 3) == 0) ? 1 : 0;
-    split_reduce_kernel<<<blocks, 256, 0, stream>>>(ws, splits, static_cast<int>(M), static_cast<int>(N), C, ldc, vec,
-                                                    bias, act);
-    return cudaGetLastError();
+    // scheduled while the GEMM that wrote ws finishes (programmatic dependent
+    // launch); the kernel waits for it before reading
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, split_reduce_kernel, ws, splits, static_cast<int>(M), static_cast<int>(N), C, ldc,
+                              vec, bias, act);
 }
 
 cudaError_t zero_fill_launch(float *C, int64_t M, int64_t N, int64_t ldc, cudaStream_t stream) {

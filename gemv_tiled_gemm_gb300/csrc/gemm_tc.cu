@@ -748,6 +748,9 @@ __global__ void __launch_bounds__(256) transpose_kernel(const float *__restrict_
                                                         float *__restrict__ Bt, long long ldbt, int K, int N,
                                                         long long strideB) {
     __shared__ float tile[64][65];
+    // the GEMM that reads Bt is a dependent launch: it may be scheduled now and
+    // set itself up, and it waits for this grid before touching Bt
+    ptx::allow_next_grid();
     B += blockIdx.z * strideB;
     Bt += blockIdx.z * static_cast<long long>(N) * ldbt;
     const int n0 = blockIdx.x * 64;

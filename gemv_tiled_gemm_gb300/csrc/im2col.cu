@@ -25,6 +25,7 @@
 #include <type_traits>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace gtg {
 namespace {
@@ -44,6 +45,7 @@ constexpr int kWarpsPerCta = 8;
 // VE: elements per unit.
 template <typename V, int VE>
 __global__ void __launch_bounds__(32 * kWarpsPerCta) im2col_kernel(const Im2col g) {
+    ptx::allow_next_grid();   // the GEMM on P may be scheduled now; it waits for this grid
     const int lane = threadIdx.x & 31;
     const long long warp0 = static_cast<long long>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
     const long long nwarps = static_cast<long long>(gridDim.x) * kWarpsPerCta;
@@ -91,6 +93,7 @@ constexpr int kMaxTaps = 6144;   // 48 KB of table
 // contiguous channels of one tap (C % G == 0), read with one 16-byte load.
 template <int ESZ>
 __global__ void __launch_bounds__(32 * kWarpsPerCta) im2col_table_kernel(const Im2col g, int K) {
+    ptx::allow_next_grid();   // the GEMM on P may be scheduled now; it waits for this grid
     constexpr int G = 16 / ESZ;
     extern __shared__ Tap tab[];
     const int nchunks = (K + G - 1) / G;                 // 16-byte chunks per row (the last may run into padding)
@@ -133,6 +136,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) im2col_table_kernel(const I
 // of the row (padding) are written as zeros.
 template <int ESZ>
 __global__ void __launch_bounds__(32 * kWarpsPerCta) im2col_linear_kernel(const Im2col g, int K) {
+    ptx::allow_next_grid();   // the GEMM on P may be scheduled now; it waits for this grid
     using E = typename std::conditional<ESZ == 2, uint16_t, float>::type;
     extern __shared__ Tap tab[];
     for (int k = threadIdx.x; k < K; k += blockDim.x) {
