@@ -163,9 +163,10 @@ void gemv_plan(const DeviceInfo &dev, const GemvArgs &g, gtg_plan *plan) {
     // One CTA per SM (it fills the register file); every CTA (cluster) owns an
     // equal share of the rows.
     plan->kernel = GTG_KERNEL_GEMV;
-    plan->bm = l.kind == kStream ? 1 : (l.kind == kRound ? kRows : kSplitRows);
+    const bool two_rows = l.kind == kStream && g.a_elem == 2 && g.batch == 2;   // see pick() in gemv_kernels.cuh
+    plan->bm = l.kind == kStream ? (two_rows ? 2 : 1) : (l.kind == kRound ? kRows : kSplitRows);
     plan->bn = l.chunk;
-    plan->bk = l.kind == kSplit || l.kind == kCluster ? split_unroll(g.a_elem) : kUnroll;
+    plan->bk = l.kind == kSplit || l.kind == kCluster ? split_unroll(g.a_elem) : (two_rows ? 2 : kUnroll);
     plan->stages = l.nchunks;
     plan->grid = l.grid;
     plan->threads = l.threads;

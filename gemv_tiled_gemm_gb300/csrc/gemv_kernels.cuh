@@ -731,7 +731,16 @@ enum Kind { kStream = 0, kSplit = 1, kRound = 2, kCluster = 3 };
 template <typename T, int BATCH>
 void *pick(int kind, bool vec) {
     if constexpr (BATCH <= 2) {
-        if (kind == kStream) return reinterpret_cast<void *>(gemv_stream_kernel<T, BATCH, 1, kUnroll, kStreamThreads>);
+        if (kind == kStream) {
+            // BF16 rows at batch 2: two rows per warp, so each x value read
+            // from shared memory serves both (measured, 4096^2 / 8192^2 /
+            // 16384^2: 0.45 / 0.56 / 0.61 -> 0.54 / 0.84 / 0.88 of the copy
+            // peak); one row per warp everywhere else (two rows were slower
+            // for BF16 at batch 1 and for FP32)
+            if constexpr (sizeof(T) == 2 && BATCH == 2)
+                return reinterpret_cast<void *>(gemv_stream_kernel<T, BATCH, 2, 2, kStreamThreads>);
+            return reinterpret_cast<void *>(gemv_stream_kernel<T, BATCH, 1, kUnroll, kStreamThreads>);
+        }
     }
     if (kind == kSplit)
         return reinterpret_cast<void *>(
