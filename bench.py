@@ -41,6 +41,7 @@ GEMV_GROUP = 8
 CONV_LAYERS = [
     ("f4: bf16 conv 3x3 64->64, 56x56, batch 32, pad 1", 32, 56, 56, 64, 64, 3, 3, 1, 1, 20),
     ("f4: bf16 conv 3x3 256->256, 14x14, batch 64, pad 1", 64, 14, 14, 256, 256, 3, 3, 1, 1, 20),
+    ("f4: bf16 conv 3x3 512->512, 7x7, batch 64, pad 1", 64, 7, 7, 512, 512, 3, 3, 1, 1, 20),
     ("f4: bf16 conv 1x1 256->1024, 14x14, batch 64", 64, 14, 14, 256, 1024, 1, 1, 1, 0, 20),
     ("f4: bf16 conv 7x7/2 3->64, 224x224, batch 16, pad 3", 16, 224, 224, 3, 64, 7, 7, 2, 3, 10),
 ]

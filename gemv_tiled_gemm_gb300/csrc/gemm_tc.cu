@@ -1210,7 +1210,8 @@ void fill_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan, int spl
 // Implicit-GEMM convolution on the single-CTA kernel: Y (N*OH*OW x CO) =
 // patches(X) x Wt with the A tiles loaded by TMA in im2col mode.
 template <int BN>
-cudaError_t conv_launch_impl(const DeviceInfo &dev, const ConvArgs &c, cudaStream_t stream, int attr_bit) {
+cudaError_t conv_launch_impl(const DeviceInfo &dev, const ConvArgs &c, cudaStream_t stream, int attr_bit,
+                             int splits) {
     using S = Shape<false, BN>;
     auto kern = tc_gemm_kernel<false, BN, true>;
     {
@@ -1261,8 +1262,18 @@ cudaError_t conv_launch_impl(const DeviceInfo &dev, const ConvArgs &c, cudaStrea
     p.cv_ph = static_cast<int>(c.ph);
     p.cv_dw = static_cast<int>(c.dw);
     p.cv_dh = static_cast<int>(c.dh);
-    const int grid = static_cast<int>(std::min<int64_t>(p.num_tiles, dev.sms));
-    return launch_pdl(kern, grid, S::SMEM, stream, ta, tb, p);
+    // K split into ranges like a GEMM's: partial tiles to workspace slabs, then
+    // the ordered reduction applies the bias and activation
+    GemmArgs gg{c.prec, M, c.CO, K, nullptr, 0, nullptr, 0, c.Y, c.CO};
+    gg.bias = c.bias;
+    gg.act = c.act;
+    gtg_plan plan{};
+    plan.splits = splits;
+    float *ws = nullptr;
+    cudaError_t e = begin_split(gg, plan, p, &ws, stream);
+    const int grid = static_cast<int>(std::min<int64_t>(p.num_units, dev.sms));
+    if (e == cudaSuccess) e = launch_pdl(kern, grid, S::SMEM, stream, ta, tb, p);
+    return finish_split(gg, p, ws, e, stream);
 }
 
 }  // namespace
@@ -1319,6 +1330,7 @@ constexpr double kSliceUs = 0.30;        // one 128 x 256 x (128 bytes of K) sli
 constexpr double kFillSlices = 4.0;
 constexpr double kReduceFixedUs = 3.0;   // the reduction's launch and allocation
 constexpr double kHbmBytesPerUs = 6.0e6;
+constexpr double kConvSlice = 2.0;        // an implicit convolution's K slice against a GEMM's
 double tc_cost(const DeviceInfo &dev, const GemmArgs &g, int bm, int bn, int slots, double rel, int splits,
                int bk_elems) {
     const int64_t num_kb = (g.K + bk_elems - 1) / bk_elems;
@@ -1403,23 +1415,40 @@ bool tc_conv_eligible(const DeviceInfo &dev, const ConvArgs &c) {
 }
 
 cudaError_t tc_conv_launch(const DeviceInfo &dev, const ConvArgs &c, cudaStream_t stream) {
-    // tile width by the same estimate as the GEMM planner (single CTAs, whole K)
+    // tile width and K split by the same estimate as the GEMM planner (single
+    // CTAs), with a K slice of im2col loads costing about twice a GEMM's
+    // (measured on 3x3 layers of 64 to 512 channels: the estimate then picks
+    // the fastest of splits 1-6 and widths 64-256 on each, e.g. 512 -> 512
+    // channels at 7x7 x 64: 3 K ranges, 32.6 -> 22.1 us);
+    // gtg_force_gemm_splits applies here too
     GemmArgs g{c.prec, c.N * c.OH * c.OW, c.CO, c.KH * c.KW * c.C, nullptr, 0, nullptr, 0, nullptr, 0};
+    const int64_t num_kb = g.K / 64;
+    int forced = g_force_splits.load();
+    if (forced > 1 && num_kb < 2 * forced) forced = 0;
+    const int split_opts[6] = {1, 2, 3, 4, 6, 8};
     const int widths[3] = {256, 128, 64};
     const double rel[3] = {1.0, 0.5 / 0.8, 0.25 / 0.5};
-    int best = 0;
+    int best = 0, best_s = 1;
     double best_cost = 0;
-    for (int i = 0; i < 3; ++i) {
-        const double cost = tc_cost(dev, g, kBM, widths[i], dev.sms, rel[i], 1, 64);
-        if (i == 0 || cost < best_cost) {
-            best = i;
-            best_cost = cost;
+    bool first = true;
+    for (int si = 0; si < 6; ++si) {
+        const int sp = forced > 0 ? forced : split_opts[si];
+        if (forced > 0 && si > 0) break;
+        if (sp > 1 && num_kb < 2 * sp) continue;
+        for (int i = 0; i < 3; ++i) {
+            const double cost = tc_cost(dev, g, kBM, widths[i], dev.sms, kConvSlice * rel[i], sp, 64);
+            if (first || cost < best_cost) {
+                best = i;
+                best_s = sp;
+                best_cost = cost;
+                first = false;
+            }
         }
     }
     switch (widths[best]) {
-        case 256: return conv_launch_impl<256>(dev, c, stream, 7);
-        case 128: return conv_launch_impl<128>(dev, c, stream, 8);
-        default: return conv_launch_impl<64>(dev, c, stream, 9);
+        case 256: return conv_launch_impl<256>(dev, c, stream, 7, best_s);
+        case 128: return conv_launch_impl<128>(dev, c, stream, 8, best_s);
+        default: return conv_launch_impl<64>(dev, c, stream, 9, best_s);
     }
 }
 

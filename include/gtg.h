@@ -480,10 +480,11 @@ GTG_API gtg_status gtg_plan_gemv_bf16(int64_t M, int64_t N, const gtg_bf16 *A, i
 
 /*
  * Testing and tuning hook: with splits > 0 every tensor-core GEMM of a single
- * product that has at least 2 * splits K slices computes K in `splits`
- * ranges whose partial tiles are added in order by a second kernel (workspace
- * from the stream-ordered pool); 0 restores the planner's own choice.
- * Process-wide; results stay within the same bounds.
+ * product (and every implicit-GEMM convolution) that has at least 2 * splits
+ * K slices computes K in `splits` ranges whose partial tiles are added in
+ * order by a second kernel (workspace from the stream-ordered pool); 0
+ * restores the planner's own choice. Process-wide; results stay within the
+ * same bounds.
  */
 GTG_API void gtg_force_gemm_splits(int splits);
 

@@ -197,3 +197,31 @@ def test_implicit_gemm_refuses_what_it_cannot_take(conv_path):
     st = gtg.conv2d_nhwc("bf16", 1, 8, 8, 32, 16, 3, 3, 1, 1, 0, 0, 1, 1, X.data_ptr(), Wt.data_ptr(), Y.data_ptr(),
                          None, s)
     assert st == gtg.GTG_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("splits", [2, 3, 5])
+def test_implicit_gemm_conv_split_k(conv_path, splits):
+    # K split into ranges (forced): each range's partial tiles go to a workspace
+    # slab and the ordered reduction adds them and applies bias + ReLU; ragged
+    # output (stride 2), three 64-channel blocks x 9 taps = 27 K slices, CO = 72
+    g = PCG32(2700 + splits)
+    X, Xf = _draw("bf16", g, (2, 15, 13, 192))
+    Wt, Wf = _draw("bf16", g, (3, 3, 192, 72), (9 * 192) ** -0.5)
+    bias = g.uniform_f32((72,))
+    conv_path("implicit")
+    gtg.gtg_force_gemm_splits(splits)
+    try:
+        Y = run_conv("bf16", X, Wt, 2, 1, 1, bias, "relu")
+    finally:
+        gtg.gtg_force_gemm_splits(0)
+    check("bf16", Xf, Wf, Y, 2, 1, 1, bias, "relu")
+
+
+def test_deep_layer_takes_k_ranges_and_matches():
+    # 3 x 3, 512 -> 512 channels on 7 x 7 images: few tiles, 72 K slices; the
+    # planner splits K here (parity only: the split is the planner's choice)
+    g = PCG32(2800)
+    X, Xf = _draw("bf16", g, (4, 7, 7, 512))
+    Wt, Wf = _draw("bf16", g, (3, 3, 512, 512), (9 * 512) ** -0.5)
+    Y = run_conv("bf16", X, Wt, 1, 1, 1)
+    check("bf16", Xf, Wf, Y, 1, 1, 1)
