@@ -70,12 +70,13 @@ struct Load<__half> {
     }
 };
 
-// Each thread owns 8 rows x TN columns of the tile (TN = 8, or 4 for twice
-// the threads on the same tile when tiles are few).
-template <typename T, int BM, int BN, bool VEC, int TN = 8>
+// Each thread owns TM rows x TN columns of the tile: 8 x 8; 8 x 4 (twice the
+// threads on the same tile when tiles are few); 16 x 8 (256 x 128 tiles for
+// large products: more multiply-adds per shared-memory read).
+template <typename T, int BM, int BN, bool VEC, int TN = 8, int TM = 8>
 struct SimtTile {
     static constexpr int TX = BN / TN;             // threads along N
-    static constexpr int TY = BM / 8;              // threads along M
+    static constexpr int TY = BM / TM;             // threads along M
     static constexpr int THREADS = TX * TY;
 
     static constexpr int A_V4 = BM * kBK / 4 / THREADS;   // 4-element A groups per thread
@@ -87,13 +88,15 @@ struct SimtTile {
 // K range [z * k_per, (z + 1) * k_per) and writes its FP32 partial product to
 // the workspace slice ws + z * M * N (leading dimension N) instead of C;
 // split_reduce_kernel then adds the S slices in order z = 0 .. S-1.
-template <typename T, int BM, int BN, bool VEC, int TN>
-__global__ void __launch_bounds__(SimtTile<T, BM, BN, VEC, TN>::THREADS)
+template <typename T, int BM, int BN, bool VEC, int TN, int TM>
+__global__ void __launch_bounds__(SimtTile<T, BM, BN, VEC, TN, TM>::THREADS)
     simt_gemm_kernel(int M, int N, int K, const T *__restrict__ A, long long lda,
                      const T *__restrict__ B, long long ldb, float *__restrict__ C, long long ldc,
                      int c_vec, int k_per, float *__restrict__ ws, const float *__restrict__ bias, int act) {
-    using L = SimtTile<T, BM, BN, VEC, TN>;
+    using L = SimtTile<T, BM, BN, VEC, TN, TM>;
     constexpr int QN = TN / 2;   // column pairs per thread
+    constexpr int PM = TM / 2;   // row pairs per thread
+    constexpr int RQ = TM / 4;   // row quads per thread, BM / RQ rows apart
     // a following dependent launch (the split reduction) may be scheduled now;
     // it waits for this grid before reading anything this grid writes
     ptx::allow_next_grid();
@@ -190,9 +193,9 @@ __global__ void __launch_bounds__(SimtTile<T, BM, BN, VEC, TN>::THREADS)
     // of a packed FMA is one IEEE fused multiply-add, so every output sees the
     // same operations in the same K order as with scalar FMAs (and the same
     // result).
-    float2 d[4][QN][2];
+    float2 d[PM][QN][2];
 #pragma unroll
-    for (int p = 0; p < 4; ++p)
+    for (int p = 0; p < PM; ++p)
 #pragma unroll
         for (int q = 0; q < QN; ++q) d[p][q][0] = d[p][q][1] = make_float2(0.f, 0.f);
 
@@ -213,18 +216,21 @@ __global__ void __launch_bounds__(SimtTile<T, BM, BN, VEC, TN>::THREADS)
         }
 #pragma unroll
         for (int k = 0; k < kBK; ++k) {
-            const float4 a0 = *reinterpret_cast<const float4 *>(&As[cur][k][ty * 4]);
-            const float4 a1 = *reinterpret_cast<const float4 *>(&As[cur][k][BM / 2 + ty * 4]);
+            float2 ap[PM];
+#pragma unroll
+            for (int rq = 0; rq < RQ; ++rq) {
+                const float4 a = *reinterpret_cast<const float4 *>(&As[cur][k][rq * (BM / RQ) + ty * 4]);
+                ap[2 * rq] = make_float2(a.x, a.y);
+                ap[2 * rq + 1] = make_float2(a.z, a.w);
+            }
             const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[cur][k][tx * 4]);
             const float4 b1 = TN == 8 ? *reinterpret_cast<const float4 *>(&Bs[cur][k][BN / 2 + tx * 4]) : b0;
-            const float2 ap[4] = {make_float2(a0.x, a0.y), make_float2(a0.z, a0.w), make_float2(a1.x, a1.y),
-                                  make_float2(a1.z, a1.w)};
             const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
                                   make_float2(b1.z, b1.w)};
             const float2 bs[4] = {make_float2(b0.y, b0.x), make_float2(b0.w, b0.z), make_float2(b1.y, b1.x),
                                   make_float2(b1.w, b1.z)};
 #pragma unroll
-            for (int p = 0; p < 4; ++p)
+            for (int p = 0; p < PM; ++p)
 #pragma unroll
                 for (int q = 0; q < QN; ++q) {
                     d[p][q][0] = __ffma2_rn(ap[p], bp[q], d[p][q][0]);
@@ -238,9 +244,9 @@ __global__ void __launch_bounds__(SimtTile<T, BM, BN, VEC, TN>::THREADS)
         __syncthreads();
     }
 
-    float acc[8][TN];
+    float acc[TM][TN];
 #pragma unroll
-    for (int p = 0; p < 4; ++p)
+    for (int p = 0; p < PM; ++p)
 #pragma unroll
         for (int q = 0; q < QN; ++q) {
             acc[2 * p][2 * q] = d[p][q][0].x;
@@ -248,11 +254,11 @@ __global__ void __launch_bounds__(SimtTile<T, BM, BN, VEC, TN>::THREADS)
             acc[2 * p][2 * q + 1] = d[p][q][1].x;
             acc[2 * p + 1][2 * q] = d[p][q][1].y;
         }
-    // rows ty*4 + i (i < 4) and BM/2 + ty*4 + i; columns tx*4 + j and (TN = 8)
+    // rows (i / 4) * (BM / RQ) + ty*4 + i % 4; columns tx*4 + j and (TN = 8)
     // BN/2 + tx*4 + j.
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int row = m0 + (i < 4 ? ty * 4 + i : BM / 2 + ty * 4 + (i - 4));
+    for (int i = 0; i < TM; ++i) {
+        const int row = m0 + (i / 4) * (BM / RQ) + ty * 4 + (i % 4);
         if (row >= M) continue;
         float *crow = C + static_cast<long long>(row) * ldc;
 #pragma unroll
@@ -328,9 +334,9 @@ __global__ void zero_fill_kernel(float *C, long long M, long long N, long long l
         C[(i / N) * ldc + (i % N)] = 0.f;
 }
 
-template <typename T, int BM, int BN, bool VEC, int TN>
+template <typename T, int BM, int BN, bool VEC, int TN, int TM = 8>
 cudaError_t launch_one(const GemmArgs &g, int splits, cudaStream_t stream) {
-    using L = SimtTile<T, BM, BN, VEC, TN>;
+    using L = SimtTile<T, BM, BN, VEC, TN, TM>;
     dim3 grid(static_cast<unsigned>((g.N + BN - 1) / BN), static_cast<unsigned>((g.M + BM - 1) / BM),
               static_cast<unsigned>(splits));
     const int c_vec = ((reinterpret_cast<uintptr_t>(g.C) & 15) == 0 && (g.ldc & 3) == 0) ? 1 : 0;
@@ -341,7 +347,7 @@ cudaError_t launch_one(const GemmArgs &g, int splits, cudaStream_t stream) {
         e = ws_alloc(reinterpret_cast<void **>(&ws), static_cast<size_t>(splits) * g.M * g.N * sizeof(float), stream);
         if (e != cudaSuccess) return e;
     }
-    simt_gemm_kernel<T, BM, BN, VEC, TN><<<grid, L::THREADS, 0, stream>>>(
+    simt_gemm_kernel<T, BM, BN, VEC, TN, TM><<<grid, L::THREADS, 0, stream>>>(
         static_cast<int>(g.M), static_cast<int>(g.N), static_cast<int>(g.K),
         static_cast<const T *>(g.A), g.lda, static_cast<const T *>(g.B), g.ldb, g.C, g.ldc, c_vec, k_per, ws,
         g.bias, g.act);
@@ -356,6 +362,7 @@ cudaError_t launch_one(const GemmArgs &g, int splits, cudaStream_t stream) {
 
 template <typename T, bool VEC>
 cudaError_t launch_typed(const GemmArgs &g, const gtg_plan &plan, cudaStream_t stream) {
+    if (plan.bm == 256) return launch_one<T, 256, 128, VEC, 8, 16>(g, plan.splits, stream);
     if (plan.bm == 128) return launch_one<T, 128, 128, VEC, 8>(g, plan.splits, stream);
     return launch_one<T, 64, 64, VEC, 4>(g, plan.splits, stream);
 }
@@ -370,7 +377,8 @@ bool vec_ok(const GemmArgs &g) {
 }  // namespace
 
 // Tile: 128 x 128 (8 warps, 8 x 8 outputs per thread) when there are enough
-// such tiles for every SM. Otherwise, when K is long enough, 128 x 128 tiles
+// such tiles for every SM, or 256 x 128 (8 warps, 16 x 8 per thread) when
+// their waves come out ahead. Otherwise, when K is long enough, 128 x 128 tiles
 // split in K so that the CTAs fill at least three quarters of the SMs once
 // (one CTA of 8 warps per SM); else 64 x 64 tiles of 4 warps (8 x 4 outputs
 // per thread), whose small grids split K (plan->splits) so that about six
@@ -403,6 +411,18 @@ void simt_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
     }
     plan->bm = plan->bn = big ? 128 : 64;
     plan->threads = big ? 256 : 128;
+    if (big) {
+        // 256 x 128 tiles (16 x 8 outputs per thread) do a 128 x 128 tile's work
+        // about 8 % faster but come in half as many units: take them when their
+        // wave count says so (measured, FP32: 8192^2 x 4096 46.4 -> 50.0,
+        // 3000^3 43.9 -> 47.0, 4096 x 2048 x 4096 39.3 -> 43.5 TFLOP/s; kept at
+        // 128 x 128 for 4096^3 and 2560^2 x 2048, where they were slower)
+        const int64_t t256 = ((g.M + 255) / 256) * ((g.N + 127) / 128);
+        const int64_t t128 = ((g.M + 127) / 128) * ((g.N + 127) / 128);
+        const double w256 = static_cast<double>((t256 + dev.sms - 1) / dev.sms) * 2.0 / 1.08;
+        const double w128 = static_cast<double>((t128 + dev.sms - 1) / dev.sms);
+        if (t256 >= dev.sms && w256 < w128) plan->bm = 256;
+    }
     const int64_t tiles = ((g.M + plan->bm - 1) / plan->bm) * ((g.N + plan->bn - 1) / plan->bn);
     int64_t splits = 1;
     if (!big) {

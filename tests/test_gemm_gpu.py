@@ -172,13 +172,15 @@ def test_cta_pair_kernel_c_stores(mode, prec, M, N, K, cpad):
     (1000, 1100, 2000, 128, 256, 2),    # ragged edges, K ranges of 63 slices
     (256, 256, 256, 64, 128, None),     # small: 4-warp 64 x 64 tiles (K split by the wave model)
     (4096, 4096, 512, 128, 256, 1),     # enough big tiles for every SM
+    (3000, 3000, 3000, 256, 256, 1),    # 256 x 128 tiles (16 x 8 outputs per thread), ragged edges
+    (2999, 3012, 1001, 256, 256, 1),    # the same with scalar loads (K rows not 16-byte aligned)
 ])
 def test_simt_tile_choice_and_parity(M, N, K, bm, threads, splits):
     p = gtg_plan("f32", M, N, K)
     assert p["kernel"] == "simt" and p["bm"] == bm and p["threads"] == threads, p
     if splits is not None:
         assert p["splits"] == splits, p
-    if M * N * K <= 3e9:
+    if M * N * K <= 3e10:
         A, B = inputs("f32", M, N, K, 700 + M)
         C = run_gemm("f32", A, B, expect_kernel="simt")
         check_gemm("f32", A, B, C, rows=np.unique(np.concatenate([sample_rows(M, seed=5), np.arange(M - 70, M)])))
