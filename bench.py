@@ -46,6 +46,9 @@ CONV_LAYERS = [
     ("f4: bf16 conv 7x7/2 3->64, 224x224, batch 16, pad 3", 16, 224, 224, 3, 64, 7, 7, 2, 3, 10),
 ]
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# the part's nominal figures (dense BF16 tensor rate, HBM3e bandwidth), reported
+# beside the measured denominators
+NOMINAL = {"bf16_tflops": 2250.0, "hbm_gbs": 7900.0}
 
 
 def parse_args():
@@ -310,12 +313,14 @@ def gpu_arm(args, rank, world, local_rank):
                 "traffic": committed_traffic("gemm_bf16_8192", tc_files),
                 "peak_source": f"{peak_src} bf16 {peak_kind}",
                 "algorithmic_flops_per_launch": flops, "kernel": gemm_kernel,
-                "plan": plan}
+                "plan": plan, "peak_nominal": NOMINAL["bf16_tflops"],
+                "frac_nominal": round(gemm_tflops / world / NOMINAL["bf16_tflops"], 4)}
     gemv_roofline = {"bound": "hbm", "achieved": round(v1_gbs / world, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(v1_gbs / world / hbm_peak, 4),
                      "traffic": committed_traffic("gemv_f32_4096_b1", gv_files),
                      "peak_source": f"{peak_src} hbm copy", "algorithmic_bytes_per_launch": v1_bytes,
-                     "kernel": gemv_kernel, "plan": vplan}
+                     "kernel": gemv_kernel, "plan": vplan, "peak_nominal": NOMINAL["hbm_gbs"],
+                     "frac_nominal": round(v1_gbs / world / NOMINAL["hbm_gbs"], 4)}
 
     result = {
         "metric": METRIC, "value": round(gemm_tflops, 1), "unit": "TFLOP/s", "n_gpus": world,
