@@ -153,7 +153,7 @@ gtg_status validate_gemv(const GemvArgs &g) {
     return GTG_OK;
 }
 
-gtg_status plan_gemm_impl(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
+gtg_status plan_gemm_impl(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan, bool may_repack = true) {
     std::memset(plan, 0, sizeof(*plan));
     if (g.M == 0 || g.N == 0) {
         plan->kernel = GTG_KERNEL_NONE;
@@ -164,7 +164,8 @@ gtg_status plan_gemm_impl(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *pl
         return GTG_OK;
     }
     if (!(dev.cc_major == 10 && dev.cc_minor == 3)) return GTG_ERR_UNSUPPORTED;
-    if (g.prec != GTG_PREC_F32 && !g_force_simt.load() && tc_supported(dev) && tc_eligible(g))
+    if (g.prec != GTG_PREC_F32 && !g_force_simt.load() && tc_supported(dev) &&
+        (tc_eligible(g) || (may_repack && tc_eligible_repacked(g))))
         tc_plan(dev, g, plan);
     else
         simt_plan(dev, g, plan);
@@ -256,7 +257,8 @@ gtg_status gemm_tf32_noalloc(int64_t M, int64_t N, int64_t K, const float *A, in
     DeviceInfo dev;
     if ((st = current_device(&dev)) != GTG_OK) return st;
     gtg_plan plan;
-    if ((st = plan_gemm_impl(dev, g, &plan)) != GTG_OK) return st;
+    // no repacked operands here (they would need pool memory)
+    if ((st = plan_gemm_impl(dev, g, &plan, false)) != GTG_OK) return st;
     if (plan.kernel == GTG_KERNEL_SIMT) {
         // one K split: the SIMT kernel then writes C directly and needs no workspace
         plan.grid /= plan.splits;

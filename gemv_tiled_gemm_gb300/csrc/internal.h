@@ -72,6 +72,9 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 // ---- tcgen05 tensor-core GEMM (gemm_tc.cu)
 bool tc_supported(const DeviceInfo &dev);
 bool tc_eligible(const GemmArgs &g);
+// as tc_eligible, for a single product whose A (or 16-bit B) is first copied
+// into 16-byte rows because its base or row stride does not suit TMA
+bool tc_eligible_repacked(const GemmArgs &g);
 void tc_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan);
 cudaError_t tc_launch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan,
                       cudaStream_t stream);

@@ -200,11 +200,27 @@ def test_padded_leading_dimensions(prec, cpad):
 
 
 @pytest.mark.parametrize("prec", ["f32", "tf32", "bf16"])
-def test_unaligned_layouts_fall_back(prec):
-    M, N, K = 97, 61, 43   # odd leading dimensions: no 16-byte rows
+def test_unaligned_layouts(prec):
+    # odd leading dimensions and bases off 16 bytes: the tensor-core paths copy
+    # A (and 16-bit B) into 16-byte rows first; FP32 stays on the SIMT kernel
+    M, N, K = 97, 61, 43
     A, B = inputs(prec, M, N, K, 12)
-    C = run_gemm(prec, A, B, a_off=1, b_off=3, c_off=1, expect_kernel="simt")
+    C = run_gemm(prec, A, B, a_off=1, b_off=3, c_off=1, expect_kernel="simt" if prec == "f32" else "tcgen05")
     check_gemm(prec, A, B, C)
+
+
+@pytest.mark.parametrize("prec,M,N,K,a_off,b_off", [
+    ("bf16", 1000, 701, 1501, 0, 0),     # odd K and N: neither A's nor B's rows are 16-byte multiples
+    ("f16", 513, 264, 1500, 3, 0),       # A's base 6 bytes off, K * 2 = 3000-byte rows
+    ("bf16", 300, 1100, 256, 0, 5),      # only B repacked (N * 2 = 2200-byte rows, base off)
+    ("tf32", 700, 500, 1501, 1, 1),      # TF32: A repacked, B through its transpose as always
+    ("bf16", 4000, 3000, 2001, 0, 0),    # large enough for the CTA-pair kernel after the copy
+])
+def test_repacked_operands_on_the_tensor_cores(prec, M, N, K, a_off, b_off):
+    A, B = inputs(prec, M, N, K, 1300 + K)
+    C = run_gemm(prec, A, B, a_off=a_off, b_off=b_off, expect_kernel="tcgen05")
+    rows = np.unique(np.concatenate([sample_rows(M, seed=7), np.arange(max(0, M - 70), M)]))
+    check_gemm(prec, A, B, C, rows=rows)
 
 
 @pytest.mark.parametrize("prec", ["tf32", "bf16"])
