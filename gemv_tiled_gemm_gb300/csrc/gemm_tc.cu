@@ -816,10 +816,13 @@ cudaError_t transpose_launch(const float *B, int64_t ldb, float *Bt, int64_t ldb
 // read): gives the tensor memory accelerator the 16-byte aligned base and row
 // stride it needs when the caller's layout has neither.
 template <typename E>
-__global__ void __launch_bounds__(256) repack_rows_kernel(const E *__restrict__ src, long long lds,
+__global__ void __launch_bounds__(256) repack_rows_kernel(const E *__restrict__ src, long long lds, long long sstride,
                                                          E *__restrict__ dst, long long ldd, long long rows,
                                                          long long cols) {
     ptx::allow_next_grid();   // the GEMM reading dst waits for this grid
+    // blockIdx.y: item of a batch (sstride apart in src, rows * ldd apart in dst)
+    src += blockIdx.y * sstride;
+    dst += blockIdx.y * rows * ldd;
     const long long total = rows * cols;
     for (long long i = blockIdx.x * 256ll + threadIdx.x; i < total; i += gridDim.x * 256ll) {
         const long long r = i / cols, c = i - r * cols;
@@ -827,16 +830,17 @@ __global__ void __launch_bounds__(256) repack_rows_kernel(const E *__restrict__ 
     }
 }
 
-cudaError_t repack_launch(const void *src, int64_t lds, void *dst, int64_t ldd, int64_t rows, int64_t cols,
-                          int64_t elem, cudaStream_t stream) {
+cudaError_t repack_launch(const void *src, int64_t lds, int64_t sstride, void *dst, int64_t ldd, int64_t rows,
+                          int64_t cols, int64_t items, int64_t elem, cudaStream_t stream) {
     const long long total = rows * cols;
-    const unsigned blocks = static_cast<unsigned>(std::min<long long>((total + 255) / 256, 8192));
+    const dim3 grid(static_cast<unsigned>(std::min<long long>((total + 255) / 256, 8192)),
+                    static_cast<unsigned>(items));
     if (elem == 4)
-        repack_rows_kernel<float><<<blocks, 256, 0, stream>>>(static_cast<const float *>(src), lds,
-                                                              static_cast<float *>(dst), ldd, rows, cols);
+        repack_rows_kernel<float><<<grid, 256, 0, stream>>>(static_cast<const float *>(src), lds, sstride,
+                                                            static_cast<float *>(dst), ldd, rows, cols);
     else
-        repack_rows_kernel<uint16_t><<<blocks, 256, 0, stream>>>(static_cast<const uint16_t *>(src), lds,
-                                                                 static_cast<uint16_t *>(dst), ldd, rows, cols);
+        repack_rows_kernel<uint16_t><<<grid, 256, 0, stream>>>(static_cast<const uint16_t *>(src), lds, sstride,
+                                                               static_cast<uint16_t *>(dst), ldd, rows, cols);
     return cudaGetLastError();
 }
 
@@ -1502,14 +1506,16 @@ cudaError_t tc_launch_aligned(const DeviceInfo &dev, const GemmArgs &g, const gt
     }
 }
 
-bool tma_operand_ok(const void *p, int64_t ld, int64_t elem) {
-    return (reinterpret_cast<uintptr_t>(p) & 15) == 0 && (ld * elem) % 16 == 0;
+// Base, row stride and (for batch items) item stride all on 16 bytes.
+bool tma_operand_ok(const void *p, int64_t ld, int64_t stride, int64_t batch, int64_t elem) {
+    return (reinterpret_cast<uintptr_t>(p) & 15) == 0 && (ld * elem) % 16 == 0 &&
+           (batch == 1 || (stride * elem) % 16 == 0);
 }
 }  // namespace
 
 bool tc_eligible_repacked(const GemmArgs &g) {
     if (g.prec != GTG_PREC_TF32 && g.prec != GTG_PREC_BF16 && g.prec != GTG_PREC_F16) return false;
-    if (g.batch != 1) return false;
+    if (g.batch > 65535 || g.batch * ((g.M + 127) / 128) * ((g.N + 63) / 64) > INT32_MAX) return false;
     if (g.M > INT32_MAX || g.N > INT32_MAX || g.K > INT32_MAX) return false;
     const int64_t elem = g.prec == GTG_PREC_TF32 ? 4 : 2;
     const int64_t ka = (g.K + 16 / elem - 1) / (16 / elem) * (16 / elem), nb = (g.N + 7) / 8 * 8;
@@ -1517,33 +1523,37 @@ bool tc_eligible_repacked(const GemmArgs &g) {
     return g.M > 0 && g.N > 0 && g.K > 0;
 }
 
-// Operands whose base or row stride the tensor memory accelerator cannot take
-// (a single product) are first copied into 16-byte rows from the pool: A for
-// every precision, B for 16-bit inputs (TF32 B goes through its transpose in
-// any case).
+// Operands whose base, row stride or item stride the tensor memory
+// accelerator cannot take are first copied into 16-byte rows (and items of
+// whole rows) from the pool: A for every precision, B for 16-bit inputs (TF32
+// B goes through its transpose in any case). A shared operand (item stride 0)
+// is copied once.
 cudaError_t tc_launch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan, cudaStream_t stream) {
     const bool tf32 = g.prec == GTG_PREC_TF32;
     const int64_t elem = tf32 ? 4 : 2;
-    const bool a_bad = !tma_operand_ok(g.A, g.lda, elem);
-    const bool b_bad = !tf32 && !tma_operand_ok(g.B, g.ldb, elem);
+    const bool a_bad = !tma_operand_ok(g.A, g.lda, g.strideA, g.batch, elem);
+    const bool b_bad = !tf32 && !tma_operand_ok(g.B, g.ldb, g.strideB, g.batch, elem);
     if (!a_bad && !b_bad) return tc_launch_aligned(dev, g, plan, stream);
-    if (g.batch != 1) return cudaErrorInvalidValue;   // batches are planned onto the SIMT kernel instead
     GemmArgs g2 = g;
     void *pa = nullptr, *pb = nullptr;
     cudaError_t e = cudaSuccess;
     if (a_bad) {
         const int64_t ld = (g.K + 16 / elem - 1) / (16 / elem) * (16 / elem);
-        e = ws_alloc(&pa, static_cast<size_t>(g.M * ld * elem), stream);
-        if (e == cudaSuccess) e = repack_launch(g.A, g.lda, pa, ld, g.M, g.K, elem, stream);
+        const int64_t items = g.batch > 1 && g.strideA != 0 ? g.batch : 1;
+        e = ws_alloc(&pa, static_cast<size_t>(items * g.M * ld * elem), stream);
+        if (e == cudaSuccess) e = repack_launch(g.A, g.lda, g.strideA, pa, ld, g.M, g.K, items, elem, stream);
         g2.A = pa;
         g2.lda = ld;
+        g2.strideA = items > 1 ? g.M * ld : 0;
     }
     if (e == cudaSuccess && b_bad) {
         const int64_t ld = (g.N + 7) / 8 * 8;
-        e = ws_alloc(&pb, static_cast<size_t>(g.K * ld * 2), stream);
-        if (e == cudaSuccess) e = repack_launch(g.B, g.ldb, pb, ld, g.K, g.N, 2, stream);
+        const int64_t items = g.batch > 1 && g.strideB != 0 ? g.batch : 1;
+        e = ws_alloc(&pb, static_cast<size_t>(items * g.K * ld * 2), stream);
+        if (e == cudaSuccess) e = repack_launch(g.B, g.ldb, g.strideB, pb, ld, g.K, g.N, items, 2, stream);
         g2.B = pb;
         g2.ldb = ld;
+        g2.strideB = items > 1 ? g.K * ld : 0;
     }
     if (e == cudaSuccess) e = tc_launch_aligned(dev, g2, plan, stream);
     // stream-ordered: released once the GEMM has read them

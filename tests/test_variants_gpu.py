@@ -150,6 +150,42 @@ def test_strided_batched_c_stores(mode):
         assert np.all(np.isnan(C[b * sC + M * N: (b + 1) * sC]))
 
 
+@pytest.mark.parametrize("prec", ["bf16", "f16", "tf32"])
+@pytest.mark.parametrize("case", ["odd_strides", "odd_ld_shared_B", "odd_ld_shared_A"])
+def test_strided_batched_repacked(prec, case):
+    # item strides or leading dimensions off 16 bytes: the items are copied into
+    # aligned rows (a shared operand once) and the batch runs as one
+    # tensor-core launch; checked per item against the oracle
+    torch = _t()
+    g = PCG32(970 + len(case))
+    batch, M, N, K = 3, 300, 264, 136
+    lda, ldb, ldc = K, N, N
+    sA, sB, sC = M * lda + 1, K * ldb + 3, M * ldc
+    if case == "odd_ld_shared_B":
+        lda, ldb = K + 1, N + 3
+        sA, sB = M * lda, 0
+    if case == "odd_ld_shared_A":
+        lda, ldb = K + 3, N + 1
+        sA, sB = 0, K * ldb
+    A_host, A_f = _draw(prec, g, (max(1, batch * sA) + M * lda + 8,))
+    B_host, B_f = _draw(prec, g, (max(1, batch * sB) + K * ldb + 8,))
+    dA, dB = _dev(prec, A_host), _dev(prec, B_host)
+    dC = torch.full((batch * sC + 8,), float("nan"), device="cuda")
+    s = int(torch.cuda.current_stream().cuda_stream)
+    st = gtg.gemm_strided_batched(prec, M, N, K, dA.data_ptr(), lda, sA, dB.data_ptr(), ldb, sB,
+                                  dC.data_ptr(), ldc, sC, batch, None, s)
+    assert st == gtg.GTG_OK, gtg.status_string(st)
+    assert gtg.gtg_sync_status(s) == gtg.GTG_OK
+    C = dC.cpu().numpy()
+    for b in range(batch):
+        Ab = A_f[b * sA: b * sA + M * lda].reshape(M, lda)[:, :K]
+        Bb = B_f[b * sB: b * sB + K * ldb].reshape(K, ldb)[:, :N]
+        ref, E = oracle.gemm(Ab, Bb)
+        got = C[b * sC: b * sC + M * ldc].reshape(M, ldc)[:, :N]
+        ratio, bad = parity_ratio(got, ref, E, prec, K)
+        assert bad == 0, (b, ratio)
+
+
 def test_strided_batched_plans_one_launch_for_all_items():
     torch = _t()
     batch, M, N, K = 40, 512, 512, 64
