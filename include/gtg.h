@@ -118,9 +118,10 @@ GTG_API gtg_status gemm_f32(int64_t M, int64_t N, int64_t K,
  * `stream`) and is returned to it (cudaFreeAsync on `stream`) after the
  * multiply, so it never blocks the host; if the pool cannot supply it the
  * call returns GTG_ERR_LAUNCH and launches nothing.
- * The tensor-core kernel needs a 16-byte aligned A with lda a multiple of 4
- * (the TMA rules); other layouts are computed by the exact FP32 kernel of
- * gemm_f32, whose result also meets the TF32 accuracy.
+ * The tensor-core kernel reads A through TMA, which needs a 16-byte aligned
+ * base and lda a multiple of 4; for other layouts A is first copied into
+ * such rows in a second temporary from the same pool (4 * M * roundup(K, 4)
+ * bytes, released the same way).
  */
 GTG_API gtg_status gemm_tf32(int64_t M, int64_t N, int64_t K,
                      const float *A, int64_t lda,
@@ -136,9 +137,11 @@ GTG_API gtg_status gemm_tf32(int64_t M, int64_t N, int64_t K,
  *   A  M x K bf16, lda >= max(K, 1);  B  K x N bf16, ldb >= max(N, 1)
  *   C  M x N FP32, ldc >= max(N, 1), overwritten
  * Pointers must be 2-byte (A, B) and 4-byte (C) aligned. The tensor-core
- * kernel needs 16-byte aligned A and B and lda, ldb multiples of 8 (the TMA
- * rules); other layouts are computed by the SIMT kernel in FP32 (exact
- * products, FP32 accumulation), which meets the same accuracy.
+ * kernels read A and B through TMA, which needs 16-byte aligned bases and
+ * lda, ldb multiples of 8; an operand in another layout is first copied into
+ * such rows in a temporary from the library's stream-ordered pool (released
+ * on `stream` after the multiply; GTG_ERR_LAUNCH if the pool cannot supply
+ * it).
  */
 GTG_API gtg_status gemm_bf16(int64_t M, int64_t N, int64_t K,
                      const gtg_bf16 *A, int64_t lda,
@@ -381,10 +384,12 @@ GTG_API gtg_status gtg_pool_trim(void);
  *   epilogue   as for gemm_*_ex (the same bias for every item), or NULL
  *
  * The tensor-core kernels walk the output tiles of all items in one launch
- * (their tensor maps get the batch as a third dimension, so strideA and,
- * for 16-bit inputs, strideB must be multiples of 16 bytes); other layouts
- * run item by item on the SIMT kernel. Errors as for the single calls; no
- * item is computed if the arguments of any item are invalid.
+ * (their tensor maps get the batch as a third dimension). When strideA or,
+ * for 16-bit inputs, strideB or a leading dimension is not a multiple of 16
+ * bytes, the items of that operand (one copy if its stride is 0) are first
+ * copied into aligned rows in a temporary from the pool; FP32 batches run
+ * item by item on the SIMT kernel. Errors as for the single calls; no item
+ * is computed if the arguments of any item are invalid.
  */
 GTG_API gtg_status gemm_strided_batched(int precision, int64_t M, int64_t N, int64_t K,
                                         const void *A, int64_t lda, int64_t strideA,
