@@ -209,6 +209,15 @@ def test_unaligned_layouts(prec):
     check_gemm(prec, A, B, C)
 
 
+@pytest.mark.parametrize("prec", ["bf16", "tf32"])
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (5, 3, 1), (130, 9, 17), (2, 257, 3), (129, 1, 1001)])
+def test_repacked_tiny_operands(prec, M, N, K):
+    # degenerate sizes whose rows are shorter than 16 bytes: the copies pad
+    # them to whole 16-byte rows and TMA fills the rest of each box with zeros
+    A, B = inputs(prec, M, N, K, 1400 + M + N + K)
+    check_gemm(prec, A, B, run_gemm(prec, A, B, expect_kernel="tcgen05"))
+
+
 @pytest.mark.parametrize("prec,M,N,K,a_off,b_off", [
     ("bf16", 1000, 701, 1501, 0, 0),     # odd K and N: neither A's nor B's rows are 16-byte multiples
     ("f16", 513, 264, 1500, 3, 0),       # A's base 6 bytes off, K * 2 = 3000-byte rows
