@@ -823,16 +823,28 @@ __global__ void __launch_bounds__(256) repack_rows_kernel(const E *__restrict__ 
     // blockIdx.y: item of a batch (sstride apart in src, rows * ldd apart in dst)
     src += blockIdx.y * sstride;
     dst += blockIdx.y * rows * ldd;
-    const long long total = rows * cols;
+    // a thread gathers one 16-byte group of a destination row (ldd is a
+    // multiple of the group, so every group store is aligned) with element
+    // loads, which any source alignment allows; past `cols` it writes zeros
+    constexpr int V = 16 / sizeof(E);
+    const long long groups = (cols + V - 1) / V;
+    const long long total = rows * groups;
     for (long long i = blockIdx.x * 256ll + threadIdx.x; i < total; i += gridDim.x * 256ll) {
-        const long long r = i / cols, c = i - r * cols;
-        dst[r * ldd + c] = src[r * lds + c];
+        const long long r = i / groups, c0 = (i - r * groups) * V;
+        union {
+            uint4 v;
+            E e[V];
+        } u;
+        const E *s = src + r * lds + c0;
+#pragma unroll
+        for (int j = 0; j < V; ++j) u.e[j] = c0 + j < cols ? s[j] : E(0);
+        *reinterpret_cast<uint4 *>(dst + r * ldd + c0) = u.v;
     }
 }
 
 cudaError_t repack_launch(const void *src, int64_t lds, int64_t sstride, void *dst, int64_t ldd, int64_t rows,
                           int64_t cols, int64_t items, int64_t elem, cudaStream_t stream) {
-    const long long total = rows * cols;
+    const long long total = rows * ((cols + 16 / elem - 1) / (16 / elem));
     const dim3 grid(static_cast<unsigned>(std::min<long long>((total + 255) / 256, 8192)),
                     static_cast<unsigned>(items));
     if (elem == 4)
