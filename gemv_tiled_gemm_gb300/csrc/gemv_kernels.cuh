@@ -433,7 +433,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const Params p
     const int ntasks = (r_end - r_begin + ROWS - 1) / ROWS;
     const int my_tasks = ntasks > warp ? (ntasks - warp + kWarps - 1) / kWarps : 0;
     const int nu = p.N / VE;                          // whole 16-byte units per row
-    const int ipr = (nu + 32 * U - 1) / (32 * U);     // iterations per task
+    // iterations per task; at least one, whose trailing-entry step covers a
+    // row shorter than one unit (N < VE with padded, aligned rows)
+    const int ipr = max(1, (nu + 32 * U - 1) / (32 * U));
     const int total = my_tasks * ipr;
 
     if (threadIdx.x < 32) {

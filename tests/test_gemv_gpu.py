@@ -85,6 +85,26 @@ def test_vectors_that_do_not_fit_shared_memory():
     check(A, x, run_gemv(A, x))
 
 
+@pytest.mark.parametrize("M,N,lda,batch", [(37, 3, 4, 1), (37, 3, 4, 2), (300, 1, 4, 1), (5, 2, 8, 2), (200, 7, 8, 1)])
+def test_rows_shorter_than_one_16_byte_unit(M, N, lda, batch):
+    # aligned, padded rows with fewer than four FP32 entries: the streaming
+    # kernel's only work per row is its trailing-entry step
+    g = PCG32(35 + N + lda)
+    A = g.uniform_f32((M, N))
+    X = g.uniform_f32((batch, N))
+    check(A, X, run_gemv(A, X, lda=lda))
+
+
+@pytest.mark.parametrize("M,N,lda,batch", [(37, 7, 8, 1), (100, 5, 16, 2), (64, 1, 8, 1)])
+def test_bf16_rows_shorter_than_one_16_byte_unit(M, N, lda, batch):
+    from seeded import bf16_bits_to_f32
+    g = PCG32(36 + N + lda)
+    A = g.normal_bf16((M, N))
+    X = g.uniform_f32((batch, N))
+    Y = run_gemv(A, X, lda=lda, prec="bf16")
+    check(bf16_bits_to_f32(A), X, Y)
+
+
 def test_scalar_path_for_unaligned_rows():
     g = PCG32(32)
     A = g.uniform_f32((257, 1001))
