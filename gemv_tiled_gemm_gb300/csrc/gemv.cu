@@ -105,7 +105,15 @@ Layout layout(const DeviceInfo &dev, const GemvArgs &g) {
     l.grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(dev.sms, g.M)));
     l.cluster = 1;
     l.ublock = 0;
-    if (!gemv_vec(g)) return l;
+    if (!gemv_vec(g)) {
+        // FP32 rows off 16 bytes at batch 1-2 with x in one chunk: the
+        // streaming kernel that peels each row's head to reach aligned loads
+        if (g.a_elem == 4 && g.batch <= 2 && l.nchunks == 1) {
+            l.kind = kPeel;
+            l.threads = kPeelThreads;
+        }
+        return l;
+    }
     if (l.nchunks == 1) {
         if (g.batch <= 2) {
             l.kind = kStream;
@@ -164,7 +172,7 @@ void gemv_plan(const DeviceInfo &dev, const GemvArgs &g, gtg_plan *plan) {
     // equal share of the rows.
     plan->kernel = GTG_KERNEL_GEMV;
     const bool two_rows = l.kind == kStream && g.a_elem == 2 && g.batch == 2;   // see pick() in gemv_kernels.cuh
-    plan->bm = l.kind == kStream ? (two_rows ? 2 : 1) : (l.kind == kRound ? kRows : kSplitRows);
+    plan->bm = l.kind == kStream ? (two_rows ? 2 : 1) : (l.kind == kPeel ? 1 : (l.kind == kRound ? kRows : kSplitRows));
     plan->bn = l.chunk;
     plan->bk = l.kind == kSplit || l.kind == kCluster ? split_unroll(g.a_elem) : (two_rows ? 2 : kUnroll);
     plan->stages = l.nchunks;
@@ -198,7 +206,7 @@ cudaError_t gemv_launch(const DeviceInfo &dev, const GemvArgs &g, const gtg_plan
     p.act = g.act;
     p.ublock = l.ublock;
     // bulk copies of x need 16-byte aligned rows of a multiple of 16 bytes
-    p.x_bulk = l.kind != kRound && (reinterpret_cast<uintptr_t>(g.x) & 15) == 0 && g.N % 4 == 0 &&
+    p.x_bulk = l.kind != kRound && l.kind != kPeel && (reinterpret_cast<uintptr_t>(g.x) & 15) == 0 && g.N % 4 == 0 &&
                (g.batch == 1 || g.ldx % 4 == 0);
     p.status = dev.status;
     p.wait_limit_ns = wait_limit_setting();

@@ -714,6 +714,98 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
     ptx::cluster_sync();   // no CTA leaves while another may still read its shared memory
 }
 
+// FP32 rows that are not 16-byte aligned (lda not a multiple of 4, or A off
+// 16 bytes), batch 1-2, all of x in one chunk: one row per warp, each row's
+// first h = 0..3 entries (up to its first 16-byte boundary) taken by single
+// loads and the rest by aligned 16-byte loads (four per lane in flight, the
+// next four issued before the current ones are used). x is staged at its own
+// offsets, so a 16-byte unit of the row meets x at column h + 4j and x is
+// read one value at a time when h != 0. nu counts the whole units that every
+// row has after its head; the entries past them are single loads too.
+constexpr int kPeelThreads = 1024;
+
+template <int BATCH>
+__global__ void __launch_bounds__(kPeelThreads, 1) gemv_stream_peel_kernel(const Params p) {
+    constexpr int U = 4, kWarps = kPeelThreads / 32;
+    extern __shared__ float4 xs_raw[];
+    float *xs = reinterpret_cast<float *>(xs_raw);
+    const float *A = static_cast<const float *>(p.A);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r_begin = static_cast<int>(static_cast<long long>(p.M) * blockIdx.x / gridDim.x);
+    const int r_end = static_cast<int>(static_cast<long long>(p.M) * (blockIdx.x + 1) / gridDim.x);
+    const int nu = p.N >= 3 ? (p.N - 3) / 4 : 0;
+    ptx::wait_prior_grid();
+    ptx::allow_next_grid();
+    stage_x<BATCH, kPeelThreads>(xs, p, 0, p.N);
+    __syncthreads();
+
+    for (int row = r_begin + warp; row < r_end; row += kWarps) {
+        const float *a = A + static_cast<long long>(row) * p.lda;
+        const int h = static_cast<int>(((16u - (reinterpret_cast<uintptr_t>(a) & 15u)) & 15u) >> 2);
+        const float *av = a + h;   // 16-byte aligned
+        float acc[BATCH];
+#pragma unroll
+        for (int b = 0; b < BATCH; ++b) acc[b] = 0.f;
+        auto load = [&](int jb, float4 (&dst)[U]) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = jb + 32 * u + lane;
+                dst[u] = j < nu ? ptx::ld_stream_f4(av + 4 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        };
+        float4 nxt[U];
+        load(0, nxt);
+        for (int jb = 0; jb < nu; jb += 32 * U) {
+            float4 cur[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) cur[u] = nxt[u];
+            if (jb + 32 * U < nu) load(jb + 32 * U, nxt);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = jb + 32 * u + lane;
+                if (j < nu) {
+                    const int col = h + 4 * j;
+#pragma unroll
+                    for (int b = 0; b < BATCH; ++b) {
+                        const float *xp = xs + b * p.chunk + col;
+                        float x0, x1, x2, x3;
+                        if (h == 0) {
+                            const float4 xv = *reinterpret_cast<const float4 *>(xp);
+                            x0 = xv.x, x1 = xv.y, x2 = xv.z, x3 = xv.w;
+                        } else {
+                            x0 = xp[0], x1 = xp[1], x2 = xp[2], x3 = xp[3];
+                        }
+                        float t = acc[b];
+                        t = fmaf(cur[u].x, x0, t);
+                        t = fmaf(cur[u].y, x1, t);
+                        t = fmaf(cur[u].z, x2, t);
+                        t = fmaf(cur[u].w, x3, t);
+                        acc[b] = t;
+                    }
+                }
+            }
+        }
+        // the head [0, h) and the entries past the whole units
+        if (lane < h && lane < p.N) {
+            const float v = ptx::ld_stream_f1(a + lane);
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) acc[b] = fmaf(v, xs[b * p.chunk + lane], acc[b]);
+        }
+        for (int jt = h + 4 * nu + lane; jt < p.N; jt += 32) {
+            const float v = ptx::ld_stream_f1(a + jt);
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) acc[b] = fmaf(v, xs[b * p.chunk + jt], acc[b]);
+        }
+#pragma unroll
+        for (int b = 0; b < BATCH; ++b) {
+            float v = acc[b];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+            if (lane == 0) p.y[static_cast<long long>(b) * p.ldy + row] = apply_epilogue(v, p.bias, row, p.act);
+        }
+    }
+}
+
 // Kernel choice, for aligned rows: batch <= 2 with x in one staging chunk ->
 // gemv_stream_kernel (32 warps, one row each); batch >= 3 with x in one CTA ->
 // gemv_blocks_kernel without a cluster (16 warps, 4 rows x half the columns
@@ -728,10 +820,13 @@ constexpr int kSplitRows = 4, kSplitSegs = 2;
 // 16 bytes (FP32) or four of 8 bytes (BF16), the same bytes either way
 constexpr int split_unroll(int elem_bytes) { return elem_bytes == 2 ? 4 : 2; }
 
-enum Kind { kStream = 0, kSplit = 1, kRound = 2, kCluster = 3 };
+enum Kind { kStream = 0, kSplit = 1, kRound = 2, kCluster = 3, kPeel = 4 };
 
 template <typename T, int BATCH>
 void *pick(int kind, bool vec) {
+    if constexpr (BATCH <= 2 && sizeof(T) == 4) {
+        if (kind == kPeel) return reinterpret_cast<void *>(gemv_stream_peel_kernel<BATCH>);
+    }
     if constexpr (BATCH <= 2) {
         if (kind == kStream) {
             // BF16 rows at batch 2: two rows per warp, so each x value read

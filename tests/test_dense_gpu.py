@@ -75,6 +75,7 @@ GEMV_CASES = [
     (1523, 1030, 4, 2),      # column-split kernel, ragged width, padded rows
     (300, 7000, 8, 0),       # chunked x: round kernel
     (257, 1001, 3, 1),       # unaligned rows: scalar round kernel
+    (257, 1001, 1, 1),       # unaligned rows at batch 1: peeled streaming kernel
 ]
 
 

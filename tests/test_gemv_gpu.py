@@ -105,6 +105,19 @@ def test_bf16_rows_shorter_than_one_16_byte_unit(M, N, lda, batch):
     check(bf16_bits_to_f32(A), X, Y)
 
 
+@pytest.mark.parametrize("batch", [1, 2])
+@pytest.mark.parametrize("M,N,lda,a_off", [(1000, 4095, 4095, 0), (333, 1001, 1003, 1), (301, 517, 517, 2),
+                                           (64, 3, 3, 1), (77, 5, 7, 3), (40, 2, 2, 0), (2000, 8190, 8190, 0)])
+def test_unaligned_rows_at_batch_1_and_2(batch, M, N, lda, a_off):
+    # FP32 rows off 16 bytes: each row's first entries up to its 16-byte
+    # boundary are single loads, the rest aligned 16-byte loads (rows shorter
+    # than a unit are all head and tail)
+    g = PCG32(37 + N + lda + a_off)
+    A = g.uniform_f32((M, N))
+    X = g.uniform_f32((batch, N))
+    check(A, X, run_gemv(A, X, lda=lda, a_off=a_off))
+
+
 def test_scalar_path_for_unaligned_rows():
     g = PCG32(32)
     A = g.uniform_f32((257, 1001))
