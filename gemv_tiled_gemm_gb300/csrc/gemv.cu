@@ -106,11 +106,23 @@ Layout layout(const DeviceInfo &dev, const GemvArgs &g) {
     l.cluster = 1;
     l.ublock = 0;
     if (!gemv_vec(g)) {
-        // FP32 rows off 16 bytes at batch 1-2 with x in one chunk: the
-        // streaming kernel that peels each row's head to reach aligned loads
-        if (g.a_elem == 4 && g.batch <= 2 && l.nchunks == 1) {
-            l.kind = kPeel;
-            l.threads = kPeelThreads;
+        // FP32 rows off 16 bytes with x in one chunk: kernels that peel each
+        // row's head to reach aligned loads (batch 1-2: streaming, one row per
+        // warp; batch 3-8: row blocks of rows four apart, if their partial
+        // sums fit beside x)
+        if (g.a_elem == 4 && l.nchunks == 1) {
+            if (g.batch <= 2) {
+                l.kind = kPeel;
+                l.threads = kPeelThreads;
+                return l;
+            }
+            const int64_t rows_cta = (g.M + dev.sms - 1) / dev.sms;
+            const int64_t groups = (rows_cta + 4 * kSplitRows - 1) / (4 * kSplitRows) * 4;
+            const int64_t part = groups * kSplitSegs * kSplitRows * g.batch * 4;
+            if (l.smem + part <= limit) {
+                l.kind = kPeelSplit;
+                l.smem = static_cast<int>(l.smem + part);
+            }
         }
         return l;
     }
@@ -174,7 +186,8 @@ void gemv_plan(const DeviceInfo &dev, const GemvArgs &g, gtg_plan *plan) {
     const bool two_rows = l.kind == kStream && g.a_elem == 2 && g.batch == 2;   // see pick() in gemv_kernels.cuh
     plan->bm = l.kind == kStream ? (two_rows ? 2 : 1) : (l.kind == kPeel ? 1 : (l.kind == kRound ? kRows : kSplitRows));
     plan->bn = l.chunk;
-    plan->bk = l.kind == kSplit || l.kind == kCluster ? split_unroll(g.a_elem) : (two_rows ? 2 : kUnroll);
+    plan->bk = l.kind == kSplit || l.kind == kCluster || l.kind == kPeelSplit ? split_unroll(g.a_elem)
+                                                                               : (two_rows ? 2 : kUnroll);
     plan->stages = l.nchunks;
     plan->grid = l.grid;
     plan->threads = l.threads;
@@ -206,7 +219,9 @@ cudaError_t gemv_launch(const DeviceInfo &dev, const GemvArgs &g, const gtg_plan
     p.act = g.act;
     p.ublock = l.ublock;
     // bulk copies of x need 16-byte aligned rows of a multiple of 16 bytes
-    p.x_bulk = l.kind != kRound && l.kind != kPeel && (reinterpret_cast<uintptr_t>(g.x) & 15) == 0 && g.N % 4 == 0 &&
+    // (the peeled kernels stage x themselves: at its own offsets, or quad-transposed)
+    p.x_bulk = (l.kind == kStream || l.kind == kSplit || l.kind == kCluster) &&
+               (reinterpret_cast<uintptr_t>(g.x) & 15) == 0 && g.N % 4 == 0 &&
                (g.batch == 1 || g.ldx % 4 == 0);
     p.status = dev.status;
     p.wait_limit_ns = wait_limit_setting();

@@ -239,6 +239,34 @@ __device__ __forceinline__ void fma_quad(float (&acc)[ROWS][BATCH], const typena
     }
 }
 
+// acc[r][b] += the four FP32 elements of row r at column h + 4j times vector
+// b, staged quad-transposed (entry c at (c % 4) * q + c / 4): lane j reads
+// word j (+1 past the wrap) of each of four quarter rows, so the 32 lanes
+// read consecutive words (gemv_blocks_kernel with PEEL).
+template <int ROWS, int BATCH>
+__device__ __forceinline__ void fma_quad_peeled(float (&acc)[ROWS][BATCH], const float4 (&raw)[ROWS],
+                                                const float *xs, int chunk, int q, int h, int j) {
+    float a[ROWS][4];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) Quad<float>::widen(raw[r], a[r]);
+    const float *xe[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) xe[e] = xs + ((h + e) & 3) * q + ((h + e) >> 2) + j;
+#pragma unroll
+    for (int b = 0; b < BATCH; ++b) {
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = xe[e][b * chunk];
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            float s = acc[r][b];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s = fmaf(a[r][e], v[e], s);
+            acc[r][b] = s;
+        }
+    }
+}
+
 // Reduce-scatter over the 32 lanes of a warp for P values per lane (P a power
 // of two, at most 32). Lane offsets go 16, 8, 4, 2, 1: while a lane holds more
 // than one value, each level sends half of them to the partner lane and keeps
@@ -543,8 +571,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const Params p
 // partials, read through distributed shared memory, in rank order, and a
 // second cluster barrier keeps every CTA's shared memory alive until the
 // others have read it. p.chunk >= (block width + 1) * VE.
-template <typename T, int BATCH, int ROWS, int WC, int U, int kThreads, bool CLUSTER>
+//
+// PEEL (FP32, C = 1): rows that do not start on 16 bytes. Rows kPhase = 4
+// apart start 16 * lda bytes apart, so they share their offset from a 16-byte
+// boundary: a task takes ROWS rows kPhase apart (rows b + i + kPhase * r of a
+// block of kPhase * ROWS rows, i = 0..kPhase-1), skips their first h = 0..3
+// entries (single loads) to reach aligned 16-byte loads, and meets x at
+// column h + 4j. x is staged quad-transposed (entry c at (c % 4) * xq + c / 4,
+// xq = p.chunk / 4), so the lanes' reads of one of the four columns of a unit
+// are consecutive words whatever h is. nu counts the whole units every row has
+// after its head; the at most six entries past them are single loads too.
+template <typename T, int BATCH, int ROWS, int WC, int U, int kThreads, bool CLUSTER, bool PEEL = false>
 __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p) {
+    static_assert(!PEEL || (!CLUSTER && sizeof(T) == 4), "peeled rows: FP32, one CTA per row block");
+    constexpr int kPhase = 4;
     constexpr int kWarps = kThreads / 32;
     using Q = Quad<T>;
     using Raw = typename Q::Raw;
@@ -557,14 +597,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
     const int r_begin = static_cast<int>(static_cast<long long>(p.M) * cid / ncl);
     const int r_end = static_cast<int>(static_cast<long long>(p.M) * (cid + 1) / ncl);
     const int rows = r_end - r_begin;
-    const int ngroups = (rows + ROWS - 1) / ROWS;
+    const int ngroups = PEEL ? (rows + kPhase * ROWS - 1) / (kPhase * ROWS) * kPhase : (rows + ROWS - 1) / ROWS;
     const int ntasks = ngroups * WC;
-    const int nu = p.N / VE;
+    const int nu = PEEL ? (p.N >= 3 ? (p.N - 3) / VE : 0) : p.N / VE;
     const int ub0 = min(c * p.ublock, nu);                       // this CTA's units [ub0, ub1)
     const int ub1 = c == C - 1 ? nu : min(ub0 + p.ublock, nu);
     const int nub = ub1 - ub0;
-    const int tail = c == C - 1 ? p.N - VE * nu : 0;             // trailing entries (last block)
-    const int xlen = VE * nub + tail;                            // staged entries per vector
+    const int tail = PEEL ? 0 : (c == C - 1 ? p.N - VE * nu : 0);   // trailing entries (last block)
+    const int xlen = PEEL ? p.N : VE * nub + tail;               // staged entries per vector
+    const int xq = p.chunk / 4;                                  // PEEL: quads per staged vector
     const int segu = ((nub + WC - 1) / WC + 31) / 32 * 32;
     float *xs = reinterpret_cast<float *>(xs_raw);               // [BATCH][chunk]
     float *part = xs + BATCH * p.chunk;                          // [group][segment][row][batch]
@@ -587,12 +628,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
         // a bulk prefetch takes a 16-byte aligned start and length, so it
         // covers the 16-byte blocks inside [start, end) of the part (rows
         // start on 16 bytes, a BF16 column block may start 8 bytes past one)
-        const long long skew = static_cast<long long>(VE) * ub0 * static_cast<long long>(sizeof(T)) & 15;
-        const long long lead = skew ? 16 - skew : 0;
-        const long long span = static_cast<long long>(VE) * nub * static_cast<long long>(sizeof(T)) - lead;
-        const uint32_t bytes = span >= 16 ? static_cast<uint32_t>(min(kPrefetch, span / 16 * 16)) : 0u;
-        for (int r = r_begin + static_cast<int>(threadIdx.x); bytes > 0 && r < r_end; r += 32)
-            ptx::prefetch_l2(reinterpret_cast<const char *>(A + static_cast<long long>(r) * p.lda) + lead, bytes);
+        if constexpr (PEEL) {
+            // each row from its first 16-byte boundary
+            const long long row_bytes = 4ll * p.N;
+            for (int r = r_begin + static_cast<int>(threadIdx.x); r < r_end; r += 32) {
+                const char *rp = reinterpret_cast<const char *>(A + static_cast<long long>(r) * p.lda);
+                const long long lead = static_cast<long long>((16u - (reinterpret_cast<uintptr_t>(rp) & 15u)) & 15u);
+                const long long span = row_bytes - lead;
+                if (span >= 16) ptx::prefetch_l2(rp + lead, static_cast<uint32_t>(min(kPrefetch, span / 16 * 16)));
+            }
+        } else {
+            const long long skew = static_cast<long long>(VE) * ub0 * static_cast<long long>(sizeof(T)) & 15;
+            const long long lead = skew ? 16 - skew : 0;
+            const long long span = static_cast<long long>(VE) * nub * static_cast<long long>(sizeof(T)) - lead;
+            const uint32_t bytes = span >= 16 ? static_cast<uint32_t>(min(kPrefetch, span / 16 * 16)) : 0u;
+            for (int r = r_begin + static_cast<int>(threadIdx.x); bytes > 0 && r < r_end; r += 32)
+                ptx::prefetch_l2(reinterpret_cast<const char *>(A + static_cast<long long>(r) * p.lda) + lead, bytes);
+        }
     }
     ptx::wait_prior_grid();
     ptx::allow_next_grid();
@@ -610,12 +662,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
     }
 
     const T *arow[ROWS];
-    int j0 = 0, j1 = 0;
+    int j0 = 0, j1 = 0, h = 0;
+    // PEEL: the first row of row group rg (rows first + kPhase * r)
+    auto first_row = [&](int rg) { return r_begin + rg / kPhase * (kPhase * ROWS) + rg % kPhase; };
+    // a task with no row in range (PEEL, fewer than kPhase * ROWS rows left) is skipped
+    auto live = [&](int task) { return !PEEL || first_row(task / WC) < r_end; };
     auto setup = [&](int task) {
         const int rg = task / WC, cs = task - rg * WC;
+        if constexpr (PEEL) {
+            // rows past the end repeat the last row in range with the same phase
+            const int first = first_row(rg);
+            const int last = (r_end - 1 - first) / kPhase;
 #pragma unroll
-        for (int r = 0; r < ROWS; ++r)
-            arow[r] = A + static_cast<long long>(min(r_begin + rg * ROWS + r, r_end - 1)) * p.lda;
+            for (int r = 0; r < ROWS; ++r)
+                arow[r] = A + static_cast<long long>(first + kPhase * min(r, last)) * p.lda;
+            h = static_cast<int>(((16u - (reinterpret_cast<uintptr_t>(arow[0]) & 15u)) & 15u) >> 2);
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) arow[r] += h;   // 16-byte aligned
+        } else {
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r)
+                arow[r] = A + static_cast<long long>(min(r_begin + rg * ROWS + r, r_end - 1)) * p.lda;
+        }
         j0 = cs * segu;
         j1 = min(j0 + segu, nub);
     };
@@ -629,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
     };
 
     Raw nxt[U][ROWS];
-    if (warp < ntasks) {
+    if (warp < ntasks && live(warp)) {
         setup(warp);
         if (j0 < j1) load(j0, nxt);
     }
@@ -640,12 +708,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
 #pragma unroll
         for (int b = 0; b < BATCH; ++b) {
             const float *src = p.x + static_cast<long long>(b) * p.ldx + VE * ub0;
-            for (int j = threadIdx.x; j < xlen; j += kThreads) xs[b * p.chunk + j] = __ldg(src + j);
+            for (int j = threadIdx.x; j < xlen; j += kThreads)
+                xs[b * p.chunk + (PEEL ? (j & 3) * xq + (j >> 2) : j)] = __ldg(src + j);
         }
         __syncthreads();
     }
 
     for (int task = warp; ok && task < ntasks; task += kWarps) {
+        if (!live(task)) continue;
         if (task != warp) {
             setup(task);
             if (j0 < j1) load(j0, nxt);
@@ -666,7 +736,27 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int j = jb + 32 * u + lane;
-                if (j < j1) fma_quad<T, ROWS, BATCH>(acc, cur[u], xs, p.chunk, VE * j);
+                if constexpr (PEEL) {
+                    if (j < j1) fma_quad_peeled<ROWS, BATCH>(acc, cur[u], xs, p.chunk, xq, h, j);
+                } else {
+                    if (j < j1) fma_quad<T, ROWS, BATCH>(acc, cur[u], xs, p.chunk, VE * j);
+                }
+            }
+        }
+        if constexpr (PEEL) {
+            // the head [0, h) and the entries past the whole units
+            if (cs == WC - 1) {
+                auto single = [&](int col) {
+                    const float *xc = xs + (col & 3) * xq + (col >> 2);
+#pragma unroll
+                    for (int r = 0; r < ROWS; ++r) {
+                        const float a = Elem<T>::one(arow[r] - h + col);
+#pragma unroll
+                        for (int b = 0; b < BATCH; ++b) acc[r][b] = fmaf(a, xc[b * p.chunk], acc[r][b]);
+                    }
+                };
+                if (lane < h && lane < p.N) single(lane);
+                for (int col = h + VE * nu + lane; col < p.N; col += 32) single(col);
             }
         }
         if (cs == WC - 1 && lane < tail) {
@@ -685,7 +775,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
         // one CTA holds whole rows: its segment sums are the totals
         for (int idx = threadIdx.x; idx < rows * BATCH; idx += kThreads) {
             const int rl = idx / BATCH, b = idx - rl * BATCH;
-            const int rg = rl / ROWS, r = rl - rg * ROWS;
+            int rg, r;
+            if constexpr (PEEL) {
+                const int blk = rl / (kPhase * ROWS), off = rl - blk * (kPhase * ROWS);
+                rg = blk * kPhase + off % kPhase;
+                r = off / kPhase;
+            } else {
+                rg = rl / ROWS;
+                r = rl - rg * ROWS;
+            }
             float v = 0.f;
 #pragma unroll
             for (int cs = 0; cs < WC; ++cs) v += part[((rg * WC + cs) * ROWS + r) * BATCH + b];
@@ -820,12 +918,18 @@ constexpr int kSplitRows = 4, kSplitSegs = 2;
 // 16 bytes (FP32) or four of 8 bytes (BF16), the same bytes either way
 constexpr int split_unroll(int elem_bytes) { return elem_bytes == 2 ? 4 : 2; }
 
-enum Kind { kStream = 0, kSplit = 1, kRound = 2, kCluster = 3, kPeel = 4 };
+enum Kind { kStream = 0, kSplit = 1, kRound = 2, kCluster = 3, kPeel = 4, kPeelSplit = 5 };
 
 template <typename T, int BATCH>
 void *pick(int kind, bool vec) {
     if constexpr (BATCH <= 2 && sizeof(T) == 4) {
         if (kind == kPeel) return reinterpret_cast<void *>(gemv_stream_peel_kernel<BATCH>);
+    }
+    if constexpr (BATCH >= 3 && sizeof(T) == 4) {
+        if (kind == kPeelSplit)
+            return reinterpret_cast<void *>(
+                gemv_blocks_kernel<T, BATCH, kSplitRows, kSplitSegs, split_unroll(sizeof(T)), kRoundThreads, false,
+                                   true>);
     }
     if constexpr (BATCH <= 2) {
         if (kind == kStream) {

@@ -118,12 +118,46 @@ def test_unaligned_rows_at_batch_1_and_2(batch, M, N, lda, a_off):
     check(A, X, run_gemv(A, X, lda=lda, a_off=a_off))
 
 
+@pytest.mark.parametrize("batch", [3, 5, 8])
+@pytest.mark.parametrize("M,N,lda,a_off", [(1000, 4095, 4095, 0), (333, 1001, 1003, 1), (301, 517, 518, 2),
+                                           (700, 2048, 2048, 1), (64, 3, 3, 1), (77, 5, 7, 3), (40, 2, 2, 0),
+                                           (609, 9, 9, 2), (2000, 4094, 4094, 0), (151, 6000, 6001, 3)])
+def test_unaligned_rows_at_batch_3_to_8(batch, M, N, lda, a_off):
+    # FP32 rows off 16 bytes at batch >= 3: tasks of four rows four apart
+    # (the same offset from a 16-byte boundary), each row's head by single
+    # loads and the rest by aligned 16-byte loads; lda % 4 of 3, 1, 2 and 0
+    # (with A off 16 bytes), fewer than 16 rows per CTA (row groups left
+    # empty), rows shorter than one unit
+    g = PCG32(38 + N + lda + a_off + batch)
+    A = g.uniform_f32((M, N))
+    X = g.uniform_f32((batch, N))
+    if a_off == 0:
+        plan = _plan(A, X, lda=lda)
+        assert plan["bm"] == 4 and plan["bk"] == 2 and plan["threads"] == 512 and plan["cluster"] == 1, plan
+    check(A, X, run_gemv(A, X, lda=lda, a_off=a_off))
+
+
+def test_unaligned_rows_at_batch_8_are_deterministic():
+    g = PCG32(39)
+    A = g.uniform_f32((3001, 3001))
+    X = g.uniform_f32((8, 3001))
+    Y1, Y2 = run_gemv(A, X), run_gemv(A, X)
+    assert np.array_equal(Y1, Y2)
+    check(A, X, Y1)
+
+
 def test_scalar_path_for_unaligned_rows():
+    # batch 3 here takes the peeled row-block kernel; x too long for one
+    # staging chunk at batch 8 takes the chunked scalar kernel
     g = PCG32(32)
     A = g.uniform_f32((257, 1001))
     X = g.uniform_f32((3, 1001))
     check(A, X, run_gemv(A, X, a_off=1))               # A not 16-byte aligned
     check(A, X, run_gemv(A, X, lda=1003))              # lda not a multiple of 4
+    A = g.uniform_f32((150, 9001))
+    X = g.uniform_f32((8, 9001))
+    assert _plan(A, X)["bm"] == 2 and _plan(A, X)["stages"] > 1
+    check(A, X, run_gemv(A, X))
 
 
 def test_padded_batch_strides():
