@@ -106,12 +106,12 @@ Layout layout(const DeviceInfo &dev, const GemvArgs &g) {
     l.cluster = 1;
     l.ublock = 0;
     if (!gemv_vec(g)) {
-        // FP32 rows off 16 bytes with x in one chunk: kernels that peel each
-        // row's head to reach aligned loads (batch 1-2: streaming, one row per
-        // warp; batch 3-8: row blocks of rows four apart, if their partial
-        // sums fit beside x)
-        if (g.a_elem == 4 && l.nchunks == 1) {
-            if (g.batch <= 2) {
+        // rows off 16 bytes with x in one chunk: kernels that peel each row's
+        // head to reach aligned loads (FP32 batch 1-2: streaming, one row per
+        // warp; FP32 batch 3-8 and BF16: row blocks of rows four apart, if
+        // their partial sums fit beside x)
+        if (l.nchunks == 1) {
+            if (g.a_elem == 4 && g.batch <= 2) {
                 l.kind = kPeel;
                 l.threads = kPeelThreads;
                 return l;

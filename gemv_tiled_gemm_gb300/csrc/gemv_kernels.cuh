@@ -239,16 +239,16 @@ __device__ __forceinline__ void fma_quad(float (&acc)[ROWS][BATCH], const typena
     }
 }
 
-// acc[r][b] += the four FP32 elements of row r at column h + 4j times vector
-// b, staged quad-transposed (entry c at (c % 4) * q + c / 4): lane j reads
-// word j (+1 past the wrap) of each of four quarter rows, so the 32 lanes
-// read consecutive words (gemv_blocks_kernel with PEEL).
-template <int ROWS, int BATCH>
-__device__ __forceinline__ void fma_quad_peeled(float (&acc)[ROWS][BATCH], const float4 (&raw)[ROWS],
+// acc[r][b] += the four elements of row r at column h + 4j times vector b,
+// staged quad-transposed (entry c at (c % 4) * q + c / 4): lane j reads word
+// j (+1 past the wrap) of each of four quarter rows, so the 32 lanes read
+// consecutive words (gemv_blocks_kernel with PEEL).
+template <typename T, int ROWS, int BATCH>
+__device__ __forceinline__ void fma_quad_peeled(float (&acc)[ROWS][BATCH], const typename Quad<T>::Raw (&raw)[ROWS],
                                                 const float *xs, int chunk, int q, int h, int j) {
     float a[ROWS][4];
 #pragma unroll
-    for (int r = 0; r < ROWS; ++r) Quad<float>::widen(raw[r], a[r]);
+    for (int r = 0; r < ROWS; ++r) Quad<T>::widen(raw[r], a[r]);
     const float *xe[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) xe[e] = xs + ((h + e) & 3) * q + ((h + e) >> 2) + j;
@@ -572,19 +572,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const Params p
 // second cluster barrier keeps every CTA's shared memory alive until the
 // others have read it. p.chunk >= (block width + 1) * VE.
 //
-// PEEL (FP32, C = 1): rows that do not start on 16 bytes. Rows kPhase = 4
-// apart start 16 * lda bytes apart, so they share their offset from a 16-byte
+// PEEL (C = 1): rows that do not start on a boundary of the lane load (16
+// bytes FP32, 8 bytes BF16). Rows kPhase = 4 apart start 4 * lda elements
+// apart, a whole number of loads, so they share their offset from a load
 // boundary: a task takes ROWS rows kPhase apart (rows b + i + kPhase * r of a
 // block of kPhase * ROWS rows, i = 0..kPhase-1), skips their first h = 0..3
-// entries (single loads) to reach aligned 16-byte loads, and meets x at
+// entries (single loads) to reach aligned loads of four entries, and meets x at
 // column h + 4j. x is staged quad-transposed (entry c at (c % 4) * xq + c / 4,
 // xq = p.chunk / 4), so the lanes' reads of one of the four columns of a unit
 // are consecutive words whatever h is. nu counts the whole units every row has
 // after its head; the at most six entries past them are single loads too.
 template <typename T, int BATCH, int ROWS, int WC, int U, int kThreads, bool CLUSTER, bool PEEL = false>
 __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p) {
-    static_assert(!PEEL || (!CLUSTER && sizeof(T) == 4), "peeled rows: FP32, one CTA per row block");
+    static_assert(!PEEL || !CLUSTER, "peeled rows: one CTA per row block");
     constexpr int kPhase = 4;
+    constexpr unsigned kLoadBytes = 4 * sizeof(T);   // one lane load: four entries
     constexpr int kWarps = kThreads / 32;
     using Q = Quad<T>;
     using Raw = typename Q::Raw;
@@ -630,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
         // start on 16 bytes, a BF16 column block may start 8 bytes past one)
         if constexpr (PEEL) {
             // each row from its first 16-byte boundary
-            const long long row_bytes = 4ll * p.N;
+            const long long row_bytes = static_cast<long long>(sizeof(T)) * p.N;
             for (int r = r_begin + static_cast<int>(threadIdx.x); r < r_end; r += 32) {
                 const char *rp = reinterpret_cast<const char *>(A + static_cast<long long>(r) * p.lda);
                 const long long lead = static_cast<long long>((16u - (reinterpret_cast<uintptr_t>(rp) & 15u)) & 15u);
@@ -676,9 +678,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
 #pragma unroll
             for (int r = 0; r < ROWS; ++r)
                 arow[r] = A + static_cast<long long>(first + kPhase * min(r, last)) * p.lda;
-            h = static_cast<int>(((16u - (reinterpret_cast<uintptr_t>(arow[0]) & 15u)) & 15u) >> 2);
+            const unsigned mis = static_cast<unsigned>(reinterpret_cast<uintptr_t>(arow[0]) & (kLoadBytes - 1));
+            h = static_cast<int>(((kLoadBytes - mis) & (kLoadBytes - 1)) / sizeof(T));
 #pragma unroll
-            for (int r = 0; r < ROWS; ++r) arow[r] += h;   // 16-byte aligned
+            for (int r = 0; r < ROWS; ++r) arow[r] += h;   // on a load boundary
         } else {
 #pragma unroll
             for (int r = 0; r < ROWS; ++r)
@@ -737,7 +740,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
             for (int u = 0; u < U; ++u) {
                 const int j = jb + 32 * u + lane;
                 if constexpr (PEEL) {
-                    if (j < j1) fma_quad_peeled<ROWS, BATCH>(acc, cur[u], xs, p.chunk, xq, h, j);
+                    if (j < j1) fma_quad_peeled<T, ROWS, BATCH>(acc, cur[u], xs, p.chunk, xq, h, j);
                 } else {
                     if (j < j1) fma_quad<T, ROWS, BATCH>(acc, cur[u], xs, p.chunk, VE * j);
                 }
@@ -925,7 +928,7 @@ void *pick(int kind, bool vec) {
     if constexpr (BATCH <= 2 && sizeof(T) == 4) {
         if (kind == kPeel) return reinterpret_cast<void *>(gemv_stream_peel_kernel<BATCH>);
     }
-    if constexpr (BATCH >= 3 && sizeof(T) == 4) {
+    if constexpr (BATCH >= 3 || sizeof(T) == 2) {
         if (kind == kPeelSplit)
             return reinterpret_cast<void *>(
                 gemv_blocks_kernel<T, BATCH, kSplitRows, kSplitSegs, split_unroll(sizeof(T)), kRoundThreads, false,

@@ -137,6 +137,24 @@ def test_unaligned_rows_at_batch_3_to_8(batch, M, N, lda, a_off):
     check(A, X, run_gemv(A, X, lda=lda, a_off=a_off))
 
 
+@pytest.mark.parametrize("batch", [1, 2, 3, 8])
+@pytest.mark.parametrize("M,N,lda,a_off", [(1000, 4095, 4095, 0), (333, 1001, 1003, 1), (301, 517, 518, 2),
+                                           (700, 2048, 2052, 0), (64, 3, 3, 1), (77, 5, 7, 3), (609, 9, 9, 2),
+                                           (151, 6000, 6001, 3), (500, 4100, 4100, 5)])
+def test_bf16_unaligned_rows_take_peeled_row_blocks(batch, M, N, lda, a_off):
+    # BF16 rows off 16 bytes: tasks of four rows four apart share the offset
+    # from an 8-byte boundary (the lane load), their heads are single loads;
+    # lda % 8 of 7, 3, 6, 4 (8-byte aligned rows, h = 0) and 5 with offsets
+    from seeded import bf16_bits_to_f32
+    g = PCG32(41 + N + lda + a_off + batch)
+    A = g.normal_bf16((M, N))
+    X = g.uniform_f32((batch, N))
+    if a_off == 0:
+        plan = _plan(A, X, prec="bf16", lda=lda)
+        assert plan["kernel"] == "gemv" and plan["bm"] == 4 and plan["bk"] == 4 and plan["threads"] == 512, plan
+    check(bf16_bits_to_f32(A), X, run_gemv(A, X, lda=lda, a_off=a_off, prec="bf16"))
+
+
 def test_unaligned_rows_at_batch_8_are_deterministic():
     g = PCG32(39)
     A = g.uniform_f32((3001, 3001))
