@@ -911,7 +911,10 @@ __global__ void __launch_bounds__(kPeelThreads, 1) gemv_stream_peel_kernel(const
 // gemv_stream_kernel (32 warps, one row each); batch >= 3 with x in one CTA ->
 // gemv_blocks_kernel without a cluster (16 warps, 4 rows x half the columns
 // per task); x too large for one CTA -> gemv_blocks_kernel over a cluster.
-// Otherwise gemv_kernel (16 warps, two rows per task, x chunked if needed).
+// Rows off 16 bytes with x in one chunk: FP32 batch <= 2 ->
+// gemv_stream_peel_kernel; FP32 batch >= 3 and BF16 -> gemv_blocks_kernel
+// with PEEL. Otherwise gemv_kernel (16 warps, two rows per task, x chunked
+// if needed).
 constexpr int kStreamThreads = 1024;
 constexpr int kRoundThreads = 512;
 constexpr int kRows = 2;

@@ -178,7 +178,11 @@ GTG_API gtg_status gemm_f16(int64_t M, int64_t N, int64_t K,
  *          (ldy >= M; ignored when batch == 1), overwritten
  *   batch  1 <= batch <= 8
  * Pointers must be 4-byte aligned; a 16-byte aligned A with lda % 4 == 0
- * enables 128-bit row loads.
+ * enables 128-bit row loads throughout. Other rows take their first 0-3
+ * entries (up to a 16-byte boundary) by single loads and the rest by 128-bit
+ * loads when the vectors and the rows' partial sums fit one CTA's shared
+ * memory (N up to about 51200 / batch entries); beyond that the rows are
+ * read one entry per load. The result is the same either way.
  */
 GTG_API gtg_status gemv_f32(int64_t M, int64_t N,
                     const float *A, int64_t lda,
@@ -203,7 +207,11 @@ GTG_API gtg_status gemv_f32(int64_t M, int64_t N,
  * pieces, 6 * batch * roundup(N, 8) bytes, and the partial sums of the row
  * tiles whose columns are shared between SMs).
  *   Arguments as gemv_f32; A must be 2-byte aligned (x and y 4-byte); a
- *   16-byte aligned A with lda % 8 == 0 enables 128-bit row loads.
+ *   16-byte aligned A with lda % 8 == 0 enables 128-bit row loads. Other
+ *   rows take their first 0-3 entries (up to an 8-byte boundary) by single
+ *   loads and the rest by 64-bit loads when the vectors and the rows'
+ *   partial sums fit one CTA's shared memory (N up to about 51200 / batch
+ *   entries), else one entry per load.
  */
 GTG_API gtg_status gemv_bf16(int64_t M, int64_t N,
                              const gtg_bf16 *A, int64_t lda,
