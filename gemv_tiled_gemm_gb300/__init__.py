@@ -26,6 +26,7 @@ LIB_PATH = os.path.join(_PKG, "libgtg.so")
 GTG_OK, GTG_ERR_INVALID_VALUE, GTG_ERR_MISALIGNED, GTG_ERR_ALIAS = 0, 1, 2, 3
 GTG_ERR_UNSUPPORTED, GTG_ERR_LAUNCH, GTG_ERR_TIMEOUT, GTG_ERR_DEVICE = 4, 5, 6, 7
 GTG_ERR_SCRATCH_LIMIT = 8
+GTG_ERR_BOUNDS = 9
 PREC = {"f32": 0, "tf32": 1, "bf16": 2, "f16": 3}
 KERNELS = {0: "none", 1: "simt", 2: "tcgen05", 3: "zero_fill", 4: "gemv"}
 
@@ -80,15 +81,26 @@ SIGNATURES = {
                              ctypes.POINTER(GtgPlan)]),
     "gtg_plan_gemv_bf16": (_int, [_i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _int,
                              ctypes.POINTER(GtgPlan)]),
+    "gtg_version": (_int, []),
+}
+
+# include/gtg_testing.h: path switches, failure-path hooks and probes for
+# tests and tuning (the failure-path hooks act only with GTG_TESTING=1 in the
+# environment)
+TESTING_SIGNATURES = {
     "gtg_force_simt": (None, [_int]),
     "gtg_force_gemm_splits": (None, [_int]),
     "gtg_force_c_store": (None, [_int]),
     "gtg_conv_force_path": (None, [_int]),
-    "gtg_test_skip_vector_copy": (None, [_int]),
     "gtg_gemv_force_path": (None, [_int]),
     "gtg_set_wait_limit_ns": (None, [ctypes.c_uint64]),
-    "gtg_test_drop_load": (None, [_int]),
-    "gtg_version": (_int, []),
+    "gtg_test_drop_load": (_int, [_int]),
+    "gtg_test_skip_vector_copy": (_int, [_int]),
+    "gtg_test_inject_launch_failure": (_int, [_int]),
+    "gtg_test_workspace_allocations": (ctypes.c_uint64, []),
+    "gtg_plan_gemm_tf32_noalloc": (_int, [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64,
+                                          ctypes.POINTER(GtgPlan)]),
+    "gtg_debug_build": (_int, []),
 }
 
 
@@ -114,7 +126,7 @@ def lib():
                 raise GtgError(-1, f"{LIB_PATH} is missing: build it first "
                                    "(python -c 'import __graft_entry__ as g; g.build()')")
             handle = ctypes.CDLL(LIB_PATH)
-            for name, (res, args) in SIGNATURES.items():
+            for name, (res, args) in {**SIGNATURES, **TESTING_SIGNATURES}.items():
                 fn = getattr(handle, name)
                 fn.restype = res
                 fn.argtypes = args
@@ -241,6 +253,8 @@ def last_cuda_error() -> str:
     return lib().gtg_last_cuda_error().decode()
 
 
+# ---- testing and tuning hooks (include/gtg_testing.h) ---------------------------
+
 def gtg_force_simt(force: bool) -> None:
     lib().gtg_force_simt(1 if force else 0)
 
@@ -252,11 +266,6 @@ def gtg_gemv_force_path(path="auto") -> None:
     """Tuning/testing hook for BF16 GEMVs of batch 3-8: "auto" (the planner),
     "cuda_cores", or "tensor_cores" (whenever the layout allows)."""
     lib().gtg_gemv_force_path(GEMV_PATHS[path] if isinstance(path, str) else int(path))
-
-
-def gtg_test_skip_vector_copy(on: bool) -> None:
-    """Testing hook: the next bulk-staged GEMV announces its vector copies but issues none."""
-    lib().gtg_test_skip_vector_copy(1 if on else 0)
 
 
 def gtg_conv_force_path(mode: str) -> None:
@@ -278,8 +287,38 @@ def gtg_set_wait_limit_ns(ns: int) -> None:
     lib().gtg_set_wait_limit_ns(ns)
 
 
-def gtg_test_drop_load(slice_index: int) -> None:
-    lib().gtg_test_drop_load(slice_index)
+def gtg_test_drop_load(slice_index: int) -> int:
+    """Failure-path hook (needs GTG_TESTING=1): the next tensor-core GEMM leaves out one K-slice load."""
+    return lib().gtg_test_drop_load(slice_index)
+
+
+def gtg_test_skip_vector_copy(on: bool) -> int:
+    """Failure-path hook (needs GTG_TESTING=1): the next bulk-staged GEMV announces its
+    vector copies but issues none."""
+    return lib().gtg_test_skip_vector_copy(1 if on else 0)
+
+
+def gtg_test_inject_launch_failure(n: int) -> int:
+    """Failure-path hook (needs GTG_TESTING=1): the n-th dispatched call from now on
+    returns GTG_ERR_LAUNCH before launching anything (0 cancels)."""
+    return lib().gtg_test_inject_launch_failure(int(n))
+
+
+def gtg_test_workspace_allocations() -> int:
+    return int(lib().gtg_test_workspace_allocations())
+
+
+def plan_gemm_tf32_noalloc(M, N, K, A, lda, B, ldb, C, ldc) -> dict:
+    """The kernel gemm_tf32_noalloc would launch for these arguments."""
+    plan = GtgPlan()
+    st = lib().gtg_plan_gemm_tf32_noalloc(M, N, K, A, lda, B, ldb, C, ldc, ctypes.byref(plan))
+    if st != GTG_OK:
+        raise GtgError(st, "gtg_plan_gemm_tf32_noalloc")
+    return plan.as_dict()
+
+
+def gtg_debug_build() -> int:
+    return lib().gtg_debug_build()
 
 
 def gtg_version() -> int:

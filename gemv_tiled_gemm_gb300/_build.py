@@ -34,7 +34,7 @@ def sources() -> list[str]:
 
 def _deps() -> list[str]:
     return (sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h"))
-            + [os.path.join(INCLUDE, "gtg.h"), os.path.abspath(__file__)])
+            + glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)])
 
 
 def up_to_date() -> bool:

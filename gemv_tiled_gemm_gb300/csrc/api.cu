@@ -3,11 +3,13 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <vector>
 
 #include "gtg.h"
+#include "gtg_testing.h"
 #include "internal.h"
 
 namespace gtg {
@@ -21,9 +23,45 @@ __device__ int g_device_status = 0;
 thread_local char t_cuda_error[256] = "no error";
 std::atomic<int> g_force_simt{0};
 
-void note_cuda_error(cudaError_t e) {
-    std::strncpy(t_cuda_error, cudaGetErrorString(e), sizeof(t_cuda_error) - 1);
+void note_text(const char *text) {
+    std::strncpy(t_cuda_error, text, sizeof(t_cuda_error) - 1);
     t_cuda_error[sizeof(t_cuda_error) - 1] = '\0';
+}
+
+void note_cuda_error(cudaError_t e) { note_text(cudaGetErrorString(e)); }
+
+// The failure-path hooks act only when GTG_TESTING=1 is in the environment.
+bool testing_enabled() {
+    const char *v = std::getenv("GTG_TESTING");
+    return v != nullptr && std::strcmp(v, "1") == 0;
+}
+
+// Host-side fault injection: when the countdown reaches zero, the dispatch
+// that took it there fails with GTG_ERR_LAUNCH before launching anything.
+// GTG_FAULT_INJECT=<n> in the environment arms it once, at the first dispatch.
+std::atomic<long long> g_inject_countdown{0};
+std::once_flag g_inject_env_once;
+
+void read_fault_inject_env() {
+    std::call_once(g_inject_env_once, [] {
+        const char *v = std::getenv("GTG_FAULT_INJECT");
+        if (v == nullptr) return;
+        const long long n = std::strtoll(v, nullptr, 10);
+        if (n > 0) g_inject_countdown.store(n);
+    });
+}
+
+bool injected_failure() {
+    read_fault_inject_env();
+    long long c = g_inject_countdown.load();
+    while (c > 0) {
+        if (g_inject_countdown.compare_exchange_weak(c, c - 1)) {
+            if (c != 1) return false;
+            note_text("injected launch failure");
+            return true;
+        }
+    }
+    return false;
 }
 
 struct DeviceTable {
@@ -176,6 +214,7 @@ gtg_status run_gemm(const GemmArgs &g, cudaStream_t stream) {
     gtg_status st = g.batch == 1 ? validate_gemm(g) : validate_batched(g);
     if (st != GTG_OK) return st;
     if (g.M == 0 || g.N == 0 || g.batch == 0) return GTG_OK;
+    if (injected_failure()) return GTG_ERR_LAUNCH;
     DeviceInfo dev;
     if ((st = current_device(&dev)) != GTG_OK) return st;
     gtg_plan plan;
@@ -227,6 +266,7 @@ static gtg_status run_gemv(const GemvArgs &g, cudaStream_t stream) {
     const int batch = g.batch;
     gtg_status st = validate_gemv(g);
     if (st != GTG_OK || M == 0) return st;
+    if (injected_failure()) return GTG_ERR_LAUNCH;
     DeviceInfo dev;
     if ((st = current_device(&dev)) != GTG_OK) return st;
     if (!(dev.cc_major == 10 && dev.cc_minor == 3)) return GTG_ERR_UNSUPPORTED;
@@ -247,6 +287,22 @@ static gtg_status run_gemv(const GemvArgs &g, cudaStream_t stream) {
     return GTG_OK;
 }
 
+// The plan of gemm_tf32_noalloc: never a K split (split partial products
+// would need a workspace) and never the CTA-pair kernel (the fixed-scratch
+// launch runs the single-CTA tensor-core kernel), no repacked operands.
+static gtg_status plan_noalloc_impl(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
+    gtg_status st = plan_gemm_impl(dev, g, plan, false);
+    if (st != GTG_OK) return st;
+    if (plan->kernel == GTG_KERNEL_TCGEN05) {
+        tc_plan_unsplit_single(dev, g, plan);
+    } else if (plan->kernel == GTG_KERNEL_SIMT && plan->splits > 1) {
+        // one K range: the SIMT kernel then writes C directly
+        plan->grid /= plan->splits;
+        plan->splits = 1;
+    }
+    return GTG_OK;
+}
+
 gtg_status gemm_tf32_noalloc(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
                              int64_t ldb, float *C, int64_t ldc, cudaStream_t stream) {
     const GemmArgs g{GTG_PREC_TF32, M, N, K, A, lda, B, ldb, C, ldc};
@@ -254,16 +310,11 @@ gtg_status gemm_tf32_noalloc(int64_t M, int64_t N, int64_t K, const float *A, in
     if (st != GTG_OK) return st;
     if (M == 0 || N == 0) return GTG_OK;
     if (tf32_bt_bytes(N, K) > tf32_fixed_scratch_bytes()) return GTG_ERR_SCRATCH_LIMIT;
+    if (injected_failure()) return GTG_ERR_LAUNCH;
     DeviceInfo dev;
     if ((st = current_device(&dev)) != GTG_OK) return st;
     gtg_plan plan;
-    // no repacked operands here (they would need pool memory)
-    if ((st = plan_gemm_impl(dev, g, &plan, false)) != GTG_OK) return st;
-    if (plan.kernel == GTG_KERNEL_SIMT) {
-        // one K split: the SIMT kernel then writes C directly and needs no workspace
-        plan.grid /= plan.splits;
-        plan.splits = 1;
-    }
+    if ((st = plan_noalloc_impl(dev, g, &plan)) != GTG_OK) return st;
     cudaError_t e = cudaSuccess;
     switch (plan.kernel) {
         case GTG_KERNEL_ZERO_FILL: e = zero_fill_launch(g.C, g.M, g.N, g.ldc, stream); break;
@@ -276,6 +327,20 @@ gtg_status gemm_tf32_noalloc(int64_t M, int64_t N, int64_t K, const float *A, in
         return GTG_ERR_LAUNCH;
     }
     return GTG_OK;
+}
+
+gtg_status gtg_plan_gemm_tf32_noalloc(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                                      const float *B, int64_t ldb, const float *C, int64_t ldc, gtg_plan *plan) {
+    if (plan == nullptr) return GTG_ERR_INVALID_VALUE;
+    const GemmArgs g{GTG_PREC_TF32, M, N, K, A, lda, B, ldb, const_cast<float *>(C), ldc};
+    gtg_status st = validate_gemm(g);
+    if (st != GTG_OK) return st;
+    std::memset(plan, 0, sizeof(*plan));
+    if (M == 0 || N == 0) return GTG_OK;
+    if (tf32_bt_bytes(N, K) > tf32_fixed_scratch_bytes()) return GTG_ERR_SCRATCH_LIMIT;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != GTG_OK) return st;
+    return plan_noalloc_impl(dev, g, plan);
 }
 
 gtg_status gemv_f32(int64_t M, int64_t N, const float *A, int64_t lda, const float *x, int64_t ldx,
@@ -438,6 +503,8 @@ const char *gtg_status_string(gtg_status s) {
         case GTG_ERR_DEVICE: return "CUDA runtime error";
         case GTG_ERR_SCRATCH_LIMIT:
             return "problem too large for the fixed scratch of gemm_tf32_noalloc (N * roundup(K, 4) * 4 > 16 MiB)";
+        case GTG_ERR_BOUNDS:
+            return "a kernel computed an address outside an operand and skipped the access (GTG_DEBUG build)";
         default: return "unknown status";
     }
 }
@@ -452,6 +519,7 @@ gtg_status gemm_host(int precision, int64_t M, int64_t N, int64_t K, const void 
     }
     gtg_status st = validate_gemm(g);
     if (st != GTG_OK || M == 0 || N == 0) return st;
+    if (injected_failure()) return GTG_ERR_LAUNCH;
     DeviceInfo dev;
     if ((st = current_device(&dev)) != GTG_OK) return st;
     if (!(dev.cc_major == 10 && dev.cc_minor == 3)) return GTG_ERR_UNSUPPORTED;
@@ -542,6 +610,7 @@ gtg_status conv2d_nhwc(int precision, int64_t N, int64_t H, int64_t W, int64_t C
     }
     gtg_status st = validate_conv(c);
     if (st != GTG_OK || N == 0 || CO == 0) return st;
+    if (injected_failure()) return GTG_ERR_LAUNCH;
     DeviceInfo dev;
     if ((st = current_device(&dev)) != GTG_OK) return st;
     if (!(dev.cc_major == 10 && dev.cc_minor == 3)) return GTG_ERR_UNSUPPORTED;
@@ -599,9 +668,34 @@ void gtg_force_simt(int force) { g_force_simt.store(force ? 1 : 0); }
 
 void gtg_set_wait_limit_ns(uint64_t ns) { tc_set_wait_limit_ns(ns); }
 
-void gtg_test_drop_load(int slice) { tc_drop_next_load(slice); }
+gtg_status gtg_test_drop_load(int slice) {
+    if (!testing_enabled()) return GTG_ERR_UNSUPPORTED;
+    tc_drop_next_load(slice);
+    return GTG_OK;
+}
 
-void gtg_test_skip_vector_copy(int on) { gemv_skip_next_x(on); }
+gtg_status gtg_test_skip_vector_copy(int on) {
+    if (!testing_enabled()) return GTG_ERR_UNSUPPORTED;
+    gemv_skip_next_x(on);
+    return GTG_OK;
+}
+
+gtg_status gtg_test_inject_launch_failure(int n) {
+    if (!testing_enabled()) return GTG_ERR_UNSUPPORTED;
+    read_fault_inject_env();   // so that the environment's value cannot overwrite this one later
+    g_inject_countdown.store(n > 0 ? n : 0);
+    return GTG_OK;
+}
+
+uint64_t gtg_test_workspace_allocations(void) { return ws_alloc_count(); }
+
+int gtg_debug_build(void) {
+#ifdef GTG_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
 
 void gtg_gemv_force_path(int mode) { gemv_force_path(mode); }
 

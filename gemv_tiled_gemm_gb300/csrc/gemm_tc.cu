@@ -1444,6 +1444,27 @@ void tc_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
     }
 }
 
+void tc_plan_unsplit_single(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
+    const bool tf32 = g.prec == GTG_PREC_TF32;
+    const int bk = tf32 ? 32 : 64;
+    const int widths[3] = {256, 128, 64};
+    const double rel[3] = {1.0, 0.5 / 0.8, 0.25 / 0.5};
+    int best = 0;
+    double best_cost = 0;
+    for (int i = 0; i < 3; ++i) {
+        const double c = tc_cost(dev, g, kBM, widths[i], dev.sms, rel[i], 1, bk);
+        if (i == 0 || c < best_cost) {
+            best_cost = c;
+            best = i;
+        }
+    }
+    switch (widths[best]) {
+        case 256: tf32 ? fill_plan<true, 256>(dev, g, plan, 1) : fill_plan<false, 256>(dev, g, plan, 1); break;
+        case 128: tf32 ? fill_plan<true, 128>(dev, g, plan, 1) : fill_plan<false, 128>(dev, g, plan, 1); break;
+        default: tf32 ? fill_plan<true, 64>(dev, g, plan, 1) : fill_plan<false, 64>(dev, g, plan, 1); break;
+    }
+}
+
 bool tc_conv_eligible(const DeviceInfo &dev, const ConvArgs &c) {
     if (!tc_supported(dev) || encode_im2col_fn() == nullptr) return false;
     if (c.prec != GTG_PREC_BF16 && c.prec != GTG_PREC_F16) return false;

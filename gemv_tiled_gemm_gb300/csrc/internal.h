@@ -89,6 +89,9 @@ void tc_force_c_store(int mode);    // CTA-pair kernel's C stores: 0 auto, 1 dir
 // (gemm_tc.cu), for callers that cannot allocate device memory
 size_t tf32_fixed_scratch_bytes();
 size_t tf32_bt_bytes(int64_t N, int64_t K);
+// the single-CTA tile width for a product computed in one K range (no
+// workspace); replaces *plan (the fixed-scratch launch runs only that kernel)
+void tc_plan_unsplit_single(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan);
 cudaError_t tc_launch_tf32_fixed_scratch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan,
                                          cudaStream_t stream);
 
@@ -120,6 +123,7 @@ gtg_status gemm_host_pipeline(const DeviceInfo &dev, const GemmArgs &g, gtg_stat
 // stream ordered after the last use); ws_trim returns the reserved pages.
 cudaError_t ws_alloc(void **p, size_t bytes, cudaStream_t stream);
 cudaError_t ws_trim();
+uint64_t ws_alloc_count();   // ws_alloc calls so far (every device)
 
 // ---- implicit-GEMM convolution on the tensor cores (gemm_tc.cu): A tiles
 // loaded from X by TMA in im2col mode (16-bit, C % 64 == 0, small windows)

@@ -5,6 +5,7 @@
 // reserved across synchronisations, so that a call after a synchronisation
 // reuses pages instead of mapping them again (a mapping can hold the host
 // for most of a millisecond); gtg_pool_trim hands them back.
+#include <atomic>
 #include <mutex>
 
 #include "internal.h"
@@ -50,7 +51,14 @@ cudaError_t device_pool(int device, cudaMemPool_t *out) {
 
 }  // namespace
 
+namespace {
+std::atomic<uint64_t> g_ws_allocs{0};
+}
+
+uint64_t ws_alloc_count() { return g_ws_allocs.load(); }
+
 cudaError_t ws_alloc(void **p, size_t bytes, cudaStream_t stream) {
+    g_ws_allocs.fetch_add(1);
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
     cudaMemPool_t pool;

@@ -46,6 +46,8 @@
  *    (device properties and a table of kernel attributes).
  *  - Thread safety: calls may be made concurrently from several host
  *    threads; the host-side state is guarded by a mutex.
+ *  - Testing: hooks for test suites and tuning (path switches, failure
+ *    injection, wait limits) are declared in gtg_testing.h, not here.
  */
 #ifndef GTG_H
 #define GTG_H
@@ -79,7 +81,9 @@ enum {
     GTG_ERR_LAUNCH = 5,        /* the CUDA launch failed (cudaGetLastError text via gtg_last_cuda_error) */
     GTG_ERR_TIMEOUT = 6,       /* device side: a pipeline wait exceeded its time limit */
     GTG_ERR_DEVICE = 7,        /* a CUDA runtime call failed (no device, context error, ...) */
-    GTG_ERR_SCRATCH_LIMIT = 8  /* gemm_tf32_noalloc: B^T would not fit its fixed 16 MiB scratch */
+    GTG_ERR_SCRATCH_LIMIT = 8, /* gemm_tf32_noalloc: B^T would not fit its fixed 16 MiB scratch */
+    GTG_ERR_BOUNDS = 9         /* device side, GTG_DEBUG builds only: a kernel computed an address
+                                  outside one of its operands and skipped that access */
 };
 
 /*
@@ -490,81 +494,6 @@ GTG_API gtg_status gtg_plan_gemv(int64_t M, int64_t N, const float *A, int64_t l
 GTG_API gtg_status gtg_plan_gemv_bf16(int64_t M, int64_t N, const gtg_bf16 *A, int64_t lda,
                               const float *x, int64_t ldx, const float *y, int64_t ldy,
                               int batch, gtg_plan *plan);
-
-/*
- * Testing and tuning hook: with splits > 0 every tensor-core GEMM of a single
- * product (and every implicit-GEMM convolution) that has at least 2 * splits
- * K slices computes K in `splits` ranges whose partial tiles are added in
- * order by a second kernel (workspace from the stream-ordered pool); 0
- * restores the planner's own choice. Process-wide; results stay within the
- * same bounds.
- */
-GTG_API void gtg_force_gemm_splits(int splits);
-
-/*
- * Testing and tuning hook for how the CTA-pair tensor-core kernel (16-bit
- * and TF32 inputs, 256 x 256 tiles) writes C: 0 (default) lets each call
- * choose; 1 always stores each thread's row of the tile straight to global
- * memory; 2 goes through shared memory and tensor stores (32 x 32 FP32
- * blocks) whenever C's layout allows them (16-byte aligned base, ldc and
- * batch stride multiples of 4 elements, K not split). Other values act as 0.
- * Process-wide; results are identical in every mode.
- */
-GTG_API void gtg_force_c_store(int mode);
-
-/*
- * Testing hook for conv2d_nhwc: 0 (default) lets each call choose; 1 always
- * writes the patch matrix and multiplies it (im2col + GEMM); 2 requires the
- * implicit GEMM, whose tensor-core kernel loads the patches straight from X
- * with TMA in im2col mode, and makes a call that cannot take it return
- * GTG_ERR_UNSUPPORTED. Process-wide.
- */
-GTG_API void gtg_conv_force_path(int mode);
-
-/*
- * Testing hook: force the tensor-core GEMM paths onto the SIMT kernel
- * (force = 1) or restore the normal choice (force = 0). Process-wide.
- */
-GTG_API void gtg_force_simt(int force);
-
-/*
- * Time limit of every pipeline wait inside the tensor-core GEMM kernels and
- * of the GEMV kernels' wait for their bulk-copied vectors, in nanoseconds
- * (0 restores the default of 2 s). A wait that runs out makes the
- * kernel stop, release its resources and latch GTG_ERR_TIMEOUT for
- * gtg_sync_status(). Process-wide; applies to later launches.
- */
-GTG_API void gtg_set_wait_limit_ns(uint64_t ns);
-
-/*
- * Testing hook for the failure path: the next tensor-core GEMM launch leaves
- * out the load of K slice `slice` (counted over the tiles of the first CTA or
- * CTA pair), so the wait for it can only run out. The call that launches it
- * returns GTG_OK; gtg_sync_status() then reports GTG_ERR_TIMEOUT and later
- * calls work normally. A negative value cancels a pending drop.
- */
-GTG_API void gtg_test_drop_load(int slice);
-
-/*
- * Testing hook for the GEMV failure path: with on != 0, the next GEMV launch
- * that stages its vectors by bulk copies announces the copies to its
- * mbarrier but issues none, so its bounded wait can only run out; the call
- * returns GTG_OK and gtg_sync_status() reports GTG_ERR_TIMEOUT. 0 cancels.
- */
-GTG_API void gtg_test_skip_vector_copy(int on);
-
-/*
- * gtg_gemv_force_path -- tuning / testing hook for gemv_bf16 with batch 3..8.
- * By default (mode 0) such a call runs on the tensor cores (the vectors split
- * into three BF16 pieces each, see gemv_bf16) when the tensor memory
- * accelerator can read the matrix (16-byte aligned A, lda * 2 a multiple of
- * 16), it has at least 2^25 elements and batch >= 6, else on the CUDA-core
- * kernels.
- * Mode 1 always takes the CUDA-core kernels; mode 2 takes the tensor cores
- * whenever the layout allows, at any size. Other values act as 0.
- * Process-wide.
- */
-GTG_API void gtg_gemv_force_path(int mode);
 
 /* Version of this ABI (major * 10000 + minor * 100 + patch). */
 GTG_API int gtg_version(void);

@@ -12,6 +12,19 @@ from gemv_tiled_gemm_gb300 import _build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "gtg.h")
+TESTING_HEADER = os.path.join(ROOT, "include", "gtg_testing.h")
+
+
+def _has_device():
+    import torch
+    return torch.cuda.is_available()
+
+
+# Calls below that pass validation with fake addresses would launch kernels on
+# a machine with a GPU; those parts run only where no device exists (there
+# the call stops at the device lookup). The GPU tests cover the same paths
+# with real buffers.
+no_device_only = pytest.mark.skipif(_has_device(), reason="would launch with fake device addresses")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -20,10 +33,15 @@ def built():
     gtg.lib()
 
 
-def declared_functions():
-    text = open(HEADER).read()
+def _declared(path):
+    text = open(path).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return re.findall(r"GTG_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def declared_functions():
+    """Every exported function: the product ABI plus the testing header."""
+    return _declared(HEADER) + _declared(TESTING_HEADER)
 
 
 def test_header_declares_the_entry_points():
@@ -37,8 +55,73 @@ def test_library_exports_every_declared_symbol():
     handle = ctypes.CDLL(gtg.LIB_PATH)
     for name in declared_functions():
         assert hasattr(handle, name), f"{name} declared in gtg.h but not exported"
-    # and the binding covers each one with a signature
-    assert set(declared_functions()) == set(gtg.SIGNATURES)
+    # and the binding covers each one with a signature, in the matching table
+    assert set(_declared(HEADER)) == set(gtg.SIGNATURES)
+    assert set(_declared(TESTING_HEADER)) == set(gtg.TESTING_SIGNATURES)
+
+
+def test_product_header_holds_no_testing_hook():
+    names = set(_declared(HEADER))
+    hooks = {n for n in names if n.startswith(("gtg_test_", "gtg_force_")) or n.endswith("_force_path")
+             or n == "gtg_set_wait_limit_ns"}
+    assert not hooks, hooks
+    assert not set(_declared(HEADER)) & set(_declared(TESTING_HEADER))
+
+
+def test_failure_hooks_need_the_testing_switch():
+    # the hooks read GTG_TESTING when called; without it they arm nothing
+    import subprocess
+    import sys
+    code = ("import gemv_tiled_gemm_gb300 as g; "
+            "print(g.gtg_test_drop_load(1), g.gtg_test_skip_vector_copy(1), g.gtg_test_inject_launch_failure(1))")
+    env = {k: v for k, v in os.environ.items() if k != "GTG_TESTING"}
+    out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.split() == [str(gtg.GTG_ERR_UNSUPPORTED)] * 3
+    # with it, they arm (and are cancelled again here)
+    assert gtg.gtg_test_drop_load(-1) == gtg.GTG_OK
+    assert gtg.gtg_test_skip_vector_copy(False) == gtg.GTG_OK
+    assert gtg.gtg_test_inject_launch_failure(0) == gtg.GTG_OK
+
+
+@no_device_only
+def test_injected_launch_failure_stops_the_dispatcher():
+    # Valid arguments at fake addresses: without a GPU the call would fail
+    # looking for the device (GTG_ERR_DEVICE); the injected failure comes
+    # first, in the dispatcher, before any CUDA call. Calls that fail
+    # validation do not count towards the injection.
+    ok_args = (4, 4, 4, A, 4, B, 4, C, 4)
+    assert gtg.gtg_test_inject_launch_failure(2) == gtg.GTG_OK
+    assert gtg.gemm_f32(-1, 4, 4, A, 4, B, 4, C, 4) == gtg.GTG_ERR_INVALID_VALUE   # not counted
+    first = gtg.gemm_f32(*ok_args)                                                 # counted: 1
+    assert first != gtg.GTG_ERR_LAUNCH
+    assert gtg.gemv_f32(4, 4, A, 4, B, 4, C, 4, 1) == gtg.GTG_ERR_LAUNCH             # counted: 2, fires
+    assert gtg.last_cuda_error() == "injected launch failure"
+    assert gtg.gemm_f32(*ok_args) == first                                         # disarmed again
+    # every dispatching entry point takes part
+    for call in (lambda: gtg.gemm_tf32(*ok_args), lambda: gtg.gemm_bf16(*ok_args),
+                 lambda: gtg.gemm_tf32_noalloc(*ok_args),
+                 lambda: gtg.gemm_strided_batched("bf16", 4, 4, 4, A, 4, 16, B, 4, 16, C, 4, 16, 2),
+                 lambda: gtg.gemv_bf16(4, 4, A, 4, B, 4, C, 4, 2),
+                 lambda: gtg.conv2d_nhwc("bf16", 1, 4, 4, 8, 8, 3, 3, 1, 1, 1, 1, 1, 1, A, B, C),
+                 lambda: gtg.gemm_host("f32", 4, 4, 4, A, 4, B, 4, C, 4)):
+        assert gtg.gtg_test_inject_launch_failure(1) == gtg.GTG_OK
+        assert call() == gtg.GTG_ERR_LAUNCH
+    assert gtg.gtg_test_inject_launch_failure(0) == gtg.GTG_OK
+
+
+@no_device_only
+def test_fault_inject_environment_variable():
+    import subprocess
+    import sys
+    code = ("import gemv_tiled_gemm_gb300 as g; A, B, C = 1 << 32, 2 << 32, 3 << 32; "
+            "print(*[g.gemm_f32(4, 4, 4, A, 4, B, 4, C, 4) for _ in range(4)])")
+    env = {k: v for k, v in os.environ.items() if k != "GTG_TESTING"}
+    env["GTG_FAULT_INJECT"] = "3"
+    out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True)
+    assert out.returncode == 0, out.stderr
+    st = [int(v) for v in out.stdout.split()]
+    assert st[2] == gtg.GTG_ERR_LAUNCH and gtg.GTG_ERR_LAUNCH not in (st[0], st[1], st[3]), st
 
 
 def test_only_the_c_abi_is_exported():
@@ -85,9 +168,10 @@ def test_gemm_alignment_and_alias(fn, elem):
     assert fn(4, 4, 4, A, 4, B, 4, A + 4 * elem, 4) == gtg.GTG_ERR_ALIAS
     assert fn(4, 4, 4, A, 4, B, 4, B, 4) == gtg.GTG_ERR_ALIAS
     # adjacent, touching but not overlapping, is fine as far as validation goes
-    # (it then needs a device, which this container does not have)
-    st = fn(4, 4, 4, A, 4, A + 16 * elem, 4, A + 32 * elem, 4)
-    assert st not in (gtg.GTG_ERR_ALIAS, gtg.GTG_ERR_INVALID_VALUE, gtg.GTG_ERR_MISALIGNED)
+    # (it then needs a device: checked only where none exists, see no_device_only)
+    if not _has_device():
+        st = fn(4, 4, 4, A, 4, A + 16 * elem, 4, A + 32 * elem, 4)
+        assert st not in (gtg.GTG_ERR_ALIAS, gtg.GTG_ERR_INVALID_VALUE, gtg.GTG_ERR_MISALIGNED)
 
 
 def test_gemm_host_argument_validation():

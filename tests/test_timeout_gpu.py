@@ -55,7 +55,7 @@ def test_wait_that_runs_out_is_reported_and_context_survives(prec, shape, kernel
     A, B = _operands(prec, M, N, K, 90)
     gtg.gtg_set_wait_limit_ns(SHORT_LIMIT_NS)
     try:
-        gtg.gtg_test_drop_load(2)
+        assert gtg.gtg_test_drop_load(2) == gtg.GTG_OK
         st, status, plan = _launch(prec, A, B)
     finally:
         gtg.gtg_test_drop_load(-1)
@@ -98,7 +98,7 @@ def test_gemv_vector_wait_that_runs_out_is_reported(M, N, batch, kernel):
     assert (plan["bm"] == 1) == (kernel == "stream") and (plan["cluster"] > 1) == (kernel == "cluster"), plan
     gtg.gtg_set_wait_limit_ns(SHORT_LIMIT_NS)
     try:
-        gtg.gtg_test_skip_vector_copy(True)
+        assert gtg.gtg_test_skip_vector_copy(True) == gtg.GTG_OK
         st = gtg.gemv_f32(M, N, A.data_ptr(), N, X.data_ptr(), N, Y.data_ptr(), M, batch, s)
         status = gtg.gtg_sync_status(s)
     finally:
@@ -130,7 +130,7 @@ def test_tensor_core_gemv_wait_that_runs_out_is_reported(M, N):
     try:
         plan = gtg.plan_gemv(M, N, A.data_ptr(), N, X.data_ptr(), N, Y.data_ptr(), M, 8, precision="bf16")
         assert plan["kernel"] == "tcgen05", plan
-        gtg.gtg_test_drop_load(1)
+        assert gtg.gtg_test_drop_load(1) == gtg.GTG_OK
         st = gtg.gemv_bf16(M, N, A.data_ptr(), N, X.data_ptr(), N, Y.data_ptr(), M, 8, s)
         status = gtg.gtg_sync_status(s)
     finally:
