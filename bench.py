@@ -559,10 +559,13 @@ def sweep(dev, stream, peaks, l2):
     gemm_cfg("1: f32 256^3", "f32", 256, 256, 256, A, B, f32_peak, "fp32 simt (2070 MHz)", 200)
     A, B = gemm_uniform_f32(3, 1024, 1024, 1024)
     gemm_cfg("3a: f32 1024^3", "f32", 1024, 1024, 1024, A, B, f32_peak, "fp32 simt (2070 MHz)", 50)
-    gemm_cfg("3a: tf32 1024^3", "tf32", 1024, 1024, 1024, A, B, tf32_peak, "bf16 burst / 2", 100)
+    gemm_cfg("3a: tf32 1024^3", "tf32", 1024, 1024, 1024, A, B, tf32_peak, "bf16 burst / 2 (derived)", 100)
     A, B = gemm_uniform_f32(4, 1000, 700, 1500)
     gemm_cfg("3b: f32 1000x700x1500", "f32", 1000, 700, 1500, A, B, f32_peak, "fp32 simt (2070 MHz)", 50)
-    gemm_cfg("3b: tf32 1000x700x1500", "tf32", 1000, 700, 1500, A, B, tf32_peak, "bf16 burst / 2", 100)
+    gemm_cfg("3b: tf32 1000x700x1500", "tf32", 1000, 700, 1500, A, B, tf32_peak, "bf16 burst / 2 (derived)", 100)
+    A, B = gemm_uniform_f32(3, 8192, 8192, 8192)
+    gemm_cfg("tf32 8192^3", "tf32", 8192, 8192, 8192, A, B, tf32_peak, "bf16 burst / 2 (derived)", 20)
+    del A, B
     (A, B), = gemm_normal_bf16(5, [(4096, 4096, 4096)])
     gemm_cfg("4: bf16 4096^3", "bf16", 4096, 4096, 4096, A, B, bf16_peak, "bf16 burst", 50)
     shapes = [(8192, 8192, 8192), (16384, 4096, 4096)]
@@ -820,6 +823,24 @@ def reference_arm(args, rank, world):
             "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def summary_of(res: dict) -> dict:
+    """One [rate, fraction of peak] pair per configuration of the workload
+    list (GEMM TFLOP/s, GEMV GB/s) plus the in-step GEMV fractions, printed
+    last on the line so that a reader keeping only its tail still has them."""
+    out = {"headline bf16 8192^3 in step": [res.get("value"), res.get("roofline", {}).get("frac")]}
+    gv = res.get("gemv", {})
+    if gv:
+        out["in-step gemv 4096^2 b1 / b8 frac"] = [gv.get("roofline", {}).get("frac"), gv.get("batch8_frac")]
+    for row in res.get("configs", []):
+        name = row.get("config", "")
+        keep = name[:1].isdigit() or name.startswith("f2: bf16-matrix gemv 4096") or name.startswith("tf32 8192")
+        if not keep:
+            continue
+        rate = row.get("TFLOP/s", row.get("GB/s"))
+        out[name.replace("x4096x4096", "x4096^2").replace(" gemv", "")] = [rate, row.get("frac")]
+    return out
+
+
 def main():
     args = parse_args()
     rank = int(os.environ.get("RANK", "0"))
@@ -861,6 +882,7 @@ def main():
     if rank == 0:
         if not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline()
+        res["summary"] = summary_of(res)
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch

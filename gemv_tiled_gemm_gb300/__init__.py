@@ -21,7 +21,10 @@ import os
 import threading
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libgtg.so")
+# GTG_DEBUG=1 loads the checking build (kernels verify every address they
+# compute; see _build.py), made by _build.build(debug=True)
+DEBUG = os.environ.get("GTG_DEBUG") == "1"
+LIB_PATH = os.path.join(_PKG, "libgtg_debug.so" if DEBUG else "libgtg.so")
 
 GTG_OK, GTG_ERR_INVALID_VALUE, GTG_ERR_MISALIGNED, GTG_ERR_ALIAS = 0, 1, 2, 3
 GTG_ERR_UNSUPPORTED, GTG_ERR_LAUNCH, GTG_ERR_TIMEOUT, GTG_ERR_DEVICE = 4, 5, 6, 7
@@ -101,6 +104,7 @@ TESTING_SIGNATURES = {
     "gtg_plan_gemm_tf32_noalloc": (_int, [_i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64,
                                           ctypes.POINTER(GtgPlan)]),
     "gtg_debug_build": (_int, []),
+    "gtg_test_debug_shrink_extent": (_int, [_int]),
 }
 
 
@@ -123,8 +127,9 @@ def lib():
     with _lock:
         if _lib is None:
             if not os.path.exists(LIB_PATH):
-                raise GtgError(-1, f"{LIB_PATH} is missing: build it first "
-                                   "(python -c 'import __graft_entry__ as g; g.build()')")
+                how = ("python -m gemv_tiled_gemm_gb300._build --debug" if DEBUG
+                       else "python -c 'import __graft_entry__ as g; g.build()'")
+                raise GtgError(-1, f"{LIB_PATH} is missing: build it first ({how})")
             handle = ctypes.CDLL(LIB_PATH)
             for name, (res, args) in {**SIGNATURES, **TESTING_SIGNATURES}.items():
                 fn = getattr(handle, name)
@@ -319,6 +324,12 @@ def plan_gemm_tf32_noalloc(M, N, K, A, lda, B, ldb, C, ldc) -> dict:
 
 def gtg_debug_build() -> int:
     return lib().gtg_debug_build()
+
+
+def gtg_test_debug_shrink_extent(elements: int) -> int:
+    """GTG_DEBUG builds (needs GTG_TESTING=1): the GEMV kernels check their loads
+    against an extent `elements` shorter than the matrix, so their checks fire."""
+    return lib().gtg_test_debug_shrink_extent(int(elements))
 
 
 def gtg_version() -> int:

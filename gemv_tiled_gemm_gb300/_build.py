@@ -3,6 +3,13 @@
 Each .cu file compiles in parallel to an object under ``_build/``; the
 objects link into ``gemv_tiled_gemm_gb300/libgtg.so`` against the shared
 CUDA runtime.
+
+``build(debug=True)`` makes the checking variant instead: the same sources
+compiled with GTG_DEBUG defined into ``_build_debug/`` and
+``libgtg_debug.so``. Its index-heavy kernels check every address they compute
+against the extent of its operand and latch GTG_ERR_BOUNDS (skipping the
+access) instead of reading or writing outside it. The package loads it
+instead of libgtg.so when GTG_DEBUG=1 is in the environment.
 """
 
 from __future__ import annotations
@@ -19,6 +26,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgtg.so")
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libgtg_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -37,17 +46,20 @@ def _deps() -> list[str]:
             + glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)])
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(debug: bool = False) -> bool:
+    lib = LIB_DEBUG if debug else LIB
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def _compile(src: str, verbose: bool) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
+def _compile(src: str, verbose: bool, debug: bool) -> str:
+    obj = os.path.join(BUILD_DEBUG if debug else BUILD, os.path.basename(src).replace(".cu", ".o"))
     cmd = [nvcc(), *ARCH, "-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
            "-I", INCLUDE, "-c", src, "-o", obj]
+    if debug:
+        cmd.insert(1, "-DGTG_DEBUG=1")
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -56,23 +68,26 @@ def _compile(src: str, verbose: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile every kernel and the C ABI into libgtg.so; returns its path."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    """Compile every kernel and the C ABI into libgtg.so (libgtg_debug.so with
+    debug=True); returns its path."""
+    lib = LIB_DEBUG if debug else LIB
+    if not force and up_to_date(debug):
+        return lib
+    os.makedirs(BUILD_DEBUG if debug else BUILD, exist_ok=True)
     srcs = sources()
     with ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose), srcs))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, verbose, debug), srcs))
+    tmp = lib + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
            "-Xlinker", "-rpath,$ORIGIN"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force=True, verbose=True))
+    import sys
+    print(build(force=True, verbose=True, debug="--debug" in sys.argv))

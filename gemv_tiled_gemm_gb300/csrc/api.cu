@@ -40,6 +40,7 @@ bool testing_enabled() {
 // that took it there fails with GTG_ERR_LAUNCH before launching anything.
 // GTG_FAULT_INJECT=<n> in the environment arms it once, at the first dispatch.
 std::atomic<long long> g_inject_countdown{0};
+std::atomic<int> g_debug_shrink{0};   // GTG_DEBUG builds: see gtg_test_debug_shrink_extent
 std::once_flag g_inject_env_once;
 
 void read_fault_inject_env() {
@@ -240,6 +241,9 @@ gtg_status run_gemm(const GemmArgs &g, cudaStream_t stream) {
 }
 
 }  // namespace
+
+int debug_shrink_setting() { return g_debug_shrink.load(); }
+
 }  // namespace gtg
 
 using namespace gtg;
@@ -293,6 +297,10 @@ static gtg_status run_gemv(const GemvArgs &g, cudaStream_t stream) {
 static gtg_status plan_noalloc_impl(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
     gtg_status st = plan_gemm_impl(dev, g, plan, false);
     if (st != GTG_OK) return st;
+    // the tensor-core kernel reads the caller's A through TMA (16-byte base and
+    // rows); gemm_tf32 would copy another layout, which needs pool memory
+    const bool a_tma = (reinterpret_cast<uintptr_t>(g.A) & 15) == 0 && (g.lda * 4) % 16 == 0;
+    if (plan->kernel == GTG_KERNEL_TCGEN05 && !a_tma) simt_plan(dev, g, plan);
     if (plan->kernel == GTG_KERNEL_TCGEN05) {
         tc_plan_unsplit_single(dev, g, plan);
     } else if (plan->kernel == GTG_KERNEL_SIMT && plan->splits > 1) {
@@ -688,6 +696,17 @@ gtg_status gtg_test_inject_launch_failure(int n) {
 }
 
 uint64_t gtg_test_workspace_allocations(void) { return ws_alloc_count(); }
+
+gtg_status gtg_test_debug_shrink_extent(int elements) {
+#ifdef GTG_DEBUG
+    if (!testing_enabled()) return GTG_ERR_UNSUPPORTED;
+    g_debug_shrink.store(elements > 0 ? elements : 0);
+    return GTG_OK;
+#else
+    (void)elements;
+    return GTG_ERR_UNSUPPORTED;
+#endif
+}
 
 int gtg_debug_build(void) {
 #ifdef GTG_DEBUG

@@ -84,15 +84,20 @@ struct SimtTile {
     static_assert(A_V4 >= 1 && B_V4 >= 1, "tile too small for its thread count");
 };
 
-// Split K: with gridDim.z = S > 1 the CTA at blockIdx.z = z multiplies the
-// K range [z * k_per, (z + 1) * k_per) and writes its FP32 partial product to
-// the workspace slice ws + z * M * N (leading dimension N) instead of C;
-// split_reduce_kernel then adds the S slices in order z = 0 .. S-1.
+// gridDim.z has one of two meanings.
+// Strided batch (batched != 0): the CTA at blockIdx.z = b multiplies item b,
+// whose operands and output start sA, sB, sC elements after those of item 0;
+// every item of the batch runs in this one launch.
+// Split K (batched == 0, gridDim.z = S > 1): the CTA at blockIdx.z = z
+// multiplies the K range [z * k_per, (z + 1) * k_per) and writes its FP32
+// partial product to the workspace slice ws + z * M * N (leading dimension N)
+// instead of C; split_reduce_kernel then adds the S slices in order z = 0 .. S-1.
 template <typename T, int BM, int BN, bool VEC, int TN, int TM>
 __global__ void __launch_bounds__(SimtTile<T, BM, BN, VEC, TN, TM>::THREADS)
     simt_gemm_kernel(int M, int N, int K, const T *__restrict__ A, long long lda,
                      const T *__restrict__ B, long long ldb, float *__restrict__ C, long long ldc,
-                     int c_vec, int k_per, float *__restrict__ ws, const float *__restrict__ bias, int act) {
+                     int c_vec, int k_per, float *__restrict__ ws, const float *__restrict__ bias, int act,
+                     int batched, long long sA, long long sB, long long sC) {
     using L = SimtTile<T, BM, BN, VEC, TN, TM>;
     constexpr int QN = TN / 2;   // column pairs per thread
     constexpr int PM = TM / 2;   // row pairs per thread
@@ -100,7 +105,11 @@ __global__ void __launch_bounds__(SimtTile<T, BM, BN, VEC, TN, TM>::THREADS)
     // a following dependent launch (the split reduction) may be scheduled now;
     // it waits for this grid before reading anything this grid writes
     ptx::allow_next_grid();
-    if (gridDim.z > 1) {
+    if (batched) {
+        A += blockIdx.z * sA;
+        B += blockIdx.z * sB;
+        C += blockIdx.z * sC;
+    } else if (gridDim.z > 1) {
         bias = nullptr;   // partial products: the reduction applies the epilogue
         act = 0;
         const int z = blockIdx.z;
@@ -337,8 +346,25 @@ __global__ void zero_fill_kernel(float *C, long long M, long long N, long long l
 template <typename T, int BM, int BN, bool VEC, int TN, int TM = 8>
 cudaError_t launch_one(const GemmArgs &g, int splits, cudaStream_t stream) {
     using L = SimtTile<T, BM, BN, VEC, TN, TM>;
-    dim3 grid(static_cast<unsigned>((g.N + BN - 1) / BN), static_cast<unsigned>((g.M + BM - 1) / BM),
-              static_cast<unsigned>(splits));
+    const dim3 tiles(static_cast<unsigned>((g.N + BN - 1) / BN), static_cast<unsigned>((g.M + BM - 1) / BM));
+    if (g.batch > 1) {
+        // a strided batch: every item in one launch (blockIdx.z), in chunks of
+        // at most 65535 items (the grid's z limit); no K split
+        const int c_vec = ((reinterpret_cast<uintptr_t>(g.C) & 15) == 0 && (g.ldc & 3) == 0 && (g.strideC & 3) == 0)
+                              ? 1 : 0;
+        for (int64_t b0 = 0; b0 < g.batch; b0 += 65535) {
+            const dim3 grid(tiles.x, tiles.y, static_cast<unsigned>(std::min<int64_t>(g.batch - b0, 65535)));
+            simt_gemm_kernel<T, BM, BN, VEC, TN, TM><<<grid, L::THREADS, 0, stream>>>(
+                static_cast<int>(g.M), static_cast<int>(g.N), static_cast<int>(g.K),
+                static_cast<const T *>(g.A) + b0 * g.strideA, g.lda, static_cast<const T *>(g.B) + b0 * g.strideB,
+                g.ldb, g.C + b0 * g.strideC, g.ldc, c_vec, 0, nullptr, g.bias, g.act, 1, g.strideA, g.strideB,
+                g.strideC);
+            const cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
+    const dim3 grid(tiles.x, tiles.y, static_cast<unsigned>(splits));
     const int c_vec = ((reinterpret_cast<uintptr_t>(g.C) & 15) == 0 && (g.ldc & 3) == 0) ? 1 : 0;
     const int k_per = static_cast<int>(((g.K + kBK - 1) / kBK + splits - 1) / splits * kBK);
     float *ws = nullptr;
@@ -350,7 +376,7 @@ cudaError_t launch_one(const GemmArgs &g, int splits, cudaStream_t stream) {
     simt_gemm_kernel<T, BM, BN, VEC, TN, TM><<<grid, L::THREADS, 0, stream>>>(
         static_cast<int>(g.M), static_cast<int>(g.N), static_cast<int>(g.K),
         static_cast<const T *>(g.A), g.lda, static_cast<const T *>(g.B), g.ldb, g.C, g.ldc, c_vec, k_per, ws,
-        g.bias, g.act);
+        g.bias, g.act, 0, 0, 0, 0);
     e = cudaGetLastError();
     if (splits > 1) {
         if (e == cudaSuccess) e = split_reduce_launch(ws, splits, g.M, g.N, g.C, g.ldc, g.bias, g.act, stream);
@@ -368,10 +394,11 @@ cudaError_t launch_typed(const GemmArgs &g, const gtg_plan &plan, cudaStream_t s
 }
 
 bool vec_ok(const GemmArgs &g) {
-    // 4 consecutive elements per load: 16 bytes for FP32, 8 for BF16 / FP16.
+    // 4 consecutive elements per load: 16 bytes for FP32, 8 for BF16 / FP16;
+    // in a batch every item keeps the alignment of the first
     const uintptr_t mask = (g.prec == GTG_PREC_BF16 || g.prec == GTG_PREC_F16) ? 7 : 15;
     return (reinterpret_cast<uintptr_t>(g.A) & mask) == 0 && (reinterpret_cast<uintptr_t>(g.B) & mask) == 0 &&
-           (g.lda % 4) == 0 && (g.ldb % 4) == 0;
+           (g.lda % 4) == 0 && (g.ldb % 4) == 0 && (g.batch == 1 || ((g.strideA % 4) == 0 && (g.strideB % 4) == 0));
 }
 
 }  // namespace
@@ -389,7 +416,10 @@ bool vec_ok(const GemmArgs &g) {
 // fast or faster on every small shape tried (256^3 to 2048^3, 1000 x 700 x
 // 1500, 1024^2 x 4096).
 void simt_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
-    const int64_t big_tiles = ((g.M + 127) / 128) * ((g.N + 127) / 128);
+    // a strided batch runs all its items in one launch: tiles count over the
+    // whole batch, and K is never split (the items fill the GPU instead)
+    const int64_t items = std::max<int64_t>(g.batch, 1);
+    const int64_t big_tiles = items * ((g.M + 127) / 128) * ((g.N + 127) / 128);
     const int64_t kslices = (g.K + kBK - 1) / kBK;
     const bool big = big_tiles >= dev.sms;
     plan->kernel = GTG_KERNEL_SIMT;
@@ -397,7 +427,7 @@ void simt_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
     plan->smem = 0;
     plan->cluster = 1;
     plan->stages = 2;   // double-buffered shared-memory slices
-    if (!big && big_tiles > 0) {
+    if (!big && big_tiles > 0 && items == 1) {
         int64_t fill = std::min<int64_t>(dev.sms / big_tiles, kslices / 32);
         if (fill >= 2 && 4 * big_tiles * fill >= 3 * dev.sms) {
             const int64_t k_per = (kslices + fill - 1) / fill;   // every split owns K slices
@@ -417,15 +447,15 @@ void simt_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
         // wave count says so (measured, FP32: 8192^2 x 4096 46.4 -> 50.0,
         // 3000^3 43.9 -> 47.0, 4096 x 2048 x 4096 39.3 -> 43.5 TFLOP/s; kept at
         // 128 x 128 for 4096^3 and 2560^2 x 2048, where they were slower)
-        const int64_t t256 = ((g.M + 255) / 256) * ((g.N + 127) / 128);
-        const int64_t t128 = ((g.M + 127) / 128) * ((g.N + 127) / 128);
+        const int64_t t256 = items * ((g.M + 255) / 256) * ((g.N + 127) / 128);
+        const int64_t t128 = items * ((g.M + 127) / 128) * ((g.N + 127) / 128);
         const double w256 = static_cast<double>((t256 + dev.sms - 1) / dev.sms) * 2.0 / 1.08;
         const double w128 = static_cast<double>((t128 + dev.sms - 1) / dev.sms);
         if (t256 >= dev.sms && w256 < w128) plan->bm = 256;
     }
-    const int64_t tiles = ((g.M + plan->bm - 1) / plan->bm) * ((g.N + plan->bn - 1) / plan->bn);
+    const int64_t tiles = items * ((g.M + plan->bm - 1) / plan->bm) * ((g.N + plan->bn - 1) / plan->bn);
     int64_t splits = 1;
-    if (!big) {
+    if (!big && items == 1) {
         // the busiest SM's K work: ceil(CTAs / SMs) CTAs of ceil(slices / S)
         // slices each; a split must save more than a fixed allowance for the
         // extra partial-product traffic and the reduction launch
@@ -452,24 +482,13 @@ void simt_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
 cudaError_t simt_launch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan,
                         cudaStream_t stream) {
     (void)dev;
-    const int64_t elem = (g.prec == GTG_PREC_BF16 || g.prec == GTG_PREC_F16) ? 2 : 4;
-    for (int64_t b = 0; b < g.batch; ++b) {   // a strided batch runs item by item
-        GemmArgs gb = g;
-        gb.A = static_cast<const char *>(g.A) + b * g.strideA * elem;
-        gb.B = static_cast<const char *>(g.B) + b * g.strideB * elem;
-        gb.C = g.C + b * g.strideC;
-        gb.batch = 1;
-        const bool vec = vec_ok(gb);
-        cudaError_t e;
-        if (g.prec == GTG_PREC_BF16)
-            e = vec ? launch_typed<uint16_t, true>(gb, plan, stream) : launch_typed<uint16_t, false>(gb, plan, stream);
-        else if (g.prec == GTG_PREC_F16)
-            e = vec ? launch_typed<__half, true>(gb, plan, stream) : launch_typed<__half, false>(gb, plan, stream);
-        else
-            e = vec ? launch_typed<float, true>(gb, plan, stream) : launch_typed<float, false>(gb, plan, stream);
-        if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
+    // a strided batch is one launch over all items (blockIdx.z), see launch_one
+    const bool vec = vec_ok(g);
+    if (g.prec == GTG_PREC_BF16)
+        return vec ? launch_typed<uint16_t, true>(g, plan, stream) : launch_typed<uint16_t, false>(g, plan, stream);
+    if (g.prec == GTG_PREC_F16)
+        return vec ? launch_typed<__half, true>(g, plan, stream) : launch_typed<__half, false>(g, plan, stream);
+    return vec ? launch_typed<float, true>(g, plan, stream) : launch_typed<float, false>(g, plan, stream);
 }
 
 cudaError_t epilogue_fill_launch(float *C, int64_t M, int64_t N, int64_t ldc, const float *bias, int per_column,

@@ -27,6 +27,18 @@
 // writes B^T (N x K, K-major) into a temporary buffer taken from the
 // device's stream-ordered memory pool, and both operands are then K-major.
 //
+// TF32 rounding: the TF32 MMA ignores the 13 low mantissa bits of its FP32
+// operands (truncation, up to 2^-10 relative per operand, which with both
+// operands reaches the 4 * 2^-11 * sum|a*b| error bound). So both operands
+// are rounded to the nearest TF32 value first, by one preparation kernel that
+// writes B^T and a rounded copy of A (16-byte rows, so any layout of A
+// works) into pool buffers. The entry point without allocation has no room
+// for the copy of A: its single-CTA kernel (ROUND_A) rounds each A tile in
+// shared memory instead, with four converter warps between the tile's TMA
+// load and the MMAs that read it. (Measured: that extra wait per K slice cost
+// the CTA-pair kernel more than half its rate -- TF32 8192^3 950 -> 330
+// TFLOP/s -- where the copy of A costs one more pass over A in HBM.)
+//
 // Every mbarrier wait is bounded in time. On expiry the waiting thread
 // latches GTG_ERR_TIMEOUT in the library status word, raises a shared abort
 // flag that makes the other roles stop, waits (bounded) for its own copies
@@ -45,6 +57,8 @@ namespace gtg {
 namespace {
 
 constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2-5 epilogue
+constexpr int kConvWarps = 4;  // ROUND_A kernels: warps 6-9 round A tiles to TF32 in shared memory
+__host__ __device__ constexpr int threads_for(bool round_a) { return round_a ? kThreads + 32 * kConvWarps : kThreads; }
 constexpr int kBM = 128;
 constexpr int kGroup = 16;     // row-tiles per raster group
 constexpr int kSmemBudget = 200 * 1024;
@@ -67,7 +81,7 @@ struct Shape {
     static constexpr int STAGES_RAW = kSmemBudget / STAGE_BYTES;
     static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
     static constexpr int TMEM_COLS = 2 * BN;       // two FP32 accumulators
-    static constexpr int NBARS = 2 * STAGES + 5;
+    static constexpr int NBARS = (TF32 ? 3 : 2) * STAGES + 5;   // TF32: a "converted" barrier per stage
     static constexpr int SMEM = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + NBARS * 8 + 16;
     static constexpr uint32_t IDESC = ptx::make_idesc(TF32 ? 2u : 1u, 0u, B_KMAJOR ? 0u : 1u, BM, BN);
     static_assert(BN % BCH_N == 0 && BN >= 64 && BN <= 256, "tile width");
@@ -182,14 +196,44 @@ __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, const TcP
     }
 }
 
+// Rounds BYTES of FP32 values in shared memory at `addr` to TF32 in place
+// (one warp; every lane loads all its 16-byte pieces first, then rounds and
+// stores them), then orders the writes before the tensor cores' reads.
+template <int BYTES>
+__device__ __forceinline__ void round_tile_tf32(uint32_t addr, int lane) {
+    constexpr int kPieces = BYTES / (32 * 16);
+    static_assert(kPieces * 32 * 16 == BYTES, "whole 512-byte passes");
+    uint4 v[kPieces];
+#pragma unroll
+    for (int i = 0; i < kPieces; ++i) v[i] = ptx::ld_shared_v4(addr + (i * 32 + lane) * 16);
+#pragma unroll
+    for (int i = 0; i < kPieces; ++i)
+        ptx::st_shared_v4(addr + (i * 32 + lane) * 16, ptx::tf32_round(v[i].x), ptx::tf32_round(v[i].y),
+                          ptx::tf32_round(v[i].z), ptx::tf32_round(v[i].w));
+    ptx::fence_proxy_async_smem();
+}
+
+// A bounded wait that every lane of a warp makes and that ends the same way
+// for all of them (so that the warp never diverges on an abort).
+__device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                              const TcParams &p) {
+    const bool ok = wait_bar(bar, parity, abort_flag, p);
+    return __all_sync(0xFFFFFFFFu, ok);
+}
+
 // IM2COL: A is not a matrix in memory but the patch matrix of a convolution
 // (rows = output pixels in (n, oh, ow) order, K = (kh, kw, channel)); each
 // 128 x 64 A tile is one TMA im2col load of 128 output pixels' 64 channels
 // at one window tap, straight from the channels-last image.
-template <bool TF32, int BN, bool IM2COL = false>
-__global__ void __launch_bounds__(kThreads, 1)
+//
+// ROUND_A (TF32 only, the entry point without allocation): A is the caller's
+// matrix, not yet rounded; warps 6-9 round each A tile in shared memory to
+// TF32 before the MMAs of its stage may read it.
+template <bool TF32, int BN, bool IM2COL = false, bool ROUND_A = false>
+__global__ void __launch_bounds__(threads_for(ROUND_A), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const TcParams p) {
+    static_assert(!ROUND_A || TF32, "only TF32 operands are rounded");
     using S = Shape<TF32, BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -201,12 +245,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     const uint32_t bar0 = ptx::smem_addr(bars);
     // barrier map: full[s] = s, empty[s] = STAGES + s, acc_full[a] = 2*STAGES + a,
-    // acc_empty[a] = 2*STAGES + 2 + a, drain = 2*STAGES + 4
+    // acc_empty[a] = 2*STAGES + 2 + a, drain = 2*STAGES + 4, TF32: conv[s] = 2*STAGES + 5 + s
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (S::STAGES + s); };
     auto accf_bar = [&](int a) { return bar0 + 8u * (2 * S::STAGES + a); };
     auto acce_bar = [&](int a) { return bar0 + 8u * (2 * S::STAGES + 2 + a); };
     const uint32_t drain_bar = bar0 + 8u * (2 * S::STAGES + 4);
+    auto conv_bar = [&](int s) { return bar0 + 8u * (2 * S::STAGES + 5 + s); };
+    // the MMAs of a stage wait for its A tile rounded (ROUND_A) or just loaded
+    auto ready_bar = [&](int s) { return ROUND_A ? conv_bar(s) : full_bar(s); };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -215,6 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < S::STAGES; ++s) {
             ptx::mbar_init(full_bar(s), 1);
             ptx::mbar_init(empty_bar(s), 1);
+            if constexpr (ROUND_A) ptx::mbar_init(conv_bar(s), kConvWarps);
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(accf_bar(a), 1);
@@ -314,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
                     const int s = static_cast<int>(it % S::STAGES);
                     const uint32_t ph = (it / S::STAGES) & 1u;
-                    if (!wait_bar(full_bar(s), ph, abort_flag, p)) {
+                    if (!wait_bar(ready_bar(s), ph, abort_flag, p)) {
                         ok = false;
                         break;
                     }
@@ -349,6 +397,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // nothing may still be writing TMEM when it is released
                 ptx::mma_commit(drain_bar);
                 wait_drain(drain_bar, 0u, p);
+            }
+        }
+    } else if (warp >= 6) {
+        // ------------------------------------------------ ROUND_A: A tiles rounded in place (warps 6-9)
+        if constexpr (ROUND_A) {
+            constexpr int kPart = S::A_BYTES / kConvWarps;
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.num_units; t += gridDim.x) {
+                const Unit u = unit_of(t, p);
+                for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
+                    const int s = static_cast<int>(it % S::STAGES);
+                    const uint32_t ph = (it / S::STAGES) & 1u;
+                    if (!warp_wait_bar(full_bar(s), ph, abort_flag, p)) {
+                        ok = false;
+                        break;
+                    }
+                    round_tile_tf32<kPart>(sA + s * S::A_BYTES + (warp - 6) * kPart, lane);
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(conv_bar(s));
+                }
             }
         }
     } else {
@@ -737,24 +806,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::cluster_sync();
 }
 
+__device__ __forceinline__ float tf32_rounded(float v) { return __uint_as_float(ptx::tf32_round(__float_as_uint(v))); }
+
 // B (K x N, leading dimension ldb) -> Bt (N x K, leading dimension ldbt, a
-// multiple of 4), through a 64 x 64 shared-memory tile. VEC: B's rows are
+// multiple of 4) with every value rounded to the nearest TF32 value (the
+// operand the TF32 MMA reads), through a 64 x 64 shared-memory tile. VEC: B's rows are
 // 16-byte aligned (base and ldb), so every thread moves 16-byte pieces both
 // ways (a row of B or Bt is 16 of them per tile); edges of the matrix take
 // single elements. blockIdx.z walks the items of a batch (strideB apart in
 // B, N * ldbt apart in Bt).
+// One 64 x 64 tile of B^T: rows n0.. of Bt, columns k0.. (a whole CTA of 256
+// threads; every thread reaches both barriers).
 template <bool VEC>
-__global__ void __launch_bounds__(256) transpose_kernel(const float *__restrict__ B, long long ldb,
-                                                        float *__restrict__ Bt, long long ldbt, int K, int N,
-                                                        long long strideB) {
-    __shared__ float tile[64][65];
-    // the GEMM that reads Bt is a dependent launch: it may be scheduled now and
-    // set itself up, and it waits for this grid before touching Bt
-    ptx::allow_next_grid();
-    B += blockIdx.z * strideB;
-    Bt += blockIdx.z * static_cast<long long>(N) * ldbt;
-    const int n0 = blockIdx.x * 64;
-    for (int k0 = blockIdx.y * 64; k0 < K; k0 += gridDim.y * 64) {
+__device__ __forceinline__ void transpose_tile(const float *__restrict__ B, long long ldb, float *__restrict__ Bt,
+                                               long long ldbt, int K, int N, int n0, int k0, float (&tile)[64][65],
+                                               int *status) {
+#ifdef GTG_DEBUG
+    // this item's B (K rows of ldb) and Bt (N rows of ldbt)
+    const float *b_hi = B + (static_cast<long long>(K) - 1) * ldb + N, *bt_hi = Bt + static_cast<long long>(N) * ldbt;
+#endif
+    (void)status;
+    {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int idx = static_cast<int>(threadIdx.x) + 256 * i;
@@ -763,7 +835,7 @@ __global__ void __launch_bounds__(256) transpose_kernel(const float *__restrict_
             float v[4] = {0.f, 0.f, 0.f, 0.f};
             if (k < K) {
                 const float *src = B + static_cast<long long>(k) * ldb + n;
-                if (VEC && n + 3 < N) {
+                if (VEC && n + 3 < N && GTG_DEBUG_IN(src, 16, B, b_hi, status)) {
                     const float4 q = __ldg(reinterpret_cast<const float4 *>(src));
                     v[0] = q.x;
                     v[1] = q.y;
@@ -772,7 +844,7 @@ __global__ void __launch_bounds__(256) transpose_kernel(const float *__restrict_
                 } else {
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        if (n + j < N) v[j] = __ldg(src + j);
+                        if (n + j < N && GTG_DEBUG_IN(src + j, 4, B, b_hi, status)) v[j] = __ldg(src + j);
                 }
             }
 #pragma unroll
@@ -784,14 +856,17 @@ __global__ void __launch_bounds__(256) transpose_kernel(const float *__restrict_
             const int idx = static_cast<int>(threadIdx.x) + 256 * i;
             const int r = idx >> 4, c = (idx & 15) * 4;   // row n0 + r of Bt, columns k0 + c .. + 3
             const int n = n0 + r, k = k0 + c;
-            if (n < N) {
+            if (n < N && k < K) {
                 float *dst = Bt + static_cast<long long>(n) * ldbt + k;
-                if (k + 3 < K) {
-                    *reinterpret_cast<float4 *>(dst) = make_float4(tile[c][r], tile[c + 1][r], tile[c + 2][r], tile[c + 3][r]);
+                if (!GTG_DEBUG_IN(dst, 4ull * min(4, K - k), Bt, bt_hi, status)) {
+                } else if (k + 3 < K) {
+                    *reinterpret_cast<float4 *>(dst) = make_float4(tf32_rounded(tile[c][r]), tf32_rounded(tile[c + 1][r]),
+                                                                   tf32_rounded(tile[c + 2][r]),
+                                                                   tf32_rounded(tile[c + 3][r]));
                 } else {
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        if (k + j < K) dst[j] = tile[c + j][r];
+                        if (k + j < K) dst[j] = tf32_rounded(tile[c + j][r]);
                 }
             }
         }
@@ -799,16 +874,136 @@ __global__ void __launch_bounds__(256) transpose_kernel(const float *__restrict_
     }
 }
 
+template <bool VEC>
+__global__ void __launch_bounds__(256) transpose_kernel(const float *__restrict__ B, long long ldb,
+                                                        float *__restrict__ Bt, long long ldbt, int K, int N,
+                                                        long long strideB, int *status) {
+    __shared__ float tile[64][65];
+    // the GEMM that reads Bt is a dependent launch: it may be scheduled now and
+    // set itself up, and it waits for this grid before touching Bt
+    ptx::allow_next_grid();
+    B += blockIdx.z * strideB;
+    Bt += blockIdx.z * static_cast<long long>(N) * ldbt;
+    for (int k0 = blockIdx.y * 64; k0 < K; k0 += gridDim.y * 64)
+        transpose_tile<VEC>(B, ldb, Bt, ldbt, K, N, blockIdx.x * 64, k0, tile, status);
+}
+
+// Both TF32 operands prepared by one launch: blocks [0, tiles_n * tiles_k)
+// each write one 64 x 64 tile of B^T, the others copy rows of A into A'
+// (rows of ldk >= K elements, zero past K, 16-byte aligned, so that any
+// layout of A works), every value rounded to the nearest TF32 value.
+// blockIdx.y walks the items of a batch; an operand shared by every item
+// (item stride 0) is prepared once (items_a or items_b = 1).
+struct Tf32Prep {
+    const float *A;
+    long long lda, strideA;
+    float *Ap;
+    long long ldk;          // row stride of A' and B^T
+    int items_a;
+    const float *B;
+    long long ldb, strideB;
+    float *Bt;
+    int items_b;
+    int M, N, K;
+    int tiles_n, tiles_k;   // 64 x 64 tiles of B^T per item
+    int a_vec;              // A's base and rows are 16-byte aligned
+    int *status;
+};
+
+template <bool VEC_B>
+__global__ void __launch_bounds__(256) tf32_prep_kernel(const Tf32Prep q) {
+    __shared__ float tile[64][65];
+    ptx::allow_next_grid();   // the GEMM is a dependent launch; it waits for this grid
+    const int item = static_cast<int>(blockIdx.y);
+    const int tb = q.tiles_n * q.tiles_k;
+    if (static_cast<int>(blockIdx.x) < tb) {
+        if (item >= q.items_b) return;   // the whole CTA: no barrier is left behind
+        const int t = static_cast<int>(blockIdx.x);
+        transpose_tile<VEC_B>(q.B + item * q.strideB, q.ldb, q.Bt + static_cast<long long>(item) * q.N * q.ldk, q.ldk,
+                              q.K, q.N, (t % q.tiles_n) * 64, (t / q.tiles_n) * 64, tile, q.status);
+        return;
+    }
+    if (item >= q.items_a) return;
+    const float *A = q.A + item * q.strideA;
+    float *Ap = q.Ap + static_cast<long long>(item) * q.M * q.ldk;
+#ifdef GTG_DEBUG
+    const float *a_hi = A + (static_cast<long long>(q.M) - 1) * q.lda + q.K;
+    const float *ap_hi = Ap + static_cast<long long>(q.M) * q.ldk;
+#endif
+    const long long per_row = q.ldk / 4;   // 16-byte groups of a row of A'
+    const long long groups = static_cast<long long>(q.M) * per_row;
+    const long long nblk = static_cast<long long>(gridDim.x) - tb;
+    for (long long i = (static_cast<long long>(blockIdx.x) - tb) * 256 + threadIdx.x; i < groups; i += nblk * 256) {
+        const long long r = i / per_row;
+        const int c = static_cast<int>(i - r * per_row) * 4;
+        const float *src = A + r * q.lda + c;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        if (q.a_vec && c + 3 < q.K && GTG_DEBUG_IN(src, 16, A, a_hi, q.status)) {
+            const float4 t = __ldg(reinterpret_cast<const float4 *>(src));
+            v[0] = t.x;
+            v[1] = t.y;
+            v[2] = t.z;
+            v[3] = t.w;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (c + j < q.K && GTG_DEBUG_IN(src + j, 4, A, a_hi, q.status)) v[j] = __ldg(src + j);
+        }
+        float *dst = Ap + r * q.ldk + c;
+        if (GTG_DEBUG_IN(dst, 16, Ap, ap_hi, q.status))
+            *reinterpret_cast<float4 *>(dst) = make_float4(tf32_rounded(v[0]), tf32_rounded(v[1]), tf32_rounded(v[2]),
+                                                           tf32_rounded(v[3]));
+    }
+}
+
 // Bt = B^T on `stream` (the TF32 kernels' K-major copy of B).
 cudaError_t transpose_launch(const float *B, int64_t ldb, float *Bt, int64_t ldbt, int64_t K, int64_t N,
-                             int64_t batch, int64_t strideB, cudaStream_t stream) {
+                             int64_t batch, int64_t strideB, int *status, cudaStream_t stream) {
     const dim3 grid(static_cast<unsigned>((N + 63) / 64), static_cast<unsigned>(std::min<int64_t>((K + 63) / 64, 65535)),
                     static_cast<unsigned>(batch));
     const bool vec = (reinterpret_cast<uintptr_t>(B) & 15) == 0 && (ldb & 3) == 0 && (batch == 1 || (strideB & 3) == 0);
     if (vec)
-        transpose_kernel<true><<<grid, 256, 0, stream>>>(B, ldb, Bt, ldbt, static_cast<int>(K), static_cast<int>(N), strideB);
+        transpose_kernel<true><<<grid, 256, 0, stream>>>(B, ldb, Bt, ldbt, static_cast<int>(K), static_cast<int>(N), strideB,
+                                                         status);
     else
-        transpose_kernel<false><<<grid, 256, 0, stream>>>(B, ldb, Bt, ldbt, static_cast<int>(K), static_cast<int>(N), strideB);
+        transpose_kernel<false><<<grid, 256, 0, stream>>>(B, ldb, Bt, ldbt, static_cast<int>(K), static_cast<int>(N), strideB,
+                                                          status);
+    return cudaGetLastError();
+}
+
+// Both TF32 operands on `stream`, one launch (see tf32_prep_kernel).
+cudaError_t tf32_prep_launch(const DeviceInfo &dev, const GemmArgs &g, float *Ap, float *Bt, int64_t ldk,
+                             int64_t items_a, int64_t items_b, cudaStream_t stream) {
+    Tf32Prep q;
+    q.A = static_cast<const float *>(g.A);
+    q.lda = g.lda;
+    q.strideA = g.strideA;
+    q.Ap = Ap;
+    q.ldk = ldk;
+    q.items_a = static_cast<int>(items_a);
+    q.B = static_cast<const float *>(g.B);
+    q.ldb = g.ldb;
+    q.strideB = g.strideB;
+    q.Bt = Bt;
+    q.items_b = static_cast<int>(items_b);
+    q.M = static_cast<int>(g.M);
+    q.N = static_cast<int>(g.N);
+    q.K = static_cast<int>(g.K);
+    q.tiles_n = static_cast<int>((g.N + 63) / 64);
+    q.tiles_k = static_cast<int>((g.K + 63) / 64);
+    q.a_vec = (reinterpret_cast<uintptr_t>(g.A) & 15) == 0 && (g.lda & 3) == 0 && (items_a == 1 || (g.strideA & 3) == 0);
+    q.status = dev.status;
+    const int64_t tb = static_cast<int64_t>(q.tiles_n) * q.tiles_k;
+    const int64_t a_groups = g.M * (ldk / 4);
+    const int64_t a_blocks = std::max<int64_t>(1, std::min<int64_t>((a_groups + 255) / 256, 8ll * dev.sms));
+    if (tb + a_blocks > INT32_MAX || std::max(items_a, items_b) > 65535) return cudaErrorInvalidValue;
+    const dim3 grid(static_cast<unsigned>(tb + a_blocks), static_cast<unsigned>(std::max(items_a, items_b)));
+    const bool vec_b = (reinterpret_cast<uintptr_t>(g.B) & 15) == 0 && (g.ldb & 3) == 0 &&
+                       (items_b == 1 || (g.strideB & 3) == 0);
+    if (vec_b)
+        tf32_prep_kernel<true><<<grid, 256, 0, stream>>>(q);
+    else
+        tf32_prep_kernel<false><<<grid, 256, 0, stream>>>(q);
     return cudaGetLastError();
 }
 
@@ -818,11 +1013,15 @@ cudaError_t transpose_launch(const float *B, int64_t ldb, float *Bt, int64_t ldb
 template <typename E>
 __global__ void __launch_bounds__(256) repack_rows_kernel(const E *__restrict__ src, long long lds, long long sstride,
                                                          E *__restrict__ dst, long long ldd, long long rows,
-                                                         long long cols) {
+                                                         long long cols, int *status) {
     ptx::allow_next_grid();   // the GEMM reading dst waits for this grid
     // blockIdx.y: item of a batch (sstride apart in src, rows * ldd apart in dst)
     src += blockIdx.y * sstride;
     dst += blockIdx.y * rows * ldd;
+#ifdef GTG_DEBUG
+    const E *s_hi = src + (rows - 1) * lds + cols, *d_hi = dst + rows * ldd;
+#endif
+    (void)status;
     // a thread gathers one 16-byte group of a destination row (ldd is a
     // multiple of the group, so every group store is aligned) with element
     // loads, which any source alignment allows; past `cols` it writes zeros
@@ -837,22 +1036,23 @@ __global__ void __launch_bounds__(256) repack_rows_kernel(const E *__restrict__ 
         } u;
         const E *s = src + r * lds + c0;
 #pragma unroll
-        for (int j = 0; j < V; ++j) u.e[j] = c0 + j < cols ? s[j] : E(0);
-        *reinterpret_cast<uint4 *>(dst + r * ldd + c0) = u.v;
+        for (int j = 0; j < V; ++j)
+            u.e[j] = c0 + j < cols && GTG_DEBUG_IN(s + j, sizeof(E), src, s_hi, status) ? s[j] : E(0);
+        if (GTG_DEBUG_IN(dst + r * ldd + c0, 16, dst, d_hi, status)) *reinterpret_cast<uint4 *>(dst + r * ldd + c0) = u.v;
     }
 }
 
 cudaError_t repack_launch(const void *src, int64_t lds, int64_t sstride, void *dst, int64_t ldd, int64_t rows,
-                          int64_t cols, int64_t items, int64_t elem, cudaStream_t stream) {
+                          int64_t cols, int64_t items, int64_t elem, int *status, cudaStream_t stream) {
     const long long total = rows * ((cols + 16 / elem - 1) / (16 / elem));
     const dim3 grid(static_cast<unsigned>(std::min<long long>((total + 255) / 256, 8192)),
                     static_cast<unsigned>(items));
     if (elem == 4)
         repack_rows_kernel<float><<<grid, 256, 0, stream>>>(static_cast<const float *>(src), lds, sstride,
-                                                            static_cast<float *>(dst), ldd, rows, cols);
+                                                            static_cast<float *>(dst), ldd, rows, cols, status);
     else
         repack_rows_kernel<uint16_t><<<grid, 256, 0, stream>>>(static_cast<const uint16_t *>(src), lds, sstride,
-                                                               static_cast<uint16_t *>(dst), ldd, rows, cols);
+                                                               static_cast<uint16_t *>(dst), ldd, rows, cols, status);
     return cudaGetLastError();
 }
 
@@ -1010,11 +1210,11 @@ AttrCache &attr_cache() {
 // scheduled while the previous kernel in the stream finishes; the kernel
 // itself waits for that kernel before touching global memory.
 template <typename Kern>
-cudaError_t launch_pdl(Kern kern, int grid, int smem, cudaStream_t stream, const CUtensorMap &ta,
+cudaError_t launch_pdl(Kern kern, int grid, int threads, int smem, cudaStream_t stream, const CUtensorMap &ta,
                        const CUtensorMap &tb, const TcParams &p) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -1042,20 +1242,9 @@ cudaError_t launch_impl(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
     }
     CUtensorMap ta, tb;
     if (!encode_3d(&ta, g.prec, g.A, g.K, g.M, g.lda, g.batch, g.strideA, S::BK, S::BM)) return cudaErrorInvalidValue;
-    float *bt = nullptr;
     if constexpr (S::B_KMAJOR) {
-        const int64_t ldbt = (g.K + 3) / 4 * 4;   // 16-byte rows for the tensor map
-        cudaError_t e = ws_alloc(reinterpret_cast<void **>(&bt), static_cast<size_t>(g.batch * g.N * ldbt) * 4, stream);
-        if (e != cudaSuccess) return e;
-        if ((e = transpose_launch(static_cast<const float *>(g.B), g.ldb, bt, ldbt, g.K, g.N, g.batch, g.strideB,
-                                  stream)) != cudaSuccess) {
-            cudaFreeAsync(bt, stream);
-            return e;
-        }
-        if (!encode_3d(&tb, g.prec, bt, g.K, g.N, ldbt, g.batch, g.N * ldbt, S::BK, BN)) {
-            cudaFreeAsync(bt, stream);
-            return cudaErrorInvalidValue;
-        }
+        // TF32: g.B is already B^T (N x K, rounded), written by the preparation kernel
+        if (!encode_3d(&tb, g.prec, g.B, g.K, g.N, g.ldb, g.batch, g.strideB, S::BK, BN)) return cudaErrorInvalidValue;
     } else {
         if (!encode_3d(&tb, g.prec, g.B, g.N, g.K, g.ldb, g.batch, g.strideB, S::BCH_N, S::BK))
             return cudaErrorInvalidValue;
@@ -1082,13 +1271,8 @@ cudaError_t launch_impl(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
     p.act = g.act;
     float *ws = nullptr;
     cudaError_t e = begin_split(g, plan, p, &ws, stream);
-    if (e == cudaSuccess) e = launch_pdl(kern, plan.grid, S::SMEM, stream, ta, tb, p);
+    if (e == cudaSuccess) e = launch_pdl(kern, plan.grid, kThreads, S::SMEM, stream, ta, tb, p);
     e = finish_split(g, p, ws, e, stream);
-    if (bt != nullptr) {
-        // stream-ordered: released once the GEMM has finished reading it
-        cudaError_t f = cudaFreeAsync(bt, stream);
-        if (e == cudaSuccess) e = f;
-    }
     return e;
 }
 
@@ -1129,20 +1313,10 @@ cudaError_t launch_pair(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
     }
     CUtensorMap ta, tb;
     if (!encode_3d(&ta, g.prec, g.A, g.K, g.M, g.lda, g.batch, g.strideA, S::BK, S::BM)) return cudaErrorInvalidValue;
-    float *bt = nullptr;
     if constexpr (S::B_KMAJOR) {
-        const int64_t ldbt = (g.K + 3) / 4 * 4;   // 16-byte rows for the tensor map
-        cudaError_t e = ws_alloc(reinterpret_cast<void **>(&bt), static_cast<size_t>(g.batch * g.N * ldbt) * 4, stream);
-        if (e != cudaSuccess) return e;
-        if ((e = transpose_launch(static_cast<const float *>(g.B), g.ldb, bt, ldbt, g.K, g.N, g.batch, g.strideB,
-                                  stream)) != cudaSuccess) {
-            cudaFreeAsync(bt, stream);
-            return e;
-        }
-        if (!encode_3d(&tb, g.prec, bt, g.K, g.N, ldbt, g.batch, g.N * ldbt, S::BK, S::BN / 2)) {
-            cudaFreeAsync(bt, stream);
+        // TF32: g.B is already B^T (N x K, rounded), written by the preparation kernel
+        if (!encode_3d(&tb, g.prec, g.B, g.K, g.N, g.ldb, g.batch, g.strideB, S::BK, S::BN / 2))
             return cudaErrorInvalidValue;
-        }
     } else {
         if (!encode_3d(&tb, g.prec, g.B, g.N, g.K, g.ldb, g.batch, g.strideB, S::BCH_N, S::BK))
             return cudaErrorInvalidValue;
@@ -1208,11 +1382,6 @@ cudaError_t launch_pair(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
         cfg.numAttrs = 2;
         e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p);
         e = finish_split(g, p, ws, e, stream);
-    }
-    if (bt != nullptr) {
-        // stream-ordered: released once the GEMM has finished reading it
-        cudaError_t f = cudaFreeAsync(bt, stream);
-        if (e == cudaSuccess) e = f;
     }
     return e;
 }
@@ -1316,7 +1485,7 @@ cudaError_t conv_launch_impl(const DeviceInfo &dev, const ConvArgs &c, cudaStrea
     float *ws = nullptr;
     cudaError_t e = begin_split(gg, plan, p, &ws, stream);
     const int grid = static_cast<int>(std::min<int64_t>(p.num_units, dev.sms));
-    if (e == cudaSuccess) e = launch_pdl(kern, grid, S::SMEM, stream, ta, tb, p);
+    if (e == cudaSuccess) e = launch_pdl(kern, grid, kThreads, S::SMEM, stream, ta, tb, p);
     return finish_split(gg, p, ws, e, stream);
 }
 
@@ -1344,16 +1513,18 @@ bool tc_supported(const DeviceInfo &dev) {
 bool tc_eligible(const GemmArgs &g) {
     if (g.prec != GTG_PREC_TF32 && g.prec != GTG_PREC_BF16 && g.prec != GTG_PREC_F16) return false;
     const int64_t elem = g.prec == GTG_PREC_TF32 ? 4 : 2;
+    // 16-bit operands are read by TMA in place; TF32 operands go through the
+    // preparation kernel (a rounded copy of A, the rounded B^T) in any layout
+    const bool tf32 = g.prec == GTG_PREC_TF32;
     if (g.batch > 1) {
-        // batch strides are tensor-map strides (A always; B unless it goes through the transpose)
-        if ((g.strideA * elem) % 16 || (g.strideA * elem) >= (1ll << 40)) return false;
-        if (g.prec != GTG_PREC_TF32 && ((g.strideB * elem) % 16 || (g.strideB * elem) >= (1ll << 40))) return false;
+        // batch strides are tensor-map strides
+        if (!tf32 && ((g.strideA * elem) % 16 || (g.strideA * elem) >= (1ll << 40))) return false;
+        if (!tf32 && ((g.strideB * elem) % 16 || (g.strideB * elem) >= (1ll << 40))) return false;
         if (g.batch > 65535 || g.batch * ((g.M + 127) / 128) * ((g.N + 63) / 64) > INT32_MAX) return false;
     }
     const auto a = reinterpret_cast<uintptr_t>(g.A), b = reinterpret_cast<uintptr_t>(g.B);
-    if ((a & 15) || (g.lda * elem) % 16) return false;           // TMA base and row stride of A
-    // 16-bit B is read by TMA in place; TF32 B goes through the transpose kernel
-    if (g.prec != GTG_PREC_TF32 && ((b & 15) || (g.ldb * elem) % 16)) return false;
+    if (!tf32 && ((a & 15) || (g.lda * elem) % 16)) return false;   // TMA base and row stride of A
+    if (!tf32 && ((b & 15) || (g.ldb * elem) % 16)) return false;
     if (g.M > INT32_MAX || g.N > INT32_MAX || g.K > INT32_MAX) return false;
     if ((g.lda * elem) >= (1ll << 40) || (g.ldb * elem) >= (1ll << 40)) return false;
     return g.M > 0 && g.N > 0 && g.K > 0;
@@ -1444,6 +1615,8 @@ void tc_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
     }
 }
 
+// (The plan of gemm_tf32_noalloc: its single-CTA kernel has the four
+// converter warps that round A in shared memory.)
 void tc_plan_unsplit_single(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan) {
     const bool tf32 = g.prec == GTG_PREC_TF32;
     const int bk = tf32 ? 32 : 64;
@@ -1463,6 +1636,7 @@ void tc_plan_unsplit_single(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *
         case 128: tf32 ? fill_plan<true, 128>(dev, g, plan, 1) : fill_plan<false, 128>(dev, g, plan, 1); break;
         default: tf32 ? fill_plan<true, 64>(dev, g, plan, 1) : fill_plan<false, 64>(dev, g, plan, 1); break;
     }
+    plan->threads = threads_for(tf32);
 }
 
 bool tc_conv_eligible(const DeviceInfo &dev, const ConvArgs &c) {
@@ -1564,6 +1738,31 @@ bool tc_eligible_repacked(const GemmArgs &g) {
 cudaError_t tc_launch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan, cudaStream_t stream) {
     const bool tf32 = g.prec == GTG_PREC_TF32;
     const int64_t elem = tf32 ? 4 : 2;
+    if (tf32) {
+        // A' (rounded copy of A) and B^T (rounded), both with rows of ldk
+        // elements, in one pool buffer; a shared operand is prepared once
+        const int64_t ldk = (g.K + 3) / 4 * 4;
+        const int64_t items_a = g.batch > 1 && g.strideA != 0 ? g.batch : 1;
+        const int64_t items_b = g.batch > 1 && g.strideB != 0 ? g.batch : 1;
+        const size_t a_bytes = (static_cast<size_t>(items_a * g.M * ldk) * 4 + 255) / 256 * 256;
+        const size_t b_bytes = static_cast<size_t>(items_b * g.N * ldk) * 4;
+        void *ws = nullptr;
+        cudaError_t e = ws_alloc(&ws, a_bytes + b_bytes, stream);
+        if (e != cudaSuccess) return e;
+        float *Ap = static_cast<float *>(ws);
+        float *Bt = reinterpret_cast<float *>(static_cast<char *>(ws) + a_bytes);
+        e = tf32_prep_launch(dev, g, Ap, Bt, ldk, items_a, items_b, stream);
+        GemmArgs g2 = g;
+        g2.A = Ap;
+        g2.lda = ldk;
+        g2.strideA = items_a > 1 ? g.M * ldk : 0;
+        g2.B = Bt;
+        g2.ldb = ldk;
+        g2.strideB = items_b > 1 ? g.N * ldk : 0;
+        if (e == cudaSuccess) e = tc_launch_aligned(dev, g2, plan, stream);
+        const cudaError_t f = cudaFreeAsync(ws, stream);   // stream-ordered: after the GEMM has read it
+        return e != cudaSuccess ? e : f;
+    }
     const bool a_bad = !tma_operand_ok(g.A, g.lda, g.strideA, g.batch, elem);
     const bool b_bad = !tf32 && !tma_operand_ok(g.B, g.ldb, g.strideB, g.batch, elem);
     if (!a_bad && !b_bad) return tc_launch_aligned(dev, g, plan, stream);
@@ -1574,7 +1773,7 @@ cudaError_t tc_launch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &
         const int64_t ld = (g.K + 16 / elem - 1) / (16 / elem) * (16 / elem);
         const int64_t items = g.batch > 1 && g.strideA != 0 ? g.batch : 1;
         e = ws_alloc(&pa, static_cast<size_t>(items * g.M * ld * elem), stream);
-        if (e == cudaSuccess) e = repack_launch(g.A, g.lda, g.strideA, pa, ld, g.M, g.K, items, elem, stream);
+        if (e == cudaSuccess) e = repack_launch(g.A, g.lda, g.strideA, pa, ld, g.M, g.K, items, elem, dev.status, stream);
         g2.A = pa;
         g2.lda = ld;
         g2.strideA = items > 1 ? g.M * ld : 0;
@@ -1583,7 +1782,7 @@ cudaError_t tc_launch(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &
         const int64_t ld = (g.N + 7) / 8 * 8;
         const int64_t items = g.batch > 1 && g.strideB != 0 ? g.batch : 1;
         e = ws_alloc(&pb, static_cast<size_t>(items * g.K * ld * 2), stream);
-        if (e == cudaSuccess) e = repack_launch(g.B, g.ldb, g.strideB, pb, ld, g.K, g.N, items, 2, stream);
+        if (e == cudaSuccess) e = repack_launch(g.B, g.ldb, g.strideB, pb, ld, g.K, g.N, items, 2, dev.status, stream);
         g2.B = pb;
         g2.ldb = ld;
         g2.strideB = items > 1 ? g.K * ld : 0;
@@ -1645,7 +1844,7 @@ template <int BN>
 cudaError_t launch_tf32_fixed(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan &plan,
                               cudaStream_t stream, float *bt, int attr_bit) {
     using S = Shape<true, BN>;
-    auto kern = tc_gemm_kernel<true, BN>;
+    auto kern = tc_gemm_kernel<true, BN, false, true>;   // A rounded in shared memory (no room for a copy)
     {
         AttrCache &ac = attr_cache();
         std::lock_guard<std::mutex> lk(ac.mu);
@@ -1662,7 +1861,7 @@ cudaError_t launch_tf32_fixed(const DeviceInfo &dev, const GemmArgs &g, const gt
     if (!encode_3d(&tb, GTG_PREC_TF32, bt, g.K, g.N, ldbt, 1, 0, S::BK, BN)) return cudaErrorInvalidValue;
     // B^T overwrites every element the GEMM reads, so the array's previous
     // contents never matter and nothing needs clearing.
-    cudaError_t e = transpose_launch(static_cast<const float *>(g.B), g.ldb, bt, ldbt, g.K, g.N, 1, 0, stream);
+    cudaError_t e = transpose_launch(static_cast<const float *>(g.B), g.ldb, bt, ldbt, g.K, g.N, 1, 0, dev.status, stream);
     if (e != cudaSuccess) return e;
     TcParams p;
     p.C = g.C;
@@ -1687,7 +1886,7 @@ cudaError_t launch_tf32_fixed(const DeviceInfo &dev, const GemmArgs &g, const gt
     p.drop_slice = take_drop_slice();
     p.bias = g.bias;
     p.act = g.act;
-    kern<<<plan.grid, kThreads, S::SMEM, stream>>>(ta, tb, p);
+    kern<<<plan.grid, threads_for(true), S::SMEM, stream>>>(ta, tb, p);
     return cudaGetLastError();
 }
 
@@ -1700,9 +1899,10 @@ cudaError_t tc_launch_tf32_fixed_scratch(const DeviceInfo &dev, const GemmArgs &
     const cudaError_t e = fixed_scratch_address(dev.id, &bt);
     if (e != cudaSuccess) return e;
     switch (plan.bn) {
-        case 256: return launch_tf32_fixed<256>(dev, g, plan, stream, bt, 0);
-        case 128: return launch_tf32_fixed<128>(dev, g, plan, stream, bt, 2);
-        case 64: return launch_tf32_fixed<64>(dev, g, plan, stream, bt, 4);
+        // attribute-cache bits of their own: these are the ROUND_A kernels
+        case 256: return launch_tf32_fixed<256>(dev, g, plan, stream, bt, 11);
+        case 128: return launch_tf32_fixed<128>(dev, g, plan, stream, bt, 12);
+        case 64: return launch_tf32_fixed<64>(dev, g, plan, stream, bt, 13);
         default: return cudaErrorInvalidValue;
     }
 }

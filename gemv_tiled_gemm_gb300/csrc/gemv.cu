@@ -226,6 +226,7 @@ cudaError_t gemv_launch(const DeviceInfo &dev, const GemvArgs &g, const gtg_plan
     p.status = dev.status;
     p.wait_limit_ns = wait_limit_setting();
     p.skip_x = p.x_bulk ? take_gemv_skip_x() : 0;
+    p.dbg_shrink = debug_shrink_setting();
     void *args[] = {&p};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.grid);

@@ -59,7 +59,38 @@ struct Params {
     int *status;         // the library's device status word (set on a timed-out wait)
     unsigned long long wait_limit_ns;   // bound of every mbarrier wait
     int skip_x;          // testing hook: announce the bulk copies of x but issue none (the wait runs out)
+    int dbg_shrink;      // GTG_DEBUG builds: elements taken off the checked extent of A (testing); else 0
 };
+
+// GTG_DEBUG builds: the extents every computed address of a GEMV kernel is
+// checked against: the matrix (A up to its last element, less p.dbg_shrink
+// elements), the outputs (batch rows of y) and the dynamic shared memory.
+#ifdef GTG_DEBUG
+struct DebugBounds {
+    const void *a_hi;
+    const float *y_hi;
+    const char *s_lo, *s_hi;
+};
+template <typename T, int BATCH>
+__device__ __forceinline__ DebugBounds debug_bounds(const Params &p, const void *smem) {
+    DebugBounds d;
+    const long long a_elems = p.M > 0 ? (static_cast<long long>(p.M) - 1) * p.lda + p.N - p.dbg_shrink : 0;
+    d.a_hi = static_cast<const T *>(p.A) + a_elems;
+    d.y_hi = p.y + static_cast<long long>(BATCH - 1) * p.ldy + p.M;
+    d.s_lo = static_cast<const char *>(smem);
+    d.s_hi = d.s_lo + dynamic_smem_bytes();
+    return d;
+}
+#define GV_BOUNDS(T, BATCH, smem) const DebugBounds dbg = debug_bounds<T, BATCH>(p, smem)
+#define GV_A(ptr, bytes) GTG_DEBUG_IN((ptr), (bytes), p.A, dbg.a_hi, p.status)
+#define GV_Y(ptr) GTG_DEBUG_IN((ptr), 4, p.y, dbg.y_hi, p.status)
+#define GV_S(ptr, bytes) GTG_DEBUG_IN((ptr), (bytes), dbg.s_lo, dbg.s_hi, p.status)
+#else
+#define GV_BOUNDS(T, BATCH, smem) static_cast<void>(0)
+#define GV_A(ptr, bytes) true
+#define GV_Y(ptr) true
+#define GV_S(ptr, bytes) true
+#endif
 
 // Matrix element types. kVec = elements per 16-byte load; widen() turns one
 // such load into FP32 values in column order; one() reads a single element.
@@ -141,11 +172,15 @@ __device__ __forceinline__ float4 ld16(const T *p) {
 
 template <int BATCH, int kThreads>
 __device__ __forceinline__ void stage_x(float *xs, const Params &p, int c0, int len) {
+#ifdef GTG_DEBUG
+    const char *s_hi = reinterpret_cast<const char *>(xs) + dynamic_smem_bytes();
+#endif
 #pragma unroll
     for (int b = 0; b < BATCH; ++b) {
         const float *src = p.x + static_cast<long long>(b) * p.ldx + c0;
         float *dst = xs + b * p.chunk;
-        for (int j = threadIdx.x; j < len; j += kThreads) dst[j] = __ldg(src + j);
+        for (int j = threadIdx.x; j < len; j += kThreads)
+            if (GTG_DEBUG_IN(dst + j, 4, xs, s_hi, p.status)) dst[j] = __ldg(src + j);
     }
 }
 
@@ -160,8 +195,12 @@ __device__ __forceinline__ void stage_x_bulk(float *xs, const Params &p, uint32_
         if (!p.skip_x)
 #pragma unroll
             for (int b = 0; b < BATCH; ++b)
-                ptx::bulk_load(ptx::smem_addr(xs + b * p.chunk), p.x + static_cast<long long>(b) * p.ldx,
-                               static_cast<uint32_t>(p.N * 4), bar);
+#ifdef GTG_DEBUG
+                if (GTG_DEBUG_IN(xs + b * p.chunk, 4ull * p.N, xs, reinterpret_cast<const char *>(xs) + dynamic_smem_bytes(),
+                                 p.status))
+#endif
+                    ptx::bulk_load(ptx::smem_addr(xs + b * p.chunk), p.x + static_cast<long long>(b) * p.ldx,
+                                   static_cast<uint32_t>(p.N * 4), bar);
     }
 }
 
@@ -325,7 +364,8 @@ __device__ __forceinline__ void store_task_totals(const float (&acc)[ROWS][BATCH
 
 template <typename T, int BATCH, int ROWS, int U, bool VEC>
 __device__ __forceinline__ void accumulate(float (&acc)[ROWS][BATCH], const T *const (&arow)[ROWS],
-                                           const float *xs, int chunk, int c0, int len, int lane) {
+                                           const float *xs, int chunk, int c0, int len, int lane, const Params &p) {
+    GV_BOUNDS(T, BATCH, xs);
     if constexpr (VEC) {
         constexpr int VE = Elem<T>::kVec;
         const int nu = len / VE;
@@ -335,21 +375,28 @@ __device__ __forceinline__ void accumulate(float (&acc)[ROWS][BATCH], const T *c
 #pragma unroll
             for (int u = 0; u < U; ++u)
 #pragma unroll
-                for (int r = 0; r < ROWS; ++r) a[u][r] = ld16(arow[r] + c0 + VE * (j + 32 * u));
+                for (int r = 0; r < ROWS; ++r) {
+                    const T *q = arow[r] + c0 + VE * (j + 32 * u);
+                    a[u][r] = GV_A(q, 16) ? ld16(q) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
 #pragma unroll
             for (int u = 0; u < U; ++u) fma_unit<T, ROWS, BATCH>(acc, a[u], xs, chunk, VE * (j + 32 * u));
         }
         for (; j < nu; j += 32) {
             float4 a[ROWS];
 #pragma unroll
-            for (int r = 0; r < ROWS; ++r) a[r] = ld16(arow[r] + c0 + VE * j);
+            for (int r = 0; r < ROWS; ++r) {
+                const T *q = arow[r] + c0 + VE * j;
+                a[r] = GV_A(q, 16) ? ld16(q) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
             fma_unit<T, ROWS, BATCH>(acc, a, xs, chunk, VE * j);
         }
         const int jt = VE * nu + lane;   // fewer than VE trailing entries
         if (jt < len) {
 #pragma unroll
             for (int r = 0; r < ROWS; ++r) {
-                const float a = Elem<T>::one(arow[r] + c0 + jt);
+                const T *q = arow[r] + c0 + jt;
+                const float a = GV_A(q, sizeof(T)) ? Elem<T>::one(q) : 0.f;
 #pragma unroll
                 for (int b = 0; b < BATCH; ++b) acc[r][b] = fmaf(a, xs[b * chunk + jt], acc[r][b]);
             }
@@ -361,7 +408,10 @@ __device__ __forceinline__ void accumulate(float (&acc)[ROWS][BATCH], const T *c
 #pragma unroll
             for (int u = 0; u < U; ++u)
 #pragma unroll
-                for (int r = 0; r < ROWS; ++r) a[u][r] = Elem<T>::one(arow[r] + c0 + j + 32 * u);
+                for (int r = 0; r < ROWS; ++r) {
+                    const T *q = arow[r] + c0 + j + 32 * u;
+                    a[u][r] = GV_A(q, sizeof(T)) ? Elem<T>::one(q) : 0.f;
+                }
 #pragma unroll
             for (int u = 0; u < U; ++u)
 #pragma unroll
@@ -374,7 +424,8 @@ __device__ __forceinline__ void accumulate(float (&acc)[ROWS][BATCH], const T *c
         for (; j < len; j += 32) {
 #pragma unroll
             for (int r = 0; r < ROWS; ++r) {
-                const float a = Elem<T>::one(arow[r] + c0 + j);
+                const T *q = arow[r] + c0 + j;
+                const float a = GV_A(q, sizeof(T)) ? Elem<T>::one(q) : 0.f;
 #pragma unroll
                 for (int b = 0; b < BATCH; ++b) acc[r][b] = fmaf(a, xs[b * chunk + j], acc[r][b]);
             }
@@ -390,6 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Params p) {
     float *xs = reinterpret_cast<float *>(xs_raw);
     const T *A = static_cast<const T *>(p.A);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    GV_BOUNDS(T, BATCH, xs);
 
     // this CTA's rows: [r_begin, r_end), equal shares of M
     const int r_begin = static_cast<int>(static_cast<long long>(p.M) * blockIdx.x / gridDim.x);
@@ -426,15 +478,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Params p) {
                 stage_x<BATCH, kThreads>(xs, p, c0, len);
                 __syncthreads();              // the chunk is in place
             }
-            if (active) accumulate<T, BATCH, ROWS, U, VEC>(acc, arow, xs, p.chunk, c0, len, lane);
+            if (active) accumulate<T, BATCH, ROWS, U, VEC>(acc, arow, xs, p.chunk, c0, len, lane, p);
         }
         if (active) {
             int vi;
             const float tot = task_total<ROWS, BATCH>(acc, lane, vi);
             if (vi >= 0) {
                 const int r = vi / BATCH, b = vi - r * BATCH;
-                if (row0 + r < r_end)
-                    p.y[static_cast<long long>(b) * p.ldy + row0 + r] = apply_epilogue(tot, p.bias, row0 + r, p.act);
+                float *dst = p.y + static_cast<long long>(b) * p.ldy + row0 + r;
+                if (row0 + r < r_end && GV_Y(dst)) *dst = apply_epilogue(tot, p.bias, row0 + r, p.act);
             }
         }
     }
@@ -456,6 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const Params p
     float *xs = reinterpret_cast<float *>(xs_raw);
     const T *A = static_cast<const T *>(p.A);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    GV_BOUNDS(T, BATCH, xs);
     const int r_begin = static_cast<int>(static_cast<long long>(p.M) * blockIdx.x / gridDim.x);
     const int r_end = static_cast<int>(static_cast<long long>(p.M) * (blockIdx.x + 1) / gridDim.x);
     const int ntasks = (r_end - r_begin + ROWS - 1) / ROWS;
@@ -483,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const Params p
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int j = blk * 32 * U + 32 * u + lane;
-                dst[u][r] = j < nu ? ld16(a + VE * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+                dst[u][r] = j < nu && GV_A(a + VE * j, 16) ? ld16(a + VE * j) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
     };
@@ -534,7 +587,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const Params p
             if (jt < p.N) {
 #pragma unroll
                 for (int r = 0; r < ROWS; ++r) {
-                    const float a = Elem<T>::one(A + static_cast<long long>(min(row_of(t, r), r_end - 1)) * p.lda + jt);
+                    const T *q = A + static_cast<long long>(min(row_of(t, r), r_end - 1)) * p.lda + jt;
+                    const float a = GV_A(q, sizeof(T)) ? Elem<T>::one(q) : 0.f;
 #pragma unroll
                     for (int b = 0; b < BATCH; ++b) acc[r][b] = fmaf(a, xs[b * p.chunk + jt], acc[r][b]);
                 }
@@ -544,7 +598,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const Params p
             if (vi >= 0) {
                 const int r = vi / BATCH, b = vi - r * BATCH;
                 const int row = row_of(t, r);
-                if (row < r_end) p.y[static_cast<long long>(b) * p.ldy + row] = apply_epilogue(tot, p.bias, row, p.act);
+                float *dst = p.y + static_cast<long long>(b) * p.ldy + row;
+                if (row < r_end && GV_Y(dst)) *dst = apply_epilogue(tot, p.bias, row, p.act);
             }
 #pragma unroll
             for (int r = 0; r < ROWS; ++r)
@@ -615,6 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
     const T *A = static_cast<const T *>(p.A) + VE * static_cast<long long>(ub0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t bar = ptx::smem_addr(&xbar);
+    GV_BOUNDS(T, BATCH, xs);
 
     if (p.x_bulk && threadIdx.x == 0) {
         ptx::mbar_init(bar, 1);
@@ -657,9 +713,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
             if (xlen > 0 && !p.skip_x)
 #pragma unroll
                 for (int b = 0; b < BATCH; ++b)
-                    ptx::bulk_load(ptx::smem_addr(xs + b * p.chunk),
-                                   p.x + static_cast<long long>(b) * p.ldx + VE * ub0,
-                                   static_cast<uint32_t>(xlen * 4), bar);
+                    if (GV_S(xs + b * p.chunk, 4ull * xlen))
+                        ptx::bulk_load(ptx::smem_addr(xs + b * p.chunk),
+                                       p.x + static_cast<long long>(b) * p.ldx + VE * ub0,
+                                       static_cast<uint32_t>(xlen * 4), bar);
         }
     }
 
@@ -695,7 +752,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
         for (int u = 0; u < U; ++u) {
             const int j = jb + 32 * u + lane;
 #pragma unroll
-            for (int r = 0; r < ROWS; ++r) dst[u][r] = j < j1 ? Q::load(arow[r] + VE * j) : Q::zero();
+            for (int r = 0; r < ROWS; ++r)
+                dst[u][r] = j < j1 && GV_A(arow[r] + VE * j, kLoadBytes) ? Q::load(arow[r] + VE * j) : Q::zero();
         }
     };
 
@@ -711,8 +769,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
 #pragma unroll
         for (int b = 0; b < BATCH; ++b) {
             const float *src = p.x + static_cast<long long>(b) * p.ldx + VE * ub0;
-            for (int j = threadIdx.x; j < xlen; j += kThreads)
-                xs[b * p.chunk + (PEEL ? (j & 3) * xq + (j >> 2) : j)] = __ldg(src + j);
+            for (int j = threadIdx.x; j < xlen; j += kThreads) {
+                float *d = xs + b * p.chunk + (PEEL ? (j & 3) * xq + (j >> 2) : j);
+                if (GV_S(d, 4)) *d = __ldg(src + j);
+            }
         }
         __syncthreads();
     }
@@ -753,7 +813,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
                     const float *xc = xs + (col & 3) * xq + (col >> 2);
 #pragma unroll
                     for (int r = 0; r < ROWS; ++r) {
-                        const float a = Elem<T>::one(arow[r] - h + col);
+                        const T *q = arow[r] - h + col;
+                        const float a = GV_A(q, sizeof(T)) ? Elem<T>::one(q) : 0.f;
 #pragma unroll
                         for (int b = 0; b < BATCH; ++b) acc[r][b] = fmaf(a, xc[b * p.chunk], acc[r][b]);
                     }
@@ -766,12 +827,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
             const int jt = VE * nub + lane;
 #pragma unroll
             for (int r = 0; r < ROWS; ++r) {
-                const float a = Elem<T>::one(arow[r] + jt);
+                const T *q = arow[r] + jt;
+                const float a = GV_A(q, sizeof(T)) ? Elem<T>::one(q) : 0.f;
 #pragma unroll
                 for (int b = 0; b < BATCH; ++b) acc[r][b] = fmaf(a, xs[b * p.chunk + jt], acc[r][b]);
             }
         }
-        store_task_totals<ROWS, BATCH>(acc, part + static_cast<long long>(task) * ROWS * BATCH, lane);
+        if (GV_S(part + static_cast<long long>(task) * ROWS * BATCH, 4ull * ROWS * BATCH))
+            store_task_totals<ROWS, BATCH>(acc, part + static_cast<long long>(task) * ROWS * BATCH, lane);
     }
     __syncthreads();
     if (C == 1) {
@@ -790,7 +853,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
             float v = 0.f;
 #pragma unroll
             for (int cs = 0; cs < WC; ++cs) v += part[((rg * WC + cs) * ROWS + r) * BATCH + b];
-            p.y[static_cast<long long>(b) * p.ldy + r_begin + rl] = apply_epilogue(v, p.bias, r_begin + rl, p.act);
+            float *dst = p.y + static_cast<long long>(b) * p.ldy + r_begin + rl;
+            if (GV_Y(dst)) *dst = apply_epilogue(v, p.bias, r_begin + rl, p.act);
         }
         return;
     }
@@ -801,7 +865,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
         float v = 0.f;
 #pragma unroll
         for (int cs = 0; cs < WC; ++cs) v += part[((rg * WC + cs) * ROWS + r) * BATCH + b];
-        mine[idx] = v;
+        if (GV_S(mine + idx, 4)) mine[idx] = v;
     }
     ptx::cluster_sync();   // every CTA's partials are complete and visible to the cluster
     const uint32_t mine_addr = ptx::smem_addr(mine);
@@ -810,7 +874,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
         if (rl % C != c) continue;   // rows are shared out round-robin over the cluster
         float v = 0.f;
         for (int cc = 0; cc < C; ++cc) v += ptx::ld_cluster_f32(ptx::map_to_rank(mine_addr, cc) + 4u * idx);
-        p.y[static_cast<long long>(b) * p.ldy + r_begin + rl] = apply_epilogue(v, p.bias, r_begin + rl, p.act);
+        float *dst = p.y + static_cast<long long>(b) * p.ldy + r_begin + rl;
+        if (GV_Y(dst)) *dst = apply_epilogue(v, p.bias, r_begin + rl, p.act);
     }
     ptx::cluster_sync();   // no CTA leaves while another may still read its shared memory
 }
@@ -832,6 +897,7 @@ __global__ void __launch_bounds__(kPeelThreads, 1) gemv_stream_peel_kernel(const
     float *xs = reinterpret_cast<float *>(xs_raw);
     const float *A = static_cast<const float *>(p.A);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    GV_BOUNDS(float, BATCH, xs);
     const int r_begin = static_cast<int>(static_cast<long long>(p.M) * blockIdx.x / gridDim.x);
     const int r_end = static_cast<int>(static_cast<long long>(p.M) * (blockIdx.x + 1) / gridDim.x);
     const int nu = p.N >= 3 ? (p.N - 3) / 4 : 0;
@@ -851,7 +917,8 @@ __global__ void __launch_bounds__(kPeelThreads, 1) gemv_stream_peel_kernel(const
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int j = jb + 32 * u + lane;
-                dst[u] = j < nu ? ptx::ld_stream_f4(av + 4 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+                dst[u] = j < nu && GV_A(av + 4 * j, 16) ? ptx::ld_stream_f4(av + 4 * j)
+                                                        : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         };
         float4 nxt[U];
@@ -888,12 +955,12 @@ __global__ void __launch_bounds__(kPeelThreads, 1) gemv_stream_peel_kernel(const
         }
         // the head [0, h) and the entries past the whole units
         if (lane < h && lane < p.N) {
-            const float v = ptx::ld_stream_f1(a + lane);
+            const float v = GV_A(a + lane, 4) ? ptx::ld_stream_f1(a + lane) : 0.f;
 #pragma unroll
             for (int b = 0; b < BATCH; ++b) acc[b] = fmaf(v, xs[b * p.chunk + lane], acc[b]);
         }
         for (int jt = h + 4 * nu + lane; jt < p.N; jt += 32) {
-            const float v = ptx::ld_stream_f1(a + jt);
+            const float v = GV_A(a + jt, 4) ? ptx::ld_stream_f1(a + jt) : 0.f;
 #pragma unroll
             for (int b = 0; b < BATCH; ++b) acc[b] = fmaf(v, xs[b * p.chunk + jt], acc[b]);
         }
@@ -902,7 +969,8 @@ __global__ void __launch_bounds__(kPeelThreads, 1) gemv_stream_peel_kernel(const
             float v = acc[b];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-            if (lane == 0) p.y[static_cast<long long>(b) * p.ldy + row] = apply_epilogue(v, p.bias, row, p.act);
+            float *dst = p.y + static_cast<long long>(b) * p.ldy + row;
+            if (lane == 0 && GV_Y(dst)) *dst = apply_epilogue(v, p.bias, row, p.act);
         }
     }
 }

@@ -37,7 +37,19 @@ struct Im2col {
     int N, H, W, C, OH, OW, KH, KW;
     int sh, sw, ph, pw, dh, dw;
     long long M;                   // N * OH * OW rows
+    int *status;                   // the library's device status word (GTG_DEBUG checks)
 };
+
+// GTG_DEBUG builds: reads of X and writes of P are checked against their extents.
+#ifdef GTG_DEBUG
+#define IM_X(ptr, bytes) \
+    GTG_DEBUG_IN((ptr), (bytes), g.X, static_cast<const char *>(g.X) + static_cast<long long>(g.N) * g.H * g.W * g.C * ESZ_, g.status)
+#define IM_P(ptr, bytes) \
+    GTG_DEBUG_IN((ptr), (bytes), g.P, static_cast<const char *>(g.P) + g.M * g.ldp * ESZ_, g.status)
+#else
+#define IM_X(ptr, bytes) true
+#define IM_P(ptr, bytes) true
+#endif
 
 constexpr int kWarpsPerCta = 8;
 
@@ -53,6 +65,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) im2col_kernel(const Im2col 
     const int chunks = g.KH * g.KW * cc;           // chunks per row of P
     const V *X = static_cast<const V *>(g.X);
     const V zero{};
+    constexpr long long ESZ_ = sizeof(V) / VE;
     for (long long m = warp0; m < g.M; m += nwarps) {
         const int ow = static_cast<int>(m % g.OW);
         const long long t = m / g.OW;
@@ -66,7 +79,8 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) im2col_kernel(const Im2col 
         for (int q = lane; q < chunks; q += 32) {
             const int ih = ih0 + kh * g.dh, iw = iw0 + kw * g.dw;
             const bool inside = ih >= 0 && ih < g.H && iw >= 0 && iw < g.W;
-            dst[q] = inside ? X[((static_cast<long long>(n) * g.H + ih) * g.W + iw) * cc + c] : zero;
+            const V *src = X + ((static_cast<long long>(n) * g.H + ih) * g.W + iw) * cc + c;
+            if (IM_P(dst + q, sizeof(V))) dst[q] = inside && IM_X(src, sizeof(V)) ? *src : zero;
             c += 32;
             while (c >= cc) {   // carry into kw, then kh
                 c -= cc;
@@ -109,6 +123,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) im2col_table_kernel(const I
     const int lane = threadIdx.x & 31;
     const int nwarps = gridDim.x * kWarpsPerCta;
     const char *X = static_cast<const char *>(g.X);
+    constexpr long long ESZ_ = ESZ;
     for (int m = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5); m < g.M; m += nwarps) {
         const int ow = m % g.OW, t = m / g.OW;
         const int oh = t % g.OH, n = t / g.OH;
@@ -121,9 +136,9 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) im2col_table_kernel(const I
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
             const Tap tp = tab[q];
             const int ih = ih0 + (tp.dy_dx >> 16), iw = iw0 + (tp.dy_dx & 0xFFFF);
-            if (ih >= 0 && ih < g.H && iw >= 0 && iw < g.W)
-                v = *reinterpret_cast<const uint4 *>(X + (corner + tp.off) * ESZ);
-            dst[q] = v;
+            const char *src = X + (corner + tp.off) * ESZ;
+            if (ih >= 0 && ih < g.H && iw >= 0 && iw < g.W && IM_X(src, 16)) v = *reinterpret_cast<const uint4 *>(src);
+            if (IM_P(dst + q, 16)) dst[q] = v;
         }
     }
 }
@@ -151,6 +166,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) im2col_linear_kernel(const 
     const int nwarps = gridDim.x * kWarpsPerCta;
     const E *X = static_cast<const E *>(g.X);
     const int width = static_cast<int>(g.ldp);
+    constexpr long long ESZ_ = ESZ;
     for (int m = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5); m < g.M; m += nwarps) {
         const int ow = m % g.OW, t = m / g.OW;
         const int oh = t % g.OH, n = t / g.OH;
@@ -167,7 +183,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) im2col_linear_kernel(const 
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const int k = k0 + 32 * u;
-                    v[u] = k < K ? X[corner + tab[k].off] : E{};
+                    v[u] = k < K && IM_X(X + corner + tab[k].off, ESZ) ? X[corner + tab[k].off] : E{};
                 }
             } else {
 #pragma unroll
@@ -177,13 +193,14 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) im2col_linear_kernel(const 
                     if (k < K) {
                         const Tap tp = tab[k];
                         const int ih = ih0 + (tp.dy_dx >> 16), iw = iw0 + (tp.dy_dx & 0xFFFF);
-                        if (ih >= 0 && ih < g.H && iw >= 0 && iw < g.W) v[u] = X[corner + tp.off];
+                        if (ih >= 0 && ih < g.H && iw >= 0 && iw < g.W && IM_X(X + corner + tp.off, ESZ))
+                            v[u] = X[corner + tp.off];
                     }
                 }
             }
 #pragma unroll
             for (int u = 0; u < 8; ++u)
-                if (k0 + 32 * u < width) dst[k0 + 32 * u] = v[u];
+                if (k0 + 32 * u < width && IM_P(dst + k0 + 32 * u, ESZ)) dst[k0 + 32 * u] = v[u];
         }
     }
 }
@@ -218,6 +235,7 @@ cudaError_t im2col_launch(const DeviceInfo &dev, const ConvArgs &c, void *P, int
     g.dh = static_cast<int>(c.dh);
     g.dw = static_cast<int>(c.dw);
     g.M = c.N * c.OH * c.OW;
+    g.status = dev.status;
     const int esz = c.elem;
     const int ve = 16 / esz;
     const int K = static_cast<int>(c.KH * c.KW * c.C);

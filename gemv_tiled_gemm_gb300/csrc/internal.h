@@ -66,6 +66,36 @@ __host__ __device__ __forceinline__ float apply_epilogue(float v, const float *b
     return v;
 }
 
+// GTG_DEBUG builds (libgtg_debug.so): the index-heavy kernels check every
+// global address they compute, and every shared-memory index they write,
+// against the extent of the operand or buffer it belongs to before using it.
+// A failed check latches GTG_ERR_BOUNDS in the status word (read by
+// gtg_sync_status) and the access is skipped: a load gives zero, a store is
+// dropped. Release builds compile the checks away (they are constant true).
+#ifdef GTG_DEBUG
+__device__ __forceinline__ bool debug_in(const void *p, unsigned long long bytes, const void *lo, const void *hi,
+                                         int *status) {
+    const unsigned long long a = reinterpret_cast<unsigned long long>(p);
+    if (a >= reinterpret_cast<unsigned long long>(lo) && a + bytes <= reinterpret_cast<unsigned long long>(hi))
+        return true;
+    atomicCAS(status, 0, static_cast<int>(GTG_ERR_BOUNDS));
+    return false;
+}
+__device__ __forceinline__ unsigned dynamic_smem_bytes() {
+    unsigned v;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(v));
+    return v;
+}
+#define GTG_DEBUG_IN(p, bytes, lo, hi, status) ::gtg::debug_in((p), (bytes), (lo), (hi), (status))
+#else
+#define GTG_DEBUG_IN(p, bytes, lo, hi, status) true
+#endif
+
+// Elements by which GTG_DEBUG builds shrink the matrix extent the GEMV
+// kernels check against (testing: makes the last loads fail their check
+// without any access outside the real matrix); 0 in release builds.
+int debug_shrink_setting();
+
 // Time limit for any pipeline wait inside a kernel (nanoseconds).
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 

@@ -246,6 +246,26 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+// An FP32 value (as its bit pattern) rounded to the nearest TF32 value, ties
+// away from zero, as an FP32 bit pattern with the 13 low mantissa bits clear.
+// TF32 keeps 10 of FP32's 23 mantissa bits. In sign-magnitude form, adding
+// 2^12 (half a unit of the 10th mantissa bit) to the magnitude and clearing
+// the 13 dropped bits rounds half up in magnitude; a carry out of the
+// mantissa moves to the next binade, as it should. Infinities and NaNs
+// (exponent all ones) are left as they are. The TF32 tensor-core MMA ignores
+// the 13 low bits of its FP32 operands (it truncates); operands rounded
+// first carry at most half a TF32 unit of error.
+__device__ __forceinline__ uint32_t tf32_round(uint32_t f32_bits) {
+    return (f32_bits & 0x7F800000u) == 0x7F800000u ? f32_bits : ((f32_bits + 0x1000u) & 0xFFFFE000u);
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }

@@ -114,8 +114,11 @@ GTG_API gtg_status gemm_f32(int64_t M, int64_t N, int64_t K,
  * gemm_tf32 -- C = A*B with FP32 storage, TF32 multiplication on the tensor
  * cores (tcgen05.mma kind::tf32) and FP32 accumulation in tensor memory
  * ("Matrix Operations", "Performance Considerations": tensor cores). Same
- * arguments and layouts as gemm_f32. Each product uses the operands reduced
- * to TF32 precision (10 explicit mantissa bits) by the tensor core.
+ * arguments and layouts as gemm_f32. Each product uses the operands rounded
+ * to the nearest TF32 value (10 explicit mantissa bits, ties away from zero)
+ * before the tensor core multiplies them: B as it is transposed, A in shared
+ * memory between its load and the multiply. (The tensor core itself would
+ * truncate, which can cost twice the error of rounding.)
  * The TF32 tensor-core MMA reads B only K-major, so the call first writes
  * B^T into a temporary buffer of 4 * N * roundup(K, 4) bytes. That buffer
  * comes from the library's stream-ordered workspace pool (allocated on
@@ -399,9 +402,10 @@ GTG_API gtg_status gtg_pool_trim(void);
  * (their tensor maps get the batch as a third dimension). When strideA or,
  * for 16-bit inputs, strideB or a leading dimension is not a multiple of 16
  * bytes, the items of that operand (one copy if its stride is 0) are first
- * copied into aligned rows in a temporary from the pool; FP32 batches run
- * item by item on the SIMT kernel. Errors as for the single calls; no item
- * is computed if the arguments of any item are invalid.
+ * copied into aligned rows in a temporary from the pool. FP32 batches run
+ * on the SIMT kernel, also in one launch over all items (at most 65535 items
+ * per launch; larger batches take several). Errors as for the single calls;
+ * no item is computed if the arguments of any item are invalid.
  */
 GTG_API gtg_status gemm_strided_batched(int precision, int64_t M, int64_t N, int64_t K,
                                         const void *A, int64_t lda, int64_t strideA,

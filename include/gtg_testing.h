@@ -9,7 +9,8 @@
  *    they select among kernels that compute the same product within the same
  *    bounds. Process-wide, in effect for later calls.
  *  - Failure-path hooks (gtg_test_drop_load, gtg_test_skip_vector_copy,
- *    gtg_test_inject_launch_failure): they make a later call fail on purpose.
+ *    gtg_test_inject_launch_failure, gtg_test_debug_shrink_extent): they
+ *    make a later call fail on purpose.
  *    They act only when the environment variable GTG_TESTING is "1" at the
  *    time of the hook call; otherwise they change nothing and return
  *    GTG_ERR_UNSUPPORTED. No hook faults, traps or hangs the GPU: a kernel
@@ -127,6 +128,17 @@ GTG_API uint64_t gtg_test_workspace_allocations(void);
 GTG_API gtg_status gtg_plan_gemm_tf32_noalloc(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
                                               const float *B, int64_t ldb, const float *C, int64_t ldc,
                                               gtg_plan *plan);
+
+/*
+ * GTG_DEBUG builds only: the GEMV kernels check their matrix loads against
+ * an extent `elements` shorter than the real one, so that the last loads of
+ * a call fail their check (the access is skipped; nothing outside the real
+ * matrix is touched) and GTG_ERR_BOUNDS is latched for gtg_sync_status(): a
+ * test that the checks are live. 0 restores the real extent.
+ * Returns GTG_OK; GTG_ERR_UNSUPPORTED in a release build or without
+ * GTG_TESTING=1.
+ */
+GTG_API gtg_status gtg_test_debug_shrink_extent(int elements);
 
 /* 1 if this library was built with GTG_DEBUG (kernels check the addresses
  * they compute and latch GTG_ERR_BOUNDS instead of making an access outside

@@ -124,6 +124,25 @@ def test_fault_inject_environment_variable():
     assert st[2] == gtg.GTG_ERR_LAUNCH and gtg.GTG_ERR_LAUNCH not in (st[0], st[1], st[3]), st
 
 
+def test_debug_build_compiles_and_reports_itself():
+    """The GTG_DEBUG variant (bounds-checking kernels) builds with the same
+    sources and exports the same symbols; each library reports which it is."""
+    import subprocess
+    import sys
+    path = _build.build(debug=True)
+    assert os.path.basename(path) == "libgtg_debug.so"
+    code = "import gemv_tiled_gemm_gb300 as g; print(g.gtg_debug_build(), g.gtg_test_debug_shrink_extent(0))"
+    env = dict(os.environ, GTG_DEBUG="1", GTG_TESTING="1")
+    out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.split() == ["1", str(gtg.GTG_OK)]
+    assert gtg.gtg_debug_build() == 0
+    assert gtg.gtg_test_debug_shrink_extent(1) == gtg.GTG_ERR_UNSUPPORTED   # release build
+    nm = lambda p: {l.split()[-1] for l in subprocess.run(["nm", "-D", "--defined-only", p], capture_output=True,
+                                                           text=True).stdout.splitlines() if " T " in l}
+    assert nm(path) == nm(gtg.LIB_PATH)
+
+
 def test_only_the_c_abi_is_exported():
     import subprocess
     out = subprocess.run(["nm", "-D", "--defined-only", gtg.LIB_PATH], capture_output=True,

@@ -204,6 +204,29 @@ def test_strided_batched_plans_one_launch_for_all_items():
         assert bad == 0, (b, ratio)
 
 
+def test_f32_strided_batch_in_one_launch_past_the_grid_z_limit():
+    """FP32 batches run on the SIMT kernel in one launch over blockIdx.z; more
+    than 65535 items take a second launch. Tiny ragged items with one shared
+    B: stacked, the items' A rows form one matrix whose product with B the
+    oracle computes in a single call."""
+    torch = _t()
+    batch, M, N, K = 70001, 3, 5, 7
+    g = PCG32(960)
+    A = g.uniform_f32((batch, M, K))
+    B = g.uniform_f32((K, N))
+    dA, dB = _dev("f32", A), _dev("f32", B)
+    dC = torch.full((batch, M, N), float("nan"), device="cuda")
+    s = int(torch.cuda.current_stream().cuda_stream)
+    st = gtg.gemm_strided_batched("f32", M, N, K, dA.data_ptr(), K, M * K, dB.data_ptr(), N, 0,
+                                  dC.data_ptr(), N, M * N, batch, None, s)
+    assert st == gtg.GTG_OK and gtg.gtg_sync_status(s) == gtg.GTG_OK
+    plan = gtg.plan_gemm("f32", M, N, K, dA.data_ptr(), K, dB.data_ptr(), N, dC.data_ptr(), N)
+    assert plan["kernel"] == "simt"
+    ref, E = oracle.gemm(A.reshape(batch * M, K), B)
+    ratio, bad = parity_ratio(dC.cpu().numpy().reshape(batch * M, N), ref, E, "f32", K)
+    assert bad == 0, ratio
+
+
 def test_strided_batched_validation():
     A, B, C = 1 << 32, 2 << 32, 3 << 32
     f = gtg.gemm_strided_batched
