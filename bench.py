@@ -307,7 +307,10 @@ def gpu_arm(args, rank, world, local_rank):
     gv_files = ["gemv.cu", "gemv_kernels.cuh", "ptx.cuh"]
     gemm_kernel = ("tc_gemm_pair_kernel (CTA pair, 256x256 tile)" if plan.get("cluster") == 2
                    else f"tc_gemm_kernel<bf16, BN={plan.get('bn')}>")
-    gemv_kernel = {1: "gemv_stream_kernel<batch=1>", 4: "gemv_blocks_kernel"}.get(vplan.get("bm"), "gemv_kernel")
+    if vplan.get("bm") == 1 and vplan.get("smem", 0) > 4 * vplan.get("bn", 0):
+        gemv_kernel = "gemv_ring_kernel<batch=1>"   # per-warp partial sums beside the staged x
+    else:
+        gemv_kernel = {1: "gemv_stream_kernel<batch=1>", 4: "gemv_blocks_kernel"}.get(vplan.get("bm"), "gemv_kernel")
     roofline = {"bound": "tensor", "achieved": round(gemm_tflops / world, 1), "peak": bf16_peak,
                 "unit": "TFLOP/s", "frac": round(gemm_tflops / world / bf16_peak, 4),
                 "traffic": committed_traffic("gemm_bf16_8192", tc_files),

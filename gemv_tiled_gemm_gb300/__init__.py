@@ -264,12 +264,14 @@ def gtg_force_simt(force: bool) -> None:
     lib().gtg_force_simt(1 if force else 0)
 
 
-GEMV_PATHS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2}
+GEMV_PATHS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2, "no_ring": 3}
 
 
 def gtg_gemv_force_path(path="auto") -> None:
-    """Tuning/testing hook for BF16 GEMVs of batch 3-8: "auto" (the planner),
-    "cuda_cores", or "tensor_cores" (whenever the layout allows)."""
+    """Tuning/testing hook for the GEMV kernel choice: "auto" (the planner),
+    "cuda_cores" or "tensor_cores" (BF16 matrices at batch 3-8, whenever the
+    layout allows), or "no_ring" (CUDA cores, and the streaming kernel
+    instead of the ring kernel for one or two vectors)."""
     lib().gtg_gemv_force_path(GEMV_PATHS[path] if isinstance(path, str) else int(path))
 
 

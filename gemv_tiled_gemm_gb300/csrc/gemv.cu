@@ -16,7 +16,7 @@ std::atomic<int> g_gemv_skip_x{0};
 
 void gemv_skip_next_x(int on) { g_gemv_skip_x.store(on ? 1 : 0); }
 std::atomic<int> g_gemv_path{0};
-void gemv_force_path(int mode) { g_gemv_path.store(mode == 1 || mode == 2 ? mode : 0); }
+void gemv_force_path(int mode) { g_gemv_path.store(mode >= 1 && mode <= 3 ? mode : 0); }
 int take_gemv_skip_x() { return g_gemv_skip_x.exchange(0); }
 
 namespace {
@@ -126,6 +126,27 @@ Layout layout(const DeviceInfo &dev, const GemvArgs &g) {
         }
         return l;
     }
+    // one or two vectors with x in one CTA: equal step ranges per warp, loads
+    // in a ring (FP32 rows at batch 1-2 from any size, BF16 rows at batch 1
+    // from 2^25 elements; measured against the streaming kernel: FP32 4096^2 /
+    // 8192^2 / 16384^2 batch 1 0.92 / 0.97 / 1.01 -> 0.95 / 1.04 / 1.06 of the
+    // copy peak, BF16 16384 x 4096 batch 1 0.75 -> 0.89; BF16 4096^2 batch 1
+    // 0.65 -> 0.62 and batch 2 0.54 -> 0.42 stay on the streaming kernel)
+    if (l.nchunks == 1 && g.batch <= 2 && g_gemv_path.load() != 3 &&
+        (g.a_elem == 4 || (g.batch == 1 && g.M * g.N >= (int64_t{1} << 25)))) {
+        const int64_t rows_cta = (g.M + l.grid - 1) / l.grid;
+        const int64_t nu = g.N / (16 / g.a_elem);
+        const int64_t spr = std::max<int64_t>(1, (nu + 32 * kRingLoads - 1) / (32 * kRingLoads));
+        const int64_t warps = kStreamThreads / 32;
+        const int64_t L = (rows_cta * spr + warps - 1) / warps;
+        const int64_t part = warps * ((L + spr - 1) / spr + 1) * g.batch * 4;
+        if (l.smem + part <= limit) {
+            l.kind = kRing;
+            l.threads = kStreamThreads;
+            l.smem = static_cast<int>(l.smem + part);
+            return l;
+        }
+    }
     if (l.nchunks == 1) {
         if (g.batch <= 2) {
             l.kind = kStream;
@@ -175,7 +196,7 @@ Layout layout(const DeviceInfo &dev, const GemvArgs &g) {
 
 void gemv_plan(const DeviceInfo &dev, const GemvArgs &g, gtg_plan *plan) {
     const int path = g_gemv_path.load();
-    if (path != 1 && gemv_tc_eligible(dev, g, path == 2)) {
+    if (path != 1 && path != 3 && gemv_tc_eligible(dev, g, path == 2)) {
         gemv_tc_plan(dev, g, plan);
         return;
     }
@@ -183,6 +204,18 @@ void gemv_plan(const DeviceInfo &dev, const GemvArgs &g, gtg_plan *plan) {
     // One CTA per SM (it fills the register file); every CTA (cluster) owns an
     // equal share of the rows.
     plan->kernel = GTG_KERNEL_GEMV;
+    plan->splits = 1;
+    if (l.kind == kRing) {
+        plan->bm = 1;
+        plan->bn = l.chunk;
+        plan->bk = kRingLoads * (kRingDepth - 1);
+        plan->stages = 1;
+        plan->grid = l.grid;
+        plan->threads = l.threads;
+        plan->smem = l.smem;
+        plan->cluster = 1;
+        return;
+    }
     const bool two_rows = l.kind == kStream && g.a_elem == 2 && g.batch == 2;   // see pick() in gemv_kernels.cuh
     plan->bm = l.kind == kStream ? (two_rows ? 2 : 1) : (l.kind == kPeel ? 1 : (l.kind == kRound ? kRows : kSplitRows));
     plan->bn = l.chunk;
@@ -220,7 +253,7 @@ cudaError_t gemv_launch(const DeviceInfo &dev, const GemvArgs &g, const gtg_plan
     p.ublock = l.ublock;
     // bulk copies of x need 16-byte aligned rows of a multiple of 16 bytes
     // (the peeled kernels stage x themselves: at its own offsets, or quad-transposed)
-    p.x_bulk = (l.kind == kStream || l.kind == kSplit || l.kind == kCluster) &&
+    p.x_bulk = (l.kind == kStream || l.kind == kSplit || l.kind == kCluster || l.kind == kRing) &&
                (reinterpret_cast<uintptr_t>(g.x) & 15) == 0 && g.N % 4 == 0 &&
                (g.batch == 1 || g.ldx % 4 == 0);
     p.status = dev.status;

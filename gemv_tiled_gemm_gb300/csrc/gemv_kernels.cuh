@@ -880,6 +880,175 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
     ptx::cluster_sync();   // no CTA leaves while another may still read its shared memory
 }
 
+// gemv_ring_kernel: how many rows a warp's range of L steps can meet when a
+// row takes spr steps (a range may start inside a row).
+__host__ __device__ constexpr int ring_slots(int L, int spr) { return (L + spr - 1) / spr + 1; }
+
+// One or two vectors, 16-byte aligned rows, all of x in one CTA: the CTA's
+// rows are read in steps -- a step is U x 32 consecutive 16-byte loads of
+// one row, one per lane per load -- and the CTA's rows x spr steps (spr =
+// steps per row), row after row, are cut into one contiguous range per warp
+// of equal length (the last shorter). Every warp streams the same bytes
+// whatever the row count (one row per warp would leave 5 of 32 warps idle at
+// 27 rows per SM and give others two rows at 54), and a range spans few
+// rows.
+//
+// The loads run one ring turn ahead of the arithmetic: a ring of D register
+// sets of U loads each, unrolled so that every set sits in fixed registers.
+// The producer is straight-line code: each load carries its predicate on the
+// instruction (loads past the row's end, or past the warp's range, read
+// nothing and give zeros) and the move to the next row is a select between
+// two pointer increments. Lanes past the row's end read x from a block of
+// zeros. When the consumer leaves a row (or its range ends) the warp totals
+// of its BATCH sums go to shared memory, in the slot of (warp, row within
+// the warp's range); after a barrier each (row, vector) adds the slots of
+// the warps whose ranges meet its row, in warp order, so the result does not
+// depend on scheduling.
+template <typename T, int BATCH, int U, int D, int kThreads>
+__global__ void __launch_bounds__(kThreads, 1) gemv_ring_kernel(const Params p) {
+    constexpr int kWarps = kThreads / 32;
+    constexpr int VE = Elem<T>::kVec;   // entries per 16-byte load
+    extern __shared__ float4 xs_raw[];
+    __shared__ __align__(8) unsigned long long xbar;
+    __shared__ float4 xzero[2];         // x of the lanes past the end of a row
+    const T *A = static_cast<const T *>(p.A);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r_begin = static_cast<int>(static_cast<long long>(p.M) * blockIdx.x / gridDim.x);
+    const int r_end = static_cast<int>(static_cast<long long>(p.M) * (blockIdx.x + 1) / gridDim.x);
+    const int rows = r_end - r_begin;
+    const int nu = p.N / VE;                                   // whole 16-byte loads per row
+    const int spr = max(1, (nu + 32 * U - 1) / (32 * U));       // steps per row (at least one: it adds the trailing entries)
+    const int L = (rows * spr + kWarps - 1) / kWarps;          // steps per warp
+    const int kslots = ring_slots(L, spr);                     // rows a range can meet
+    const int s_first = min(warp * L, rows * spr);
+    const int mine = min(s_first + L, rows * spr) - s_first;
+    float *xs = reinterpret_cast<float *>(xs_raw);   // [BATCH][chunk]
+    float *part = xs + BATCH * p.chunk;              // [warp][slot][batch]
+    const uint32_t bar = ptx::smem_addr(&xbar);
+    GV_BOUNDS(T, BATCH, xs);
+
+    if (threadIdx.x < 2) xzero[threadIdx.x] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (p.x_bulk && threadIdx.x == 0) {
+        ptx::mbar_init(bar, 1);
+        ptx::fence_barrier_init();
+    }
+    const int row0 = s_first / spr, st0 = s_first - row0 * spr;   // where the range starts (CTA-local row)
+    // While the previous kernel in the stream drains: the start of each
+    // warp's range (at most 4 KB) is requested into L2.
+    if (mine > 0 && lane == 0) {
+        const long long j0 = 32ll * U * st0;
+        const long long span = (min(32ll * U * mine, nu - j0) * 16) & ~15ll;
+        if (span > 0)
+            ptx::prefetch_l2(A + static_cast<long long>(r_begin + row0) * p.lda + VE * j0,
+                             static_cast<uint32_t>(min(span, 4096ll)));
+    }
+    ptx::wait_prior_grid();
+    ptx::allow_next_grid();
+    if (p.x_bulk) {
+        __syncthreads();   // the barrier is initialised
+        if (threadIdx.x == 0) {
+            ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(BATCH * p.N * 4));
+            if (p.N > 0 && !p.skip_x)
+#pragma unroll
+                for (int b = 0; b < BATCH; ++b)
+                    if (GV_S(xs + b * p.chunk, 4ull * p.N))
+                        ptx::bulk_load(ptx::smem_addr(xs + b * p.chunk), p.x + static_cast<long long>(b) * p.ldx,
+                                       static_cast<uint32_t>(p.N * 4), bar);
+        }
+    }
+
+    // producer: step ps of the current row and the lane's load address in it
+    int ps = st0;
+    const T *pa = A + static_cast<long long>(r_begin + row0) * p.lda + VE * (32 * U * st0 + lane);
+    const long long jump = p.lda - static_cast<long long>(VE) * 32 * U * (spr - 1);
+    auto issue = [&](float4 (&dst)[U], bool valid) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const T *q = pa + VE * 32 * u;
+            const bool pr = valid && 32 * (U * ps + u) + lane < nu && GV_A(q, 16);
+            dst[u] = ptx::ld_stream_f4_if(q, pr);
+        }
+        const bool wrap = ++ps == spr;
+        ps = wrap ? 0 : ps;
+        pa += wrap ? jump : static_cast<long long>(VE) * 32 * U;
+    };
+
+    float4 ring[D][U];
+#pragma unroll
+    for (int d = 0; d < D - 1; ++d) issue(ring[d], d < mine);
+
+    bool ok = true;
+    if (p.x_bulk) {
+        ok = __all_sync(0xFFFFFFFFu, wait_x(bar, p));
+    } else {
+#pragma unroll
+        for (int b = 0; b < BATCH; ++b) {
+            const float *src = p.x + static_cast<long long>(b) * p.ldx;
+            for (int j = threadIdx.x; j < p.N; j += kThreads)
+                if (GV_S(xs + b * p.chunk + j, 4)) xs[b * p.chunk + j] = __ldg(src + j);
+        }
+    }
+    __syncthreads();   // x (when staged by the threads) and the zero block are in place
+
+    // consumer: CTA-local row cr, step cs
+    int cr = row0, cs = st0;
+    float acc[1][BATCH];
+#pragma unroll
+    for (int b = 0; b < BATCH; ++b) acc[0][b] = 0.f;
+    const float *zero = reinterpret_cast<const float *>(xzero);
+    auto consume = [&](const float4 (&cur)[U], int k) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = 32 * (U * cs + u) + lane;
+            const bool in = j < nu;
+            const float4 one[1] = {cur[u]};
+            fma_unit<T, 1, BATCH>(acc, one, in ? xs + VE * j : zero, in ? p.chunk : 0, 0);
+        }
+        const bool wrap = ++cs == spr;
+        if (wrap || k == mine - 1) {
+            if (wrap) {
+                // fewer than VE trailing entries when N is not a multiple of
+                // VE: added by the warp that holds the row's last step
+                const int jt = VE * nu + lane;
+                if (jt < p.N) {
+                    const T *q = A + static_cast<long long>(r_begin + cr) * p.lda + jt;
+                    const float a = GV_A(q, sizeof(T)) ? Elem<T>::one(q) : 0.f;
+#pragma unroll
+                    for (int b = 0; b < BATCH; ++b) acc[0][b] = fmaf(a, xs[b * p.chunk + jt], acc[0][b]);
+                }
+            }
+            float *slot = part + (static_cast<long long>(warp) * kslots + (cr - row0)) * BATCH;
+            if (GV_S(slot, 4ull * BATCH)) store_task_totals<1, BATCH>(acc, slot, lane);
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) acc[0][b] = 0.f;
+        }
+        cs = wrap ? 0 : cs;
+        cr += wrap ? 1 : 0;
+    };
+
+    if (ok) {
+        // the range rounded up to whole turns of the ring; steps past its end
+        // load nothing and are not consumed
+        for (int base = 0; base < mine; base += D) {
+#pragma unroll
+            for (int d = 0; d < D; ++d) {
+                issue(ring[(d + D - 1) % D], base + d + D - 1 < mine);
+                if (base + d < mine) consume(ring[d], base + d);
+            }
+        }
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < rows * BATCH; idx += kThreads) {
+        const int rl = idx / BATCH, b = idx - rl * BATCH;
+        const int w_lo = rl * spr / L, w_hi = ((rl + 1) * spr - 1) / L;   // the warps whose ranges meet row rl
+        float v = 0.f;
+        for (int w = w_lo; w <= w_hi; ++w)
+            v += part[(static_cast<long long>(w) * kslots + (rl - w * L / spr)) * BATCH + b];
+        float *dst = p.y + static_cast<long long>(b) * p.ldy + r_begin + rl;
+        if (GV_Y(dst)) *dst = apply_epilogue(v, p.bias, r_begin + rl, p.act);
+    }
+}
+
 // FP32 rows that are not 16-byte aligned (lda not a multiple of 4, or A off
 // 16 bytes), batch 1-2, all of x in one chunk: one row per warp, each row's
 // first h = 0..3 entries (up to its first 16-byte boundary) taken by single
@@ -992,10 +1161,23 @@ constexpr int kSplitRows = 4, kSplitSegs = 2;
 // 16 bytes (FP32) or four of 8 bytes (BF16), the same bytes either way
 constexpr int split_unroll(int elem_bytes) { return elem_bytes == 2 ? 4 : 2; }
 
-enum Kind { kStream = 0, kSplit = 1, kRound = 2, kCluster = 3, kPeel = 4, kPeelSplit = 5 };
+enum Kind { kStream = 0, kSplit = 1, kRound = 2, kCluster = 3, kPeel = 4, kPeelSplit = 5, kRing = 6 };
+
+// gemv_ring_kernel: 16-byte loads per ring set and sets in the ring.
+// Measured against other shapes of the ring at batch 1-2 (one process, CUDA
+// events, A rotated past L2): 4 x 2 beat 1 x 8 (0.84 against 0.95 of the copy
+// peak at 4096^2 FP32 batch 1) and 2 x 4 (0.93); deeper rings with fewer
+// warps (512 threads x 16 or 24 sets, 256 threads x 32) were slower still.
+constexpr int kRingLoads = 4, kRingDepth = 2;
 
 template <typename T, int BATCH>
 void *pick(int kind, bool vec) {
+    if constexpr (BATCH <= 2) {
+        if (kind == kRing) return reinterpret_cast<void *>(gemv_ring_kernel<T, BATCH, kRingLoads, kRingDepth, kStreamThreads>);
+    }
+
+
+
     if constexpr (BATCH <= 2 && sizeof(T) == 4) {
         if (kind == kPeel) return reinterpret_cast<void *>(gemv_stream_peel_kernel<BATCH>);
     }

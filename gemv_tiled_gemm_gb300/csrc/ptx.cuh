@@ -365,6 +365,33 @@ __device__ __forceinline__ uint2 ld_stream_u2(const void *p) {
     return v;
 }
 
+// The same loads under a predicate: with `pred` false nothing is read (the
+// address need not be valid) and the result is zero. The predicate sits on
+// the load instruction itself, so the caller's code has no branch around it.
+__device__ __forceinline__ float4 ld_stream_f4_if(const void *p, bool pred) {
+    float4 v;
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "mov.b32 %0, 0;\n\tmov.b32 %1, 0;\n\tmov.b32 %2, 0;\n\tmov.b32 %3, 0;\n\t"
+        "@q ld.global.nc.L1::no_allocate.L2::256B.v4.f32 {%0, %1, %2, %3}, [%4];\n\t}"
+        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+        : "l"(p), "r"(static_cast<int>(pred)));
+    return v;
+}
+
+__device__ __forceinline__ uint2 ld_stream_u2_if(const void *p, bool pred) {
+    uint2 v;
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %3, 0;\n\t"
+        "mov.b32 %0, 0;\n\tmov.b32 %1, 0;\n\t"
+        "@q ld.global.nc.L1::no_allocate.L2::256B.v2.u32 {%0, %1}, [%2];\n\t}"
+        : "=r"(v.x), "=r"(v.y)
+        : "l"(p), "r"(static_cast<int>(pred)));
+    return v;
+}
+
 __device__ __forceinline__ uint16_t ld_stream_u16(const uint16_t *p) {
     uint16_t v;
     asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));

@@ -67,13 +67,16 @@ GTG_API void gtg_conv_force_path(int mode);
 GTG_API void gtg_force_simt(int force);
 
 /*
- * gemv_bf16 with batch 3..8: by default (mode 0) such a call runs on the
- * tensor cores (the vectors split into three BF16 pieces each, see gemv_bf16)
- * when the tensor memory accelerator can read the matrix (16-byte aligned A,
- * lda * 2 a multiple of 16), it has at least 2^25 elements and batch >= 6,
- * else on the CUDA-core kernels. Mode 1 always takes the CUDA-core kernels;
- * mode 2 takes the tensor cores whenever the layout allows, at any size.
- * Other values act as 0.
+ * GEMV kernel choice. gemv_bf16 with batch 3..8: by default (mode 0) such a
+ * call runs on the tensor cores (the vectors split into three BF16 pieces
+ * each, see gemv_bf16) when the tensor memory accelerator can read the
+ * matrix (16-byte aligned A, lda * 2 a multiple of 16), it has at least 2^25
+ * elements and batch >= 6, else on the CUDA-core kernels. Mode 1 always takes
+ * the CUDA-core kernels; mode 2 takes the tensor cores whenever the layout
+ * allows, at any size. Mode 3 takes the CUDA-core kernels and, for one or two
+ * vectors, the streaming kernel (one row per warp) instead of the ring kernel
+ * (equal step ranges per warp) that mode 0 picks for FP32 rows and for BF16
+ * rows at batch 1 from 2^25 elements. Other values act as 0.
  */
 GTG_API void gtg_gemv_force_path(int mode);
 

@@ -267,11 +267,15 @@ def test_gemv_bf16_batch2_two_rows_per_warp(M, N, lda):
     g = PCG32(1080 + M + N)
     A = g.normal_bf16((M, N))
     X = g.uniform_f32((2, N))
-    plan = gtg.plan_gemv(M, N, 1 << 32, lda, 2 << 32, N, 3 << 32, M, 2, precision="bf16")
-    assert plan["kernel"] == "gemv" and plan["bm"] == 2 and plan["threads"] == 1024, plan
-    _check_gemv(A, X, run_gemv(A, X, lda=lda, prec="bf16"))
-    # batch 1 keeps one row per warp
-    assert gtg.plan_gemv(M, N, 1 << 32, lda, 2 << 32, N, 3 << 32, M, 1, precision="bf16")["bm"] == 1
+    gtg.gtg_gemv_force_path("no_ring")
+    try:
+        plan = gtg.plan_gemv(M, N, 1 << 32, lda, 2 << 32, N, 3 << 32, M, 2, precision="bf16")
+        assert plan["kernel"] == "gemv" and plan["bm"] == 2 and plan["threads"] == 1024, plan
+        _check_gemv(A, X, run_gemv(A, X, lda=lda, prec="bf16"))
+        # batch 1 keeps one row per warp
+        assert gtg.plan_gemv(M, N, 1 << 32, lda, 2 << 32, N, 3 << 32, M, 1, precision="bf16")["bm"] == 1
+    finally:
+        gtg.gtg_gemv_force_path("auto")
 
 
 @pytest.mark.parametrize("M,N,batch", [(4096, 4096, 8), (300, 16, 4), (2000, 1000, 3)])
