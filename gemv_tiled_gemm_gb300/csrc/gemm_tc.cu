@@ -18,7 +18,10 @@
 //   * epilogue: four warps read TMEM (tcgen05.ld, one row per thread) and
 //     store the rows that exist (row < M, col < N);
 //   * scheduling: a persistent grid (at most one CTA per SM) walks the
-//     output tiles in groups of GROUP row-tiles for L2 reuse.
+//     output tiles in groups of row-tiles for L2 reuse (the CTA-pair kernel:
+//     odd groups walk the columns backwards and odd waves read K from its
+//     end, so that each wave starts on the operand slices the previous one
+//     read last).
 //
 // Operand layouts: A is row-major M x K, i.e. "K-major" for the MMA; B is
 // row-major K x N, i.e. "MN-major". BF16 operands are read in their given
@@ -520,7 +523,17 @@ struct PairShape {
     static_assert(B_KMAJOR || B_CHUNKS * BCH_BYTES == B_BYTES, "MN-major B is whole column blocks");
 };
 
-constexpr int kPairGroup = 8;   // pair row-tiles per raster group
+// Raster of the pair kernel's tiles: groups of kPairGroup pair row-tiles,
+// each walked column by column (a wave of 76 clusters covers 12 row-tiles x
+// about 6 column-tiles), odd groups walking the columns right to left so that
+// a group starts on the B columns the previous one ended on. With the K order
+// alternating from wave to wave (see the producer), a wave starts on the A
+// and B slices the previous wave read last. DRAM reads per BF16 8192^3
+// launch (ncu): 1.086 GB with groups of 8 walked left to right, 0.873 with
+// both reversals, 0.826 = 3.08 x (A + B) with groups of 12 (groups of 4 / 6 /
+// 10 / 11 / 13 / 14 / 16: 1.106 / 1.000 / 0.915 / 0.854 / 0.881 / 0.896 /
+// 0.911 GB).
+constexpr int kPairGroup = 12;
 
 __device__ __forceinline__ void pair_tile_coords(int t, const TcParams &p, int &mb, int &nb) {
     const int per_group = kPairGroup * p.num_n;
@@ -530,6 +543,7 @@ __device__ __forceinline__ void pair_tile_coords(int t, const TcParams &p, int &
     const int r = t - g * per_group;
     mb = first + r % gs;
     nb = r / gs;
+    if (g & 1) nb = p.num_n - 1 - nb;
 }
 
 // Tile of pair-kernel unit tt: row tile mb, first column c0 and width w.
@@ -625,7 +639,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int col0 = c0 + static_cast<int>(rank) * (w / 2);
                 // both CTAs' A rows and B halves: (16 KB + w/2 columns x 128 B) each
                 const uint32_t stage_tx = 2u * static_cast<uint32_t>(S::A_BYTES + (w / 2) * 128);
-                for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
+                // odd waves read K from the end (the MMA only needs slices in
+                // matching pairs; accumulation order stays fixed per tile)
+                const bool rev = ((t - cluster_id) / nclusters) & 1;
+                for (int ki = u.kb0; ki < u.kb1; ++ki, ++it) {
+                    const int kb = rev ? u.kb1 - 1 - (ki - u.kb0) : ki;
                     const int s = static_cast<int>(it % S::STAGES);
                     const uint32_t ph = (it / S::STAGES) & 1u;
                     if (!wait_bar(empty_bar(s), ph ^ 1u, abort_flag, p)) {
@@ -680,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pair_tile(u.tt, p, mb, c0, w);
                 // the instruction descriptor's N (bits 17-22, N / 8) for this unit's width
                 const uint32_t idesc = (p.idesc & ~(0x3Fu << 17)) | (static_cast<uint32_t>(w >> 3) << 17);
-                for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {
+                for (int kb = u.kb0; kb < u.kb1; ++kb, ++it) {   // K order does not matter here: the stages hold it
                     const int s = static_cast<int>(it % S::STAGES);
                     const uint32_t ph = (it / S::STAGES) & 1u;
                     if (!wait_bar(full_bar(s), ph, abort_flag, p)) {
@@ -1249,7 +1267,7 @@ cudaError_t launch_impl(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
         if (!encode_3d(&tb, g.prec, g.B, g.N, g.K, g.ldb, g.batch, g.strideB, S::BCH_N, S::BK))
             return cudaErrorInvalidValue;
     }
-    TcParams p;
+    TcParams p{};
     p.C = g.C;
     p.ldc = g.ldc;
     p.M = static_cast<int>(g.M);
@@ -1321,7 +1339,7 @@ cudaError_t launch_pair(const DeviceInfo &dev, const GemmArgs &g, const gtg_plan
         if (!encode_3d(&tb, g.prec, g.B, g.N, g.K, g.ldb, g.batch, g.strideB, S::BCH_N, S::BK))
             return cudaErrorInvalidValue;
     }
-    TcParams p;
+    TcParams p{};
     p.C = g.C;
     p.ldc = g.ldc;
     p.M = static_cast<int>(g.M);
@@ -1441,7 +1459,7 @@ cudaError_t conv_launch_impl(const DeviceInfo &dev, const ConvArgs &c, cudaStrea
     CUtensorMap ta, tb;
     if (!encode_im2col(&ta, c)) return cudaErrorInvalidValue;
     if (!encode_3d(&tb, c.prec, c.Wt, c.CO, K, c.CO, 1, 0, S::BCH_N, S::BK)) return cudaErrorInvalidValue;
-    TcParams p;
+    TcParams p{};
     p.C = c.Y;
     p.ldc = c.CO;
     p.M = static_cast<int>(M);
@@ -1863,7 +1881,7 @@ cudaError_t launch_tf32_fixed(const DeviceInfo &dev, const GemmArgs &g, const gt
     // contents never matter and nothing needs clearing.
     cudaError_t e = transpose_launch(static_cast<const float *>(g.B), g.ldb, bt, ldbt, g.K, g.N, 1, 0, dev.status, stream);
     if (e != cudaSuccess) return e;
-    TcParams p;
+    TcParams p{};
     p.C = g.C;
     p.ldc = g.ldc;
     p.M = static_cast<int>(g.M);
