@@ -105,6 +105,7 @@ TESTING_SIGNATURES = {
                                           ctypes.POINTER(GtgPlan)]),
     "gtg_debug_build": (_int, []),
     "gtg_test_debug_shrink_extent": (_int, [_int]),
+    "gtg_plan_conv2d": (_int, [_int] + [_i64] * 13 + [_ptr, _ptr, _ptr, ctypes.POINTER(GtgPlan)]),
 }
 
 
@@ -276,8 +277,21 @@ def gtg_gemv_force_path(path="auto") -> None:
 
 
 def gtg_conv_force_path(mode: str) -> None:
-    """Testing hook: conv2d_nhwc path, "auto", "explicit" (im2col + GEMM) or "implicit"."""
-    lib().gtg_conv_force_path({"auto": 0, "explicit": 1, "implicit": 2}[mode])
+    """Testing hook: conv2d_nhwc path, "auto", "explicit" (im2col + GEMM),
+    "implicit" (any tensor-core kernel), "implicit_single" (single-CTA tiles)
+    or "implicit_pair" (CTA pairs)."""
+    lib().gtg_conv_force_path({"auto": 0, "explicit": 1, "implicit": 2, "implicit_single": 3,
+                               "implicit_pair": 4}[mode])
+
+
+def plan_conv2d(precision, N, H, W, C, CO, KH, KW, stride_h, stride_w, pad_h, pad_w, dil_h, dil_w, X, Wt, Y) -> dict:
+    """The kernel a conv2d_nhwc call with these arguments would run (testing probe)."""
+    plan = GtgPlan()
+    st = lib().gtg_plan_conv2d(PREC[precision], N, H, W, C, CO, KH, KW, stride_h, stride_w, pad_h, pad_w, dil_h,
+                               dil_w, X, Wt, Y, ctypes.byref(plan))
+    if st != GTG_OK:
+        raise GtgError(st, "gtg_plan_conv2d")
+    return plan.as_dict()
 
 
 def gtg_force_gemm_splits(splits: int) -> None:

@@ -385,7 +385,8 @@ gtg_status gemv_bf16_ex(int64_t M, int64_t N, const gtg_bf16 *A, int64_t lda, co
 }
 
 // Testing hook: 0 chooses the convolution path, 1 always writes the patch
-// matrix, 2 requires the implicit GEMM (GTG_ERR_UNSUPPORTED otherwise).
+// matrix, 2 requires the implicit GEMM (GTG_ERR_UNSUPPORTED otherwise), 3 and
+// 4 require it on single-CTA tiles or on CTA pairs.
 static std::atomic<int> g_conv_mode{0};
 
 static gtg_status validate_conv(ConvArgs &c) {
@@ -626,16 +627,18 @@ gtg_status conv2d_nhwc(int precision, int64_t N, int64_t H, int64_t W, int64_t C
     // a 1x1 window at stride 1 without padding reads X itself as the patch matrix
     const bool direct = KH == 1 && KW == 1 && stride_h == 1 && stride_w == 1 && pad_h == 0 && pad_w == 0;
     const int mode = g_conv_mode.load();
-    if ((mode == 2 || (mode == 0 && !direct)) && tc_conv_eligible(dev, c)) {
+    const bool implicit_only = mode >= 2;
+    if ((implicit_only || (mode == 0 && !direct)) && tc_conv_eligible(dev, c)) {
         // implicit GEMM: the tensor-core kernel reads the patches from X itself
-        const cudaError_t e = tc_conv_launch(dev, c, stream);
+        const cudaError_t e = tc_conv_launch(dev, c, stream, mode == 3 ? 1 : (mode == 4 ? 2 : 0));
+        if (e == cudaErrorNotSupported) return GTG_ERR_UNSUPPORTED;
         if (e != cudaSuccess) {
             note_cuda_error(e);
             return GTG_ERR_LAUNCH;
         }
         return GTG_OK;
     }
-    if (mode == 2) return GTG_ERR_UNSUPPORTED;
+    if (implicit_only) return GTG_ERR_UNSUPPORTED;
     const void *A = X;
     int64_t lda = C;
     void *P = nullptr;
@@ -722,7 +725,38 @@ void gtg_force_gemm_splits(int splits) { tc_force_splits(splits); }
 
 void gtg_force_c_store(int mode) { tc_force_c_store(mode); }
 
-void gtg_conv_force_path(int mode) { g_conv_mode.store(mode == 1 || mode == 2 ? mode : 0); }
+void gtg_conv_force_path(int mode) { g_conv_mode.store(mode >= 1 && mode <= 4 ? mode : 0); }
+
+gtg_status gtg_plan_conv2d(int precision, int64_t N, int64_t H, int64_t W, int64_t C, int64_t CO, int64_t KH,
+                           int64_t KW, int64_t stride_h, int64_t stride_w, int64_t pad_h, int64_t pad_w,
+                           int64_t dil_h, int64_t dil_w, const void *X, const void *Wt, const float *Y,
+                           gtg_plan *plan) {
+    if (plan == nullptr) return GTG_ERR_INVALID_VALUE;
+    ConvArgs c;
+    c.prec = precision;
+    c.N = N; c.H = H; c.W = W; c.C = C; c.CO = CO; c.KH = KH; c.KW = KW;
+    c.sh = stride_h; c.sw = stride_w; c.ph = pad_h; c.pw = pad_w; c.dh = dil_h; c.dw = dil_w;
+    c.X = X; c.Wt = Wt; c.Y = const_cast<float *>(Y);
+    gtg_status st = validate_conv(c);
+    if (st != GTG_OK) return st;
+    std::memset(plan, 0, sizeof(*plan));
+    if (N == 0 || CO == 0) return GTG_OK;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != GTG_OK) return st;
+    if (!(dev.cc_major == 10 && dev.cc_minor == 3)) return GTG_ERR_UNSUPPORTED;
+    const bool direct = KH == 1 && KW == 1 && stride_h == 1 && stride_w == 1 && pad_h == 0 && pad_w == 0;
+    const int mode = g_conv_mode.load();
+    if ((mode >= 2 || (mode == 0 && !direct)) && tc_conv_eligible(dev, c))
+        return tc_conv_plan(dev, c, mode == 3 ? 1 : (mode == 4 ? 2 : 0), plan) ? GTG_OK : GTG_ERR_UNSUPPORTED;
+    if (mode >= 2) return GTG_ERR_UNSUPPORTED;
+    // the explicit route: the plan of the product P x Wt (P's rows padded to 8 elements unless X is P)
+    const int64_t M = N * c.OH * c.OW, K = KH * KW * C;
+    const int64_t lda = direct ? C : (K + 7) / 8 * 8;
+    // (the patch matrix comes from the pool: 256-byte aligned)
+    const void *P = direct ? X : reinterpret_cast<const void *>(uintptr_t{1} << 40);
+    const GemmArgs g{precision, M, CO, K, P, lda, Wt, CO, c.Y, CO};
+    return plan_gemm_impl(dev, g, plan);
+}
 
 int gtg_version(void) { return 100; }
 

@@ -568,7 +568,10 @@ __device__ __noinline__ void spin_ns(uint64_t ns) {
     }
 }
 
-template <bool TF32>
+// IM2COL (16-bit only): A is the patch matrix of a convolution, each CTA's
+// 128 rows of a K slice one TMA im2col load from the channels-last image, as
+// in the single-CTA kernel.
+template <bool TF32, bool IM2COL = false>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const TcParams p) {
@@ -637,6 +640,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pair_tile(u.tt, p, mb, c0, w);
                 const int row0 = mb * 2 * S::BM + static_cast<int>(rank) * S::BM;
                 const int col0 = c0 + static_cast<int>(rank) * (w / 2);
+                int w0 = 0, h0 = 0, n0 = 0;   // IM2COL: window corner of this CTA's first output pixel
+                if constexpr (IM2COL) {
+                    const int q = row0 / p.cv_ow;
+                    w0 = (row0 - q * p.cv_ow) * p.cv_sw - p.cv_pw;
+                    h0 = (q % p.cv_oh) * p.cv_sh - p.cv_ph;
+                    n0 = q / p.cv_oh;
+                }
                 // both CTAs' A rows and B halves: (16 KB + w/2 columns x 128 B) each
                 const uint32_t stage_tx = 2u * static_cast<uint32_t>(S::A_BYTES + (w / 2) * 128);
                 // odd waves read K from the end (the MMA only needs slices in
@@ -653,7 +663,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (p.drop_slice == static_cast<int>(it) && cluster_id == 0 && leader) continue;
                     if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), stage_tx);
                     const uint32_t fb = leader_full0 + 8u * s;
-                    ptx::tma_load_3d_pair(sA + s * S::A_BYTES, &tmA, fb, kb * S::BK, row0, bi);
+                    if constexpr (IM2COL) {
+                        // K slice kb = (kh, kw, channel block cb)
+                        const int tap = kb / p.cv_cb, cb = kb - tap * p.cv_cb;
+                        const int kh = tap / p.cv_kw, kw = tap - kh * p.cv_kw;
+                        ptx::tma_load_im2col_4d_pair(sA + s * S::A_BYTES, &tmA, fb, cb * S::BK, w0, h0, n0,
+                                                     static_cast<uint16_t>(kw * p.cv_dw),
+                                                     static_cast<uint16_t>(kh * p.cv_dh));
+                    } else {
+                        ptx::tma_load_3d_pair(sA + s * S::A_BYTES, &tmA, fb, kb * S::BK, row0, bi);
+                    }
                     if constexpr (S::B_KMAJOR) {
                         // this CTA's 128 rows of B^T
                         ptx::tma_load_3d_pair(sB + s * S::B_BYTES, &tmB, fb, kb * S::BK, col0, bi);
@@ -1507,6 +1526,92 @@ cudaError_t conv_launch_impl(const DeviceInfo &dev, const ConvArgs &c, cudaStrea
     return finish_split(gg, p, ws, e, stream);
 }
 
+// Implicit-GEMM convolution on the CTA-pair kernel: 256 x 256 tiles of Y,
+// each CTA's 128 output pixels of a K slice one TMA im2col load (the map's
+// 128-pixel x 64-channel box is the single-CTA kernel's), half of B per CTA.
+cudaError_t conv_launch_pair(const DeviceInfo &dev, const ConvArgs &c, cudaStream_t stream, int splits) {
+    using S = PairShape<false>;
+    auto kern = tc_gemm_pair_kernel<false, true>;
+    {
+        AttrCache &ac = attr_cache();
+        std::lock_guard<std::mutex> lk(ac.mu);
+        const int d = dev.id & 63;
+        if (!(ac.done[d] >> 14 & 1)) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+            if (e != cudaSuccess) return e;
+            ac.done[d] |= 1ull << 14;
+        }
+    }
+    const int64_t M = c.N * c.OH * c.OW, K = c.KH * c.KW * c.C;
+    CUtensorMap ta, tb;
+    if (!encode_im2col(&ta, c)) return cudaErrorInvalidValue;
+    if (!encode_3d(&tb, c.prec, c.Wt, c.CO, K, c.CO, 1, 0, S::BCH_N, S::BK)) return cudaErrorInvalidValue;
+    TcParams p{};
+    p.C = c.Y;
+    p.ldc = c.CO;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(c.CO);
+    p.num_m = static_cast<int>((M + 2 * S::BM - 1) / (2 * S::BM));
+    p.num_n = static_cast<int>((c.CO + S::BN - 1) / S::BN);
+    p.num_kb = static_cast<int>(K / S::BK);
+    p.tiles_per_batch = p.num_m * p.num_n;
+    p.num_tiles = p.tiles_per_batch;
+    p.strideC = 0;
+    p.idesc = idesc16(c.prec, 2 * S::BM, S::BN);
+    const auto yaddr = reinterpret_cast<uintptr_t>(c.Y);
+    p.c_vec = ((yaddr & 31) == 0 && (c.CO & 7) == 0) ? 2 : (((yaddr & 15) == 0 && (c.CO & 3) == 0) ? 1 : 0);
+    p.tail_start = INT32_MAX;
+    p.c_tma = 0;
+    p.status = dev.status;
+    p.wait_limit_ns = wait_limit_ns();
+    p.drop_slice = take_drop_slice();
+    p.bias = c.bias;
+    p.act = c.act;
+    p.cv_ow = static_cast<int>(c.OW);
+    p.cv_oh = static_cast<int>(c.OH);
+    p.cv_cb = static_cast<int>(c.C / S::BK);
+    p.cv_kw = static_cast<int>(c.KW);
+    p.cv_sw = static_cast<int>(c.sw);
+    p.cv_sh = static_cast<int>(c.sh);
+    p.cv_pw = static_cast<int>(c.pw);
+    p.cv_ph = static_cast<int>(c.ph);
+    p.cv_dw = static_cast<int>(c.dw);
+    p.cv_dh = static_cast<int>(c.dh);
+    GemmArgs gg{c.prec, M, c.CO, K, nullptr, 0, nullptr, 0, c.Y, c.CO};
+    gg.bias = c.bias;
+    gg.act = c.act;
+    gtg_plan plan{};
+    plan.splits = splits;
+    float *ws = nullptr;
+    cudaError_t e = begin_split(gg, plan, p, &ws, stream);
+    const int clusters = static_cast<int>(std::min<int64_t>(p.num_units, dev.sms / 2));
+    // Y by tensor stores on the same terms as a GEMM's C (see launch_pair)
+    const int waves = (p.num_units + clusters - 1) / std::max(clusters, 1);
+    const int c_mode = g_c_store_mode.load();
+    CUtensorMap tc = ta;   // not read unless c_tma
+    p.c_tma = c_mode != 1 && (c_mode == 2 || p.num_kb <= 8 || waves <= 8) && p.splits == 1 &&
+              (yaddr & 15) == 0 && (c.CO & 3) == 0 &&
+              encode_3d(&tc, GTG_PREC_TF32, c.Y, c.CO, M, c.CO, 1, 0, 32, 32);
+    if (e == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = static_cast<size_t>(S::SMEM);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p);
+    }
+    return finish_split(gg, p, ws, e, stream);
+}
+
 }  // namespace
 
 
@@ -1564,6 +1669,7 @@ constexpr double kFillSlices = 4.0;
 constexpr double kReduceFixedUs = 3.0;   // the reduction's launch and allocation
 constexpr double kHbmBytesPerUs = 6.0e6;
 constexpr double kConvSlice = 2.0;        // an implicit convolution's K slice against a GEMM's
+constexpr double kConvPairRel = 1.0 / 1.15;   // a pair slice (256 x 256 per 2 SMs) against a 128 x 256 one
 double tc_cost(const DeviceInfo &dev, const GemmArgs &g, int bm, int bn, int slots, double rel, int splits,
                int bk_elems) {
     const int64_t num_kb = (g.K + bk_elems - 1) / bk_elems;
@@ -1671,13 +1777,15 @@ bool tc_conv_eligible(const DeviceInfo &dev, const ConvArgs &c) {
     return true;
 }
 
-cudaError_t tc_conv_launch(const DeviceInfo &dev, const ConvArgs &c, cudaStream_t stream) {
-    // tile width and K split by the same estimate as the GEMM planner (single
-    // CTAs), with a K slice of im2col loads costing about twice a GEMM's
-    // (measured on 3x3 layers of 64 to 512 channels: the estimate then picks
-    // the fastest of splits 1-6 and widths 64-256 on each, e.g. 512 -> 512
-    // channels at 7x7 x 64: 3 K ranges, 32.6 -> 22.1 us);
-    // gtg_force_gemm_splits applies here too
+// The implicit convolution's kernel: the width of single-CTA tiles (or the
+// CTA pair) and the K split, by the same estimate as the GEMM planner, with a
+// K slice of im2col loads costing about twice a GEMM's (measured on 3x3
+// layers of 64 to 512 channels: the estimate then picks the fastest of splits
+// 1-6 and widths 64-256 on each, e.g. 512 -> 512 channels at 7x7 x 64: 3 K
+// ranges, 32.6 -> 22.1 us). choice: 0 any kernel, 1 single CTAs only, 2 the
+// CTA pair only. gtg_force_gemm_splits applies here too. Returns false if
+// `choice` rules out every kernel.
+bool tc_conv_choose(const DeviceInfo &dev, const ConvArgs &c, int choice, bool *pair, int *width, int *splits) {
     GemmArgs g{c.prec, c.N * c.OH * c.OW, c.CO, c.KH * c.KW * c.C, nullptr, 0, nullptr, 0, nullptr, 0};
     const int64_t num_kb = g.K / 64;
     int forced = g_force_splits.load();
@@ -1685,28 +1793,70 @@ cudaError_t tc_conv_launch(const DeviceInfo &dev, const ConvArgs &c, cudaStream_
     const int split_opts[6] = {1, 2, 3, 4, 6, 8};
     const int widths[3] = {256, 128, 64};
     const double rel[3] = {1.0, 0.5 / 0.8, 0.25 / 0.5};
-    int best = 0, best_s = 1;
-    double best_cost = 0;
+    const bool pair_ok = choice != 1 && (dev.sms & 1) == 0 && g_pair_enabled.load();
     bool first = true;
+    double best_cost = 0;
     for (int si = 0; si < 6; ++si) {
         const int sp = forced > 0 ? forced : split_opts[si];
         if (forced > 0 && si > 0) break;
         if (sp > 1 && num_kb < 2 * sp) continue;
-        for (int i = 0; i < 3; ++i) {
-            const double cost = tc_cost(dev, g, kBM, widths[i], dev.sms, kConvSlice * rel[i], sp, 64);
+        if (choice != 2) {
+            for (int i = 0; i < 3; ++i) {
+                const double cost = tc_cost(dev, g, kBM, widths[i], dev.sms, kConvSlice * rel[i], sp, 64);
+                if (first || cost < best_cost) {
+                    *pair = false;
+                    *width = widths[i];
+                    *splits = sp;
+                    best_cost = cost;
+                    first = false;
+                }
+            }
+        }
+        if (pair_ok) {
+            const double cost = tc_cost(dev, g, 2 * kBM, 256, dev.sms / 2, kConvSlice * kConvPairRel, sp, 64);
             if (first || cost < best_cost) {
-                best = i;
-                best_s = sp;
+                *pair = true;
+                *width = 256;
+                *splits = sp;
                 best_cost = cost;
                 first = false;
             }
         }
     }
-    switch (widths[best]) {
-        case 256: return conv_launch_impl<256>(dev, c, stream, 7, best_s);
-        case 128: return conv_launch_impl<128>(dev, c, stream, 8, best_s);
-        default: return conv_launch_impl<64>(dev, c, stream, 9, best_s);
+    return !first;
+}
+
+cudaError_t tc_conv_launch(const DeviceInfo &dev, const ConvArgs &c, cudaStream_t stream, int choice) {
+    bool pair = false;
+    int width = 256, splits = 1;
+    if (!tc_conv_choose(dev, c, choice, &pair, &width, &splits)) return cudaErrorNotSupported;
+    if (pair) return conv_launch_pair(dev, c, stream, splits);
+    switch (width) {
+        case 256: return conv_launch_impl<256>(dev, c, stream, 7, splits);
+        case 128: return conv_launch_impl<128>(dev, c, stream, 8, splits);
+        default: return conv_launch_impl<64>(dev, c, stream, 9, splits);
     }
+}
+
+bool tc_conv_plan(const DeviceInfo &dev, const ConvArgs &c, int choice, gtg_plan *plan) {
+    bool pair = false;
+    int width = 256, splits = 1;
+    if (!tc_conv_choose(dev, c, choice, &pair, &width, &splits)) return false;
+    GemmArgs g{c.prec, c.N * c.OH * c.OW, c.CO, c.KH * c.KW * c.C, nullptr, 0, nullptr, 0, nullptr, 0};
+    if (pair) {
+        fill_pair_plan(dev, g, plan, splits);
+        // no half tiles for a convolution: every unit is a 256 x 256 tile (and K range)
+        const int64_t tiles = ((g.M + 255) / 256) * ((g.N + 255) / 256) * splits;
+        plan->grid = static_cast<int>(2 * std::min<int64_t>(tiles, dev.sms / 2));
+        return true;
+    }
+    switch (width) {
+        case 256: fill_plan<false, 256>(dev, g, plan, splits); break;
+        case 128: fill_plan<false, 128>(dev, g, plan, splits); break;
+        default: fill_plan<false, 64>(dev, g, plan, splits); break;
+    }
+    plan->threads = kThreads;
+    return true;
 }
 
 

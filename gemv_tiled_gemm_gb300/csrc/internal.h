@@ -157,8 +157,12 @@ uint64_t ws_alloc_count();   // ws_alloc calls so far (every device)
 
 // ---- implicit-GEMM convolution on the tensor cores (gemm_tc.cu): A tiles
 // loaded from X by TMA in im2col mode (16-bit, C % 64 == 0, small windows)
+// choice: 0 any kernel, 1 single-CTA tiles only, 2 the CTA pair only
+// (tc_conv_launch returns cudaErrorNotSupported, tc_conv_plan false, if
+// `choice` rules out every kernel)
 bool tc_conv_eligible(const DeviceInfo &dev, const ConvArgs &c);
-cudaError_t tc_conv_launch(const DeviceInfo &dev, const ConvArgs &c, cudaStream_t stream);
+cudaError_t tc_conv_launch(const DeviceInfo &dev, const ConvArgs &c, cudaStream_t stream, int choice);
+bool tc_conv_plan(const DeviceInfo &dev, const ConvArgs &c, int choice, gtg_plan *plan);
 
 // ---- im2col (im2col.cu): the patch matrix P (N*OH*OW x KH*KW*C, ldp >= K)
 cudaError_t im2col_launch(const DeviceInfo &dev, const ConvArgs &c, void *P, int64_t ldp, cudaStream_t stream);

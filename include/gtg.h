@@ -332,11 +332,17 @@ GTG_API gtg_status gemv_bf16_ex(int64_t M, int64_t N, const gtg_bf16 *A, int64_t
  *              OH = (H + 2 pad_h - dil_h (KH - 1) - 1) / stride_h + 1 (floor),
  *              OW likewise
  *   epilogue   optional bias (CO values, one per output channel) and activation
- * The call writes the patch matrix P (N*OH*OW x KH*KW*C, rows padded to a
- * multiple of 8 elements) into a temporary from the device's stream-ordered
- * memory pool, freed on the stream after the product; a 1x1 window with
- * stride 1 and no padding needs none (X is P). Then Y = P * Wt through the
- * GEMM kernels of gemm_<precision>.
+ * 16-bit layers with C a multiple of 64 (16-byte aligned X and Wt, CO a
+ * multiple of 8, window offsets below 256 and strides up to 8) run as an
+ * implicit GEMM: the tensor-core kernel (single-CTA tiles of 128 x 64..256 or
+ * CTA pairs with 256 x 256 tiles, whichever the planner estimates faster)
+ * loads each tile of the patch matrix straight from X with a TMA im2col copy,
+ * and no temporary is needed unless K is split. Other layers write the patch
+ * matrix P (N*OH*OW x KH*KW*C, rows padded to a multiple of 8 elements) into
+ * a temporary from the device's stream-ordered memory pool, freed on the
+ * stream after the product; a 1x1 window with stride 1 and no padding needs
+ * none (X is P). Then Y = P * Wt through the GEMM kernels of
+ * gemm_<precision>.
  * Errors: GTG_ERR_INVALID_VALUE for sizes < 1 (N, CO may be 0: nothing is
  * done), strides or dilations < 1, negative padding, a window larger than the
  * padded image, N*OH*OW or KH*KW*C above 2^31 - 1, an unknown precision or

@@ -56,11 +56,26 @@ GTG_API void gtg_force_c_store(int mode);
 /*
  * conv2d_nhwc: 0 (default) lets each call choose; 1 always writes the patch
  * matrix and multiplies it (im2col + GEMM); 2 requires the implicit GEMM,
- * whose tensor-core kernel loads the patches straight from X with TMA in
+ * whose tensor-core kernels load the patches straight from X with TMA in
  * im2col mode, and makes a call that cannot take it return
- * GTG_ERR_UNSUPPORTED.
+ * GTG_ERR_UNSUPPORTED; 3 and 4 require the implicit GEMM on single-CTA tiles
+ * (128 x 64..256) or on CTA pairs (256 x 256) respectively, likewise. Other
+ * values act as 0.
  */
 GTG_API void gtg_conv_force_path(int mode);
+
+/*
+ * Which kernel conv2d_nhwc would run for these arguments under the current
+ * gtg_conv_force_path mode (no launch, no device work apart from reading the
+ * device's properties once): the implicit GEMM's tensor-core kernel (bm, bn,
+ * cluster = 2 for CTA pairs, splits), or, for the im2col route, the plan of
+ * the product of the patch matrix and Wt. Returns the status the call itself
+ * would return before launching.
+ */
+GTG_API gtg_status gtg_plan_conv2d(int precision, int64_t N, int64_t H, int64_t W, int64_t C, int64_t CO,
+                                   int64_t KH, int64_t KW, int64_t stride_h, int64_t stride_w, int64_t pad_h,
+                                   int64_t pad_w, int64_t dil_h, int64_t dil_w, const void *X, const void *Wt,
+                                   const float *Y, gtg_plan *plan);
 
 /* Force the tensor-core GEMM paths onto the SIMT kernel (force = 1) or
  * restore the normal choice (force = 0). */
