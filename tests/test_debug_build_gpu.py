@@ -45,7 +45,7 @@ def _gemv(A, X, lda):
 
 
 @pytest.mark.parametrize("M,N,lda,batch", [
-    (700, 1024, 1024, 1),    # streaming kernel
+    (700, 1024, 1024, 1),    # ring kernel (one or two vectors)
     (700, 1024, 1024, 8),    # row blocks
     (700, 1023, 1025, 1),    # peeled rows, one per warp
     (700, 1023, 1025, 5),    # peeled row blocks
