@@ -10,7 +10,8 @@
 // that sets the speed.
 //
 // GB300 form:
-//   * a warp (not a thread) owns ROWS rows at a time and streams them with
+//   * a warp (not a thread) owns ROWS rows at a time (or, in the ring kernel,
+//     an equal range of row segments) and streams them with
 //     coalesced 128-bit loads that bypass L1 (each lane keeps U x ROWS loads
 //     in flight), so a row is one contiguous burst instead of the pages'
 //     one-row-per-thread pattern whose neighbouring threads are a full row
@@ -1145,7 +1146,9 @@ __global__ void __launch_bounds__(kPeelThreads, 1) gemv_stream_peel_kernel(const
 }
 
 // Kernel choice, for aligned rows: batch <= 2 with x in one staging chunk ->
-// gemv_stream_kernel (32 warps, one row each); batch >= 3 with x in one CTA ->
+// gemv_ring_kernel (32 warps, equal step ranges) for FP32 rows and for BF16
+// rows at batch 1 from 2^25 elements, else gemv_stream_kernel (32 warps, one
+// row each, two BF16 rows at batch 2); batch >= 3 with x in one CTA ->
 // gemv_blocks_kernel without a cluster (16 warps, 4 rows x half the columns
 // per task); x too large for one CTA -> gemv_blocks_kernel over a cluster.
 // Rows off 16 bytes with x in one chunk: FP32 batch <= 2 ->
