@@ -172,25 +172,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
             const long long fp = min(f1, f0 + kStages);   // the first stages: A now, the pieces after the wait
+            // unit f = (tile t, slice k), stepped without a 64-bit division per
+            // unit (measured: batch 8 at 8192^2 and 16384^2 0.5 us faster)
+            const int t0 = static_cast<int>(f0 / p.ks);
+            const int k0 = static_cast<int>(f0 - static_cast<long long>(t0) * p.ks);
+            int t = t0, k = k0;
+            auto next = [&] {
+                if (++k == p.ks) {
+                    k = 0;
+                    ++t;
+                }
+            };
             uint32_t it = 0;
-            for (long long f = f0; f < fp; ++f, ++it) {
+            for (long long f = f0; f < fp; ++f, ++it, next()) {
                 if (p.drop_slice == static_cast<int>(it) && blockIdx.x == 0) continue;
-                const int t = static_cast<int>(f / p.ks);
-                const int k = static_cast<int>(f - static_cast<long long>(t) * p.ks);
                 ptx::mbar_arrive_expect_tx(full_bar(static_cast<int>(it)), kStageBytes);
                 ptx::tma_load_3d(sA + it * kABytes, &tmA, full_bar(static_cast<int>(it)), k * kBK, t * kBM, 0);
             }
             ptx::wait_prior_grid();
             it = 0;
-            for (long long f = f0; f < fp; ++f, ++it) {
+            for (long long f = f0, kx = k0; f < fp; ++f, ++it, kx = kx + 1 == p.ks ? 0 : kx + 1) {
                 if (p.drop_slice == static_cast<int>(it) && blockIdx.x == 0) continue;
-                const int k = static_cast<int>(f - (f / p.ks) * p.ks);
-                ptx::tma_load_3d(sB + it * kBBytes, &tmX, full_bar(static_cast<int>(it)), k * kBK, 0, 0);
+                ptx::tma_load_3d(sB + it * kBBytes, &tmX, full_bar(static_cast<int>(it)), static_cast<int>(kx) * kBK,
+                                 0, 0);
             }
             bool ok = true;
-            for (long long f = fp; ok && f < f1; ++f, ++it) {
-                const int t = static_cast<int>(f / p.ks);
-                const int k = static_cast<int>(f - static_cast<long long>(t) * p.ks);
+            for (long long f = fp; ok && f < f1; ++f, ++it, next()) {
                 const int s = static_cast<int>(it % kStages);
                 const uint32_t ph = (it / kStages) & 1u;
                 if (!wait_bar(empty_bar(s), ph ^ 1u, abort_flag, p)) {
