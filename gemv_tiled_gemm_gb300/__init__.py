@@ -265,14 +265,16 @@ def gtg_force_simt(force: bool) -> None:
     lib().gtg_force_simt(1 if force else 0)
 
 
-GEMV_PATHS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2, "no_ring": 3}
+GEMV_PATHS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2, "no_ring": 3, "no_xi": 4}
 
 
 def gtg_gemv_force_path(path="auto") -> None:
     """Tuning/testing hook for the GEMV kernel choice: "auto" (the planner),
     "cuda_cores" or "tensor_cores" (BF16 matrices at batch 3-8, whenever the
-    layout allows), or "no_ring" (CUDA cores, and the streaming kernel
-    instead of the ring kernel for one or two vectors)."""
+    layout allows), "no_ring" (CUDA cores, and the streaming kernel
+    instead of the ring kernel for one or two vectors) or "no_xi" (CUDA
+    cores, and at batch 8 the vectors staged one after another instead of
+    interleaved)."""
     lib().gtg_gemv_force_path(GEMV_PATHS[path] if isinstance(path, str) else int(path))
 
 

@@ -16,7 +16,7 @@ std::atomic<int> g_gemv_skip_x{0};
 
 void gemv_skip_next_x(int on) { g_gemv_skip_x.store(on ? 1 : 0); }
 std::atomic<int> g_gemv_path{0};
-void gemv_force_path(int mode) { g_gemv_path.store(mode >= 1 && mode <= 3 ? mode : 0); }
+void gemv_force_path(int mode) { g_gemv_path.store(mode >= 1 && mode <= 4 ? mode : 0); }
 int take_gemv_skip_x() { return g_gemv_skip_x.exchange(0); }
 
 namespace {
@@ -156,6 +156,24 @@ Layout layout(const DeviceInfo &dev, const GemvArgs &g) {
         // partial sums of one CTA's rows: groups x segments x rows x batch floats
         const int64_t rows_cta = (g.M + dev.sms - 1) / dev.sms;
         const int64_t part = (rows_cta + kSplitRows - 1) / kSplitRows * kSplitSegs * kSplitRows * g.batch * 4;
+        if (g.batch == 8 && g_gemv_path.load() != 4) {
+            // the vectors staged interleaved, two per packed FMA (gemv_blocks_kernel
+            // with XI). Measured against the vectors staged one after another
+            // (one process, both forms, A rotated past L2, us): batch 8 FP32
+            // 4096^2 13.6 -> 13.2, 16384 x 4096 43.7 -> 42.5; BF16 4096^2
+            // 11.9 -> 11.3, 16384 x 4096 37.4 -> 32.4; but batch 4 FP32 / BF16
+            // 4096^2 11.4 / 8.4 -> 12.2 / 9.1 (the threads' staging of x costs
+            // more than the packed FMAs save), so batch 4 keeps the bulk copies
+            const int64_t xi_floats = (g.N + 3) / 4 * xi_group_floats(g.batch);
+            const int64_t xi_chunk = ((xi_floats + g.batch - 1) / g.batch + 3) / 4 * 4;
+            const int64_t smem = xi_chunk * g.batch * 4 + part;
+            if (smem <= limit) {
+                l.kind = kSplitXi;
+                l.chunk = static_cast<int>(xi_chunk);
+                l.smem = static_cast<int>(smem);
+                return l;
+            }
+        }
         if (l.smem + part <= limit) {
             l.kind = kSplit;
             l.smem = static_cast<int>(l.smem + part);
@@ -196,7 +214,7 @@ Layout layout(const DeviceInfo &dev, const GemvArgs &g) {
 
 void gemv_plan(const DeviceInfo &dev, const GemvArgs &g, gtg_plan *plan) {
     const int path = g_gemv_path.load();
-    if (path != 1 && path != 3 && gemv_tc_eligible(dev, g, path == 2)) {
+    if ((path == 0 || path == 2) && gemv_tc_eligible(dev, g, path == 2)) {
         gemv_tc_plan(dev, g, plan);
         return;
     }
@@ -219,7 +237,7 @@ void gemv_plan(const DeviceInfo &dev, const GemvArgs &g, gtg_plan *plan) {
     const bool two_rows = l.kind == kStream && g.a_elem == 2 && g.batch == 2;   // see pick() in gemv_kernels.cuh
     plan->bm = l.kind == kStream ? (two_rows ? 2 : 1) : (l.kind == kPeel ? 1 : (l.kind == kRound ? kRows : kSplitRows));
     plan->bn = l.chunk;
-    plan->bk = l.kind == kSplit || l.kind == kCluster || l.kind == kPeelSplit ? split_unroll(g.a_elem)
+    plan->bk = l.kind == kSplit || l.kind == kSplitXi || l.kind == kCluster || l.kind == kPeelSplit ? split_unroll(g.a_elem)
                                                                                : (two_rows ? 2 : kUnroll);
     plan->stages = l.nchunks;
     plan->grid = l.grid;

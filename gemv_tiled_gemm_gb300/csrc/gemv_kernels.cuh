@@ -279,6 +279,42 @@ __device__ __forceinline__ void fma_quad(float (&acc)[ROWS][BATCH], const typena
     }
 }
 
+// fma_quad with the vectors staged interleaved (XI): the BATCH values of
+// column c sit together at xg + (c % 4) * BATCH, xg the base of the lane's
+// group of four columns. Two vectors go through one packed FMA (the matrix
+// value in both halves, the two vectors' x values, the two sums): each sum
+// still takes its products in column order, one rounding each, as in
+// fma_quad.
+template <typename T, int ROWS, int BATCH>
+__device__ __forceinline__ void fma_quad_xi(float2 (&acc)[ROWS][BATCH / 2], const typename Quad<T>::Raw (&raw)[ROWS],
+                                            const float *xg) {
+    static_assert(BATCH % 4 == 0, "whole 16-byte reads of x");
+    float a[ROWS][4];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) Quad<T>::widen(raw[r], a[r]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        float2 xv[BATCH / 2];
+#pragma unroll
+        for (int q = 0; q < BATCH / 4; ++q) {
+            const float4 v = *reinterpret_cast<const float4 *>(xg + e * BATCH + 4 * q);
+            xv[2 * q] = make_float2(v.x, v.y);
+            xv[2 * q + 1] = make_float2(v.z, v.w);
+        }
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            const float2 ad = make_float2(a[r][e], a[r][e]);
+#pragma unroll
+            for (int h = 0; h < BATCH / 2; ++h) acc[r][h] = __ffma2_rn(ad, xv[h], acc[r][h]);
+        }
+    }
+}
+
+// XI layout: floats per group of four columns (their 4 x BATCH values and 16
+// bytes of padding, so that lanes reading consecutive groups meet different
+// shared-memory banks).
+__host__ __device__ constexpr int xi_group_floats(int batch) { return 4 * batch + 4; }
+
 // acc[r][b] += the four elements of row r at column h + 4j times vector b,
 // staged quad-transposed (entry c at (c % 4) * q + c / 4): lane j reads word
 // j (+1 past the wrap) of each of four quarter rows, so the 32 lanes read
@@ -628,6 +664,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const Params p
 // second cluster barrier keeps every CTA's shared memory alive until the
 // others have read it. p.chunk >= (block width + 1) * VE.
 //
+// XI (C = 1, BATCH a multiple of 4): the threads stage x interleaved, the
+// BATCH values of a column side by side (groups of four columns padded by 16
+// bytes, so lanes reading consecutive groups meet different banks), and the
+// arithmetic takes two vectors per packed FMA (fma_quad_xi): half the FMA
+// instructions, the same products in the same order, so the result is
+// bit-identical to the plain staging.
+//
 // PEEL (C = 1): rows that do not start on a boundary of the lane load (16
 // bytes FP32, 8 bytes BF16). Rows kPhase = 4 apart start 4 * lda elements
 // apart, a whole number of loads, so they share their offset from a load
@@ -638,9 +681,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const Params p
 // xq = p.chunk / 4), so the lanes' reads of one of the four columns of a unit
 // are consecutive words whatever h is. nu counts the whole units every row has
 // after its head; the at most six entries past them are single loads too.
-template <typename T, int BATCH, int ROWS, int WC, int U, int kThreads, bool CLUSTER, bool PEEL = false>
+template <typename T, int BATCH, int ROWS, int WC, int U, int kThreads, bool CLUSTER, bool PEEL = false,
+          bool XI = false>
 __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p) {
     static_assert(!PEEL || !CLUSTER, "peeled rows: one CTA per row block");
+    static_assert(!XI || (!PEEL && !CLUSTER && BATCH % 4 == 0), "interleaved vectors: one CTA, whole rows");
     constexpr int kPhase = 4;
     constexpr unsigned kLoadBytes = 4 * sizeof(T);   // one lane load: four entries
     constexpr int kWarps = kThreads / 32;
@@ -766,6 +811,40 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
     bool ok = true;
     if (p.x_bulk) {
         ok = __all_sync(0xFFFFFFFFu, wait_x(bar, p));
+    } else if constexpr (XI) {
+        // one thread per group of four columns: a 16-byte read of each vector
+        // (single reads at the end of x or for unaligned vectors), then the
+        // group's columns written out interleaved
+        constexpr int GS = xi_group_floats(BATCH);
+        const bool vec = (reinterpret_cast<uintptr_t>(p.x) & 15) == 0 && (p.ldx & 3) == 0;
+        for (int g = threadIdx.x; 4 * g < xlen; g += kThreads) {
+            const int c0 = 4 * g;
+            float v[BATCH][4];
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) {
+                const float *src = p.x + static_cast<long long>(b) * p.ldx + c0;
+                if (vec && c0 + 4 <= xlen) {
+                    const float4 t = __ldg(reinterpret_cast<const float4 *>(src));
+                    v[b][0] = t.x;
+                    v[b][1] = t.y;
+                    v[b][2] = t.z;
+                    v[b][3] = t.w;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) v[b][e] = c0 + e < xlen ? __ldg(src + e) : 0.f;
+                }
+            }
+            float *dst = xs + static_cast<long long>(g) * GS;
+            if (GV_S(dst, 16ull * BATCH)) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+#pragma unroll
+                    for (int q = 0; q < BATCH / 4; ++q)
+                        *reinterpret_cast<float4 *>(dst + e * BATCH + 4 * q) =
+                            make_float4(v[4 * q][e], v[4 * q + 1][e], v[4 * q + 2][e], v[4 * q + 3][e]);
+            }
+        }
+        __syncthreads();
     } else {
 #pragma unroll
         for (int b = 0; b < BATCH; ++b) {
@@ -790,7 +869,47 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
         for (int r = 0; r < ROWS; ++r)
 #pragma unroll
             for (int b = 0; b < BATCH; ++b) acc[r][b] = 0.f;
-        for (int jb = j0; jb < j1; jb += 32 * U) {
+        if constexpr (XI) {
+            constexpr int GS = xi_group_floats(BATCH);
+            float2 acc2[ROWS][BATCH / 2];
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+                for (int h = 0; h < BATCH / 2; ++h) acc2[r][h] = make_float2(0.f, 0.f);
+            for (int jb = j0; jb < j1; jb += 32 * U) {
+                Raw cur[U][ROWS];
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int r = 0; r < ROWS; ++r) cur[u][r] = nxt[u][r];
+                if (jb + 32 * U < j1) load(jb + 32 * U, nxt);
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int j = jb + 32 * u + lane;   // group j holds columns 4j .. 4j + 3
+                    if (j < j1) fma_quad_xi<T, ROWS, BATCH>(acc2, cur[u], xs + static_cast<long long>(j) * GS);
+                }
+            }
+            if (cs == WC - 1 && lane < tail) {
+                const int jt = VE * nub + lane;
+                const float *xc = xs + static_cast<long long>(jt >> 2) * GS + (jt & 3) * BATCH;
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r) {
+                    const T *q = arow[r] + jt;
+                    const float a = GV_A(q, sizeof(T)) ? Elem<T>::one(q) : 0.f;
+#pragma unroll
+                    for (int h = 0; h < BATCH / 2; ++h)
+                        acc2[r][h] = make_float2(fmaf(a, xc[2 * h], acc2[r][h].x), fmaf(a, xc[2 * h + 1], acc2[r][h].y));
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+                for (int h = 0; h < BATCH / 2; ++h) {
+                    acc[r][2 * h] = acc2[r][h].x;
+                    acc[r][2 * h + 1] = acc2[r][h].y;
+                }
+        }
+        for (int jb = j0; !XI && jb < j1; jb += 32 * U) {
             Raw cur[U][ROWS];
 #pragma unroll
             for (int u = 0; u < U; ++u)
@@ -824,7 +943,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
                 for (int col = h + VE * nu + lane; col < p.N; col += 32) single(col);
             }
         }
-        if (cs == WC - 1 && lane < tail) {
+        if (!XI && cs == WC - 1 && lane < tail) {
             const int jt = VE * nub + lane;
 #pragma unroll
             for (int r = 0; r < ROWS; ++r) {
@@ -1150,7 +1269,8 @@ __global__ void __launch_bounds__(kPeelThreads, 1) gemv_stream_peel_kernel(const
 // rows at batch 1 from 2^25 elements, else gemv_stream_kernel (32 warps, one
 // row each, two BF16 rows at batch 2); batch >= 3 with x in one CTA ->
 // gemv_blocks_kernel without a cluster (16 warps, 4 rows x half the columns
-// per task); x too large for one CTA -> gemv_blocks_kernel over a cluster.
+// per task; at batch 8 with the vectors staged interleaved, XI); x too large
+// for one CTA -> gemv_blocks_kernel over a cluster.
 // Rows off 16 bytes with x in one chunk: FP32 batch <= 2 ->
 // gemv_stream_peel_kernel; FP32 batch >= 3 and BF16 -> gemv_blocks_kernel
 // with PEEL. Otherwise gemv_kernel (16 warps, two rows per task, x chunked
@@ -1164,7 +1284,7 @@ constexpr int kSplitRows = 4, kSplitSegs = 2;
 // 16 bytes (FP32) or four of 8 bytes (BF16), the same bytes either way
 constexpr int split_unroll(int elem_bytes) { return elem_bytes == 2 ? 4 : 2; }
 
-enum Kind { kStream = 0, kSplit = 1, kRound = 2, kCluster = 3, kPeel = 4, kPeelSplit = 5, kRing = 6 };
+enum Kind { kStream = 0, kSplit = 1, kRound = 2, kCluster = 3, kPeel = 4, kPeelSplit = 5, kRing = 6, kSplitXi = 7 };
 
 // gemv_ring_kernel: 16-byte loads per ring set and sets in the ring.
 // Measured against other shapes of the ring at batch 1-2 (one process, CUDA
@@ -1201,6 +1321,11 @@ void *pick(int kind, bool vec) {
                 return reinterpret_cast<void *>(gemv_stream_kernel<T, BATCH, 2, 2, kStreamThreads>);
             return reinterpret_cast<void *>(gemv_stream_kernel<T, BATCH, 1, kUnroll, kStreamThreads>);
         }
+    }
+    if constexpr (BATCH % 4 == 0) {
+        if (kind == kSplitXi)
+            return reinterpret_cast<void *>(gemv_blocks_kernel<T, BATCH, kSplitRows, kSplitSegs, split_unroll(sizeof(T)),
+                                                               kRoundThreads, false, false, true>);
     }
     if (kind == kSplit)
         return reinterpret_cast<void *>(

@@ -91,7 +91,10 @@ GTG_API void gtg_force_simt(int force);
  * allows, at any size. Mode 3 takes the CUDA-core kernels and, for one or two
  * vectors, the streaming kernel (one row per warp) instead of the ring kernel
  * (equal step ranges per warp) that mode 0 picks for FP32 rows and for BF16
- * rows at batch 1 from 2^25 elements. Other values act as 0.
+ * rows at batch 1 from 2^25 elements. Mode 4 takes the CUDA-core kernels and,
+ * at batch 8, stages the vectors one after another by bulk copies instead of
+ * interleaved for packed FMAs (the same result, bit for bit). Other values
+ * act as 0.
  */
 GTG_API void gtg_gemv_force_path(int mode);
 

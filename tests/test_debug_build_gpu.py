@@ -46,7 +46,8 @@ def _gemv(A, X, lda):
 
 @pytest.mark.parametrize("M,N,lda,batch", [
     (700, 1024, 1024, 1),    # ring kernel (one or two vectors)
-    (700, 1024, 1024, 8),    # row blocks
+    (700, 1024, 1024, 8),    # row blocks, vectors staged interleaved by the threads
+    (700, 1024, 1024, 4),    # row blocks, vectors by bulk copies
     (700, 1023, 1025, 1),    # peeled rows, one per warp
     (700, 1023, 1025, 5),    # peeled row blocks
 ])
