@@ -568,9 +568,9 @@ __device__ __noinline__ void spin_ns(uint64_t ns) {
     }
 }
 
-// IM2COL (16-bit only): A is the patch matrix of a convolution, each CTA's
-// 128 rows of a K slice one TMA im2col load from the channels-last image, as
-// in the single-CTA kernel.
+// IM2COL: A is the patch matrix of a convolution, each CTA's 128 rows of a K
+// slice one TMA im2col load from the channels-last image (for TF32, the
+// rounded copy of it), as in the single-CTA kernel.
 template <bool TF32, bool IM2COL = false>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -1193,18 +1193,20 @@ PFN_cuTensorMapEncodeIm2col_v12000 encode_im2col_fn() {
 int im2col_lower(int64_t pad) { return static_cast<int>(-pad); }
 int im2col_upper(int64_t pad, int64_t window, int64_t dil) { return static_cast<int>(pad - (window - 1) * dil); }
 
-// X (N x H x W x C, 16-bit, channels last) as 128-pixel x 64-channel im2col tiles.
+// X (N x H x W x C, channels last) as im2col tiles of 128 pixels x one
+// 128-byte channel block (64 16-bit or 32 TF32 channels).
 bool encode_im2col(CUtensorMap *map, const ConvArgs &c) {
     auto fn = encode_im2col_fn();
     if (!fn) return false;
-    const uint64_t e = 2;
+    const uint64_t e = c.prec == GTG_PREC_TF32 ? 4 : 2;
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(c.C), static_cast<cuuint64_t>(c.W), static_cast<cuuint64_t>(c.H),
                           static_cast<cuuint64_t>(c.N)};
     cuuint64_t strides[3] = {c.C * e, c.W * c.C * e, c.H * c.W * c.C * e};
     int lower[2] = {im2col_lower(c.pw), im2col_lower(c.ph)};                   // W, then H
     int upper[2] = {im2col_upper(c.pw, c.KW, c.dw), im2col_upper(c.ph, c.KH, c.dh)};
     cuuint32_t estr[4] = {1, static_cast<cuuint32_t>(c.sw), static_cast<cuuint32_t>(c.sh), 1};
-    CUresult r = fn(map, tma_type(c.prec), 4, const_cast<void *>(c.X), dims, strides, lower, upper, 64, 128, estr,
+    CUresult r = fn(map, tma_type(c.prec), 4, const_cast<void *>(c.X), dims, strides, lower, upper,
+                    static_cast<cuuint32_t>(128 / e), 128, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -1458,12 +1460,13 @@ void fill_plan(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *plan, int spl
 }
 
 // Implicit-GEMM convolution on the single-CTA kernel: Y (N*OH*OW x CO) =
-// patches(X) x Wt with the A tiles loaded by TMA in im2col mode.
-template <int BN>
+// patches(X) x Wt with the A tiles loaded by TMA in im2col mode. TF32: X and
+// Wt are the rounded image and the rounded W^T (CO x K) of tc_conv_launch.
+template <bool TF32, int BN>
 cudaError_t conv_launch_impl(const DeviceInfo &dev, const ConvArgs &c, cudaStream_t stream, int attr_bit,
                              int splits) {
-    using S = Shape<false, BN>;
-    auto kern = tc_gemm_kernel<false, BN, true>;
+    using S = Shape<TF32, BN>;
+    auto kern = tc_gemm_kernel<TF32, BN, true>;
     {
         AttrCache &ac = attr_cache();
         std::lock_guard<std::mutex> lk(ac.mu);
@@ -1477,7 +1480,11 @@ cudaError_t conv_launch_impl(const DeviceInfo &dev, const ConvArgs &c, cudaStrea
     const int64_t M = c.N * c.OH * c.OW, K = c.KH * c.KW * c.C;
     CUtensorMap ta, tb;
     if (!encode_im2col(&ta, c)) return cudaErrorInvalidValue;
-    if (!encode_3d(&tb, c.prec, c.Wt, c.CO, K, c.CO, 1, 0, S::BCH_N, S::BK)) return cudaErrorInvalidValue;
+    if constexpr (TF32) {
+        if (!encode_3d(&tb, c.prec, c.Wt, K, c.CO, K, 1, 0, S::BK, BN)) return cudaErrorInvalidValue;
+    } else {
+        if (!encode_3d(&tb, c.prec, c.Wt, c.CO, K, c.CO, 1, 0, S::BCH_N, S::BK)) return cudaErrorInvalidValue;
+    }
     TcParams p{};
     p.C = c.Y;
     p.ldc = c.CO;
@@ -1492,7 +1499,7 @@ cudaError_t conv_launch_impl(const DeviceInfo &dev, const ConvArgs &c, cudaStrea
     p.kps = p.num_kb;
     p.num_units = p.num_tiles;
     p.strideC = 0;
-    p.idesc = idesc16(c.prec, S::BM, BN);
+    p.idesc = TF32 ? S::IDESC : idesc16(c.prec, S::BM, BN);
     const auto yaddr = reinterpret_cast<uintptr_t>(c.Y);
     p.c_vec = ((yaddr & 31) == 0 && (c.CO & 7) == 0) ? 2 : (((yaddr & 15) == 0 && (c.CO & 3) == 0) ? 1 : 0);
     p.tail_start = INT32_MAX;
@@ -1529,23 +1536,29 @@ cudaError_t conv_launch_impl(const DeviceInfo &dev, const ConvArgs &c, cudaStrea
 // Implicit-GEMM convolution on the CTA-pair kernel: 256 x 256 tiles of Y,
 // each CTA's 128 output pixels of a K slice one TMA im2col load (the map's
 // 128-pixel x 64-channel box is the single-CTA kernel's), half of B per CTA.
-cudaError_t conv_launch_pair(const DeviceInfo &dev, const ConvArgs &c, cudaStream_t stream, int splits) {
-    using S = PairShape<false>;
-    auto kern = tc_gemm_pair_kernel<false, true>;
+template <bool TF32>
+cudaError_t conv_launch_pair(const DeviceInfo &dev, const ConvArgs &c, cudaStream_t stream, int splits, int attr_bit) {
+    using S = PairShape<TF32>;
+    auto kern = tc_gemm_pair_kernel<TF32, true>;
     {
         AttrCache &ac = attr_cache();
         std::lock_guard<std::mutex> lk(ac.mu);
         const int d = dev.id & 63;
-        if (!(ac.done[d] >> 14 & 1)) {
+        if (!(ac.done[d] >> attr_bit & 1)) {
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
             if (e != cudaSuccess) return e;
-            ac.done[d] |= 1ull << 14;
+            ac.done[d] |= 1ull << attr_bit;
         }
     }
     const int64_t M = c.N * c.OH * c.OW, K = c.KH * c.KW * c.C;
     CUtensorMap ta, tb;
     if (!encode_im2col(&ta, c)) return cudaErrorInvalidValue;
-    if (!encode_3d(&tb, c.prec, c.Wt, c.CO, K, c.CO, 1, 0, S::BCH_N, S::BK)) return cudaErrorInvalidValue;
+    if constexpr (TF32) {
+        // this CTA's 128 rows of the rounded W^T
+        if (!encode_3d(&tb, c.prec, c.Wt, K, c.CO, K, 1, 0, S::BK, S::BN / 2)) return cudaErrorInvalidValue;
+    } else {
+        if (!encode_3d(&tb, c.prec, c.Wt, c.CO, K, c.CO, 1, 0, S::BCH_N, S::BK)) return cudaErrorInvalidValue;
+    }
     TcParams p{};
     p.C = c.Y;
     p.ldc = c.CO;
@@ -1557,7 +1570,7 @@ cudaError_t conv_launch_pair(const DeviceInfo &dev, const ConvArgs &c, cudaStrea
     p.tiles_per_batch = p.num_m * p.num_n;
     p.num_tiles = p.tiles_per_batch;
     p.strideC = 0;
-    p.idesc = idesc16(c.prec, 2 * S::BM, S::BN);
+    p.idesc = TF32 ? ptx::make_idesc(2u, 0u, 0u, 2 * S::BM, S::BN) : idesc16(c.prec, 2 * S::BM, S::BN);
     const auto yaddr = reinterpret_cast<uintptr_t>(c.Y);
     p.c_vec = ((yaddr & 31) == 0 && (c.CO & 7) == 0) ? 2 : (((yaddr & 15) == 0 && (c.CO & 3) == 0) ? 1 : 0);
     p.tail_start = INT32_MAX;
@@ -1765,9 +1778,14 @@ void tc_plan_unsplit_single(const DeviceInfo &dev, const GemmArgs &g, gtg_plan *
 
 bool tc_conv_eligible(const DeviceInfo &dev, const ConvArgs &c) {
     if (!tc_supported(dev) || encode_im2col_fn() == nullptr) return false;
-    if (c.prec != GTG_PREC_BF16 && c.prec != GTG_PREC_F16) return false;
-    if (c.C % 64 || (c.CO * 2) % 16) return false;                          // 128-byte channel blocks, B rows
-    if ((reinterpret_cast<uintptr_t>(c.X) & 15) || (reinterpret_cast<uintptr_t>(c.Wt) & 15)) return false;
+    if (c.prec == GTG_PREC_TF32) {
+        // X and Wt are read through their rounded copies (any alignment)
+        if (c.C % 32) return false;                                          // 128-byte channel blocks
+    } else {
+        if (c.prec != GTG_PREC_BF16 && c.prec != GTG_PREC_F16) return false;
+        if (c.C % 64 || (c.CO * 2) % 16) return false;                      // 128-byte channel blocks, B rows
+        if ((reinterpret_cast<uintptr_t>(c.X) & 15) || (reinterpret_cast<uintptr_t>(c.Wt) & 15)) return false;
+    }
     if (c.sw > 8 || c.sh > 8) return false;                                  // TMA traversal steps
     const int64_t corners[4] = {-c.pw, -c.ph, c.pw - (c.KW - 1) * c.dw, c.ph - (c.KH - 1) * c.dh};
     for (int64_t v : corners)
@@ -1787,7 +1805,8 @@ bool tc_conv_eligible(const DeviceInfo &dev, const ConvArgs &c) {
 // `choice` rules out every kernel.
 bool tc_conv_choose(const DeviceInfo &dev, const ConvArgs &c, int choice, bool *pair, int *width, int *splits) {
     GemmArgs g{c.prec, c.N * c.OH * c.OW, c.CO, c.KH * c.KW * c.C, nullptr, 0, nullptr, 0, nullptr, 0};
-    const int64_t num_kb = g.K / 64;
+    const int bk = c.prec == GTG_PREC_TF32 ? 32 : 64;   // K elements per 128-byte slice
+    const int64_t num_kb = g.K / bk;
     int forced = g_force_splits.load();
     if (forced > 1 && num_kb < 2 * forced) forced = 0;
     const int split_opts[6] = {1, 2, 3, 4, 6, 8};
@@ -1802,7 +1821,7 @@ bool tc_conv_choose(const DeviceInfo &dev, const ConvArgs &c, int choice, bool *
         if (sp > 1 && num_kb < 2 * sp) continue;
         if (choice != 2) {
             for (int i = 0; i < 3; ++i) {
-                const double cost = tc_cost(dev, g, kBM, widths[i], dev.sms, kConvSlice * rel[i], sp, 64);
+                const double cost = tc_cost(dev, g, kBM, widths[i], dev.sms, kConvSlice * rel[i], sp, bk);
                 if (first || cost < best_cost) {
                     *pair = false;
                     *width = widths[i];
@@ -1813,7 +1832,7 @@ bool tc_conv_choose(const DeviceInfo &dev, const ConvArgs &c, int choice, bool *
             }
         }
         if (pair_ok) {
-            const double cost = tc_cost(dev, g, 2 * kBM, 256, dev.sms / 2, kConvSlice * kConvPairRel, sp, 64);
+            const double cost = tc_cost(dev, g, 2 * kBM, 256, dev.sms / 2, kConvSlice * kConvPairRel, sp, bk);
             if (first || cost < best_cost) {
                 *pair = true;
                 *width = 256;
@@ -1830,12 +1849,47 @@ cudaError_t tc_conv_launch(const DeviceInfo &dev, const ConvArgs &c, cudaStream_
     bool pair = false;
     int width = 256, splits = 1;
     if (!tc_conv_choose(dev, c, choice, &pair, &width, &splits)) return cudaErrorNotSupported;
-    if (pair) return conv_launch_pair(dev, c, stream, splits);
-    switch (width) {
-        case 256: return conv_launch_impl<256>(dev, c, stream, 7, splits);
-        case 128: return conv_launch_impl<128>(dev, c, stream, 8, splits);
-        default: return conv_launch_impl<64>(dev, c, stream, 9, splits);
+    if (c.prec != GTG_PREC_TF32) {
+        if (pair) return conv_launch_pair<false>(dev, c, stream, splits, 14);
+        switch (width) {
+            case 256: return conv_launch_impl<false, 256>(dev, c, stream, 7, splits);
+            case 128: return conv_launch_impl<false, 128>(dev, c, stream, 8, splits);
+            default: return conv_launch_impl<false, 64>(dev, c, stream, 9, splits);
+        }
     }
+    // TF32: the MMA truncates its operands, so the image and the weights are
+    // first rounded to the nearest TF32 value (as gemm_tf32 does), the image
+    // into a copy of its own size (not the KH*KW times larger patch matrix),
+    // the weights into W^T (CO x K, the K-major B of the TF32 kernels); the
+    // product then reads the patches from the rounded image
+    const int64_t pixels = c.N * c.H * c.W, K = c.KH * c.KW * c.C;
+    const size_t x_bytes = (static_cast<size_t>(pixels * c.C) * 4 + 255) / 256 * 256;
+    const size_t w_bytes = static_cast<size_t>(c.CO * K) * 4;
+    void *ws = nullptr;
+    cudaError_t e = ws_alloc(&ws, x_bytes + w_bytes, stream);
+    if (e != cudaSuccess) return e;
+    float *Xr = static_cast<float *>(ws);
+    float *Wr = reinterpret_cast<float *>(static_cast<char *>(ws) + x_bytes);
+    GemmArgs gx{GTG_PREC_TF32, pixels, 0, c.C, c.X, c.C, nullptr, 0, nullptr, 0};   // the image alone (no B)
+    e = tf32_prep_launch(dev, gx, Xr, nullptr, c.C, 1, 1, stream);
+    if (e == cudaSuccess)
+        e = transpose_launch(static_cast<const float *>(c.Wt), c.CO, Wr, K, K, c.CO, 1, 0, dev.status, stream);
+    ConvArgs cr = c;
+    cr.X = Xr;
+    cr.Wt = Wr;
+    if (e == cudaSuccess) {
+        if (pair) {
+            e = conv_launch_pair<true>(dev, cr, stream, splits, 18);
+        } else {
+            switch (width) {
+                case 256: e = conv_launch_impl<true, 256>(dev, cr, stream, 15, splits); break;
+                case 128: e = conv_launch_impl<true, 128>(dev, cr, stream, 16, splits); break;
+                default: e = conv_launch_impl<true, 64>(dev, cr, stream, 17, splits); break;
+            }
+        }
+    }
+    const cudaError_t f = cudaFreeAsync(ws, stream);   // stream-ordered: after the product has read it
+    return e != cudaSuccess ? e : f;
 }
 
 bool tc_conv_plan(const DeviceInfo &dev, const ConvArgs &c, int choice, gtg_plan *plan) {
@@ -1850,10 +1904,11 @@ bool tc_conv_plan(const DeviceInfo &dev, const ConvArgs &c, int choice, gtg_plan
         plan->grid = static_cast<int>(2 * std::min<int64_t>(tiles, dev.sms / 2));
         return true;
     }
+    const bool tf32 = c.prec == GTG_PREC_TF32;
     switch (width) {
-        case 256: fill_plan<false, 256>(dev, g, plan, splits); break;
-        case 128: fill_plan<false, 128>(dev, g, plan, splits); break;
-        default: fill_plan<false, 64>(dev, g, plan, splits); break;
+        case 256: tf32 ? fill_plan<true, 256>(dev, g, plan, splits) : fill_plan<false, 256>(dev, g, plan, splits); break;
+        case 128: tf32 ? fill_plan<true, 128>(dev, g, plan, splits) : fill_plan<false, 128>(dev, g, plan, splits); break;
+        default: tf32 ? fill_plan<true, 64>(dev, g, plan, splits) : fill_plan<false, 64>(dev, g, plan, splits); break;
     }
     plan->threads = kThreads;
     return true;

@@ -337,7 +337,10 @@ GTG_API gtg_status gemv_bf16_ex(int64_t M, int64_t N, const gtg_bf16 *A, int64_t
  * implicit GEMM: the tensor-core kernel (single-CTA tiles of 128 x 64..256 or
  * CTA pairs with 256 x 256 tiles, whichever the planner estimates faster)
  * loads each tile of the patch matrix straight from X with a TMA im2col copy,
- * and no temporary is needed unless K is split. Other layers write the patch
+ * and no temporary is needed unless K is split. TF32 layers with C a multiple
+ * of 32 (same window and stride limits, any alignment) take the same route
+ * from a copy of X rounded to TF32 (a temporary of X's size from the pool)
+ * and the rounded W^T (CO x K), as gemm_tf32 rounds its operands. Other layers write the patch
  * matrix P (N*OH*OW x KH*KW*C, rows padded to a multiple of 8 elements) into
  * a temporary from the device's stream-ordered memory pool, freed on the
  * stream after the product; a 1x1 window with stride 1 and no padding needs
