@@ -45,6 +45,10 @@ CONV_LAYERS = [
     ("f4: bf16 conv 1x1 256->1024, 14x14, batch 64", 64, 14, 14, 256, 1024, 1, 1, 1, 0, 20),
     ("f4: bf16 conv 7x7/2 3->64, 224x224, batch 16, pad 3", 16, 224, 224, 3, 64, 7, 7, 2, 3, 10),
 ]
+# the same network's layers in TF32 (FP32 storage): implicit GEMM from a rounded copy of the image
+CONV_LAYERS_TF32 = [
+    ("f4: tf32 conv 3x3 256->256, 56x56, batch 16, pad 1", 16, 56, 56, 256, 256, 3, 3, 1, 1, 10),
+]
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # the part's nominal figures (dense BF16 tensor rate, HBM3e bandwidth), reported
 # beside the measured denominators
@@ -606,15 +610,21 @@ def sweep(dev, stream, peaks, l2):
                                   2 * batch * M * K + 2 * (1 if shared_B else batch) * K * N + 4 * batch * M * N,
                                   ms, bf16_peak, "tensor")})
 
-    def conv_cfg(name, N, H, W, C, CO, KH, KW, st, pd, iters):
+    def conv_cfg(name, N, H, W, C, CO, KH, KW, st, pd, iters, prec="bf16"):
         g = PCG32(20 + C + CO)
-        X = torch.from_numpy(g.normal_bf16((N, H, W, C)).view(np.int16)).to(dev)
-        Wt = torch.from_numpy(g.normal_bf16((KH, KW, C, CO), (KH * KW * C) ** -0.5).view(np.int16)).to(dev)
+        if prec == "tf32":
+            X = torch.from_numpy(g.uniform_f32((N, H, W, C))).to(dev)
+            Wt = torch.from_numpy(g.uniform_f32((KH, KW, C, CO)) * np.float32((KH * KW * C) ** -0.5)).to(dev)
+            esz, peak, peak_name = 4, tf32_peak, "bf16 burst / 2 (derived)"
+        else:
+            X = torch.from_numpy(g.normal_bf16((N, H, W, C)).view(np.int16)).to(dev)
+            Wt = torch.from_numpy(g.normal_bf16((KH, KW, C, CO), (KH * KW * C) ** -0.5).view(np.int16)).to(dev)
+            esz, peak, peak_name = 2, bf16_peak, "bf16 burst"
         OH, OW = gtg.conv_out_size(H, W, KH, KW, st, pd)
         Y = torch.empty((N, OH, OW, CO), device=dev)
 
         def call(i):
-            rc = gtg.conv2d_nhwc("bf16", N, H, W, C, CO, KH, KW, st, st, pd, pd, 1, 1, X.data_ptr(), Wt.data_ptr(),
+            rc = gtg.conv2d_nhwc(prec, N, H, W, C, CO, KH, KW, st, st, pd, pd, 1, 1, X.data_ptr(), Wt.data_ptr(),
                                  Y.data_ptr(), None, sh)
             assert rc == gtg.GTG_OK, rc
 
@@ -623,22 +633,25 @@ def sweep(dev, stream, peaks, l2):
         tf = 2.0 * M * K * CO / (ms * 1e-3) / 1e12
         direct = KH == 1 and KW == 1 and st == 1 and pd == 0
         # the implicit GEMM takes 16-bit layers with whole 64-channel blocks
-        # (the bench's window sizes, strides and paddings are all within its limits)
-        implicit = not direct and C % 64 == 0 and CO % 8 == 0
-        plan = gtg.plan_conv2d("bf16", N, H, W, C, CO, KH, KW, st, st, pd, pd, 1, 1, X.data_ptr(), Wt.data_ptr(),
+        # and TF32 layers with whole 32-channel blocks (the bench's window
+        # sizes, strides and paddings are all within its limits)
+        implicit = not direct and (C % 32 == 0 if prec == "tf32" else (C % 64 == 0 and CO % 8 == 0))
+        plan = gtg.plan_conv2d(prec, N, H, W, C, CO, KH, KW, st, st, pd, pd, 1, 1, X.data_ptr(), Wt.data_ptr(),
                                Y.data_ptr())
         kern = (f"CTA pair {plan['bm']}x{plan['bn']}" if plan["cluster"] == 2 else f"{plan['bm']}x{plan['bn']} tiles")
         kern += f", {plan['splits']} K ranges" if plan["splits"] > 1 else ""
         label = ("implicit GEMM" if implicit else ("GEMM on X" if direct else "im2col + GEMM")) + f"; {kern}"
-        out.append({"config": name, "path": f"bf16 conv ({label})",
-                    "gemm_shape": [M, CO, K], "ms": round(ms, 4), "ms_best": round(ms_best, 4), "TFLOP/s": round(tf, 2), "peak": bf16_peak,
-                    "peak_name": "bf16 burst", "frac": round(tf / bf16_peak, 4),
-                    "im2col_bytes": 0 if (direct or implicit) else M * ((K + 7) // 8 * 8) * 2,
-                    **roofline_of(2.0 * M * K * CO, 2 * N * H * W * C + 2 * KH * KW * C * CO + 4 * M * CO, ms, bf16_peak,
+        out.append({"config": name, "path": f"{prec} conv ({label})",
+                    "gemm_shape": [M, CO, K], "ms": round(ms, 4), "ms_best": round(ms_best, 4), "TFLOP/s": round(tf, 2), "peak": peak,
+                    "peak_name": peak_name, "frac": round(tf / peak, 4),
+                    "im2col_bytes": 0 if (direct or implicit) else M * ((K + 7) // 8 * 8) * esz,
+                    **roofline_of(2.0 * M * K * CO, esz * (N * H * W * C + KH * KW * C * CO) + 4 * M * CO, ms, peak,
                                   "tensor")})
 
     for layer in CONV_LAYERS:
         conv_cfg(*layer)
+    for layer in CONV_LAYERS_TF32:
+        conv_cfg(*layer, prec="tf32")
     torch.cuda.empty_cache()
 
     batched_cfg("f2: bf16 strided batch 16 x 2048^3", 16, 2048, 2048, 2048, 20)
