@@ -37,8 +37,8 @@ struct Layout {
     int kind;
     int threads;
     int grid;
-    int cluster;   // CTAs per cluster (column blocks); 1 unless kind == kCluster
-    int ublock;    // kCluster: 4-column units per column block
+    int cluster;   // CTAs per cluster (column blocks); 1 unless kind is kCluster or kClusterXi
+    int ublock;    // kCluster, kClusterXi: 4-column units per column block
 };
 
 void *kernel_of(const GemvArgs &g, int kind) {
@@ -49,16 +49,16 @@ void *kernel_of(const GemvArgs &g, int kind) {
 // once. Not every cluster size tiles the GPU's SMs: on a 152-SM GB300 all 76
 // pairs fit but only 36 of 38 quads, so the grid is sized to what fits (a
 // second wave of clusters would double the time). Cached per configuration.
-int max_active_clusters(const DeviceInfo &dev, const GemvArgs &g, int cluster, int smem, int grid) {
+int max_active_clusters(const DeviceInfo &dev, const GemvArgs &g, int kind, int cluster, int smem, int grid) {
     static std::mutex mu;
-    static std::map<std::tuple<int, int, int, int, int>, int> cache;
-    const auto key = std::make_tuple(dev.id, g.a_elem, g.batch, cluster, smem);
+    static std::map<std::tuple<int, int, int, int, int, int>, int> cache;
+    const auto key = std::make_tuple(dev.id, g.a_elem, g.batch, kind, cluster, smem);
     {
         std::lock_guard<std::mutex> lock(mu);
         auto it = cache.find(key);
         if (it != cache.end()) return it->second;
     }
-    void *kern = kernel_of(g, kCluster);
+    void *kern = kernel_of(g, kind);
     int n = 0;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
         cudaLaunchConfig_t cfg = {};
@@ -182,30 +182,40 @@ Layout layout(const DeviceInfo &dev, const GemvArgs &g) {
     }
     // x does not fit one CTA: split the columns over the CTAs of a cluster
     // (units of the blocks kernel's four-column loads)
+    // (units of the blocks kernel's four-column loads); at batch 8 each CTA's
+    // block of the vectors is staged interleaved (XI) where it fits, else as
+    // one vector after another
     const int VE = 4;
     const int64_t nu = g.N / VE;
+    const bool xi_ok = g.batch == 8 && g_gemv_path.load() != 4;
     for (int C = 2; C <= 8; C *= 2) {
-        int grid = dev.sms / C * C;
-        if (grid == 0) continue;
         const int ub = static_cast<int>((nu + C - 1) / C);
-        const int cchunk = ((ub + 1) * VE + 7) / 8 * 8;
-        int smem = cluster_smem(g, static_cast<int>((g.M + grid / C - 1) / (grid / C)), cchunk);
-        if (smem > limit) continue;
-        const int fit = max_active_clusters(dev, g, C, smem, grid);
-        if (fit <= 0) continue;
-        if (fit < grid / C) {
-            grid = fit * C;
-            smem = cluster_smem(g, static_cast<int>((g.M + fit - 1) / fit), cchunk);
+        for (int xi = xi_ok ? 1 : 0; xi >= 0; --xi) {
+            int grid = dev.sms / C * C;
+            if (grid == 0) continue;
+            // staged floats per vector: the block's units and the trailing entries
+            const int cchunk = xi ? static_cast<int>(((int64_t{ub} + 1) * xi_group_floats(g.batch) + g.batch - 1) /
+                                                     g.batch + 3) / 4 * 4
+                                  : ((ub + 1) * VE + 7) / 8 * 8;
+            const int kind = xi ? kClusterXi : kCluster;
+            int smem = cluster_smem(g, static_cast<int>((g.M + grid / C - 1) / (grid / C)), cchunk);
             if (smem > limit) continue;
+            const int fit = max_active_clusters(dev, g, kind, C, smem, grid);
+            if (fit <= 0) continue;
+            if (fit < grid / C) {
+                grid = fit * C;
+                smem = cluster_smem(g, static_cast<int>((g.M + fit - 1) / fit), cchunk);
+                if (smem > limit) continue;
+            }
+            l.kind = kind;
+            l.cluster = C;
+            l.grid = grid;
+            l.chunk = cchunk;
+            l.nchunks = 1;
+            l.ublock = ub;
+            l.smem = smem;
+            return l;
         }
-        l.kind = kCluster;
-        l.cluster = C;
-        l.grid = grid;
-        l.chunk = cchunk;
-        l.nchunks = 1;
-        l.ublock = ub;
-        l.smem = smem;
-        return l;
     }
     return l;   // the round kernel, x staged chunk by chunk
 }
@@ -237,8 +247,9 @@ void gemv_plan(const DeviceInfo &dev, const GemvArgs &g, gtg_plan *plan) {
     const bool two_rows = l.kind == kStream && g.a_elem == 2 && g.batch == 2;   // see pick() in gemv_kernels.cuh
     plan->bm = l.kind == kStream ? (two_rows ? 2 : 1) : (l.kind == kPeel ? 1 : (l.kind == kRound ? kRows : kSplitRows));
     plan->bn = l.chunk;
-    plan->bk = l.kind == kSplit || l.kind == kSplitXi || l.kind == kCluster || l.kind == kPeelSplit ? split_unroll(g.a_elem)
-                                                                               : (two_rows ? 2 : kUnroll);
+    const bool blocks = l.kind == kSplit || l.kind == kSplitXi || l.kind == kCluster || l.kind == kClusterXi ||
+                        l.kind == kPeelSplit;
+    plan->bk = blocks ? split_unroll(g.a_elem) : (two_rows ? 2 : kUnroll);
     plan->stages = l.nchunks;
     plan->grid = l.grid;
     plan->threads = l.threads;
@@ -294,7 +305,7 @@ cudaError_t gemv_launch(const DeviceInfo &dev, const GemvArgs &g, const gtg_plan
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = l.kind == kCluster ? 2 : 1;
+    cfg.numAttrs = l.kind == kCluster || l.kind == kClusterXi ? 2 : 1;
     return cudaLaunchKernelExC(&cfg, kern, args);
 }
 

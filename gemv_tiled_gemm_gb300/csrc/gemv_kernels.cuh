@@ -664,7 +664,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const Params p
 // second cluster barrier keeps every CTA's shared memory alive until the
 // others have read it. p.chunk >= (block width + 1) * VE.
 //
-// XI (C = 1, BATCH a multiple of 4): the threads stage x interleaved, the
+// XI (BATCH a multiple of 4; with or without a cluster, each CTA its own
+// column block): the threads stage x interleaved, the
 // BATCH values of a column side by side (groups of four columns padded by 16
 // bytes, so lanes reading consecutive groups meet different banks), and the
 // arithmetic takes two vectors per packed FMA (fma_quad_xi): half the FMA
@@ -685,7 +686,7 @@ template <typename T, int BATCH, int ROWS, int WC, int U, int kThreads, bool CLU
           bool XI = false>
 __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p) {
     static_assert(!PEEL || !CLUSTER, "peeled rows: one CTA per row block");
-    static_assert(!XI || (!PEEL && !CLUSTER && BATCH % 4 == 0), "interleaved vectors: one CTA, whole rows");
+    static_assert(!XI || (!PEEL && BATCH % 4 == 0), "interleaved vectors: aligned rows, whole 16-byte reads");
     constexpr int kPhase = 4;
     constexpr unsigned kLoadBytes = 4 * sizeof(T);   // one lane load: four entries
     constexpr int kWarps = kThreads / 32;
@@ -822,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_blocks_kernel(const Params p
             float v[BATCH][4];
 #pragma unroll
             for (int b = 0; b < BATCH; ++b) {
-                const float *src = p.x + static_cast<long long>(b) * p.ldx + c0;
+                const float *src = p.x + static_cast<long long>(b) * p.ldx + VE * ub0 + c0;
                 if (vec && c0 + 4 <= xlen) {
                     const float4 t = __ldg(reinterpret_cast<const float4 *>(src));
                     v[b][0] = t.x;
@@ -1284,7 +1285,8 @@ constexpr int kSplitRows = 4, kSplitSegs = 2;
 // 16 bytes (FP32) or four of 8 bytes (BF16), the same bytes either way
 constexpr int split_unroll(int elem_bytes) { return elem_bytes == 2 ? 4 : 2; }
 
-enum Kind { kStream = 0, kSplit = 1, kRound = 2, kCluster = 3, kPeel = 4, kPeelSplit = 5, kRing = 6, kSplitXi = 7 };
+enum Kind { kStream = 0, kSplit = 1, kRound = 2, kCluster = 3, kPeel = 4, kPeelSplit = 5, kRing = 6, kSplitXi = 7,
+            kClusterXi = 8 };
 
 // gemv_ring_kernel: 16-byte loads per ring set and sets in the ring.
 // Measured against other shapes of the ring at batch 1-2 (one process, CUDA
@@ -1326,6 +1328,9 @@ void *pick(int kind, bool vec) {
         if (kind == kSplitXi)
             return reinterpret_cast<void *>(gemv_blocks_kernel<T, BATCH, kSplitRows, kSplitSegs, split_unroll(sizeof(T)),
                                                                kRoundThreads, false, false, true>);
+        if (kind == kClusterXi)
+            return reinterpret_cast<void *>(gemv_blocks_kernel<T, BATCH, kSplitRows, kSplitSegs, split_unroll(sizeof(T)),
+                                                               kRoundThreads, true, false, true>);
     }
     if (kind == kSplit)
         return reinterpret_cast<void *>(

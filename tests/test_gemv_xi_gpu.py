@@ -1,6 +1,8 @@
 """GPU parity of the row-block GEMV kernel at batch 8 with the vectors staged
 interleaved (the eight values of a column side by side, two vectors per
-packed FMA) against the FP64 oracle, through the C ABI.
+packed FMA) against the FP64 oracle, through the C ABI: in one CTA per block
+of rows, and over clusters (each CTA its own block of columns) when the
+vectors are too long for one CTA.
 
 The threads stage x themselves: 16-byte reads of each vector where x is
 16-byte aligned with ldx a multiple of 4, single reads otherwise and for the
@@ -123,3 +125,53 @@ def test_deterministic():
 @pytest.mark.parametrize("batch", [3, 4, 6, 7])
 def test_other_batches_keep_the_plain_staging(batch):
     assert not is_xi(plan_of(4096, 4096, batch), 4096, batch)
+
+
+def _plans(M, N, prec="f32", lda=None):
+    """The plan at batch 8 with the interleaved staging and with the vectors
+    staged one after another (mode "no_xi")."""
+    gtg.gtg_gemv_force_path("cuda_cores")
+    try:
+        xi = plan_of(M, N, 8, prec, lda)
+        gtg.gtg_gemv_force_path("no_xi")
+        plain = plan_of(M, N, 8, prec, lda)
+    finally:
+        gtg.gtg_gemv_force_path("auto")
+    return xi, plain
+
+
+CLUSTER_CASES = [("f32", 1000, 8192, None), ("f32", 333, 9001, 9004), ("f32", 2048, 16384, None),
+                 ("f32", 77, 12345, 12348), ("bf16", 1000, 8192, None), ("bf16", 301, 10001, 10008)]
+
+
+@pytest.mark.parametrize("prec,M,N,lda", CLUSTER_CASES)
+def test_batch8_over_clusters(prec, M, N, lda):
+    xi, plain = _plans(M, N, prec, lda)
+    assert xi["cluster"] > 1 and plain["cluster"] > 1, (xi, plain)
+    assert xi["bn"] > plain["bn"], (xi, plain)   # 36 floats per four columns instead of 32
+    g = PCG32(4200 + M + N)
+    A = g.normal_bf16((M, N)) if prec == "bf16" else g.uniform_f32((M, N))
+    X = g.uniform_f32((8, N))
+    gtg.gtg_gemv_force_path("cuda_cores")
+    try:
+        Y = run_gemv(A, X, lda=lda, prec=prec)
+    finally:
+        gtg.gtg_gemv_force_path("auto")
+    check(bf16_bits_to_f32(A) if prec == "bf16" else A, X, Y)
+
+
+@pytest.mark.parametrize("prec,M,N,lda,ldx,x_off", [("f32", 77, 12345, 12348, None, 0),
+                                                    ("f32", 500, 8192, None, 8195, 1),
+                                                    ("bf16", 301, 10001, 10008, None, 0)])
+def test_clusters_same_bits_as_the_plain_staging(prec, M, N, lda, ldx, x_off):
+    g = PCG32(4300 + M + N)
+    A = g.normal_bf16((M, N)) if prec == "bf16" else g.uniform_f32((M, N))
+    X = g.uniform_f32((8, N))
+    gtg.gtg_gemv_force_path("cuda_cores")
+    try:
+        y_xi = run_gemv(A, X, lda=lda, ldx=ldx, x_off=x_off, prec=prec)
+        gtg.gtg_gemv_force_path("no_xi")
+        y_plain = run_gemv(A, X, lda=lda, ldx=ldx, x_off=x_off, prec=prec)
+    finally:
+        gtg.gtg_gemv_force_path("auto")
+    assert np.array_equal(y_xi.view(np.uint32), y_plain.view(np.uint32))

@@ -81,7 +81,7 @@ def test_wait_limit_default_restored():
 @pytest.mark.parametrize("M,N,batch,kernel", [
     (4096, 4096, 1, "stream"),       # one row per warp, vectors in one bulk copy each
     (4096, 4096, 4, "split"),        # 4 rows x half the columns per task (batch 8 stages x by threads)
-    (8192, 8192, 8, "cluster"),      # column blocks over a 2-CTA cluster
+    (2048, 16384, 4, "cluster"),     # column blocks over a 2-CTA cluster (batch 8 stages x by threads)
 ])
 def test_gemv_vector_wait_that_runs_out_is_reported(M, N, batch, kernel):
     """The GEMV kernels wait (bounded) for their bulk-copied vectors; a hook
