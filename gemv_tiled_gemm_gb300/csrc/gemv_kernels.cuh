@@ -1271,7 +1271,7 @@ __global__ void __launch_bounds__(kPeelThreads, 1) gemv_stream_peel_kernel(const
 // row each, two BF16 rows at batch 2); batch >= 3 with x in one CTA ->
 // gemv_blocks_kernel without a cluster (16 warps, 4 rows x half the columns
 // per task; at batch 8 with the vectors staged interleaved, XI); x too large
-// for one CTA -> gemv_blocks_kernel over a cluster.
+// for one CTA -> gemv_blocks_kernel over a cluster (XI as well at batch 8).
 // Rows off 16 bytes with x in one chunk: FP32 batch <= 2 ->
 // gemv_stream_peel_kernel; FP32 batch >= 3 and BF16 -> gemv_blocks_kernel
 // with PEEL. Otherwise gemv_kernel (16 warps, two rows per task, x chunked
